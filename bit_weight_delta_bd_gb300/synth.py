@@ -1,0 +1,94 @@
+"""Seeded synthetic inputs for the BitDelta path (shared by tests and bench).
+
+This module only draws random numbers and rounds them to bf16; it holds none
+of the method's arithmetic (no Delta, sign, alpha, packing or linear), so both
+the CPU oracle and the CUDA path can take their inputs from it without sharing
+any computation.
+
+Distributions follow the BitDelta post ("BitDelta: Tek bir GPU kumesinden 14
+Zen modeli sunmak", section "Matematiksel temel", the Laplace model
+Delta_ij ~ Laplace(0, b)) and the workload shapes of the serving setup:
+
+* ``W_base`` ~ N(0, 0.02) drawn in fp32, rounded to bf16 (RNE);
+* ``Delta`` ~ Laplace(0, b) drawn in fp64; ``W_ft = bf16(W_base + Delta)``;
+* ``x`` ~ N(0, 1) drawn in fp32, rounded to bf16;
+* variant ids ~ Zipf(s = 1.1) over ranks 1..V, id = rank - 1, drawn by inverse
+  CDF from uniforms (``searchsorted(..., side="right")``).
+
+Draw order within one generator is W_base, Delta, x (then variant ids).
+bf16 tensors are returned as their uint16 bit patterns.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    """Round fp32 (or fp64 via fp32) to bf16 with round-to-nearest-even."""
+    f = np.ascontiguousarray(a, dtype=np.float32)
+    u = f.view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (np.ascontiguousarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def base_weight(rng: np.random.Generator, d_out: int, d_in: int, std: float = 0.02) -> np.ndarray:
+    return f32_to_bf16_bits(rng.standard_normal((d_out, d_in), dtype=np.float32) * np.float32(std))
+
+
+def finetuned_weight(rng: np.random.Generator, w_base_bits: np.ndarray, b: float) -> np.ndarray:
+    """bf16(W_base + Laplace(0, b)) with the Laplace draw in fp64."""
+    delta = rng.laplace(0.0, b, size=w_base_bits.shape)
+    return f32_to_bf16_bits(bf16_bits_to_f32(w_base_bits).astype(np.float64) + delta)
+
+
+def activations(rng: np.random.Generator, T: int, d_in: int) -> np.ndarray:
+    return f32_to_bf16_bits(rng.standard_normal((T, d_in), dtype=np.float32))
+
+
+def zipf_variant_ids(rng: np.random.Generator, T: int, V: int, s: float = 1.1) -> np.ndarray:
+    ranks = np.arange(1, V + 1, dtype=np.float64)
+    p = ranks ** (-s)
+    cdf = np.cumsum(p / p.sum())
+    cdf[-1] = 1.0
+    u = rng.random(T)
+    return np.minimum(np.searchsorted(cdf, u, side="right"), V - 1).astype(np.int32)
+
+
+def single_problem(seed: int, d_out: int, d_in: int, T: int, b: float = 1e-3):
+    """(W_base, W_ft, x) bf16 bit patterns for one linear; draw order W_base, Delta, x."""
+    rng = np.random.default_rng(seed)
+    wb = base_weight(rng, d_out, d_in)
+    wf = finetuned_weight(rng, wb, b)
+    x = activations(rng, T, d_in)
+    return wb, wf, x
+
+
+def multi_problem(seed: int, d_out: int, d_in: int, T: int, V: int, b_lo: float = 5e-4, b_hi: float = 2e-3):
+    """(W_base, [W_ft_v], x, vid, b) for V variants sharing one W_base.
+
+    The per-variant Laplace scales b_v ~ U[b_lo, b_hi] are drawn first, then
+    W_base, then each variant's Delta in order, then x, then the Zipf ids.
+    """
+    rng = np.random.default_rng(seed)
+    b = rng.uniform(b_lo, b_hi, size=V)
+    wb = base_weight(rng, d_out, d_in)
+    wfs = [finetuned_weight(rng, wb, float(b[v])) for v in range(V)]
+    x = activations(rng, T, d_in)
+    vid = zipf_variant_ids(rng, T, V)
+    return wb, wfs, x, vid, b
+
+
+def sample_rows(seed: int, d_out: int, n: int) -> np.ndarray:
+    """A sorted seeded subset of row indices that always includes the first
+    and the last row (so tile edges and the ragged tail are covered)."""
+    rng = np.random.default_rng(seed + 7919)
+    n = min(n, d_out)
+    pick = rng.choice(d_out, size=n, replace=False)
+    pick[0] = 0
+    if n > 1:
+        pick[1] = d_out - 1
+    return np.unique(pick).astype(np.int64)

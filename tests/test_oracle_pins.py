@@ -1,0 +1,344 @@
+"""Pins of the CPU oracle to what the BitDelta post and the mathematics fix.
+
+Nothing here compares the oracle with itself: every check is a closed form, a
+brute-force search, an exact rational computation, a hand-built bit pattern, a
+value the post prints, or a special case that reduces to a numpy routine.
+Source: "BitDelta: Tek bir GPU kumesinden 14 Zen modeli sunmak" (Hanzo blog,
+2026-02-28), sections "Matematiksel temel", "Sunum mimarisi" and
+"Altyapi ayrintilari".
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from bit_weight_delta_bd_gb300 import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _bits(values) -> np.ndarray:
+    """Exact bf16 bit patterns of values that bf16 represents exactly."""
+    f = np.asarray(values, dtype=np.float32)
+    b = synth.f32_to_bf16_bits(f)
+    assert np.array_equal(synth.bf16_bits_to_f32(b), f), "test value not exact in bf16"
+    return b
+
+
+def _delta(wb_bits, wf_bits):
+    return synth.bf16_bits_to_f32(wf_bits).astype(np.float64) - synth.bf16_bits_to_f32(wb_bits).astype(np.float64)
+
+
+# --------------------------------------------------------------------------------------------
+# eq. (3): alpha = mean|Delta| is the L2-optimal scale for the sign code (brute-force search)
+# --------------------------------------------------------------------------------------------
+
+def _argmin_scale(delta: np.ndarray, s: np.ndarray) -> float:
+    """Brute force: grid of 10^4 points over [0, 2 max|Delta|], then golden-section refinement."""
+    top = 2.0 * float(np.max(np.abs(delta))) if delta.size else 0.0
+    if top == 0.0:
+        return 0.0
+    grid = np.linspace(0.0, top, 10001)
+    err = ((delta[None, :] - grid[:, None] * s[None, :]) ** 2).sum(axis=1)
+    k = int(np.argmin(err))
+    lo, hi = grid[max(k - 1, 0)], grid[min(k + 1, len(grid) - 1)]
+
+    def f(a):
+        return float(((delta - a * s) ** 2).sum())
+
+    g = (math.sqrt(5.0) - 1.0) / 2.0
+    a, b = lo, hi
+    c, d = b - g * (b - a), a + g * (b - a)
+    for _ in range(200):
+        if f(c) < f(d):
+            b = d
+        else:
+            a = c
+        c, d = b - g * (b - a), a + g * (b - a)
+    return 0.5 * (a + b)
+
+
+def _tiny_cases():
+    rng = np.random.default_rng(11)
+    cases = []
+    for d_out, d_in in [(4, 32), (8, 32), (3, 64)]:
+        wb = synth.base_weight(rng, d_out, d_in)
+        wf = synth.finetuned_weight(rng, wb, 1e-3)
+        cases.append((wb, wf))
+    # an all-zero-delta row and a single-nonzero row
+    wb = synth.base_weight(rng, 4, 32)
+    wf = wb.copy()
+    wf[1, 7] = synth.f32_to_bf16_bits(np.array([0.5], np.float32))[0]
+    wf[2] = synth.finetuned_weight(rng, wb[2:3], 2e-3)[0]
+    cases.append((wb, wf))
+    return cases
+
+
+@pytest.mark.parametrize("case", range(4))
+def test_alpha_is_l2_optimal_per_row(case):
+    wb, wf = _tiny_cases()[case]
+    signs, alpha = oracle.compress(wb, wf, per_row=True)
+    s = oracle.unpack_signs(signs, wb.shape[1]).astype(np.float64)
+    delta = _delta(wb, wf)
+    for i in range(wb.shape[0]):
+        a_star = _argmin_scale(delta[i], s[i])
+        assert alpha[i] == pytest.approx(a_star, rel=1e-6, abs=1e-12), (i, alpha[i], a_star)
+
+
+@pytest.mark.parametrize("case", range(4))
+def test_alpha_is_l2_optimal_per_matrix(case):
+    wb, wf = _tiny_cases()[case]
+    signs, alpha = oracle.compress(wb, wf, per_row=False)
+    assert alpha.shape == (1,)
+    s = oracle.unpack_signs(signs, wb.shape[1]).astype(np.float64).ravel()
+    a_star = _argmin_scale(_delta(wb, wf).ravel(), s)
+    assert alpha[0] == pytest.approx(a_star, rel=1e-6, abs=1e-12)
+
+
+def test_alpha_all_zero_delta_is_zero():
+    wb = synth.base_weight(np.random.default_rng(3), 5, 64)
+    for per_row in (True, False):
+        signs, alpha = oracle.compress(wb, wb, per_row=per_row)
+        assert np.all(alpha == 0.0)
+        assert np.all(signs == 0xFFFFFFFF)  # sign(0) := +1 everywhere
+
+
+# --------------------------------------------------------------------------------------------
+# bit layout: hand-built rows (tests/golden/hand_bits.txt)
+# --------------------------------------------------------------------------------------------
+
+def _hand_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "hand_bits.txt")) as fh:
+        for line in fh:
+            if not line.strip() or line.startswith("#"):
+                continue
+            name, cols, words = [p.strip() for p in line.split("|")]
+            wf = np.full(64, -1.0, np.float32)
+            if cols:
+                for item in cols.split(","):
+                    c, v = item.split("=")
+                    wf[int(c)] = np.float32(float(v))
+            rows.append((name, wf, [int(w, 16) for w in words.split()]))
+    return rows
+
+
+def test_hand_built_bit_patterns():
+    rows = _hand_rows()
+    assert len(rows) >= 8
+    wf = np.stack([r[1] for r in rows])
+    wb = np.zeros_like(wf)
+    signs, _ = oracle.compress(_bits(wb), _bits(wf), per_row=True)
+    for k, (name, _, words) in enumerate(rows):
+        assert [int(w) for w in signs[k]] == words, name
+
+
+def test_byte_view_is_int8_rows_of_d_in_over_8():
+    """Little-endian byte view = int8 [d_out][d_in/8], bit k of byte c <-> column 8c+k."""
+    rng = np.random.default_rng(5)
+    s = np.where(rng.random((6, 96)) < 0.5, -1, 1).astype(np.int8)
+    packed = oracle.pack_signs(s)
+    as_bytes = packed.view(np.uint8)
+    assert as_bytes.shape == (6, 96 // 8)
+    expect = np.packbits((s > 0).astype(np.uint8), axis=1, bitorder="little")
+    assert np.array_equal(as_bytes, expect)
+
+
+def test_pack_unpack_round_trips():
+    rng = np.random.default_rng(6)
+    s = np.where(rng.random((9, 128)) < 0.3, -1, 1).astype(np.int8)
+    assert np.array_equal(oracle.unpack_signs(oracle.pack_signs(s), 128), s)
+    bits = rng.integers(0, 2**32, size=(7, 4), dtype=np.uint64).astype(np.uint32)
+    assert np.array_equal(oracle.pack_signs(oracle.unpack_signs(bits, 128)), bits)
+
+
+def test_compress_rejects_d_in_not_multiple_of_32():
+    wb = np.zeros((2, 48), np.uint16)
+    with pytest.raises(ValueError):
+        oracle.compress(wb, wb, per_row=True)
+
+
+# --------------------------------------------------------------------------------------------
+# sizes the page prints
+# --------------------------------------------------------------------------------------------
+
+def test_page_sizes():
+    n = 0
+    with open(os.path.join(GOLDEN, "page_sizes.txt")) as fh:
+        for line in fh:
+            if not line.strip() or line.startswith("#"):
+                continue
+            name, d_out, d_in, n_alpha, expect = line.split("--")[0].split()
+            assert oracle.compressed_bytes(int(d_out), int(d_in), int(n_alpha)) == int(expect), name
+            n += 1
+    assert n == 2
+    # per-row alpha adds 4 bytes per output row (float32, one per output dimension)
+    assert oracle.compressed_bytes(4096, 4096, 4096) == 4096 * 512 + 4 * 4096
+
+
+def test_page_memory_arithmetic():
+    vals = {}
+    with open(os.path.join(GOLDEN, "page_memory.txt")) as fh:
+        for line in fh:
+            if line.strip() and not line.startswith("#"):
+                k, v = line.split()
+                vals[k] = float(v)
+    params, nv = int(vals["params"]), int(vals["variants"])
+    base_bytes = 2 * params  # bf16
+    assert base_bytes / 1e9 == vals["base_gb"]
+    assert nv * base_bytes / 1e12 == pytest.approx(vals["naive_tb"])
+    delta_bytes = oracle.compressed_bytes(params, 1, 0)
+    total = base_bytes + nv * delta_bytes
+    assert total / 1e9 == pytest.approx(vals["bitdelta_gb_approx"], abs=1.0)
+    assert 100 * (1 - total / (nv * base_bytes)) == pytest.approx(vals["reduction_pct_approx"], abs=0.5)
+
+
+# --------------------------------------------------------------------------------------------
+# eq. (2) and the listing: reconstruction invariants
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("per_row", [True, False])
+def test_reconstruction_invariants(per_row):
+    wb, wf, _ = synth.single_problem(21, 24, 96, 1)
+    signs, alpha = oracle.compress(wb, wf, per_row=per_row)
+    weff = oracle.reconstruct(wb, signs, alpha, per_row)
+    base = synth.bf16_bits_to_f32(wb).astype(np.float64)
+    a = alpha.astype(np.float64)[:, None] if per_row else np.float64(alpha[0])
+    diff = weff - base
+    assert np.array_equal(np.abs(diff), np.broadcast_to(a, diff.shape))
+    delta = _delta(wb, wf)
+    code = np.where(delta < 0, -1.0, 1.0)
+    assert np.array_equal(np.sign(diff), code)
+    assert (delta == 0).any(), "fixture should exercise sign(0)"
+
+
+# --------------------------------------------------------------------------------------------
+# the linear: special cases that reduce to numpy, and exact rational arithmetic
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("per_row", [True, False])
+def test_zero_delta_is_plain_gemm(per_row):
+    rng = np.random.default_rng(8)
+    wb = synth.base_weight(rng, 40, 96)
+    x = synth.activations(rng, 5, 96)
+    signs, alpha = oracle.compress(wb, wb, per_row=per_row)
+    y = oracle.linear(x, wb, signs, alpha, per_row)
+    ref = synth.bf16_bits_to_f32(x).astype(np.float64) @ synth.bf16_bits_to_f32(wb).astype(np.float64).T
+    assert y.shape == (5, 40)
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("direction", [+1.0, -1.0])
+def test_zero_base_is_alpha_times_token_sum(direction):
+    rng = np.random.default_rng(9)
+    mags = rng.integers(1, 9, size=(12, 64)).astype(np.float32) / 64.0
+    wb = np.zeros((12, 64), np.float32)
+    wf = direction * mags
+    signs, alpha = oracle.compress(_bits(wb), _bits(wf), per_row=True)
+    x = synth.activations(rng, 3, 64)
+    y = oracle.linear(x, _bits(wb), signs, alpha, True)
+    xs = synth.bf16_bits_to_f32(x).astype(np.float64).sum(axis=1)
+    ref = direction * xs[:, None] * mags.astype(np.float64).mean(axis=1)[None, :]
+    np.testing.assert_allclose(y, ref, rtol=1e-6, atol=0)
+
+
+def test_linear_exact_rationals():
+    """Dyadic inputs: the exact result, computed with Fractions, must be reproduced exactly."""
+    rng = np.random.default_rng(10)
+    d_out, d_in, T = 6, 64, 3
+    wb = rng.integers(-8, 9, size=(d_out, d_in)).astype(np.float32) / 64.0
+    e = rng.integers(5, 9, size=d_out)
+    s = np.where(rng.random((d_out, d_in)) < 0.5, -1.0, 1.0).astype(np.float32)
+    wf = wb + s * (2.0 ** (-e.astype(np.float32)))[:, None]
+    x = rng.integers(-4, 5, size=(T, d_in)).astype(np.float32)
+    signs, alpha = oracle.compress(_bits(wb), _bits(wf), per_row=True)
+    assert np.array_equal(alpha, (2.0 ** -e).astype(np.float32))
+    y = oracle.linear(_bits(x), _bits(wb), signs, alpha, True)
+    for t in range(T):
+        for i in range(d_out):
+            exact = sum(Fraction(float(x[t, j])) * (Fraction(float(wb[i, j])) +
+                                                     Fraction(1, 2 ** int(e[i])) * int(s[i, j]))
+                        for j in range(d_in))
+            assert Fraction(y[t, i]) == exact
+
+
+def test_linear_rows_subset_matches_listed_rows():
+    wb, wf, x = synth.single_problem(12, 33, 64, 2)
+    signs, alpha = oracle.compress(wb, wf, per_row=True)
+    y_all = oracle.linear(x, wb, signs, alpha, True)
+    rows = np.array([0, 5, 32], np.int64)
+    y_sub = oracle.linear(x, wb, signs, alpha, True, rows=rows)
+    assert np.array_equal(y_sub, y_all[:, rows])
+    s2, a2 = oracle.compress_rows(wb, wf, rows)
+    assert np.array_equal(s2, signs[rows]) and np.array_equal(a2, alpha[rows])
+
+
+# --------------------------------------------------------------------------------------------
+# the Laplace model of section "Matematiksel temel"
+# --------------------------------------------------------------------------------------------
+
+def test_laplace_statistics():
+    """For Delta ~ Laplace(0, b): E|Delta| = b, and E(Delta - alpha s)^2 / E Delta^2 -> 1/2."""
+    b = 1e-3
+    wb, wf, _ = synth.single_problem(13, 256, 4096, 1, b=b)
+    signs, alpha = oracle.compress(wb, wf, per_row=False)
+    assert alpha[0] == pytest.approx(b, rel=0.01)
+    delta = _delta(wb, wf)
+    s = oracle.unpack_signs(signs, 4096).astype(np.float64)
+    ratio = np.linalg.norm(delta - alpha[0] * s) / np.linalg.norm(delta)
+    assert ratio == pytest.approx(1 / math.sqrt(2), rel=0.01)
+    # about 4% of the deltas are exactly zero after bf16 rounding; they all got +1
+    zero = delta == 0
+    assert 0.02 < zero.mean() < 0.08
+    assert np.all(s[zero] == 1)
+
+
+# --------------------------------------------------------------------------------------------
+# the router (section "Sunum mimarisi", serving steps 1-3)
+# --------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("T,V", [(0, 3), (1, 1), (64, 14), (257, 5), (1000, 64)])
+def test_route_is_stable_sort_by_key(T, V):
+    rng = np.random.default_rng(T + V)
+    vid = rng.integers(-1, V, size=T).astype(np.int32)
+    if T > 4:
+        vid[::7] = V + 3  # out of range: routed as base and counted
+        vid[1] = -5
+    perm, seg, n_bad = oracle.route(vid, V)
+    key = np.where((vid >= -1) & (vid < V), vid + 1, 0)
+    assert n_bad == int(((vid < -1) | (vid >= V)).sum())
+    assert np.array_equal(perm, np.argsort(key, kind="stable"))
+    counts = np.bincount(key, minlength=V + 1)
+    assert np.array_equal(seg, np.concatenate([[0], np.cumsum(counts)]).astype(np.int32))
+
+
+def test_multi_routes_each_token_to_its_variant():
+    """W_base = 0 and all-plus signs: y[t][i] = alpha_{vid[t]}[i] * sum_j x[t][j] (0 for base tokens)."""
+    rng = np.random.default_rng(14)
+    V, d_out, d_in, T = 4, 8, 64, 9
+    wb = np.zeros((d_out, d_in), np.float32)
+    signs_l, alpha_l = [], []
+    for v in range(V):
+        wf = np.full((d_out, d_in), 2.0 ** -(v + 3), np.float32) * (1 + np.arange(d_out))[:, None]
+        s, a = oracle.compress(_bits(wb), _bits(wf), per_row=True)
+        signs_l.append(s)
+        alpha_l.append(a)
+    vid = np.array([0, 3, -1, 2, 2, 1, 0, -1, 3], np.int32)
+    x = synth.activations(rng, T, d_in)
+    y = oracle.linear_multi(x, vid, signs_l, alpha_l, True, _bits(wb))
+    xs = synth.bf16_bits_to_f32(x).astype(np.float64).sum(axis=1)
+    for t in range(T):
+        expect = np.zeros(d_out) if vid[t] < 0 else 2.0 ** -(vid[t] + 3) * (1 + np.arange(d_out)) * xs[t]
+        np.testing.assert_allclose(y[t], expect, rtol=1e-12, atol=1e-15)
+
+
+def test_synth_zipf_ids_in_range_and_skewed():
+    rng = np.random.default_rng(0)
+    vid = synth.zipf_variant_ids(rng, 20000, 14)
+    assert vid.min() >= 0 and vid.max() <= 13
+    counts = np.bincount(vid, minlength=14) / 20000
+    p = np.arange(1, 15, dtype=np.float64) ** -1.1
+    np.testing.assert_allclose(counts, p / p.sum(), atol=0.01)
