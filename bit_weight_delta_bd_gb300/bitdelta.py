@@ -1,0 +1,224 @@
+"""Thin ctypes binding of libbitdelta.so (include/bitdelta.h).
+
+Argument marshalling only: every function here checks that its torch tensors
+live on the current CUDA device with the expected dtype and layout, passes
+their device pointers and the current CUDA stream to the C entry point of the
+same name, and raises ``BitDeltaError`` on a non-OK status.  All arithmetic
+runs in the library's sm_103a kernels; there is no fallback path, so a missing
+or unloadable library raises instead of computing anything.
+
+PyTorch is used for device memory and streams only.  bf16 buffers may be
+passed as ``torch.bfloat16`` or as their ``torch.uint16``/``torch.int16`` bit
+patterns.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libbitdelta.so")
+
+BD_OK = 0
+BD_ERR_INVALID_ARG = 1
+BD_ERR_UNSUPPORTED_SHAPE = 2
+BD_ERR_MISALIGNED = 3
+BD_ERR_BAD_VARIANT = 4
+BD_ERR_NONFINITE = 5
+BD_ERR_CUDA = 6
+BD_ERR_TIMEOUT = 7
+BD_ERR_WORKSPACE = 8
+BD_ERR_DEVICE = 9
+
+BD_ALPHA_PER_MATRIX = 0
+BD_ALPHA_PER_ROW = 1
+BD_OUT_BF16 = 0
+BD_OUT_F32 = 1
+BD_MAX_VARIANTS = 64
+
+# Every symbol include/bitdelta.h declares.
+EXPORTS = (
+    "bd_version", "bd_status_string",
+    "bd_compress_workspace_size", "bd_compress",
+    "bd_linear_workspace_size", "bd_linear",
+    "bd_linear_multi_workspace_size", "bd_linear_multi",
+    "bd_route_workspace_size", "bd_route",
+    "bd_debug_reconstruct", "bd_check_async",
+)
+
+
+class BitDeltaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = int(status)
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+_lib = None
+_lock = threading.Lock()
+_i64, _i32, _vp, _sz, _int = ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libbitdelta.so (built by ``bit_weight_delta_bd_gb300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(f"libbitdelta.so is not built ({path}); run __graft_entry__.build() first")
+        lib = ctypes.CDLL(path)
+        sig = {
+            "bd_version": ([], _int),
+            "bd_status_string": ([_int], ctypes.c_char_p),
+            "bd_compress_workspace_size": ([_i64, _i64, _int], _sz),
+            "bd_compress": ([_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp, _sz, _vp], _int),
+            "bd_linear_workspace_size": ([_i64, _i64, _i64], _sz),
+            "bd_linear": ([_vp, _i64, _vp, _vp, _vp, _int, _i64, _i64, _vp, _int, _vp, _sz, _vp], _int),
+            "bd_linear_multi_workspace_size": ([_i64, _i32, _i64, _i64], _sz),
+            "bd_linear_multi": ([_vp, _i64, _vp, _i32, _vp, _vp, _int, _vp, _i64, _i64, _vp, _int, _vp, _sz, _vp],
+                                _int),
+            "bd_route_workspace_size": ([_i64, _i32], _sz),
+            "bd_route": ([_vp, _i64, _i32, _vp, _vp, _vp, _sz, _vp], _int),
+            "bd_debug_reconstruct": ([_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp], _int),
+            "bd_check_async": ([_vp, _vp], _int),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().bd_status_string(int(status)).decode()
+    except RuntimeError:
+        return f"status {status}"
+
+
+def _check(status: int, where: str) -> None:
+    if status != BD_OK:
+        raise BitDeltaError(status, where)
+
+
+_BF16_LIKE = (torch.bfloat16, torch.uint16, torch.int16)
+
+
+def _ptr(t: torch.Tensor | None, name: str, dtypes=None, allow_none: bool = False) -> int | None:
+    if t is None:
+        if allow_none:
+            return None
+        raise ValueError(f"{name} is required")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"{name} is on {t.device}, not the current device")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name} has dtype {t.dtype}, expected one of {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _ws(ws: torch.Tensor) -> tuple[int, int]:
+    if ws.dtype != torch.uint8:
+        raise ValueError("workspace must be a torch.uint8 tensor")
+    return _ptr(ws, "ws"), ws.numel()
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace (the library requires zeros before first use)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# ------------------------------------------------------------------------------- sizes
+
+def bd_version() -> int:
+    return int(load().bd_version())
+
+
+def bd_compress_workspace_size(d_out: int, d_in: int, alpha_mode: int) -> int:
+    return int(load().bd_compress_workspace_size(d_out, d_in, alpha_mode))
+
+
+def bd_linear_workspace_size(T: int, d_out: int, d_in: int) -> int:
+    return int(load().bd_linear_workspace_size(T, d_out, d_in))
+
+
+def bd_linear_multi_workspace_size(T: int, V: int, d_out: int, d_in: int) -> int:
+    return int(load().bd_linear_multi_workspace_size(T, V, d_out, d_in))
+
+
+def bd_route_workspace_size(T: int, V: int) -> int:
+    return int(load().bd_route_workspace_size(T, V))
+
+
+# ------------------------------------------------------------------------------- calls
+
+def bd_compress(w_base, w_ft, alpha_mode, signs, alpha, ws, stream=None) -> None:
+    d_out, d_in = w_base.shape
+    if tuple(w_ft.shape) != (d_out, d_in):
+        raise ValueError("w_ft shape differs from w_base")
+    wsp, wsn = _ws(ws)
+    _check(load().bd_compress(_ptr(w_base, "w_base", _BF16_LIKE), _ptr(w_ft, "w_ft", _BF16_LIKE), d_out, d_in,
+                              int(alpha_mode), _ptr(signs, "signs", (torch.int32, torch.uint32)),
+                              _ptr(alpha, "alpha", (torch.float32,)), wsp, wsn, _stream(stream)), "bd_compress")
+
+
+def bd_linear(x, w_base, signs, alpha, alpha_mode, y, ws, stream=None) -> None:
+    T, d_in = x.shape
+    d_out = w_base.shape[0]
+    out_dtype = BD_OUT_F32 if y.dtype == torch.float32 else BD_OUT_BF16
+    wsp, wsn = _ws(ws)
+    _check(load().bd_linear(_ptr(x, "x", _BF16_LIKE), T, _ptr(w_base, "w_base", _BF16_LIKE),
+                            _ptr(signs, "signs", (torch.int32, torch.uint32)), _ptr(alpha, "alpha", (torch.float32,)),
+                            int(alpha_mode), d_out, d_in, _ptr(y, "y", (torch.float32, torch.bfloat16)), out_dtype,
+                            wsp, wsn, _stream(stream)), "bd_linear")
+
+
+def bd_linear_multi(x, vid, signs_list, alpha_list, alpha_mode, w_base, y, ws, stream=None) -> None:
+    T, d_in = x.shape
+    d_out = w_base.shape[0]
+    V = len(signs_list)
+    if len(alpha_list) != V:
+        raise ValueError("signs_list and alpha_list differ in length")
+    s_tab = (ctypes.c_void_p * max(V, 1))(*[_ptr(s, "signs", (torch.int32, torch.uint32)) for s in signs_list])
+    a_tab = (ctypes.c_void_p * max(V, 1))(*[_ptr(a, "alpha", (torch.float32,)) for a in alpha_list])
+    out_dtype = BD_OUT_F32 if y.dtype == torch.float32 else BD_OUT_BF16
+    wsp, wsn = _ws(ws)
+    _check(load().bd_linear_multi(_ptr(x, "x", _BF16_LIKE), T, _ptr(vid, "vid", (torch.int32,)), V,
+                                  ctypes.addressof(s_tab), ctypes.addressof(a_tab), int(alpha_mode),
+                                  _ptr(w_base, "w_base", _BF16_LIKE), d_out, d_in,
+                                  _ptr(y, "y", (torch.float32, torch.bfloat16)), out_dtype, wsp, wsn,
+                                  _stream(stream)), "bd_linear_multi")
+
+
+def bd_route(vid, V, perm, seg_off, ws, stream=None) -> None:
+    T = vid.numel()
+    wsp, wsn = _ws(ws)
+    _check(load().bd_route(_ptr(vid, "vid", (torch.int32,)), T, int(V), _ptr(perm, "perm", (torch.int32,)),
+                           _ptr(seg_off, "seg_off", (torch.int32,)), wsp, wsn, _stream(stream)), "bd_route")
+
+
+def bd_debug_reconstruct(w_base, signs, alpha, alpha_mode, w_eff, stream=None) -> None:
+    d_out, d_in = w_base.shape
+    _check(load().bd_debug_reconstruct(_ptr(w_base, "w_base", _BF16_LIKE),
+                                       _ptr(signs, "signs", (torch.int32, torch.uint32)),
+                                       _ptr(alpha, "alpha", (torch.float32,)), int(alpha_mode), d_out, d_in,
+                                       _ptr(w_eff, "w_eff", (torch.float32,)), _stream(stream)),
+           "bd_debug_reconstruct")
+
+
+def bd_check_async(ws, stream=None) -> int:
+    """Waits for the stream and returns (and clears) the asynchronous status."""
+    wsp, _ = _ws(ws)
+    return int(load().bd_check_async(wsp, _stream(stream)))

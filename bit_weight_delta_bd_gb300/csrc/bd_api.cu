@@ -1,0 +1,299 @@
+// C ABI of libbitdelta.so: argument checks, workspace layout and dispatch to
+// the sm_103a kernels.  Every entry point is declared and documented in
+// include/bitdelta.h.
+#include <atomic>
+#include <cstring>
+
+#include "../../include/bitdelta.h"
+#include "bd_internal.h"
+
+namespace {
+
+constexpr int kVersion = 10000;  // 1.0.0
+constexpr size_t kWsHeader = 256;  // error word + padding; scratch starts here
+
+// Per-device cache of (compute capability, SM count); the only global state.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_dev_cc[kMaxDevices];
+std::atomic<int> g_dev_sms[kMaxDevices];
+
+bd_status device_info(int* sm_count)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return BD_ERR_DEVICE;
+    int cc = g_dev_cc[dev].load(std::memory_order_acquire);
+    if (cc == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return BD_ERR_CUDA;
+        cc = major * 10 + minor;
+        g_dev_sms[dev].store(sms, std::memory_order_relaxed);
+        g_dev_cc[dev].store(cc, std::memory_order_release);
+    }
+    if (cc != 103) return BD_ERR_DEVICE;
+    *sm_count = g_dev_sms[dev].load(std::memory_order_relaxed);
+    return BD_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb)
+{
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+bd_status check_d_in(int64_t d_in) { return (d_in > 0 && d_in % 128 == 0) ? BD_OK : BD_ERR_UNSUPPORTED_SHAPE; }
+
+bd_status check_ws(const void* ws, size_t ws_bytes, size_t need)
+{
+    if (!ws || ws_bytes < need) return BD_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return BD_ERR_MISALIGNED;
+    return BD_OK;
+}
+
+bd_status launched(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
+
+uint32_t* err_word(void* ws) { return static_cast<uint32_t*>(ws); }
+
+}  // namespace
+
+extern "C" {
+
+int bd_version(void) { return kVersion; }
+
+const char* bd_status_string(bd_status s)
+{
+    switch (s) {
+        case BD_OK: return "BD_OK";
+        case BD_ERR_INVALID_ARG: return "BD_ERR_INVALID_ARG: invalid argument";
+        case BD_ERR_UNSUPPORTED_SHAPE: return "BD_ERR_UNSUPPORTED_SHAPE: d_in must be a positive multiple of 128";
+        case BD_ERR_MISALIGNED: return "BD_ERR_MISALIGNED: pointer alignment rule broken";
+        case BD_ERR_BAD_VARIANT: return "BD_ERR_BAD_VARIANT: variant id outside [-1, V)";
+        case BD_ERR_NONFINITE: return "BD_ERR_NONFINITE: non-finite delta in compression";
+        case BD_ERR_CUDA: return "BD_ERR_CUDA: CUDA runtime error";
+        case BD_ERR_TIMEOUT: return "BD_ERR_TIMEOUT: an in-kernel wait timed out";
+        case BD_ERR_WORKSPACE: return "BD_ERR_WORKSPACE: workspace missing or too small";
+        case BD_ERR_DEVICE: return "BD_ERR_DEVICE: current device is not compute capability 10.3";
+    }
+    return "BD_ERR_UNKNOWN";
+}
+
+// ------------------------------------------------------------------ compress
+
+size_t bd_compress_workspace_size(int64_t d_out, int64_t /*d_in*/, int alpha_mode)
+{
+    if (d_out < 0) return 0;
+    size_t n = kWsHeader;
+    if (alpha_mode == BD_ALPHA_PER_MATRIX) {
+        const size_t ctas = static_cast<size_t>((d_out + bd::kCompressRowsPerCta - 1) / bd::kCompressRowsPerCta);
+        n += ctas * sizeof(double);
+    }
+    return (n + 255) & ~static_cast<size_t>(255);
+}
+
+bd_status bd_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out, int64_t d_in, int alpha_mode,
+                      uint32_t* signs, float* alpha, void* ws, size_t ws_bytes, void* stream)
+{
+    if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+    if (d_out < 0) return BD_ERR_UNSUPPORTED_SHAPE;
+    if (bd_status s = check_d_in(d_in)) return s;
+    if (bd_status s = check_ws(ws, ws_bytes, bd_compress_workspace_size(d_out, d_in, alpha_mode))) return s;
+    if (d_out == 0) return BD_OK;
+    if (!w_base || !w_ft || !signs || !alpha) return BD_ERR_INVALID_ARG;
+    if (!aligned(w_base, 16) || !aligned(w_ft, 16) || !aligned(signs, 16) || !aligned(alpha, 4))
+        return BD_ERR_MISALIGNED;
+    const size_t wbytes = static_cast<size_t>(d_out) * d_in * 2;
+    const size_t sbytes = static_cast<size_t>(d_out) * (d_in / 8);
+    const size_t abytes = (alpha_mode == BD_ALPHA_PER_ROW ? static_cast<size_t>(d_out) : 1u) * 4;
+    if (overlaps(signs, sbytes, w_base, wbytes) || overlaps(signs, sbytes, w_ft, wbytes) ||
+        overlaps(alpha, abytes, w_base, wbytes) || overlaps(alpha, abytes, w_ft, wbytes) ||
+        overlaps(signs, sbytes, alpha, abytes) || overlaps(ws, ws_bytes, signs, sbytes) ||
+        overlaps(ws, ws_bytes, alpha, abytes))
+        return BD_ERR_INVALID_ARG;
+    int sms = 0;
+    if (bd_status s = device_info(&sms)) return s;
+    auto* partials = reinterpret_cast<double*>(static_cast<char*>(ws) + kWsHeader);
+    return launched(bd::launch_compress(w_base, w_ft, d_out, d_in, alpha_mode == BD_ALPHA_PER_ROW, signs, alpha,
+                                        partials, err_word(ws), static_cast<cudaStream_t>(stream)));
+}
+
+bd_status bd_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, const float* alpha, int alpha_mode,
+                               int64_t d_out, int64_t d_in, float* w_eff, void* stream)
+{
+    if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+    if (d_out < 0) return BD_ERR_UNSUPPORTED_SHAPE;
+    if (bd_status s = check_d_in(d_in)) return s;
+    if (d_out == 0) return BD_OK;
+    if (!w_base || !signs || !alpha || !w_eff) return BD_ERR_INVALID_ARG;
+    int sms = 0;
+    if (bd_status s = device_info(&sms)) return s;
+    return launched(bd::launch_debug_reconstruct(w_base, signs, alpha, alpha_mode == BD_ALPHA_PER_ROW, d_out, d_in,
+                                                 w_eff, static_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------------------ linear
+
+size_t bd_linear_workspace_size(int64_t /*T*/, int64_t /*d_out*/, int64_t /*d_in*/) { return kWsHeader; }
+
+static bd_status check_linear_common(const uint16_t* x, int64_t T, const uint16_t* w_base, int64_t d_out,
+                                     int64_t d_in, void* y, int out_dtype, void* ws, size_t ws_bytes, size_t ws_need)
+{
+    if (out_dtype != BD_OUT_BF16 && out_dtype != BD_OUT_F32) return BD_ERR_INVALID_ARG;
+    if (T < 0 || d_out < 0) return BD_ERR_UNSUPPORTED_SHAPE;
+    if (bd_status s = check_d_in(d_in)) return s;
+    if (bd_status s = check_ws(ws, ws_bytes, ws_need)) return s;
+    if (T == 0 || d_out == 0) return BD_OK;
+    if (!x || !w_base || !y) return BD_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(w_base, 16) || !aligned(y, 16)) return BD_ERR_MISALIGNED;
+    const size_t ybytes = static_cast<size_t>(T) * d_out * (out_dtype == BD_OUT_F32 ? 4 : 2);
+    if (overlaps(y, ybytes, x, static_cast<size_t>(T) * d_in * 2) ||
+        overlaps(y, ybytes, w_base, static_cast<size_t>(d_out) * d_in * 2) || overlaps(y, ybytes, ws, ws_bytes))
+        return BD_ERR_INVALID_ARG;
+    return BD_OK;
+}
+
+bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const uint32_t* signs, const float* alpha,
+                    int alpha_mode, int64_t d_out, int64_t d_in, void* y, int out_dtype, void* ws, size_t ws_bytes,
+                    void* stream)
+{
+    if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+    if (bd_status s = check_linear_common(x, T, w_base, d_out, d_in, y, out_dtype, ws, ws_bytes,
+                                          bd_linear_workspace_size(T, d_out, d_in)))
+        return s;
+    if (T == 0 || d_out == 0) return BD_OK;
+    if (!signs || !alpha) return BD_ERR_INVALID_ARG;
+    if (!aligned(signs, 16) || !aligned(alpha, 4)) return BD_ERR_MISALIGNED;
+    const size_t ybytes = static_cast<size_t>(T) * d_out * (out_dtype == BD_OUT_F32 ? 4 : 2);
+    const size_t abytes = (alpha_mode == BD_ALPHA_PER_ROW ? static_cast<size_t>(d_out) : 1u) * 4;
+    if (overlaps(y, ybytes, signs, static_cast<size_t>(d_out) * (d_in / 8)) || overlaps(y, ybytes, alpha, abytes))
+        return BD_ERR_INVALID_ARG;
+    int sms = 0;
+    if (bd_status s = device_info(&sms)) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t ysz = out_dtype == BD_OUT_F32 ? 4 : 2;
+
+    if (T > bd::kSkinnyMaxTokens && bd::prefill_available()) {
+        bd::PrefillArgs p{};
+        p.x = x; p.w_base = w_base; p.signs = signs; p.alpha = alpha;
+        p.per_row = alpha_mode == BD_ALPHA_PER_ROW;
+        p.T = T; p.d_out = d_out; p.d_in = d_in; p.y = y; p.out_f32 = out_dtype == BD_OUT_F32;
+        p.err = err_word(ws);
+        return launched(bd::launch_prefill(p, sms, st));
+    }
+    // decode kernel over groups of up to 64 tokens
+    for (int64_t t0 = 0; t0 < T; t0 += bd::kSkinnyMaxTokens) {
+        bd::SkinnyArgs a{};
+        a.x = x + t0 * d_in;
+        a.vid = nullptr;
+        a.w_base = w_base;
+        a.T = (T - t0) < bd::kSkinnyMaxTokens ? (T - t0) : bd::kSkinnyMaxTokens;
+        a.d_out = d_out; a.d_in = d_in; a.V = 1;
+        a.per_row = alpha_mode == BD_ALPHA_PER_ROW;
+        a.signs[0] = signs; a.alpha[0] = alpha;
+        a.y = static_cast<char*>(y) + static_cast<size_t>(t0) * d_out * ysz;
+        a.out_f32 = out_dtype == BD_OUT_F32;
+        a.err = err_word(ws);
+        if (bd_status s = launched(bd::launch_skinny(a, sms, st))) return s;
+    }
+    return BD_OK;
+}
+
+size_t bd_linear_multi_workspace_size(int64_t /*T*/, int32_t /*V*/, int64_t /*d_out*/, int64_t /*d_in*/)
+{
+    return kWsHeader;
+}
+
+bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int32_t V,
+                          const uint32_t* const* signs_tab, const float* const* alpha_tab, int alpha_mode,
+                          const uint16_t* w_base, int64_t d_out, int64_t d_in, void* y, int out_dtype, void* ws,
+                          size_t ws_bytes, void* stream)
+{
+    if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+    if (V < 1 || V > BD_MAX_VARIANTS) return BD_ERR_INVALID_ARG;
+    if (bd_status s = check_linear_common(x, T, w_base, d_out, d_in, y, out_dtype, ws, ws_bytes,
+                                          bd_linear_multi_workspace_size(T, V, d_out, d_in)))
+        return s;
+    if (T == 0 || d_out == 0) return BD_OK;
+    if (!vid || !signs_tab || !alpha_tab) return BD_ERR_INVALID_ARG;
+    if (!aligned(vid, 4)) return BD_ERR_MISALIGNED;
+    const size_t ybytes = static_cast<size_t>(T) * d_out * (out_dtype == BD_OUT_F32 ? 4 : 2);
+    const size_t abytes = (alpha_mode == BD_ALPHA_PER_ROW ? static_cast<size_t>(d_out) : 1u) * 4;
+    for (int v = 0; v < V; ++v) {
+        if (!signs_tab[v] || !alpha_tab[v]) return BD_ERR_INVALID_ARG;
+        if (!aligned(signs_tab[v], 16) || !aligned(alpha_tab[v], 4)) return BD_ERR_MISALIGNED;
+        if (overlaps(y, ybytes, signs_tab[v], static_cast<size_t>(d_out) * (d_in / 8)) ||
+            overlaps(y, ybytes, alpha_tab[v], abytes))
+            return BD_ERR_INVALID_ARG;
+    }
+    if (overlaps(y, ybytes, vid, static_cast<size_t>(T) * 4)) return BD_ERR_INVALID_ARG;
+    int sms = 0;
+    if (bd_status s = device_info(&sms)) return s;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const size_t ysz = out_dtype == BD_OUT_F32 ? 4 : 2;
+    for (int64_t t0 = 0; t0 < T; t0 += bd::kSkinnyMaxTokens) {
+        bd::SkinnyArgs a{};
+        a.x = x + t0 * d_in;
+        a.vid = vid + t0;
+        a.w_base = w_base;
+        a.T = (T - t0) < bd::kSkinnyMaxTokens ? (T - t0) : bd::kSkinnyMaxTokens;
+        a.d_out = d_out; a.d_in = d_in; a.V = V;
+        a.per_row = alpha_mode == BD_ALPHA_PER_ROW;
+        for (int v = 0; v < V; ++v) {
+            a.signs[v] = signs_tab[v];
+            a.alpha[v] = alpha_tab[v];
+        }
+        a.y = static_cast<char*>(y) + static_cast<size_t>(t0) * d_out * ysz;
+        a.out_f32 = out_dtype == BD_OUT_F32;
+        a.err = err_word(ws);
+        if (bd_status s = launched(bd::launch_skinny(a, sms, st))) return s;
+    }
+    return BD_OK;
+}
+
+// ------------------------------------------------------------------ router
+
+size_t bd_route_workspace_size(int64_t /*T*/, int32_t /*V*/) { return kWsHeader; }
+
+bd_status bd_route(const int32_t* vid, int64_t T, int32_t V, int32_t* perm, int32_t* seg_off, void* ws,
+                   size_t ws_bytes, void* stream)
+{
+    if (V < 0 || V > BD_MAX_VARIANTS) return BD_ERR_INVALID_ARG;
+    if (T < 0 || T > INT32_MAX) return BD_ERR_UNSUPPORTED_SHAPE;
+    if (bd_status s = check_ws(ws, ws_bytes, bd_route_workspace_size(T, V))) return s;
+    if (!seg_off || (T > 0 && (!vid || !perm))) return BD_ERR_INVALID_ARG;
+    if (!aligned(seg_off, 4) || (T > 0 && (!aligned(vid, 4) || !aligned(perm, 4)))) return BD_ERR_MISALIGNED;
+    if (overlaps(perm, static_cast<size_t>(T) * 4, vid, static_cast<size_t>(T) * 4) ||
+        overlaps(seg_off, static_cast<size_t>(V + 2) * 4, vid, static_cast<size_t>(T) * 4) ||
+        overlaps(seg_off, static_cast<size_t>(V + 2) * 4, perm, static_cast<size_t>(T) * 4))
+        return BD_ERR_INVALID_ARG;
+    int sms = 0;
+    if (bd_status s = device_info(&sms)) return s;
+    return launched(bd::launch_route(vid, T, V, perm, seg_off, err_word(ws), static_cast<cudaStream_t>(stream)));
+}
+
+// ------------------------------------------------------------------ async errors
+
+bd_status bd_check_async(void* ws, void* stream)
+{
+    if (!ws) return BD_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return BD_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess) return BD_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return BD_ERR_CUDA;
+    if (word == 0) return BD_OK;
+    const uint32_t zero = 0;
+    if (cudaMemcpyAsync(ws, &zero, sizeof zero, cudaMemcpyHostToDevice, st) != cudaSuccess) return BD_ERR_CUDA;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return BD_ERR_CUDA;
+    if (word & (1u << BD_ERR_TIMEOUT)) return BD_ERR_TIMEOUT;
+    if (word & (1u << BD_ERR_BAD_VARIANT)) return BD_ERR_BAD_VARIANT;
+    if (word & (1u << BD_ERR_NONFINITE)) return BD_ERR_NONFINITE;
+    return BD_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,66 @@
+// Internal interface between the C ABI (bd_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace bd {
+
+constexpr int kMaxVariants = 64;
+
+// ---- compression (bd_compress.cu) -------------------------------------------------------------
+
+// Rows handled by one compression CTA (one warp per row).
+constexpr int kCompressRowsPerCta = 8;
+
+cudaError_t launch_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out, int64_t d_in, bool per_row,
+                            uint32_t* signs, float* alpha, double* partials, uint32_t* err, cudaStream_t stream);
+
+cudaError_t launch_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, const float* alpha, bool per_row,
+                                     int64_t d_out, int64_t d_in, float* w_eff, cudaStream_t stream);
+
+// ---- decode / multi-variant linear (bd_skinny.cu) ---------------------------------------------
+
+// Tokens one skinny launch covers (8 MMA n-tiles of 8 tokens).
+constexpr int kSkinnyMaxTokens = 64;
+
+struct SkinnyArgs {
+    const uint16_t* x;        // [T][d_in] bf16 bits
+    const int32_t* vid;       // [T] or null (single variant: every token uses variant 0)
+    const uint16_t* w_base;   // [d_out][d_in]
+    int64_t T, d_out, d_in;
+    int V;                    // number of variants addressed by vid (1 for single)
+    int per_row;
+    const uint32_t* signs[kMaxVariants];
+    const float* alpha[kMaxVariants];
+    void* y;                  // [T][d_out]
+    int out_f32;
+    uint32_t* err;
+};
+
+cudaError_t launch_skinny(const SkinnyArgs& a, int sm_count, cudaStream_t stream);
+
+// ---- router (bd_route.cu) ---------------------------------------------------------------------
+
+cudaError_t launch_route(const int32_t* vid, int64_t T, int V, int32_t* perm, int32_t* seg_off, uint32_t* err,
+                         cudaStream_t stream);
+
+// ---- prefill GEMM (bd_prefill.cu) -------------------------------------------------------------
+
+struct PrefillArgs {
+    const uint16_t* x;        // [T][d_in]
+    const uint16_t* w_base;   // [d_out][d_in]
+    const uint32_t* signs;    // [d_out][d_in/32]
+    const float* alpha;
+    int per_row;
+    int64_t T, d_out, d_in;
+    void* y;
+    int out_f32;
+    uint32_t* err;
+};
+
+bool prefill_available();
+cudaError_t launch_prefill(const PrefillArgs& a, int sm_count, cudaStream_t stream);
+
+}  // namespace bd

@@ -1,0 +1,171 @@
+/*
+ * bitdelta.h -- C ABI of libbitdelta.so, the GB300 (sm_103a) BitDelta path.
+ *
+ * BitDelta ("BitDelta: Tek bir GPU kumesinden 14 Zen modeli sunmak", Hanzo
+ * blog, 2026-02-28) stores a fine-tuned variant of a base model as the sign
+ * of its weight delta, one bit per weight, plus a float32 scale alpha, and
+ * serves it with a fused kernel that reads the base weight and the bits
+ * together without ever writing the effective weight to device memory.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named as device buffers must point to device memory of the
+ *    current CUDA device; host arrays are marked "host".  The caller owns
+ *    every buffer; the library never allocates or frees memory.
+ *  - bf16 tensors are passed as uint16_t bit patterns, row-major, contiguous.
+ *  - Packed signs: uint32 [d_out][d_in/32]; bit b of word w of row r holds
+ *    column 32*w + b; bit = 1 <=> sign +1; sign(0) := +1 (also for -0.0).
+ *    On a little-endian GPU the same bytes are the int8 [d_out][d_in/8]
+ *    layout of the post's storage format (section "Altyapi ayrintilari").
+ *  - alpha: float32, one per output row (BD_ALPHA_PER_ROW) or one per matrix
+ *    (BD_ALPHA_PER_MATRIX).
+ *  - Shapes: d_in must be a positive multiple of 128 (every packed sign row
+ *    then starts on a 16-byte boundary, which the bulk copies need);
+ *    d_out >= 0 and T >= 0 are otherwise free (zero sizes are a no-op).
+ *  - Alignment: bf16 and sign buffers and y must be 16-byte aligned; alpha,
+ *    vid, perm, seg_off 4-byte aligned; workspaces 256-byte aligned.
+ *  - Asynchrony: all work is enqueued on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream).  The return value reports only the
+ *    synchronous argument checks and launch errors.
+ *  - Workspace: a caller-owned device buffer of at least the size that the
+ *    matching *_workspace_size function returns.  Its first 4 bytes are the
+ *    asynchronous error word; fill the buffer with zeros once before its
+ *    first use.  Errors found by a kernel (an out-of-range variant id, a
+ *    non-finite delta, a wait that timed out) set bits there; read and clear
+ *    them with bd_check_async.  Calls that share a workspace must be ordered
+ *    on one stream.
+ *  - No exceptions cross this boundary.  The library keeps no mutable global
+ *    state other than a per-device attribute cache, so it may be called from
+ *    several host threads.
+ */
+#ifndef BITDELTA_H
+#define BITDELTA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum bd_status {
+    BD_OK = 0,
+    BD_ERR_INVALID_ARG = 1,       /* null pointer, bad enum, aliasing output, V out of range */
+    BD_ERR_UNSUPPORTED_SHAPE = 2, /* d_in not a positive multiple of 128, negative size */
+    BD_ERR_MISALIGNED = 3,        /* a pointer breaks the alignment rules above */
+    BD_ERR_BAD_VARIANT = 4,       /* (async) a variant id outside [-1, V) */
+    BD_ERR_NONFINITE = 5,         /* (async) a non-finite delta met by bd_compress */
+    BD_ERR_CUDA = 6,              /* a CUDA runtime call or launch failed */
+    BD_ERR_TIMEOUT = 7,           /* (async) a bounded in-kernel wait gave up */
+    BD_ERR_WORKSPACE = 8,         /* workspace null or smaller than required */
+    BD_ERR_DEVICE = 9             /* current device is not a compute capability 10.3 GPU */
+} bd_status;
+
+typedef enum bd_alpha_mode { BD_ALPHA_PER_MATRIX = 0, BD_ALPHA_PER_ROW = 1 } bd_alpha_mode;
+
+typedef enum bd_out_dtype { BD_OUT_BF16 = 0, BD_OUT_F32 = 1 } bd_out_dtype;
+
+/* Largest number of variants one bd_linear_multi call can address. */
+#define BD_MAX_VARIANTS 64
+
+/* Library version, major*10000 + minor*100 + patch. */
+int bd_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* bd_status_string(bd_status status);
+
+/* ------------------------------------------------------------------------
+ * Compression -- section "Matematiksel temel", eqs. (1)-(3):
+ *   Delta = W_ft - W_base,  alpha = mean |Delta| (per row or per matrix),
+ *   signs = sign(Delta) packed one bit per weight.
+ * w_base, w_ft : device bf16 [d_out][d_in]
+ * signs        : device uint32 [d_out][d_in/32] (written)
+ * alpha        : device float32 [d_out] (per row) or [1] (per matrix) (written)
+ * Delta is formed in fp32 registers (the sign is always exact); alpha is
+ * accumulated in fp64 and rounded to float32 once.  The result does not
+ * depend on launch timing (no floating-point atomics).  A non-finite delta
+ * sets BD_ERR_NONFINITE in the error word; the signs of that row are still
+ * written and its alpha is then undefined.
+ * ------------------------------------------------------------------------ */
+size_t bd_compress_workspace_size(int64_t d_out, int64_t d_in, int alpha_mode);
+
+bd_status bd_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out, int64_t d_in, int alpha_mode,
+                      uint32_t* signs, float* alpha, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Fused linear -- section "Sunum mimarisi": the conceptual
+ * fused_bitdelta_linear listing and the fused-kernel paragraph after it:
+ *   y[t][r] = sum_j x[t][j] * (W_base[r][j] + alpha_r * s_rj)
+ * computed in one pass that reads W_base and the packed bits together; the
+ * effective weight exists only in registers / shared memory.
+ * x     : device bf16 [T][d_in] (the listing's [batch, seq, d_in] flattened)
+ * w_base: device bf16 [d_out][d_in];  signs, alpha as produced by bd_compress
+ * y     : device [T][d_out], bf16 (BD_OUT_BF16) or float32 (BD_OUT_F32);
+ *         must not overlap any input.
+ * Accumulation is fp32.  T <= 64 runs the decode kernel (the base and the
+ * sign contraction are kept apart, so W_eff is never rounded); larger T runs
+ * the prefill GEMM, which rounds W_eff to bf16 in shared memory before the
+ * tensor-core contraction.  For a given (T, d_in) the result of a row does
+ * not depend on d_out, so a row-sharded call reproduces the unsharded one
+ * bit for bit.
+ * ------------------------------------------------------------------------ */
+size_t bd_linear_workspace_size(int64_t T, int64_t d_out, int64_t d_in);
+
+bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const uint32_t* signs, const float* alpha,
+                    int alpha_mode, int64_t d_out, int64_t d_in, void* y, int out_dtype, void* ws, size_t ws_bytes,
+                    void* stream);
+
+/* ------------------------------------------------------------------------
+ * Multi-variant fused linear -- section "Sunum mimarisi": one W_base in
+ * device memory, shared read by every variant's delta in the delta cache,
+ * and a router that picks each request's variant (serving steps 1-3).
+ * Token t uses variant vid[t]; vid[t] == -1 means the base model alone.
+ * x        : device bf16 [T][d_in];  vid: device int32 [T]
+ * signs_tab: host array of V device pointers, each uint32 [d_out][d_in/32]
+ * alpha_tab: host array of V device pointers, each float32 [d_out] or [1]
+ * y        : device [T][d_out] in the caller's token order.
+ * 1 <= V <= BD_MAX_VARIANTS.  Each W_base tile is read from device memory
+ * once per group of up to 64 tokens; the tokens are grouped by variant
+ * inside the kernel and every active variant's sign tile is applied to its
+ * own tokens only.  An id outside [-1, V) sets BD_ERR_BAD_VARIANT in the
+ * error word and that token is computed as a base-model token.
+ * ------------------------------------------------------------------------ */
+size_t bd_linear_multi_workspace_size(int64_t T, int32_t V, int64_t d_out, int64_t d_in);
+
+bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int32_t V,
+                          const uint32_t* const* signs_tab, const float* const* alpha_tab, int alpha_mode,
+                          const uint16_t* w_base, int64_t d_out, int64_t d_in, void* y, int out_dtype, void* ws,
+                          size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Router on its own (the grouping that bd_linear_multi does internally).
+ * perm   : device int32 [T]   -- token indices, stably sorted by vid+1
+ * seg_off: device int32 [V+2] -- seg_off[k] = number of tokens with
+ *          vid+1 < k; segment 0 holds the base-model tokens.
+ * Out-of-range ids are grouped with the base tokens and flagged
+ * (BD_ERR_BAD_VARIANT).  0 <= V <= BD_MAX_VARIANTS.
+ * ------------------------------------------------------------------------ */
+size_t bd_route_workspace_size(int64_t T, int32_t V);
+
+bd_status bd_route(const int32_t* vid, int64_t T, int32_t V, int32_t* perm, int32_t* seg_off, void* ws,
+                   size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Test aid, not on the serving path: writes W_eff = W_base + alpha * s as
+ * float32 [d_out][d_in] so the elementwise identities |W_eff - W_base| =
+ * alpha and sign(W_eff - W_base) = s of section "Matematiksel temel",
+ * eq. (2), can be checked on the device's own unpacking.
+ * ------------------------------------------------------------------------ */
+bd_status bd_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, const float* alpha, int alpha_mode,
+                               int64_t d_out, int64_t d_in, float* w_eff, void* stream);
+
+/* Waits for `stream`, then reads and clears the error word in `ws`.
+ * Returns BD_OK, or the first asynchronous error found (in the order
+ * BD_ERR_TIMEOUT, BD_ERR_BAD_VARIANT, BD_ERR_NONFINITE). */
+bd_status bd_check_async(void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BITDELTA_H */

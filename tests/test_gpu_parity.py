@@ -1,0 +1,406 @@
+"""GPU parity of libbitdelta.so against the fp64 CPU oracle, through the C ABI.
+
+Packed signs and routing must match bit for bit, alpha to 1e-6 relative, and
+linear outputs within the tolerances of tests/helpers.py.  Workloads follow
+the BitDelta serving setup: a 256x256 tiny linear, the 28672x8192 FFN-shaped
+decode GEMV (T = 1, 4, 16), and the 8192x8192 multi-tenant decode with 14
+variants and 64 Zipf-routed tokens; plus ragged shapes, exact dyadic inputs
+(where any summation order is exact, so results must be bit-identical), row
+sharding, canary guards, determinism and argument errors.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_weight_delta_bd_gb300 import bitdelta as bd
+from bit_weight_delta_bd_gb300 import synth
+from helpers import bf16_half_ulp, check_linear, fp32_bound, to_dev, u32, y_host  # noqa: F401
+
+pytestmark = pytest.mark.gpu
+
+PR, PM = bd.BD_ALPHA_PER_ROW, bd.BD_ALPHA_PER_MATRIX
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    import __graft_entry__
+
+    __graft_entry__.build()
+    torch.cuda.set_device(0)
+    return torch.device("cuda:0")
+
+
+def gpu_compress(wb_d, wf_d, mode, dev):
+    d_out, d_in = wb_d.shape
+    signs = torch.empty((d_out, d_in // 32), dtype=torch.int32, device=dev)
+    alpha = torch.empty(d_out if mode == PR else 1, dtype=torch.float32, device=dev)
+    ws = bd.new_workspace(bd.bd_compress_workspace_size(d_out, d_in, mode), dev)
+    bd.bd_compress(wb_d, wf_d, mode, signs, alpha, ws)
+    assert bd.bd_check_async(ws) == bd.BD_OK
+    return signs, alpha
+
+
+def gpu_linear(x_d, wb_d, signs, alpha, mode, dev, f32=True):
+    T, d_out = x_d.shape[0], wb_d.shape[0]
+    y = torch.empty((T, d_out), dtype=torch.float32 if f32 else torch.bfloat16, device=dev)
+    ws = bd.new_workspace(bd.bd_linear_workspace_size(T, d_out, wb_d.shape[1]), dev)
+    bd.bd_linear(x_d, wb_d, signs, alpha, mode, y, ws)
+    assert bd.bd_check_async(ws) == bd.BD_OK
+    return y
+
+
+def assert_alpha(a_gpu, a_ref):
+    a_gpu = np.asarray(a_gpu, np.float64)
+    a_ref = np.asarray(a_ref, np.float64)
+    np.testing.assert_allclose(a_gpu, a_ref, rtol=1e-6, atol=0)
+
+
+# ============================================================================ compress
+
+def test_compress_tiny_per_matrix(dev):
+    wb, wf, _ = synth.single_problem(0, 256, 256, 4)
+    s_ref, a_ref = oracle.compress(wb, wf, per_row=False)
+    s, a = gpu_compress(to_dev(wb, dev), to_dev(wf, dev), PM, dev)
+    assert np.array_equal(u32(s), s_ref)
+    assert_alpha(a.cpu().numpy(), a_ref)
+
+
+@pytest.mark.parametrize("mode", [PR, PM])
+@pytest.mark.parametrize("d_out,d_in", [(1, 128), (17, 384), (33, 1024), (100, 256), (8, 8192 + 128)])
+def test_compress_shapes(dev, mode, d_out, d_in):
+    wb, wf, _ = synth.single_problem(d_out * 7 + d_in, d_out, d_in, 1)
+    s_ref, a_ref = oracle.compress(wb, wf, per_row=mode == PR)
+    s, a = gpu_compress(to_dev(wb, dev), to_dev(wf, dev), mode, dev)
+    assert np.array_equal(u32(s), s_ref)
+    assert_alpha(a.cpu().numpy(), a_ref)
+
+
+@pytest.fixture(scope="module")
+def decode_problem():
+    """The 28672 x 8192 FFN-shaped matrix of the decode workload, seed 0."""
+    wb, wf, _ = synth.single_problem(0, 28672, 8192, 1)
+    return wb, wf
+
+
+def test_compress_ffn_full_and_deterministic(dev, decode_problem):
+    wb, wf = decode_problem
+    s_ref, a_ref = oracle.compress(wb, wf, per_row=True)
+    wb_d, wf_d = to_dev(wb, dev), to_dev(wf, dev)
+    s1, a1 = gpu_compress(wb_d, wf_d, PR, dev)
+    assert np.array_equal(u32(s1), s_ref)
+    assert_alpha(a1.cpu().numpy(), a_ref)
+    s2, a2 = gpu_compress(wb_d, wf_d, PR, dev)
+    assert torch.equal(s1, s2) and torch.equal(a1, a2)
+    # per-matrix alpha on the same data (same bits)
+    s3, a3 = gpu_compress(wb_d, wf_d, PM, dev)
+    _, am_ref = oracle.compress(wb, wf, per_row=False)
+    assert torch.equal(s3, s1)
+    assert_alpha(a3.cpu().numpy(), am_ref)
+
+
+def test_compress_nonfinite_is_flagged(dev):
+    wb, wf, _ = synth.single_problem(3, 16, 256, 1)
+    wf = wf.copy()
+    wf[5, 17] = 0x7F80  # +inf
+    d = to_dev(wb, dev), to_dev(wf, dev)
+    signs = torch.empty((16, 8), dtype=torch.int32, device=dev)
+    alpha = torch.empty(16, dtype=torch.float32, device=dev)
+    ws = bd.new_workspace(bd.bd_compress_workspace_size(16, 256, PR), dev)
+    bd.bd_compress(d[0], d[1], PR, signs, alpha, ws)
+    assert bd.bd_check_async(ws) == bd.BD_ERR_NONFINITE
+    assert bd.bd_check_async(ws) == bd.BD_OK  # cleared
+    s_ref, _ = oracle.compress(wb, wf, per_row=True)
+    assert np.array_equal(u32(signs), s_ref)  # bits still written
+
+
+# ============================================================================ linear
+
+def test_linear_tiny(dev):
+    wb, wf, x = synth.single_problem(0, 256, 256, 4)
+    s_ref, a_ref = oracle.compress(wb, wf, per_row=False)
+    y_ref = oracle.linear(x, wb, s_ref, a_ref, per_row=False)
+    wb_d = to_dev(wb, dev)
+    s, a = gpu_compress(wb_d, to_dev(wf, dev), PM, dev)
+    for f32 in (True, False):
+        y = gpu_linear(to_dev(x, dev), wb_d, s, a, PM, dev, f32=f32)
+        check_linear(y_host(y), y_ref, bf16_out=not f32,
+                     bound=fp32_bound(x, wb, a.cpu().numpy(), False) if f32 else None, what=f"tiny f32={f32}")
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 9, 17, 33, 64, 65, 130])
+@pytest.mark.parametrize("d_out,d_in", [(1, 128), (17, 384), (48, 1024)])
+def test_linear_shapes(dev, T, d_out, d_in):
+    wb, wf, x = synth.single_problem(T * 131 + d_out, d_out, d_in, T)
+    s_ref, a_ref = oracle.compress(wb, wf, per_row=True)
+    y_ref = oracle.linear(x, wb, s_ref, a_ref, per_row=True)
+    wb_d = to_dev(wb, dev)
+    s, a = gpu_compress(wb_d, to_dev(wf, dev), PR, dev)
+    y = gpu_linear(to_dev(x, dev), wb_d, s, a, PR, dev)
+    check_linear(y_host(y), y_ref, bf16_out=False, bound=fp32_bound(x, wb, a.cpu().numpy(), True),
+                 what=f"T={T} {d_out}x{d_in}")
+
+
+def _dyadic_problem(seed, d_out, d_in, T, per_row):
+    """x in {-4..4}, W_base in {k/64}, Delta = +-2^-e: every partial sum is exact in fp32."""
+    rng = np.random.default_rng(seed)
+    wb = rng.integers(-8, 9, size=(d_out, d_in)).astype(np.float32) / 64.0
+    e = rng.integers(5, 9, size=d_out if per_row else 1).astype(np.float32)
+    s = np.where(rng.random((d_out, d_in)) < 0.5, -1.0, 1.0).astype(np.float32)
+    step = 2.0 ** -e
+    wf = wb + s * (step[:, None] if per_row else step[0])
+    x = rng.integers(-4, 5, size=(T, d_in)).astype(np.float32)
+    return synth.f32_to_bf16_bits(wb), synth.f32_to_bf16_bits(wf), synth.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("per_row", [True, False])
+@pytest.mark.parametrize("T", [1, 5, 16, 64, 100])
+def test_linear_exact_dyadic_bit_identical(dev, per_row, T):
+    wb, wf, x = _dyadic_problem(T, 40, 1024, T, per_row)
+    s_ref, a_ref = oracle.compress(wb, wf, per_row=per_row)
+    y_ref = oracle.linear(x, wb, s_ref, a_ref, per_row=per_row)
+    mode = PR if per_row else PM
+    wb_d = to_dev(wb, dev)
+    s, a = gpu_compress(wb_d, to_dev(wf, dev), mode, dev)
+    assert np.array_equal(u32(s), s_ref)
+    assert np.array_equal(a.cpu().numpy(), a_ref)
+    y = gpu_linear(to_dev(x, dev), wb_d, s, a, mode, dev)
+    assert np.array_equal(y.cpu().numpy().astype(np.float64), y_ref)
+
+
+@pytest.mark.parametrize("T", [1, 4, 16])
+def test_linear_ffn_decode_sampled_rows(dev, decode_problem, T):
+    wb, wf = decode_problem
+    x = synth.activations(np.random.default_rng(100 + T), T, 8192)
+    rows = synth.sample_rows(T, 28672, 384)
+    s_rows, a_rows = oracle.compress_rows(wb, wf, rows)
+    # the oracle indexes signs/alpha by absolute row: place the sampled rows
+    s_full = np.zeros((28672, 256), np.uint32)
+    a_full = np.zeros(28672, np.float32)
+    s_full[rows], a_full[rows] = s_rows, a_rows
+    y_ref = oracle.linear(x, wb, s_full, a_full, per_row=True, rows=rows)
+    wb_d = to_dev(wb, dev)
+    s, a = gpu_compress(wb_d, to_dev(wf, dev), PR, dev)
+    assert np.array_equal(u32(s)[rows], s_rows)
+    x_d = to_dev(x, dev)
+    for f32 in (True, False):
+        y = gpu_linear(x_d, wb_d, s, a, PR, dev, f32=f32)
+        yg = y_host(y)[:, rows]
+        check_linear(yg, y_ref, bf16_out=not f32,
+                     bound=fp32_bound(x, wb, a.cpu().numpy(), True, rows=rows) if f32 else None,
+                     what=f"ffn T={T} f32={f32}")
+
+
+@pytest.mark.parametrize("T", [4, 64])
+def test_linear_row_sharding_is_bit_identical(dev, T):
+    d_out, d_in = 300, 1024
+    wb, wf, x = synth.single_problem(77, d_out, d_in, T)
+    wb_d, x_d = to_dev(wb, dev), to_dev(x, dev)
+    s, a = gpu_compress(wb_d, to_dev(wf, dev), PR, dev)
+    y_full = gpu_linear(x_d, wb_d, s, a, PR, dev)
+    parts = []
+    for r0, r1 in [(0, 37), (37, 160), (160, 300)]:
+        parts.append(gpu_linear(x_d, wb_d[r0:r1], s[r0:r1], a[r0:r1], PR, dev))
+    assert torch.equal(torch.cat(parts, dim=1), y_full)
+
+
+def test_linear_zero_sizes_are_noops(dev):
+    wb = torch.zeros((4, 128), dtype=torch.int16, device=dev)
+    s = torch.zeros((4, 4), dtype=torch.int32, device=dev)
+    a = torch.zeros(4, dtype=torch.float32, device=dev)
+    ws = bd.new_workspace(256, dev)
+    x0 = torch.zeros((0, 128), dtype=torch.int16, device=dev)
+    y0 = torch.zeros((0, 4), dtype=torch.float32, device=dev)
+    lib = bd.load()
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.bd_linear(x0.data_ptr(), 0, wb.data_ptr(), s.data_ptr(), a.data_ptr(), PR, 4, 128, y0.data_ptr(),
+                         1, ws.data_ptr(), ws.numel(), st) == bd.BD_OK
+    assert lib.bd_compress(wb.data_ptr(), wb.data_ptr(), 0, 128, PR, s.data_ptr(), a.data_ptr(), ws.data_ptr(),
+                           ws.numel(), st) == bd.BD_OK
+
+
+# ============================================================================ multi-variant
+
+@pytest.fixture(scope="module")
+def multi_problem():
+    """8192 x 8192 shared W_base, 14 variants (b ~ U[5e-4, 2e-3]), 64 Zipf tokens."""
+    return synth.multi_problem(0, 8192, 8192, 64, 14)
+
+
+def test_multi_tenant_sampled_rows(dev, multi_problem):
+    wb, wfs, x, vid, _ = multi_problem
+    rows = synth.sample_rows(5, 8192, 256)
+    refs = [oracle.compress_rows(wb, wf, rows) for wf in wfs]
+    wb_d = to_dev(wb, dev)
+    s_l, a_l = [], []
+    for v, wf in enumerate(wfs):
+        s, a = gpu_compress(wb_d, to_dev(wf, dev), PR, dev)
+        assert np.array_equal(u32(s)[rows], refs[v][0]), f"variant {v} bits"
+        assert_alpha(a.cpu().numpy()[rows], refs[v][1])
+        s_l.append(s)
+        a_l.append(a)
+    s_full, a_full = [], []
+    for s_rows, a_rows in refs:
+        sf = np.zeros((8192, 256), np.uint32)
+        af = np.zeros(8192, np.float32)
+        sf[rows], af[rows] = s_rows, a_rows
+        s_full.append(sf)
+        a_full.append(af)
+    y_ref = oracle.linear_multi(x, vid, s_full, a_full, True, wb, rows=rows)
+    x_d, vid_d = to_dev(x, dev), to_dev(vid, dev)
+    for f32 in (True, False):
+        y = torch.empty((64, 8192), dtype=torch.float32 if f32 else torch.bfloat16, device=dev)
+        ws = bd.new_workspace(bd.bd_linear_multi_workspace_size(64, 14, 8192, 8192), dev)
+        bd.bd_linear_multi(x_d, vid_d, s_l, a_l, PR, wb_d, y, ws)
+        assert bd.bd_check_async(ws) == bd.BD_OK
+        check_linear(y_host(y)[:, rows], y_ref, bf16_out=not f32, what=f"multi f32={f32}")
+
+
+def _dyadic_multi(seed, V, d_out, d_in, T):
+    rng = np.random.default_rng(seed)
+    wb = rng.integers(-8, 9, size=(d_out, d_in)).astype(np.float32) / 64.0
+    wfs = []
+    for v in range(V):
+        s = np.where(rng.random((d_out, d_in)) < 0.5, -1.0, 1.0).astype(np.float32)
+        wfs.append(synth.f32_to_bf16_bits(wb + s * 2.0 ** -(3 + v % 6)))
+    x = rng.integers(-4, 5, size=(T, d_in)).astype(np.float32)
+    return synth.f32_to_bf16_bits(wb), wfs, synth.f32_to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("V,T", [(1, 1), (3, 10), (14, 64), (64, 64), (5, 150)])
+def test_multi_exact_routing_signature(dev, V, T):
+    """Distinct variant scales and sign patterns: a token routed to the wrong
+    variant changes its output by an exact, visible amount."""
+    d_out, d_in = 33, 512
+    wb, wfs, x = _dyadic_multi(V * 1000 + T, V, d_out, d_in, T)
+    rng = np.random.default_rng(T)
+    vid = rng.integers(-1, V, size=T).astype(np.int32)
+    refs = [oracle.compress(wb, wf, per_row=True) for wf in wfs]
+    y_ref = oracle.linear_multi(x, vid, [r[0] for r in refs], [r[1] for r in refs], True, wb)
+    wb_d = to_dev(wb, dev)
+    s_l, a_l = zip(*[gpu_compress(wb_d, to_dev(wf, dev), PR, dev) for wf in wfs])
+    y = torch.empty((T, d_out), dtype=torch.float32, device=dev)
+    ws = bd.new_workspace(256, dev)
+    bd.bd_linear_multi(to_dev(x, dev), to_dev(vid, dev), list(s_l), list(a_l), PR, wb_d, y, ws)
+    assert bd.bd_check_async(ws) == bd.BD_OK
+    assert np.array_equal(y.cpu().numpy().astype(np.float64), y_ref)
+
+
+def test_multi_bad_variant_flagged_and_computed_as_base(dev):
+    V, d_out, d_in, T = 3, 20, 256, 12
+    wb, wfs, x = _dyadic_multi(9, V, d_out, d_in, T)
+    vid = np.array([0, 1, 2, -1, 7, -3, 2, 1, 0, 3, -1, 1], np.int32)
+    refs = [oracle.compress(wb, wf, per_row=True) for wf in wfs]
+    y_ref = oracle.linear_multi(x, vid, [r[0] for r in refs], [r[1] for r in refs], True, wb)
+    wb_d = to_dev(wb, dev)
+    s_l, a_l = zip(*[gpu_compress(wb_d, to_dev(wf, dev), PR, dev) for wf in wfs])
+    y = torch.empty((T, d_out), dtype=torch.float32, device=dev)
+    ws = bd.new_workspace(256, dev)
+    bd.bd_linear_multi(to_dev(x, dev), to_dev(vid, dev), list(s_l), list(a_l), PR, wb_d, y, ws)
+    assert bd.bd_check_async(ws) == bd.BD_ERR_BAD_VARIANT
+    assert np.array_equal(y.cpu().numpy().astype(np.float64), y_ref)
+
+
+# ============================================================================ router
+
+@pytest.mark.parametrize("T,V", [(0, 3), (1, 0), (1, 1), (64, 14), (1000, 64), (5000, 7)])
+def test_route_bit_exact(dev, T, V):
+    rng = np.random.default_rng(T * 3 + V)
+    vid = rng.integers(-1, max(V, 1), size=T).astype(np.int32) if V > 0 else -np.ones(T, np.int32)
+    perm_ref, seg_ref, n_bad = oracle.route(vid, V)
+    vid_d = to_dev(vid, dev) if T else torch.zeros(1, dtype=torch.int32, device=dev)
+    perm = torch.full((max(T, 1),), -7, dtype=torch.int32, device=dev)
+    seg = torch.full((V + 2,), -7, dtype=torch.int32, device=dev)
+    ws = bd.new_workspace(bd.bd_route_workspace_size(T, V), dev)
+    lib = bd.load()
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.bd_route(vid_d.data_ptr(), T, V, perm.data_ptr(), seg.data_ptr(), ws.data_ptr(), ws.numel(),
+                        st) == bd.BD_OK
+    assert bd.bd_check_async(ws) == (bd.BD_OK if n_bad == 0 else bd.BD_ERR_BAD_VARIANT)
+    assert np.array_equal(perm.cpu().numpy()[:T], perm_ref)
+    assert np.array_equal(seg.cpu().numpy(), seg_ref)
+
+
+def test_route_flags_out_of_range(dev):
+    vid = np.array([2, -1, 9, 0, -4, 1], np.int32)
+    perm_ref, seg_ref, n_bad = oracle.route(vid, 3)
+    assert n_bad == 2
+    perm = torch.empty(6, dtype=torch.int32, device=dev)
+    seg = torch.empty(5, dtype=torch.int32, device=dev)
+    ws = bd.new_workspace(256, dev)
+    bd.bd_route(to_dev(vid, dev), 3, perm, seg, ws)
+    assert bd.bd_check_async(ws) == bd.BD_ERR_BAD_VARIANT
+    assert np.array_equal(perm.cpu().numpy(), perm_ref)
+    assert np.array_equal(seg.cpu().numpy(), seg_ref)
+
+
+# ============================================================================ invariants / hygiene
+
+@pytest.mark.parametrize("mode", [PR, PM])
+def test_reconstruction_invariants_on_device(dev, mode):
+    wb, wf, _ = synth.single_problem(31, 64, 512, 1)
+    wb_d = to_dev(wb, dev)
+    s, a = gpu_compress(wb_d, to_dev(wf, dev), mode, dev)
+    weff = torch.empty((64, 512), dtype=torch.float32, device=dev)
+    bd.bd_debug_reconstruct(wb_d, s, a, mode, weff)
+    torch.cuda.synchronize()
+    w = synth.bf16_bits_to_f32(wb).astype(np.float64)
+    al = a.cpu().numpy().astype(np.float64)
+    al = al[:, None] if mode == PR else al[0]
+    diff = weff.cpu().numpy().astype(np.float64) - w
+    delta = synth.bf16_bits_to_f32(wf).astype(np.float64) - w
+    code = np.where(delta < 0, -1.0, 1.0)
+    assert np.array_equal(np.sign(diff), code)  # sign(W_eff - W_base) = sign(Delta), sign(0) = +1
+    np.testing.assert_allclose(np.abs(diff), np.broadcast_to(al, diff.shape), rtol=2 ** -16)  # |.| = alpha
+
+
+def test_canary_guards_untouched(dev):
+    """Outputs written inside larger buffers: the 64 KiB of 0xA5 after each must survive."""
+    guard = 65536
+    d_out, d_in, T = 37, 384, 19
+    wb, wf, x = synth.single_problem(41, d_out, d_in, T)
+    wb_d, wf_d, x_d = to_dev(wb, dev), to_dev(wf, dev), to_dev(x, dev)
+    n_s = d_out * d_in // 32
+    sbuf = torch.full((n_s + guard // 4,), -1515870811, dtype=torch.int32, device=dev)  # 0xA5A5A5A5
+    abuf = torch.full((d_out + guard // 4,), 0.0, dtype=torch.float32, device=dev)
+    abuf.view(torch.int32)[:] = -1515870811
+    ybuf = torch.empty((T * d_out + guard // 4,), dtype=torch.float32, device=dev)
+    ybuf.view(torch.int32)[:] = -1515870811
+    ws = bd.new_workspace(256, dev)
+    s = sbuf[:n_s].view(d_out, d_in // 32)
+    a = abuf[:d_out]
+    bd.bd_compress(wb_d, wf_d, PR, s, a, ws)
+    y = ybuf[:T * d_out].view(T, d_out)
+    bd.bd_linear(x_d, wb_d, s, a, PR, y, ws)
+    bd.bd_linear_multi(x_d, torch.zeros(T, dtype=torch.int32, device=dev), [s], [a], PR, wb_d, y, ws)
+    assert bd.bd_check_async(ws) == bd.BD_OK
+    for buf, n in ((sbuf, n_s), (abuf.view(torch.int32), d_out), (ybuf.view(torch.int32), T * d_out)):
+        assert bool((buf[n:] == -1515870811).all())
+
+
+def test_argument_errors(dev):
+    lib = bd.load()
+    st = torch.cuda.current_stream().cuda_stream
+    wb = torch.zeros((16, 256), dtype=torch.int16, device=dev)
+    s = torch.zeros((16, 8), dtype=torch.int32, device=dev)
+    a = torch.zeros(16, dtype=torch.float32, device=dev)
+    x = torch.zeros((4, 256), dtype=torch.int16, device=dev)
+    y = torch.zeros((4, 16), dtype=torch.float32, device=dev)
+    ws = bd.new_workspace(1024, dev)
+    P = lambda t, off=0: t.data_ptr() + off  # noqa: E731
+    assert lib.bd_linear(P(x, 2), 4, P(wb), P(s), P(a), PR, 16, 256, P(y), 1, P(ws), 1024, st) == bd.BD_ERR_MISALIGNED
+    assert lib.bd_linear(P(x), 4, P(wb), P(s), P(a), PR, 16, 96, P(y), 1, P(ws), 1024, st) == \
+        bd.BD_ERR_UNSUPPORTED_SHAPE
+    assert lib.bd_linear(P(x), 4, P(wb), P(s), P(a), PR, 16, 256, P(y), 1, P(ws), 16, st) == bd.BD_ERR_WORKSPACE
+    assert lib.bd_linear(P(x), 4, P(wb), P(s), P(a), PR, 16, 256, P(x), 1, P(ws), 1024, st) == \
+        bd.BD_ERR_INVALID_ARG  # y aliases x
+    assert lib.bd_linear(P(x), 4, P(wb), P(s), P(a), 7, 16, 256, P(y), 1, P(ws), 1024, st) == bd.BD_ERR_INVALID_ARG
+    tab = (ctypes.c_void_p * 1)(P(s))
+    atab = (ctypes.c_void_p * 1)(P(a))
+    vid = torch.zeros(4, dtype=torch.int32, device=dev)
+    assert lib.bd_linear_multi(P(x), 4, P(vid), 0, ctypes.addressof(tab), ctypes.addressof(atab), PR, P(wb), 16, 256,
+                               P(y), 1, P(ws), 1024, st) == bd.BD_ERR_INVALID_ARG  # V = 0
+    assert lib.bd_compress(P(wb), P(wb), 16, 256, PR, P(s), P(a), P(ws, 16), 1000, st) == bd.BD_ERR_MISALIGNED
