@@ -154,7 +154,9 @@ class GpuRun:
         self.alpha = [torch.empty(wl.n_alpha, dtype=torch.float32, device=dev) for _ in wl.wf]
         self.ys = [torch.empty((T, wl.d_out), dtype=torch.bfloat16, device=dev) for T in wl.tokens]
         self.ws = bd.new_workspace(max(bd.bd_compress_workspace_size(wl.d_out, wl.d_in, PR),
-                                       bd.bd_linear_workspace_size(64, wl.d_out, wl.d_in)), dev)
+                                       bd.bd_linear_workspace_size(64, wl.d_out, wl.d_in),
+                                       bd.bd_linear_multi_workspace_size(64, max(len(wl.wf), 1), wl.d_out,
+                                                                         wl.d_in)), dev)
         self.vid = None if wl.vid is None else torch.from_numpy(wl.vid).to(dev)
         self.flush = None
         if wl.name == "multi":

@@ -203,9 +203,15 @@ bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const 
     return BD_OK;
 }
 
-size_t bd_linear_multi_workspace_size(int64_t /*T*/, int32_t /*V*/, int64_t /*d_out*/, int64_t /*d_in*/)
+// Multi-variant workspace: the error word, then (at 1 KiB) x of one token
+// group sorted by variant for the TMA loads.
+size_t bd_linear_multi_workspace_size(int64_t T, int32_t V, int64_t /*d_out*/, int64_t d_in)
 {
-    return kWsHeader;
+    if (T < 0 || d_in < 0 || V < 1 || V > BD_MAX_VARIANTS) return kWsHeader;
+    const int64_t group = bd::skinny_group_tokens(true, V);
+    const int64_t tg = T < group ? T : group;
+    const size_t n = 1024 + static_cast<size_t>(tg) * static_cast<size_t>(d_in) * 2;
+    return (n + 255) & ~static_cast<size_t>(255);
 }
 
 bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int32_t V,
@@ -235,12 +241,13 @@ bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int3
     if (bd_status s = device_info(&sms)) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t ysz = out_dtype == BD_OUT_F32 ? 4 : 2;
-    for (int64_t t0 = 0; t0 < T; t0 += bd::kSkinnyMaxTokens) {
+    const int64_t group = bd::skinny_group_tokens(true, V);
+    for (int64_t t0 = 0; t0 < T; t0 += group) {
         bd::SkinnyArgs a{};
         a.x = x + t0 * d_in;
         a.vid = vid + t0;
         a.w_base = w_base;
-        a.T = (T - t0) < bd::kSkinnyMaxTokens ? (T - t0) : bd::kSkinnyMaxTokens;
+        a.T = (T - t0) < group ? (T - t0) : group;
         a.d_out = d_out; a.d_in = d_in; a.V = V;
         a.per_row = alpha_mode == BD_ALPHA_PER_ROW;
         for (int v = 0; v < V; ++v) {
@@ -250,6 +257,7 @@ bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int3
         a.y = static_cast<char*>(y) + static_cast<size_t>(t0) * d_out * ysz;
         a.out_f32 = out_dtype == BD_OUT_F32;
         a.err = err_word(ws);
+        a.x_sorted = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + 1024);
         if (bd_status s = launched(bd::launch_skinny(a, sms, st))) return s;
     }
     return BD_OK;

@@ -37,9 +37,14 @@ struct SkinnyArgs {
     void* y;                  // [T][d_out]
     int out_f32;
     uint32_t* err;
+    uint16_t* x_sorted;       // multi-variant only: [T][d_in] scratch for x sorted by variant
 };
 
 cudaError_t launch_skinny(const SkinnyArgs& a, int sm_count, cudaStream_t stream);
+
+// Largest token group one skinny launch accepts (64, or fewer for the
+// multi-variant kernel when many variants would overflow shared memory).
+int skinny_group_tokens(bool multi, int V);
 
 // ---- router (bd_route.cu) ---------------------------------------------------------------------
 

@@ -9,55 +9,86 @@
 // base and the sign contraction are separate bf16 MMAs (s in {-1,+1} is exact
 // in bf16) that share the x operand, accumulated in fp32.
 //
-// Work split.  A CTA owns 16 output rows (one m16 MMA tile) and KS warps;
-// warp k reduces the k-th of KS equal slices of d_in (KS depends only on
-// d_in, so a row's arithmetic never depends on d_out).  Each warp runs its
-// own pipeline of `stages` shared-memory stages filled by bulk async copies
-// (cp.async.bulk + mbarrier): a stage holds 16 rows x 128 columns of W_base
-// (row pitch 272 B, so the fragment loads below are bank-conflict free) and,
-// per active variant, 16 rows x 4 sign words.  x is read straight from L2.
+// Work split.  A CTA owns a block of 16*NCONS output rows and one of CK equal
+// slices of d_in; the CK CTAs of a thread-block cluster cover all of d_in and
+// reduce their partial sums through distributed shared memory, in rank order
+// (CK depends on d_in and the kernel flavour only, never on d_out, so a row's
+// arithmetic does not change when the rows are sharded).  Inside the CTA one
+// producer thread streams 128-column stages into a ring of shared-memory
+// buffers with a handful of 2-D TMA boxes per stage and NCONS consumer warps
+// (16 rows each) run the MMAs:
+//   - W_base: two boxes [block rows x 64 columns], 128-byte swizzle;
+//   - x: two boxes [8*NT tokens x 64 columns], 128-byte swizzle (for the
+//     multi-variant kernel, from a copy of x already sorted by variant);
+//   - sign bits: one box [block rows x 4 words] per active variant;
+//   - full/empty mbarriers between producer and consumers, all waits bounded.
+// The swizzle puts 16-byte chunk c of a 128-byte row r at chunk c ^ (r % 8),
+// so the fragment loads below are bank-conflict free.
 //
 // Fragments.  mma.m16n8k16 wants, per thread (g = lane/4, q = lane%4), A
 // elements (row g / g+8, k = 2q,2q+1,2q+8,2q+9) and B elements (token g,
 // same k).  Any permutation of k applied to both operands leaves the sum
 // unchanged, so logical k {2q,2q+1,2q+8,2q+9} of MMA step m is mapped to
-// physical columns 16q+4m+{0,1,2,3} of the 64-column half-chunk: every
-// thread then reads 16 consecutive columns (two 16-byte loads) of its rows
-// and of its token, and the 16 sign bits of those columns are one half-word.
-// Bits become bf16 +-1 pairs with 2 integer ops per register.
+// physical columns 16q+4m+{0,1,2,3} of a 64-column half-stage: every thread
+// then reads 16 consecutive columns (two 16-byte loads) of its rows and of
+// its token, and the 16 sign bits of those columns are one half-word.  Bits
+// become bf16 +-1 pairs with 2 integer ops per register.
 //
 // Multi-variant.  The CTA groups its tokens by variant (stable counting
-// sort, key = vid+1, so base tokens come first) and walks 8-token tiles of
-// that order.  The base MMA runs once per tile; for every variant present in
-// the tile it expands that variant's bits once and runs the sign MMA with x
-// masked to the tile's tokens of that variant.  W_base is read once per CTA
-// whatever the number of variants; the sign bits of every active variant are
-// read once.
+// sort, key = vid+1, so base tokens come first); x rows are staged in that
+// order and processed as 8-token tiles.  The base MMA runs once per tile; for
+// every variant present in the tile the consumer expands that variant's bits
+// once and runs the sign MMA with x masked to the tile's tokens of that
+// variant.  W_base is read once per CTA whatever the number of variants; the
+// sign bits of every active variant are read once.  A small pre-pass
+// (gather_sorted_x) writes x in that sorted order into the workspace so that
+// it can be loaded by TMA boxes.
+#include <cooperative_groups.h>
+
 #include "bd_device.cuh"
+#include "bd_tma.h"
+
+namespace cg = cooperative_groups;
 
 namespace bd {
 namespace {
 
-constexpr int kChunk = 128;                 // columns per pipeline stage
-constexpr int kWPitch = 272;                // staged W row pitch (256 data + 16 pad)
-constexpr int kWStageBytes = 16 * kWPitch;  // 4352
-constexpr int kSignTileBytes = 16 * 16;     // 16 rows x 4 words
+constexpr int kChunk = 128;        // columns per pipeline stage
+constexpr int kHalfRowBytes = 128;  // one 64-column half of a staged row (one swizzle atom)
+constexpr int kSignRowBytes = 16;  // 4 sign words per row per stage
 constexpr int kMaxStages = 4;
-constexpr int kMaxWarps = 8;
 constexpr int kMaxKeys = kMaxVariants + 1;
+constexpr int kSingleConsumers = 4;  // 64 rows per CTA, up to three CTAs per SM
+constexpr int kMultiConsumers = 6;   // 96 rows per CTA: three 14-variant stages fit in shared memory
+constexpr size_t kSingleBudget = 66u * 1024u;  // three CTAs per SM (measured best on GB300)
+constexpr size_t kMultiBudget = 220u * 1024u;
 
-struct alignas(16) SkinnyShared {
-    uint64_t mbar[kMaxWarps][kMaxStages];
-    const uint32_t* sign_ptr[kSkinnyMaxTokens];  // per active slot
-    const float* alpha_ptr[kSkinnyMaxTokens];
-    int key[kSkinnyMaxTokens];       // key of token t (caller order)
-    int perm[kSkinnyMaxTokens];      // sorted position -> token
-    int keyp[kSkinnyMaxTokens];      // sorted position -> key
+struct SkinnyParams {
+    CUtensorMap sign_map[kMaxVariants];  // [d_out][d_in/32] uint32, box 4 x block rows
+    CUtensorMap w_map;                   // [d_out][d_in] bf16, box 64 x block rows, 128B swizzle
+    CUtensorMap x_map;                   // [T][d_in] bf16 (sorted copy for multi), box 64 x 8*NT, 128B swizzle
+    const int32_t* vid;
+    const float* alpha[kMaxVariants];
+    void* y;
+    uint32_t* err;
+    int64_t T, d_out, d_in;
+    int V, per_row, out_f32;
+    int CK, stages, sign_slots;
+};
+
+struct SkinnyShared {
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
+    int key[kSkinnyMaxTokens];   // key of token t (caller order)
+    int perm[kSkinnyMaxTokens];  // sorted position -> token
+    int keyp[kSkinnyMaxTokens];  // sorted position -> key
     int seg[kMaxKeys + 1];
     int slot_of_key[kMaxKeys];
+    int act[kSkinnyMaxTokens];   // slot -> variant id
     int tile_first[kSkinnyMaxTokens / 8];
     int tile_last[kSkinnyMaxTokens / 8];
     int n_act;
+    volatile int abort;
 };
 
 // 16 sign bits (bit b = column b) -> 8 registers of bf16 pairs (+1 / -1);
@@ -78,33 +109,37 @@ __device__ __forceinline__ void mma4(float (&acc)[4], const uint32_t (&r0)[8], c
     mma_bf16_16816(acc, r0[6], r1[6], r0[7], r1[7], xb.z, xb.w);
 }
 
-// Two CTAs per SM fit the register file only for the smaller token tiles.
-template <int NT, bool MULTI>
-constexpr int ctas_per_sm() { return (MULTI || NT >= 4) ? 1 : 2; }
-
-template <int NT, bool MULTI>
-__global__ void __launch_bounds__(32 * kMaxWarps, ctas_per_sm<NT, MULTI>())
-    skinny_kernel(const __grid_constant__ SkinnyArgs a, int KS, int stages, int sign_slots)
+// Bounded wait that also gives up as soon as another warp of the CTA has
+// timed out (sets the CTA-wide abort flag and the error word on timeout).
+__device__ __forceinline__ bool wait_or_abort(SkinnyShared& sh, uint64_t* bar, uint32_t parity, uint32_t* err)
 {
-    extern __shared__ __align__(128) uint8_t dyn_smem[];
-    __shared__ SkinnyShared sh;
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (sh.abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            sh.abort = 1;
+            raise_error(err, kErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
 
-    const int tid = threadIdx.x;
-    const int warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, q = lane & 3;
-    const int T = static_cast<int>(a.T);
-    const int64_t d_in = a.d_in;
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x) * 16;
-    const int valid_rows = static_cast<int>(a.d_out - row0 < 16 ? a.d_out - row0 : 16);
-
-    // ---------------------------------------------------------------- routing (per CTA)
+// Groups the T (<= 64) tokens by key = vid + 1 (0 = base model or an
+// out-of-range id) with a stable counting sort: perm[pos] = token,
+// keyp[pos] = its key; lists the active variants (slot -> id).  Every CTA of
+// a launch, and the x gather pre-pass, computes the same result.
+template <bool MULTI>
+__device__ void route_tokens(SkinnyShared& sh, const int32_t* vid, int T, int V, uint32_t* err, int tid)
+{
     if (MULTI) {
         if (tid < kSkinnyMaxTokens) {
             int k = kMaxKeys;  // past T: never counted
             if (tid < T) {
-                const int v = a.vid[tid];
-                const bool ok = (v >= -1 && v < a.V);
-                if (!ok && blockIdx.x == 0) raise_error(a.err, kErrBadVariant);
+                const int v = vid[tid];
+                const bool ok = (v >= -1 && v < V);
+                if (!ok && blockIdx.x == 0) raise_error(err, kErrBadVariant);
                 k = ok ? v + 1 : 0;
             }
             sh.key[tid] = k;
@@ -112,17 +147,16 @@ __global__ void __launch_bounds__(32 * kMaxWarps, ctas_per_sm<NT, MULTI>())
         __syncthreads();
         if (tid == 0) {
             int cnt[kMaxKeys];
-            for (int k = 0; k <= a.V; ++k) cnt[k] = 0;
+            for (int k = 0; k <= V; ++k) cnt[k] = 0;
             for (int t = 0; t < T; ++t) ++cnt[sh.key[t]];
             sh.seg[0] = 0;
             int n_act = 0;
-            for (int k = 0; k <= a.V; ++k) {
+            for (int k = 0; k <= V; ++k) {
                 sh.seg[k + 1] = sh.seg[k] + cnt[k];
                 sh.slot_of_key[k] = -1;
                 if (k >= 1 && cnt[k] > 0) {
                     sh.slot_of_key[k] = n_act;
-                    sh.sign_ptr[n_act] = a.signs[k - 1];
-                    sh.alpha_ptr[n_act] = a.alpha[k - 1];
+                    sh.act[n_act] = k - 1;
                     ++n_act;
                 }
             }
@@ -131,10 +165,10 @@ __global__ void __launch_bounds__(32 * kMaxWarps, ctas_per_sm<NT, MULTI>())
         __syncthreads();
         if (tid < T) {
             const int k = sh.key[tid];
-            int rank = 0;
-            for (int t = 0; t < tid; ++t) rank += (sh.key[t] == k);
-            sh.perm[sh.seg[k] + rank] = tid;
-            sh.keyp[sh.seg[k] + rank] = k;
+            int r = 0;
+            for (int t = 0; t < tid; ++t) r += (sh.key[t] == k);
+            sh.perm[sh.seg[k] + r] = tid;
+            sh.keyp[sh.seg[k] + r] = k;
         }
     } else {
         if (tid < T) {
@@ -143,14 +177,55 @@ __global__ void __launch_bounds__(32 * kMaxWarps, ctas_per_sm<NT, MULTI>())
         }
         if (tid == 0) {
             sh.n_act = 1;
+            sh.act[0] = 0;
             sh.slot_of_key[0] = -1;
             sh.slot_of_key[1] = 0;
-            sh.sign_ptr[0] = a.signs[0];
-            sh.alpha_ptr[0] = a.alpha[0];
         }
     }
-    if (lane == 0 && warp < KS)
-        for (int s = 0; s < stages; ++s) mbar_init(&sh.mbar[warp][s], 1);
+    __syncthreads();
+}
+
+template <bool MULTI>
+constexpr int ctas_per_sm()
+{
+    return MULTI ? 1 : 2;
+}
+
+template <int NT, bool MULTI, int NCONS>
+__global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
+    skinny_kernel(const __grid_constant__ SkinnyParams p)
+{
+    constexpr int kRows = 16 * NCONS;       // rows per CTA
+    constexpr int kSignTile = kRows * kSignRowBytes;
+    constexpr int kThreads = 32 * (NCONS + 1);
+    constexpr int Tpad = 8 * NT;
+
+    extern __shared__ uint8_t dyn_raw[];
+    __shared__ SkinnyShared sh;
+    // 1024-byte aligned base for the stage ring (the allocation has the slack)
+    uint8_t* dyn = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, q = lane & 3;
+    const int T = static_cast<int>(p.T);
+    const int64_t d_in = p.d_in;
+    const int CK = p.CK;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int64_t row0 = static_cast<int64_t>(blockIdx.x / CK) * kRows;
+    const int valid_rows = static_cast<int>(p.d_out - row0 < kRows ? p.d_out - row0 : kRows);
+
+    // ---------------------------------------------------------------- routing (per CTA)
+    route_tokens<MULTI>(sh, p.vid, T, p.V, p.err, tid);
+    if (tid == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], NCONS);
+        }
+        sh.abort = 0;
+        fence_mbarrier_init();
+    }
     __syncthreads();
     if (tid < NT) {
         const int p0 = 8 * tid;
@@ -160,70 +235,87 @@ __global__ void __launch_bounds__(32 * kMaxWarps, ctas_per_sm<NT, MULTI>())
     }
     __syncthreads();
 
-    // ---------------------------------------------------------------- per-warp K slice
+    // ---------------------------------------------------------------- pipeline
+    // stage layout: [W half 0 | W half 1 | x half 0 | x half 1 | sign tiles], 1024-byte aligned
+    const int stages = p.stages;
     const int n_act = sh.n_act;
-    const int stage_bytes = kWStageBytes + sign_slots * kSignTileBytes;
+    constexpr int kWHalf = kRows * kHalfRowBytes;
+    constexpr int kXHalf = Tpad * kHalfRowBytes;
+    constexpr int kSignOff = 2 * kWHalf + 2 * kXHalf;
+    const int stage_bytes = (kSignOff + p.sign_slots * kSignTile + 1023) & ~1023;
     const int nc = static_cast<int>(d_in / kChunk);
-    const int c_begin = static_cast<int>(static_cast<int64_t>(warp) * nc / KS);
-    const int c_end = static_cast<int>(static_cast<int64_t>(warp + 1) * nc / KS);
+    const int c_begin = static_cast<int>(static_cast<int64_t>(rank) * nc / CK);
+    const int c_end = static_cast<int>(static_cast<int64_t>(rank + 1) * nc / CK);
     const int n_chunks = c_end - c_begin;
-    uint8_t* wsm = dyn_smem + static_cast<size_t>(warp) * stages * stage_bytes;
-    const uint32_t tx_bytes = static_cast<uint32_t>(valid_rows) * (256u + 16u * n_act);
-    const int64_t sign_row_words = d_in / 32;
-
-    auto issue = [&](int c, int s) {
-        uint8_t* st = wsm + s * stage_bytes;
-        uint64_t* bar = &sh.mbar[warp][s];
-        if (lane == 0) mbar_arrive_expect_tx(bar, tx_bytes);
-        __syncwarp();
-        if (lane < valid_rows)
-            bulk_g2s(st + lane * kWPitch, a.w_base + (row0 + lane) * d_in + static_cast<int64_t>(c) * kChunk, 256,
-                     bar);
-        for (int idx = lane; idx < n_act * 16; idx += 32) {
-            const int slot = idx >> 4, i = idx & 15;
-            if (i < valid_rows)
-                bulk_g2s(st + kWStageBytes + slot * kSignTileBytes + i * 16,
-                         sh.sign_ptr[slot] + (row0 + i) * sign_row_words + c * 4, 16, bar);
-        }
-    };
 
     float accb[NT][4], accs[NT][4];
-    int my_key[NT];
-    const uint16_t* xrow[NT];
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
+    for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) accb[j][e] = accs[j][e] = 0.0f;
-        const int p = 8 * j + g;
-        my_key[j] = p < T ? sh.keyp[p] : -1;
-        xrow[j] = p < T ? a.x + static_cast<int64_t>(sh.perm[p]) * d_in : nullptr;
-    }
 
-    bool timed_out = false;
-    int issued = 0;
-    if (warp < KS) {
-        const int pre = n_chunks < stages ? n_chunks : stages;
-        for (int i = 0; i < pre; ++i) issue(c_begin + i, i);
-        issued = pre;
+    if (warp == NCONS) {
+        // ------------------------------------------------------------ producer warp
+        const uint32_t tx = static_cast<uint32_t>(2 * kWHalf + 2 * kXHalf + n_act * kSignTile);
+        int issued = 0;
         for (int i = 0; i < n_chunks; ++i) {
             const int s = i % stages;
-            const uint32_t parity = static_cast<uint32_t>(i / stages) & 1u;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(&sh.mbar[warp][s], parity))) {
-                timed_out = true;
-                // drain what is still in flight before the smem is reused
-                for (int k = i + 1; k < issued; ++k)
-                    mbar_wait_bounded(&sh.mbar[warp][k % stages], static_cast<uint32_t>(k / stages) & 1u);
+            if (i >= stages &&
+                !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty[s], static_cast<uint32_t>(i / stages - 1) & 1u,
+                                                       p.err)))
                 break;
+            uint8_t* st = dyn + static_cast<size_t>(s) * stage_bytes;
+            const int col = (c_begin + i) * kChunk;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&sh.full[s], tx);
+                tma_load_2d(st, &p.w_map, col, static_cast<int>(row0), &sh.full[s]);
+                tma_load_2d(st + kWHalf, &p.w_map, col + 64, static_cast<int>(row0), &sh.full[s]);
+                tma_load_2d(st + 2 * kWHalf, &p.x_map, col, 0, &sh.full[s]);
+                tma_load_2d(st + 2 * kWHalf + kXHalf, &p.x_map, col + 64, 0, &sh.full[s]);
             }
-            const uint8_t* st = wsm + s * stage_bytes;
-            const int c = c_begin + i;
+            __syncwarp();
+            for (int a = lane; a < n_act; a += 32)
+                tma_load_2d(st + kSignOff + a * kSignTile, &p.sign_map[sh.act[a]], col / 32, static_cast<int>(row0),
+                            &sh.full[s]);
+            ++issued;
+        }
+        // every issued stage must have landed before the CTA reuses or frees the memory
+        for (int i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+            const int s = i % stages;
+            const uint32_t par = static_cast<uint32_t>(i / stages) & 1u;
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(&sh.full[s], par) && global_timer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ consumer warps
+        const int rl0 = 16 * warp + g;  // local rows rl0 and rl0 + 8 (both = g mod 8)
+        const int c0 = ((2 * q) ^ g) << 4, c1 = ((2 * q + 1) ^ g) << 4;  // swizzled chunk offsets
+        int my_key[NT];
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+            const int pos = 8 * j + g;
+            my_key[j] = pos < T ? sh.keyp[pos] : -1;
+        }
+        for (int i = 0; i < n_chunks; ++i) {
+            const int s = i % stages;
+            if (!__all_sync(0xffffffffu,
+                            wait_or_abort(sh, &sh.full[s], static_cast<uint32_t>(i / stages) & 1u, p.err)))
+                break;
+            const uint8_t* st = dyn + static_cast<size_t>(s) * stage_bytes;
+            const uint32_t* sgn = reinterpret_cast<const uint32_t*>(st + kSignOff);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const uint4* w0 = reinterpret_cast<const uint4*>(st + g * kWPitch + h * 128 + q * 32);
-                const uint4* w1 = reinterpret_cast<const uint4*>(st + (g + 8) * kWPitch + h * 128 + q * 32);
+                const uint8_t* wst = st + h * kWHalf;
+                const uint8_t* xst = st + 2 * kWHalf + h * kXHalf;
                 uint32_t W0[8], W1[8];
                 {
-                    const uint4 u0 = w0[0], u1 = w0[1], v0 = w1[0], v1 = w1[1];
+                    const uint8_t* r0p = wst + rl0 * kHalfRowBytes;
+                    const uint8_t* r1p = wst + (rl0 + 8) * kHalfRowBytes;
+                    const uint4 u0 = *reinterpret_cast<const uint4*>(r0p + c0);
+                    const uint4 u1 = *reinterpret_cast<const uint4*>(r0p + c1);
+                    const uint4 v0 = *reinterpret_cast<const uint4*>(r1p + c0);
+                    const uint4 v1 = *reinterpret_cast<const uint4*>(r1p + c1);
                     W0[0] = u0.x; W0[1] = u0.y; W0[2] = u0.z; W0[3] = u0.w;
                     W0[4] = u1.x; W0[5] = u1.y; W0[6] = u1.z; W0[7] = u1.w;
                     W1[0] = v0.x; W1[1] = v0.y; W1[2] = v0.z; W1[3] = v0.w;
@@ -234,18 +326,14 @@ __global__ void __launch_bounds__(32 * kMaxWarps, ctas_per_sm<NT, MULTI>())
                 uint32_t S0[8], S1[8];
                 int cur_slot = -1;
                 if (!MULTI) {
-                    const uint32_t* sb = reinterpret_cast<const uint32_t*>(st + kWStageBytes);
-                    expand_signs((sb[g * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
-                    expand_signs((sb[(g + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
+                    expand_signs((sgn[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
+                    expand_signs((sgn[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
                 }
-                const int64_t xcol = static_cast<int64_t>(c) * kChunk + h * 64 + q * 16;
 #pragma unroll
                 for (int j = 0; j < NT; ++j) {
-                    uint4 xa = make_uint4(0u, 0u, 0u, 0u), xb = xa;
-                    if (xrow[j] != nullptr) {
-                        xa = ld_nc_v4(xrow[j] + xcol);
-                        xb = ld_nc_v4(xrow[j] + xcol + 8);
-                    }
+                    const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
+                    const uint4 xa = *reinterpret_cast<const uint4*>(xr + c0);
+                    const uint4 xb = *reinterpret_cast<const uint4*>(xr + c1);
                     mma4(accb[j], W0, W1, xa, xb);
                     if (!MULTI) {
                         mma4(accs[j], S0, S1, xa, xb);
@@ -257,10 +345,9 @@ __global__ void __launch_bounds__(32 * kMaxWarps, ctas_per_sm<NT, MULTI>())
                             if (slot < 0) continue;
                             if (slot != cur_slot) {
                                 cur_slot = slot;
-                                const uint32_t* sb =
-                                    reinterpret_cast<const uint32_t*>(st + kWStageBytes + slot * kSignTileBytes);
-                                expand_signs((sb[g * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
-                                expand_signs((sb[(g + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
+                                const uint32_t* sb = sgn + slot * (kSignTile / 4);
+                                expand_signs((sb[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
+                                expand_signs((sb[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
                             }
                             const bool mine = (my_key[j] == k);
                             const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -270,107 +357,188 @@ __global__ void __launch_bounds__(32 * kMaxWarps, ctas_per_sm<NT, MULTI>())
                 }
             }
             __syncwarp();
-            if (i + stages < n_chunks) {
-                fence_proxy_async_smem();
-                issue(c + stages, s);
-                ++issued;
-            }
+            if (lane == 0) mbar_arrive(&sh.empty[s]);
         }
-        if (timed_out && lane == 0) raise_error(a.err, kErrTimeout);
     }
 
-    // ---------------------------------------------------------------- K-slice reduction
-    constexpr int Tpad = NT * 8;
-    __syncthreads();  // every warp has drained its pipeline: reuse the stage memory
-    float* red_b = reinterpret_cast<float*>(dyn_smem);
-    float* red_s = red_b + KS * 16 * Tpad;
-    if (warp < KS) {
+    // ---------------------------------------------------------------- cluster K reduction
+    __syncthreads();  // pipeline drained: the stage memory becomes the reduction buffer
+    float* red_b = reinterpret_cast<float*>(dyn);
+    float* red_s = red_b + kRows * Tpad;
+    if (warp < NCONS) {
+        const int r0 = 16 * warp + g;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
-            const int p = 8 * j + 2 * q;
-            float* rb0 = red_b + (warp * 16 + g) * Tpad + p;
-            float* rb1 = red_b + (warp * 16 + g + 8) * Tpad + p;
-            float* rs0 = red_s + (warp * 16 + g) * Tpad + p;
-            float* rs1 = red_s + (warp * 16 + g + 8) * Tpad + p;
-            rb0[0] = accb[j][0]; rb0[1] = accb[j][1]; rb1[0] = accb[j][2]; rb1[1] = accb[j][3];
-            rs0[0] = accs[j][0]; rs0[1] = accs[j][1]; rs1[0] = accs[j][2]; rs1[1] = accs[j][3];
+            const int pos = 8 * j + 2 * q;
+            red_b[r0 * Tpad + pos] = accb[j][0];
+            red_b[r0 * Tpad + pos + 1] = accb[j][1];
+            red_b[(r0 + 8) * Tpad + pos] = accb[j][2];
+            red_b[(r0 + 8) * Tpad + pos + 1] = accb[j][3];
+            red_s[r0 * Tpad + pos] = accs[j][0];
+            red_s[r0 * Tpad + pos + 1] = accs[j][1];
+            red_s[(r0 + 8) * Tpad + pos] = accs[j][2];
+            red_s[(r0 + 8) * Tpad + pos + 1] = accs[j][3];
         }
     }
-    __syncthreads();
-    for (int o = tid; o < 16 * T; o += blockDim.x) {
-        const int p = o >> 4, r = o & 15;
+    cluster.sync();
+    const int r_lo = rank * kRows / CK, r_hi = (rank + 1) * kRows / CK;
+    const int nr = r_hi - r_lo;
+    for (int o = tid; o < nr * T; o += kThreads) {
+        const int pos = o / nr, r = r_lo + o % nr;
         if (r >= valid_rows) continue;
-        float b = 0.0f, s = 0.0f;
-        for (int k = 0; k < KS; ++k) {
-            b += red_b[(k * 16 + r) * Tpad + p];
-            s += red_s[(k * 16 + r) * Tpad + p];
+        float b = 0.0f, sg = 0.0f;
+        for (int k = 0; k < CK; ++k) {
+            const float* pb = cluster.map_shared_rank(red_b, k);
+            const float* ps = cluster.map_shared_rank(red_s, k);
+            b += pb[r * Tpad + pos];
+            sg += ps[r * Tpad + pos];
         }
-        const int key = sh.keyp[p];
+        const int key = sh.keyp[pos];
         const int slot = key >= 1 ? sh.slot_of_key[key] : -1;
         const int64_t row = row0 + r;
         float y = b;
-        if (slot >= 0) {
-            const float al = sh.alpha_ptr[slot][a.per_row ? row : 0];
-            y = fmaf(al, s, b);
-        }
-        const int64_t idx = static_cast<int64_t>(sh.perm[p]) * a.d_out + row;
-        if (a.out_f32)
-            static_cast<float*>(a.y)[idx] = y;
+        if (slot >= 0) y = fmaf(p.alpha[sh.act[slot]][p.per_row ? row : 0], sg, b);
+        const int64_t idx = static_cast<int64_t>(sh.perm[pos]) * p.d_out + row;
+        if (p.out_f32)
+            static_cast<float*>(p.y)[idx] = y;
         else
-            static_cast<__nv_bfloat16*>(a.y)[idx] = __float2bfloat16_rn(y);
+            static_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(y);
+    }
+    cluster.sync();  // peers may still read this CTA's partials until here
+}
+
+template <int NT, bool MULTI, int NCONS>
+cudaError_t launch_cfg(const SkinnyParams& prm, size_t smem, cudaStream_t stream)
+{
+    auto kern = skinny_kernel<NT, MULTI, NCONS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    constexpr int kRows = 16 * NCONS;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(static_cast<unsigned>((prm.d_out + kRows - 1) / kRows * prm.CK));
+    cfg.blockDim = dim3(32 * (NCONS + 1));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(prm.CK);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
+template <bool MULTI, int NCONS>
+cudaError_t launch_nt(int nt, const SkinnyParams& prm, size_t smem, cudaStream_t stream)
+{
+    switch (nt) {
+        case 1: return launch_cfg<1, MULTI, NCONS>(prm, smem, stream);
+        case 2: return launch_cfg<2, MULTI, NCONS>(prm, smem, stream);
+        case 4: return launch_cfg<4, MULTI, NCONS>(prm, smem, stream);
+        default: return launch_cfg<8, MULTI, NCONS>(prm, smem, stream);
     }
 }
 
-template <int NT, bool MULTI>
-cudaError_t launch_nt(const SkinnyArgs& a, int KS, int stages, int sign_slots, size_t smem, cudaStream_t stream)
+int tiles_for(int T) { return T <= 8 ? 1 : T <= 16 ? 2 : T <= 32 ? 4 : 8; }
+
+size_t stage_bytes_for(int rows, int sign_slots, int nt)
 {
-    auto kern = skinny_kernel<NT, MULTI>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>((a.d_out + 15) / 16);
-    kern<<<grid, 32 * kMaxWarps, smem, stream>>>(a, KS, stages, sign_slots);
-    return cudaGetLastError();
+    const size_t raw = 2u * rows * kHalfRowBytes + 2u * (8u * nt) * kHalfRowBytes +
+                       static_cast<size_t>(sign_slots) * rows * kSignRowBytes;
+    return (raw + 1023u) & ~static_cast<size_t>(1023u);
+}
+
+// Writes x in the order of the per-CTA router (sorted by variant) so the
+// multi-variant kernel can load it with TMA boxes.
+__global__ void __launch_bounds__(256) gather_sorted_x_kernel(const uint16_t* __restrict__ x,
+                                                               const int32_t* __restrict__ vid, int T, int V,
+                                                               int64_t d_in, uint16_t* __restrict__ xs)
+{
+    __shared__ SkinnyShared sh;
+    route_tokens<true>(sh, vid, T, V, nullptr, threadIdx.x);
+    const int64_t nvec = d_in / 8;
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < T * nvec;
+         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t pos = idx / nvec, v = idx % nvec;
+        reinterpret_cast<uint4*>(xs + pos * d_in)[v] = ld_nc_v4(x + static_cast<int64_t>(sh.perm[pos]) * d_in + 8 * v);
+    }
 }
 
 }  // namespace
 
+int skinny_group_tokens(bool multi, int V)
+{
+    if (!multi) return kSkinnyMaxTokens;
+    const int rows = 16 * kMultiConsumers;
+    for (int G = kSkinnyMaxTokens; G > 8; G /= 2) {
+        const int slots = V < G ? V : G;
+        if (3 * stage_bytes_for(rows, slots, tiles_for(G)) + 1024 <= kMultiBudget) return G;
+    }
+    return 8;
+}
+
 cudaError_t launch_skinny(const SkinnyArgs& a, int /*sm_count*/, cudaStream_t stream)
 {
     const bool multi = a.vid != nullptr;
+    const int rows = 16 * (multi ? kMultiConsumers : kSingleConsumers);
     const int nc = static_cast<int>(a.d_in / kChunk);
     const int T = static_cast<int>(a.T);
-    const int nt = T <= 8 ? 1 : T <= 16 ? 2 : T <= 32 ? 4 : 8;
-    int sign_slots = 1;
-    if (multi) sign_slots = a.V < T ? a.V : T;
-    const size_t stage_bytes = kWStageBytes + static_cast<size_t>(sign_slots) * kSignTileBytes;
-    // Two CTAs per SM (<= ~110 KB each) where the registers allow it, else one
-    // (<= ~200 KB).
-    const size_t budget = (multi || nt >= 4) ? 200u * 1024u : 110u * 1024u;
-    // K slices: up to 8, each warp needing at least two stages in the budget.
-    // The count depends on d_in (and, for many variants, on the stage size),
-    // never on d_out.
-    int KS = nc < kMaxWarps ? nc : kMaxWarps;
-    while (KS > 1 && static_cast<size_t>(KS) * 2 * stage_bytes > budget) --KS;
+    const int nt = tiles_for(T);
+    if (T < 1 || T > skinny_group_tokens(multi, a.V)) return cudaErrorInvalidValue;
+    if (multi && a.x_sorted == nullptr) return cudaErrorInvalidValue;
+
+    static thread_local SkinnyParams prm;  // ~9 KB: kept off the stack
+    prm.vid = a.vid;
+    prm.y = a.y;
+    prm.err = a.err;
+    prm.T = a.T;
+    prm.d_out = a.d_out;
+    prm.d_in = a.d_in;
+    prm.V = a.V;
+    prm.per_row = a.per_row;
+    prm.out_f32 = a.out_f32;
+    for (int v = 0; v < a.V; ++v) {
+        prm.alpha[v] = a.alpha[v];
+        if (!encode_tma_2d(&prm.sign_map[v], CU_TENSOR_MAP_DATA_TYPE_UINT32, a.signs[v],
+                           static_cast<uint64_t>(a.d_in / 32), static_cast<uint64_t>(a.d_out),
+                           static_cast<uint64_t>(a.d_in / 8), 4, static_cast<uint32_t>(rows),
+                           CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+    const uint16_t* xsrc = multi ? a.x_sorted : a.x;
+    if (!encode_tma_2d(&prm.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
+                       static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, 64,
+                       static_cast<uint32_t>(rows), CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xsrc, static_cast<uint64_t>(a.d_in),
+                       static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, 64,
+                       static_cast<uint32_t>(8 * nt), CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    // K slices per cluster: a function of d_in and the kernel flavour only
+    // (one per 4096 columns single-variant, per 2048 multi-variant, at most 4;
+    // measured best on GB300 for d_in = 8192).
+    int ck = multi ? nc / 16 : nc / 32;
+    ck = ck < 1 ? 1 : ck > 4 ? 4 : ck;
+    prm.CK = ck;
+    prm.sign_slots = multi ? (a.V < T ? a.V : T) : 1;
+    const size_t stage_bytes = stage_bytes_for(rows, prm.sign_slots, nt);
+    const size_t budget = multi ? kMultiBudget : kSingleBudget;
     int stages = kMaxStages;
-    while (stages > 2 && static_cast<size_t>(KS) * stages * stage_bytes > budget) --stages;
-    const size_t pipe = static_cast<size_t>(KS) * stages * stage_bytes;
-    const size_t red = 2u * KS * 16u * (nt * 8u) * sizeof(float);
-    const size_t smem = pipe > red ? pipe : red;
+    while (stages > 2 && stages * stage_bytes + 1024 > budget) --stages;
+    prm.stages = stages;
+    const size_t red = 2u * rows * (8u * nt) * sizeof(float);
+    size_t smem = stages * stage_bytes;
+    smem = (smem > red ? smem : red) + 1024;
     if (smem > 227u * 1024u) return cudaErrorInvalidConfiguration;
     if (multi) {
-        switch (nt) {
-            case 1: return launch_nt<1, true>(a, KS, stages, sign_slots, smem, stream);
-            case 2: return launch_nt<2, true>(a, KS, stages, sign_slots, smem, stream);
-            case 4: return launch_nt<4, true>(a, KS, stages, sign_slots, smem, stream);
-            default: return launch_nt<8, true>(a, KS, stages, sign_slots, smem, stream);
-        }
+        const int64_t nvec = static_cast<int64_t>(T) * (a.d_in / 8);
+        const int blocks = static_cast<int>((nvec + 255) / 256 < 1024 ? (nvec + 255) / 256 : 1024);
+        gather_sorted_x_kernel<<<blocks, 256, 0, stream>>>(a.x, a.vid, T, a.V, a.d_in, a.x_sorted);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        return launch_nt<true, kMultiConsumers>(nt, prm, smem, stream);
     }
-    switch (nt) {
-        case 1: return launch_nt<1, false>(a, KS, stages, sign_slots, smem, stream);
-        case 2: return launch_nt<2, false>(a, KS, stages, sign_slots, smem, stream);
-        case 4: return launch_nt<4, false>(a, KS, stages, sign_slots, smem, stream);
-        default: return launch_nt<8, false>(a, KS, stages, sign_slots, smem, stream);
-    }
+    return launch_nt<false, kSingleConsumers>(nt, prm, smem, stream);
 }
 
 }  // namespace bd

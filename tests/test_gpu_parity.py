@@ -283,7 +283,7 @@ def test_multi_exact_routing_signature(dev, V, T):
     wb_d = to_dev(wb, dev)
     s_l, a_l = zip(*[gpu_compress(wb_d, to_dev(wf, dev), PR, dev) for wf in wfs])
     y = torch.empty((T, d_out), dtype=torch.float32, device=dev)
-    ws = bd.new_workspace(256, dev)
+    ws = bd.new_workspace(bd.bd_linear_multi_workspace_size(T, V, d_out, d_in), dev)
     bd.bd_linear_multi(to_dev(x, dev), to_dev(vid, dev), list(s_l), list(a_l), PR, wb_d, y, ws)
     assert bd.bd_check_async(ws) == bd.BD_OK
     assert np.array_equal(y.cpu().numpy().astype(np.float64), y_ref)
@@ -298,7 +298,7 @@ def test_multi_bad_variant_flagged_and_computed_as_base(dev):
     wb_d = to_dev(wb, dev)
     s_l, a_l = zip(*[gpu_compress(wb_d, to_dev(wf, dev), PR, dev) for wf in wfs])
     y = torch.empty((T, d_out), dtype=torch.float32, device=dev)
-    ws = bd.new_workspace(256, dev)
+    ws = bd.new_workspace(bd.bd_linear_multi_workspace_size(T, V, d_out, d_in), dev)
     bd.bd_linear_multi(to_dev(x, dev), to_dev(vid, dev), list(s_l), list(a_l), PR, wb_d, y, ws)
     assert bd.bd_check_async(ws) == bd.BD_ERR_BAD_VARIANT
     assert np.array_equal(y.cpu().numpy().astype(np.float64), y_ref)
@@ -369,7 +369,7 @@ def test_canary_guards_untouched(dev):
     abuf.view(torch.int32)[:] = -1515870811
     ybuf = torch.empty((T * d_out + guard // 4,), dtype=torch.float32, device=dev)
     ybuf.view(torch.int32)[:] = -1515870811
-    ws = bd.new_workspace(256, dev)
+    ws = bd.new_workspace(bd.bd_linear_multi_workspace_size(T, 1, d_out, d_in), dev)
     s = sbuf[:n_s].view(d_out, d_in // 32)
     a = abuf[:d_out]
     bd.bd_compress(wb_d, wf_d, PR, s, a, ws)
