@@ -38,6 +38,7 @@ BD_ALPHA_PER_ROW = 1
 BD_OUT_BF16 = 0
 BD_OUT_F32 = 1
 BD_MAX_VARIANTS = 64
+BD_NOALLOC_MAX_ROWS = 262144
 
 # Every symbol include/bitdelta.h declares.
 EXPORTS = (
@@ -46,7 +47,7 @@ EXPORTS = (
     "bd_linear_workspace_size", "bd_linear",
     "bd_linear_multi_workspace_size", "bd_linear_multi",
     "bd_route_workspace_size", "bd_route",
-    "bd_debug_reconstruct", "bd_check_async",
+    "bd_debug_reconstruct", "bd_check_async", "bd_compress_noalloc",
 )
 
 
@@ -84,6 +85,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "bd_route": ([_vp, _i64, _i32, _vp, _vp, _vp, _sz, _vp], _int),
             "bd_debug_reconstruct": ([_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp], _int),
             "bd_check_async": ([_vp, _vp], _int),
+            "bd_compress_noalloc": ([_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp], _int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -172,6 +174,19 @@ def bd_compress(w_base, w_ft, alpha_mode, signs, alpha, ws, stream=None) -> None
     _check(load().bd_compress(_ptr(w_base, "w_base", _BF16_LIKE), _ptr(w_ft, "w_ft", _BF16_LIKE), d_out, d_in,
                               int(alpha_mode), _ptr(signs, "signs", (torch.int32, torch.uint32)),
                               _ptr(alpha, "alpha", (torch.float32,)), wsp, wsn, _stream(stream)), "bd_compress")
+
+
+def bd_compress_noalloc(w_base, w_ft, alpha_mode, signs, alpha, stream=None) -> None:
+    """bd_compress without a workspace, for callers that cannot allocate
+    device memory; the library keeps the scratch in a fixed device array
+    (at most BD_NOALLOC_MAX_ROWS rows; calls that overlap on the GPU race)."""
+    d_out, d_in = w_base.shape
+    if tuple(w_ft.shape) != (d_out, d_in):
+        raise ValueError("w_ft shape differs from w_base")
+    _check(load().bd_compress_noalloc(_ptr(w_base, "w_base", _BF16_LIKE), _ptr(w_ft, "w_ft", _BF16_LIKE), d_out,
+                                      d_in, int(alpha_mode), _ptr(signs, "signs", (torch.int32, torch.uint32)),
+                                      _ptr(alpha, "alpha", (torch.float32,)), _stream(stream)),
+           "bd_compress_noalloc")
 
 
 def bd_linear(x, w_base, signs, alpha, alpha_mode, y, ws, stream=None) -> None:

@@ -159,6 +159,33 @@ bd_status bd_route(const int32_t* vid, int64_t T, int32_t V, int32_t* perm, int3
 bd_status bd_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, const float* alpha, int alpha_mode,
                                int64_t d_out, int64_t d_in, float* w_eff, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Compression that allocates nothing (the BitDelta post has no counterpart
+ * for this entry point; it exists for callers of this library).
+ * Some callers cannot call cudaMalloc or hand the library a workspace: code
+ * running under an allocator that is locked or reserved by a framework,
+ * code that must not allocate while a stream is being captured, or plain C
+ * hosts with no device allocator of their own.  This variant computes
+ * exactly what bd_compress computes, but keeps the per-matrix partial sums
+ * in a fixed device array of the library (256 KiB per GPU that loads the
+ * library, held until the process exits) instead of in `ws`.
+ *  - d_out may be at most BD_NOALLOC_MAX_ROWS, else BD_ERR_UNSUPPORTED_SHAPE.
+ *  - The first call on a device looks up that array's device address (once
+ *    per device, with the device current); make that first call before any
+ *    stream capture.
+ *  - All calls share the one array: calls that may run at the same time on
+ *    the GPU (other streams, other host threads) race and must be ordered
+ *    by the caller.  Each call overwrites every partial sum it reads, so the
+ *    array needs no clearing between calls.
+ *  - There is no error word: a non-finite delta shows up as a non-finite
+ *    alpha (the row's, or the matrix's).
+ * Other arguments, conventions and results are those of bd_compress.
+ * ------------------------------------------------------------------------ */
+#define BD_NOALLOC_MAX_ROWS 262144
+
+bd_status bd_compress_noalloc(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out, int64_t d_in,
+                              int alpha_mode, uint32_t* signs, float* alpha, void* stream);
+
 /* Waits for `stream`, then reads and clears the error word in `ws`.
  * Returns BD_OK, or the first asynchronous error found (in the order
  * BD_ERR_TIMEOUT, BD_ERR_BAD_VARIANT, BD_ERR_NONFINITE). */
