@@ -9,8 +9,11 @@ the roofline of the dominant kernel (CUDA-event timed inside the timed
 region), the CPU oracle timed on the host cores, an end-to-end number with
 host buffers, and the SM clocks sampled during the timed region.
 
-Other workloads (--workload): tiny (256x256, T=4, per-matrix alpha) and
-multi (8192x8192 shared W_base, 14 variants, 64 Zipf-routed tokens).
+Other workloads (--workload): tiny (256x256, T=4, per-matrix alpha), multi
+(8192x8192 shared W_base, 14 variants, 64 Zipf-routed tokens) and prefill
+(4096 tokens x 8192x8192, the tensor-core path, reported in TFLOP/s).  The
+default decode line also carries a short prefill measurement under
+"prefill", since the metric names prefill TFLOP/s.
 
 `python bench.py --impl reference` times the CPU oracle instead (the
 reference arm), on bounded samples of the same workload.
@@ -43,7 +46,14 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # one ncu capture, keyed by kernel; each entry records the sha256 of the
 # kernel's source file at capture time and is ignored once that source has
 # changed.  Summaries of the captures are in profiles/.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # (kernel, workload): (source sha256[:16], source file, bytes per launch)
+    ("skinny_kernel<1,false>", "decode"): ("e9981b99d57d6e73", "bd_skinny.cu", 499_425_536 + 3_763_456),
+    ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_613_184 + 7_913_728),
+    ("prefill_kernel", "prefill"): ("7c5aa4018aaeb9a3", "bd_prefill.cu", 612_366_592 + 63_392_000),
+    ("gather_sorted_x + skinny_kernel<8,true>", "multi"): ("e9981b99d57d6e73", "bd_skinny.cu",
+                                                           255_675_648 + 4_176_384),
+}
 
 
 def parse_args():
@@ -52,7 +62,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    p.add_argument("--workload", choices=["decode", "tiny", "multi"], default="decode")
+    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill"], default="decode")
+    p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement of the decode line")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
@@ -103,6 +114,14 @@ class Workload:
             self.wf = [synth.finetuned_weight(rng, self.wb, 1e-3)]
             self.xs = [synth.activations(rng, T, d_in) for T in self.tokens]
             self.vid = None
+        elif name == "prefill":
+            d_out, d_in = 8192, 8192
+            self.tokens = [4096]
+            self.per_row = True
+            self.wb, wf, x = synth.single_problem(seed + 3, d_out, d_in, 4096)
+            self.wf = [wf]
+            self.xs = [x]
+            self.vid = None
         else:  # multi
             d_out, d_in = 8192, 8192
             self.tokens = [64]
@@ -119,6 +138,10 @@ class Workload:
             c["workload"] = "decode_ffn_28672x8192_T1_4_16"
             c["step"] = "bd_compress + bd_linear at T=1, 4, 16 (one variant)"
             c["l2"] = "inputs larger than L2 (W_base 470 MB, W_ft 470 MB vs 126.5 MB L2)"
+        elif self.name == "prefill":
+            c["workload"] = "prefill_4096x8192x8192"
+            c["step"] = "bd_linear at T=4096, one variant (compressed once, untimed); tensor-core path"
+            c["l2"] = "inputs larger than L2 (W_base 134 MB + x 67 MB + y 67 MB vs 126.5 MB L2)"
         elif self.name == "tiny":
             c["workload"] = "tiny_256x256_T4"
             c["step"] = "bd_compress + bd_linear at T=4"
@@ -159,12 +182,13 @@ class GpuRun:
                                                                          wl.d_in)), dev)
         self.vid = None if wl.vid is None else torch.from_numpy(wl.vid).to(dev)
         self.flush = None
-        if wl.name == "multi":
+        if wl.name in ("multi", "prefill"):
             for v in range(len(wl.wf)):  # variants are compressed once, before timing
                 bd.bd_compress(self.wb, self.wf[v], PR, self.signs[v], self.alpha[v], self.ws)
             torch.cuda.synchronize()
             self.wf = []  # W_ft is not needed any more
             torch.cuda.empty_cache()
+        if wl.name == "multi":
             self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def calls(self):
@@ -176,9 +200,17 @@ class GpuRun:
             T = wl.tokens[0]
             nbytes = (2 * wl.d_out * wl.d_in + len(active) * (wl.d_out * wl.d_in // 8 + 4 * wl.n_alpha) +
                       2 * T * wl.d_in + 2 * T * wl.d_out + 4 * T)
-            out.append(("linear_multi_T64", "skinny_kernel<8,true>", nbytes, 4 * T * wl.d_out * wl.d_in,
+            out.append(("linear_multi_T64", "gather_sorted_x + skinny_kernel<8,true>", nbytes,
+                        4 * T * wl.d_out * wl.d_in,
                         lambda: bd.bd_linear_multi(self.xs[0], self.vid, self.signs, self.alpha, self.mode, self.wb,
                                                    self.ys[0], self.ws)))
+            return out
+        if wl.name == "prefill":
+            T = wl.tokens[0]
+            out.append((f"linear_T{T}", "prefill_kernel", linear_bytes(T, wl.d_out, wl.d_in, wl.n_alpha),
+                        2 * T * wl.d_out * wl.d_in,
+                        lambda: bd.bd_linear(self.xs[0], self.wb, self.signs[0], self.alpha[0], self.mode, self.ys[0],
+                                             self.ws)))
             return out
         out.append(("compress", "compress_kernel", compress_bytes(wl.d_out, wl.d_in, wl.n_alpha), 0,
                     lambda: bd.bd_compress(self.wb, self.wf[0], self.mode, self.signs[0], self.alpha[0], self.ws)))
@@ -306,7 +338,8 @@ def _step_bytes_rows(wl: Workload):
         out.append(("linear_multi", "", 2 * wl.d_out * wl.d_in + len(active) * (wl.d_out * wl.d_in // 8 + 4 * wl.n_alpha)
                     + 2 * T * wl.d_in + 2 * T * wl.d_out + 4 * T))
         return out
-    out.append(("compress", "", compress_bytes(wl.d_out, wl.d_in, wl.n_alpha)))
+    if wl.name != "prefill":
+        out.append(("compress", "", compress_bytes(wl.d_out, wl.d_in, wl.n_alpha)))
     for T in wl.tokens:
         out.append((f"linear_T{T}", "", linear_bytes(T, wl.d_out, wl.d_in, wl.n_alpha)))
     return out
@@ -437,9 +470,16 @@ def run_gpu(args):
     tr = NCU_TRAFFIC.get((dom, wl.name))
     if tr is not None and tr[0] == _src_sha(tr[1]):
         traffic = tr[2]
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)",
-                "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_ms * 1e3}
+    if wl.name == "prefill":
+        flops_per_launch = calls[0][3]
+        tf = flops_per_launch / (avg_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                    "frac": tf / bf16_peak, "traffic": traffic, "peak_source": f"{peak_src} (bf16_tflops, burst)",
+                    "flops_per_launch": flops_per_launch, "avg_launch_us": avg_ms * 1e3}
+    else:
+        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)",
+                    "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_ms * 1e3}
     kernels = {k: {"launches": v["launches"], "avg_us": v["total_ms"] / v["launches"] * 1e3,
                    "share": v["total_ms"] / sum(x["total_ms"] for x in per_kernel.values()),
                    "GBps": v["bytes"] / (v["total_ms"] * 1e-3) / 1e9,
@@ -454,6 +494,19 @@ def run_gpu(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e["ms_per_step"] = float(t.item())
         e2e["value"] = world * step_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9
+        if wl.name == "prefill":
+            e2e["value"] = world * calls[0][3] / (e2e["ms_per_step"] * 1e-3) / 1e12
+            e2e["unit"] = "TFLOP/s"
+
+    prefill = None
+    if wl.name == "decode" and not args.no_prefill:
+        prefill = measure_prefill(dev, args.seed + rank, bf16_peak, peak_src)
+        if world > 1:
+            t = torch.tensor([prefill["avg_us"]], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            prefill["avg_us"] = float(t.item())
+            prefill["tflops"] = world * prefill["flops_per_launch"] / (prefill["avg_us"] * 1e-6) / 1e12
+            prefill["frac"] = prefill["tflops"] / world / bf16_peak
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
@@ -461,19 +514,51 @@ def run_gpu(args):
         cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        unit = "GB/s"
+        if wl.name == "prefill":  # this workload's own figure is tensor throughput
+            value = world * calls[0][3] / (ms_per_step * 1e-3) / 1e12
+            unit = "TFLOP/s"
+        line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
                 "data": "synthetic (seeded numpy; shapes and distributions of the BitDelta serving setup)",
                 "config": {**wl.config(), "parallelism": f"replicas x{world} (no exchange step)"},
                 "tokens_per_s": world * tokens / (ms_per_step * 1e-3),
                 "frac_hbm_step": value / world / hbm_peak,
-                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-                "gpu_launches": len(calls) * args.steps}
+                "roofline": roofline, "kernels": kernels, "prefill": prefill, "cpu_baseline": cpu, "e2e": e2e,
+                "clocks": clk, "gpu_launches": (2 if wl.name == "multi" else 1) * len(calls) * args.steps}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def measure_prefill(dev, seed, bf16_peak, peak_src, reps=20):
+    """Tensor-core prefill on its own: 4096 tokens x W_base [8192 x 8192], one
+    variant; median of `reps` CUDA-event-timed calls."""
+    import torch
+
+    wl = Workload("prefill", seed)
+    run = GpuRun(wl, dev)
+    fn = run.calls()[0][4]
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    stream = torch.cuda.current_stream()
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    if run.bd.bd_check_async(run.ws) != run.bd.BD_OK:
+        raise RuntimeError("asynchronous error in the prefill measurement")
+    us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
+    flops = 2 * 4096 * 8192 * 8192
+    tf = flops / (us * 1e-6) / 1e12
+    return {"workload": "prefill_4096x8192x8192", "kernel": "prefill_kernel", "bound": "tensor", "avg_us": us,
+            "flops_per_launch": flops, "tflops": tf, "peak": bf16_peak, "frac": tf / bf16_peak,
+            "peak_source": f"{peak_src} (bf16_tflops, burst)", "reps": reps}
 
 
 def run_e2e(run: GpuRun, calls, wl: Workload, steps: int, stream):
@@ -483,6 +568,9 @@ def run_e2e(run: GpuRun, calls, wl: Workload, steps: int, stream):
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
     if wl.name == "multi":
         h_in = [(pin(run.xs[0]), run.xs[0]), (pin(run.vid), run.vid)]
+        h_out = [(pin(run.ys[0]), run.ys[0])]
+    elif wl.name == "prefill":
+        h_in = [(pin(run.xs[0]), run.xs[0])]
         h_out = [(pin(run.ys[0]), run.ys[0])]
     else:
         h_in = [(pin(run.wb), run.wb), (pin(run.wf[0]), run.wf[0])] + [(pin(x), x) for x in run.xs]

@@ -1,11 +1,350 @@
-// Prefill GEMM (tensor-core path for T > 64).  Not built yet: bd_linear runs
-// the decode kernel over 64-token groups until this path is available.
-#include "bd_internal.h"
+// Prefill (T > 64) fused BitDelta linear on the 5th-generation tensor cores
+// (section "Sunum mimarisi" of the BitDelta post: W_eff = W_base + alpha*s is
+// rebuilt on chip, never in HBM, and the rebuild is fused with the matmul).
+//
+//   D[r][t] = sum_k W_eff[r][k] * x[t][k],   y[t][r] = D[r][t]
+//
+// One CTA computes a 128-row x 256-token tile of y^T over all of d_in, in
+// 64-column k-steps through a 4-stage ring:
+//   warp 0      TMA producer: x tile [256 x 64] (128-byte swizzle), W_base
+//               tile [128 x 64] (128-byte swizzle) and the sign words of the
+//               tile's rows, all completing on one mbarrier per stage;
+//   warps 2..5  transform: thread = one row of the tile (TMEM lane); reads its
+//               64 W_base values from shared memory, adds +alpha or -alpha per
+//               sign bit with packed bf16 adds (W_eff rounded to bf16, the
+//               MMA's input precision), and writes them into the stage's
+//               A-operand columns of tensor memory with tcgen05.st;
+//   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=256,
+//               K=16; A from tensor memory, B from shared memory, fp32
+//               accumulator in tensor memory) and frees each stage with
+//               tcgen05.commit;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator, bf16/fp32 stores.
+// So W_eff never goes through shared memory: per k-step the shared memory
+// sees the W and x tiles written once by TMA, W read once by the transform
+// and x read once by the tensor core.
+//
+// Every mbarrier wait is bounded; a timeout sets the error word, stops every
+// role at its next wait, drains the copies in flight, waits for the issued
+// MMAs and frees tensor memory.
+#include "bd_device.cuh"
+#include "bd_tma.h"
 
 namespace bd {
+namespace {
 
-bool prefill_available() { return false; }
+constexpr int BM = 128;  // W rows per tile (MMA M, TMEM lanes)
+constexpr int BN = 256;  // tokens per tile (MMA N)
+constexpr int BK = 64;   // k-step (one 128-byte swizzle atom of bf16)
+constexpr int kStages = 4;
+constexpr int kXBytes = BN * BK * 2;                      // 32768
+constexpr int kWBytes = BM * BK * 2;                      // 16384
+constexpr int kSBytes = BM * 16;                          // 4 sign words per row (128 columns)
+constexpr int kStageBytes = kXBytes + kWBytes + kSBytes;  // 51200 (multiple of 1024)
+constexpr int kThreads = 192;                             // 6 warps
+constexpr int kTmemCols = 512;                            // D: 256 columns; A ring: 4 x 32 columns
+constexpr int kDCol = 0;
+constexpr int kACol = 256;
 
-cudaError_t launch_prefill(const PrefillArgs&, int, cudaStream_t) { return cudaErrorNotSupported; }
+struct PrefillParams {
+    CUtensorMap x_map;  // [T][d_in] bf16, box 64 x 256, 128B swizzle
+    CUtensorMap w_map;  // [d_out][d_in] bf16, box 64 x 128, 128B swizzle
+    CUtensorMap s_map;  // [d_out][d_in/32] u32, box 4 x 128
+    const float* alpha;
+    void* y;
+    uint32_t* err;
+    int64_t T, d_out, d_in;
+    int per_row, out_f32;
+};
+
+struct PrefillShared {
+    uint64_t full[kStages];   // TMA landed
+    uint64_t afull[kStages];  // transform wrote the A stage (4 warp arrivals)
+    uint64_t empty[kStages];  // MMAs reading the stage finished (tcgen05.commit)
+    uint64_t accum;           // all MMAs finished
+    uint32_t tmem_base;
+    volatile int abort;
+};
+
+// ------------------------------------------------------------------ tcgen05 wrappers
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D(tmem) (+)= A(tmem) * B(smem desc)^T, kind::f16
+__device__ __forceinline__ void mma_ts(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_taddr),
+        "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+        "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+        "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr)
+        : "memory");
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes, 8-row groups 1024 bytes apart (tile base 1024-byte aligned).
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);  // start address
+    d |= static_cast<uint64_t>(1) << 16;                  // leading byte offset (unused for this layout)
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;          // stride byte offset: 8 rows x 128 B
+    d |= static_cast<uint64_t>(1) << 46;                  // descriptor version
+    d |= static_cast<uint64_t>(2) << 61;                  // layout: 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
+// K-major, N = 256, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
+                            (static_cast<uint32_t>(BM >> 4) << 24);
+
+__device__ __forceinline__ bool pwait(PrefillShared& sh, uint64_t* bar, uint32_t parity, uint32_t* err)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (sh.abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            sh.abort = 1;
+            raise_error(err, kErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p)
+{
+    extern __shared__ uint8_t dyn_raw[];
+    __shared__ PrefillShared sh;
+    uint8_t* dyn = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t tok0 = static_cast<int64_t>(blockIdx.x) * BN;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.y) * BM;
+    const int nk = static_cast<int>(p.d_in / BK);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.afull[s], 4);
+            mbar_init(&sh.empty[s], 1);
+        }
+        mbar_init(&sh.accum, 1);
+        sh.abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) tmem_alloc(&sh.tmem_base, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % kStages;
+                if (i >= kStages && !pwait(sh, &sh.empty[s], static_cast<uint32_t>(i / kStages - 1) & 1u, p.err))
+                    break;
+                uint8_t* st = dyn + s * kStageBytes;
+                mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
+                tma_load_2d(st, &p.x_map, i * BK, static_cast<int>(tok0), &sh.full[s]);
+                tma_load_2d(st + kXBytes, &p.w_map, i * BK, static_cast<int>(row0), &sh.full[s]);
+                tma_load_2d(st + kXBytes + kWBytes, &p.s_map, 4 * (i / 2), static_cast<int>(row0), &sh.full[s]);
+                ++issued;
+            }
+            // copies still in flight must land before the CTA ends
+            for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i) {
+                const int s = i % kStages;
+                const uint32_t par = static_cast<uint32_t>(i / kStages) & 1u;
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&sh.full[s], par) && global_timer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            int done = 0;
+            for (int i = 0; i < nk; ++i) {
+                const int s = i % kStages;
+                if (!pwait(sh, &sh.afull[s], static_cast<uint32_t>(i / kStages) & 1u, p.err)) break;
+                tc_fence_after();
+                const uint64_t bdesc = smem_desc_sw128(smem_u32(dyn + s * kStageBytes));
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)
+                    mma_ts(tmem + kDCol, tmem + kACol + 32 * s + 8 * kk, bdesc + static_cast<uint64_t>(2 * kk),
+                           kIdesc, (i | kk) != 0 ? 1u : 0u);
+                mma_commit(&sh.empty[s]);
+                ++done;
+            }
+            mma_commit(&sh.accum);  // fires once every MMA issued above has completed
+            // tensor memory is freed below only after those MMAs are done
+            const uint64_t t0 = global_timer_ns();
+            while (done > 0 && !mbar_try_wait(&sh.accum, 0u) && global_timer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ transform, then epilogue
+        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int rl = 32 * quarter + lane;
+        const int64_t row = row0 + rl;
+        float a = 0.0f;
+        if (row < p.d_out) a = p.alpha[p.per_row ? row : 0];
+        const uint32_t ab = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a)));
+        const uint32_t neg = ((ab << 16) | ab) ^ 0x80008000u;  // (-alpha, -alpha) as bf16x2
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+        bool ok = true;
+        for (int i = 0; i < nk; ++i) {
+            const int s = i % kStages;
+            if (!__all_sync(0xffffffffu, pwait(sh, &sh.full[s], static_cast<uint32_t>(i / kStages) & 1u, p.err))) {
+                ok = false;
+                break;
+            }
+            const uint8_t* st = dyn + s * kStageBytes;
+            const uint8_t* wrow = st + kXBytes + rl * 128;
+            const uint32_t* srow = reinterpret_cast<const uint32_t*>(st + kXBytes + kWBytes + rl * 16);
+            const uint32_t words[2] = {srow[2 * (i & 1)], srow[2 * (i & 1) + 1]};
+            uint32_t v[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 u = *reinterpret_cast<const uint4*>(wrow + ((c ^ (rl & 7)) << 4));
+                v[4 * c + 0] = u.x;
+                v[4 * c + 1] = u.y;
+                v[4 * c + 2] = u.z;
+                v[4 * c + 3] = u.w;
+            }
+#pragma unroll
+            for (int hw = 0; hw < 4; ++hw) {  // 16 columns per sign half-word
+                const uint32_t h = (words[hw >> 1] >> (16 * (hw & 1))) & 0xFFFFu;
+                const uint32_t z = (h | (h << 15)) & 0x55555555u;
+#pragma unroll
+                for (int pp = 0; pp < 8; ++pp) {
+                    const uint32_t add = neg ^ ((z << (15 - 2 * pp)) & 0x80008000u);  // +alpha where bit = 1
+                    __nv_bfloat162 w2 = *reinterpret_cast<__nv_bfloat162*>(&v[8 * hw + pp]);
+                    const __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(&add);
+                    w2 = __hadd2(w2, a2);
+                    v[8 * hw + pp] = *reinterpret_cast<uint32_t*>(&w2);
+                }
+            }
+            tmem_st32(lane_addr + kACol + 32 * s, v);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh.afull[s]);
+        }
+        // epilogue
+        if (ok && __all_sync(0xffffffffu, pwait(sh, &sh.accum, 0u, p.err))) {
+            tc_fence_after();
+            for (int cb = 0; cb < BN / 32; ++cb) {
+                uint32_t d[32];
+                tmem_ld32(lane_addr + kDCol + 32 * cb, d);
+                if (row < p.d_out) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int64_t t = tok0 + 32 * cb + j;
+                        if (t < p.T) {
+                            const float val = __uint_as_float(d[j]);
+                            if (p.out_f32)
+                                static_cast<float*>(p.y)[t * p.d_out + row] = val;
+                            else
+                                static_cast<__nv_bfloat16*>(p.y)[t * p.d_out + row] = __float2bfloat16_rn(val);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+bool prefill_available() { return true; }
+
+cudaError_t launch_prefill(const PrefillArgs& a, int /*sm_count*/, cudaStream_t stream)
+{
+    static thread_local PrefillParams prm;
+    if (!encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, static_cast<uint64_t>(a.d_in),
+                       static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, BK, BN,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tma_2d(&prm.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
+                       static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, BK, BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tma_2d(&prm.s_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.signs, static_cast<uint64_t>(a.d_in / 32),
+                       static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in / 8), 4, BM,
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    prm.alpha = a.alpha;
+    prm.y = a.y;
+    prm.err = a.err;
+    prm.T = a.T;
+    prm.d_out = a.d_out;
+    prm.d_in = a.d_in;
+    prm.per_row = a.per_row;
+    prm.out_f32 = a.out_f32;
+    const size_t smem = static_cast<size_t>(kStages) * kStageBytes + 1024;
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>((a.T + BN - 1) / BN), static_cast<unsigned>((a.d_out + BM - 1) / BM));
+    prefill_kernel<<<grid, kThreads, smem, stream>>>(prm);
+    return cudaGetLastError();
+}
 
 }  // namespace bd

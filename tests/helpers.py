@@ -9,7 +9,9 @@ reaches ~2e-2 when |y| ~ 8.  fp32 outputs must in addition meet the fp32
 dot-product bound (n + 4) * 2^-22 * sum_j |x_j| (|w_j| + alpha): fp32
 accumulation in any order keeps the error under (n + 4) * 2^-24 times that
 sum when every addition rounds to nearest; the factor 4 of slack covers
-tensor-core accumulators that truncate instead of rounding.
+tensor-core accumulators that truncate instead of rounding.  The prefill path
+(T > 64) rounds W_eff to bf16 before its contraction, which adds up to
+2^-9 * |x_j| * (|w_j| + alpha) per term to that bound.
 """
 from __future__ import annotations
 
@@ -65,8 +67,12 @@ def check_linear(y_gpu: np.ndarray, y_ref: np.ndarray, bf16_out: bool, bound: np
     return fro
 
 
-def fp32_bound(x_bits, wb_bits, alpha, per_row: bool, rows=None) -> np.ndarray:
-    """(n + 4) * 2^-22 * sum_j |x_j| (|w_j| + alpha) for the listed rows."""
+PREFILL_MIN_T = 65  # bd_linear runs the tensor-core prefill GEMM from this many tokens on
+
+
+def fp32_bound(x_bits, wb_bits, alpha, per_row: bool, rows=None, weff_bf16: bool = False) -> np.ndarray:
+    """(n + 4) * 2^-22 * sum_j |x_j| (|w_j| + alpha) for the listed rows
+    (plus 2^-9 times the same sum when W_eff is rounded to bf16)."""
     x = np.abs(synth.bf16_bits_to_f32(x_bits).astype(np.float64))
     wb = wb_bits if rows is None else wb_bits[rows]
     w = np.abs(synth.bf16_bits_to_f32(wb).astype(np.float64))
@@ -78,4 +84,4 @@ def fp32_bound(x_bits, wb_bits, alpha, per_row: bool, rows=None) -> np.ndarray:
         a = np.full(w.shape[0], float(a[0]))
     s = x @ w.T + x.sum(axis=1)[:, None] * a[None, :]
     n = wb.shape[1]
-    return (n + 4) * 2.0 ** -22 * s + 1e-30
+    return ((n + 4) * 2.0 ** -22 + (2.0 ** -9 if weff_bf16 else 0.0)) * s + 1e-30

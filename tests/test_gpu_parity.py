@@ -17,7 +17,7 @@ import torch
 import oracle
 from bit_weight_delta_bd_gb300 import bitdelta as bd
 from bit_weight_delta_bd_gb300 import synth
-from helpers import bf16_half_ulp, check_linear, fp32_bound, to_dev, u32, y_host  # noqa: F401
+from helpers import PREFILL_MIN_T, bf16_half_ulp, check_linear, fp32_bound, to_dev, u32, y_host  # noqa: F401
 
 pytestmark = pytest.mark.gpu
 
@@ -131,8 +131,8 @@ def test_linear_tiny(dev):
                      bound=fp32_bound(x, wb, a.cpu().numpy(), False) if f32 else None, what=f"tiny f32={f32}")
 
 
-@pytest.mark.parametrize("T", [1, 3, 8, 9, 17, 33, 64, 65, 130])
-@pytest.mark.parametrize("d_out,d_in", [(1, 128), (17, 384), (48, 1024)])
+@pytest.mark.parametrize("T", [1, 3, 8, 9, 17, 33, 64, 65, 130, 300])
+@pytest.mark.parametrize("d_out,d_in", [(1, 128), (17, 384), (48, 1024), (200, 640)])
 def test_linear_shapes(dev, T, d_out, d_in):
     wb, wf, x = synth.single_problem(T * 131 + d_out, d_out, d_in, T)
     s_ref, a_ref = oracle.compress(wb, wf, per_row=True)
@@ -140,7 +140,8 @@ def test_linear_shapes(dev, T, d_out, d_in):
     wb_d = to_dev(wb, dev)
     s, a = gpu_compress(wb_d, to_dev(wf, dev), PR, dev)
     y = gpu_linear(to_dev(x, dev), wb_d, s, a, PR, dev)
-    check_linear(y_host(y), y_ref, bf16_out=False, bound=fp32_bound(x, wb, a.cpu().numpy(), True),
+    check_linear(y_host(y), y_ref, bf16_out=False,
+                 bound=fp32_bound(x, wb, a.cpu().numpy(), True, weff_bf16=T >= PREFILL_MIN_T),
                  what=f"T={T} {d_out}x{d_in}")
 
 
@@ -194,7 +195,7 @@ def test_linear_ffn_decode_sampled_rows(dev, decode_problem, T):
                      what=f"ffn T={T} f32={f32}")
 
 
-@pytest.mark.parametrize("T", [4, 64])
+@pytest.mark.parametrize("T", [4, 64, 300])
 def test_linear_row_sharding_is_bit_identical(dev, T):
     d_out, d_in = 300, 1024
     wb, wf, x = synth.single_problem(77, d_out, d_in, T)
@@ -205,6 +206,33 @@ def test_linear_row_sharding_is_bit_identical(dev, T):
     for r0, r1 in [(0, 37), (37, 160), (160, 300)]:
         parts.append(gpu_linear(x_d, wb_d[r0:r1], s[r0:r1], a[r0:r1], PR, dev))
     assert torch.equal(torch.cat(parts, dim=1), y_full)
+
+
+@pytest.fixture(scope="module")
+def prefill_problem():
+    """Prefill workload: 4096 tokens x W_base [8192 x 8192], one variant, per-row alpha."""
+    return synth.single_problem(3, 8192, 8192, 4096)
+
+
+def test_prefill_4096_tokens_sampled_rows(dev, prefill_problem):
+    wb, wf, x = prefill_problem
+    rows = synth.sample_rows(11, 8192, 48)
+    s_rows, a_rows = oracle.compress_rows(wb, wf, rows)
+    s_full = np.zeros((8192, 256), np.uint32)
+    a_full = np.zeros(8192, np.float32)
+    s_full[rows], a_full[rows] = s_rows, a_rows
+    toks = np.unique(np.concatenate([np.arange(0, 4096, 37), [4095]]))
+    y_ref = oracle.linear(x[toks], wb, s_full, a_full, per_row=True, rows=rows)
+    wb_d = to_dev(wb, dev)
+    s, a = gpu_compress(wb_d, to_dev(wf, dev), PR, dev)
+    assert np.array_equal(u32(s)[rows], s_rows)
+    x_d = to_dev(x, dev)
+    for f32 in (True, False):
+        y = gpu_linear(x_d, wb_d, s, a, PR, dev, f32=f32)
+        yg = y_host(y)[np.ix_(toks, rows)]
+        check_linear(yg, y_ref, bf16_out=not f32,
+                     bound=fp32_bound(x[toks], wb, a.cpu().numpy(), True, rows=rows, weff_bf16=True) if f32 else None,
+                     what=f"prefill f32={f32}")
 
 
 def test_linear_zero_sizes_are_noops(dev):
