@@ -13,7 +13,9 @@ Other workloads (--workload): tiny (256x256, T=4, per-matrix alpha), multi
 (8192x8192 shared W_base, 14 variants, 64 Zipf-routed tokens) and prefill
 (4096 tokens x 8192x8192, the tensor-core path, reported in TFLOP/s).  The
 default decode line also carries a short prefill measurement under
-"prefill", since the metric names prefill TFLOP/s.
+"prefill", since the metric names prefill TFLOP/s.  slice: the 8-layer slice of
+a 70B-shaped stack (56 linears, 14 variants compressed on the GPU, 32 decode
+tokens routed by Zipf), one step = the 56 multi-variant linears.
 
 `python bench.py --impl reference` times the CPU oracle instead (the
 reference arm), on bounded samples of the same workload.
@@ -62,7 +64,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill"], default="decode")
+    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill", "slice"], default="decode")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement of the decode line")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
@@ -105,6 +107,14 @@ class Workload:
         from bit_weight_delta_bd_gb300 import synth
 
         self.name = name
+        if name == "slice":  # weights are drawn on the device by SliceRun
+            self.tokens = [32]
+            self.per_row = True
+            self.vid = synth.zipf_variant_ids(np.random.default_rng(seed), 32, 14)
+            self.d_out = self.d_in = 0
+            self.wf, self.xs, self.wb = [None] * 14, [], None
+            self.n_alpha = 0
+            return
         if name in ("decode", "tiny"):
             d_out, d_in = (28672, 8192) if name == "decode" else (256, 256)
             self.tokens = [1, 4, 16] if name == "decode" else [4]
@@ -138,6 +148,13 @@ class Workload:
             c["workload"] = "decode_ffn_28672x8192_T1_4_16"
             c["step"] = "bd_compress + bd_linear at T=1, 4, 16 (one variant)"
             c["l2"] = "inputs larger than L2 (W_base 470 MB, W_ft 470 MB vs 126.5 MB L2)"
+        elif self.name == "slice":
+            c = {"workload": "slice_8_layers_70b_shapes_V14_T32", "layers": 8,
+                 "linears": "q/o 8192x8192, k/v 8192->1024, gate/up 8192->28672, down 28672->8192",
+                 "variants": 14, "active_variants": int(len(set(int(v) for v in self.vid))), "tokens": [32],
+                 "alpha": "per_row",
+                 "step": "56 bd_linear_multi calls (variants compressed on the GPU once, untimed)",
+                 "l2": "inputs larger than L2 (13.7 GB of W_base per step)"}
         elif self.name == "prefill":
             c["workload"] = "prefill_4096x8192x8192"
             c["step"] = "bd_linear at T=4096, one variant (compressed once, untimed); tensor-core path"
@@ -220,6 +237,62 @@ class GpuRun:
                         4 * T * wl.d_out * wl.d_in,
                         (lambda i=i: bd.bd_linear(self.xs[i], self.wb, self.signs[0], self.alpha[0], self.mode,
                                                   self.ys[i], self.ws))))
+        return out
+
+
+class SliceRun:
+    """The 8-layer slice resident on the device: per linear W_base and the 14
+    variants' packed signs and alpha (compressed here, on the GPU, from
+    on-device seeded draws), plus that linear's 32-token input."""
+
+    def __init__(self, wl: Workload, dev, seed: int, layers: int = 8):
+        import torch
+
+        from bit_weight_delta_bd_gb300 import bitdelta as bd
+        from bit_weight_delta_bd_gb300 import synth
+
+        self.bd, self.torch, self.wl = bd, torch, wl
+        V, T = 14, 32
+        scales = synth.slice_variant_scales(seed, V)
+        ws_bytes = max(max(bd.bd_compress_workspace_size(d_out, d_in, bd.BD_ALPHA_PER_ROW),
+                           bd.bd_linear_multi_workspace_size(T, V, d_out, d_in))
+                       for _, d_out, d_in in synth.SLICE_LINEARS)
+        self.ws = bd.new_workspace(ws_bytes, dev)
+        self.vid = torch.from_numpy(wl.vid).to(dev)
+        rng = np.random.default_rng(seed + 17)
+        self.mats = []
+        for layer in range(layers):
+            for m, (name, d_out, d_in) in enumerate(synth.SLICE_LINEARS):
+                wb = synth.device_base_weight(synth.slice_seed(seed, layer, m), d_out, d_in, dev)
+                signs, alphas = [], []
+                for v in range(V):
+                    wf = synth.device_finetuned_weight(synth.slice_seed(seed, layer, m, v), wb, float(scales[v]))
+                    sg = torch.empty((d_out, d_in // 32), dtype=torch.int32, device=dev)
+                    al = torch.empty(d_out, dtype=torch.float32, device=dev)
+                    bd.bd_compress(wb, wf, bd.BD_ALPHA_PER_ROW, sg, al, self.ws)
+                    del wf
+                    signs.append(sg)
+                    alphas.append(al)
+                x = torch.from_numpy(synth.activations(rng, T, d_in).view(np.int16)).to(dev)
+                y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
+                self.mats.append((f"L{layer}.{name}", d_out, d_in, wb, signs, alphas, x, y))
+        torch.cuda.synchronize()
+        if bd.bd_check_async(self.ws) != bd.BD_OK:
+            raise RuntimeError("asynchronous error while compressing the slice")
+        self.flush = None
+        self.xs = [mt[6] for mt in self.mats]
+        self.ys = [mt[7] for mt in self.mats]
+
+    def calls(self):
+        bd, wl = self.bd, self.wl
+        active = len(set(int(v) for v in wl.vid if v >= 0))
+        T = 32
+        out = []
+        for label, d_out, d_in, wb, signs, alphas, x, y in self.mats:
+            nbytes = 2 * d_out * d_in + active * (d_out * d_in // 8 + 4 * d_out) + 2 * T * d_in + 2 * T * d_out + 4 * T
+            out.append((label, "gather_sorted_x + skinny_kernel<4,true>", nbytes, 4 * T * d_out * d_in,
+                        (lambda wb=wb, signs=signs, alphas=alphas, x=x, y=y:
+                         bd.bd_linear_multi(x, self.vid, signs, alphas, bd.BD_ALPHA_PER_ROW, wb, y, self.ws))))
         return out
 
 
@@ -400,7 +473,7 @@ def run_gpu(args):
     from bit_weight_delta_bd_gb300 import bitdelta as bd
 
     wl = Workload(args.workload, args.seed + rank)
-    run = GpuRun(wl, dev)
+    run = SliceRun(wl, dev, args.seed + rank) if wl.name == "slice" else GpuRun(wl, dev)
     calls = run.calls()
     stream = torch.cuda.current_stream()
 
@@ -509,7 +582,7 @@ def run_gpu(args):
             prefill["frac"] = prefill["tflops"] / world / bf16_peak
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
+    if rank == 0 and world == 1 and not args.no_cpu and wl.name != "slice":
         gbs, cores, sample = oracle_time(wl)
         cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
 
@@ -526,7 +599,7 @@ def run_gpu(args):
                 "tokens_per_s": world * tokens / (ms_per_step * 1e-3),
                 "frac_hbm_step": value / world / hbm_peak,
                 "roofline": roofline, "kernels": kernels, "prefill": prefill, "cpu_baseline": cpu, "e2e": e2e,
-                "clocks": clk, "gpu_launches": (2 if wl.name == "multi" else 1) * len(calls) * args.steps}
+                "clocks": clk, "gpu_launches": (2 if wl.name in ("multi", "slice") else 1) * len(calls) * args.steps}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -569,6 +642,9 @@ def run_e2e(run: GpuRun, calls, wl: Workload, steps: int, stream):
     if wl.name == "multi":
         h_in = [(pin(run.xs[0]), run.xs[0]), (pin(run.vid), run.vid)]
         h_out = [(pin(run.ys[0]), run.ys[0])]
+    elif wl.name == "slice":
+        h_in = [(pin(x), x) for x in run.xs] + [(pin(run.vid), run.vid)]
+        h_out = [(pin(y), y) for y in run.ys]
     elif wl.name == "prefill":
         h_in = [(pin(run.xs[0]), run.xs[0])]
         h_out = [(pin(run.ys[0]), run.ys[0])]

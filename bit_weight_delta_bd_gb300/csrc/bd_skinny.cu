@@ -59,7 +59,8 @@ constexpr int kSignRowBytes = 16;  // 4 sign words per row per stage
 constexpr int kMaxStages = 4;
 constexpr int kMaxKeys = kMaxVariants + 1;
 constexpr int kSingleConsumers = 4;  // 64 rows per CTA, up to three CTAs per SM
-constexpr int kMultiConsumers = 6;   // 96 rows per CTA: three 14-variant stages fit in shared memory
+constexpr int kMultiConsumers = 8;   // 128 rows per CTA, 2 stages (measured best on GB300)
+constexpr int kMultiStages = 2;
 constexpr size_t kSingleBudget = 66u * 1024u;  // three CTAs per SM (measured best on GB300)
 constexpr size_t kMultiBudget = 220u * 1024u;
 
@@ -87,6 +88,8 @@ struct SkinnyShared {
     int act[kSkinnyMaxTokens];   // slot -> variant id
     int tile_first[kSkinnyMaxTokens / 8];
     int tile_last[kSkinnyMaxTokens / 8];
+    int slot_tile_first[kSkinnyMaxTokens];  // 8-token tiles spanned by each active variant
+    int slot_tile_last[kSkinnyMaxTokens];
     int n_act;
     volatile int abort;
 };
@@ -233,6 +236,11 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
         sh.tile_first[tid] = p0 < T ? sh.keyp[p0] : 1;
         sh.tile_last[tid] = p0 < T ? sh.keyp[p1] : 0;  // empty range past T
     }
+    if (MULTI && tid < sh.n_act) {
+        const int k = sh.act[tid] + 1;
+        sh.slot_tile_first[tid] = sh.seg[k] / 8;
+        sh.slot_tile_last[tid] = (sh.seg[k + 1] - 1) / 8;
+    }
     __syncthreads();
 
     // ---------------------------------------------------------------- pipeline
@@ -324,34 +332,42 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
                 const int sign_word = 2 * h + (q >> 1);
                 const uint32_t sign_shift = 16u * (q & 1);
                 uint32_t S0[8], S1[8];
-                int cur_slot = -1;
                 if (!MULTI) {
                     expand_signs((sgn[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
                     expand_signs((sgn[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
-                }
 #pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
-                    const uint4 xa = *reinterpret_cast<const uint4*>(xr + c0);
-                    const uint4 xb = *reinterpret_cast<const uint4*>(xr + c1);
-                    mma4(accb[j], W0, W1, xa, xb);
-                    if (!MULTI) {
+                    for (int j = 0; j < NT; ++j) {
+                        const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
+                        const uint4 xa = *reinterpret_cast<const uint4*>(xr + c0);
+                        const uint4 xb = *reinterpret_cast<const uint4*>(xr + c1);
+                        mma4(accb[j], W0, W1, xa, xb);
                         mma4(accs[j], S0, S1, xa, xb);
-                    } else {
-                        const int kf = sh.tile_first[j] > 1 ? sh.tile_first[j] : 1;
-                        const int kl = sh.tile_last[j];
-                        for (int k = kf; k <= kl; ++k) {
-                            const int slot = sh.slot_of_key[k];
-                            if (slot < 0) continue;
-                            if (slot != cur_slot) {
-                                cur_slot = slot;
-                                const uint32_t* sb = sgn + slot * (kSignTile / 4);
-                                expand_signs((sb[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
-                                expand_signs((sb[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
-                            }
-                            const bool mine = (my_key[j] == k);
+                    }
+                } else {
+                    // base contraction for every tile: independent accumulator chains
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
+                        mma4(accb[j], W0, W1, *reinterpret_cast<const uint4*>(xr + c0),
+                             *reinterpret_cast<const uint4*>(xr + c1));
+                    }
+                    // sign contraction: each active variant's bits expanded once, applied to
+                    // its own tokens of the tiles it spans (warp-uniform tile predicates)
+                    for (int a = 0; a < n_act; ++a) {
+                        const uint32_t* sb = sgn + a * (kSignTile / 4);
+                        expand_signs((sb[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
+                        expand_signs((sb[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
+                        const int key = sh.act[a] + 1;
+                        const int tf = sh.slot_tile_first[a], tl = sh.slot_tile_last[a];
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) {
+                            if (j < tf || j > tl) continue;
+                            const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
+                            const bool mine = (my_key[j] == key);
                             const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                            mma4(accs[j], S0, S1, mine ? xa : z, mine ? xb : z);
+                            const uint4 xa = mine ? *reinterpret_cast<const uint4*>(xr + c0) : z;
+                            const uint4 xb = mine ? *reinterpret_cast<const uint4*>(xr + c1) : z;
+                            mma4(accs[j], S0, S1, xa, xb);
                         }
                     }
                 }
@@ -473,7 +489,7 @@ int skinny_group_tokens(bool multi, int V)
     const int rows = 16 * kMultiConsumers;
     for (int G = kSkinnyMaxTokens; G > 8; G /= 2) {
         const int slots = V < G ? V : G;
-        if (3 * stage_bytes_for(rows, slots, tiles_for(G)) + 1024 <= kMultiBudget) return G;
+        if (kMultiStages * stage_bytes_for(rows, slots, tiles_for(G)) + 1024 <= kMultiBudget) return G;
     }
     return 8;
 }
@@ -514,16 +530,15 @@ cudaError_t launch_skinny(const SkinnyArgs& a, int /*sm_count*/, cudaStream_t st
                        static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, 64,
                        static_cast<uint32_t>(8 * nt), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    // K slices per cluster: a function of d_in and the kernel flavour only
-    // (one per 4096 columns single-variant, per 2048 multi-variant, at most 4;
-    // measured best on GB300 for d_in = 8192).
-    int ck = multi ? nc / 16 : nc / 32;
+    // K slices per cluster: a function of d_in only (one per 4096 columns, at
+    // most 4; measured best on GB300 for d_in = 8192).
+    int ck = nc / 32;
     ck = ck < 1 ? 1 : ck > 4 ? 4 : ck;
     prm.CK = ck;
     prm.sign_slots = multi ? (a.V < T ? a.V : T) : 1;
     const size_t stage_bytes = stage_bytes_for(rows, prm.sign_slots, nt);
     const size_t budget = multi ? kMultiBudget : kSingleBudget;
-    int stages = kMaxStages;
+    int stages = multi ? kMultiStages : kMaxStages;
     while (stages > 2 && stages * stage_bytes + 1024 > budget) --stages;
     prm.stages = stages;
     const size_t red = 2u * rows * (8u * nt) * sizeof(float);

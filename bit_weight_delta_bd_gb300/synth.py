@@ -92,3 +92,50 @@ def sample_rows(seed: int, d_out: int, n: int) -> np.ndarray:
     if n > 1:
         pick[1] = d_out - 1
     return np.unique(pick).astype(np.int64)
+
+
+# ------------------------------------------------------------------------------------------
+# On-device draws for workloads too large to draw on the host (the 8-layer slice).  Same
+# distributions as above; torch's seeded CUDA generator; the Laplace draw is the inverse CDF
+# of a uniform draw, in fp32.  Still no method arithmetic.
+
+# (name, d_out, d_in) of the seven linears of one 70B-shaped decoder layer
+SLICE_LINEARS = (("q", 8192, 8192), ("k", 1024, 8192), ("v", 1024, 8192), ("o", 8192, 8192),
+                 ("gate", 28672, 8192), ("up", 28672, 8192), ("down", 8192, 28672))
+
+
+def slice_seed(seed: int, layer: int, matrix: int, variant: int = -1) -> int:
+    """Seed of one matrix's W_base (variant = -1) or of one variant's delta."""
+    return seed * 1_000_003 + layer * 1009 + matrix * 101 + (variant + 1) * 7_919_993
+
+
+def device_generator(seed: int, device):
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def device_base_weight(seed: int, d_out: int, d_in: int, device, std: float = 0.02):
+    """bf16 W_base ~ N(0, std) drawn on `device` (fp32 draw, RNE to bf16)."""
+    import torch
+
+    g = device_generator(seed, device)
+    return (torch.randn(d_out, d_in, generator=g, device=device, dtype=torch.float32) * std).to(torch.bfloat16)
+
+
+def device_finetuned_weight(seed: int, w_base, b: float):
+    """bf16(W_base + Laplace(0, b)) drawn on W_base's device."""
+    import torch
+
+    g = device_generator(seed, w_base.device)
+    # uniform on the open interval (0, 1): rand() may return 0, whose inverse CDF is infinite
+    u = torch.rand(w_base.shape, generator=g, device=w_base.device, dtype=torch.float32)
+    u = u * (1.0 - 2.0 ** -23) + 2.0 ** -24 - 0.5
+    delta = -b * torch.sign(u) * torch.log1p(-2.0 * u.abs())
+    return (w_base.float() + delta).to(torch.bfloat16)
+
+
+def slice_variant_scales(seed: int, V: int, b_lo: float = 5e-4, b_hi: float = 2e-3) -> np.ndarray:
+    return np.random.default_rng(seed).uniform(b_lo, b_hi, size=V)

@@ -45,6 +45,8 @@ def test_status_strings(lib):
 
 def test_workspace_sizes(lib):
     assert bd.bd_linear_workspace_size(4, 100, 256) >= 256
+    # multi: error word + x of one token group sorted by variant
+    assert bd.bd_linear_multi_workspace_size(64, 14, 8192, 8192) >= 1024 + 64 * 8192 * 2
     assert bd.bd_route_workspace_size(100, 14) >= 256
     pm = bd.bd_compress_workspace_size(28672, 8192, bd.BD_ALPHA_PER_MATRIX)
     pr = bd.bd_compress_workspace_size(28672, 8192, bd.BD_ALPHA_PER_ROW)
@@ -98,7 +100,7 @@ def test_multi_and_route_argument_checks(lib):
     atab = (ctypes.c_void_p * 2)(A + (3 << 30), A + (7 << 30))
     m = lambda V=2, vid=A + (8 << 30), t=tab: lib.bd_linear_multi(  # noqa: E731
         A, 4, vid, V, ctypes.addressof(t), ctypes.addressof(atab), 1, A + (1 << 30), 16, 256, A + (4 << 30), 1,
-        A + (5 << 30), 4096, None)
+        A + (5 << 30), 1 << 29, None)
     assert m(V=0) == bd.BD_ERR_INVALID_ARG
     assert m(V=65) == bd.BD_ERR_INVALID_ARG
     assert m(vid=A + (8 << 30) + 2) == bd.BD_ERR_MISALIGNED
