@@ -377,7 +377,7 @@ def oracle_time(wl: Workload, budget_s: float = 12.0, threads: int = 0):
             t_used += time.perf_counter() - t0
             n += 1
         return step_bytes * n / t_used / 1e9, cores, f"{n} whole steps ({t_used:.2f} s on {cores} threads)"
-    rows_done, t_used, chunk = 0, 0.0, 64
+    rows_done, t_used, chunk = 0, 0.0, 16
     while (t_used < budget_s or rows_done == 0) and rows_done < d_out:
         r = np.arange(rows_done, min(d_out, rows_done + chunk), dtype=np.int64)
         t0 = time.perf_counter()
@@ -433,8 +433,8 @@ def run_reference(args):
         return 0
     wl = Workload(args.workload, args.seed)
     step_bytes = sum(c[2] for c in _step_bytes_rows(wl))
-    # each step is a bounded sample so that the whole run stays near 150 s
-    budget = max(0.02, min(12.0, 150.0 / max(args.steps + args.warmup, 1)))
+    # each step is a bounded sample so that the whole run stays near 90 s of oracle time
+    budget = max(0.01, min(12.0, 90.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
         oracle_time(wl, budget_s=budget / 4)
     vals = []

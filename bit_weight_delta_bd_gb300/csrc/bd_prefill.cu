@@ -9,8 +9,10 @@
 //   warp 0      TMA producer: x tile [256 x 64] (128-byte swizzle), W_base
 //               tile [128 x 64] (128-byte swizzle) and the sign words of the
 //               tile's rows, all completing on one mbarrier per stage;
-//   warps 2..5  transform: thread = one row of the tile (TMEM lane); reads its
-//               64 W_base values from shared memory, adds +alpha or -alpha per
+//   warps 2..9  transform: thread = one row of the tile (TMEM lane) and one
+//               32-column half of the k-step (two warps per TMEM lane
+//               quarter); reads its 32 W_base values from shared memory, adds
+//               +alpha or -alpha per
 //               sign bit with packed bf16 adds (W_eff rounded to bf16, the
 //               MMA's input precision), and writes them into the stage's
 //               A-operand columns of tensor memory with tcgen05.st;
@@ -18,7 +20,8 @@
 //               K=16; A from tensor memory, B from shared memory, fp32
 //               accumulator in tensor memory) and frees each stage with
 //               tcgen05.commit;
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator, bf16/fp32 stores.
+//   warps 2..9  epilogue: tcgen05.ld of the accumulator (each warp half of
+//               the token columns of its lane quarter), bf16/fp32 stores.
 // So W_eff never goes through shared memory: per k-step the shared memory
 // sees the W and x tiles written once by TMA, W read once by the transform
 // and x read once by the tensor core.
@@ -41,7 +44,7 @@ constexpr int kXBytes = BN * BK * 2;                      // 32768
 constexpr int kWBytes = BM * BK * 2;                      // 16384
 constexpr int kSBytes = BM * 16;                          // 4 sign words per row (128 columns)
 constexpr int kStageBytes = kXBytes + kWBytes + kSBytes;  // 51200 (multiple of 1024)
-constexpr int kThreads = 192;                             // 6 warps
+constexpr int kThreads = 320;                             // 10 warps
 constexpr int kTmemCols = 512;                            // D: 256 columns; A ring: 4 x 32 columns
 constexpr int kDCol = 0;
 constexpr int kACol = 256;
@@ -59,7 +62,7 @@ struct PrefillParams {
 
 struct PrefillShared {
     uint64_t full[kStages];   // TMA landed
-    uint64_t afull[kStages];  // transform wrote the A stage (4 warp arrivals)
+    uint64_t afull[kStages];  // transform wrote the A stage (8 warp arrivals)
     uint64_t empty[kStages];  // MMAs reading the stage finished (tcgen05.commit)
     uint64_t accum;           // all MMAs finished
     uint32_t tmem_base;
@@ -100,7 +103,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.afull[s], 4);
+            mbar_init(&sh.afull[s], 8);
             mbar_init(&sh.empty[s], 1);
         }
         mbar_init(&sh.accum, 1);
@@ -161,7 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
     } else {
         // ------------------------------------------------------------ transform, then epilogue
-        const int quarter = warp & 3;  // TMEM lanes 32*quarter .. +31
+        const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
+        const int ch = (warp - 2) >> 2;   // column half of the k-step (warps 2..5 -> 0, 6..9 -> 1)
         const int rl = 32 * quarter + lane;
         const int64_t row = row0 + rl;
         float a = 0.0f;
@@ -179,19 +183,20 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             const uint8_t* st = dyn + s * kStageBytes;
             const uint8_t* wrow = st + kXBytes + rl * 128;
             const uint32_t* srow = reinterpret_cast<const uint32_t*>(st + kXBytes + kWBytes + rl * 16);
-            const uint32_t words[2] = {srow[2 * (i & 1)], srow[2 * (i & 1) + 1]};
-            uint32_t v[32];
+            const uint32_t word = srow[2 * (i & 1) + ch];  // sign bits of this warp's 32 columns
+            uint32_t v[16];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint4 u = *reinterpret_cast<const uint4*>(wrow + ((c ^ (rl & 7)) << 4));
+            for (int c = 0; c < 4; ++c) {
+                const int cc = 4 * ch + c;  // 16-byte chunk within the 128-byte row
+                const uint4 u = *reinterpret_cast<const uint4*>(wrow + ((cc ^ (rl & 7)) << 4));
                 v[4 * c + 0] = u.x;
                 v[4 * c + 1] = u.y;
                 v[4 * c + 2] = u.z;
                 v[4 * c + 3] = u.w;
             }
 #pragma unroll
-            for (int hw = 0; hw < 4; ++hw) {  // 16 columns per sign half-word
-                const uint32_t h = (words[hw >> 1] >> (16 * (hw & 1))) & 0xFFFFu;
+            for (int hw = 0; hw < 2; ++hw) {  // 16 columns per sign half-word
+                const uint32_t h = (word >> (16 * hw)) & 0xFFFFu;
                 const uint32_t z = (h | (h << 15)) & 0x55555555u;
 #pragma unroll
                 for (int pp = 0; pp < 8; ++pp) {
@@ -202,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     v[8 * hw + pp] = *reinterpret_cast<uint32_t*>(&w2);
                 }
             }
-            tmem_st32(lane_addr + kACol + 32 * s, v);
+            tmem_st16(lane_addr + kACol + 32 * s + 16 * ch, v);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh.afull[s]);
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         // epilogue
         if (ok && __all_sync(0xffffffffu, pwait(sh, &sh.accum, 0u, p.err))) {
             tc_fence_after();
-            for (int cb = 0; cb < BN / 32; ++cb) {
+            for (int cb = ch * (BN / 64); cb < (ch + 1) * (BN / 64); ++cb) {
                 uint32_t d[32];
                 tmem_ld32(lane_addr + kDCol + 32 * cb, d);
                 if (row < p.d_out) {

@@ -59,10 +59,10 @@ constexpr int kSignRowBytes = 16;  // 4 sign words per row per stage
 constexpr int kMaxStages = 4;
 constexpr int kMaxKeys = kMaxVariants + 1;
 constexpr int kSingleConsumers = 4;  // 64 rows per CTA, up to three CTAs per SM
-constexpr int kMultiConsumers = 8;   // 128 rows per CTA, 2 stages (measured best on GB300)
+constexpr int kMultiConsumers = 8;   // 128 rows per CTA (64 with the token split), 2 stages
 constexpr int kMultiStages = 2;
 constexpr size_t kSingleBudget = 66u * 1024u;  // three CTAs per SM (measured best on GB300)
-constexpr size_t kMultiBudget = 220u * 1024u;
+constexpr size_t kMultiBudget = 110u * 1024u;  // two CTAs per SM
 
 struct SkinnyParams {
     CUtensorMap sign_map[kMaxVariants];  // [d_out][d_in/32] uint32, box 4 x block rows
@@ -191,14 +191,21 @@ __device__ void route_tokens(SkinnyShared& sh, const int32_t* vid, int T, int V,
 template <bool MULTI>
 constexpr int ctas_per_sm()
 {
-    return MULTI ? 1 : 2;
+    return 2;
 }
 
 template <int NT, bool MULTI, int NCONS>
 __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
     skinny_kernel(const __grid_constant__ SkinnyParams p)
 {
-    constexpr int kRows = 16 * NCONS;       // rows per CTA
+    // Multi-variant with >= 2 token tiles: two warps per 16-row tile, each
+    // owning half of the (variant-sorted) tiles, to halve the accumulators per
+    // warp (two CTAs per SM) while each variant's bits are still expanded by
+    // the one warp whose tiles hold its tokens.
+    constexpr int TS = (MULTI && NT >= 2) ? 2 : 1;
+    constexpr int NTW = NT / TS;                // token tiles per warp
+    constexpr int kRowTiles = NCONS / TS;
+    constexpr int kRows = 16 * kRowTiles;       // rows per CTA
     constexpr int kSignTile = kRows * kSignRowBytes;
     constexpr int kThreads = 32 * (NCONS + 1);
     constexpr int Tpad = 8 * NT;
@@ -256,9 +263,9 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
     const int c_end = static_cast<int>(static_cast<int64_t>(rank + 1) * nc / CK);
     const int n_chunks = c_end - c_begin;
 
-    float accb[NT][4], accs[NT][4];
+    float accb[NTW][4], accs[NTW][4];
 #pragma unroll
-    for (int j = 0; j < NT; ++j)
+    for (int j = 0; j < NTW; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) accb[j][e] = accs[j][e] = 0.0f;
 
@@ -297,12 +304,13 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
         }
     } else {
         // ------------------------------------------------------------ consumer warps
-        const int rl0 = 16 * warp + g;  // local rows rl0 and rl0 + 8 (both = g mod 8)
+        const int rl0 = 16 * (warp % kRowTiles) + g;  // local rows rl0 and rl0 + 8 (both = g mod 8)
+        const int j0 = (warp / kRowTiles) * NTW;       // first token tile of this warp
         const int c0 = ((2 * q) ^ g) << 4, c1 = ((2 * q + 1) ^ g) << 4;  // swizzled chunk offsets
-        int my_key[NT];
+        int my_key[NTW];
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int pos = 8 * j + g;
+        for (int j = 0; j < NTW; ++j) {
+            const int pos = 8 * (j0 + j) + g;
             my_key[j] = pos < T ? sh.keyp[pos] : -1;
         }
         for (int i = 0; i < n_chunks; ++i) {
@@ -346,23 +354,24 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
                 } else {
                     // base contraction for every tile: independent accumulator chains
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) {
-                        const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
+                    for (int j = 0; j < NTW; ++j) {
+                        const uint8_t* xr = xst + (8 * (j0 + j) + g) * kHalfRowBytes;
                         mma4(accb[j], W0, W1, *reinterpret_cast<const uint4*>(xr + c0),
                              *reinterpret_cast<const uint4*>(xr + c1));
                     }
                     // sign contraction: each active variant's bits expanded once, applied to
                     // its own tokens of the tiles it spans (warp-uniform tile predicates)
                     for (int a = 0; a < n_act; ++a) {
+                        const int tf = sh.slot_tile_first[a] - j0, tl = sh.slot_tile_last[a] - j0;
+                        if (tl < 0 || tf >= NTW) continue;  // no token of this variant in my tiles
                         const uint32_t* sb = sgn + a * (kSignTile / 4);
                         expand_signs((sb[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
                         expand_signs((sb[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
                         const int key = sh.act[a] + 1;
-                        const int tf = sh.slot_tile_first[a], tl = sh.slot_tile_last[a];
 #pragma unroll
-                        for (int j = 0; j < NT; ++j) {
+                        for (int j = 0; j < NTW; ++j) {
                             if (j < tf || j > tl) continue;
-                            const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
+                            const uint8_t* xr = xst + (8 * (j0 + j) + g) * kHalfRowBytes;
                             const bool mine = (my_key[j] == key);
                             const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                             const uint4 xa = mine ? *reinterpret_cast<const uint4*>(xr + c0) : z;
@@ -382,10 +391,11 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
     float* red_b = reinterpret_cast<float*>(dyn);
     float* red_s = red_b + kRows * Tpad;
     if (warp < NCONS) {
-        const int r0 = 16 * warp + g;
+        const int r0 = 16 * (warp % kRowTiles) + g;
+        const int j0 = (warp / kRowTiles) * NTW;
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int pos = 8 * j + 2 * q;
+        for (int j = 0; j < NTW; ++j) {
+            const int pos = 8 * (j0 + j) + 2 * q;
             red_b[r0 * Tpad + pos] = accb[j][0];
             red_b[r0 * Tpad + pos + 1] = accb[j][1];
             red_b[(r0 + 8) * Tpad + pos] = accb[j][2];
@@ -429,7 +439,7 @@ cudaError_t launch_cfg(const SkinnyParams& prm, size_t smem, cudaStream_t stream
     auto kern = skinny_kernel<NT, MULTI, NCONS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    constexpr int kRows = 16 * NCONS;
+    constexpr int kRows = 16 * NCONS / ((MULTI && NT >= 2) ? 2 : 1);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>((prm.d_out + kRows - 1) / kRows * prm.CK));
     cfg.blockDim = dim3(32 * (NCONS + 1));
@@ -457,6 +467,9 @@ cudaError_t launch_nt(int nt, const SkinnyParams& prm, size_t smem, cudaStream_t
 }
 
 int tiles_for(int T) { return T <= 8 ? 1 : T <= 16 ? 2 : T <= 32 ? 4 : 8; }
+
+// Rows per CTA (the multi-variant kernel splits 8 token tiles over two warps).
+int rows_for(bool multi, int nt) { return multi ? 16 * kMultiConsumers / (nt >= 2 ? 2 : 1) : 16 * kSingleConsumers; }
 
 size_t stage_bytes_for(int rows, int sign_slots, int nt)
 {
@@ -486,10 +499,10 @@ __global__ void __launch_bounds__(256) gather_sorted_x_kernel(const uint16_t* __
 int skinny_group_tokens(bool multi, int V)
 {
     if (!multi) return kSkinnyMaxTokens;
-    const int rows = 16 * kMultiConsumers;
     for (int G = kSkinnyMaxTokens; G > 8; G /= 2) {
         const int slots = V < G ? V : G;
-        if (kMultiStages * stage_bytes_for(rows, slots, tiles_for(G)) + 1024 <= kMultiBudget) return G;
+        const int nt = tiles_for(G);
+        if (kMultiStages * stage_bytes_for(rows_for(true, nt), slots, nt) + 1024 <= kMultiBudget) return G;
     }
     return 8;
 }
@@ -497,10 +510,10 @@ int skinny_group_tokens(bool multi, int V)
 cudaError_t launch_skinny(const SkinnyArgs& a, int /*sm_count*/, cudaStream_t stream)
 {
     const bool multi = a.vid != nullptr;
-    const int rows = 16 * (multi ? kMultiConsumers : kSingleConsumers);
     const int nc = static_cast<int>(a.d_in / kChunk);
     const int T = static_cast<int>(a.T);
     const int nt = tiles_for(T);
+    const int rows = rows_for(multi, nt);
     if (T < 1 || T > skinny_group_tokens(multi, a.V)) return cudaErrorInvalidValue;
     if (multi && a.x_sorted == nullptr) return cudaErrorInvalidValue;
 
