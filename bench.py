@@ -47,14 +47,20 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
 # one ncu capture, keyed by kernel; each entry records the sha256 of the
 # kernel's source file at capture time and is ignored once that source has
-# changed.  Summaries of the captures are in profiles/.
+# changed.  Summaries of the captures are in profiles/.  An entry whose value
+# is a float is a ratio (traffic / algorithmic bytes) taken on one launch of a
+# smaller call of the same kernel and applied to the average launch: the
+# slice workload (56 calls, 26 GB resident) is captured on its 28672x8192
+# gate projection only, whose traffic tracks the algorithmic bytes.
 NCU_TRAFFIC = {
-    # (kernel, workload): (source sha256[:16], source file, bytes per launch)
-    ("skinny_kernel<1,false>", "decode"): ("e9981b99d57d6e73", "bd_skinny.cu", 499_425_536 + 3_763_456),
+    # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
+    ("skinny_kernel<1,false>", "decode"): ("626c1a5ceec5ed51", "bd_skinny.cu", 499_453_696 + 3_220_224),
     ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_613_184 + 7_913_728),
-    ("prefill_kernel", "prefill"): ("7c5aa4018aaeb9a3", "bd_prefill.cu", 612_366_592 + 63_392_000),
-    ("gather_sorted_x + skinny_kernel<8,true>", "multi"): ("e9981b99d57d6e73", "bd_skinny.cu",
-                                                           255_675_648 + 4_176_384),
+    ("prefill_kernel", "prefill"): ("d0586c42d68bd685", "bd_prefill.cu", 613_019_648 + 63_200_000),
+    ("gather_sorted_x + skinny_kernel<8,true>", "multi"): ("626c1a5ceec5ed51", "bd_skinny.cu",
+                                                           254_434_816 + 4_267_520),
+    ("gather_sorted_x + skinny_kernel<4,true>", "slice"): ("626c1a5ceec5ed51", "bd_skinny.cu",
+                                                           (796_455_936 + 5_525_248) / 796_344_448),
 }
 
 
@@ -542,7 +548,7 @@ def run_gpu(args):
     traffic = None
     tr = NCU_TRAFFIC.get((dom, wl.name))
     if tr is not None and tr[0] == _src_sha(tr[1]):
-        traffic = tr[2]
+        traffic = tr[2] * bytes_per_launch if isinstance(tr[2], float) else tr[2]
     if wl.name == "prefill":
         flops_per_launch = calls[0][3]
         tf = flops_per_launch / (avg_ms * 1e-3) / 1e12
