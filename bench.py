@@ -57,10 +57,6 @@ NCU_TRAFFIC = {
     ("skinny_kernel<1,false>", "decode"): ("626c1a5ceec5ed51", "bd_skinny.cu", 499_453_696 + 3_220_224),
     ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_613_184 + 7_913_728),
     ("prefill_kernel", "prefill"): ("d0586c42d68bd685", "bd_prefill.cu", 613_019_648 + 63_200_000),
-    ("gather_sorted_x + skinny_kernel<8,true>", "multi"): ("626c1a5ceec5ed51", "bd_skinny.cu",
-                                                           254_434_816 + 4_267_520),
-    ("gather_sorted_x + skinny_kernel<4,true>", "slice"): ("626c1a5ceec5ed51", "bd_skinny.cu",
-                                                           (796_455_936 + 5_525_248) / 796_344_448),
 }
 
 
@@ -223,7 +219,7 @@ class GpuRun:
             T = wl.tokens[0]
             nbytes = (2 * wl.d_out * wl.d_in + len(active) * (wl.d_out * wl.d_in // 8 + 4 * wl.n_alpha) +
                       2 * T * wl.d_in + 2 * T * wl.d_out + 4 * T)
-            out.append(("linear_multi_T64", "gather_sorted_x + skinny_kernel<8,true>", nbytes,
+            out.append(("linear_multi_T64", "multi_prepare + multi_kernel<8>", nbytes,
                         4 * T * wl.d_out * wl.d_in,
                         lambda: bd.bd_linear_multi(self.xs[0], self.vid, self.signs, self.alpha, self.mode, self.wb,
                                                    self.ys[0], self.ws)))
@@ -296,7 +292,7 @@ class SliceRun:
         out = []
         for label, d_out, d_in, wb, signs, alphas, x, y in self.mats:
             nbytes = 2 * d_out * d_in + active * (d_out * d_in // 8 + 4 * d_out) + 2 * T * d_in + 2 * T * d_out + 4 * T
-            out.append((label, "gather_sorted_x + skinny_kernel<4,true>", nbytes, 4 * T * d_out * d_in,
+            out.append((label, "multi_prepare + multi_kernel<4>", nbytes, 4 * T * d_out * d_in,
                         (lambda wb=wb, signs=signs, alphas=alphas, x=x, y=y:
                          bd.bd_linear_multi(x, self.vid, signs, alphas, bd.BD_ALPHA_PER_ROW, wb, y, self.ws))))
         return out

@@ -203,15 +203,34 @@ bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const 
     return BD_OK;
 }
 
-// Multi-variant workspace: the error word, then (at 1 KiB) x of one token
-// group sorted by variant for the TMA loads.
+// Multi-variant workspace for one group of up to 64 tokens: the error word,
+// then (at 1 KiB) x sorted by variant, the zero-padded per-variant x tiles of
+// the sign phases and the per-token corrections.
+namespace {
+
+struct MultiWs {
+    size_t xs, xp, corr, total;
+};
+
+MultiWs multi_ws_layout(int64_t T, int32_t V, int64_t d_in)
+{
+    const int64_t tg = T < bd::kSkinnyMaxTokens ? T : bd::kSkinnyMaxTokens;
+    const auto up = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
+    MultiWs w{};
+    w.xs = 1024;
+    w.xp = w.xs + up(static_cast<size_t>(tg) * static_cast<size_t>(d_in) * 2);
+    const size_t ptiles = static_cast<size_t>(bd::multi_max_ptiles(static_cast<int>(tg), V));
+    w.corr = w.xp + up(ptiles * 8 * static_cast<size_t>(d_in) * 2);
+    w.total = w.corr + up(static_cast<size_t>(tg) * 4);
+    return w;
+}
+
+}  // namespace
+
 size_t bd_linear_multi_workspace_size(int64_t T, int32_t V, int64_t /*d_out*/, int64_t d_in)
 {
     if (T < 0 || d_in < 0 || V < 1 || V > BD_MAX_VARIANTS) return kWsHeader;
-    const int64_t group = bd::skinny_group_tokens(true, V);
-    const int64_t tg = T < group ? T : group;
-    const size_t n = 1024 + static_cast<size_t>(tg) * static_cast<size_t>(d_in) * 2;
-    return (n + 255) & ~static_cast<size_t>(255);
+    return multi_ws_layout(T, V, d_in).total;
 }
 
 bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int32_t V,
@@ -241,9 +260,10 @@ bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int3
     if (bd_status s = device_info(&sms)) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t ysz = out_dtype == BD_OUT_F32 ? 4 : 2;
-    const int64_t group = bd::skinny_group_tokens(true, V);
+    const int64_t group = bd::kSkinnyMaxTokens;
+    const MultiWs lay = multi_ws_layout(T, V, d_in);
     for (int64_t t0 = 0; t0 < T; t0 += group) {
-        bd::SkinnyArgs a{};
+        bd::MultiArgs a{};
         a.x = x + t0 * d_in;
         a.vid = vid + t0;
         a.w_base = w_base;
@@ -257,8 +277,10 @@ bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int3
         a.y = static_cast<char*>(y) + static_cast<size_t>(t0) * d_out * ysz;
         a.out_f32 = out_dtype == BD_OUT_F32;
         a.err = err_word(ws);
-        a.x_sorted = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + 1024);
-        if (bd_status s = launched(bd::launch_skinny(a, sms, st))) return s;
+        a.x_sorted = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + lay.xs);
+        a.xp = reinterpret_cast<uint8_t*>(static_cast<char*>(ws) + lay.xp);
+        a.corr = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.corr);
+        if (bd_status s = launched(bd::launch_multi(a, st))) return s;
     }
     return BD_OK;
 }

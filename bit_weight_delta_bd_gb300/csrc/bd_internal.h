@@ -46,6 +46,31 @@ cudaError_t launch_skinny(const SkinnyArgs& a, int sm_count, cudaStream_t stream
 // multi-variant kernel when many variants would overflow shared memory).
 int skinny_group_tokens(bool multi, int V);
 
+// ---- multi-variant linear (bd_multi.cu) -------------------------------------------------------
+
+struct MultiArgs {
+    const uint16_t* x;        // [T][d_in] bf16 bits, T <= kSkinnyMaxTokens
+    const int32_t* vid;       // [T]
+    const uint16_t* w_base;   // [d_out][d_in]
+    int64_t T, d_out, d_in;
+    int V;
+    int per_row;
+    const uint32_t* signs[kMaxVariants];
+    const float* alpha[kMaxVariants];
+    void* y;                  // [T][d_out]
+    int out_f32;
+    uint32_t* err;
+    uint16_t* x_sorted;       // scratch [T][d_in]: x sorted by variant
+    uint8_t* xp;              // scratch [multi_max_ptiles(T, V)][8][d_in] bf16: padded per-variant tiles
+    float* corr;              // scratch [T]: per-token correction of the recoded sign contraction
+};
+
+// Upper bound of the zero-padded 8-token tiles of a group of T tokens over V
+// variants: sum over variants of ceil(n_v / 8) <= (T + 7 min(T, V)) / 8.
+int multi_max_ptiles(int T, int V);
+
+cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream);
+
 // ---- router (bd_route.cu) ---------------------------------------------------------------------
 
 cudaError_t launch_route(const int32_t* vid, int64_t T, int V, int32_t* perm, int32_t* seg_off, uint32_t* err,

@@ -129,6 +129,12 @@ bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const 
  * inside the kernel and every active variant's sign tile is applied to its
  * own tokens only.  An id outside [-1, V) sets BD_ERR_BAD_VARIANT in the
  * error word and that token is computed as a base-model token.
+ * Accumulation is fp32.  The sign contraction runs on an exact recoding of
+ * the +-1 operand: each sign bit becomes a mantissa or sign bit of a
+ * constant of its column (mod 4), and the token's share of those constants
+ * is subtracted once at the end; its fp32 rounding error is at most about 20
+ * times that of the plain form (relative to alpha * sum_j |x_j|), and
+ * non-finite x give non-finite outputs.
  * ------------------------------------------------------------------------ */
 size_t bd_linear_multi_workspace_size(int64_t T, int32_t V, int64_t d_out, int64_t d_in);
 
