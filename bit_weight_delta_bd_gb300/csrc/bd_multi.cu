@@ -25,24 +25,26 @@
 // accumulators of the base phase through a small per-warp shared buffer.
 //
 // Sign operand recoding (exact).  Expanding 16 sign bits into eight bf16 +-1
-// pairs needs a shift and a mask per pair.  Here each operand element is
-// v = a_c + b instead, with b the sign bit (1 for s = +1) and a_c a constant
-// of the column residue c = j mod 4: the bit stays where it is and becomes
-// mantissa bit 4, 5 or 6 of a bf16 whose exponent gives that bit the value
-// exactly 1 (a = 8, 4, 2 for c = 0, 1, 2), or the sign bit of +-0.5
-// (a = -0.5, c = 3).  A 32-bit sign word rotated by 0, 4, 8 and 12 bits puts
-// every one of its bits on such a place, so each bf16 pair of the MMA operand
-// is one (rotated word & mask) ^ constant.  With s = 2b - 1:
+// pairs needs a shift and a mask per pair.  Here the sign contraction runs on
+// operand elements v = a_c + b instead, with b the sign bit (1 for s = +1) and
+// a_c a constant of the column residue c = j mod 4 (a = 8, 4, 2, -0.5).  The
+// bit is never moved: each bf16 pair of the operand is
+// (rotated sign word & mask_c) ^ const, a -0.5 whose mantissa bit 4, 5 or 6
+// (c = 0, 1, 2) or sign bit (c = 3) is the sign bit, and the x operand is
+// pre-scaled by -16, -8, -4 or 1 so that each product equals x_j (a_c + b_j)
+// exactly.  A 32-bit sign word rotated by 0, 4, 8 and 12 bits puts every one
+// of its bits on such a place.  With s = 2b - 1:
 //   sum_j x_j s_j = 2 M - C,   M = sum_j x_j v_j,   C = sum_j x_j (2 a_j + 1),
 // where C depends on the token only and is computed once by the prepare pass
-// (fp64, rounded to fp32).  Every product x_j v_j is exact in fp32 (at most
-// 12 significant bits); M is accumulated in fp32 like the plain form.  The
-// x operand of the sign MMA is permuted inside every 32-column group to the
-// order in which the rotated words deliver the bits; both operands use the
-// same permutation of k, so the contraction is unchanged.
+// (fp64, rounded to fp32).  Every product is exact in fp32 (at most 12
+// significant bits); M is accumulated in fp32 like the plain form.  The x
+// operand of the sign MMA is also permuted inside every 32-column group to
+// the order in which the rotated words deliver the bits; both operands use
+// the same permutation of k, so the contraction is unchanged.
 #include <cooperative_groups.h>
 
 #include "bd_device.cuh"
+#include "bd_tcgen05.cuh"
 #include "bd_tma.h"
 
 namespace cg = cooperative_groups;
@@ -50,38 +52,51 @@ namespace cg = cooperative_groups;
 namespace bd {
 namespace {
 
-constexpr int kConsumers = 8;
-constexpr int kRows = 16 * kConsumers;  // output rows per CTA
-constexpr int kThreads = 32 * (kConsumers + 1);
-constexpr int kStages = 2;
-constexpr int kChunk = 128;           // d_in columns per chunk
-constexpr int kHalfRowBytes = 128;    // 64 bf16 columns: one 128-byte swizzle atom
-constexpr int kWHalf = kRows * kHalfRowBytes;  // 16 KB
-constexpr int kSignChunk = kRows * 16;          // 4 sign words x 128 rows = 2 KB
-constexpr int kPadTile = 8 * kChunk * 2;       // one 8-token tile of one chunk = 2 KB
+constexpr int kConsumers = 8;                 // warps 0..7: variant phases, then the epilogue
+constexpr int kVarProducerWarp = kConsumers;  // warp 8: TMA of the variant phases
+constexpr int kBaseWarp = kConsumers + 1;     // warp 9: tensor memory, base-phase TMA and tcgen05 MMAs
+constexpr int kRows = 16 * kConsumers;        // 128 output rows per CTA = tensor-memory lanes
+constexpr int kThreads = 32 * (kConsumers + 2);
+constexpr int kChunk = 128;                   // d_in columns per chunk
+constexpr int kHalfRowBytes = 128;            // 64 bf16 columns: one 128-byte swizzle atom
+constexpr int kWTile = kRows * kHalfRowBytes; // W_base box [128 rows x 64 columns] = 16 KB
+constexpr int kBaseStages = 3;
+constexpr int kVarStages = 2;
+constexpr int kVarSlot = 16 * 1024;
+constexpr int kSignChunk = kRows * 16;        // 4 sign words x 128 rows = 2 KB
+constexpr int kPadTile = 8 * kChunk * 2;      // one 8-token tile of one chunk = 2 KB
 constexpr int kMaxTok = kSkinnyMaxTokens;
 constexpr int kMaxKeys = kMaxVariants + 1;
-constexpr int kMaxGroup = 8;          // chunks per variant stage
+constexpr int kPhaseTiles = 4;                // padded tiles per variant phase (more: several phases)
+constexpr int kTmemCols = 64;
 
-// Recoding: kind k = column residue mod 4.  Bit positions lo (k) and hi (k+16)
-// of the operand register, their mask, and the constant bf16 pair a_k (the
-// sign-bit kind stores -0.5 and the XOR flips it to +0.5 when the bit is 1).
+// Chunks per variant stage for a phase of L padded tiles.
+__host__ __device__ constexpr int phase_group(int L)
+{
+    return kVarSlot / (kSignChunk + L * kPadTile) < 8 ? kVarSlot / (kSignChunk + L * kPadTile) : 8;
+}
+
+// Recoding: kind k = column residue mod 4.  The operand pair of kind k is
+// (rotated word & recode_mask(k)) ^ kRecodeConst: one bf16 -0.5 per half with
+// the kind's bit placed into mantissa bit 4, 5 or 6 (value -0.5 - b/16,
+// -0.5 - b/8, -0.5 - b/4) or XORed into the sign bit (-0.5 + b).  The x
+// operand of kind k is pre-scaled by recode_sigma(k) = -16, -8, -4, 1 (exact
+// power-of-two scalings), which makes every product x * (a_k + b) with
+// a_k = 8, 4, 2, -0.5.
+constexpr uint32_t kRecodeConst = 0xBF00BF00u;
 __host__ __device__ constexpr uint32_t recode_mask(int k)
 {
     return k == 0 ? 0x00100010u : k == 1 ? 0x00200020u : k == 2 ? 0x00400040u : 0x80008000u;
 }
-__host__ __device__ constexpr uint32_t recode_const(int k)  // 8, 4, 2, -0.5 (bf16 pairs)
-{
-    return k == 0 ? 0x41004100u : k == 1 ? 0x40804080u : k == 2 ? 0x40004000u : 0xBF00BF00u;
-}
 __host__ __device__ constexpr int recode_lo_bit(int k) { return k == 0 ? 4 : k == 1 ? 5 : k == 2 ? 6 : 15; }
+__host__ __device__ constexpr float recode_sigma(int k) { return k == 0 ? -16.0f : k == 1 ? -8.0f : k == 2 ? -4.0f : 1.0f; }
 // 2 a_k + 1 for the per-token correction C.
 __host__ __device__ constexpr double recode_corr(int k) { return k == 0 ? 17.0 : k == 1 ? 9.0 : k == 2 ? 5.0 : 0.0; }
 
 struct MultiParams {
     CUtensorMap sign_map[kMaxVariants];  // [d_out][d_in/32] uint32, box 4 x 128 rows
     CUtensorMap w_map;                   // [d_out][d_in] bf16, box 64 x 128 rows, 128B swizzle
-    CUtensorMap x_map;                   // sorted x [T][d_in] bf16, box 64 x 8*NT, 128B swizzle
+    CUtensorMap x_map;                   // sorted x [T][d_in] bf16, box 64 x max(16, 8*NT), 128B swizzle
     const uint8_t* xp;                   // padded, permuted tiles of the variant phases
     const float* corr;                   // C per sorted position
     const int32_t* vid;
@@ -97,6 +112,9 @@ struct Routing {
     int key[kMaxTok];    // key of token t (caller order); key = vid + 1, 0 = base model
     int perm[kMaxTok];   // sorted position -> token
     int keyp[kMaxTok];   // sorted position -> key
+    int rank[kMaxTok];   // token t -> rank among the earlier tokens with its key
+    int cnt[kMaxKeys];   // tokens per key
+    int cnt0[kMaxKeys];  // tokens per key among tokens 0..31
     int seg[kMaxKeys + 1];
     int slot_of_key[kMaxKeys];
     int act[kMaxTok];    // slot -> variant id
@@ -107,64 +125,106 @@ struct Routing {
 };
 
 struct MultiShared {
-    uint64_t full[kStages];
-    uint64_t empty[kStages];
-    Routing rt;
-    int grp[kMaxTok];    // slot -> chunks per variant stage
+    uint64_t full_v[kVarStages];    // variant stage landed (TMA)
+    uint64_t empty_v[kVarStages];   // variant stage consumed (8 consumer warps)
+    uint64_t full_b[kBaseStages];   // base stage landed (TMA)
+    uint64_t empty_b[kBaseStages];  // base stage read by the tensor core (tcgen05.commit)
+    uint64_t accum;                 // every base MMA complete
+    uint32_t tmem_base;
     volatile int abort;
+    Routing rt;
     float flush[kConsumers][16 * 8];
 };
 
 // Stable counting sort of the T (<= 64) tokens by key = vid + 1 (ids outside
 // [-1, V) become base tokens and are flagged by block 0 of a launch), then
-// the active variants in key order and their padded tiles.  Uses threads
-// 0..63 of the block and ends with __syncthreads.
+// the active variants in key order and their padded tiles.  Needs at least 96
+// threads; ends with __syncthreads.  Ranks come from __match_any_sync inside
+// each 32-token warp plus warp 0's per-key counts; the per-key offsets, slots
+// and padded-tile offsets from one warp's chunked prefix scans.
 __device__ void route_group(Routing& rt, const int32_t* vid, int T, int V, uint32_t* err, int tid)
 {
+    const int lane = tid & 31, warp = tid >> 5;
+    if (tid < kMaxKeys) {
+        rt.cnt[tid] = 0;
+        rt.cnt0[tid] = 0;
+    }
+    __syncthreads();
     if (tid < kMaxTok) {
-        int k = kMaxKeys;  // past T: never counted
+        int k = -1;
         if (tid < T) {
             const int v = vid[tid];
             const bool ok = (v >= -1 && v < V);
             if (!ok && blockIdx.x == 0 && blockIdx.y == 0) raise_error(err, kErrBadVariant);
             k = ok ? v + 1 : 0;
+            rt.key[tid] = k;
         }
-        rt.key[tid] = k;
-    }
-    __syncthreads();
-    if (tid == 0) {
-        int cnt[kMaxKeys];
-        for (int k = 0; k <= V; ++k) cnt[k] = 0;
-        for (int t = 0; t < T; ++t) ++cnt[rt.key[t]];
-        rt.seg[0] = 0;
-        int n_act = 0, pt = 0;
-        for (int k = 0; k <= V; ++k) {
-            rt.seg[k + 1] = rt.seg[k] + cnt[k];
-            rt.slot_of_key[k] = -1;
-            if (k >= 1 && cnt[k] > 0) {
-                rt.slot_of_key[k] = n_act;
-                rt.act[n_act] = k - 1;
-                rt.len[n_act] = (cnt[k] + 7) / 8;
-                rt.ptile[n_act] = pt;
-                pt += rt.len[n_act];
-                ++n_act;
+        // lanes past T get distinct negative labels and never match a real key
+        const unsigned peers = __match_any_sync(0xffffffffu, tid < T ? k : -1 - lane);
+        if (tid < T) {
+            rt.rank[tid] = __popc(peers & ((1u << lane) - 1u));
+            if (lane == __ffs(peers) - 1) {
+                atomicAdd(&rt.cnt[k], __popc(peers));
+                if (warp == 0) rt.cnt0[k] = __popc(peers);
             }
         }
-        rt.n_act = n_act;
-        rt.n_ptiles = pt;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int carry_seg = 0, carry_slot = 0, carry_pt = 0;
+        for (int base = 0; base <= V; base += 32) {
+            const int k = base + lane;
+            const int c = k <= V ? rt.cnt[k] : 0;
+            const int a = (k >= 1 && c > 0) ? 1 : 0;
+            const int ln = a ? (c + 7) / 8 : 0;
+            int sc = c, sa = a, sl = ln;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int tc = __shfl_up_sync(0xffffffffu, sc, o);
+                const int ta = __shfl_up_sync(0xffffffffu, sa, o);
+                const int tl = __shfl_up_sync(0xffffffffu, sl, o);
+                if (lane >= o) {
+                    sc += tc;
+                    sa += ta;
+                    sl += tl;
+                }
+            }
+            if (k <= V) {
+                rt.seg[k] = carry_seg + sc - c;
+                rt.slot_of_key[k] = a ? carry_slot + sa - 1 : -1;
+                if (a) {
+                    rt.act[carry_slot + sa - 1] = k - 1;
+                    rt.len[carry_slot + sa - 1] = ln;
+                    rt.ptile[carry_slot + sa - 1] = carry_pt + sl - ln;
+                }
+            }
+            carry_seg += __shfl_sync(0xffffffffu, sc, 31);
+            carry_slot += __shfl_sync(0xffffffffu, sa, 31);
+            carry_pt += __shfl_sync(0xffffffffu, sl, 31);
+        }
+        if (lane == 0) {
+            rt.seg[V + 1] = carry_seg;
+            rt.n_act = carry_slot;
+            rt.n_ptiles = carry_pt;
+        }
     }
     __syncthreads();
     if (tid < T) {
         const int k = rt.key[tid];
-        int r = 0;
-        for (int t = 0; t < tid; ++t) r += (rt.key[t] == k);
-        rt.perm[rt.seg[k] + r] = tid;
-        rt.keyp[rt.seg[k] + r] = k;
+        const int pos = rt.seg[k] + rt.rank[tid] + (warp == 1 ? rt.cnt0[k] : 0);
+        rt.perm[pos] = tid;
+        rt.keyp[pos] = k;
     }
     __syncthreads();
 }
 
 // ---------------------------------------------------------------- prepare pass
+
+// bf16 bits of sigma * x for a power-of-two sigma (exact up to overflow).
+__device__ __forceinline__ uint16_t scaled_bits(uint16_t xb, float sigma)
+{
+    return __bfloat16_as_ushort(__float2bfloat16_rn(sigma * __bfloat162float(__ushort_as_bfloat16(xb))));
+}
 
 // One block per sorted token position (blocks 0..T-1) and one per empty row
 // of a padded tile (the rest).  Writes, for the CTA-level layout of the main
@@ -242,7 +302,8 @@ __global__ void __launch_bounds__(256) multi_prepare_kernel(const uint16_t* __re
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
                     const int lo = (recode_lo_bit(k) + 4 * i) & 31, hi = (recode_lo_bit(k) + 16 + 4 * i) & 31;
-                    o[k] = static_cast<uint32_t>(v[lo]) | (static_cast<uint32_t>(v[hi]) << 16);
+                    o[k] = static_cast<uint32_t>(scaled_bits(v[lo], recode_sigma(k))) |
+                           (static_cast<uint32_t>(scaled_bits(v[hi], recode_sigma(k))) << 16);
                 }
                 *reinterpret_cast<uint4*>(tile + ((i * 8 + g) * 4 + q) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
             }
@@ -278,43 +339,43 @@ __device__ __forceinline__ bool wait_or_abort(MultiShared& sh, uint64_t* bar, ui
     return true;
 }
 
-__device__ __forceinline__ void mma4(float (&acc)[4], const uint32_t (&r0)[8], const uint32_t (&r1)[8],
-                                     const uint4 xa, const uint4 xb)
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p)
 {
-    mma_bf16_16816(acc, r0[0], r1[0], r0[1], r1[1], xa.x, xa.y);
-    mma_bf16_16816(acc, r0[2], r1[2], r0[3], r1[3], xa.z, xa.w);
-    mma_bf16_16816(acc, r0[4], r1[4], r0[5], r1[5], xb.x, xb.y);
-    mma_bf16_16816(acc, r0[6], r1[6], r0[7], r1[7], xb.z, xb.w);
+    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
-constexpr int base_stage_bytes(int nt) { return 2 * kWHalf + 2 * (8 * nt) * kHalfRowBytes; }
-
-// Consumer side of one variant phase with L padded tiles: the sign MMAs over
-// the CTA's d_in slice, then alpha * 2M added into the base accumulators.
-// Returns false when the pipeline was aborted.  i_stage is the running stage
-// counter shared with the producer's schedule.
+// Consumer side of one variant phase over L padded tiles (tiles t0 ..
+// t0 + L - 1 of the variant in slot `slot`): the sign MMAs over the CTA's
+// d_in slice, then alpha * 2M added into the per-token accumulators.
+// Returns false when the pipeline was aborted.  i_stage is the running
+// variant-stage counter shared with the producer's schedule.
 template <int NT, int L>
-__device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams& p, uint8_t* ring, int stage_bytes,
-                                              int slot, int n_chunks, int& i_stage, float (&acc_b)[NT][4],
-                                              int warp, int g, int q, int64_t row0)
+__device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams& p, const uint8_t* vring, int slot,
+                                              int t0, int n_chunks, int& i_stage, float (&acc_b)[NT][4], int warp,
+                                              int g, int q, int64_t row0)
 {
-    float acc[L][4];
+    constexpr int grp = phase_group(L);
+    // Variants with one or two tiles keep two accumulator sets (even and odd
+    // MMA steps) so that consecutive MMAs do not wait on each other.
+    constexpr int NS = L <= 2 ? 2 : 1;
+    float acc[L][NS][4];
 #pragma unroll
     for (int r = 0; r < L; ++r)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[r][e] = 0.0f;
+        for (int h = 0; h < NS; ++h)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[r][h][e] = 0.0f;
     const int rl0 = 16 * warp + g;
-    const int grp = sh.grp[slot];
     bool ok = true;
     for (int c0 = 0; c0 < n_chunks; c0 += grp) {
         const int cnt = n_chunks - c0 < grp ? n_chunks - c0 : grp;
-        const int s = i_stage % kStages;
-        if (!__all_sync(0xffffffffu, wait_or_abort(sh, &sh.full[s], static_cast<uint32_t>(i_stage / kStages) & 1u,
-                                                   p.err))) {
+        const int s = i_stage % kVarStages;
+        if (!__all_sync(0xffffffffu,
+                        wait_or_abort(sh, &sh.full_v[s], static_cast<uint32_t>(i_stage / kVarStages) & 1u, p.err))) {
             ok = false;
             break;
         }
-        const uint8_t* st = ring + static_cast<size_t>(s) * stage_bytes;
+        const uint8_t* st = vring + static_cast<size_t>(s) * kVarSlot;
         const uint8_t* pads = st + cnt * kSignChunk;
         for (int cc = 0; cc < cnt; ++cc) {
             const uint32_t* sg = reinterpret_cast<const uint32_t*>(st + cc * kSignChunk);
@@ -326,23 +387,23 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
                 uint32_t a0[4], a1[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    a0[k] = (u0 & recode_mask(k)) ^ recode_const(k);
-                    a1[k] = (u1 & recode_mask(k)) ^ recode_const(k);
+                    a0[k] = (u0 & recode_mask(k)) ^ kRecodeConst;
+                    a1[k] = (u1 & recode_mask(k)) ^ kRecodeConst;
                 }
 #pragma unroll
                 for (int r = 0; r < L; ++r) {
                     const uint4 xv = *reinterpret_cast<const uint4*>(pc + r * kPadTile + i * 512);
-                    mma_bf16_16816(acc[r], a0[0], a1[0], a0[1], a1[1], xv.x, xv.y);
-                    mma_bf16_16816(acc[r], a0[2], a1[2], a0[3], a1[3], xv.z, xv.w);
+                    mma_bf16_16816(acc[r][0], a0[0], a1[0], a0[1], a1[1], xv.x, xv.y);
+                    mma_bf16_16816(acc[r][NS - 1], a0[2], a1[2], a0[3], a1[3], xv.z, xv.w);
                 }
             }
         }
         __syncwarp();
-        if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty[s]);
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty_v[s]);
         ++i_stage;
     }
     if (!ok) return false;
-    // alpha * 2M into the base accumulators of the variant's tokens
+    // alpha * 2M into the accumulators of the variant's tokens
     const Routing& rt = sh.rt;
     const int v = rt.act[slot];
     const int seg0 = rt.seg[v + 1], n = rt.seg[v + 2] - seg0;
@@ -353,13 +414,17 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
     float* fl = sh.flush[warp];
 #pragma unroll
     for (int r = 0; r < L; ++r) {
-        fl[g * 8 + 2 * q] = acc[r][0];
-        fl[g * 8 + 2 * q + 1] = acc[r][1];
-        fl[(g + 8) * 8 + 2 * q] = acc[r][2];
-        fl[(g + 8) * 8 + 2 * q + 1] = acc[r][3];
+        if constexpr (NS == 2) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[r][0][e] += acc[r][1][e];
+        }
+        fl[g * 8 + 2 * q] = acc[r][0][0];
+        fl[g * 8 + 2 * q + 1] = acc[r][0][1];
+        fl[(g + 8) * 8 + 2 * q] = acc[r][0][2];
+        fl[(g + 8) * 8 + 2 * q + 1] = acc[r][0][3];
         __syncwarp();
-        const int lo = seg0 + 8 * r;
-        const int hi = seg0 + (8 * r + 8 < n ? 8 * r + 8 : n);
+        const int lo = seg0 + 8 * (t0 + r);
+        const int hi = seg0 + (8 * (t0 + r) + 8 < n ? 8 * (t0 + r) + 8 : n);
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             if (8 * j + 8 <= lo || 8 * j >= hi) continue;  // warp-uniform
@@ -378,58 +443,52 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
 }
 
 template <int NT>
-__device__ __forceinline__ bool run_variant(int len, MultiShared& sh, const MultiParams& p, uint8_t* ring,
-                                            int stage_bytes, int slot, int n_chunks, int& i_stage,
-                                            float (&acc_b)[NT][4], int warp, int g, int q, int64_t row0)
+__device__ __forceinline__ bool run_phase(int L, MultiShared& sh, const MultiParams& p, const uint8_t* vring, int slot,
+                                          int t0, int n_chunks, int& i_stage, float (&acc_b)[NT][4], int warp, int g,
+                                          int q, int64_t row0)
 {
-    switch (len) {
-        case 1: return variant_phase<NT, 1>(sh, p, ring, stage_bytes, slot, n_chunks, i_stage, acc_b, warp, g, q, row0);
+    switch (L) {
+        case 1: return variant_phase<NT, 1>(sh, p, vring, slot, t0, n_chunks, i_stage, acc_b, warp, g, q, row0);
         case 2:
             if constexpr (NT >= 2)
-                return variant_phase<NT, 2>(sh, p, ring, stage_bytes, slot, n_chunks, i_stage, acc_b, warp, g, q, row0);
+                return variant_phase<NT, 2>(sh, p, vring, slot, t0, n_chunks, i_stage, acc_b, warp, g, q, row0);
             break;
         case 3:
             if constexpr (NT >= 4)
-                return variant_phase<NT, 3>(sh, p, ring, stage_bytes, slot, n_chunks, i_stage, acc_b, warp, g, q, row0);
+                return variant_phase<NT, 3>(sh, p, vring, slot, t0, n_chunks, i_stage, acc_b, warp, g, q, row0);
             break;
         case 4:
             if constexpr (NT >= 4)
-                return variant_phase<NT, 4>(sh, p, ring, stage_bytes, slot, n_chunks, i_stage, acc_b, warp, g, q, row0);
-            break;
-        case 5:
-            if constexpr (NT >= 8)
-                return variant_phase<NT, 5>(sh, p, ring, stage_bytes, slot, n_chunks, i_stage, acc_b, warp, g, q, row0);
-            break;
-        case 6:
-            if constexpr (NT >= 8)
-                return variant_phase<NT, 6>(sh, p, ring, stage_bytes, slot, n_chunks, i_stage, acc_b, warp, g, q, row0);
-            break;
-        case 7:
-            if constexpr (NT >= 8)
-                return variant_phase<NT, 7>(sh, p, ring, stage_bytes, slot, n_chunks, i_stage, acc_b, warp, g, q, row0);
-            break;
-        case 8:
-            if constexpr (NT >= 8)
-                return variant_phase<NT, 8>(sh, p, ring, stage_bytes, slot, n_chunks, i_stage, acc_b, warp, g, q, row0);
+                return variant_phase<NT, 4>(sh, p, vring, slot, t0, n_chunks, i_stage, acc_b, warp, g, q, row0);
             break;
         default: break;
     }
-    // unreachable: a variant never holds more padded tiles than the group has token tiles
+    // unreachable: a phase never holds more tiles than the group has token tiles
     sh.abort = 1;
     raise_error(p.err, kErrTimeout);
     return false;
 }
 
+// Single-thread bounded wait (sets the CTA abort flag and the error word on timeout).
+__device__ __forceinline__ bool wait1(MultiShared& sh, uint64_t* bar, uint32_t parity, uint32_t* err)
+{
+    return wait_or_abort(sh, bar, parity, err);
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constant__ MultiParams p)
 {
-    constexpr int Tpad = 8 * NT;
-    constexpr int kXHalf = Tpad * kHalfRowBytes;
-    constexpr int kStageBytes = (base_stage_bytes(NT) + 1023) & ~1023;
+    constexpr int Tpad = 8 * NT;                    // accumulator columns (sorted token positions)
+    constexpr int Npad = Tpad < 16 ? 16 : Tpad;     // tcgen05 N (M = 128 needs N % 16 == 0)
+    constexpr int kXTile = Npad * kHalfRowBytes;    // x box [Npad tokens x 64 columns]
+    constexpr int kBaseStage = kWTile + kXTile;
+    constexpr int kRedStride = Tpad + 1;            // odd: conflict-free column walks
+    constexpr uint32_t kIdesc = idesc_bf16_f32(kRows, Npad);
 
     extern __shared__ uint8_t dyn_raw[];
     __shared__ MultiShared sh;
-    uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
+    uint8_t* bring = align1024(dyn_raw);            // base ring (1024-byte aligned stages)
+    uint8_t* vring = bring + kBaseStages * kBaseStage;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -443,21 +502,23 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
 
     route_group(sh.rt, p.vid, T, p.V, p.err, tid);
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], kConsumers);
+        for (int s = 0; s < kVarStages; ++s) {
+            mbar_init(&sh.full_v[s], 1);
+            mbar_init(&sh.empty_v[s], kConsumers);
         }
+        for (int s = 0; s < kBaseStages; ++s) {
+            mbar_init(&sh.full_b[s], 1);
+            mbar_init(&sh.empty_b[s], 1);
+        }
+        mbar_init(&sh.accum, 1);
         sh.abort = 0;
         fence_mbarrier_init();
     }
-    if (tid < sh.rt.n_act) {
-        // chunks per variant stage: as many as fit one ring slot (at most 8)
-        const int per_chunk = kSignChunk + sh.rt.len[tid] * kPadTile;
-        int grp = kMaxGroup;
-        while (grp > 1 && grp * per_chunk > kStageBytes) grp >>= 1;
-        sh.grp[tid] = grp;
-    }
+    if (warp == kBaseWarp) tmem_alloc(&sh.tmem_base, kTmemCols);
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh.tmem_base;
 
     const int n_act = sh.rt.n_act;
     const int nc = static_cast<int>(p.d_in / kChunk);
@@ -471,120 +532,142 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc_b[j][e] = 0.0f;
 
-    if (warp == kConsumers) {
-        // ------------------------------------------------------------ producer warp
+    if (warp == kBaseWarp) {
+        // ------------------------------------------------------------ base phase (one thread)
+        // x . W_base^T on the tensor cores, concurrently with the variant
+        // phases: 64-column stages of W_base [128 x 64] and x [Npad x 64],
+        // tcgen05.mma M = 128, N = Npad, K = 16, fp32 accumulator in tensor
+        // memory; a stage is refilled once the MMAs reading it completed.
+        if (lane == 0) {
+            const int nk = 2 * n_chunks;
+            int issued = 0, done = 0;
+            auto issue = [&](int k) {
+                const int s = k % kBaseStages;
+                uint8_t* st = bring + static_cast<size_t>(s) * kBaseStage;
+                const int col = c_begin * kChunk + 64 * k;
+                mbar_arrive_expect_tx(&sh.full_b[s], static_cast<uint32_t>(kBaseStage));
+                tma_load_2d(st, &p.w_map, col, static_cast<int>(row0), &sh.full_b[s]);
+                tma_load_2d(st + kWTile, &p.x_map, col, 0, &sh.full_b[s]);
+            };
+            for (; issued < (nk < kBaseStages ? nk : kBaseStages); ++issued) issue(issued);
+            for (int k = 0; k < nk; ++k) {
+                const int s = k % kBaseStages;
+                if (!wait1(sh, &sh.full_b[s], static_cast<uint32_t>(k / kBaseStages) & 1u, p.err)) break;
+                tc_fence_after();
+                const uint8_t* st = bring + static_cast<size_t>(s) * kBaseStage;
+                const uint64_t adesc = smem_desc_sw128(smem_u32(st));
+                const uint64_t bdesc = smem_desc_sw128(smem_u32(st + kWTile));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tmem, adesc + static_cast<uint64_t>(2 * kk), bdesc + static_cast<uint64_t>(2 * kk), kIdesc,
+                           (k | kk) != 0 ? 1u : 0u);
+                mma_commit(&sh.empty_b[s]);
+                ++done;
+                // refill the slot of the previous stage once its MMAs are done
+                if (k >= 1 && issued < nk) {
+                    const int sp = (k - 1) % kBaseStages;
+                    if (!wait1(sh, &sh.empty_b[sp], static_cast<uint32_t>((k - 1) / kBaseStages) & 1u, p.err)) break;
+                    issue(issued++);
+                }
+            }
+            mma_commit(&sh.accum);  // fires once every MMA issued above has completed
+            // copies still in flight must land before the CTA reuses the memory
+            for (int k = done; k < issued; ++k) {
+                const int s = k % kBaseStages;
+                const uint32_t par = static_cast<uint32_t>(k / kBaseStages) & 1u;
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&sh.full_b[s], par) && global_timer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == kVarProducerWarp) {
+        // ------------------------------------------------------------ variant-phase producer
         int i = 0;
         bool ok = true;
-        auto acquire = [&](int& s) -> bool {
-            s = i % kStages;
-            if (i >= kStages &&
-                !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty[s], static_cast<uint32_t>(i / kStages - 1) & 1u,
-                                                       p.err)))
-                return false;
-            return true;
-        };
-        for (int c = 0; c < n_chunks && ok; ++c) {
-            int s;
-            if (!(ok = acquire(s))) break;
-            uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
-            const int col = (c_begin + c) * kChunk;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&sh.full[s], static_cast<uint32_t>(2 * kWHalf + 2 * kXHalf));
-                tma_load_2d(st, &p.w_map, col, static_cast<int>(row0), &sh.full[s]);
-                tma_load_2d(st + kWHalf, &p.w_map, col + 64, static_cast<int>(row0), &sh.full[s]);
-                tma_load_2d(st + 2 * kWHalf, &p.x_map, col, 0, &sh.full[s]);
-                tma_load_2d(st + 2 * kWHalf + kXHalf, &p.x_map, col + 64, 0, &sh.full[s]);
-            }
-            __syncwarp();
-            ++i;
-        }
         for (int a = 0; a < n_act && ok; ++a) {
-            const int v = sh.rt.act[a], len = sh.rt.len[a], grp = sh.grp[a];
+            const int v = sh.rt.act[a], len = sh.rt.len[a];
             const uint8_t* src = p.xp + static_cast<int64_t>(sh.rt.ptile[a]) * nc * kPadTile;
-            for (int c0 = 0; c0 < n_chunks; c0 += grp) {
-                const int cnt = n_chunks - c0 < grp ? n_chunks - c0 : grp;
-                int s;
-                if (!(ok = acquire(s))) break;
-                uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
-                if (lane == 0) {
-                    const uint32_t pad_bytes = static_cast<uint32_t>(cnt * len * kPadTile);
-                    mbar_arrive_expect_tx(&sh.full[s], static_cast<uint32_t>(cnt * kSignChunk) + pad_bytes);
-                    for (int cc = 0; cc < cnt; ++cc)
-                        tma_load_2d(st + cc * kSignChunk, &p.sign_map[v], (c_begin + c0 + cc) * 4,
-                                    static_cast<int>(row0), &sh.full[s]);
-                    bulk_g2s(st + cnt * kSignChunk, src + static_cast<int64_t>(c_begin + c0) * len * kPadTile,
-                             pad_bytes, &sh.full[s]);
+            for (int t0 = 0; t0 < len && ok; t0 += kPhaseTiles) {
+                const int L = len - t0 < kPhaseTiles ? len - t0 : kPhaseTiles;
+                const int grp = phase_group(L);
+                for (int c0 = 0; c0 < n_chunks; c0 += grp) {
+                    const int cnt = n_chunks - c0 < grp ? n_chunks - c0 : grp;
+                    const int s = i % kVarStages;
+                    if (i >= kVarStages &&
+                        !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty_v[s],
+                                                               static_cast<uint32_t>(i / kVarStages - 1) & 1u, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = vring + static_cast<size_t>(s) * kVarSlot;
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(&sh.full_v[s], static_cast<uint32_t>(cnt * (kSignChunk + L * kPadTile)));
+                        for (int cc = 0; cc < cnt; ++cc) {
+                            const int c = c_begin + c0 + cc;
+                            tma_load_2d(st + cc * kSignChunk, &p.sign_map[v], 4 * c, static_cast<int>(row0),
+                                        &sh.full_v[s]);
+                            bulk_g2s(st + cnt * kSignChunk + cc * L * kPadTile,
+                                     src + (static_cast<int64_t>(c) * len + t0) * kPadTile,
+                                     static_cast<uint32_t>(L * kPadTile), &sh.full_v[s]);
+                        }
+                    }
+                    __syncwarp();
+                    ++i;
                 }
-                __syncwarp();
-                ++i;
             }
         }
         // every issued stage must have landed before the CTA reuses the memory
-        for (int k = (i > kStages ? i - kStages : 0); k < i; ++k) {
-            const int s = k % kStages;
-            const uint32_t par = static_cast<uint32_t>(k / kStages) & 1u;
+        for (int k = (i > kVarStages ? i - kVarStages : 0); k < i; ++k) {
+            const int s = k % kVarStages;
+            const uint32_t par = static_cast<uint32_t>(k / kVarStages) & 1u;
             const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(&sh.full[s], par) && global_timer_ns() - t0 < kWaitLimitNs) {
+            while (!mbar_try_wait(&sh.full_v[s], par) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
     } else {
-        // ------------------------------------------------------------ consumer warps
-        const int rl0 = 16 * warp + g;  // local rows rl0 and rl0 + 8 (both = g mod 8)
-        const int c0 = ((2 * q) ^ g) << 4, c1 = ((2 * q + 1) ^ g) << 4;  // swizzled chunk offsets
+        // ------------------------------------------------------------ consumer warps: variant phases
         int i = 0;
         bool ok = true;
-        for (int c = 0; c < n_chunks; ++c) {
-            const int s = i % kStages;
-            if (!__all_sync(0xffffffffu,
-                            wait_or_abort(sh, &sh.full[s], static_cast<uint32_t>(i / kStages) & 1u, p.err))) {
-                ok = false;
-                break;
+        for (int a = 0; a < n_act && ok; ++a) {
+            const int len = sh.rt.len[a];
+            for (int t0 = 0; t0 < len && ok; t0 += kPhaseTiles) {
+                const int L = len - t0 < kPhaseTiles ? len - t0 : kPhaseTiles;
+                ok = run_phase<NT>(L, sh, p, vring, a, t0, n_chunks, i, acc_b, warp, g, q, row0);
             }
-            const uint8_t* st = ring + static_cast<size_t>(s) * kStageBytes;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint8_t* wst = st + h * kWHalf;
-                const uint8_t* xst = st + 2 * kWHalf + h * kXHalf;
-                uint32_t W0[8], W1[8];
-                {
-                    const uint8_t* r0p = wst + rl0 * kHalfRowBytes;
-                    const uint8_t* r1p = wst + (rl0 + 8) * kHalfRowBytes;
-                    const uint4 u0 = *reinterpret_cast<const uint4*>(r0p + c0);
-                    const uint4 u1 = *reinterpret_cast<const uint4*>(r0p + c1);
-                    const uint4 v0 = *reinterpret_cast<const uint4*>(r1p + c0);
-                    const uint4 v1 = *reinterpret_cast<const uint4*>(r1p + c1);
-                    W0[0] = u0.x; W0[1] = u0.y; W0[2] = u0.z; W0[3] = u0.w;
-                    W0[4] = u1.x; W0[5] = u1.y; W0[6] = u1.z; W0[7] = u1.w;
-                    W1[0] = v0.x; W1[1] = v0.y; W1[2] = v0.z; W1[3] = v0.w;
-                    W1[4] = v1.x; W1[5] = v1.y; W1[6] = v1.z; W1[7] = v1.w;
-                }
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
-                    mma4(acc_b[j], W0, W1, *reinterpret_cast<const uint4*>(xr + c0),
-                         *reinterpret_cast<const uint4*>(xr + c1));
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[s]);
-            ++i;
         }
-        for (int a = 0; a < n_act && ok; ++a)
-            ok = run_variant<NT>(sh.rt.len[a], sh, p, ring, kStageBytes, a, n_chunks, i, acc_b, warp, g, q, row0);
     }
 
-    // ---------------------------------------------------------------- cluster K reduction
-    __syncthreads();  // pipeline drained: the ring becomes the reduction buffer
-    float* red = reinterpret_cast<float*>(ring);
+    // ---------------------------------------------------------------- epilogue
+    // per-token sums of this CTA's slice: variant parts (registers of the
+    // consumer warps) + base part (tensor memory), then the cluster K reduction
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(bring);  // the base ring is free once every base MMA is done
+    bool base_ok = true;
     if (warp < kConsumers) {
+        base_ok = __all_sync(0xffffffffu, wait_or_abort(sh, &sh.accum, 0u, p.err));
+        tc_fence_after();
         const int r0 = 16 * warp + g;
 #pragma unroll
         for (int j = 0; j < NT; ++j) {
             const int pos = 8 * j + 2 * q;
-            red[r0 * Tpad + pos] = acc_b[j][0];
-            red[r0 * Tpad + pos + 1] = acc_b[j][1];
-            red[(r0 + 8) * Tpad + pos] = acc_b[j][2];
-            red[(r0 + 8) * Tpad + pos + 1] = acc_b[j][3];
+            red[r0 * kRedStride + pos] = acc_b[j][0];
+            red[r0 * kRedStride + pos + 1] = acc_b[j][1];
+            red[(r0 + 8) * kRedStride + pos] = acc_b[j][2];
+            red[(r0 + 8) * kRedStride + pos + 1] = acc_b[j][3];
+        }
+    }
+    __syncthreads();
+    if (warp < 4 && base_ok) {
+        tc_fence_after();
+        const int row = 32 * warp + lane;  // tensor-memory lane = local row
+#pragma unroll
+        for (int cb = 0; cb < (Tpad + 31) / 32; ++cb) {
+            uint32_t d[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * cb, d);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (32 * cb + j < Tpad) red[row * kRedStride + 32 * cb + j] += __uint_as_float(d[j]);
         }
     }
     cluster.sync();
@@ -595,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
         const int pos = o / nr, r = r_lo + o % nr;
         if (r >= valid_rows) continue;
         float y = 0.0f;
-        for (int k = 0; k < CK; ++k) y += cluster.map_shared_rank(red, k)[r * Tpad + pos];
+        for (int k = 0; k < CK; ++k) y += cluster.map_shared_rank(red, k)[r * kRedStride + pos];
         const int key = rt.keyp[pos];
         const int64_t row = row0 + r;
         if (key >= 1) y = fmaf(-p.alpha[key - 1][p.per_row ? row : 0], p.corr[pos], y);
@@ -606,6 +689,12 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
             static_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(y);
     }
     cluster.sync();  // peers may still read this CTA's partials until here
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kBaseWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
 }
 
 template <int NT>
@@ -646,6 +735,7 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
     if (T < 1 || T > kMaxTok || a.V < 1 || a.V > kMaxVariants) return cudaErrorInvalidValue;
     if (!a.x_sorted || !a.xp || !a.corr) return cudaErrorInvalidValue;
     const int nt = tiles_for(T);
+    const int npad = 8 * nt < 16 ? 16 : 8 * nt;
     static thread_local MultiParams prm;  // ~9 KB: kept off the stack
     prm.xp = a.xp;
     prm.corr = a.corr;
@@ -671,17 +761,17 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
                        static_cast<uint32_t>(kRows), CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x_sorted, static_cast<uint64_t>(a.d_in),
                        static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, 64,
-                       static_cast<uint32_t>(8 * nt), CU_TENSOR_MAP_SWIZZLE_128B))
+                       static_cast<uint32_t>(npad), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     // K slices per cluster: a function of d_in only (one per 2048 columns, at most 4)
     const int nc = static_cast<int>(a.d_in / kChunk);
     int ck = nc / 16;
     ck = ck < 1 ? 1 : ck > 4 ? 4 : ck;
     prm.CK = ck;
-    const size_t stage = static_cast<size_t>((base_stage_bytes(nt) + 1023) & ~1023);
-    const size_t red = static_cast<size_t>(kRows) * (8 * nt) * sizeof(float);
-    size_t smem = kStages * stage;
-    smem = (smem > red ? smem : red) + 1024;
+    const size_t base_stage = static_cast<size_t>(kWTile) + static_cast<size_t>(npad) * kHalfRowBytes;
+    const size_t red = static_cast<size_t>(kRows) * (8 * nt + 1) * sizeof(float);
+    if (red > kBaseStages * base_stage) return cudaErrorInvalidConfiguration;
+    const size_t smem = kBaseStages * base_stage + kVarStages * static_cast<size_t>(kVarSlot) + 1024;
 
     const int prep_blocks = T + 7 * (T < a.V ? T : a.V);
     multi_prepare_kernel<<<prep_blocks, 256, 0, stream>>>(a.x, a.vid, T, a.V, a.d_in, a.x_sorted, a.xp, a.corr);
