@@ -60,9 +60,9 @@ constexpr int kThreads = 32 * (kConsumers + 2);
 constexpr int kChunk = 128;                   // d_in columns per chunk
 constexpr int kHalfRowBytes = 128;            // 64 bf16 columns: one 128-byte swizzle atom
 constexpr int kWTile = kRows * kHalfRowBytes; // W_base box [128 rows x 64 columns] = 16 KB
-constexpr int kBaseStages = 3;
+constexpr int kBaseStages = 2;
 constexpr int kVarStages = 2;
-constexpr int kVarSlot = 16 * 1024;
+constexpr int kVarSlot = 14 * 1024;
 constexpr int kSignChunk = kRows * 16;        // 4 sign words x 128 rows = 2 KB
 constexpr int kPadTile = 8 * kChunk * 2;      // one 8-token tile of one chunk = 2 KB
 constexpr int kMaxTok = kSkinnyMaxTokens;
@@ -105,6 +105,10 @@ struct MultiParams {
     uint32_t* err;
     int64_t T, d_out, d_in;
     int V, per_row, out_f32, CK;
+    // kRecodeConst, passed at run time so that it sits in a register and each
+    // operand pair is a single three-input logic op (mask immediate, constant
+    // register) instead of two ops with two immediates
+    uint32_t recode_const;
 };
 
 // Result of the per-CTA router (identical in every CTA and in the prepare pass).
@@ -133,7 +137,6 @@ struct MultiShared {
     uint32_t tmem_base;
     volatile int abort;
     Routing rt;
-    float flush[kConsumers][16 * 8];
 };
 
 // Stable counting sort of the T (<= 64) tokens by key = vid + 1 (ids outside
@@ -346,13 +349,14 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p)
 
 // Consumer side of one variant phase over L padded tiles (tiles t0 ..
 // t0 + L - 1 of the variant in slot `slot`): the sign MMAs over the CTA's
-// d_in slice, then alpha * 2M added into the per-token accumulators.
-// Returns false when the pipeline was aborted.  i_stage is the running
-// variant-stage counter shared with the producer's schedule.
-template <int NT, int L>
+// d_in slice, then alpha * 2M of each of the phase's tokens stored into the
+// per-token sums `red` (row stride rs; every (row, token) is written by
+// exactly one phase).  Returns false when the pipeline was aborted.  i_stage
+// is the running variant-stage counter shared with the producer's schedule.
+template <int L>
 __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams& p, const uint8_t* vring, int slot,
-                                              int t0, int n_chunks, int& i_stage, float (&acc_b)[NT][4], int warp,
-                                              int g, int q, int64_t row0)
+                                              int t0, int n_chunks, int& i_stage, float* red, int rs, int warp, int g,
+                                              int q, int64_t row0)
 {
     constexpr int grp = phase_group(L);
     // Variants with one or two tiles keep two accumulator sets (even and odd
@@ -366,6 +370,7 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[r][h][e] = 0.0f;
     const int rl0 = 16 * warp + g;
+    const uint32_t rc = p.recode_const;
     bool ok = true;
     for (int c0 = 0; c0 < n_chunks; c0 += grp) {
         const int cnt = n_chunks - c0 < grp ? n_chunks - c0 : grp;
@@ -387,8 +392,8 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
                 uint32_t a0[4], a1[4];
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    a0[k] = (u0 & recode_mask(k)) ^ kRecodeConst;
-                    a1[k] = (u1 & recode_mask(k)) ^ kRecodeConst;
+                    a0[k] = (u0 & recode_mask(k)) ^ rc;
+                    a1[k] = (u1 & recode_mask(k)) ^ rc;
                 }
 #pragma unroll
                 for (int r = 0; r < L; ++r) {
@@ -403,63 +408,48 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
         ++i_stage;
     }
     if (!ok) return false;
-    // alpha * 2M into the accumulators of the variant's tokens
+    // alpha * 2M of the phase's tokens (sorted positions seg0 + 8 t0 ..)
     const Routing& rt = sh.rt;
     const int v = rt.act[slot];
-    const int seg0 = rt.seg[v + 1], n = rt.seg[v + 2] - seg0;
+    const int seg0 = rt.seg[v + 1], end = rt.seg[v + 2];
     const int64_t ra = row0 + rl0, rb = ra + 8;
     const float* al = p.alpha[v];
     const float a2a = ra < p.d_out ? 2.0f * al[p.per_row ? ra : 0] : 0.0f;
     const float a2b = rb < p.d_out ? 2.0f * al[p.per_row ? rb : 0] : 0.0f;
-    float* fl = sh.flush[warp];
 #pragma unroll
     for (int r = 0; r < L; ++r) {
-        if constexpr (NS == 2) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[r][0][e] += acc[r][1][e];
-        }
-        fl[g * 8 + 2 * q] = acc[r][0][0];
-        fl[g * 8 + 2 * q + 1] = acc[r][0][1];
-        fl[(g + 8) * 8 + 2 * q] = acc[r][0][2];
-        fl[(g + 8) * 8 + 2 * q + 1] = acc[r][0][3];
-        __syncwarp();
-        const int lo = seg0 + 8 * (t0 + r);
-        const int hi = seg0 + (8 * (t0 + r) + 8 < n ? 8 * (t0 + r) + 8 : n);
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            if (8 * j + 8 <= lo || 8 * j >= hi) continue;  // warp-uniform
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int d = 8 * j + 2 * q + e;
-                if (d >= lo && d < hi) {
-                    acc_b[j][e] = fmaf(a2a, fl[g * 8 + (d - lo)], acc_b[j][e]);
-                    acc_b[j][2 + e] = fmaf(a2b, fl[(g + 8) * 8 + (d - lo)], acc_b[j][2 + e]);
-                }
+        for (int e = 0; e < 2; ++e) {
+            const int pos = seg0 + 8 * (t0 + r) + 2 * q + e;
+            if (pos < end) {
+                const float m0 = NS == 2 ? acc[r][0][e] + acc[r][NS - 1][e] : acc[r][0][e];
+                const float m1 = NS == 2 ? acc[r][0][2 + e] + acc[r][NS - 1][2 + e] : acc[r][0][2 + e];
+                red[rl0 * rs + pos] = a2a * m0;
+                red[(rl0 + 8) * rs + pos] = a2b * m1;
             }
         }
-        __syncwarp();
     }
     return true;
 }
 
 template <int NT>
 __device__ __forceinline__ bool run_phase(int L, MultiShared& sh, const MultiParams& p, const uint8_t* vring, int slot,
-                                          int t0, int n_chunks, int& i_stage, float (&acc_b)[NT][4], int warp, int g,
+                                          int t0, int n_chunks, int& i_stage, float* red, int rs, int warp, int g,
                                           int q, int64_t row0)
 {
     switch (L) {
-        case 1: return variant_phase<NT, 1>(sh, p, vring, slot, t0, n_chunks, i_stage, acc_b, warp, g, q, row0);
+        case 1: return variant_phase<1>(sh, p, vring, slot, t0, n_chunks, i_stage, red, rs, warp, g, q, row0);
         case 2:
             if constexpr (NT >= 2)
-                return variant_phase<NT, 2>(sh, p, vring, slot, t0, n_chunks, i_stage, acc_b, warp, g, q, row0);
+                return variant_phase<2>(sh, p, vring, slot, t0, n_chunks, i_stage, red, rs, warp, g, q, row0);
             break;
         case 3:
             if constexpr (NT >= 4)
-                return variant_phase<NT, 3>(sh, p, vring, slot, t0, n_chunks, i_stage, acc_b, warp, g, q, row0);
+                return variant_phase<3>(sh, p, vring, slot, t0, n_chunks, i_stage, red, rs, warp, g, q, row0);
             break;
         case 4:
             if constexpr (NT >= 4)
-                return variant_phase<NT, 4>(sh, p, vring, slot, t0, n_chunks, i_stage, acc_b, warp, g, q, row0);
+                return variant_phase<4>(sh, p, vring, slot, t0, n_chunks, i_stage, red, rs, warp, g, q, row0);
             break;
         default: break;
     }
@@ -489,6 +479,8 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     __shared__ MultiShared sh;
     uint8_t* bring = align1024(dyn_raw);            // base ring (1024-byte aligned stages)
     uint8_t* vring = bring + kBaseStages * kBaseStage;
+    float* red = reinterpret_cast<float*>(vring + kVarStages * kVarSlot);  // per-token sums [128][Tpad + 1]
+    for (int o = threadIdx.x; o < kRows * kRedStride; o += kThreads) red[o] = 0.0f;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -525,12 +517,6 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     const int c_begin = static_cast<int>(static_cast<int64_t>(rank) * nc / CK);
     const int c_end = static_cast<int>(static_cast<int64_t>(rank + 1) * nc / CK);
     const int n_chunks = c_end - c_begin;
-
-    float acc_b[NT][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc_b[j][e] = 0.0f;
 
     if (warp == kBaseWarp) {
         // ------------------------------------------------------------ base phase (one thread)
@@ -633,41 +619,28 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
             const int len = sh.rt.len[a];
             for (int t0 = 0; t0 < len && ok; t0 += kPhaseTiles) {
                 const int L = len - t0 < kPhaseTiles ? len - t0 : kPhaseTiles;
-                ok = run_phase<NT>(L, sh, p, vring, a, t0, n_chunks, i, acc_b, warp, g, q, row0);
+                ok = run_phase<NT>(L, sh, p, vring, a, t0, n_chunks, i, red, kRedStride, warp, g, q, row0);
             }
         }
     }
 
     // ---------------------------------------------------------------- epilogue
-    // per-token sums of this CTA's slice: variant parts (registers of the
-    // consumer warps) + base part (tensor memory), then the cluster K reduction
+    // per-token sums of this CTA's slice: variant parts (already in red) +
+    // base part (tensor memory), then the cluster K reduction
     __syncthreads();
-    float* red = reinterpret_cast<float*>(bring);  // the base ring is free once every base MMA is done
-    bool base_ok = true;
-    if (warp < kConsumers) {
-        base_ok = __all_sync(0xffffffffu, wait_or_abort(sh, &sh.accum, 0u, p.err));
+    if (warp < 4) {
+        const bool base_ok = __all_sync(0xffffffffu, wait_or_abort(sh, &sh.accum, 0u, p.err));
         tc_fence_after();
-        const int r0 = 16 * warp + g;
+        if (base_ok) {
+            const int row = 32 * warp + lane;  // tensor-memory lane = local row
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int pos = 8 * j + 2 * q;
-            red[r0 * kRedStride + pos] = acc_b[j][0];
-            red[r0 * kRedStride + pos + 1] = acc_b[j][1];
-            red[(r0 + 8) * kRedStride + pos] = acc_b[j][2];
-            red[(r0 + 8) * kRedStride + pos + 1] = acc_b[j][3];
-        }
-    }
-    __syncthreads();
-    if (warp < 4 && base_ok) {
-        tc_fence_after();
-        const int row = 32 * warp + lane;  // tensor-memory lane = local row
+            for (int cb = 0; cb < (Tpad + 31) / 32; ++cb) {
+                uint32_t d[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * cb, d);
 #pragma unroll
-        for (int cb = 0; cb < (Tpad + 31) / 32; ++cb) {
-            uint32_t d[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * cb, d);
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-                if (32 * cb + j < Tpad) red[row * kRedStride + 32 * cb + j] += __uint_as_float(d[j]);
+                for (int j = 0; j < 32; ++j)
+                    if (32 * cb + j < Tpad) red[row * kRedStride + 32 * cb + j] += __uint_as_float(d[j]);
+            }
         }
     }
     cluster.sync();
@@ -748,6 +721,7 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
     prm.V = a.V;
     prm.per_row = a.per_row;
     prm.out_f32 = a.out_f32;
+    prm.recode_const = kRecodeConst;
     for (int v = 0; v < a.V; ++v) {
         prm.alpha[v] = a.alpha[v];
         if (!encode_tma_2d(&prm.sign_map[v], CU_TENSOR_MAP_DATA_TYPE_UINT32, a.signs[v],
@@ -770,8 +744,7 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
     prm.CK = ck;
     const size_t base_stage = static_cast<size_t>(kWTile) + static_cast<size_t>(npad) * kHalfRowBytes;
     const size_t red = static_cast<size_t>(kRows) * (8 * nt + 1) * sizeof(float);
-    if (red > kBaseStages * base_stage) return cudaErrorInvalidConfiguration;
-    const size_t smem = kBaseStages * base_stage + kVarStages * static_cast<size_t>(kVarSlot) + 1024;
+    const size_t smem = kBaseStages * base_stage + kVarStages * static_cast<size_t>(kVarSlot) + red + 1024;
 
     const int prep_blocks = T + 7 * (T < a.V ? T : a.V);
     multi_prepare_kernel<<<prep_blocks, 256, 0, stream>>>(a.x, a.vid, T, a.V, a.d_in, a.x_sorted, a.xp, a.corr);

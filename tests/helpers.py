@@ -11,7 +11,10 @@ accumulation in any order keeps the error under (n + 4) * 2^-24 times that
 sum when every addition rounds to nearest; the factor 4 of slack covers
 tensor-core accumulators that truncate instead of rounding.  The prefill path
 (T > 64) rounds W_eff to bf16 before its contraction, which adds up to
-2^-9 * |x_j| * (|w_j| + alpha) per term to that bound.
+2^-9 * |x_j| * (|w_j| + alpha) per term to that bound.  The multi-variant
+kernel computes sum_j x_j s_j as 2 sum_j x_j v_j - C with |v_j| <= 9 and
+|C| <= 17 sum_j |x_j| (an exact recoding of the sign operand), so its bound
+weighs alpha by 2 * 9 + 1 = 19 instead of 1 (20 with rounding slack).
 """
 from __future__ import annotations
 
@@ -85,3 +88,18 @@ def fp32_bound(x_bits, wb_bits, alpha, per_row: bool, rows=None, weff_bf16: bool
     s = x @ w.T + x.sum(axis=1)[:, None] * a[None, :]
     n = wb.shape[1]
     return ((n + 4) * 2.0 ** -22 + (2.0 ** -9 if weff_bf16 else 0.0)) * s + 1e-30
+
+
+def fp32_bound_multi(x_bits, wb_bits, alphas, vid, rows, sign_weight: float = 20.0) -> np.ndarray:
+    """Per-token form of fp32_bound for the multi-variant kernel:
+    (n + 4) * 2^-22 * sum_j |x_j| (|w_j| + sign_weight * alpha_v(t)), alpha_v of
+    the token's variant (0 for base-model tokens); alphas[v] holds the
+    per-row alpha of the listed rows."""
+    x = np.abs(synth.bf16_bits_to_f32(x_bits).astype(np.float64))
+    w = np.abs(synth.bf16_bits_to_f32(wb_bits[rows]).astype(np.float64))
+    a = np.zeros((x.shape[0], len(rows)))
+    for t, v in enumerate(np.asarray(vid)):
+        if 0 <= v < len(alphas):
+            a[t] = np.asarray(alphas[v], np.float64)
+    s = x @ w.T + sign_weight * x.sum(axis=1)[:, None] * a
+    return (wb_bits.shape[1] + 4) * 2.0 ** -22 * s + 1e-30

@@ -17,7 +17,8 @@ import torch
 import oracle
 from bit_weight_delta_bd_gb300 import bitdelta as bd
 from bit_weight_delta_bd_gb300 import synth
-from helpers import PREFILL_MIN_T, bf16_half_ulp, check_linear, fp32_bound, to_dev, u32, y_host  # noqa: F401
+from helpers import (PREFILL_MIN_T, bf16_half_ulp, check_linear, fp32_bound, fp32_bound_multi,  # noqa: F401
+                     to_dev, u32, y_host)
 
 pytestmark = pytest.mark.gpu
 
@@ -284,7 +285,8 @@ def test_multi_tenant_sampled_rows(dev, multi_problem):
         ws = bd.new_workspace(bd.bd_linear_multi_workspace_size(64, 14, 8192, 8192), dev)
         bd.bd_linear_multi(x_d, vid_d, s_l, a_l, PR, wb_d, y, ws)
         assert bd.bd_check_async(ws) == bd.BD_OK
-        check_linear(y_host(y)[:, rows], y_ref, bf16_out=not f32, what=f"multi f32={f32}")
+        bound = fp32_bound_multi(x, wb, [r[1] for r in refs], vid, rows) if f32 else None
+        check_linear(y_host(y)[:, rows], y_ref, bf16_out=not f32, bound=bound, what=f"multi f32={f32}")
 
 
 def _dyadic_multi(seed, V, d_out, d_in, T):
