@@ -204,12 +204,12 @@ bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const 
 }
 
 // Multi-variant workspace for one group of up to 64 tokens: the error word,
-// then (at 1 KiB) x sorted by variant, the zero-padded per-variant x tiles of
-// the sign phases and the per-token corrections.
+// then (at 1 KiB) the zero-padded per-variant x tiles of the sign phases and
+// the per-token partial corrections.
 namespace {
 
 struct MultiWs {
-    size_t xs, xp, corr, total;
+    size_t xp, corr, total;
 };
 
 MultiWs multi_ws_layout(int64_t T, int32_t V, int64_t d_in)
@@ -217,11 +217,10 @@ MultiWs multi_ws_layout(int64_t T, int32_t V, int64_t d_in)
     const int64_t tg = T < bd::kSkinnyMaxTokens ? T : bd::kSkinnyMaxTokens;
     const auto up = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
     MultiWs w{};
-    w.xs = 1024;
-    w.xp = w.xs + up(static_cast<size_t>(tg) * static_cast<size_t>(d_in) * 2);
+    w.xp = 1024;
     const size_t ptiles = static_cast<size_t>(bd::multi_max_ptiles(static_cast<int>(tg), V));
     w.corr = w.xp + up(ptiles * 8 * static_cast<size_t>(d_in) * 2);
-    w.total = w.corr + up(static_cast<size_t>(tg) * 4);
+    w.total = w.corr + up(static_cast<size_t>(tg) * static_cast<size_t>(bd::multi_corr_splits(d_in)) * 4);
     return w;
 }
 
@@ -277,7 +276,6 @@ bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int3
         a.y = static_cast<char*>(y) + static_cast<size_t>(t0) * d_out * ysz;
         a.out_f32 = out_dtype == BD_OUT_F32;
         a.err = err_word(ws);
-        a.x_sorted = reinterpret_cast<uint16_t*>(static_cast<char*>(ws) + lay.xs);
         a.xp = reinterpret_cast<uint8_t*>(static_cast<char*>(ws) + lay.xp);
         a.corr = reinterpret_cast<float*>(static_cast<char*>(ws) + lay.corr);
         if (bd_status s = launched(bd::launch_multi(a, st))) return s;

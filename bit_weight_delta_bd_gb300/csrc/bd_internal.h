@@ -60,14 +60,16 @@ struct MultiArgs {
     void* y;                  // [T][d_out]
     int out_f32;
     uint32_t* err;
-    uint16_t* x_sorted;       // scratch [T][d_in]: x sorted by variant
     uint8_t* xp;              // scratch [multi_max_ptiles(T, V)][8][d_in] bf16: padded per-variant tiles
-    float* corr;              // scratch [T]: per-token correction of the recoded sign contraction
+    float* corr;              // scratch [T][multi_corr_splits(d_in)]: partial corrections of the recoded sign sums
 };
 
 // Upper bound of the zero-padded 8-token tiles of a group of T tokens over V
 // variants: sum over variants of ceil(n_v / 8) <= (T + 7 min(T, V)) / 8.
 int multi_max_ptiles(int T, int V);
+
+// Column splits of the prepare pass (partial corrections per token).
+int multi_corr_splits(int64_t d_in);
 
 cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream);
 

@@ -5,24 +5,30 @@
 //
 //   y[t][r] = sum_j x[t][j] W_base[r][j]  +  alpha_v(t)[r] * sum_j x[t][j] s_v(t)[r][j]
 //
-// Work split.  A CTA owns 128 output rows (8 consumer warps of 16 rows) and
-// one of CK equal slices of d_in; the CK CTAs of a thread-block cluster cover
-// d_in and sum their partial results through distributed shared memory in
-// rank order (CK depends on d_in only).  One producer thread streams stages
-// through a two-slot shared-memory ring (TMA, full/empty mbarriers, all waits
-// bounded).  The CTA runs its slice in phases:
-//   base phase     x . W_base^T for every token of the group: W_base boxes
-//                  [128 rows x 64 columns] and x boxes [8*NT tokens x 64],
-//                  both with the 128-byte swizzle, mma.sync m16n8k16 bf16;
-//   variant phases one per variant that has tokens: its sign words (boxes
-//                  [128 rows x 4 words]) against its own tokens only, which
-//                  the prepare pass has packed into zero-padded 8-token tiles
-//                  (plain bulk copies).  No MMA carries another variant's
-//                  token, so nothing is masked; each variant's bits are read
-//                  and expanded once per CTA.
-// W_base is read from device memory once per CTA for all variants.  At the end
-// of a variant phase the warp adds alpha * (its sign sums) into the per-token
-// accumulators of the base phase through a small per-warp shared buffer.
+// Two launches per group of tokens:
+//   multi_prepare_kernel  routes the tokens (stable counting sort by vid + 1)
+//                         and writes each variant's tokens into zero-padded
+//                         8-token tiles in the order and scaling of the
+//                         recoded sign operand (below), plus per-token
+//                         partial corrections C;
+//   multi_kernel          one CTA per 128 output rows and one of CK slices of
+//                         d_in (a thread-block cluster of CK CTAs covers d_in;
+//                         CK depends on d_in only), three roles running
+//                         concurrently:
+//     warp 9   base phase: x . W_base^T for every token on the tensor cores
+//              (W_base [128 x 64] and x [Npad x 64] TMA boxes, tcgen05.mma
+//              M = 128, N = Npad, K = 16, fp32 accumulator in tensor memory);
+//     warp 8   streams the variant phases: for each active variant, its sign
+//              words (TMA boxes [128 rows x 4 words]) and its padded x tiles;
+//     warps 0-7 run the variant phases: mma.sync m16n8k16 of each variant's
+//              recoded sign operand against its own tokens only (no masking),
+//              and store alpha * 2M per token into a shared per-token buffer.
+//   The epilogue adds the tensor-memory base sums, sums the cluster's slices
+//   (every CTA stores its partial sums into the owning peer's receive slots,
+//   then each owner adds its slots in rank order) and writes y = base +
+//   alpha * (2M - C) in the caller's token order.
+// W_base is read from device memory once per CTA for all variants; each
+// active variant's bits once.
 //
 // Sign operand recoding (exact).  Expanding 16 sign bits into eight bf16 +-1
 // pairs needs a shift and a mask per pair.  Here the sign contraction runs on
@@ -35,8 +41,8 @@
 // exactly.  A 32-bit sign word rotated by 0, 4, 8 and 12 bits puts every one
 // of its bits on such a place.  With s = 2b - 1:
 //   sum_j x_j s_j = 2 M - C,   M = sum_j x_j v_j,   C = sum_j x_j (2 a_j + 1),
-// where C depends on the token only and is computed once by the prepare pass
-// (fp64, rounded to fp32).  Every product is exact in fp32 (at most 12
+// where C depends on the token only (computed once by the prepare pass, fp32
+// partial sums in a fixed order).  Every product is exact in fp32 (at most 12
 // significant bits); M is accumulated in fp32 like the plain form.  The x
 // operand of the sign MMA is also permuted inside every 32-column group to
 // the order in which the rotated words deliver the bits; both operands use
@@ -53,7 +59,7 @@ namespace bd {
 namespace {
 
 constexpr int kConsumers = 8;                 // warps 0..7: variant phases, then the epilogue
-constexpr int kVarProducerWarp = kConsumers;  // warp 8: TMA of the variant phases
+constexpr int kProducerWarp = kConsumers;     // warp 8: TMA of the variant phases
 constexpr int kBaseWarp = kConsumers + 1;     // warp 9: tensor memory, base-phase TMA and tcgen05 MMAs
 constexpr int kRows = 16 * kConsumers;        // 128 output rows per CTA = tensor-memory lanes
 constexpr int kThreads = 32 * (kConsumers + 2);
@@ -70,10 +76,19 @@ constexpr int kMaxKeys = kMaxVariants + 1;
 constexpr int kPhaseTiles = 4;                // padded tiles per variant phase (more: several phases)
 constexpr int kTmemCols = 64;
 
-// Chunks per variant stage for a phase of L padded tiles.
+// ---- multi_prepare_kernel
+constexpr int kPrepThreads = 128;             // one task (chunk, 32-column group) per thread
+constexpr int kPrepChunks = kPrepThreads / 4; // chunks per prepare block (column split)
+
+// Chunks per variant stage for a phase of L padded tiles: the largest power
+// of two (at most 8) whose stage fits one ring slot, so that it divides the
+// chunk count of a slice in the common case and the chunk loop unrolls.
 __host__ __device__ constexpr int phase_group(int L)
 {
-    return kVarSlot / (kSignChunk + L * kPadTile) < 8 ? kVarSlot / (kSignChunk + L * kPadTile) : 8;
+    return kVarSlot >= 8 * (kSignChunk + L * kPadTile)   ? 8
+           : kVarSlot >= 4 * (kSignChunk + L * kPadTile) ? 4
+           : kVarSlot >= 2 * (kSignChunk + L * kPadTile) ? 2
+                                                           : 1;
 }
 
 // Recoding: kind k = column residue mod 4.  The operand pair of kind k is
@@ -91,27 +106,27 @@ __host__ __device__ constexpr uint32_t recode_mask(int k)
 __host__ __device__ constexpr int recode_lo_bit(int k) { return k == 0 ? 4 : k == 1 ? 5 : k == 2 ? 6 : 15; }
 __host__ __device__ constexpr float recode_sigma(int k) { return k == 0 ? -16.0f : k == 1 ? -8.0f : k == 2 ? -4.0f : 1.0f; }
 // 2 a_k + 1 for the per-token correction C.
-__host__ __device__ constexpr double recode_corr(int k) { return k == 0 ? 17.0 : k == 1 ? 9.0 : k == 2 ? 5.0 : 0.0; }
+__host__ __device__ constexpr float recode_corr(int k) { return k == 0 ? 17.0f : k == 1 ? 9.0f : k == 2 ? 5.0f : 0.0f; }
 
 struct MultiParams {
     CUtensorMap sign_map[kMaxVariants];  // [d_out][d_in/32] uint32, box 4 x 128 rows
     CUtensorMap w_map;                   // [d_out][d_in] bf16, box 64 x 128 rows, 128B swizzle
-    CUtensorMap x_map;                   // sorted x [T][d_in] bf16, box 64 x max(16, 8*NT), 128B swizzle
-    const uint8_t* xp;                   // padded, permuted tiles of the variant phases
-    const float* corr;                   // C per sorted position
+    CUtensorMap x_map;                   // x [T][d_in] bf16 (caller order), box 64 x max(16, 8*NT), 128B swizzle
+    const uint8_t* xp;                   // padded, permuted, scaled tiles of the variant phases
+    const float* corr;                   // [T][nsplit] partial corrections C per sorted position
     const int32_t* vid;
     const float* alpha[kMaxVariants];
     void* y;
     uint32_t* err;
     int64_t T, d_out, d_in;
-    int V, per_row, out_f32, CK;
+    int V, per_row, out_f32, CK, nsplit;
     // kRecodeConst, passed at run time so that it sits in a register and each
     // operand pair is a single three-input logic op (mask immediate, constant
     // register) instead of two ops with two immediates
     uint32_t recode_const;
 };
 
-// Result of the per-CTA router (identical in every CTA and in the prepare pass).
+// Result of the per-block router (identical in every block of a group).
 struct Routing {
     int key[kMaxTok];    // key of token t (caller order); key = vid + 1, 0 = base model
     int perm[kMaxTok];   // sorted position -> token
@@ -124,27 +139,17 @@ struct Routing {
     int act[kMaxTok];    // slot -> variant id
     int len[kMaxTok];    // slot -> padded 8-token tiles of that variant
     int ptile[kMaxTok];  // slot -> first padded tile (over all slots)
+    int invp[kMaxTok];   // token -> sorted position
     int n_act;
     int n_ptiles;
 };
 
-struct MultiShared {
-    uint64_t full_v[kVarStages];    // variant stage landed (TMA)
-    uint64_t empty_v[kVarStages];   // variant stage consumed (8 consumer warps)
-    uint64_t full_b[kBaseStages];   // base stage landed (TMA)
-    uint64_t empty_b[kBaseStages];  // base stage read by the tensor core (tcgen05.commit)
-    uint64_t accum;                 // every base MMA complete
-    uint32_t tmem_base;
-    volatile int abort;
-    Routing rt;
-};
-
 // Stable counting sort of the T (<= 64) tokens by key = vid + 1 (ids outside
-// [-1, V) become base tokens and are flagged by block 0 of a launch), then
-// the active variants in key order and their padded tiles.  Needs at least 96
-// threads; ends with __syncthreads.  Ranks come from __match_any_sync inside
-// each 32-token warp plus warp 0's per-key counts; the per-key offsets, slots
-// and padded-tile offsets from one warp's chunked prefix scans.
+// [-1, V) become base tokens and are flagged by block 0 of a launch when err
+// is set), then the active variants in key order and their padded tiles.
+// Needs at least 96 threads; ends with __syncthreads.  Ranks come from
+// __match_any_sync inside each 32-token warp plus warp 0's per-key counts; the
+// per-key offsets, slots and padded-tile offsets from one warp's prefix scans.
 __device__ void route_group(Routing& rt, const int32_t* vid, int T, int V, uint32_t* err, int tid)
 {
     const int lane = tid & 31, warp = tid >> 5;
@@ -217,8 +222,31 @@ __device__ void route_group(Routing& rt, const int32_t* vid, int T, int V, uint3
         const int pos = rt.seg[k] + rt.rank[tid] + (warp == 1 ? rt.cnt0[k] : 0);
         rt.perm[pos] = tid;
         rt.keyp[pos] = k;
+        rt.invp[tid] = pos;
     }
     __syncthreads();
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p)
+{
+    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
+}
+
+// Bounded wait that also gives up as soon as another warp of the CTA has
+// timed out (sets the CTA-wide abort flag and the error word on timeout).
+__device__ __forceinline__ bool wait_or_abort(volatile int& abort, uint64_t* bar, uint32_t parity, uint32_t* err)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (abort) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            abort = 1;
+            raise_error(err, kErrTimeout);
+            return false;
+        }
+    }
+    return true;
 }
 
 // ---------------------------------------------------------------- prepare pass
@@ -229,22 +257,22 @@ __device__ __forceinline__ uint16_t scaled_bits(uint16_t xb, float sigma)
     return __bfloat16_as_ushort(__float2bfloat16_rn(sigma * __bfloat162float(__ushort_as_bfloat16(xb))));
 }
 
-// One block per sorted token position (blocks 0..T-1) and one per empty row
-// of a padded tile (the rest).  Writes, for the CTA-level layout of the main
-// kernel:
-//   xs   [T][d_in]   x in sorted order (base phase);
-//   xp   padded tiles: for slot a, chunk c, tile r (of len_a), a 2 KB block
-//        at ((ptile_a * nc + c * len_a + r) * 2 KB) whose 16-byte piece
-//        (i, g, q) at ((i * 8 + g) * 4 + q) * 16 holds token row g of the
-//        tile, columns 32q + 8i .. 32q + 8i + 7 of the chunk in recoded order;
-//   corr [T]         C = sum_j x_j (2 a_(j mod 4) + 1) per sorted position.
-__global__ void __launch_bounds__(256) multi_prepare_kernel(const uint16_t* __restrict__ x,
-                                                            const int32_t* __restrict__ vid, int T, int V,
-                                                            int64_t d_in, uint16_t* __restrict__ xs,
-                                                            uint8_t* __restrict__ xp, float* __restrict__ corr)
+// Block (b, s): b < T handles sorted token position b, b >= T one empty row
+// of a padded tile; s is a split of kPrepChunks chunks of d_in.  Writes:
+//   xp    padded tiles: for slot a, chunk c, tile r (of len_a), a 2 KB block
+//         at ((ptile_a * nc + c * len_a + r) * 2 KB) whose 16-byte piece
+//         (i, g, q) at ((i * 8 + g) * 4 + q) * 16 holds token row g of the
+//         tile, columns 32q + 8i .. 32q + 8i + 7 of the chunk in recoded order
+//         and scaling;
+//   corr  [T][nsplit] partial C = sum_j x_j (2 a_(j mod 4) + 1) of split s
+//         (fp32, fixed summation order).
+__global__ void __launch_bounds__(kPrepThreads) multi_prepare_kernel(const uint16_t* __restrict__ x,
+                                                                     const int32_t* __restrict__ vid, int T, int V,
+                                                                     int64_t d_in, uint8_t* __restrict__ xp,
+                                                                     float* __restrict__ corr, int nsplit)
 {
     __shared__ Routing rt;
-    __shared__ double part[8];
+    __shared__ float part[kPrepThreads / 32];
     const int tid = threadIdx.x;
     route_group(rt, vid, T, V, nullptr, tid);
     const int nc = static_cast<int>(d_in / kChunk);
@@ -271,26 +299,23 @@ __global__ void __launch_bounds__(256) multi_prepare_kernel(const uint16_t* __re
         if (slot < 0) return;  // more blocks than empty rows
     }
     const uint16_t* xrow = pos >= 0 ? x + static_cast<int64_t>(rt.perm[pos]) * d_in : nullptr;
-    double c_sum = 0.0;
-    for (int task = tid; task < nc * 4; task += blockDim.x) {
-        const int c = task >> 2, q = task & 3;
+    const int c = static_cast<int>(blockIdx.y) * kPrepChunks + (tid >> 2), q = tid & 3;
+    float c_sum = 0.0f;
+    if (c < nc) {
         const int64_t col0 = static_cast<int64_t>(c) * kChunk + 32 * q;
         uint16_t v[32];
         if (xrow) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const uint4 w = ld_nc_v4(xrow + col0 + 8 * u);
-                *reinterpret_cast<uint4*>(xs + static_cast<int64_t>(pos) * d_in + col0 + 8 * u) = w;
                 v[8 * u + 0] = static_cast<uint16_t>(w.x); v[8 * u + 1] = static_cast<uint16_t>(w.x >> 16);
                 v[8 * u + 2] = static_cast<uint16_t>(w.y); v[8 * u + 3] = static_cast<uint16_t>(w.y >> 16);
                 v[8 * u + 4] = static_cast<uint16_t>(w.z); v[8 * u + 5] = static_cast<uint16_t>(w.z >> 16);
                 v[8 * u + 6] = static_cast<uint16_t>(w.w); v[8 * u + 7] = static_cast<uint16_t>(w.w >> 16);
             }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const __nv_bfloat16 b = __ushort_as_bfloat16(v[j]);
-                c_sum += static_cast<double>(__bfloat162float(b)) * recode_corr(j & 3);
-            }
+            for (int j = 0; j < 32; ++j)
+                c_sum = fmaf(__bfloat162float(__ushort_as_bfloat16(v[j])), recode_corr(j & 3), c_sum);
         } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0;  // padding row of a tile
@@ -313,39 +338,30 @@ __global__ void __launch_bounds__(256) multi_prepare_kernel(const uint16_t* __re
         }
     }
     if (pos < 0) return;
-    // fixed-order block reduction of C (deterministic)
+    // fixed-order block reduction of this split's share of C (deterministic)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) c_sum += __shfl_xor_sync(0xffffffffu, c_sum, o);
     if ((tid & 31) == 0) part[tid >> 5] = c_sum;
     __syncthreads();
     if (tid == 0) {
-        double s = 0.0;
-        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) s += part[w];
-        corr[pos] = static_cast<float>(s);
+        float s = 0.0f;
+        for (int w = 0; w < kPrepThreads / 32; ++w) s += part[w];
+        corr[static_cast<int64_t>(pos) * nsplit + blockIdx.y] = s;
     }
 }
 
-// ---------------------------------------------------------------- main kernel
+// ---------------------------------------------------------------- variant phases and the fused kernel
 
-__device__ __forceinline__ bool wait_or_abort(MultiShared& sh, uint64_t* bar, uint32_t parity, uint32_t* err)
-{
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
-        if (sh.abort) return false;
-        if (global_timer_ns() - t0 > kWaitLimitNs) {
-            sh.abort = 1;
-            raise_error(err, kErrTimeout);
-            return false;
-        }
-    }
-    return true;
-}
-
-__device__ __forceinline__ uint8_t* align1024(uint8_t* p)
-{
-    return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
-}
+struct MultiShared {
+    uint64_t full[kVarStages];      // variant stage landed (TMA)
+    uint64_t empty[kVarStages];     // variant stage consumed (8 consumer warps)
+    uint64_t full_b[kBaseStages];   // base stage landed (TMA)
+    uint64_t empty_b[kBaseStages];  // base stage read by the tensor core (tcgen05.commit)
+    uint64_t accum;                 // every base MMA complete
+    uint32_t tmem_base;
+    volatile int abort;
+    Routing rt;
+};
 
 // Consumer side of one variant phase over L padded tiles (tiles t0 ..
 // t0 + L - 1 of the variant in slot `slot`): the sign MMAs over the CTA's
@@ -375,14 +391,14 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
     for (int c0 = 0; c0 < n_chunks; c0 += grp) {
         const int cnt = n_chunks - c0 < grp ? n_chunks - c0 : grp;
         const int s = i_stage % kVarStages;
-        if (!__all_sync(0xffffffffu,
-                        wait_or_abort(sh, &sh.full_v[s], static_cast<uint32_t>(i_stage / kVarStages) & 1u, p.err))) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(sh.abort, &sh.full[s],
+                                                   static_cast<uint32_t>(i_stage / kVarStages) & 1u, p.err))) {
             ok = false;
             break;
         }
         const uint8_t* st = vring + static_cast<size_t>(s) * kVarSlot;
         const uint8_t* pads = st + cnt * kSignChunk;
-        for (int cc = 0; cc < cnt; ++cc) {
+        auto chunk = [&](int cc) {
             const uint32_t* sg = reinterpret_cast<const uint32_t*>(st + cc * kSignChunk);
             const uint32_t w0 = sg[rl0 * 4 + q], w1 = sg[(rl0 + 8) * 4 + q];
             const uint8_t* pc = pads + cc * L * kPadTile + ((g * 4 + q) << 4);
@@ -402,9 +418,15 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
                     mma_bf16_16816(acc[r][NS - 1], a0[2], a1[2], a0[3], a1[3], xv.z, xv.w);
                 }
             }
+        };
+        if (cnt == grp) {
+#pragma unroll
+            for (int cc = 0; cc < grp; ++cc) chunk(cc);  // full stage: addresses are immediates
+        } else {
+            for (int cc = 0; cc < cnt; ++cc) chunk(cc);
         }
         __syncwarp();
-        if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty_v[s]);
+        if ((threadIdx.x & 31) == 0) mbar_arrive(&sh.empty[s]);
         ++i_stage;
     }
     if (!ok) return false;
@@ -459,16 +481,12 @@ __device__ __forceinline__ bool run_phase(int L, MultiShared& sh, const MultiPar
     return false;
 }
 
-// Single-thread bounded wait (sets the CTA abort flag and the error word on timeout).
-__device__ __forceinline__ bool wait1(MultiShared& sh, uint64_t* bar, uint32_t parity, uint32_t* err)
-{
-    return wait_or_abort(sh, bar, parity, err);
-}
-
+// The fused multi-variant linear over one CTA's 128 rows and d_in slice (see
+// the file comment for the three roles), then the epilogue.
 template <int NT>
 __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constant__ MultiParams p)
 {
-    constexpr int Tpad = 8 * NT;                    // accumulator columns (sorted token positions)
+    constexpr int Tpad = 8 * NT;                    // per-token sum columns (sorted positions)
     constexpr int Npad = Tpad < 16 ? 16 : Tpad;     // tcgen05 N (M = 128 needs N % 16 == 0)
     constexpr int kXTile = Npad * kHalfRowBytes;    // x box [Npad tokens x 64 columns]
     constexpr int kBaseStage = kWTile + kXTile;
@@ -490,13 +508,12 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
     const int64_t row0 = static_cast<int64_t>(blockIdx.x / CK) * kRows;
-    const int valid_rows = static_cast<int>(p.d_out - row0 < kRows ? p.d_out - row0 : kRows);
 
     route_group(sh.rt, p.vid, T, p.V, p.err, tid);
     if (tid == 0) {
         for (int s = 0; s < kVarStages; ++s) {
-            mbar_init(&sh.full_v[s], 1);
-            mbar_init(&sh.empty_v[s], kConsumers);
+            mbar_init(&sh.full[s], 1);
+            mbar_init(&sh.empty[s], kConsumers);
         }
         for (int s = 0; s < kBaseStages; ++s) {
             mbar_init(&sh.full_b[s], 1);
@@ -521,9 +538,10 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     if (warp == kBaseWarp) {
         // ------------------------------------------------------------ base phase (one thread)
         // x . W_base^T on the tensor cores, concurrently with the variant
-        // phases: 64-column stages of W_base [128 x 64] and x [Npad x 64],
-        // tcgen05.mma M = 128, N = Npad, K = 16, fp32 accumulator in tensor
-        // memory; a stage is refilled once the MMAs reading it completed.
+        // phases: 64-column stages of W_base [128 x 64] and x [Npad x 64]
+        // (caller token order), tcgen05.mma M = 128, N = Npad, K = 16, fp32
+        // accumulator in tensor memory; a stage is refilled once the MMAs
+        // reading it completed.
         if (lane == 0) {
             const int nk = 2 * n_chunks;
             int issued = 0, done = 0;
@@ -538,7 +556,8 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
             for (; issued < (nk < kBaseStages ? nk : kBaseStages); ++issued) issue(issued);
             for (int k = 0; k < nk; ++k) {
                 const int s = k % kBaseStages;
-                if (!wait1(sh, &sh.full_b[s], static_cast<uint32_t>(k / kBaseStages) & 1u, p.err)) break;
+                if (!wait_or_abort(sh.abort, &sh.full_b[s], static_cast<uint32_t>(k / kBaseStages) & 1u, p.err))
+                    break;
                 tc_fence_after();
                 const uint8_t* st = bring + static_cast<size_t>(s) * kBaseStage;
                 const uint64_t adesc = smem_desc_sw128(smem_u32(st));
@@ -552,7 +571,9 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
                 // refill the slot of the previous stage once its MMAs are done
                 if (k >= 1 && issued < nk) {
                     const int sp = (k - 1) % kBaseStages;
-                    if (!wait1(sh, &sh.empty_b[sp], static_cast<uint32_t>((k - 1) / kBaseStages) & 1u, p.err)) break;
+                    if (!wait_or_abort(sh.abort, &sh.empty_b[sp], static_cast<uint32_t>((k - 1) / kBaseStages) & 1u,
+                                       p.err))
+                        break;
                     issue(issued++);
                 }
             }
@@ -567,7 +588,7 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
             }
         }
         __syncwarp();
-    } else if (warp == kVarProducerWarp) {
+    } else if (warp == kProducerWarp) {
         // ------------------------------------------------------------ variant-phase producer
         int i = 0;
         bool ok = true;
@@ -581,21 +602,21 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
                     const int cnt = n_chunks - c0 < grp ? n_chunks - c0 : grp;
                     const int s = i % kVarStages;
                     if (i >= kVarStages &&
-                        !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty_v[s],
+                        !__all_sync(0xffffffffu, wait_or_abort(sh.abort, &sh.empty[s],
                                                                static_cast<uint32_t>(i / kVarStages - 1) & 1u, p.err))) {
                         ok = false;
                         break;
                     }
                     uint8_t* st = vring + static_cast<size_t>(s) * kVarSlot;
                     if (lane == 0) {
-                        mbar_arrive_expect_tx(&sh.full_v[s], static_cast<uint32_t>(cnt * (kSignChunk + L * kPadTile)));
+                        mbar_arrive_expect_tx(&sh.full[s], static_cast<uint32_t>(cnt * (kSignChunk + L * kPadTile)));
                         for (int cc = 0; cc < cnt; ++cc) {
                             const int c = c_begin + c0 + cc;
                             tma_load_2d(st + cc * kSignChunk, &p.sign_map[v], 4 * c, static_cast<int>(row0),
-                                        &sh.full_v[s]);
+                                        &sh.full[s]);
                             bulk_g2s(st + cnt * kSignChunk + cc * L * kPadTile,
                                      src + (static_cast<int64_t>(c) * len + t0) * kPadTile,
-                                     static_cast<uint32_t>(L * kPadTile), &sh.full_v[s]);
+                                     static_cast<uint32_t>(L * kPadTile), &sh.full[s]);
                         }
                     }
                     __syncwarp();
@@ -608,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
             const int s = k % kVarStages;
             const uint32_t par = static_cast<uint32_t>(k / kVarStages) & 1u;
             const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(&sh.full_v[s], par) && global_timer_ns() - t0 < kWaitLimitNs) {
+            while (!mbar_try_wait(&sh.full[s], par) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
     } else {
@@ -625,11 +646,12 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     }
 
     // ---------------------------------------------------------------- epilogue
-    // per-token sums of this CTA's slice: variant parts (already in red) +
-    // base part (tensor memory), then the cluster K reduction
+    // 1. add the tensor-memory base sums (column = caller token) into the
+    //    per-token sums (column = sorted position)
     __syncthreads();
+    const Routing& rt = sh.rt;
     if (warp < 4) {
-        const bool base_ok = __all_sync(0xffffffffu, wait_or_abort(sh, &sh.accum, 0u, p.err));
+        const bool base_ok = __all_sync(0xffffffffu, wait_or_abort(sh.abort, &sh.accum, 0u, p.err));
         tc_fence_after();
         if (base_ok) {
             const int row = 32 * warp + lane;  // tensor-memory lane = local row
@@ -638,30 +660,55 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
                 uint32_t d[32];
                 tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * cb, d);
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (32 * cb + j < Tpad) red[row * kRedStride + 32 * cb + j] += __uint_as_float(d[j]);
+                for (int j = 0; j < 32; ++j) {
+                    const int t = 32 * cb + j;
+                    if (t < T) red[row * kRedStride + rt.invp[t]] += __uint_as_float(d[j]);
+                }
             }
         }
     }
+    __syncthreads();  // every base MMA complete, every copy landed: the base ring is free
+    // 2. push the per-token sums to the owners of their rows (receive slots
+    //    [CK][kRows / CK rows][Tpad + 1] in the base ring, free once every
+    //    peer got here), then each owner adds its slots in rank order
+    float* recv = reinterpret_cast<float*>(bring);
+    const int nr = kRows / CK;
     cluster.sync();
-    const Routing& rt = sh.rt;
-    const int r_lo = rank * kRows / CK, r_hi = (rank + 1) * kRows / CK;
-    const int nr = r_hi - r_lo;
+    for (int o = tid; o < kRows * T; o += kThreads) {
+        const int r = o / T, pos = o % T;
+        const int owner = r / nr;
+        float* dst = cluster.map_shared_rank(recv, owner);
+        dst[(rank * nr + (r - owner * nr)) * kRedStride + pos] = red[r * kRedStride + pos];
+    }
+    __syncthreads();  // red is read above before it is reused below
+    // per-token corrections and per-row alphas of this rank's rows, staged in red
+    float* corr_s = red;                       // [Tpad]
+    float* alpha_s = red + Tpad;               // [n_act][nr]
+    if (tid < T) {
+        float c = 0.0f;
+        for (int sp = 0; sp < p.nsplit; ++sp) c += p.corr[static_cast<int64_t>(tid) * p.nsplit + sp];
+        corr_s[tid] = c;
+    }
+    for (int o = tid; o < n_act * nr; o += kThreads) {
+        const int a = o / nr, r = o % nr;
+        const int64_t row = row0 + rank * nr + r;
+        alpha_s[o] = row < p.d_out ? p.alpha[rt.act[a]][p.per_row ? row : 0] : 0.0f;
+    }
+    cluster.sync();
     for (int o = tid; o < nr * T; o += kThreads) {
-        const int pos = o / nr, r = r_lo + o % nr;
-        if (r >= valid_rows) continue;
+        const int pos = o / nr, r = o % nr;
+        const int64_t row = row0 + rank * nr + r;
+        if (row >= p.d_out) continue;
         float y = 0.0f;
-        for (int k = 0; k < CK; ++k) y += cluster.map_shared_rank(red, k)[r * kRedStride + pos];
+        for (int k = 0; k < CK; ++k) y += recv[(k * nr + r) * kRedStride + pos];
         const int key = rt.keyp[pos];
-        const int64_t row = row0 + r;
-        if (key >= 1) y = fmaf(-p.alpha[key - 1][p.per_row ? row : 0], p.corr[pos], y);
+        if (key >= 1) y = fmaf(-alpha_s[rt.slot_of_key[key] * nr + r], corr_s[pos], y);
         const int64_t idx = static_cast<int64_t>(rt.perm[pos]) * p.d_out + row;
         if (p.out_f32)
             static_cast<float*>(p.y)[idx] = y;
         else
             static_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(y);
     }
-    cluster.sync();  // peers may still read this CTA's partials until here
     tc_fence_before();
     __syncthreads();
     if (warp == kBaseWarp) {
@@ -674,7 +721,8 @@ template <int NT>
 cudaError_t launch_nt(const MultiParams& prm, size_t smem, unsigned grid, cudaStream_t stream)
 {
     auto kern = multi_kernel<NT>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    static std::atomic<size_t> smem_set[kHostMaxDevices];
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(grid);
@@ -702,13 +750,20 @@ int multi_max_ptiles(int T, int V)
     return (t + 7 * a) / 8;
 }
 
+int multi_corr_splits(int64_t d_in)
+{
+    const int64_t nc = d_in / kChunk;
+    return static_cast<int>((nc + kPrepChunks - 1) / kPrepChunks);
+}
+
 cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
 {
     const int T = static_cast<int>(a.T);
     if (T < 1 || T > kMaxTok || a.V < 1 || a.V > kMaxVariants) return cudaErrorInvalidValue;
-    if (!a.x_sorted || !a.xp || !a.corr) return cudaErrorInvalidValue;
+    if (!a.xp || !a.corr) return cudaErrorInvalidValue;
     const int nt = tiles_for(T);
     const int npad = 8 * nt < 16 ? 16 : 8 * nt;
+    const int nsplit = multi_corr_splits(a.d_in);
     static thread_local MultiParams prm;  // ~9 KB: kept off the stack
     prm.xp = a.xp;
     prm.corr = a.corr;
@@ -721,6 +776,7 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
     prm.V = a.V;
     prm.per_row = a.per_row;
     prm.out_f32 = a.out_f32;
+    prm.nsplit = nsplit;
     prm.recode_const = kRecodeConst;
     for (int v = 0; v < a.V; ++v) {
         prm.alpha[v] = a.alpha[v];
@@ -733,7 +789,7 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
     if (!encode_tma_2d(&prm.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
                        static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, 64,
                        static_cast<uint32_t>(kRows), CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x_sorted, static_cast<uint64_t>(a.d_in),
+        !encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, static_cast<uint64_t>(a.d_in),
                        static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, 64,
                        static_cast<uint32_t>(npad), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
@@ -746,8 +802,8 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
     const size_t red = static_cast<size_t>(kRows) * (8 * nt + 1) * sizeof(float);
     const size_t smem = kBaseStages * base_stage + kVarStages * static_cast<size_t>(kVarSlot) + red + 1024;
 
-    const int prep_blocks = T + 7 * (T < a.V ? T : a.V);
-    multi_prepare_kernel<<<prep_blocks, 256, 0, stream>>>(a.x, a.vid, T, a.V, a.d_in, a.x_sorted, a.xp, a.corr);
+    const dim3 prep_grid(static_cast<unsigned>(T + 7 * (T < a.V ? T : a.V)), static_cast<unsigned>(nsplit));
+    multi_prepare_kernel<<<prep_grid, kPrepThreads, 0, stream>>>(a.x, a.vid, T, a.V, a.d_in, a.xp, a.corr, nsplit);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>((a.d_out + kRows - 1) / kRows * ck);

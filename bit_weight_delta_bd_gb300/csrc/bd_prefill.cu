@@ -269,8 +269,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, int /*sm_count*/, cudaStream_t 
     prm.per_row = a.per_row;
     prm.out_f32 = a.out_f32;
     const size_t smem = static_cast<size_t>(kStages) * kStageBytes + 1024;
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    static std::atomic<size_t> smem_set[kHostMaxDevices];
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel), smem, smem_set);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>((a.T + BN - 1) / BN), static_cast<unsigned>((a.d_out + BM - 1) / BM));
     prefill_kernel<<<grid, kThreads, smem, stream>>>(prm);

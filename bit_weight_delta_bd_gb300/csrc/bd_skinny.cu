@@ -437,7 +437,8 @@ template <int NT, bool MULTI, int NCONS>
 cudaError_t launch_cfg(const SkinnyParams& prm, size_t smem, cudaStream_t stream)
 {
     auto kern = skinny_kernel<NT, MULTI, NCONS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    static std::atomic<size_t> smem_set[kHostMaxDevices];
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem, smem_set);
     if (e != cudaSuccess) return e;
     constexpr int kRows = 16 * NCONS / ((MULTI && NT >= 2) ? 2 : 1);
     cudaLaunchConfig_t cfg{};

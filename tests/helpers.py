@@ -13,8 +13,9 @@ tensor-core accumulators that truncate instead of rounding.  The prefill path
 (T > 64) rounds W_eff to bf16 before its contraction, which adds up to
 2^-9 * |x_j| * (|w_j| + alpha) per term to that bound.  The multi-variant
 kernel computes sum_j x_j s_j as 2 sum_j x_j v_j - C with |v_j| <= 9 and
-|C| <= 17 sum_j |x_j| (an exact recoding of the sign operand), so its bound
-weighs alpha by 2 * 9 + 1 = 19 instead of 1 (20 with rounding slack).
+C = sum_j x_j c_j, 0 <= c_j <= 17, itself an fp32 sum (an exact recoding of
+the sign operand), so its bound weighs alpha by 2 * 9 + 17 / 4 + 1 < 24
+instead of 1.
 """
 from __future__ import annotations
 
@@ -90,7 +91,7 @@ def fp32_bound(x_bits, wb_bits, alpha, per_row: bool, rows=None, weff_bf16: bool
     return ((n + 4) * 2.0 ** -22 + (2.0 ** -9 if weff_bf16 else 0.0)) * s + 1e-30
 
 
-def fp32_bound_multi(x_bits, wb_bits, alphas, vid, rows, sign_weight: float = 20.0) -> np.ndarray:
+def fp32_bound_multi(x_bits, wb_bits, alphas, vid, rows, sign_weight: float = 24.0) -> np.ndarray:
     """Per-token form of fp32_bound for the multi-variant kernel:
     (n + 4) * 2^-22 * sum_j |x_j| (|w_j| + sign_weight * alpha_v(t)), alpha_v of
     the token's variant (0 for base-model tokens); alphas[v] holds the
