@@ -54,7 +54,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # gate projection only, whose traffic tracks the algorithmic bytes.
 NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
-    ("skinny_kernel<1,false>", "decode"): ("626c1a5ceec5ed51", "bd_skinny.cu", 499_453_696 + 3_220_224),
+    ("skinny_kernel<1>", "decode"): ("626c1a5ceec5ed51", "bd_skinny.cu", 499_453_696 + 3_220_224),
     ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_613_184 + 7_913_728),
     ("prefill_kernel", "prefill"): ("d0586c42d68bd685", "bd_prefill.cu", 613_019_648 + 63_200_000),
 }
@@ -235,7 +235,7 @@ class GpuRun:
                     lambda: bd.bd_compress(self.wb, self.wf[0], self.mode, self.signs[0], self.alpha[0], self.ws)))
         for i, T in enumerate(wl.tokens):
             nt = 1 if T <= 8 else 2 if T <= 16 else 4 if T <= 32 else 8
-            out.append((f"linear_T{T}", f"skinny_kernel<{nt},false>", linear_bytes(T, wl.d_out, wl.d_in, wl.n_alpha),
+            out.append((f"linear_T{T}", f"skinny_kernel<{nt}>", linear_bytes(T, wl.d_out, wl.d_in, wl.n_alpha),
                         4 * T * wl.d_out * wl.d_in,
                         (lambda i=i: bd.bd_linear(self.xs[i], self.wb, self.signs[0], self.alpha[0], self.mode,
                                                   self.ys[i], self.ws))))

@@ -189,16 +189,16 @@ bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const 
     for (int64_t t0 = 0; t0 < T; t0 += bd::kSkinnyMaxTokens) {
         bd::SkinnyArgs a{};
         a.x = x + t0 * d_in;
-        a.vid = nullptr;
         a.w_base = w_base;
+        a.signs = signs;
+        a.alpha = alpha;
         a.T = (T - t0) < bd::kSkinnyMaxTokens ? (T - t0) : bd::kSkinnyMaxTokens;
-        a.d_out = d_out; a.d_in = d_in; a.V = 1;
+        a.d_out = d_out; a.d_in = d_in;
         a.per_row = alpha_mode == BD_ALPHA_PER_ROW;
-        a.signs[0] = signs; a.alpha[0] = alpha;
         a.y = static_cast<char*>(y) + static_cast<size_t>(t0) * d_out * ysz;
         a.out_f32 = out_dtype == BD_OUT_F32;
         a.err = err_word(ws);
-        if (bd_status s = launched(bd::launch_skinny(a, sms, st))) return s;
+        if (bd_status s = launched(bd::launch_skinny(a, st))) return s;
     }
     return BD_OK;
 }

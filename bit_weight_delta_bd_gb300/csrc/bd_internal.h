@@ -20,31 +20,25 @@ cudaError_t launch_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_
 cudaError_t launch_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, const float* alpha, bool per_row,
                                      int64_t d_out, int64_t d_in, float* w_eff, cudaStream_t stream);
 
-// ---- decode / multi-variant linear (bd_skinny.cu) ---------------------------------------------
+// ---- decode linear, one variant (bd_skinny.cu) ------------------------------------------------
 
-// Tokens one skinny launch covers (8 MMA n-tiles of 8 tokens).
+// Tokens one decode launch covers (8 MMA n-tiles of 8 tokens); also the
+// token group of the multi-variant linear.
 constexpr int kSkinnyMaxTokens = 64;
 
 struct SkinnyArgs {
     const uint16_t* x;        // [T][d_in] bf16 bits
-    const int32_t* vid;       // [T] or null (single variant: every token uses variant 0)
     const uint16_t* w_base;   // [d_out][d_in]
+    const uint32_t* signs;    // [d_out][d_in/32]
+    const float* alpha;       // [d_out] or [1]
     int64_t T, d_out, d_in;
-    int V;                    // number of variants addressed by vid (1 for single)
     int per_row;
-    const uint32_t* signs[kMaxVariants];
-    const float* alpha[kMaxVariants];
     void* y;                  // [T][d_out]
     int out_f32;
     uint32_t* err;
-    uint16_t* x_sorted;       // multi-variant only: [T][d_in] scratch for x sorted by variant
 };
 
-cudaError_t launch_skinny(const SkinnyArgs& a, int sm_count, cudaStream_t stream);
-
-// Largest token group one skinny launch accepts (64, or fewer for the
-// multi-variant kernel when many variants would overflow shared memory).
-int skinny_group_tokens(bool multi, int V);
+cudaError_t launch_skinny(const SkinnyArgs& a, cudaStream_t stream);
 
 // ---- multi-variant linear (bd_multi.cu) -------------------------------------------------------
 

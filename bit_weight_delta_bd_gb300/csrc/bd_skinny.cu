@@ -1,26 +1,24 @@
-// Fused BitDelta linear for decode-sized token counts (T <= 64), one or many
-// variants sharing one W_base (section "Sunum mimarisi" of the BitDelta post:
-// the fused reconstruct+matmul kernel and the shared-read base weights under
-// a per-request delta cache).
+// Fused BitDelta linear for decode-sized token counts (T <= 64) of one variant
+// (section "Sunum mimarisi" of the BitDelta post: the fused
+// reconstruct+matmul kernel that reads W_base and the packed bits together).
 //
-//   y[t][r] = sum_j x[t][j] * W_base[r][j]  +  alpha_v(t)[r] * sum_j x[t][j] * s_v(t)[r][j]
+//   y[t][r] = sum_j x[t][j] * W_base[r][j]  +  alpha[r] * sum_j x[t][j] * s[r][j]
 //
 // which is exactly x . (W_base + alpha*s)^T with no rounding of W_eff: the
 // base and the sign contraction are separate bf16 MMAs (s in {-1,+1} is exact
 // in bf16) that share the x operand, accumulated in fp32.
 //
-// Work split.  A CTA owns a block of 16*NCONS output rows and one of CK equal
-// slices of d_in; the CK CTAs of a thread-block cluster cover all of d_in and
-// reduce their partial sums through distributed shared memory, in rank order
-// (CK depends on d_in and the kernel flavour only, never on d_out, so a row's
-// arithmetic does not change when the rows are sharded).  Inside the CTA one
-// producer thread streams 128-column stages into a ring of shared-memory
-// buffers with a handful of 2-D TMA boxes per stage and NCONS consumer warps
-// (16 rows each) run the MMAs:
+// Work split.  A CTA owns a block of 16*kConsumers output rows and one of CK
+// equal slices of d_in; the CK CTAs of a thread-block cluster cover all of
+// d_in and reduce their partial sums through distributed shared memory, in
+// rank order (CK depends on d_in only, never on d_out, so a row's arithmetic
+// does not change when the rows are sharded).  Inside the CTA one producer
+// thread streams 128-column stages into a ring of shared-memory buffers with
+// a handful of 2-D TMA boxes per stage and the consumer warps (16 rows each)
+// run the MMAs:
 //   - W_base: two boxes [block rows x 64 columns], 128-byte swizzle;
-//   - x: two boxes [8*NT tokens x 64 columns], 128-byte swizzle (for the
-//     multi-variant kernel, from a copy of x already sorted by variant);
-//   - sign bits: one box [block rows x 4 words] per active variant;
+//   - x: two boxes [8*NT tokens x 64 columns], 128-byte swizzle;
+//   - sign bits: one box [block rows x 4 words];
 //   - full/empty mbarriers between producer and consumers, all waits bounded.
 // The swizzle puts 16-byte chunk c of a 128-byte row r at chunk c ^ (r % 8),
 // so the fragment loads below are bank-conflict free.
@@ -33,16 +31,6 @@
 // then reads 16 consecutive columns (two 16-byte loads) of its rows and of
 // its token, and the 16 sign bits of those columns are one half-word.  Bits
 // become bf16 +-1 pairs with 2 integer ops per register.
-//
-// Multi-variant.  The CTA groups its tokens by variant (stable counting
-// sort, key = vid+1, so base tokens come first); x rows are staged in that
-// order and processed as 8-token tiles.  The base MMA runs once per tile; for
-// every variant present in the tile the consumer expands that variant's bits
-// once and runs the sign MMA with x masked to the tile's tokens of that
-// variant.  W_base is read once per CTA whatever the number of variants; the
-// sign bits of every active variant are read once.  A small pre-pass
-// (gather_sorted_x) writes x in that sorted order into the workspace so that
-// it can be loaded by TMA boxes.
 #include <cooperative_groups.h>
 
 #include "bd_device.cuh"
@@ -57,40 +45,26 @@ constexpr int kChunk = 128;        // columns per pipeline stage
 constexpr int kHalfRowBytes = 128;  // one 64-column half of a staged row (one swizzle atom)
 constexpr int kSignRowBytes = 16;  // 4 sign words per row per stage
 constexpr int kMaxStages = 4;
-constexpr int kMaxKeys = kMaxVariants + 1;
-constexpr int kSingleConsumers = 4;  // 64 rows per CTA, up to three CTAs per SM
-constexpr int kMultiConsumers = 8;   // 128 rows per CTA (64 with the token split), 2 stages
-constexpr int kMultiStages = 2;
-constexpr size_t kSingleBudget = 66u * 1024u;  // three CTAs per SM (measured best on GB300)
-constexpr size_t kMultiBudget = 110u * 1024u;  // two CTAs per SM
+constexpr int kConsumers = 4;      // 64 rows per CTA, up to three CTAs per SM
+constexpr int kRows = 16 * kConsumers;
+constexpr int kThreads = 32 * (kConsumers + 1);
+constexpr size_t kSmemBudget = 66u * 1024u;  // three CTAs per SM (measured best on GB300)
 
 struct SkinnyParams {
-    CUtensorMap sign_map[kMaxVariants];  // [d_out][d_in/32] uint32, box 4 x block rows
-    CUtensorMap w_map;                   // [d_out][d_in] bf16, box 64 x block rows, 128B swizzle
-    CUtensorMap x_map;                   // [T][d_in] bf16 (sorted copy for multi), box 64 x 8*NT, 128B swizzle
-    const int32_t* vid;
-    const float* alpha[kMaxVariants];
+    CUtensorMap sign_map;   // [d_out][d_in/32] uint32, box 4 x 64 rows
+    CUtensorMap w_map;      // [d_out][d_in] bf16, box 64 x 64 rows, 128B swizzle
+    CUtensorMap x_map;      // [T][d_in] bf16, box 64 x 8*NT, 128B swizzle
+    const float* alpha;
     void* y;
     uint32_t* err;
     int64_t T, d_out, d_in;
-    int V, per_row, out_f32;
-    int CK, stages, sign_slots;
+    int per_row, out_f32;
+    int CK, stages;
 };
 
 struct SkinnyShared {
     uint64_t full[kMaxStages];
     uint64_t empty[kMaxStages];
-    int key[kSkinnyMaxTokens];   // key of token t (caller order)
-    int perm[kSkinnyMaxTokens];  // sorted position -> token
-    int keyp[kSkinnyMaxTokens];  // sorted position -> key
-    int seg[kMaxKeys + 1];
-    int slot_of_key[kMaxKeys];
-    int act[kSkinnyMaxTokens];   // slot -> variant id
-    int tile_first[kSkinnyMaxTokens / 8];
-    int tile_last[kSkinnyMaxTokens / 8];
-    int slot_tile_first[kSkinnyMaxTokens];  // 8-token tiles spanned by each active variant
-    int slot_tile_last[kSkinnyMaxTokens];
-    int n_act;
     volatile int abort;
 };
 
@@ -129,85 +103,9 @@ __device__ __forceinline__ bool wait_or_abort(SkinnyShared& sh, uint64_t* bar, u
     return true;
 }
 
-// Groups the T (<= 64) tokens by key = vid + 1 (0 = base model or an
-// out-of-range id) with a stable counting sort: perm[pos] = token,
-// keyp[pos] = its key; lists the active variants (slot -> id).  Every CTA of
-// a launch, and the x gather pre-pass, computes the same result.
-template <bool MULTI>
-__device__ void route_tokens(SkinnyShared& sh, const int32_t* vid, int T, int V, uint32_t* err, int tid)
+template <int NT>
+__global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_constant__ SkinnyParams p)
 {
-    if (MULTI) {
-        if (tid < kSkinnyMaxTokens) {
-            int k = kMaxKeys;  // past T: never counted
-            if (tid < T) {
-                const int v = vid[tid];
-                const bool ok = (v >= -1 && v < V);
-                if (!ok && blockIdx.x == 0) raise_error(err, kErrBadVariant);
-                k = ok ? v + 1 : 0;
-            }
-            sh.key[tid] = k;
-        }
-        __syncthreads();
-        if (tid == 0) {
-            int cnt[kMaxKeys];
-            for (int k = 0; k <= V; ++k) cnt[k] = 0;
-            for (int t = 0; t < T; ++t) ++cnt[sh.key[t]];
-            sh.seg[0] = 0;
-            int n_act = 0;
-            for (int k = 0; k <= V; ++k) {
-                sh.seg[k + 1] = sh.seg[k] + cnt[k];
-                sh.slot_of_key[k] = -1;
-                if (k >= 1 && cnt[k] > 0) {
-                    sh.slot_of_key[k] = n_act;
-                    sh.act[n_act] = k - 1;
-                    ++n_act;
-                }
-            }
-            sh.n_act = n_act;
-        }
-        __syncthreads();
-        if (tid < T) {
-            const int k = sh.key[tid];
-            int r = 0;
-            for (int t = 0; t < tid; ++t) r += (sh.key[t] == k);
-            sh.perm[sh.seg[k] + r] = tid;
-            sh.keyp[sh.seg[k] + r] = k;
-        }
-    } else {
-        if (tid < T) {
-            sh.perm[tid] = tid;
-            sh.keyp[tid] = 1;
-        }
-        if (tid == 0) {
-            sh.n_act = 1;
-            sh.act[0] = 0;
-            sh.slot_of_key[0] = -1;
-            sh.slot_of_key[1] = 0;
-        }
-    }
-    __syncthreads();
-}
-
-template <bool MULTI>
-constexpr int ctas_per_sm()
-{
-    return 2;
-}
-
-template <int NT, bool MULTI, int NCONS>
-__global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
-    skinny_kernel(const __grid_constant__ SkinnyParams p)
-{
-    // Multi-variant with >= 2 token tiles: two warps per 16-row tile, each
-    // owning half of the (variant-sorted) tiles, to halve the accumulators per
-    // warp (two CTAs per SM) while each variant's bits are still expanded by
-    // the one warp whose tiles hold its tokens.
-    constexpr int TS = (MULTI && NT >= 2) ? 2 : 1;
-    constexpr int NTW = NT / TS;                // token tiles per warp
-    constexpr int kRowTiles = NCONS / TS;
-    constexpr int kRows = 16 * kRowTiles;       // rows per CTA
-    constexpr int kSignTile = kRows * kSignRowBytes;
-    constexpr int kThreads = 32 * (NCONS + 1);
     constexpr int Tpad = 8 * NT;
 
     extern __shared__ uint8_t dyn_raw[];
@@ -226,52 +124,38 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
     const int64_t row0 = static_cast<int64_t>(blockIdx.x / CK) * kRows;
     const int valid_rows = static_cast<int>(p.d_out - row0 < kRows ? p.d_out - row0 : kRows);
 
-    // ---------------------------------------------------------------- routing (per CTA)
-    route_tokens<MULTI>(sh, p.vid, T, p.V, p.err, tid);
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.empty[s], NCONS);
+            mbar_init(&sh.empty[s], kConsumers);
         }
         sh.abort = 0;
         fence_mbarrier_init();
     }
     __syncthreads();
-    if (tid < NT) {
-        const int p0 = 8 * tid;
-        const int p1 = (8 * tid + 7 < T - 1) ? 8 * tid + 7 : T - 1;
-        sh.tile_first[tid] = p0 < T ? sh.keyp[p0] : 1;
-        sh.tile_last[tid] = p0 < T ? sh.keyp[p1] : 0;  // empty range past T
-    }
-    if (MULTI && tid < sh.n_act) {
-        const int k = sh.act[tid] + 1;
-        sh.slot_tile_first[tid] = sh.seg[k] / 8;
-        sh.slot_tile_last[tid] = (sh.seg[k + 1] - 1) / 8;
-    }
-    __syncthreads();
 
     // ---------------------------------------------------------------- pipeline
-    // stage layout: [W half 0 | W half 1 | x half 0 | x half 1 | sign tiles], 1024-byte aligned
+    // stage layout: [W half 0 | W half 1 | x half 0 | x half 1 | sign tile], 1024-byte aligned
     const int stages = p.stages;
-    const int n_act = sh.n_act;
     constexpr int kWHalf = kRows * kHalfRowBytes;
     constexpr int kXHalf = Tpad * kHalfRowBytes;
     constexpr int kSignOff = 2 * kWHalf + 2 * kXHalf;
-    const int stage_bytes = (kSignOff + p.sign_slots * kSignTile + 1023) & ~1023;
+    constexpr int kSignTile = kRows * kSignRowBytes;
+    constexpr int kStageBytes = (kSignOff + kSignTile + 1023) & ~1023;
     const int nc = static_cast<int>(d_in / kChunk);
     const int c_begin = static_cast<int>(static_cast<int64_t>(rank) * nc / CK);
     const int c_end = static_cast<int>(static_cast<int64_t>(rank + 1) * nc / CK);
     const int n_chunks = c_end - c_begin;
 
-    float accb[NTW][4], accs[NTW][4];
+    float accb[NT][4], accs[NT][4];
 #pragma unroll
-    for (int j = 0; j < NTW; ++j)
+    for (int j = 0; j < NT; ++j)
 #pragma unroll
         for (int e = 0; e < 4; ++e) accb[j][e] = accs[j][e] = 0.0f;
 
-    if (warp == NCONS) {
+    if (warp == kConsumers) {
         // ------------------------------------------------------------ producer warp
-        const uint32_t tx = static_cast<uint32_t>(2 * kWHalf + 2 * kXHalf + n_act * kSignTile);
+        const uint32_t tx = static_cast<uint32_t>(2 * kWHalf + 2 * kXHalf + kSignTile);
         int issued = 0;
         for (int i = 0; i < n_chunks; ++i) {
             const int s = i % stages;
@@ -279,7 +163,7 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
                 !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty[s], static_cast<uint32_t>(i / stages - 1) & 1u,
                                                        p.err)))
                 break;
-            uint8_t* st = dyn + static_cast<size_t>(s) * stage_bytes;
+            uint8_t* st = dyn + static_cast<size_t>(s) * kStageBytes;
             const int col = (c_begin + i) * kChunk;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&sh.full[s], tx);
@@ -287,11 +171,9 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
                 tma_load_2d(st + kWHalf, &p.w_map, col + 64, static_cast<int>(row0), &sh.full[s]);
                 tma_load_2d(st + 2 * kWHalf, &p.x_map, col, 0, &sh.full[s]);
                 tma_load_2d(st + 2 * kWHalf + kXHalf, &p.x_map, col + 64, 0, &sh.full[s]);
+                tma_load_2d(st + kSignOff, &p.sign_map, col / 32, static_cast<int>(row0), &sh.full[s]);
             }
             __syncwarp();
-            for (int a = lane; a < n_act; a += 32)
-                tma_load_2d(st + kSignOff + a * kSignTile, &p.sign_map[sh.act[a]], col / 32, static_cast<int>(row0),
-                            &sh.full[s]);
             ++issued;
         }
         // every issued stage must have landed before the CTA reuses or frees the memory
@@ -304,21 +186,14 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
         }
     } else {
         // ------------------------------------------------------------ consumer warps
-        const int rl0 = 16 * (warp % kRowTiles) + g;  // local rows rl0 and rl0 + 8 (both = g mod 8)
-        const int j0 = (warp / kRowTiles) * NTW;       // first token tile of this warp
+        const int rl0 = 16 * warp + g;  // local rows rl0 and rl0 + 8 (both = g mod 8)
         const int c0 = ((2 * q) ^ g) << 4, c1 = ((2 * q + 1) ^ g) << 4;  // swizzled chunk offsets
-        int my_key[NTW];
-#pragma unroll
-        for (int j = 0; j < NTW; ++j) {
-            const int pos = 8 * (j0 + j) + g;
-            my_key[j] = pos < T ? sh.keyp[pos] : -1;
-        }
         for (int i = 0; i < n_chunks; ++i) {
             const int s = i % stages;
             if (!__all_sync(0xffffffffu,
                             wait_or_abort(sh, &sh.full[s], static_cast<uint32_t>(i / stages) & 1u, p.err)))
                 break;
-            const uint8_t* st = dyn + static_cast<size_t>(s) * stage_bytes;
+            const uint8_t* st = dyn + static_cast<size_t>(s) * kStageBytes;
             const uint32_t* sgn = reinterpret_cast<const uint32_t*>(st + kSignOff);
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
@@ -340,45 +215,15 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
                 const int sign_word = 2 * h + (q >> 1);
                 const uint32_t sign_shift = 16u * (q & 1);
                 uint32_t S0[8], S1[8];
-                if (!MULTI) {
-                    expand_signs((sgn[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
-                    expand_signs((sgn[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
+                expand_signs((sgn[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
+                expand_signs((sgn[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
 #pragma unroll
-                    for (int j = 0; j < NT; ++j) {
-                        const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
-                        const uint4 xa = *reinterpret_cast<const uint4*>(xr + c0);
-                        const uint4 xb = *reinterpret_cast<const uint4*>(xr + c1);
-                        mma4(accb[j], W0, W1, xa, xb);
-                        mma4(accs[j], S0, S1, xa, xb);
-                    }
-                } else {
-                    // base contraction for every tile: independent accumulator chains
-#pragma unroll
-                    for (int j = 0; j < NTW; ++j) {
-                        const uint8_t* xr = xst + (8 * (j0 + j) + g) * kHalfRowBytes;
-                        mma4(accb[j], W0, W1, *reinterpret_cast<const uint4*>(xr + c0),
-                             *reinterpret_cast<const uint4*>(xr + c1));
-                    }
-                    // sign contraction: each active variant's bits expanded once, applied to
-                    // its own tokens of the tiles it spans (warp-uniform tile predicates)
-                    for (int a = 0; a < n_act; ++a) {
-                        const int tf = sh.slot_tile_first[a] - j0, tl = sh.slot_tile_last[a] - j0;
-                        if (tl < 0 || tf >= NTW) continue;  // no token of this variant in my tiles
-                        const uint32_t* sb = sgn + a * (kSignTile / 4);
-                        expand_signs((sb[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
-                        expand_signs((sb[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
-                        const int key = sh.act[a] + 1;
-#pragma unroll
-                        for (int j = 0; j < NTW; ++j) {
-                            if (j < tf || j > tl) continue;
-                            const uint8_t* xr = xst + (8 * (j0 + j) + g) * kHalfRowBytes;
-                            const bool mine = (my_key[j] == key);
-                            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                            const uint4 xa = mine ? *reinterpret_cast<const uint4*>(xr + c0) : z;
-                            const uint4 xb = mine ? *reinterpret_cast<const uint4*>(xr + c1) : z;
-                            mma4(accs[j], S0, S1, xa, xb);
-                        }
-                    }
+                for (int j = 0; j < NT; ++j) {
+                    const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
+                    const uint4 xa = *reinterpret_cast<const uint4*>(xr + c0);
+                    const uint4 xb = *reinterpret_cast<const uint4*>(xr + c1);
+                    mma4(accb[j], W0, W1, xa, xb);
+                    mma4(accs[j], S0, S1, xa, xb);
                 }
             }
             __syncwarp();
@@ -390,12 +235,11 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
     __syncthreads();  // pipeline drained: the stage memory becomes the reduction buffer
     float* red_b = reinterpret_cast<float*>(dyn);
     float* red_s = red_b + kRows * Tpad;
-    if (warp < NCONS) {
-        const int r0 = 16 * (warp % kRowTiles) + g;
-        const int j0 = (warp / kRowTiles) * NTW;
+    if (warp < kConsumers) {
+        const int r0 = 16 * warp + g;
 #pragma unroll
-        for (int j = 0; j < NTW; ++j) {
-            const int pos = 8 * (j0 + j) + 2 * q;
+        for (int j = 0; j < NT; ++j) {
+            const int pos = 8 * j + 2 * q;
             red_b[r0 * Tpad + pos] = accb[j][0];
             red_b[r0 * Tpad + pos + 1] = accb[j][1];
             red_b[(r0 + 8) * Tpad + pos] = accb[j][2];
@@ -410,21 +254,18 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
     const int r_lo = rank * kRows / CK, r_hi = (rank + 1) * kRows / CK;
     const int nr = r_hi - r_lo;
     for (int o = tid; o < nr * T; o += kThreads) {
-        const int pos = o / nr, r = r_lo + o % nr;
+        const int t = o / nr, r = r_lo + o % nr;
         if (r >= valid_rows) continue;
         float b = 0.0f, sg = 0.0f;
         for (int k = 0; k < CK; ++k) {
             const float* pb = cluster.map_shared_rank(red_b, k);
             const float* ps = cluster.map_shared_rank(red_s, k);
-            b += pb[r * Tpad + pos];
-            sg += ps[r * Tpad + pos];
+            b += pb[r * Tpad + t];
+            sg += ps[r * Tpad + t];
         }
-        const int key = sh.keyp[pos];
-        const int slot = key >= 1 ? sh.slot_of_key[key] : -1;
         const int64_t row = row0 + r;
-        float y = b;
-        if (slot >= 0) y = fmaf(p.alpha[sh.act[slot]][p.per_row ? row : 0], sg, b);
-        const int64_t idx = static_cast<int64_t>(sh.perm[pos]) * p.d_out + row;
+        const float y = fmaf(p.alpha[p.per_row ? row : 0], sg, b);
+        const int64_t idx = static_cast<int64_t>(t) * p.d_out + row;
         if (p.out_f32)
             static_cast<float*>(p.y)[idx] = y;
         else
@@ -433,17 +274,16 @@ __global__ void __launch_bounds__(32 * (NCONS + 1), ctas_per_sm<MULTI>())
     cluster.sync();  // peers may still read this CTA's partials until here
 }
 
-template <int NT, bool MULTI, int NCONS>
-cudaError_t launch_cfg(const SkinnyParams& prm, size_t smem, cudaStream_t stream)
+template <int NT>
+cudaError_t launch_nt(const SkinnyParams& prm, size_t smem, cudaStream_t stream)
 {
-    auto kern = skinny_kernel<NT, MULTI, NCONS>;
+    auto kern = skinny_kernel<NT>;
     static std::atomic<size_t> smem_set[kHostMaxDevices];
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem, smem_set);
     if (e != cudaSuccess) return e;
-    constexpr int kRows = 16 * NCONS / ((MULTI && NT >= 2) ? 2 : 1);
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(static_cast<unsigned>((prm.d_out + kRows - 1) / kRows * prm.CK));
-    cfg.blockDim = dim3(32 * (NCONS + 1));
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -456,91 +296,39 @@ cudaError_t launch_cfg(const SkinnyParams& prm, size_t smem, cudaStream_t stream
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
-template <bool MULTI, int NCONS>
-cudaError_t launch_nt(int nt, const SkinnyParams& prm, size_t smem, cudaStream_t stream)
-{
-    switch (nt) {
-        case 1: return launch_cfg<1, MULTI, NCONS>(prm, smem, stream);
-        case 2: return launch_cfg<2, MULTI, NCONS>(prm, smem, stream);
-        case 4: return launch_cfg<4, MULTI, NCONS>(prm, smem, stream);
-        default: return launch_cfg<8, MULTI, NCONS>(prm, smem, stream);
-    }
-}
-
 int tiles_for(int T) { return T <= 8 ? 1 : T <= 16 ? 2 : T <= 32 ? 4 : 8; }
 
-// Rows per CTA (the multi-variant kernel splits 8 token tiles over two warps).
-int rows_for(bool multi, int nt) { return multi ? 16 * kMultiConsumers / (nt >= 2 ? 2 : 1) : 16 * kSingleConsumers; }
-
-size_t stage_bytes_for(int rows, int sign_slots, int nt)
+size_t stage_bytes_for(int nt)
 {
-    const size_t raw = 2u * rows * kHalfRowBytes + 2u * (8u * nt) * kHalfRowBytes +
-                       static_cast<size_t>(sign_slots) * rows * kSignRowBytes;
+    const size_t raw = 2u * kRows * kHalfRowBytes + 2u * (8u * nt) * kHalfRowBytes + kRows * kSignRowBytes;
     return (raw + 1023u) & ~static_cast<size_t>(1023u);
-}
-
-// Writes x in the order of the per-CTA router (sorted by variant) so the
-// multi-variant kernel can load it with TMA boxes.
-__global__ void __launch_bounds__(256) gather_sorted_x_kernel(const uint16_t* __restrict__ x,
-                                                               const int32_t* __restrict__ vid, int T, int V,
-                                                               int64_t d_in, uint16_t* __restrict__ xs)
-{
-    __shared__ SkinnyShared sh;
-    route_tokens<true>(sh, vid, T, V, nullptr, threadIdx.x);
-    const int64_t nvec = d_in / 8;
-    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; idx < T * nvec;
-         idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t pos = idx / nvec, v = idx % nvec;
-        reinterpret_cast<uint4*>(xs + pos * d_in)[v] = ld_nc_v4(x + static_cast<int64_t>(sh.perm[pos]) * d_in + 8 * v);
-    }
 }
 
 }  // namespace
 
-int skinny_group_tokens(bool multi, int V)
+cudaError_t launch_skinny(const SkinnyArgs& a, cudaStream_t stream)
 {
-    if (!multi) return kSkinnyMaxTokens;
-    for (int G = kSkinnyMaxTokens; G > 8; G /= 2) {
-        const int slots = V < G ? V : G;
-        const int nt = tiles_for(G);
-        if (kMultiStages * stage_bytes_for(rows_for(true, nt), slots, nt) + 1024 <= kMultiBudget) return G;
-    }
-    return 8;
-}
-
-cudaError_t launch_skinny(const SkinnyArgs& a, int /*sm_count*/, cudaStream_t stream)
-{
-    const bool multi = a.vid != nullptr;
     const int nc = static_cast<int>(a.d_in / kChunk);
     const int T = static_cast<int>(a.T);
+    if (T < 1 || T > kSkinnyMaxTokens) return cudaErrorInvalidValue;
     const int nt = tiles_for(T);
-    const int rows = rows_for(multi, nt);
-    if (T < 1 || T > skinny_group_tokens(multi, a.V)) return cudaErrorInvalidValue;
-    if (multi && a.x_sorted == nullptr) return cudaErrorInvalidValue;
 
-    static thread_local SkinnyParams prm;  // ~9 KB: kept off the stack
-    prm.vid = a.vid;
+    static thread_local SkinnyParams prm;
+    prm.alpha = a.alpha;
     prm.y = a.y;
     prm.err = a.err;
     prm.T = a.T;
     prm.d_out = a.d_out;
     prm.d_in = a.d_in;
-    prm.V = a.V;
     prm.per_row = a.per_row;
     prm.out_f32 = a.out_f32;
-    for (int v = 0; v < a.V; ++v) {
-        prm.alpha[v] = a.alpha[v];
-        if (!encode_tma_2d(&prm.sign_map[v], CU_TENSOR_MAP_DATA_TYPE_UINT32, a.signs[v],
-                           static_cast<uint64_t>(a.d_in / 32), static_cast<uint64_t>(a.d_out),
-                           static_cast<uint64_t>(a.d_in / 8), 4, static_cast<uint32_t>(rows),
-                           CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
-    }
-    const uint16_t* xsrc = multi ? a.x_sorted : a.x;
-    if (!encode_tma_2d(&prm.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
+    if (!encode_tma_2d(&prm.sign_map, CU_TENSOR_MAP_DATA_TYPE_UINT32, a.signs, static_cast<uint64_t>(a.d_in / 32),
+                       static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in / 8), 4,
+                       static_cast<uint32_t>(kRows), CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_tma_2d(&prm.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
                        static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, 64,
-                       static_cast<uint32_t>(rows), CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xsrc, static_cast<uint64_t>(a.d_in),
+                       static_cast<uint32_t>(kRows), CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, static_cast<uint64_t>(a.d_in),
                        static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, 64,
                        static_cast<uint32_t>(8 * nt), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
@@ -549,25 +337,20 @@ cudaError_t launch_skinny(const SkinnyArgs& a, int /*sm_count*/, cudaStream_t st
     int ck = nc / 32;
     ck = ck < 1 ? 1 : ck > 4 ? 4 : ck;
     prm.CK = ck;
-    prm.sign_slots = multi ? (a.V < T ? a.V : T) : 1;
-    const size_t stage_bytes = stage_bytes_for(rows, prm.sign_slots, nt);
-    const size_t budget = multi ? kMultiBudget : kSingleBudget;
-    int stages = multi ? kMultiStages : kMaxStages;
-    while (stages > 2 && stages * stage_bytes + 1024 > budget) --stages;
+    const size_t stage_bytes = stage_bytes_for(nt);
+    int stages = kMaxStages;
+    while (stages > 2 && stages * stage_bytes + 1024 > kSmemBudget) --stages;
     prm.stages = stages;
-    const size_t red = 2u * rows * (8u * nt) * sizeof(float);
+    const size_t red = 2u * kRows * (8u * nt) * sizeof(float);
     size_t smem = stages * stage_bytes;
     smem = (smem > red ? smem : red) + 1024;
     if (smem > 227u * 1024u) return cudaErrorInvalidConfiguration;
-    if (multi) {
-        const int64_t nvec = static_cast<int64_t>(T) * (a.d_in / 8);
-        const int blocks = static_cast<int>((nvec + 255) / 256 < 1024 ? (nvec + 255) / 256 : 1024);
-        gather_sorted_x_kernel<<<blocks, 256, 0, stream>>>(a.x, a.vid, T, a.V, a.d_in, a.x_sorted);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
-        return launch_nt<true, kMultiConsumers>(nt, prm, smem, stream);
+    switch (nt) {
+        case 1: return launch_nt<1>(prm, smem, stream);
+        case 2: return launch_nt<2>(prm, smem, stream);
+        case 4: return launch_nt<4>(prm, smem, stream);
+        default: return launch_nt<8>(prm, smem, stream);
     }
-    return launch_nt<false, kSingleConsumers>(nt, prm, smem, stream);
 }
 
 }  // namespace bd
