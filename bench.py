@@ -49,9 +49,7 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # kernel's source file at capture time and is ignored once that source has
 # changed.  Summaries of the captures are in profiles/.  An entry whose value
 # is a float is a ratio (traffic / algorithmic bytes) taken on one launch of a
-# smaller call of the same kernel and applied to the average launch: the
-# slice workload (56 calls, 26 GB resident) is captured on its 28672x8192
-# gate projection only, whose traffic tracks the algorithmic bytes.
+# smaller call of the same kernel and applied to the average launch.
 NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
     ("skinny_kernel<1>", "decode"): ("626c1a5ceec5ed51", "bd_skinny.cu", 499_453_696 + 3_220_224),
