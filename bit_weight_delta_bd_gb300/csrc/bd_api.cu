@@ -214,7 +214,8 @@ struct MultiWs {
 
 MultiWs multi_ws_layout(int64_t T, int32_t V, int64_t d_in)
 {
-    const int64_t tg = T < bd::kSkinnyMaxTokens ? T : bd::kSkinnyMaxTokens;
+    const int64_t group = bd::multi_group_tokens(V);
+    const int64_t tg = T < group ? T : group;
     const auto up = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
     MultiWs w{};
     w.xp = 1024;
@@ -259,7 +260,7 @@ bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int3
     if (bd_status s = device_info(&sms)) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const size_t ysz = out_dtype == BD_OUT_F32 ? 4 : 2;
-    const int64_t group = bd::kSkinnyMaxTokens;
+    const int64_t group = bd::multi_group_tokens(V);
     const MultiWs lay = multi_ws_layout(T, V, d_in);
     for (int64_t t0 = 0; t0 < T; t0 += group) {
         bd::MultiArgs a{};

@@ -62,6 +62,10 @@ struct MultiArgs {
 // variants: sum over variants of ceil(n_v / 8) <= (T + 7 min(T, V)) / 8.
 int multi_max_ptiles(int T, int V);
 
+// Tokens per multi-variant launch for V variants: 64, or fewer when a group
+// could need more zero-padded tiles than tensor memory holds.
+int multi_group_tokens(int V);
+
 // Column splits of the prepare pass (partial corrections per token).
 int multi_corr_splits(int64_t d_in);
 

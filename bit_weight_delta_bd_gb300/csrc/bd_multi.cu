@@ -67,14 +67,16 @@ constexpr int kChunk = 128;                   // d_in columns per chunk
 constexpr int kHalfRowBytes = 128;            // 64 bf16 columns: one 128-byte swizzle atom
 constexpr int kWTile = kRows * kHalfRowBytes; // W_base box [128 rows x 64 columns] = 16 KB
 constexpr int kBaseStages = 2;
-constexpr int kVarStages = 2;
-constexpr int kVarSlot = 14 * 1024;
+constexpr int kVarStages = 4;
+constexpr int kVarSlot = 15 * 1024;
 constexpr int kSignChunk = kRows * 16;        // 4 sign words x 128 rows = 2 KB
 constexpr int kPadTile = 8 * kChunk * 2;      // one 8-token tile of one chunk = 2 KB
 constexpr int kMaxTok = kSkinnyMaxTokens;
 constexpr int kMaxKeys = kMaxVariants + 1;
 constexpr int kPhaseTiles = 4;                // padded tiles per variant phase (more: several phases)
-constexpr int kTmemCols = 64;
+constexpr int kTmemCols = 256;               // base sums: columns 0..63; variant sums: 8 per padded tile
+constexpr int kVarCol = 64;
+constexpr int kMaxVarTiles = (kTmemCols - kVarCol) / 8;  // padded tiles one group may hold
 
 // ---- multi_prepare_kernel
 constexpr int kPrepThreads = 128;             // one task (chunk, 32-column group) per thread
@@ -361,17 +363,20 @@ struct MultiShared {
     uint32_t tmem_base;
     volatile int abort;
     Routing rt;
+    int col2pos[kMaxVarTiles * 8];  // variant tensor-memory column -> sorted position (-1: padding)
 };
 
 // Consumer side of one variant phase over L padded tiles (tiles t0 ..
 // t0 + L - 1 of the variant in slot `slot`): the sign MMAs over the CTA's
-// d_in slice, then alpha * 2M of each of the phase's tokens stored into the
-// per-token sums `red` (row stride rs; every (row, token) is written by
-// exactly one phase).  Returns false when the pipeline was aborted.  i_stage
-// is the running variant-stage counter shared with the producer's schedule.
+// d_in slice, then alpha * 2M of each padded tile stored into the tile's 8
+// tensor-memory columns (one 16-lane x 8-column store per tile, whose thread
+// layout is that of the MMA accumulator).  Returns false when the pipeline was
+// aborted.  i_stage is the running variant-stage counter shared with the
+// producer's schedule; rl0 is the warp's first row (its 16 rows lie in the
+// warp's tensor-memory lane quarter).
 template <int L>
 __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams& p, const uint8_t* vring, int slot,
-                                              int t0, int n_chunks, int& i_stage, float* red, int rs, int warp, int g,
+                                              int t0, int n_chunks, int& i_stage, uint32_t tmem_rows, int rl0, int g,
                                               int q, int64_t row0)
 {
     constexpr int grp = phase_group(L);
@@ -385,7 +390,7 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
         for (int h = 0; h < NS; ++h)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[r][h][e] = 0.0f;
-    const int rl0 = 16 * warp + g;
+    rl0 += g;
     const uint32_t rc = p.recode_const;
     bool ok = true;
     for (int c0 = 0; c0 < n_chunks; c0 += grp) {
@@ -430,48 +435,44 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
         ++i_stage;
     }
     if (!ok) return false;
-    // alpha * 2M of the phase's tokens (sorted positions seg0 + 8 t0 ..)
+    // alpha * 2M of the phase's tiles into tensor memory
     const Routing& rt = sh.rt;
     const int v = rt.act[slot];
-    const int seg0 = rt.seg[v + 1], end = rt.seg[v + 2];
     const int64_t ra = row0 + rl0, rb = ra + 8;
     const float* al = p.alpha[v];
     const float a2a = ra < p.d_out ? 2.0f * al[p.per_row ? ra : 0] : 0.0f;
     const float a2b = rb < p.d_out ? 2.0f * al[p.per_row ? rb : 0] : 0.0f;
 #pragma unroll
     for (int r = 0; r < L; ++r) {
+        float m[4];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-            const int pos = seg0 + 8 * (t0 + r) + 2 * q + e;
-            if (pos < end) {
-                const float m0 = NS == 2 ? acc[r][0][e] + acc[r][NS - 1][e] : acc[r][0][e];
-                const float m1 = NS == 2 ? acc[r][0][2 + e] + acc[r][NS - 1][2 + e] : acc[r][0][2 + e];
-                red[rl0 * rs + pos] = a2a * m0;
-                red[(rl0 + 8) * rs + pos] = a2b * m1;
-            }
-        }
+        for (int e = 0; e < 4; ++e) m[e] = NS == 2 ? acc[r][0][e] + acc[r][NS - 1][e] : acc[r][0][e];
+        const uint32_t col = static_cast<uint32_t>(kVarCol + 8 * (rt.ptile[slot] + t0 + r));
+        tmem_st_16x256b(tmem_rows + col, __float_as_uint(a2a * m[0]), __float_as_uint(a2a * m[1]),
+                        __float_as_uint(a2b * m[2]), __float_as_uint(a2b * m[3]));
     }
+    tmem_wait_st();
     return true;
 }
 
 template <int NT>
 __device__ __forceinline__ bool run_phase(int L, MultiShared& sh, const MultiParams& p, const uint8_t* vring, int slot,
-                                          int t0, int n_chunks, int& i_stage, float* red, int rs, int warp, int g,
+                                          int t0, int n_chunks, int& i_stage, uint32_t tmem_rows, int rl0, int g,
                                           int q, int64_t row0)
 {
     switch (L) {
-        case 1: return variant_phase<1>(sh, p, vring, slot, t0, n_chunks, i_stage, red, rs, warp, g, q, row0);
+        case 1: return variant_phase<1>(sh, p, vring, slot, t0, n_chunks, i_stage, tmem_rows, rl0, g, q, row0);
         case 2:
             if constexpr (NT >= 2)
-                return variant_phase<2>(sh, p, vring, slot, t0, n_chunks, i_stage, red, rs, warp, g, q, row0);
+                return variant_phase<2>(sh, p, vring, slot, t0, n_chunks, i_stage, tmem_rows, rl0, g, q, row0);
             break;
         case 3:
             if constexpr (NT >= 4)
-                return variant_phase<3>(sh, p, vring, slot, t0, n_chunks, i_stage, red, rs, warp, g, q, row0);
+                return variant_phase<3>(sh, p, vring, slot, t0, n_chunks, i_stage, tmem_rows, rl0, g, q, row0);
             break;
         case 4:
             if constexpr (NT >= 4)
-                return variant_phase<4>(sh, p, vring, slot, t0, n_chunks, i_stage, red, rs, warp, g, q, row0);
+                return variant_phase<4>(sh, p, vring, slot, t0, n_chunks, i_stage, tmem_rows, rl0, g, q, row0);
             break;
         default: break;
     }
@@ -497,8 +498,6 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     __shared__ MultiShared sh;
     uint8_t* bring = align1024(dyn_raw);            // base ring (1024-byte aligned stages)
     uint8_t* vring = bring + kBaseStages * kBaseStage;
-    float* red = reinterpret_cast<float*>(vring + kVarStages * kVarSlot);  // per-token sums [128][Tpad + 1]
-    for (int o = threadIdx.x; o < kRows * kRedStride; o += kThreads) red[o] = 0.0f;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -523,11 +522,19 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
         sh.abort = 0;
         fence_mbarrier_init();
     }
+    for (int c = tid; c < kMaxVarTiles * 8; c += kThreads) sh.col2pos[c] = -1;
     if (warp == kBaseWarp) tmem_alloc(&sh.tmem_base, kTmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
+    // variant tensor-memory column of every routed token (padding columns stay -1)
+    if (tid < T && sh.rt.keyp[tid] >= 1) {
+        const int k = sh.rt.keyp[tid];
+        const int a = sh.rt.slot_of_key[k];
+        const int col = 8 * sh.rt.ptile[a] + (tid - sh.rt.seg[k]);
+        if (col < kMaxVarTiles * 8) sh.col2pos[col] = tid;
+    }
 
     const int n_act = sh.rt.n_act;
     const int nc = static_cast<int>(p.d_in / kChunk);
@@ -634,40 +641,59 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
         }
     } else {
         // ------------------------------------------------------------ consumer warps: variant phases
+        // warp w owns rows 32 (w % 4) + 16 (w / 4) .. + 15: inside its tensor-memory lane quarter
+        const int rl0 = 32 * (warp & 3) + 16 * (warp >> 2);
+        const uint32_t tmem_rows = tmem + (static_cast<uint32_t>(rl0) << 16);
         int i = 0;
         bool ok = true;
         for (int a = 0; a < n_act && ok; ++a) {
             const int len = sh.rt.len[a];
             for (int t0 = 0; t0 < len && ok; t0 += kPhaseTiles) {
                 const int L = len - t0 < kPhaseTiles ? len - t0 : kPhaseTiles;
-                ok = run_phase<NT>(L, sh, p, vring, a, t0, n_chunks, i, red, kRedStride, warp, g, q, row0);
+                ok = run_phase<NT>(L, sh, p, vring, a, t0, n_chunks, i, tmem_rows, rl0, g, q, row0);
             }
         }
     }
 
     // ---------------------------------------------------------------- epilogue
-    // 1. add the tensor-memory base sums (column = caller token) into the
-    //    per-token sums (column = sorted position)
+    // 1. per-token sums of this CTA's slice, gathered from tensor memory into
+    //    shared memory (the variant ring is free): base columns (caller token
+    //    order) plus variant tile columns (alpha * 2M), by sorted position
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
     const Routing& rt = sh.rt;
+    float* red = reinterpret_cast<float*>(vring);  // [128][Tpad + 1]
     if (warp < 4) {
         const bool base_ok = __all_sync(0xffffffffu, wait_or_abort(sh.abort, &sh.accum, 0u, p.err));
         tc_fence_after();
+        const int row = 32 * warp + lane;  // tensor-memory lane = local row
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+        for (int pos = 0; pos < Tpad; ++pos) red[row * kRedStride + pos] = 0.0f;
         if (base_ok) {
-            const int row = 32 * warp + lane;  // tensor-memory lane = local row
 #pragma unroll
             for (int cb = 0; cb < (Tpad + 31) / 32; ++cb) {
                 uint32_t d[32];
-                tmem_ld32(tmem + (static_cast<uint32_t>(32 * warp) << 16) + 32 * cb, d);
+                tmem_ld32(lane_addr + 32 * cb, d);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     const int t = 32 * cb + j;
-                    if (t < T) red[row * kRedStride + rt.invp[t]] += __uint_as_float(d[j]);
+                    if (t < T) red[row * kRedStride + rt.invp[t]] = __uint_as_float(d[j]);
                 }
             }
         }
+        const int vcols = 8 * (rt.n_ptiles < kMaxVarTiles ? rt.n_ptiles : kMaxVarTiles);
+        for (int cb = 0; cb < vcols; cb += 32) {
+            uint32_t d[32];
+            tmem_ld32(lane_addr + kVarCol + cb, d);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int pos = cb + j < vcols ? sh.col2pos[cb + j] : -1;
+                if (pos >= 0) red[row * kRedStride + pos] += __uint_as_float(d[j]);
+            }
+        }
     }
-    __syncthreads();  // every base MMA complete, every copy landed: the base ring is free
+    __syncthreads();  // every base MMA complete, every copy landed: both rings are free
     // 2. push the per-token sums to the owners of their rows (receive slots
     //    [CK][kRows / CK rows][Tpad + 1] in the base ring, free once every
     //    peer got here), then each owner adds its slots in rank order
@@ -750,6 +776,13 @@ int multi_max_ptiles(int T, int V)
     return (t + 7 * a) / 8;
 }
 
+int multi_group_tokens(int V)
+{
+    for (int g = kMaxTok; g > 8; g /= 2)
+        if (multi_max_ptiles(g, V) <= kMaxVarTiles) return g;
+    return 8;
+}
+
 int multi_corr_splits(int64_t d_in)
 {
     const int64_t nc = d_in / kChunk;
@@ -799,8 +832,12 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
     ck = ck < 1 ? 1 : ck > 4 ? 4 : ck;
     prm.CK = ck;
     const size_t base_stage = static_cast<size_t>(kWTile) + static_cast<size_t>(npad) * kHalfRowBytes;
-    const size_t red = static_cast<size_t>(kRows) * (8 * nt + 1) * sizeof(float);
-    const size_t smem = kBaseStages * base_stage + kVarStages * static_cast<size_t>(kVarSlot) + red + 1024;
+    const size_t red = static_cast<size_t>(kRows) * (8 * nt + 1) * sizeof(float);  // in the variant ring, after the phases
+    if (red > kVarStages * static_cast<size_t>(kVarSlot) ||
+        red > kBaseStages * base_stage)  // receive slots live in the base ring
+        return cudaErrorInvalidConfiguration;
+    if (multi_max_ptiles(T, a.V) > kMaxVarTiles) return cudaErrorInvalidValue;
+    const size_t smem = kBaseStages * base_stage + kVarStages * static_cast<size_t>(kVarSlot) + 1024;
 
     const dim3 prep_grid(static_cast<unsigned>(T + 7 * (T < a.V ? T : a.V)), static_cast<unsigned>(nsplit));
     multi_prepare_kernel<<<prep_grid, kPrepThreads, 0, stream>>>(a.x, a.vid, T, a.V, a.d_in, a.xp, a.corr, nsplit);

@@ -66,6 +66,19 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 16 lanes x 8 columns: thread t holds lane (t / 4) columns 2(t % 4), 2(t % 4) + 1
+// in v[0], v[1] and lane 8 + t / 4, same columns, in v[2], v[3] -- the layout of
+// an mma.sync m16n8 accumulator fragment.  The lane field of taddr is the first
+// of the 16 lanes (inside the warp's lane quarter).  No wait.
+__device__ __forceinline__ void tmem_st_16x256b(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3)
+{
+    asm volatile("tcgen05.st.sync.aligned.16x256b.x1.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(v0), "r"(v1),
+                 "r"(v2), "r"(v3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32])
 {
     asm volatile(
