@@ -56,7 +56,7 @@ NCU_TRAFFIC = {
     ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_613_184 + 7_913_728),
     ("prefill_kernel", "prefill"): ("d0586c42d68bd685", "bd_prefill.cu", 613_019_648 + 63_200_000),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
-    ("multi_prepare + multi_kernel<8>", "multi"): ("96224eb073ec9f37", "bd_multi.cu", 255_510_016 + 3_557_120),
+    ("multi_prepare + multi_kernel<8>", "multi"): ("263453c7fac72f70", "bd_multi.cu", 256_120_064 + 3_429_632),
 }
 
 

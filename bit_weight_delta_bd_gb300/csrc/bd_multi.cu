@@ -67,8 +67,8 @@ constexpr int kChunk = 128;                   // d_in columns per chunk
 constexpr int kHalfRowBytes = 128;            // 64 bf16 columns: one 128-byte swizzle atom
 constexpr int kWTile = kRows * kHalfRowBytes; // W_base box [128 rows x 64 columns] = 16 KB
 constexpr int kBaseStages = 2;
-constexpr int kVarStages = 4;
-constexpr int kVarSlot = 15 * 1024;
+constexpr int kVarStages = 3;
+constexpr int kVarSlot = 20 * 1024;
 constexpr int kSignChunk = kRows * 16;        // 4 sign words x 128 rows = 2 KB
 constexpr int kPadTile = 8 * kChunk * 2;      // one 8-token tile of one chunk = 2 KB
 constexpr int kMaxTok = kSkinnyMaxTokens;
