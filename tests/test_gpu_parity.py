@@ -319,6 +319,65 @@ def test_multi_exact_routing_signature(dev, V, T):
     assert np.array_equal(y.cpu().numpy().astype(np.float64), y_ref)
 
 
+def _multi_case(dev, seed, V, d_out, d_in, vid, per_row=True, f32=True):
+    """Runs bd_linear_multi on dyadic inputs (every partial sum exact in fp32,
+    so the result must equal the fp64 oracle bit for bit) and compares."""
+    T = len(vid)
+    wb, wfs, x = _dyadic_multi(seed, V, d_out, d_in, T)
+    refs = [oracle.compress(wb, wf, per_row=per_row) for wf in wfs]
+    y_ref = oracle.linear_multi(x, np.asarray(vid, np.int32), [r[0] for r in refs], [r[1] for r in refs],
+                                per_row, wb)
+    wb_d = to_dev(wb, dev)
+    mode = PR if per_row else PM
+    s_l, a_l = zip(*[gpu_compress(wb_d, to_dev(wf, dev), mode, dev) for wf in wfs])
+    y = torch.empty((T, d_out), dtype=torch.float32 if f32 else torch.bfloat16, device=dev)
+    ws = bd.new_workspace(bd.bd_linear_multi_workspace_size(T, V, d_out, d_in), dev)
+    bd.bd_linear_multi(to_dev(x, dev), to_dev(np.asarray(vid, np.int32), dev), list(s_l), list(a_l), mode, wb_d, y, ws)
+    assert bd.bd_check_async(ws) == bd.BD_OK
+    if f32:
+        assert np.array_equal(y.cpu().numpy().astype(np.float64), y_ref)
+    else:
+        check_linear(y_host(y), y_ref, bf16_out=True, what="multi bf16")
+
+
+@pytest.mark.parametrize("d_in", [128, 384, 640, 4096])
+def test_multi_partial_stages(dev, d_in):
+    """d_in slices whose chunk count is not a multiple of the stage size (the
+    stages' chunk loop takes its runtime path), and a single-chunk d_in."""
+    vid = [0, 1, 2, -1, 1, 0, 3, 3, 2, 1, 0, 0, 4, -1, 2, 1]
+    _multi_case(dev, 11 + d_in, 5, 70, d_in, vid)
+
+
+@pytest.mark.parametrize("n_heavy", [33, 40, 64])
+def test_multi_variant_with_many_tokens(dev, n_heavy):
+    """One variant with more than 32 tokens: its 5..8 padded tiles run as two
+    phases (at most 4 tiles each)."""
+    rng = np.random.default_rng(n_heavy)
+    vid = np.full(64, 2, np.int32)
+    others = rng.choice(64, 64 - n_heavy, replace=False)
+    vid[others] = rng.integers(-1, 4, size=len(others))
+    vid[others[vid[others] == 2]] = 1
+    _multi_case(dev, 100 + n_heavy, 4, 160, 512, vid.tolist())
+
+
+@pytest.mark.parametrize("V", [24, 30, 64])
+def test_multi_many_variants_small_groups(dev, V):
+    """Many variants: token groups shrink so that no group needs more padded
+    tiles than tensor memory holds; 64 tokens over V variants."""
+    rng = np.random.default_rng(V)
+    vid = rng.integers(-1, V, size=64).astype(np.int32)
+    _multi_case(dev, 200 + V, V, 129, 256, vid.tolist())
+
+
+@pytest.mark.parametrize("T", [1, 7, 8, 9, 17, 33, 63])
+def test_multi_token_counts(dev, T):
+    """Token counts at and around the 8/16/32/64 tile boundaries, per-matrix
+    alpha, bf16 output, ragged d_out."""
+    rng = np.random.default_rng(T)
+    vid = rng.integers(-1, 6, size=T).astype(np.int32)
+    _multi_case(dev, 300 + T, 6, 200, 1024, vid.tolist(), per_row=False, f32=False)
+
+
 def test_multi_bad_variant_flagged_and_computed_as_base(dev):
     V, d_out, d_in, T = 3, 20, 256, 12
     wb, wfs, x = _dyadic_multi(9, V, d_out, d_in, T)
