@@ -547,8 +547,9 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
         // x . W_base^T on the tensor cores, concurrently with the variant
         // phases: 64-column stages of W_base [128 x 64] and x [Npad x 64]
         // (caller token order), tcgen05.mma M = 128, N = Npad, K = 16, fp32
-        // accumulator in tensor memory; a stage is refilled once the MMAs
-        // reading it completed.
+        // accumulator in tensor memory.  A slot is refilled as soon as the MMAs
+        // reading it complete (a few hundred cycles after they are issued), so
+        // that kBaseStages - 1 stages stay in flight while the next one lands.
         if (lane == 0) {
             const int nk = 2 * n_chunks;
             int issued = 0, done = 0;
@@ -575,11 +576,9 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
                            (k | kk) != 0 ? 1u : 0u);
                 mma_commit(&sh.empty_b[s]);
                 ++done;
-                // refill the slot of the previous stage once its MMAs are done
-                if (k >= 1 && issued < nk) {
-                    const int sp = (k - 1) % kBaseStages;
-                    if (!wait_or_abort(sh.abort, &sh.empty_b[sp], static_cast<uint32_t>((k - 1) / kBaseStages) & 1u,
-                                       p.err))
+                // stage k + kBaseStages into this slot once its MMAs are done
+                if (issued < nk) {
+                    if (!wait_or_abort(sh.abort, &sh.empty_b[s], static_cast<uint32_t>(k / kBaseStages) & 1u, p.err))
                         break;
                     issue(issued++);
                 }
@@ -658,7 +657,10 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     // ---------------------------------------------------------------- epilogue
     // 1. per-token sums of this CTA's slice, gathered from tensor memory into
     //    shared memory (the variant ring is free): base columns (caller token
-    //    order) plus variant tile columns (alpha * 2M), by sorted position
+    //    order) plus variant tile columns (alpha * 2M), by sorted position.
+    //    The indices (and, for the variant columns, the current sums) of a
+    //    block of columns are all loaded before its first store, so that the
+    //    loads overlap instead of each waiting for the store before it.
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -668,43 +670,60 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
         const bool base_ok = __all_sync(0xffffffffu, wait_or_abort(sh.abort, &sh.accum, 0u, p.err));
         tc_fence_after();
         const int row = 32 * warp + lane;  // tensor-memory lane = local row
+        float* rr = red + row * kRedStride;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * warp) << 16);
-        for (int pos = 0; pos < Tpad; ++pos) red[row * kRedStride + pos] = 0.0f;
         if (base_ok) {
+            // every sorted position below T is written: invp is a bijection
 #pragma unroll
             for (int cb = 0; cb < (Tpad + 31) / 32; ++cb) {
                 uint32_t d[32];
                 tmem_ld32(lane_addr + 32 * cb, d);
+                int ip[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int t = 32 * cb + j;
-                    if (t < T) red[row * kRedStride + rt.invp[t]] = __uint_as_float(d[j]);
-                }
+                for (int j = 0; j < 32; ++j) ip[j] = 32 * cb + j < T ? rt.invp[32 * cb + j] : -1;
+#pragma unroll
+                for (int j = 0; j < 32; ++j)
+                    if (ip[j] >= 0) rr[ip[j]] = __uint_as_float(d[j]);
             }
+        } else {
+            for (int pos = 0; pos < Tpad; ++pos) rr[pos] = 0.0f;
         }
         const int vcols = 8 * (rt.n_ptiles < kMaxVarTiles ? rt.n_ptiles : kMaxVarTiles);
         for (int cb = 0; cb < vcols; cb += 32) {
             uint32_t d[32];
             tmem_ld32(lane_addr + kVarCol + cb, d);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int pos = cb + j < vcols ? sh.col2pos[cb + j] : -1;
-                if (pos >= 0) red[row * kRedStride + pos] += __uint_as_float(d[j]);
+            for (int h = 0; h < 32; h += 16) {
+                int pc[16];
+                float cur[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) pc[j] = cb + h + j < vcols ? sh.col2pos[cb + h + j] : -1;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) cur[j] = pc[j] >= 0 ? rr[pc[j]] : 0.0f;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (pc[j] >= 0) rr[pc[j]] = cur[j] + __uint_as_float(d[h + j]);
             }
         }
     }
     __syncthreads();  // every base MMA complete, every copy landed: both rings are free
     // 2. push the per-token sums to the owners of their rows (receive slots
-    //    [CK][kRows / CK rows][Tpad + 1] in the base ring, free once every
-    //    peer got here), then each owner adds its slots in rank order
+    //    [CK][kRows / CK rows][kRecvStride] in the base ring, free once every
+    //    peer got here) as 16-byte stores, then each owner adds its slots in
+    //    rank order.  Columns T..Tpad-1 carry unused values.
+    constexpr int kRecvStride = Tpad + 4;           // 16-byte aligned rows
+    constexpr int kQuads = Tpad / 4;                // float4 per row (a power of two)
     float* recv = reinterpret_cast<float*>(bring);
-    const int nr = kRows / CK;
+    const int nr = kRows / CK;                      // CK is 1, 2 or 4
+    const int lnr = CK == 1 ? 7 : CK == 2 ? 6 : 5;  // log2(nr)
     cluster.sync();
-    for (int o = tid; o < kRows * T; o += kThreads) {
-        const int r = o / T, pos = o % T;
-        const int owner = r / nr;
+    for (int o = tid; o < kRows * kQuads; o += kThreads) {
+        const int r = o / kQuads, c4 = 4 * (o % kQuads);
+        const int owner = r >> lnr;
+        const float* src = red + r * kRedStride + c4;
+        const float4 v = make_float4(src[0], src[1], src[2], src[3]);
         float* dst = cluster.map_shared_rank(recv, owner);
-        dst[(rank * nr + (r - owner * nr)) * kRedStride + pos] = red[r * kRedStride + pos];
+        *reinterpret_cast<float4*>(dst + (rank * nr + (r - (owner << lnr))) * kRecvStride + c4) = v;
     }
     __syncthreads();  // red is read above before it is reused below
     // per-token corrections and per-row alphas of this rank's rows, staged in red
@@ -716,17 +735,17 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
         corr_s[tid] = c;
     }
     for (int o = tid; o < n_act * nr; o += kThreads) {
-        const int a = o / nr, r = o % nr;
+        const int a = o >> lnr, r = o & (nr - 1);
         const int64_t row = row0 + rank * nr + r;
         alpha_s[o] = row < p.d_out ? p.alpha[rt.act[a]][p.per_row ? row : 0] : 0.0f;
     }
     cluster.sync();
     for (int o = tid; o < nr * T; o += kThreads) {
-        const int pos = o / nr, r = o % nr;
+        const int pos = o >> lnr, r = o & (nr - 1);
         const int64_t row = row0 + rank * nr + r;
         if (row >= p.d_out) continue;
         float y = 0.0f;
-        for (int k = 0; k < CK; ++k) y += recv[(k * nr + r) * kRedStride + pos];
+        for (int k = 0; k < CK; ++k) y += recv[(k * nr + r) * kRecvStride + pos];
         const int key = rt.keyp[pos];
         if (key >= 1) y = fmaf(-alpha_s[rt.slot_of_key[key] * nr + r], corr_s[pos], y);
         const int64_t idx = static_cast<int64_t>(rt.perm[pos]) * p.d_out + row;
@@ -826,15 +845,15 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
                        static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, 64,
                        static_cast<uint32_t>(npad), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    // K slices per cluster: a function of d_in only (one per 2048 columns, at most 4)
+    // K slices per cluster: a function of d_in only (one per 2048 columns,
+    // rounded down to 1, 2 or 4 so that every slice owns kRows / CK rows)
     const int nc = static_cast<int>(a.d_in / kChunk);
-    int ck = nc / 16;
-    ck = ck < 1 ? 1 : ck > 4 ? 4 : ck;
+    const int ck = nc >= 64 ? 4 : nc >= 32 ? 2 : 1;
     prm.CK = ck;
     const size_t base_stage = static_cast<size_t>(kWTile) + static_cast<size_t>(npad) * kHalfRowBytes;
-    const size_t red = static_cast<size_t>(kRows) * (8 * nt + 1) * sizeof(float);  // in the variant ring, after the phases
-    if (red > kVarStages * static_cast<size_t>(kVarSlot) ||
-        red > kBaseStages * base_stage)  // receive slots live in the base ring
+    const size_t red = static_cast<size_t>(kRows) * (8 * nt + 1) * sizeof(float);   // in the variant ring
+    const size_t recv = static_cast<size_t>(kRows) * (8 * nt + 4) * sizeof(float);  // receive slots, base ring
+    if (red > kVarStages * static_cast<size_t>(kVarSlot) || recv > kBaseStages * base_stage)
         return cudaErrorInvalidConfiguration;
     if (multi_max_ptiles(T, a.V) > kMaxVarTiles) return cudaErrorInvalidValue;
     const size_t smem = kBaseStages * base_stage + kVarStages * static_cast<size_t>(kVarSlot) + 1024;

@@ -340,10 +340,12 @@ def _multi_case(dev, seed, V, d_out, d_in, vid, per_row=True, f32=True):
         check_linear(y_host(y), y_ref, bf16_out=True, what="multi bf16")
 
 
-@pytest.mark.parametrize("d_in", [128, 384, 640, 4096])
+@pytest.mark.parametrize("d_in", [128, 384, 640, 2176, 4096, 6144, 8320])
 def test_multi_partial_stages(dev, d_in):
     """d_in slices whose chunk count is not a multiple of the stage size (the
-    stages' chunk loop takes its runtime path), and a single-chunk d_in."""
+    stages' chunk loop takes its runtime path), a single-chunk d_in, and
+    chunk counts between the cluster-size steps (17, 48 and 65 chunks of 128
+    columns: one, two and four K slices of unequal length)."""
     vid = [0, 1, 2, -1, 1, 0, 3, 3, 2, 1, 0, 0, 4, -1, 2, 1]
     _multi_case(dev, 11 + d_in, 5, 70, d_in, vid)
 
