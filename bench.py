@@ -52,11 +52,11 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # smaller call of the same kernel and applied to the average launch.
 NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
-    ("skinny_kernel<1>", "decode"): ("626c1a5ceec5ed51", "bd_skinny.cu", 499_453_696 + 3_220_224),
+    ("skinny_kernel<1>", "decode"): ("60707ad3c65224a0", "bd_skinny.cu", 499_405_056 + 3_889_920),
     ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_613_184 + 7_913_728),
-    ("prefill_kernel", "prefill"): ("d0586c42d68bd685", "bd_prefill.cu", 613_019_648 + 63_200_000),
+    ("prefill_kernel", "prefill"): ("69cfd4fd49cfa372", "bd_prefill.cu", 613_093_632 + 62_800_384),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
-    ("multi_prepare + multi_kernel<8>", "multi"): ("263453c7fac72f70", "bd_multi.cu", 256_120_064 + 3_429_632),
+    ("multi_prepare + multi_kernel<8>", "multi"): ("17f4ad70d450ec79", "bd_multi.cu", 255_804_672 + 3_930_880),
 }
 
 

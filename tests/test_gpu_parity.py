@@ -350,6 +350,36 @@ def test_multi_partial_stages(dev, d_in):
     _multi_case(dev, 11 + d_in, 5, 70, d_in, vid)
 
 
+def test_multi_wide_range_activations(dev):
+    """Activations spanning 30 binades inside one token, an all-zero token, a
+    token with one huge element and a token of subnormal-range values (the
+    pre-scaled x operand of the recoded sign MMA stays exact for all of them):
+    every output stays within the fp32 bound."""
+    T, V, d_out, d_in = 12, 3, 96, 1024
+    rng = np.random.default_rng(77)
+    wb, wfs, _, _, _ = synth.multi_problem(77, d_out, d_in, T, V)
+    xf = rng.standard_normal((T, d_in)) * 2.0 ** rng.uniform(-20, 10, size=(T, d_in))
+    xf[1] = 0.0
+    xf[2] = rng.standard_normal(d_in) * 1e-3
+    xf[2, 17] = 3.0e4
+    xf[3] = rng.standard_normal(d_in) * 1e-38
+    x = synth.f32_to_bf16_bits(xf.astype(np.float32))
+    vid = np.array([0, 1, 2, 0, 1, 2, 0, 1, 2, -1, 0, 1], np.int32)
+    refs = [oracle.compress(wb, wf, per_row=True) for wf in wfs]
+    y_ref = oracle.linear_multi(x, vid, [r[0] for r in refs], [r[1] for r in refs], True, wb)
+    wb_d = to_dev(wb, dev)
+    s_l, a_l = zip(*[gpu_compress(wb_d, to_dev(wf, dev), PR, dev) for wf in wfs])
+    y = torch.empty((T, d_out), dtype=torch.float32, device=dev)
+    ws = bd.new_workspace(bd.bd_linear_multi_workspace_size(T, V, d_out, d_in), dev)
+    bd.bd_linear_multi(to_dev(x, dev), to_dev(vid, dev), list(s_l), list(a_l), PR, wb_d, y, ws)
+    assert bd.bd_check_async(ws) == bd.BD_OK
+    bound = fp32_bound_multi(x, wb, [r[1] for r in refs], vid, np.arange(d_out))
+    got = y.cpu().numpy().astype(np.float64)
+    assert np.all(np.isfinite(got))
+    assert np.all(np.abs(got - y_ref) <= bound), float(np.max(np.abs(got - y_ref) / bound))
+    assert np.array_equal(got[1], y_ref[1])  # an all-zero token gives exact zeros
+
+
 @pytest.mark.parametrize("n_heavy", [33, 40, 64])
 def test_multi_variant_with_many_tokens(dev, n_heavy):
     """One variant with more than 32 tokens: its 5..8 padded tiles run as two
