@@ -714,8 +714,8 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     constexpr int kRecvStride = Tpad + 4;           // 16-byte aligned rows
     constexpr int kQuads = Tpad / 4;                // float4 per row (a power of two)
     float* recv = reinterpret_cast<float*>(bring);
-    const int nr = kRows / CK;                      // CK is 1, 2 or 4
-    const int lnr = CK == 1 ? 7 : CK == 2 ? 6 : 5;  // log2(nr)
+    const int nr = kRows / CK;                      // CK is a power of two up to 8
+    const int lnr = 7 - (31 - __clz(CK));           // log2(nr)
     cluster.sync();
     for (int o = tid; o < kRows * kQuads; o += kThreads) {
         const int r = o / kQuads, c4 = 4 * (o % kQuads);
@@ -786,6 +786,20 @@ cudaError_t launch_nt(const MultiParams& prm, size_t smem, unsigned grid, cudaSt
 
 int tiles_for(int T) { return T <= 8 ? 1 : T <= 16 ? 2 : T <= 32 ? 4 : 8; }
 
+// SM count of the current device (cached per device).
+int sm_count()
+{
+    static std::atomic<int> sms[kHostMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kHostMaxDevices) return 1;
+    int n = sms[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 1;
+        sms[dev].store(n, std::memory_order_relaxed);
+    }
+    return n;
+}
+
 }  // namespace
 
 int multi_max_ptiles(int T, int V)
@@ -845,10 +859,16 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
                        static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, 64,
                        static_cast<uint32_t>(npad), CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    // K slices per cluster: a function of d_in only (one per 2048 columns,
-    // rounded down to 1, 2 or 4 so that every slice owns kRows / CK rows)
+    // K slices per cluster: one per 2048 columns of d_in, rounded down to a
+    // power of two (1, 2 or 4) so that every slice owns kRows / CK rows; for
+    // few row blocks (d_out = 1024: 8 blocks) doubled up to 8, the portable
+    // cluster size, while the grid is smaller than the SM count and every
+    // slice keeps at least 4 chunks
     const int nc = static_cast<int>(a.d_in / kChunk);
-    const int ck = nc >= 64 ? 4 : nc >= 32 ? 2 : 1;
+    int ck = nc >= 64 ? 4 : nc >= 32 ? 2 : 1;
+    const int64_t row_blocks = (a.d_out + kRows - 1) / kRows;
+    const int sms = sm_count();
+    while (ck < 8 && row_blocks * ck < sms && nc / (2 * ck) >= 4) ck *= 2;
     prm.CK = ck;
     const size_t base_stage = static_cast<size_t>(kWTile) + static_cast<size_t>(npad) * kHalfRowBytes;
     const size_t red = static_cast<size_t>(kRows) * (8 * nt + 1) * sizeof(float);   // in the variant ring
