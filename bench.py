@@ -60,13 +60,21 @@ NCU_TRAFFIC = {
 }
 
 
+# kernels each timed call launches: multi = prepare + fused kernel; multi_prefill =
+# router + plan + gather + grouped prefill; slice = 56 multi calls
+LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4}
+# workloads whose own figure is tensor throughput (TFLOP/s) rather than GB/s
+TENSOR_WORKLOADS = ("prefill", "multi_prefill")
+
+
 def parse_args():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill", "slice"], default="decode")
+    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill", "multi_prefill", "slice"],
+                   default="decode")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement of the decode line")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
@@ -134,11 +142,11 @@ class Workload:
             self.wf = [wf]
             self.xs = [x]
             self.vid = None
-        else:  # multi
+        else:  # multi (64 tokens, decode kernel) or multi_prefill (4096 tokens, tensor cores)
             d_out, d_in = 8192, 8192
-            self.tokens = [64]
+            self.tokens = [4096 if name == "multi_prefill" else 64]
             self.per_row = True
-            self.wb, self.wf, x, self.vid, _ = synth.multi_problem(seed, d_out, d_in, 64, 14)
+            self.wb, self.wf, x, self.vid, _ = synth.multi_problem(seed, d_out, d_in, self.tokens[0], 14)
             self.xs = [x]
         self.d_out, self.d_in = d_out, d_in
         self.n_alpha = d_out if self.per_row else 1
@@ -160,6 +168,13 @@ class Workload:
         elif self.name == "prefill":
             c["workload"] = "prefill_4096x8192x8192"
             c["step"] = "bd_linear at T=4096, one variant (compressed once, untimed); tensor-core path"
+            c["l2"] = "inputs larger than L2 (W_base 134 MB + x 67 MB + y 67 MB vs 126.5 MB L2)"
+        elif self.name == "multi_prefill":
+            c["workload"] = "multi_prefill_8192x8192_V14_T4096"
+            c["variants"] = len(self.wf)
+            c["active_variants"] = int(len(set(int(v) for v in self.vid)))
+            c["step"] = ("bd_linear_multi over 4096 Zipf(1.1)-routed tokens: router, gather, grouped tensor-core "
+                         "prefill (variants compressed once, untimed)")
             c["l2"] = "inputs larger than L2 (W_base 134 MB + x 67 MB + y 67 MB vs 126.5 MB L2)"
         elif self.name == "tiny":
             c["workload"] = "tiny_256x256_T4"
@@ -197,11 +212,11 @@ class GpuRun:
         self.ys = [torch.empty((T, wl.d_out), dtype=torch.bfloat16, device=dev) for T in wl.tokens]
         self.ws = bd.new_workspace(max(bd.bd_compress_workspace_size(wl.d_out, wl.d_in, PR),
                                        bd.bd_linear_workspace_size(64, wl.d_out, wl.d_in),
-                                       bd.bd_linear_multi_workspace_size(64, max(len(wl.wf), 1), wl.d_out,
-                                                                         wl.d_in)), dev)
+                                       bd.bd_linear_multi_workspace_size(max(64, max(wl.tokens)), max(len(wl.wf), 1),
+                                                                         wl.d_out, wl.d_in)), dev)
         self.vid = None if wl.vid is None else torch.from_numpy(wl.vid).to(dev)
         self.flush = None
-        if wl.name in ("multi", "prefill"):
+        if wl.name in ("multi", "prefill", "multi_prefill"):
             for v in range(len(wl.wf)):  # variants are compressed once, before timing
                 bd.bd_compress(self.wb, self.wf[v], PR, self.signs[v], self.alpha[v], self.ws)
             torch.cuda.synchronize()
@@ -214,13 +229,15 @@ class GpuRun:
         """[(label, kernel name, algorithmic bytes, flops, fn)] of one step."""
         bd, wl = self.bd, self.wl
         out = []
-        if wl.name == "multi":
+        if wl.name in ("multi", "multi_prefill"):
             active = sorted(set(int(v) for v in wl.vid if v >= 0))
             T = wl.tokens[0]
             nbytes = (2 * wl.d_out * wl.d_in + len(active) * (wl.d_out * wl.d_in // 8 + 4 * wl.n_alpha) +
                       2 * T * wl.d_in + 2 * T * wl.d_out + 4 * T)
-            out.append(("linear_multi_T64", "multi_prepare + multi_kernel<8>", nbytes,
-                        4 * T * wl.d_out * wl.d_in,
+            kname = ("route + gather + prefill_kernel (grouped)" if wl.name == "multi_prefill"
+                     else "multi_prepare + multi_kernel<8>")
+            flops = 2 * T * wl.d_out * wl.d_in if wl.name == "multi_prefill" else 4 * T * wl.d_out * wl.d_in
+            out.append((f"linear_multi_T{T}", kname, nbytes, flops,
                         lambda: bd.bd_linear_multi(self.xs[0], self.vid, self.signs, self.alpha, self.mode, self.wb,
                                                    self.ys[0], self.ws)))
             return out
@@ -429,6 +446,11 @@ def dist_setup():
     return world, rank, local
 
 
+def _step_flops(wl: Workload) -> int:
+    """Useful FLOPs of one step of a tensor-bound workload: 2 T d_out d_in per call."""
+    return sum(2 * T * wl.d_out * wl.d_in for T in wl.tokens)
+
+
 def run_reference(args):
     world, rank, _ = dist_setup()
     if rank != 0:
@@ -445,13 +467,18 @@ def run_reference(args):
         gbs, cores, sample = oracle_time(wl, budget_s=budget)
         vals.append(gbs)
     value = statistics.median(vals)
-    line = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference", "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_bytes / (value * 1e9) * 1e3,
+    ms_per_step = step_bytes / (value * 1e9) * 1e3
+    unit = "GB/s"
+    if wl.name in TENSOR_WORKLOADS:  # the same unit as the GPU arm's line
+        value = _step_flops(wl) / (ms_per_step * 1e-3) / 1e12
+        unit = "TFLOP/s"
+    line = {"metric": METRIC, "value": value, "unit": unit, "impl": "reference", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded numpy; shapes and distributions of the BitDelta serving setup)",
             "config": wl.config(),
-            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample},
-            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+            "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
@@ -545,7 +572,7 @@ def run_gpu(args):
     tr = NCU_TRAFFIC.get((dom, wl.name))
     if tr is not None and tr[0] == _src_sha(tr[1]):
         traffic = tr[2] * bytes_per_launch if isinstance(tr[2], float) else tr[2]
-    if wl.name == "prefill":
+    if wl.name in TENSOR_WORKLOADS:
         flops_per_launch = calls[0][3]
         tf = flops_per_launch / (avg_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
@@ -569,7 +596,7 @@ def run_gpu(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e["ms_per_step"] = float(t.item())
         e2e["value"] = world * step_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9
-        if wl.name == "prefill":
+        if wl.name in TENSOR_WORKLOADS:
             e2e["value"] = world * calls[0][3] / (e2e["ms_per_step"] * 1e-3) / 1e12
             e2e["unit"] = "TFLOP/s"
 
@@ -587,10 +614,13 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu and wl.name != "slice":
         gbs, cores, sample = oracle_time(wl)
         cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        if wl.name in TENSOR_WORKLOADS:  # in the line's own unit
+            cpu["value"] = _step_flops(wl) / (step_bytes / (gbs * 1e9)) / 1e12
+            cpu["unit"] = "TFLOP/s"
 
     if rank == 0:
         unit = "GB/s"
-        if wl.name == "prefill":  # this workload's own figure is tensor throughput
+        if wl.name in TENSOR_WORKLOADS:  # this workload's own figure is tensor throughput
             value = world * calls[0][3] / (ms_per_step * 1e-3) / 1e12
             unit = "TFLOP/s"
         line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -601,7 +631,7 @@ def run_gpu(args):
                 "tokens_per_s": world * tokens / (ms_per_step * 1e-3),
                 "frac_hbm_step": value / world / hbm_peak,
                 "roofline": roofline, "kernels": kernels, "prefill": prefill, "cpu_baseline": cpu, "e2e": e2e,
-                "clocks": clk, "gpu_launches": (2 if wl.name in ("multi", "slice") else 1) * len(calls) * args.steps}
+                "clocks": clk, "gpu_launches": LAUNCHES_PER_CALL.get(wl.name, 1) * len(calls) * args.steps}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
@@ -641,7 +671,7 @@ def run_e2e(run: GpuRun, calls, wl: Workload, steps: int, stream):
     are copied host -> device and results device -> host inside the timing."""
     torch = run.torch
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
-    if wl.name == "multi":
+    if wl.name in ("multi", "multi_prefill"):
         h_in = [(pin(run.xs[0]), run.xs[0]), (pin(run.vid), run.vid)]
         h_out = [(pin(run.ys[0]), run.ys[0])]
     elif wl.name == "slice":

@@ -225,11 +225,39 @@ MultiWs multi_ws_layout(int64_t T, int32_t V, int64_t d_in)
     return w;
 }
 
+// From this many tokens on, bd_linear_multi runs the grouped tensor-core
+// prefill (one 256-token block per variant segment piece) instead of the
+// decode kernel on 64-token groups: at 512 tokens over 14 variants the plan
+// has at most 17 blocks per row block against 8 decode groups that each
+// re-read W_base.
+constexpr int64_t kMultiPrefillMinT = 512;
+
+bool use_grouped_prefill(int64_t T) { return T >= kMultiPrefillMinT && bd::prefill_available(); }
+
+// Grouped prefill workspace: the error word, then the router's perm [T] and
+// seg_off [V + 2], the block plan and x in sorted order [T][d_in].
+struct GroupedWs {
+    size_t perm, seg, plan, xs, total;
+};
+
+GroupedWs grouped_ws_layout(int64_t T, int32_t V, int64_t d_in)
+{
+    const auto up = [](size_t n) { return (n + 255) & ~static_cast<size_t>(255); };
+    GroupedWs w{};
+    w.perm = 1024;
+    w.seg = w.perm + up(static_cast<size_t>(T) * 4);
+    w.plan = w.seg + up(static_cast<size_t>(V + 2) * 4);
+    w.xs = w.plan + up(static_cast<size_t>(bd::grouped_prefill_blocks(T, V)) * 16);
+    w.total = w.xs + up(static_cast<size_t>(T) * static_cast<size_t>(d_in) * 2);
+    return w;
+}
+
 }  // namespace
 
 size_t bd_linear_multi_workspace_size(int64_t T, int32_t V, int64_t /*d_out*/, int64_t d_in)
 {
     if (T < 0 || d_in < 0 || V < 1 || V > BD_MAX_VARIANTS) return kWsHeader;
+    if (use_grouped_prefill(T)) return grouped_ws_layout(T, V, d_in).total;
     return multi_ws_layout(T, V, d_in).total;
 }
 
@@ -259,6 +287,34 @@ bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int3
     int sms = 0;
     if (bd_status s = device_info(&sms)) return s;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (use_grouped_prefill(T)) {
+        if (T > INT32_MAX) return BD_ERR_UNSUPPORTED_SHAPE;
+        const GroupedWs lay = grouped_ws_layout(T, V, d_in);
+        char* w = static_cast<char*>(ws);
+        bd::GroupedPrefillArgs g{};
+        g.x = x;
+        g.perm = reinterpret_cast<int32_t*>(w + lay.perm);
+        g.seg_off = reinterpret_cast<int32_t*>(w + lay.seg);
+        g.w_base = w_base;
+        for (int v = 0; v < V; ++v) {
+            g.signs[v] = signs_tab[v];
+            g.alpha[v] = alpha_tab[v];
+        }
+        g.V = V;
+        g.per_row = alpha_mode == BD_ALPHA_PER_ROW;
+        g.T = T;
+        g.d_out = d_out;
+        g.d_in = d_in;
+        g.y = y;
+        g.out_f32 = out_dtype == BD_OUT_F32;
+        g.err = err_word(ws);
+        g.xs = reinterpret_cast<uint16_t*>(w + lay.xs);
+        g.plan = reinterpret_cast<int4*>(w + lay.plan);
+        if (bd_status s = launched(bd::launch_route(vid, T, V, reinterpret_cast<int32_t*>(w + lay.perm),
+                                                    reinterpret_cast<int32_t*>(w + lay.seg), g.err, st)))
+            return s;
+        return launched(bd::launch_prefill_grouped(g, st));
+    }
     const size_t ysz = out_dtype == BD_OUT_F32 ? 4 : 2;
     const int64_t group = bd::multi_group_tokens(V);
     const MultiWs lay = multi_ws_layout(T, V, d_in);

@@ -93,4 +93,27 @@ struct PrefillArgs {
 bool prefill_available();
 cudaError_t launch_prefill(const PrefillArgs& a, int sm_count, cudaStream_t stream);
 
+// Multi-variant prefill on the tensor cores: tokens routed by bd_route's
+// perm / seg_off, x gathered into sorted order, one prefill tile per
+// (256-token block inside one variant's segment, 128 rows).
+struct GroupedPrefillArgs {
+    const uint16_t* x;            // [T][d_in] caller order
+    const int32_t* perm;          // [T] sorted position -> caller token (bd_route)
+    const int32_t* seg_off;       // [V + 2] (bd_route)
+    const uint16_t* w_base;       // [d_out][d_in]
+    const uint32_t* signs[kMaxVariants];
+    const float* alpha[kMaxVariants];
+    int V, per_row;
+    int64_t T, d_out, d_in;
+    void* y;                      // [T][d_out] caller order
+    int out_f32;
+    uint32_t* err;
+    uint16_t* xs;                 // scratch [T][d_in]: x in sorted order
+    int4* plan;                   // scratch [grouped_prefill_blocks(T, V)]
+};
+
+// Upper bound of the 256-token blocks of a grouped prefill: ceil(T / 256) + V + 1.
+int grouped_prefill_blocks(int64_t T, int V);
+cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t stream);
+
 }  // namespace bd

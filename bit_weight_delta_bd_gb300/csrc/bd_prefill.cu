@@ -26,9 +26,18 @@
 // sees the W and x tiles written once by TMA, W read once by the transform
 // and x read once by the tensor core.
 //
+// Grouped form (multi-variant prefill, bd_linear_multi with large T): x is
+// gathered into token order sorted by variant (key = vid + 1), and each
+// 256-token block of the grid lies inside one key's segment, listed by a
+// plan of {first token, segment end, key}.  A block builds W_eff with its
+// key's signs and alpha (alpha = 0 for key 0, the base model: W_eff = W_base
+// exactly) and writes only the rows of its own segment, in caller order.
+//
 // Every mbarrier wait is bounded; a timeout sets the error word, stops every
 // role at its next wait, drains the copies in flight, waits for the issued
 // MMAs and frees tensor memory.
+#include <type_traits>
+
 #include "bd_device.cuh"
 #include "bd_tcgen05.cuh"
 #include "bd_tma.h"
@@ -60,6 +69,16 @@ struct PrefillParams {
     int per_row, out_f32;
 };
 
+// Multi-variant prefill: the single-variant fields describe the gathered x
+// (x_map over [T][d_in] in sorted order), W_base and y; the sign maps and
+// alphas are per variant, the plan and the permutation come from the router.
+struct GroupedPrefillParams : PrefillParams {
+    const int4* plan;                     // [grid.x] {first token, segment end, key, valid}
+    const int32_t* perm;                  // sorted position -> caller token
+    const float* alphas[kMaxVariants];
+    CUtensorMap s_maps[kMaxVariants];     // [d_out][d_in/32] u32 per variant, box 4 x 128
+};
+
 struct PrefillShared {
     uint64_t full[kStages];   // TMA landed
     uint64_t afull[kStages];  // transform wrote the A stage (8 warp arrivals)
@@ -89,14 +108,26 @@ __device__ __forceinline__ bool pwait(PrefillShared& sh, uint64_t* bar, uint32_t
     return true;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ PrefillParams p)
+template <class P>
+__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ P p)
 {
+    constexpr bool kGrouped = std::is_same<P, GroupedPrefillParams>::value;
     extern __shared__ uint8_t dyn_raw[];
     __shared__ PrefillShared sh;
     uint8_t* dyn = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t tok0 = static_cast<int64_t>(blockIdx.x) * BN;
+    int64_t tok0 = static_cast<int64_t>(blockIdx.x) * BN, tok_end = p.T;
+    const CUtensorMap* s_map = &p.s_map;
+    const float* alpha = p.alpha;
+    if constexpr (kGrouped) {
+        const int4 b = p.plan[blockIdx.x];
+        if (b.w == 0) return;  // past the plan: the whole CTA leaves before any setup
+        tok0 = b.x;
+        tok_end = b.y;
+        s_map = &p.s_maps[b.z >= 1 ? b.z - 1 : 0];
+        alpha = b.z >= 1 ? p.alphas[b.z - 1] : nullptr;  // key 0: alpha = 0, W_eff = W_base
+    }
     const int64_t row0 = static_cast<int64_t>(blockIdx.y) * BM;
     const int nk = static_cast<int>(p.d_in / BK);
 
@@ -128,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
                 tma_load_2d(st, &p.x_map, i * BK, static_cast<int>(tok0), &sh.full[s]);
                 tma_load_2d(st + kXBytes, &p.w_map, i * BK, static_cast<int>(row0), &sh.full[s]);
-                tma_load_2d(st + kXBytes + kWBytes, &p.s_map, 4 * (i / 2), static_cast<int>(row0), &sh.full[s]);
+                tma_load_2d(st + kXBytes + kWBytes, s_map, 4 * (i / 2), static_cast<int>(row0), &sh.full[s]);
                 ++issued;
             }
             // copies still in flight must land before the CTA ends
@@ -143,6 +174,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
+            // a grouped block shorter than BN tokens (a segment's tail) runs its
+            // MMAs with N = its token count rounded up to 16 (M = 128 takes N in
+            // steps of 16); the x rows past N are loaded but not multiplied
+            uint32_t idesc = kIdesc;
+            if constexpr (kGrouped) {
+                const int n = tok_end - tok0 < BN ? static_cast<int>(tok_end - tok0) : BN;
+                idesc = idesc_bf16_f32(BM, (n + 15) / 16 * 16);
+            }
             int done = 0;
             for (int i = 0; i < nk; ++i) {
                 const int s = i % kStages;
@@ -152,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
                     mma_ts(tmem + kDCol, tmem + kACol + 32 * s + 8 * kk, bdesc + static_cast<uint64_t>(2 * kk),
-                           kIdesc, (i | kk) != 0 ? 1u : 0u);
+                           idesc, (i | kk) != 0 ? 1u : 0u);
                 mma_commit(&sh.empty[s]);
                 ++done;
             }
@@ -169,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         const int rl = 32 * quarter + lane;
         const int64_t row = row0 + rl;
         float a = 0.0f;
-        if (row < p.d_out) a = p.alpha[p.per_row ? row : 0];
+        if (alpha && row < p.d_out) a = alpha[p.per_row ? row : 0];
         const uint32_t ab = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a)));
         const uint32_t neg = ((ab << 16) | ab) ^ 0x80008000u;  // (-alpha, -alpha) as bf16x2
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
@@ -221,8 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                 if (row < p.d_out) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const int64_t t = tok0 + 32 * cb + j;
-                        if (t < p.T) {
+                        int64_t t = tok0 + 32 * cb + j;
+                        if (t < tok_end) {
+                            if constexpr (kGrouped) t = p.perm[t];
                             const float val = __uint_as_float(d[j]);
                             if (p.out_f32)
                                 static_cast<float*>(p.y)[t * p.d_out + row] = val;
@@ -270,10 +310,83 @@ cudaError_t launch_prefill(const PrefillArgs& a, int /*sm_count*/, cudaStream_t 
     prm.out_f32 = a.out_f32;
     const size_t smem = static_cast<size_t>(kStages) * kStageBytes + 1024;
     static std::atomic<size_t> smem_set[kHostMaxDevices];
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel), smem, smem_set);
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel<PrefillParams>), smem, smem_set);
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>((a.T + BN - 1) / BN), static_cast<unsigned>((a.d_out + BM - 1) / BM));
-    prefill_kernel<<<grid, kThreads, smem, stream>>>(prm);
+    prefill_kernel<PrefillParams><<<grid, kThreads, smem, stream>>>(prm);
+    return cudaGetLastError();
+}
+
+namespace {
+
+// One thread: the plan of 256-token blocks, each inside one key's segment
+// [seg_off[k], seg_off[k + 1]) of the sorted tokens; entries past the plan
+// are marked invalid (their CTAs leave at once).
+__global__ void prefill_plan_kernel(const int32_t* __restrict__ seg_off, int V, int nblk, int4* __restrict__ plan)
+{
+    if (threadIdx.x != 0 || blockIdx.x != 0) return;
+    int n = 0;
+    for (int k = 0; k <= V; ++k) {
+        const int a = seg_off[k], e = seg_off[k + 1];
+        for (int t = a; t < e && n < nblk; t += BN) plan[n++] = make_int4(t, e, k, 1);
+    }
+    for (; n < nblk; ++n) plan[n] = make_int4(0, 0, 0, 0);
+}
+
+// xs[i] = x[perm[i]]: one block per sorted row, 16-byte copies (d_in % 8 == 0).
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int64_t d_in,
+                                   uint16_t* __restrict__ xs)
+{
+    const int64_t i = blockIdx.x;
+    const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(perm[i]) * d_in);
+    uint4* dst = reinterpret_cast<uint4*>(xs + i * d_in);
+    for (int64_t c = threadIdx.x; c < d_in / 8; c += blockDim.x) dst[c] = src[c];
+}
+
+}  // namespace
+
+int grouped_prefill_blocks(int64_t T, int V) { return static_cast<int>((T + BN - 1) / BN) + V + 1; }
+
+cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t stream)
+{
+    if (a.V < 1 || a.V > kMaxVariants || a.T < 1) return cudaErrorInvalidValue;
+    static thread_local GroupedPrefillParams prm;  // ~9 KB: kept off the stack
+    if (!encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.xs, static_cast<uint64_t>(a.d_in),
+                       static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, BK, BN,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tma_2d(&prm.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
+                       static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, BK, BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    for (int v = 0; v < a.V; ++v) {
+        prm.alphas[v] = a.alpha[v];
+        if (!encode_tma_2d(&prm.s_maps[v], CU_TENSOR_MAP_DATA_TYPE_UINT32, a.signs[v],
+                           static_cast<uint64_t>(a.d_in / 32), static_cast<uint64_t>(a.d_out),
+                           static_cast<uint64_t>(a.d_in / 8), 4, BM, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+    prm.s_map = prm.s_maps[0];
+    prm.alpha = nullptr;
+    prm.y = a.y;
+    prm.err = a.err;
+    prm.T = a.T;
+    prm.d_out = a.d_out;
+    prm.d_in = a.d_in;
+    prm.per_row = a.per_row;
+    prm.out_f32 = a.out_f32;
+    prm.plan = a.plan;
+    prm.perm = a.perm;
+    const int nblk = grouped_prefill_blocks(a.T, a.V);
+    prefill_plan_kernel<<<1, 32, 0, stream>>>(a.seg_off, a.V, nblk, a.plan);
+    gather_rows_kernel<<<static_cast<unsigned>(a.T), 256, 0, stream>>>(a.x, a.perm, a.d_in, a.xs);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const size_t smem = static_cast<size_t>(kStages) * kStageBytes + 1024;
+    static std::atomic<size_t> smem_set[kHostMaxDevices];
+    e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel<GroupedPrefillParams>), smem, smem_set);
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(nblk), static_cast<unsigned>((a.d_out + BM - 1) / BM));
+    prefill_kernel<GroupedPrefillParams><<<grid, kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }
 

@@ -350,6 +350,61 @@ def test_multi_partial_stages(dev, d_in):
     _multi_case(dev, 11 + d_in, 5, 70, d_in, vid)
 
 
+def test_multi_prefill_4096_tokens_sampled_rows(dev, multi_problem):
+    """Multi-tenant prefill: 4096 Zipf-routed tokens (40 of them base-model
+    tokens) over the 14 variants of the multi-tenant workload take the grouped
+    tensor-core path; sampled rows against the oracle, bf16 and fp32 output."""
+    wb, wfs, _, _, _ = multi_problem
+    rng = np.random.default_rng(21)
+    T, V = 4096, len(wfs)
+    vid = synth.zipf_variant_ids(rng, T, V)
+    vid[rng.choice(T, 40, replace=False)] = -1
+    x = synth.activations(rng, T, 8192)
+    rows = synth.sample_rows(23, 8192, 32)
+    refs = [oracle.compress_rows(wb, wf, rows) for wf in wfs]
+    s_full, a_full = [], []
+    for s_rows, a_rows in refs:
+        sf = np.zeros((8192, 256), np.uint32)
+        af = np.zeros(8192, np.float32)
+        sf[rows], af[rows] = s_rows, a_rows
+        s_full.append(sf)
+        a_full.append(af)
+    y_ref = oracle.linear_multi(x, vid, s_full, a_full, True, wb, rows=rows)
+    wb_d = to_dev(wb, dev)
+    s_l, a_l = zip(*[gpu_compress(wb_d, to_dev(wf, dev), PR, dev) for wf in wfs])
+    x_d, vid_d = to_dev(x, dev), to_dev(vid, dev)
+    ws = bd.new_workspace(bd.bd_linear_multi_workspace_size(T, V, 8192, 8192), dev)
+    for f32 in (False, True):
+        y = torch.empty((T, 8192), dtype=torch.float32 if f32 else torch.bfloat16, device=dev)
+        bd.bd_linear_multi(x_d, vid_d, list(s_l), list(a_l), PR, wb_d, y, ws)
+        assert bd.bd_check_async(ws) == bd.BD_OK
+        check_linear(y_host(y)[:, rows], y_ref, bf16_out=not f32, what=f"multi prefill f32={f32}")
+
+
+def _sized_vid(rng, sizes):
+    """Token ids with exactly sizes[k] tokens of key k (key 0 = base model, id -1), shuffled."""
+    vid = np.concatenate([np.full(n, k - 1, np.int32) for k, n in enumerate(sizes)])
+    return vid[rng.permutation(len(vid))]
+
+
+@pytest.mark.parametrize("case", ["random", "block_edges", "one_variant", "all_base"])
+def test_multi_prefill_exact(dev, case):
+    """Grouped tensor-core prefill on dyadic inputs: exact against the oracle.
+    Segments of 1, 255, 256 and 257 tokens (blocks ending at, before and after
+    a 256-token boundary), a single variant, and a batch of base-model tokens
+    only; ragged d_out."""
+    rng = np.random.default_rng(len(case))
+    if case == "random":
+        V, vid = 5, rng.integers(-1, 5, size=700).astype(np.int32)
+    elif case == "block_edges":
+        V, vid = 4, _sized_vid(rng, [331, 256, 257, 1, 255])
+    elif case == "one_variant":
+        V, vid = 1, np.zeros(512, np.int32)
+    else:
+        V, vid = 14, np.full(600, -1, np.int32)
+    _multi_case(dev, 400 + len(vid), V, 200, 512, vid.tolist())
+
+
 def test_multi_wide_range_activations(dev):
     """Activations spanning 30 binades inside one token, an all-zero token, a
     token with one huge element and a token of subnormal-range values (the
