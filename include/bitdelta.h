@@ -124,17 +124,24 @@ bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const 
  * signs_tab: host array of V device pointers, each uint32 [d_out][d_in/32]
  * alpha_tab: host array of V device pointers, each float32 [d_out] or [1]
  * y        : device [T][d_out] in the caller's token order.
- * 1 <= V <= BD_MAX_VARIANTS.  Each W_base tile is read from device memory
- * once per group of up to 64 tokens; the tokens are grouped by variant
- * inside the kernel and every active variant's sign tile is applied to its
- * own tokens only.  An id outside [-1, V) sets BD_ERR_BAD_VARIANT in the
- * error word and that token is computed as a base-model token.
- * Accumulation is fp32.  The sign contraction runs on an exact recoding of
- * the +-1 operand: each sign bit becomes a mantissa or sign bit of a
- * constant of its column (mod 4), and the token's share of those constants
- * is subtracted once at the end; its fp32 rounding error is at most about 20
- * times that of the plain form (relative to alpha * sum_j |x_j|), and
- * non-finite x give non-finite outputs.
+ * 1 <= V <= BD_MAX_VARIANTS.  An id outside [-1, V) sets BD_ERR_BAD_VARIANT
+ * in the error word and that token is computed as a base-model token.
+ * Accumulation is fp32.  Two paths, chosen by T:
+ *  - T < 512 (decode batches): groups of up to 64 tokens; each W_base tile
+ *    is read from device memory once per group, the tokens are grouped by
+ *    variant inside the kernel and every active variant's sign tile is
+ *    applied to its own tokens only.  The sign contraction runs on an exact
+ *    recoding of the +-1 operand: each sign bit becomes a mantissa or sign
+ *    bit of a constant of its column (mod 4), and the token's share of those
+ *    constants is subtracted once at the end; its fp32 rounding error is at
+ *    most about 20 times that of the plain form (relative to
+ *    alpha * sum_j |x_j|), and non-finite x give non-finite outputs.
+ *  - T >= 512 (multi-tenant prefill): the tokens are routed as by bd_route,
+ *    x is gathered by variant into the workspace, and the tensor-core
+ *    prefill GEMM runs per 256-token block of each variant's segment with
+ *    that variant's W_eff (rounded to bf16, as in bd_linear's prefill path;
+ *    W_eff = W_base for base-model tokens).  The workspace then holds the
+ *    gathered x: bd_linear_multi_workspace_size grows by 2 T d_in bytes.
  * ------------------------------------------------------------------------ */
 size_t bd_linear_multi_workspace_size(int64_t T, int32_t V, int64_t d_out, int64_t d_in);
 
