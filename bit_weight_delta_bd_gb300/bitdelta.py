@@ -48,7 +48,20 @@ EXPORTS = (
     "bd_linear_multi_workspace_size", "bd_linear_multi",
     "bd_route_workspace_size", "bd_route",
     "bd_debug_reconstruct", "bd_check_async", "bd_compress_noalloc",
+    "bd_cache_create", "bd_cache_destroy", "bd_cache_set_source", "bd_cache_step", "bd_cache_release",
+    "bd_cache_get_stats", "bd_cache_query",
 )
+BD_CACHE_SERVED = 0
+BD_CACHE_BASE = 1
+BD_CACHE_QUEUED = 2
+
+
+class CacheStats(ctypes.Structure):
+    """bd_cache_stats (include/bitdelta.h)."""
+    _fields_ = [("steps", ctypes.c_int64), ("requests", ctypes.c_int64), ("hits", ctypes.c_int64),
+                ("misses", ctypes.c_int64), ("queued", ctypes.c_int64), ("loads", ctypes.c_int64),
+                ("evictions", ctypes.c_int64), ("bytes_loaded", ctypes.c_int64), ("slots", ctypes.c_int32),
+                ("resident", ctypes.c_int32), ("pinned", ctypes.c_int32)]
 
 
 class BitDeltaError(RuntimeError):
@@ -86,6 +99,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "bd_debug_reconstruct": ([_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp], _int),
             "bd_check_async": ([_vp, _vp], _int),
             "bd_compress_noalloc": ([_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp], _int),
+            "bd_cache_create": ([_vp, _sz, _sz, _i32, ctypes.c_double, _vp, ctypes.POINTER(_vp)], _int),
+            "bd_cache_destroy": ([_vp], None),
+            "bd_cache_set_source": ([_vp, _i32, _vp, _sz], _int),
+            "bd_cache_step": ([_vp, _vp, _i64, _vp, _vp, _vp], _int),
+            "bd_cache_release": ([_vp, _vp], _int),
+            "bd_cache_get_stats": ([_vp, ctypes.POINTER(CacheStats)], _int),
+            "bd_cache_query": ([_vp, _i32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                                ctypes.POINTER(ctypes.c_double)], _int),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -237,3 +258,76 @@ def bd_check_async(ws, stream=None) -> int:
     """Waits for the stream and returns (and clears) the asynchronous status."""
     wsp, _ = _ws(ws)
     return int(load().bd_check_async(wsp, _stream(stream)))
+
+
+class DeltaCache:
+    """The bd_cache_* entry points (delta cache of section "Altyapı ayrıntıları").
+
+    ``arena`` is a torch.uint8 CUDA tensor the cache divides into slots of
+    ``slot_bytes``; ``arena=None`` with ``n_slots`` runs the policy without
+    any CUDA call (steps then report slot offsets).  Host sources are CPU
+    tensors (page-locked for asynchronous copies); they are kept referenced
+    here for as long as the cache lives."""
+
+    def __init__(self, arena, slot_bytes: int, n_pinned: int, rate_decay: float = 1.0, copy_stream=None,
+                 n_slots: int | None = None):
+        lib = load()
+        if arena is None:
+            if n_slots is None:
+                raise ValueError("a dry-run cache needs n_slots")
+            ptr, nbytes, cs = None, int(n_slots) * int(slot_bytes), None
+        else:
+            if arena.dtype != torch.uint8:
+                raise ValueError("arena must be a torch.uint8 tensor")
+            ptr, nbytes = _ptr(arena, "arena"), arena.numel()
+            cs = (copy_stream or torch.cuda.current_stream()).cuda_stream
+        h = _vp()
+        _check(lib.bd_cache_create(ptr, nbytes, int(slot_bytes), int(n_pinned), float(rate_decay), cs,
+                                   ctypes.byref(h)), "bd_cache_create")
+        self._h, self._lib, self.dry = h, lib, arena is None
+        self._arena, self._sources = arena, {}
+
+    def set_source(self, variant: int, host: torch.Tensor) -> None:
+        if host.is_cuda or not host.is_contiguous():
+            raise ValueError("a source is a contiguous CPU tensor")
+        _check(self._lib.bd_cache_set_source(self._h, int(variant), host.data_ptr(),
+                                             host.numel() * host.element_size()), "bd_cache_set_source")
+        self._sources[int(variant)] = host
+
+    def step(self, vids, stream=None):
+        """Per request: (device address or slot offset, or None; state)."""
+        import numpy as np
+
+        v = np.ascontiguousarray(np.asarray(vids, dtype=np.int32))
+        n = v.size
+        delta = (_vp * max(n, 1))()
+        state = np.zeros(max(n, 1), np.int32)
+        st = None if self.dry else _stream(stream)
+        _check(self._lib.bd_cache_step(self._h, v.ctypes.data, n, st, delta, state.ctypes.data), "bd_cache_step")
+        # a served request's slot offset 0 (dry run) reads back from ctypes as None
+        return [(delta[i] or 0) if state[i] == BD_CACHE_SERVED else None for i in range(n)], state[:n].copy()
+
+    def release(self, stream=None) -> None:
+        _check(self._lib.bd_cache_release(self._h, None if self.dry else _stream(stream)), "bd_cache_release")
+
+    def stats(self) -> dict:
+        out = CacheStats()
+        _check(self._lib.bd_cache_get_stats(self._h, ctypes.byref(out)), "bd_cache_get_stats")
+        return {name: getattr(out, name) for name, _ in CacheStats._fields_}
+
+    def query(self, variant: int):
+        r, pn, rate = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_double()
+        _check(self._lib.bd_cache_query(self._h, int(variant), ctypes.byref(r), ctypes.byref(pn), ctypes.byref(rate)),
+               "bd_cache_query")
+        return bool(r.value), bool(pn.value), rate.value
+
+    def close(self) -> None:
+        if self._h:
+            self._lib.bd_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -199,6 +199,70 @@ bd_status bd_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, co
 bd_status bd_compress_noalloc(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out, int64_t d_in,
                               int alpha_mode, uint32_t* signs, float* alpha, void* stream);
 
+/* ------------------------------------------------------------------------
+ * Delta cache -- section "Altyapı ayrıntıları": a variant's packed delta is
+ * loaded into device memory on its first request (the cold start) and stays
+ * there until evicted; eviction is request-rate-weighted LRU (the most
+ * requested variants are pinned, the others share the remaining space in
+ * least-recently-used order); requests for a variant whose delta is being
+ * loaded wait for that one load instead of starting their own.
+ *
+ * bd_cache_create: the cache divides `device_arena` (caller-owned device
+ *   memory, 256-byte aligned, or NULL) into arena_bytes / slot_bytes slots
+ *   (slot_bytes a multiple of 256) of one variant's delta each.  n_pinned
+ *   variants are pinned; request rates decay by `rate_decay` (0 < d <= 1) per
+ *   step.  Copies run on `copy_stream` (a cudaStream_t; NULL = legacy default
+ *   stream).  With device_arena == NULL no CUDA call is ever made and steps
+ *   report slot offsets instead of addresses (a dry run of the policy).  The
+ *   cache object itself is host memory owned by the library until
+ *   bd_cache_destroy.  One cache may be used from several host threads.
+ * bd_cache_set_source: the host copy (page-locked memory for asynchronous
+ *   copies) of `variant`'s delta, bytes <= slot_bytes; not allowed while the
+ *   variant is resident.
+ * bd_cache_step: one serving step; vid[n] are host variant ids of its
+ *   requests (-1 = base model).  Updates the rates and the pinned set (the
+ *   n_pinned registered variants of highest rate), loads each missing
+ *   requested variant once (most requested first) into a free slot or the
+ *   least recently used slot of an unpinned variant not used by this step,
+ *   makes `stream` wait for the loads of every slot handed out, and writes
+ *   per request state[i] (BD_CACHE_SERVED, _BASE, _QUEUED) and delta[i] (the
+ *   slot's device address, or NULL).  Queued requests found no slot: keep
+ *   them for a later step.  An id < -1 or without a source returns
+ *   BD_ERR_BAD_VARIANT and changes nothing.  Each step must be followed by
+ *   bd_cache_release before the next.
+ * bd_cache_release: records on `stream` (after the step's kernels were
+ *   enqueued) that the step's slots are free to be overwritten; later loads
+ *   into them wait for that point on the copy stream.
+ * ------------------------------------------------------------------------ */
+typedef struct bd_cache bd_cache;
+
+typedef struct bd_cache_stats {
+    int64_t steps;        /* bd_cache_step calls */
+    int64_t requests;     /* requests with a variant (base-model requests excluded) */
+    int64_t hits;         /* requests whose variant was resident or already loading */
+    int64_t misses;       /* requests whose variant their step loaded */
+    int64_t queued;       /* requests left without a slot */
+    int64_t loads;        /* host -> device copies issued */
+    int64_t evictions;    /* resident deltas replaced by another variant's */
+    int64_t bytes_loaded;
+    int32_t slots, resident, pinned;
+} bd_cache_stats;
+
+#define BD_CACHE_SERVED 0
+#define BD_CACHE_BASE 1
+#define BD_CACHE_QUEUED 2
+
+bd_status bd_cache_create(void* device_arena, size_t arena_bytes, size_t slot_bytes, int32_t n_pinned,
+                          double rate_decay, void* copy_stream, bd_cache** out);
+void bd_cache_destroy(bd_cache* cache);
+bd_status bd_cache_set_source(bd_cache* cache, int32_t variant, const void* host_src, size_t bytes);
+bd_status bd_cache_step(bd_cache* cache, const int32_t* vid, int64_t n, void* stream, const void** delta,
+                        int32_t* state);
+bd_status bd_cache_release(bd_cache* cache, void* stream);
+bd_status bd_cache_get_stats(bd_cache* cache, bd_cache_stats* out);
+/* resident / pinned (0 or 1) and current request rate of one variant */
+bd_status bd_cache_query(bd_cache* cache, int32_t variant, int32_t* resident, int32_t* pinned, double* rate);
+
 /* Waits for `stream`, then reads and clears the error word in `ws`.
  * Returns BD_OK, or the first asynchronous error found (in the order
  * BD_ERR_TIMEOUT, BD_ERR_BAD_VARIANT, BD_ERR_NONFINITE). */
