@@ -129,6 +129,14 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ------------------------------------------------------------ programmatic dependent launch
+// In a kernel launched with programmatic stream serialization: wait until the
+// preceding kernel of the stream has completed and its memory is visible
+// (returns at once when the launch had no such dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// In the preceding kernel: allow the dependent kernel to start launching now.
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ------------------------------------------------------------ loads
 
 // Read-only (non-coherent) 16-byte load of data that no kernel writes

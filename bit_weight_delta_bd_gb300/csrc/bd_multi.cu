@@ -276,6 +276,10 @@ __global__ void __launch_bounds__(kPrepThreads) multi_prepare_kernel(const uint1
     __shared__ Routing rt;
     __shared__ float part[kPrepThreads / 32];
     const int tid = threadIdx.x;
+    // the fused kernel that follows may start now: its routing and base phase
+    // read only the caller's inputs; it waits for this grid before it reads
+    // the padded tiles or the corrections
+    grid_launch_dependents();
     route_group(rt, vid, T, V, nullptr, tid);
     const int nc = static_cast<int>(d_in / kChunk);
     int slot = -1, local = 0, pos = -1;
@@ -596,6 +600,7 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
         __syncwarp();
     } else if (warp == kProducerWarp) {
         // ------------------------------------------------------------ variant-phase producer
+        grid_dependency_wait();  // the padded tiles come from the prepare pass
         int i = 0;
         bool ok = true;
         for (int a = 0; a < n_act && ok; ++a) {
@@ -730,6 +735,7 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     float* corr_s = red;                       // [Tpad]
     float* alpha_s = red + Tpad;               // [n_act][nr]
     if (tid < T) {
+        grid_dependency_wait();  // the corrections come from the prepare pass
         float c = 0.0f;
         for (int sp = 0; sp < p.nsplit; ++sp) c += p.corr[static_cast<int64_t>(tid) * p.nsplit + sp];
         corr_s[tid] = c;
@@ -774,13 +780,17 @@ cudaError_t launch_nt(const MultiParams& prm, size_t smem, unsigned grid, cudaSt
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(prm.CK);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // may start while the prepare pass runs (programmatic dependent launch):
+    // the routing, the tensor-memory setup and the base phase overlap it
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
