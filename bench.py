@@ -73,8 +73,8 @@ def parse_args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill", "multi_prefill", "slice"],
-                   default="decode")
+    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill", "multi_prefill", "materialize",
+                                          "slice"], default="decode")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement of the decode line")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
@@ -99,6 +99,11 @@ def load_peaks():
 
 
 # ----------------------------------------------------------------------------- workloads
+
+def materialize_bytes(d_out, d_in, n_alpha):
+    """W_base read, W_eff written (2 bytes each per weight), bits and alpha read."""
+    return 4 * d_out * d_in + d_out * d_in // 8 + 4 * n_alpha
+
 
 def linear_bytes(T, d_out, d_in, n_alpha, y_bytes=2):
     """Algorithmic bytes of one fused linear: W_base + bits + alpha + x + y."""
@@ -133,6 +138,14 @@ class Workload:
             self.wb = synth.base_weight(rng, d_out, d_in)
             self.wf = [synth.finetuned_weight(rng, self.wb, 1e-3)]
             self.xs = [synth.activations(rng, T, d_in) for T in self.tokens]
+            self.vid = None
+        elif name == "materialize":
+            d_out, d_in = 28672, 8192
+            self.tokens = []
+            self.per_row = True
+            self.wb, wf, _ = synth.single_problem(seed, d_out, d_in, 1)
+            self.wf = [wf]
+            self.xs = []
             self.vid = None
         elif name == "prefill":
             d_out, d_in = 8192, 8192
@@ -176,6 +189,10 @@ class Workload:
             c["step"] = ("bd_linear_multi over 4096 Zipf(1.1)-routed tokens: router, gather, grouped tensor-core "
                          "prefill (variants compressed once, untimed)")
             c["l2"] = "inputs larger than L2 (W_base 134 MB + x 67 MB + y 67 MB vs 126.5 MB L2)"
+        elif self.name == "materialize":
+            c["workload"] = "materialize_ffn_28672x8192"
+            c["step"] = "bd_materialize: W_eff = RN_bf16(W_base + alpha s) written to HBM (variant compressed once, untimed)"
+            c["l2"] = "inputs larger than L2 (W_base 470 MB in, W_eff 470 MB out vs 126.5 MB L2)"
         elif self.name == "tiny":
             c["workload"] = "tiny_256x256_T4"
             c["step"] = "bd_compress + bd_linear at T=4"
@@ -212,11 +229,13 @@ class GpuRun:
         self.ys = [torch.empty((T, wl.d_out), dtype=torch.bfloat16, device=dev) for T in wl.tokens]
         self.ws = bd.new_workspace(max(bd.bd_compress_workspace_size(wl.d_out, wl.d_in, PR),
                                        bd.bd_linear_workspace_size(64, wl.d_out, wl.d_in),
-                                       bd.bd_linear_multi_workspace_size(max(64, max(wl.tokens)), max(len(wl.wf), 1),
+                                       bd.bd_linear_multi_workspace_size(max(64, max(wl.tokens, default=0)), max(len(wl.wf), 1),
                                                                          wl.d_out, wl.d_in)), dev)
         self.vid = None if wl.vid is None else torch.from_numpy(wl.vid).to(dev)
         self.flush = None
-        if wl.name in ("multi", "prefill", "multi_prefill"):
+        if wl.name == "materialize":
+            self.w_eff = torch.empty((wl.d_out, wl.d_in), dtype=torch.int16, device=dev)
+        if wl.name in ("multi", "prefill", "multi_prefill", "materialize"):
             for v in range(len(wl.wf)):  # variants are compressed once, before timing
                 bd.bd_compress(self.wb, self.wf[v], PR, self.signs[v], self.alpha[v], self.ws)
             torch.cuda.synchronize()
@@ -240,6 +259,10 @@ class GpuRun:
             out.append((f"linear_multi_T{T}", kname, nbytes, flops,
                         lambda: bd.bd_linear_multi(self.xs[0], self.vid, self.signs, self.alpha, self.mode, self.wb,
                                                    self.ys[0], self.ws)))
+            return out
+        if wl.name == "materialize":
+            out.append(("materialize", "materialize_kernel", materialize_bytes(wl.d_out, wl.d_in, wl.n_alpha), 0,
+                        lambda: bd.bd_materialize(self.wb, self.signs[0], self.alpha[0], self.mode, self.w_eff)))
             return out
         if wl.name == "prefill":
             T = wl.tokens[0]
@@ -408,7 +431,9 @@ def oracle_time(wl: Workload, budget_s: float = 12.0, threads: int = 0):
             sf[r], af[r] = s, a
             sfs.append(sf)
             afs.append(af)
-        if wl.vid is None:
+        if wl.name == "materialize":
+            oracle.materialize(wl.wb[r], sfs[0][r], afs[0][r], True)
+        elif wl.vid is None:
             for x in wl.xs:
                 oracle.linear(x, wl.wb, sfs[0], afs[0], True, rows=r)
         else:
@@ -430,6 +455,8 @@ def _step_bytes_rows(wl: Workload):
         out.append(("linear_multi", "", 2 * wl.d_out * wl.d_in + len(active) * (wl.d_out * wl.d_in // 8 + 4 * wl.n_alpha)
                     + 2 * T * wl.d_in + 2 * T * wl.d_out + 4 * T))
         return out
+    if wl.name == "materialize":
+        return [("materialize", "", materialize_bytes(wl.d_out, wl.d_in, wl.n_alpha))]
     if wl.name != "prefill":
         out.append(("compress", "", compress_bytes(wl.d_out, wl.d_in, wl.n_alpha)))
     for T in wl.tokens:
@@ -677,6 +704,9 @@ def run_e2e(run: GpuRun, calls, wl: Workload, steps: int, stream):
     elif wl.name == "slice":
         h_in = [(pin(x), x) for x in run.xs] + [(pin(run.vid), run.vid)]
         h_out = [(pin(y), y) for y in run.ys]
+    elif wl.name == "materialize":
+        h_in = [(pin(run.wb), run.wb), (pin(run.signs[0]), run.signs[0]), (pin(run.alpha[0]), run.alpha[0])]
+        h_out = [(pin(run.w_eff), run.w_eff)]
     elif wl.name == "prefill":
         h_in = [(pin(run.xs[0]), run.xs[0])]
         h_out = [(pin(run.ys[0]), run.ys[0])]

@@ -49,7 +49,7 @@ EXPORTS = (
     "bd_route_workspace_size", "bd_route",
     "bd_debug_reconstruct", "bd_check_async", "bd_compress_noalloc",
     "bd_cache_create", "bd_cache_destroy", "bd_cache_set_source", "bd_cache_step", "bd_cache_release",
-    "bd_cache_get_stats", "bd_cache_query",
+    "bd_cache_get_stats", "bd_cache_query", "bd_materialize",
 )
 BD_CACHE_SERVED = 0
 BD_CACHE_BASE = 1
@@ -99,6 +99,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "bd_debug_reconstruct": ([_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp], _int),
             "bd_check_async": ([_vp, _vp], _int),
             "bd_compress_noalloc": ([_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp], _int),
+            "bd_materialize": ([_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp], _int),
             "bd_cache_create": ([_vp, _sz, _sz, _i32, ctypes.c_double, _vp, ctypes.POINTER(_vp)], _int),
             "bd_cache_destroy": ([_vp], None),
             "bd_cache_set_source": ([_vp, _i32, _vp, _sz], _int),
@@ -236,6 +237,13 @@ def bd_linear_multi(x, vid, signs_list, alpha_list, alpha_mode, w_base, y, ws, s
                                   _ptr(w_base, "w_base", _BF16_LIKE), d_out, d_in,
                                   _ptr(y, "y", (torch.float32, torch.bfloat16)), out_dtype, wsp, wsn,
                                   _stream(stream)), "bd_linear_multi")
+
+
+def bd_materialize(w_base, signs, alpha, alpha_mode, w_eff, stream=None) -> None:
+    d_out, d_in = w_base.shape
+    _check(load().bd_materialize(_ptr(w_base, "w_base", _BF16_LIKE), _ptr(signs, "signs", (torch.int32, torch.uint32)),
+                                 _ptr(alpha, "alpha", (torch.float32,)), int(alpha_mode), d_out, d_in,
+                                 _ptr(w_eff, "w_eff", _BF16_LIKE), _stream(stream)), "bd_materialize")
 
 
 def bd_route(vid, V, perm, seg_off, ws, stream=None) -> None:

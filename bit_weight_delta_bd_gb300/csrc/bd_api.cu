@@ -136,6 +136,27 @@ bd_status bd_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, co
                                                  w_eff, static_cast<cudaStream_t>(stream)));
 }
 
+bd_status bd_materialize(const uint16_t* w_base, const uint32_t* signs, const float* alpha, int alpha_mode,
+                         int64_t d_out, int64_t d_in, uint16_t* w_eff, void* stream)
+{
+    if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
+    if (d_out < 0) return BD_ERR_UNSUPPORTED_SHAPE;
+    if (bd_status s = check_d_in(d_in)) return s;
+    if (d_out == 0) return BD_OK;
+    if (!w_base || !signs || !alpha || !w_eff) return BD_ERR_INVALID_ARG;
+    if (!aligned(w_base, 16) || !aligned(w_eff, 16) || !aligned(signs, 4) || !aligned(alpha, 4))
+        return BD_ERR_MISALIGNED;
+    const size_t wbytes = static_cast<size_t>(d_out) * static_cast<size_t>(d_in) * 2;
+    const size_t abytes = (alpha_mode == BD_ALPHA_PER_ROW ? static_cast<size_t>(d_out) : 1u) * 4;
+    if (overlaps(w_eff, wbytes, w_base, wbytes) || overlaps(w_eff, wbytes, signs, wbytes / 16) ||
+        overlaps(w_eff, wbytes, alpha, abytes))
+        return BD_ERR_INVALID_ARG;
+    int sms = 0;
+    if (bd_status s = device_info(&sms)) return s;
+    return launched(bd::launch_materialize(w_base, signs, alpha, alpha_mode == BD_ALPHA_PER_ROW, d_out, d_in, w_eff,
+                                           sms, static_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------------ linear
 
 size_t bd_linear_workspace_size(int64_t /*T*/, int64_t /*d_out*/, int64_t /*d_in*/) { return kWsHeader; }

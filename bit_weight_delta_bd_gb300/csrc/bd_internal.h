@@ -71,6 +71,11 @@ int multi_corr_splits(int64_t d_in);
 
 cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream);
 
+// ---- materialised variant (bd_materialize.cu) -------------------------------------------------
+
+cudaError_t launch_materialize(const uint16_t* w_base, const uint32_t* signs, const float* alpha, int per_row,
+                               int64_t d_out, int64_t d_in, uint16_t* w_eff, int sm_count, cudaStream_t stream);
+
 // ---- router (bd_route.cu) ---------------------------------------------------------------------
 
 cudaError_t launch_route(const int32_t* vid, int64_t T, int V, int32_t* perm, int32_t* seg_off, uint32_t* err,

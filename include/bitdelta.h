@@ -173,6 +173,20 @@ bd_status bd_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, co
                                int64_t d_out, int64_t d_in, float* w_eff, void* stream);
 
 /* ------------------------------------------------------------------------
+ * Materialised variant -- the reading of section "Sunum mimarisi" in which a
+ * variant's effective weights are built once and a standard matmul follows
+ * (the fused entry points above never build them in device memory):
+ *   w_eff[r][j] = RN_bf16(W_base[r][j] + alpha_r * s_rj)
+ * rounded once (to nearest, ties to even) from the exact sum.
+ * w_base: device bf16 [d_out][d_in] (16-byte aligned); signs, alpha as
+ * produced by bd_compress; w_eff: device bf16 [d_out][d_in] (written,
+ * 16-byte aligned, overlapping no input).  Reads 2.125 and writes 2 bytes per
+ * weight.
+ * ------------------------------------------------------------------------ */
+bd_status bd_materialize(const uint16_t* w_base, const uint32_t* signs, const float* alpha, int alpha_mode,
+                         int64_t d_out, int64_t d_in, uint16_t* w_eff, void* stream);
+
+/* ------------------------------------------------------------------------
  * Compression that allocates nothing (the BitDelta post has no counterpart
  * for this entry point; it exists for callers of this library).
  * Some callers cannot call cudaMalloc or hand the library a workspace: code

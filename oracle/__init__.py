@@ -152,6 +152,25 @@ def reconstruct(w_base_bits, signs, alpha, per_row: bool) -> np.ndarray:
     return out
 
 
+def round_to_bf16(v: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of fp64 values rounded to nearest, ties to even, in
+    one rounding: v = m 2^e with 0.5 <= |m| < 1, the 8 significant bits are
+    rint(256 m) (numpy's rint rounds halves to even), and the result, exact
+    in fp64 and fp32 for values in bf16's normal range, is read back through
+    fp32 whose upper 16 bits it occupies."""
+    v = np.asarray(v, np.float64)
+    m, e = np.frexp(v)
+    r = np.ldexp(np.rint(m * 256.0), e - 8)
+    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def materialize(w_base_bits, signs, alpha, per_row: bool) -> np.ndarray:
+    """The variant's dense weights as bf16 bits: W_eff = W_base + alpha * s
+    (section "Matematiksel temel", eq. (2)) in fp64, rounded once to bf16 --
+    the weights a non-fused server would build before a standard matmul."""
+    return round_to_bf16(reconstruct(w_base_bits, signs, alpha, per_row))
+
+
 def linear(x_bits, w_base_bits, signs, alpha, per_row: bool, rows=None) -> np.ndarray:
     """fp64 y [T][len(rows)] (all rows when rows is None); the rows' signs
     and alpha are indexed by absolute row number."""

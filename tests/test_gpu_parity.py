@@ -209,6 +209,49 @@ def test_linear_row_sharding_is_bit_identical(dev, T):
     assert torch.equal(torch.cat(parts, dim=1), y_full)
 
 
+@pytest.mark.parametrize("d_out,d_in,per_row", [(256, 256, False), (100, 1024, True), (7, 128, True)])
+def test_materialize_bit_exact(dev, d_out, d_in, per_row):
+    """bd_materialize equals the oracle's one-rounding bf16 W_eff bit for bit."""
+    wb, wf, _ = synth.single_problem(d_out + d_in, d_out, d_in, 1)
+    mode = PR if per_row else PM
+    s, a = oracle.compress(wb, wf, per_row=per_row)
+    w_eff = torch.empty((d_out, d_in), dtype=torch.int16, device=dev)
+    bd.bd_materialize(to_dev(wb, dev), to_dev(s, dev).view(torch.int32), to_dev(a, dev), mode, w_eff)
+    assert np.array_equal(w_eff.cpu().numpy().view(np.uint16), oracle.materialize(wb, s, a, per_row))
+
+
+def test_materialize_midpoint_sums(dev):
+    """alpha = 2^-8 + 2^-30 on W_base = 1 + k 2^-7: every fp32 sum is a bf16
+    midpoint and its lost 2^-30 decides the rounding (up for +alpha, toward
+    zero for -alpha); random signs."""
+    rng = np.random.default_rng(5)
+    d_out, d_in = 64, 256
+    k = rng.integers(0, 100, size=(d_out, d_in))
+    wb = synth.f32_to_bf16_bits((1.0 + k * 2.0**-7).astype(np.float32))
+    s = rng.integers(0, 2**32, size=(d_out, d_in // 32), dtype=np.uint64).astype(np.uint32)
+    a = np.array([2.0**-8 + 2.0**-30], np.float32)
+    w_eff = torch.empty((d_out, d_in), dtype=torch.int16, device=dev)
+    bd.bd_materialize(to_dev(wb, dev), to_dev(s, dev).view(torch.int32), to_dev(a, dev), PM, w_eff)
+    ref = oracle.materialize(wb, s, a, False)
+    assert np.array_equal(w_eff.cpu().numpy().view(np.uint16), ref)
+    # the plain fp32-then-bf16 double rounding would differ on about half of them
+    dbl = synth.f32_to_bf16_bits(oracle.reconstruct(wb, s, a, False).astype(np.float32))
+    assert np.mean(dbl != ref) > 0.25
+
+
+def test_materialize_ffn_sampled_rows(dev, decode_problem):
+    """The 28672 x 8192 decode matrix: every row written, sampled rows exact."""
+    wb, wf = decode_problem
+    wb_d = to_dev(wb, dev)
+    s, a = gpu_compress(wb_d, to_dev(wf, dev), PR, dev)
+    w_eff = torch.empty((28672, 8192), dtype=torch.int16, device=dev)
+    bd.bd_materialize(wb_d, s, a, PR, w_eff)
+    rows = synth.sample_rows(17, 28672, 64)
+    s_h, a_h = s.cpu().numpy().view(np.uint32), a.cpu().numpy()
+    ref = oracle.materialize(wb[rows], s_h[rows], a_h[rows], True)
+    assert np.array_equal(w_eff.cpu().numpy().view(np.uint16)[rows], ref)
+
+
 @pytest.fixture(scope="module")
 def prefill_problem():
     """Prefill workload: 4096 tokens x W_base [8192 x 8192], one variant, per-row alpha."""

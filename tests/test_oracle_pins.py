@@ -342,3 +342,43 @@ def test_synth_zipf_ids_in_range_and_skewed():
     counts = np.bincount(vid, minlength=14) / 20000
     p = np.arange(1, 15, dtype=np.float64) ** -1.1
     np.testing.assert_allclose(counts, p / p.sum(), atol=0.01)
+
+
+# ---------------------------------------------------------------- bf16 rounding of the materialised weights
+
+def test_round_to_bf16_hand_cases():
+    """Ties go to the even significand, both signs; a value just above a tie
+    rounds up even though fp32 could not hold it (one rounding, not two)."""
+    one = np.float64(1.0)
+    cases = {
+        one: 0x3F80,
+        one + 2.0**-8: 0x3F80,               # tie between 1 and 1 + 2^-7: even (1)
+        one + 3 * 2.0**-8: 0x3F82,           # tie between 1 + 2^-7 and 1 + 2^-6: even (mantissa 2)
+        one + 2.0**-8 + 2.0**-30: 0x3F81,    # above the tie: up
+        one + 2.0**-8 - 2.0**-30: 0x3F80,    # below the tie: down
+        -(one + 3 * 2.0**-8): 0xBF82,
+        -(one + 2.0**-8 + 2.0**-30): 0xBF81,
+        0.0: 0x0000,
+    }
+    got = oracle.round_to_bf16(np.array(list(cases.keys())))
+    assert [int(g) for g in got] == list(cases.values())
+
+
+def test_round_to_bf16_matches_the_fp32_rounding_of_the_input_module():
+    """For values exactly representable in fp32 the one rounding to bf16 is
+    the fp32 -> bf16 rounding that synth implements independently."""
+    rng = np.random.default_rng(3)
+    v = (rng.standard_normal(20000) * 2.0 ** rng.integers(-20, 20, 20000)).astype(np.float32)
+    assert np.array_equal(oracle.round_to_bf16(v.astype(np.float64)), synth.f32_to_bf16_bits(v))
+
+
+def test_materialize_is_the_rounded_reconstruction():
+    """W_eff bits are the bf16 rounding of W_base + alpha s, and decoding them
+    is within half a bf16 ulp of the fp64 reconstruction."""
+    wb, wf, _ = synth.single_problem(7, 16, 64, 1)
+    s, a = oracle.compress(wb, wf, per_row=True)
+    bits = oracle.materialize(wb, s, a, True)
+    exact = oracle.reconstruct(wb, s, a, True)
+    dec = synth.bf16_bits_to_f32(bits).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(exact))) - 7)
+    assert np.all(np.abs(dec - exact) <= ulp / 2)
