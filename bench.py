@@ -54,9 +54,13 @@ NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
     ("skinny_kernel<1>", "decode"): ("60707ad3c65224a0", "bd_skinny.cu", 499_405_056 + 3_889_920),
     ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_613_184 + 7_913_728),
-    ("prefill_kernel", "prefill"): ("69cfd4fd49cfa372", "bd_prefill.cu", 613_093_632 + 62_800_384),
+    ("prefill_kernel", "prefill"): ("86b0f01954bd837e", "bd_prefill.cu", 612_407_040 + 63_377_664),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
-    ("multi_prepare + multi_kernel<8>", "multi"): ("17f4ad70d450ec79", "bd_multi.cu", 255_804_672 + 3_930_880),
+    ("multi_prepare + multi_kernel<8>", "multi"): ("d89f83fcd4e67914", "bd_multi.cu", 255_770_880 + 3_986_432),
+    # the grouped prefill_kernel only (router, plan and gather add about 134 MB of x copies)
+    ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("86b0f01954bd837e", "bd_prefill.cu",
+                                                                      912_805_888 + 66_171_648),
+    ("materialize_kernel", "materialize"): ("fae23fcd0ba90d9b", "bd_materialize.cu", 499_370_496 + 426_232_320),
 }
 
 
