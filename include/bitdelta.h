@@ -247,6 +247,11 @@ bd_status bd_compress_noalloc(const uint16_t* w_base, const uint16_t* w_ft, int6
  * bd_cache_release: records on `stream` (after the step's kernels were
  *   enqueued) that the step's slots are free to be overwritten; later loads
  *   into them wait for that point on the copy stream.
+ * bd_cache_destroy: frees the cache object and its events; copies already
+ *   issued may still be writing the arena, so the caller keeps the arena and
+ *   the host sources alive until the copy stream has drained.  A step that
+ *   fails with BD_ERR_CUDA may have handed out some slots: call
+ *   bd_cache_release before the next step.
  * ------------------------------------------------------------------------ */
 typedef struct bd_cache bd_cache;
 
