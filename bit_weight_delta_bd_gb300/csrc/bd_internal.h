@@ -12,7 +12,7 @@ constexpr int kMaxVariants = 64;
 // ---- compression (bd_compress.cu) -------------------------------------------------------------
 
 // Rows handled by one compression CTA (one warp per row).
-constexpr int kCompressRowsPerCta = 8;
+constexpr int kCompressRowsPerCta = 4;
 
 cudaError_t launch_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out, int64_t d_in, bool per_row,
                             uint32_t* signs, float* alpha, double* partials, uint32_t* err, cudaStream_t stream);
