@@ -54,7 +54,8 @@ FALLBACK_BF16_TFLOPS = 1900.0
 NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
     ("skinny_kernel<1>", "decode"): ("60707ad3c65224a0", "bd_skinny.cu", 499_405_056 + 3_889_920),
-    ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_613_184 + 7_913_728),
+    # 4 rows per CTA (kCompressRowsPerCta in bd_internal.h)
+    ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_566_080 + 7_655_936),
     ("prefill_kernel", "prefill"): ("86b0f01954bd837e", "bd_prefill.cu", 612_407_040 + 63_377_664),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
     ("multi_prepare + multi_kernel<8>", "multi"): ("d89f83fcd4e67914", "bd_multi.cu", 255_770_880 + 3_986_432),
