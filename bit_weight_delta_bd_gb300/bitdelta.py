@@ -42,7 +42,7 @@ BD_NOALLOC_MAX_ROWS = 262144
 
 # Every symbol include/bitdelta.h declares.
 EXPORTS = (
-    "bd_version", "bd_status_string",
+    "bd_version", "bd_status_string", "bd_last_cuda_error", "bd_cuda_error_string",
     "bd_compress_workspace_size", "bd_compress",
     "bd_linear_workspace_size", "bd_linear",
     "bd_linear_multi_workspace_size", "bd_linear_multi",
@@ -67,7 +67,12 @@ class CacheStats(ctypes.Structure):
 class BitDeltaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = int(status)
-        super().__init__(f"{where}: {status_string(status)}")
+        self.cuda_error = 0
+        msg = f"{where}: {status_string(status)}"
+        if self.status == BD_ERR_CUDA and _lib is not None:
+            self.cuda_error = int(_lib.bd_last_cuda_error())
+            msg += f" ({_lib.bd_cuda_error_string(self.cuda_error).decode()}, code {self.cuda_error})"
+        super().__init__(msg)
 
 
 _lib = None
@@ -87,6 +92,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
         sig = {
             "bd_version": ([], _int),
             "bd_status_string": ([_int], ctypes.c_char_p),
+            "bd_last_cuda_error": ([], _int),
+            "bd_cuda_error_string": ([_int], ctypes.c_char_p),
             "bd_compress_workspace_size": ([_i64, _i64, _int], _sz),
             "bd_compress": ([_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp, _sz, _vp], _int),
             "bd_linear_workspace_size": ([_i64, _i64, _i64], _sz),

@@ -12,7 +12,10 @@ namespace {
 constexpr int kVersion = 10000;  // 1.0.0
 constexpr size_t kWsHeader = 256;  // error word + padding; scratch starts here
 
-// Per-device cache of (compute capability, SM count); the only global state.
+// The calling thread's last failed CUDA result (bd_last_cuda_error).
+thread_local int g_last_cuda_error = 0;
+
+// Per-device cache of (compute capability, SM count).
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_dev_cc[kMaxDevices];
 std::atomic<int> g_dev_sms[kMaxDevices];
@@ -20,15 +23,15 @@ std::atomic<int> g_dev_sms[kMaxDevices];
 bd_status device_info(int* sm_count)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
+    if (const int cs_ = bd::cuda_status(cudaGetDevice(&dev))) return static_cast<bd_status>(cs_);
     if (dev < 0 || dev >= kMaxDevices) return BD_ERR_DEVICE;
     int cc = g_dev_cc[dev].load(std::memory_order_acquire);
     if (cc == 0) {
         int major = 0, minor = 0, sms = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return BD_ERR_CUDA;
+        cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return static_cast<bd_status>(bd::cuda_status(e));
         cc = major * 10 + minor;
         g_dev_sms[dev].store(sms, std::memory_order_relaxed);
         g_dev_cc[dev].store(cc, std::memory_order_release);
@@ -56,15 +59,30 @@ bd_status check_ws(const void* ws, size_t ws_bytes, size_t need)
     return BD_OK;
 }
 
-bd_status launched(cudaError_t e) { return e == cudaSuccess ? BD_OK : BD_ERR_CUDA; }
+bd_status launched(cudaError_t e) { return static_cast<bd_status>(bd::cuda_status(e)); }
 
 uint32_t* err_word(void* ws) { return static_cast<uint32_t*>(ws); }
 
 }  // namespace
 
+int bd::cuda_status(cudaError_t e)
+{
+    if (e == cudaSuccess) return BD_OK;
+    g_last_cuda_error = static_cast<int>(e);
+    return BD_ERR_CUDA;
+}
+
 extern "C" {
 
 int bd_version(void) { return kVersion; }
+
+int bd_last_cuda_error(void) { return g_last_cuda_error; }
+
+const char* bd_cuda_error_string(int code)
+{
+    const char* name = cudaGetErrorName(static_cast<cudaError_t>(code));
+    return name ? name : "unknown CUDA error";
+}
 
 const char* bd_status_string(bd_status s)
 {
@@ -390,12 +408,12 @@ bd_status bd_check_async(void* ws, void* stream)
     if (!aligned(ws, 256)) return BD_ERR_MISALIGNED;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     uint32_t word = 0;
-    if (cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, st) != cudaSuccess) return BD_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return BD_ERR_CUDA;
+    if (const int cs_ = bd::cuda_status(cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, st))) return static_cast<bd_status>(cs_);
+    if (const int cs_ = bd::cuda_status(cudaStreamSynchronize(st))) return static_cast<bd_status>(cs_);
     if (word == 0) return BD_OK;
     const uint32_t zero = 0;
-    if (cudaMemcpyAsync(ws, &zero, sizeof zero, cudaMemcpyHostToDevice, st) != cudaSuccess) return BD_ERR_CUDA;
-    if (cudaStreamSynchronize(st) != cudaSuccess) return BD_ERR_CUDA;
+    if (const int cs_ = bd::cuda_status(cudaMemcpyAsync(ws, &zero, sizeof zero, cudaMemcpyHostToDevice, st))) return static_cast<bd_status>(cs_);
+    if (const int cs_ = bd::cuda_status(cudaStreamSynchronize(st))) return static_cast<bd_status>(cs_);
     if (word & (1u << BD_ERR_TIMEOUT)) return BD_ERR_TIMEOUT;
     if (word & (1u << BD_ERR_BAD_VARIANT)) return BD_ERR_BAD_VARIANT;
     if (word & (1u << BD_ERR_NONFINITE)) return BD_ERR_NONFINITE;

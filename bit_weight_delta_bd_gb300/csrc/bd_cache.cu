@@ -31,6 +31,7 @@
 #include <vector>
 
 #include "../../include/bitdelta.h"
+#include "bd_internal.h"
 
 struct bd_cache {
     struct Slot {
@@ -124,10 +125,11 @@ bd_status bd_cache_create(void* device_arena, size_t arena_bytes, size_t slot_by
     c->slots.resize(n);
     if (c->arena) {
         for (auto& sl : c->slots) {
-            if (cudaEventCreateWithFlags(&sl.ready, cudaEventDisableTiming) != cudaSuccess ||
-                cudaEventCreateWithFlags(&sl.released, cudaEventDisableTiming) != cudaSuccess) {
+            cudaError_t e = cudaEventCreateWithFlags(&sl.ready, cudaEventDisableTiming);
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&sl.released, cudaEventDisableTiming);
+            if (e != cudaSuccess) {
                 bd_cache_destroy(c);
-                return BD_ERR_CUDA;
+                return static_cast<bd_status>(bd::cuda_status(e));
             }
         }
     }
@@ -202,12 +204,12 @@ bd_status bd_cache_step(bd_cache* c, const int32_t* vid, int64_t n, void* stream
             const bd_cache::Source& so = c->src[v];
             if (c->arena && so.bytes > 0) {
                 // the copy overwrites the slot only after the last step using it finished
-                if (sl.released_recorded && cudaStreamWaitEvent(c->copy, sl.released, 0) != cudaSuccess)
-                    return BD_ERR_CUDA;
-                if (cudaMemcpyAsync(c->arena + static_cast<size_t>(s) * c->slot_bytes, so.host, so.bytes,
-                                    cudaMemcpyHostToDevice, c->copy) != cudaSuccess ||
-                    cudaEventRecord(sl.ready, c->copy) != cudaSuccess)
-                    return BD_ERR_CUDA;
+                cudaError_t e = sl.released_recorded ? cudaStreamWaitEvent(c->copy, sl.released, 0) : cudaSuccess;
+                if (e == cudaSuccess)
+                    e = cudaMemcpyAsync(c->arena + static_cast<size_t>(s) * c->slot_bytes, so.host, so.bytes,
+                                        cudaMemcpyHostToDevice, c->copy);
+                if (e == cudaSuccess) e = cudaEventRecord(sl.ready, c->copy);
+                if (e != cudaSuccess) return static_cast<bd_status>(bd::cuda_status(e));
             }
             sl.variant = v;
             c->slot_of[v] = s;
@@ -218,7 +220,9 @@ bd_status bd_cache_step(bd_cache* c, const int32_t* vid, int64_t n, void* stream
         c->slots[s].last_use = c->tick;
         c->acquired.push_back(s);
         granted[v] = s;
-        if (c->arena && cudaStreamWaitEvent(st, c->slots[s].ready, 0) != cudaSuccess) return BD_ERR_CUDA;
+        if (c->arena)
+            if (const int cs_ = bd::cuda_status(cudaStreamWaitEvent(st, c->slots[s].ready, 0)))
+                return static_cast<bd_status>(cs_);
     }
     for (int64_t i = 0; i < n; ++i) {
         const int32_t v = vid[i];
@@ -247,7 +251,8 @@ bd_status bd_cache_release(bd_cache* c, void* stream)
     for (const int s : c->acquired) {
         auto& sl = c->slots[s];
         if (c->arena) {
-            if (cudaEventRecord(sl.released, static_cast<cudaStream_t>(stream)) != cudaSuccess) return BD_ERR_CUDA;
+            if (const int cs_ = bd::cuda_status(cudaEventRecord(sl.released, static_cast<cudaStream_t>(stream))))
+                return static_cast<bd_status>(cs_);
             sl.released_recorded = true;
         }
     }

@@ -9,6 +9,11 @@ namespace bd {
 
 constexpr int kMaxVariants = 64;
 
+// Maps a CUDA runtime result to a library status: cudaSuccess -> 0
+// (BD_OK), anything else -> BD_ERR_CUDA, with the code kept as the calling
+// thread's last CUDA error (bd_last_cuda_error).
+int cuda_status(cudaError_t e);
+
 // ---- compression (bd_compress.cu) -------------------------------------------------------------
 
 // Rows handled by one compression CTA (one warp per row).

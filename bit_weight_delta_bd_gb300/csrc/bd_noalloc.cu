@@ -27,17 +27,19 @@ double* g_partials_addr[kMaxDevices];  // device address of g_noalloc_partials, 
 bd_status scratch_for_current_device(double** out)
 {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return BD_ERR_CUDA;
+    if (const int cs_ = bd::cuda_status(cudaGetDevice(&dev))) return static_cast<bd_status>(cs_);
     if (dev < 0 || dev >= kMaxDevices) return BD_ERR_DEVICE;
     int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return BD_ERR_CUDA;
+    cudaError_t e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return static_cast<bd_status>(bd::cuda_status(e));
     if (major * 10 + minor != 103) return BD_ERR_DEVICE;
     std::lock_guard<std::mutex> lock(g_setup_mutex);
     if (g_partials_addr[dev] == nullptr) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || p == nullptr) return BD_ERR_CUDA;
+        if (const int cs_ = bd::cuda_status(cudaGetSymbolAddress(&p, g_noalloc_partials)))
+            return static_cast<bd_status>(cs_);
+        if (p == nullptr) return BD_ERR_CUDA;
         g_partials_addr[dev] = static_cast<double*>(p);
     }
     *out = g_partials_addr[dev];
@@ -79,5 +81,5 @@ extern "C" bd_status bd_compress_noalloc(const uint16_t* w_base, const uint16_t*
     // word: a non-finite delta shows up as a non-finite alpha.
     const cudaError_t e = bd::launch_compress(w_base, w_ft, d_out, d_in, alpha_mode == BD_ALPHA_PER_ROW, signs,
                                               alpha, partials, nullptr, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? BD_OK : BD_ERR_CUDA;
+    return static_cast<bd_status>(bd::cuda_status(e));
 }

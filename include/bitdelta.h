@@ -74,6 +74,16 @@ int bd_version(void);
 /* Human-readable name of a status code (static string, never NULL). */
 const char* bd_status_string(bd_status status);
 
+/* The cudaError_t code of the last CUDA runtime call or kernel launch made
+ * by this library on the calling thread that failed -- the cause behind the
+ * last BD_ERR_CUDA the thread saw -- or 0 if none has failed.  Kept per
+ * thread; a later success does not clear it. */
+int bd_last_cuda_error(void);
+
+/* CUDA's name of a cudaError_t code, e.g. "cudaErrorInvalidValue" (static
+ * string, never NULL). */
+const char* bd_cuda_error_string(int code);
+
 /* ------------------------------------------------------------------------
  * Compression -- section "Matematiksel temel", eqs. (1)-(3):
  *   Delta = W_ft - W_base,  alpha = mean |Delta| (per row or per matrix),

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from bit_weight_delta_bd_gb300 import bitdelta as bd
 
@@ -41,6 +42,26 @@ def test_status_strings(lib):
         assert s.startswith("BD_")
     assert bd.status_string(999) == "BD_ERR_UNKNOWN"
     assert bd.bd_version() == 10000
+
+
+def test_cuda_error_names(lib):
+    assert lib.bd_cuda_error_string(0).decode() == "cudaSuccess"
+    assert lib.bd_cuda_error_string(1).decode() == "cudaErrorInvalidValue"
+    assert lib.bd_cuda_error_string(2).decode() == "cudaErrorMemoryAllocation"
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="needs a machine without a usable GPU")
+def test_failed_cuda_call_keeps_its_code(lib):
+    """A call that passes every host check reaches the CUDA runtime, which
+    fails here (no GPU): the status is BD_ERR_CUDA and the runtime's own code
+    is kept for the thread and named in the Python error."""
+    st = _linear(lib)
+    assert st == bd.BD_ERR_CUDA
+    code = lib.bd_last_cuda_error()
+    assert code != 0 and lib.bd_cuda_error_string(code).decode().startswith("cudaError")
+    with pytest.raises(bd.BitDeltaError) as e:
+        bd._check(st, "bd_linear")
+    assert e.value.cuda_error == code and lib.bd_cuda_error_string(code).decode() in str(e.value)
 
 
 def test_workspace_sizes(lib):
