@@ -117,6 +117,55 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar)
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
+// ------------------------------------------------------------ clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives and waits (release /
+// acquire at cluster scope).
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrives on the mbarrier at the same shared-memory offset as `bar` in the
+// cluster's CTA of rank `cta`, with the default (CTA-scope) release.  For
+// signals whose data is already complete when the arrive is issued (tensor-
+// memory stores waited for with tcgen05.wait::st, TMA data whose
+// complete_tx was observed): a cluster-scope release would also make the
+// SM drain its memory traffic in flight, which in a TMA-fed pipeline
+// serialises the stage ring (2.4x the time of a 4096 x 8192 x 8192
+// prefill on GB300).
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t* bar, uint32_t cta)
+{
+    asm volatile(
+        "{\n\t.reg .b32 ra;\n\t"
+        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
+        "mbarrier.arrive.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
+        "r"(cta)
+        : "memory");
+}
+
+// try_wait with acquire at cluster scope: pairs with arrivals made by other
+// CTAs of the cluster (mbar_arrive_remote).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // ------------------------------------------------------------ warp MMA
 
 // D += A * B, m16n8k16, bf16 inputs, fp32 accumulate.

@@ -4,38 +4,49 @@
 //
 //   D[r][t] = sum_k W_eff[r][k] * x[t][k],   y[t][r] = D[r][t]
 //
-// One CTA computes a 128-row x 256-token tile of y^T over all of d_in, in
-// 64-column k-steps through a 4-stage ring:
-//   warp 0      TMA producer: x tile [256 x 64] (128-byte swizzle), W_base
-//               tile [128 x 64] (128-byte swizzle) and the sign words of the
-//               tile's rows, all completing on one mbarrier per stage;
+// A cluster of two CTAs computes a 256-row x 256-token tile of y^T over all
+// of d_in with 2-SM MMAs (tcgen05 .cta_group::2, M = 256): each CTA owns 128
+// rows (its tensor-memory lanes, for the A operand and the accumulator) and
+// stages half of the tile's tokens, which the pair's MMAs read from both
+// CTAs' shared memory.  So an SM takes in 34 KB per 64-column k-step (x half,
+// W_base rows, signs) instead of the 50 KB a one-CTA 128 x 256 tile needs for
+// the same FLOPs.  Per CTA, through a 6-stage ring:
+//   warp 0      TMA producer: x tile [128 tokens x 64] (128-byte swizzle),
+//               W_base tile [128 x 64] (128-byte swizzle) and the sign words
+//               of the tile's rows, all completing on one mbarrier per stage;
 //   warps 2..9  transform: thread = one row of the tile (TMEM lane) and one
 //               32-column half of the k-step (two warps per TMEM lane
 //               quarter); reads its 32 W_base values from shared memory, adds
-//               +alpha or -alpha per
-//               sign bit with packed bf16 adds (W_eff rounded to bf16, the
-//               MMA's input precision), and writes them into the stage's
-//               A-operand columns of tensor memory with tcgen05.st;
-//   warp 1      one thread issues tcgen05.mma (kind::f16, M=128, N=256,
-//               K=16; A from tensor memory, B from shared memory, fp32
-//               accumulator in tensor memory) and frees each stage with
-//               tcgen05.commit;
-//   warps 2..9  epilogue: tcgen05.ld of the accumulator (each warp half of
-//               the token columns of its lane quarter), bf16/fp32 stores.
+//               +alpha or -alpha per sign bit with packed bf16 adds (W_eff
+//               rounded to bf16, the MMA's input precision), writes them into
+//               the stage's A-operand columns of its CTA's tensor memory with
+//               tcgen05.st and arrives on the even CTA's stage barrier;
+//   warp 1      in the even CTA, one thread issues the pair's tcgen05.mma
+//               (kind::f16, M=256, N=256, K=16; A from tensor memory, B from
+//               shared memory, fp32 accumulator in tensor memory) once both
+//               CTAs' transforms of a stage are in, and frees the stage in both
+//               CTAs with a multicast tcgen05.commit;
+//   warps 2..9  epilogue: tcgen05.ld of the CTA's accumulator rows (each warp
+//               half of the token columns of its lane quarter), bf16/fp32
+//               stores.
 // So W_eff never goes through shared memory: per k-step the shared memory
 // sees the W and x tiles written once by TMA, W read once by the transform
-// and x read once by the tensor core.
+// and x read once by the tensor cores.
 //
 // Grouped form (multi-variant prefill, bd_linear_multi with large T): x is
 // gathered into token order sorted by variant (key = vid + 1), and each
 // 256-token block of the grid lies inside one key's segment, listed by a
 // plan of {first token, segment end, key}.  A block builds W_eff with its
 // key's signs and alpha (alpha = 0 for key 0, the base model: W_eff = W_base
-// exactly) and writes only the rows of its own segment, in caller order.
+// exactly) and writes only the rows of its own segment, in caller order.  A
+// block of n < 256 tokens (a segment's tail) runs its MMAs with N = n rounded
+// up to 16, the even CTA staging the first N/2 of its tokens and the odd CTA
+// the next N/2.
 //
 // Every mbarrier wait is bounded; a timeout sets the error word, stops every
-// role at its next wait, drains the copies in flight, waits for the issued
-// MMAs and frees tensor memory.
+// role of the CTA at its next wait (the other CTA of the pair then times out
+// on its own waits), drains the copies in flight, waits for the issued MMAs,
+// and the pair frees its tensor memory together.
 #include <type_traits>
 
 #include "bd_device.cuh"
@@ -45,21 +56,24 @@
 namespace bd {
 namespace {
 
-constexpr int BM = 128;  // W rows per tile (MMA M, TMEM lanes)
-constexpr int BN = 256;  // tokens per tile (MMA N)
-constexpr int BK = 64;   // k-step (one 128-byte swizzle atom of bf16)
-constexpr int kStages = 4;
-constexpr int kXBytes = BN * BK * 2;                      // 32768
+constexpr int BM = 128;        // W rows per CTA (tensor-memory lanes); a pair covers 2 * BM (MMA M)
+constexpr int BN = 256;        // tokens per pair tile (MMA N)
+constexpr int BNH = BN / 2;    // tokens staged per CTA
+constexpr int BK = 64;         // k-step (one 128-byte swizzle atom of bf16)
+constexpr int kStages = 6;
+constexpr int kXBytes = BNH * BK * 2;                     // 16384
 constexpr int kWBytes = BM * BK * 2;                      // 16384
 constexpr int kSBytes = BM * 16;                          // 4 sign words per row (128 columns)
-constexpr int kStageBytes = kXBytes + kWBytes + kSBytes;  // 51200 (multiple of 1024)
+constexpr int kStageBytes = kXBytes + kWBytes + kSBytes;  // 34816 (multiple of 1024)
 constexpr int kThreads = 320;                             // 10 warps
-constexpr int kTmemCols = 512;                            // D: 256 columns; A ring: 4 x 32 columns
+constexpr int kTmemCols = 512;                            // D: 256 columns; A ring: 6 x 32 columns
 constexpr int kDCol = 0;
 constexpr int kACol = 256;
+constexpr uint16_t kPairMask = 0x3;  // both CTAs of the cluster
+static_assert(kACol + 32 * kStages <= kTmemCols, "tensor-memory columns");
 
 struct PrefillParams {
-    CUtensorMap x_map;  // [T][d_in] bf16, box 64 x 256, 128B swizzle
+    CUtensorMap x_map;  // [T][d_in] bf16, box 64 x 128, 128B swizzle
     CUtensorMap w_map;  // [d_out][d_in] bf16, box 64 x 128, 128B swizzle
     CUtensorMap s_map;  // [d_out][d_in/32] u32, box 4 x 128
     const float* alpha;
@@ -80,24 +94,23 @@ struct GroupedPrefillParams : PrefillParams {
 };
 
 struct PrefillShared {
-    uint64_t full[kStages];   // TMA landed
-    uint64_t afull[kStages];  // transform wrote the A stage (8 warp arrivals)
-    uint64_t empty[kStages];  // MMAs reading the stage finished (tcgen05.commit)
-    uint64_t accum;           // all MMAs finished
+    uint64_t full[kStages];   // this CTA's TMA landed
+    uint64_t afull[kStages];  // even CTA: both CTAs' transforms wrote the A stage (16 warp arrivals)
+    uint64_t empty[kStages];  // the pair MMAs reading the stage finished (multicast tcgen05.commit)
+    uint64_t accum;           // all pair MMAs finished (multicast tcgen05.commit)
     uint32_t tmem_base;
     volatile int abort;
 };
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
-// K-major, N = 256, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BN >> 3) << 17) |
-                            (static_cast<uint32_t>(BM >> 4) << 24);
-
+// Bounded wait; kCluster: acquire at cluster scope (a barrier that the other
+// CTA of the pair arrives on).
+template <bool kCluster = false>
 __device__ __forceinline__ bool pwait(PrefillShared& sh, uint64_t* bar, uint32_t parity, uint32_t* err)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    auto poll = [&] { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll()) return true;
     const uint64_t t0 = global_timer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!poll()) {
         if (sh.abort) return false;
         if (global_timer_ns() - t0 > kWaitLimitNs) {
             sh.abort = 1;
@@ -109,7 +122,7 @@ __device__ __forceinline__ bool pwait(PrefillShared& sh, uint64_t* bar, uint32_t
 }
 
 template <class P>
-__global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ P p)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ P p)
 {
     constexpr bool kGrouped = std::is_same<P, GroupedPrefillParams>::value;
     extern __shared__ uint8_t dyn_raw[];
@@ -117,33 +130,48 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
     uint8_t* dyn = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int64_t tok0 = static_cast<int64_t>(blockIdx.x) * BN, tok_end = p.T;
+    // grid x = 2 * token block + rank in the pair (pairs lie along the
+    // cluster's x dimension), grid y = row pair: consecutive clusters share
+    // W_base rows and walk the token blocks
+    const uint32_t rank = cluster_ctarank();  // 0: even CTA (rows 0..127 of the pair, issues the MMAs)
+    const int tblk = static_cast<int>(blockIdx.x >> 1);
+    int64_t tok0 = static_cast<int64_t>(tblk) * BN, tok_end = p.T;
     const CUtensorMap* s_map = &p.s_map;
     const float* alpha = p.alpha;
     if constexpr (kGrouped) {
-        const int4 b = p.plan[blockIdx.x];
-        if (b.w == 0) return;  // past the plan: the whole CTA leaves before any setup
+        const int4 b = p.plan[tblk];
+        if (b.w == 0) return;  // past the plan: both CTAs of the pair leave before any setup
         tok0 = b.x;
         tok_end = b.y;
         s_map = &p.s_maps[b.z >= 1 ? b.z - 1 : 0];
         alpha = b.z >= 1 ? p.alphas[b.z - 1] : nullptr;  // key 0: alpha = 0, W_eff = W_base
     }
-    const int64_t row0 = static_cast<int64_t>(blockIdx.y) * BM;
+    // MMA N: the whole tile, or a grouped tail's token count rounded up to 16;
+    // this CTA stages tokens tok0 + rank * N/2 .. + N/2 - 1 (rows past N/2 of
+    // the 128-token box are loaded but not multiplied)
+    int nmma = BN;
+    if constexpr (kGrouped) {
+        const int n = tok_end - tok0 < BN ? static_cast<int>(tok_end - tok0) : BN;
+        nmma = (n + 15) / 16 * 16;
+    }
+    const int64_t xtok = tok0 + static_cast<int64_t>(rank) * (nmma / 2);
+    const int64_t row0 = (2 * static_cast<int64_t>(blockIdx.y) + rank) * BM;
     const int nk = static_cast<int>(p.d_in / BK);
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&sh.full[s], 1);
-            mbar_init(&sh.afull[s], 8);
+            mbar_init(&sh.afull[s], 16);
             mbar_init(&sh.empty[s], 1);
         }
         mbar_init(&sh.accum, 1);
         sh.abort = 0;
         fence_mbarrier_init();
     }
-    if (warp == 1) tmem_alloc(&sh.tmem_base, kTmemCols);
+    if (warp == 1) tmem_alloc_pair(&sh.tmem_base, kTmemCols);
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers are initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
@@ -157,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
                     break;
                 uint8_t* st = dyn + s * kStageBytes;
                 mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
-                tma_load_2d(st, &p.x_map, i * BK, static_cast<int>(tok0), &sh.full[s]);
+                tma_load_2d(st, &p.x_map, i * BK, static_cast<int>(xtok), &sh.full[s]);
                 tma_load_2d(st + kXBytes, &p.w_map, i * BK, static_cast<int>(row0), &sh.full[s]);
                 tma_load_2d(st + kXBytes + kWBytes, s_map, 4 * (i / 2), static_cast<int>(row0), &sh.full[s]);
                 ++issued;
@@ -172,30 +200,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            // a grouped block shorter than BN tokens (a segment's tail) runs its
-            // MMAs with N = its token count rounded up to 16 (M = 128 takes N in
-            // steps of 16); the x rows past N are loaded but not multiplied
-            uint32_t idesc = kIdesc;
-            if constexpr (kGrouped) {
-                const int n = tok_end - tok0 < BN ? static_cast<int>(tok_end - tok0) : BN;
-                idesc = idesc_bf16_f32(BM, (n + 15) / 16 * 16);
-            }
+        // ------------------------------------------------------------ MMA issuer (even CTA)
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc = idesc_bf16_f32(2 * BM, nmma);
             int done = 0;
             for (int i = 0; i < nk; ++i) {
                 const int s = i % kStages;
-                if (!pwait(sh, &sh.afull[s], static_cast<uint32_t>(i / kStages) & 1u, p.err)) break;
+                if (!pwait<true>(sh, &sh.afull[s], static_cast<uint32_t>(i / kStages) & 1u, p.err)) break;
                 tc_fence_after();
                 const uint64_t bdesc = smem_desc_sw128(smem_u32(dyn + s * kStageBytes));
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_ts(tmem + kDCol, tmem + kACol + 32 * s + 8 * kk, bdesc + static_cast<uint64_t>(2 * kk),
-                           idesc, (i | kk) != 0 ? 1u : 0u);
-                mma_commit(&sh.empty[s]);
+                    mma_ts_pair(tmem + kDCol, tmem + kACol + 32 * s + 8 * kk, bdesc + static_cast<uint64_t>(2 * kk),
+                                idesc, (i | kk) != 0 ? 1u : 0u);
+                mma_commit_pair(&sh.empty[s], kPairMask);
                 ++done;
             }
-            mma_commit(&sh.accum);  // fires once every MMA issued above has completed
+            mma_commit_pair(&sh.accum, kPairMask);  // fires once every MMA issued above has completed
             // tensor memory is freed below only after those MMAs are done
             const uint64_t t0 = global_timer_ns();
             while (done > 0 && !mbar_try_wait(&sh.accum, 0u) && global_timer_ns() - t0 < kWaitLimitNs) {
@@ -249,12 +270,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
             tmem_st16(lane_addr + kACol + 32 * s + 16 * ch, v);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.afull[s]);
+            if (lane == 0) mbar_arrive_remote(&sh.afull[s], 0);
         }
         // epilogue
         if (ok && __all_sync(0xffffffffu, pwait(sh, &sh.accum, 0u, p.err))) {
             tc_fence_after();
             for (int cb = ch * (BN / 64); cb < (ch + 1) * (BN / 64); ++cb) {
+                if (32 * cb >= nmma) break;
                 uint32_t d[32];
                 tmem_ld32(lane_addr + kDCol + 32 * cb, d);
                 if (row < p.d_out) {
@@ -275,11 +297,15 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_const
         }
     }
 
+    // the pair's MMAs read both CTAs' shared and tensor memory: neither CTA
+    // frees tensor memory or ends before the even CTA's issuer has seen them
+    // finish (or given up)
     tc_fence_before();
     __syncthreads();
+    cluster_sync_all();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
 
@@ -291,7 +317,7 @@ cudaError_t launch_prefill(const PrefillArgs& a, int /*sm_count*/, cudaStream_t 
 {
     static thread_local PrefillParams prm;
     if (!encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.x, static_cast<uint64_t>(a.d_in),
-                       static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, BK, BN,
+                       static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, BK, BNH,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tma_2d(&prm.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
                        static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, BK, BM,
@@ -312,7 +338,8 @@ cudaError_t launch_prefill(const PrefillArgs& a, int /*sm_count*/, cudaStream_t 
     static std::atomic<size_t> smem_set[kHostMaxDevices];
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel<PrefillParams>), smem, smem_set);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>((a.T + BN - 1) / BN), static_cast<unsigned>((a.d_out + BM - 1) / BM));
+    const dim3 grid(static_cast<unsigned>(2 * ((a.T + BN - 1) / BN)),
+                    static_cast<unsigned>((a.d_out + 2 * BM - 1) / (2 * BM)));
     prefill_kernel<PrefillParams><<<grid, kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }
@@ -352,7 +379,7 @@ cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t str
     if (a.V < 1 || a.V > kMaxVariants || a.T < 1) return cudaErrorInvalidValue;
     static thread_local GroupedPrefillParams prm;  // ~9 KB: kept off the stack
     if (!encode_tma_2d(&prm.x_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.xs, static_cast<uint64_t>(a.d_in),
-                       static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, BK, BN,
+                       static_cast<uint64_t>(a.T), static_cast<uint64_t>(a.d_in) * 2, BK, BNH,
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tma_2d(&prm.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
                        static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, BK, BM,
@@ -385,7 +412,7 @@ cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t str
     static std::atomic<size_t> smem_set[kHostMaxDevices];
     e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel<GroupedPrefillParams>), smem, smem_set);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(nblk), static_cast<unsigned>((a.d_out + BM - 1) / BM));
+    const dim3 grid(static_cast<unsigned>(2 * nblk), static_cast<unsigned>((a.d_out + 2 * BM - 1) / (2 * BM)));
     prefill_kernel<GroupedPrefillParams><<<grid, kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }

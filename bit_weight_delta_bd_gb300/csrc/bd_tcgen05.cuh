@@ -118,6 +118,52 @@ __device__ __forceinline__ void mma_ss(uint32_t d_taddr, uint64_t a_desc, uint64
         : "memory");
 }
 
+// ---------------------------------------------------------------- CTA pairs
+// The .cta_group::2 forms, for a kernel whose MMAs span the two CTAs of a
+// cluster pair (M = 256: A rows 0..127 and D rows 0..127 in the even CTA's
+// tensor memory, rows 128..255 in the odd CTA's; B split along N, the first
+// N/2 rows in the even CTA's shared memory, the rest at the same offset in the
+// odd CTA's).  A kernel uses either these or the cta_group::1 forms, never
+// both.  Allocation and deallocation are collective: one warp of each CTA of
+// the pair executes them, and both receive the same tensor-memory address.
+
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D(tmem, both CTAs) (+)= A(tmem, both CTAs) * B(smem desc, both CTAs)^T,
+// kind::f16; issued by one thread of the even CTA.
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_taddr, uint32_t a_taddr, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_taddr),
+        "r"(a_taddr), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on the mbarrier at this shared-memory offset in every CTA of
+// cta_mask when all pair MMAs issued so far by this thread have completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask)
+{
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
+}
+
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
 // K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
