@@ -56,12 +56,12 @@ NCU_TRAFFIC = {
     ("skinny_kernel<1>", "decode"): ("60707ad3c65224a0", "bd_skinny.cu", 499_405_056 + 3_889_920),
     # 4 rows per CTA (kCompressRowsPerCta in bd_internal.h)
     ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_566_080 + 7_655_936),
-    ("prefill_kernel", "prefill"): ("75a701b8cef13e5f", "bd_prefill.cu", 628_431_872 + 62_987_776),
+    ("prefill_kernel", "prefill"): ("705a6fbf4f52e879", "bd_prefill.cu", 591_238_912 + 67_592_704),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
     ("multi_prepare + multi_kernel<8>", "multi"): ("d89f83fcd4e67914", "bd_multi.cu", 255_770_880 + 3_986_432),
     # the grouped prefill_kernel only (router, plan and gather add about 134 MB of x copies)
-    ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("75a701b8cef13e5f", "bd_prefill.cu",
-                                                                      886_299_648 + 65_342_208),
+    ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("705a6fbf4f52e879", "bd_prefill.cu",
+                                                                      1_097_012_736 + 64_569_088),
     ("materialize_kernel", "materialize"): ("fae23fcd0ba90d9b", "bd_materialize.cu", 499_370_496 + 426_232_320),
 }
 

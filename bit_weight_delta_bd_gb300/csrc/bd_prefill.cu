@@ -4,31 +4,35 @@
 //
 //   D[r][t] = sum_k W_eff[r][k] * x[t][k],   y[t][r] = D[r][t]
 //
-// A cluster of two CTAs computes a 256-row x 256-token tile of y^T over all
+// A cluster of two CTAs computes 256-row x 256-token tiles of y^T over all
 // of d_in with 2-SM MMAs (tcgen05 .cta_group::2, M = 256): each CTA owns 128
 // rows (its tensor-memory lanes, for the A operand and the accumulator) and
 // stages half of the tile's tokens, which the pair's MMAs read from both
 // CTAs' shared memory.  So an SM takes in 34 KB per 64-column k-step (x half,
 // W_base rows, signs) instead of the 50 KB a one-CTA 128 x 256 tile needs for
-// the same FLOPs.  Per CTA, through a 6-stage ring:
-//   warp 0      TMA producer: x tile [128 tokens x 64] (128-byte swizzle),
-//               W_base tile [128 x 64] (128-byte swizzle) and the sign words
-//               of the tile's rows, all completing on one mbarrier per stage;
-//   warps 2..9  transform: thread = one row of the tile (TMEM lane) and one
-//               32-column half of the k-step (two warps per TMEM lane
-//               quarter); reads its 32 W_base values from shared memory, adds
-//               +alpha or -alpha per sign bit with packed bf16 adds (W_eff
-//               rounded to bf16, the MMA's input precision), writes them into
-//               the stage's A-operand columns of its CTA's tensor memory with
-//               tcgen05.st and arrives on the even CTA's stage barrier;
-//   warp 1      in the even CTA, one thread issues the pair's tcgen05.mma
-//               (kind::f16, M=256, N=256, K=16; A from tensor memory, B from
-//               shared memory, fp32 accumulator in tensor memory) once both
-//               CTAs' transforms of a stage are in, and frees the stage in both
-//               CTAs with a multicast tcgen05.commit;
-//   warps 2..9  epilogue: tcgen05.ld of the CTA's accumulator rows (each warp
-//               half of the token columns of its lane quarter), bf16/fp32
-//               stores.
+// the same FLOPs.  The pairs are persistent (one per two SMs that can hold
+// one; pair c takes tiles c, c + C, ...), so each role runs ahead into the
+// next tile while the current one drains.  Per CTA, through a 6-stage ring:
+//   warp 0       TMA producer: x tile [128 tokens x 64] (128-byte swizzle),
+//                W_base tile [128 x 64] (128-byte swizzle) and the sign words
+//                of the tile's rows, all completing on one mbarrier per stage;
+//   warps 2..9   transform: thread = one row of the tile (TMEM lane) and one
+//                32-column half of the k-step (two warps per TMEM lane
+//                quarter); reads its 32 W_base values from shared memory,
+//                adds +alpha or -alpha per sign bit with packed bf16 adds
+//                (W_eff rounded to bf16, the MMA's input precision), writes
+//                them into the stage's A-operand columns of its CTA's tensor
+//                memory with tcgen05.st and arrives on the even CTA's stage
+//                barrier;
+//   warp 1       in the even CTA, one thread issues the pair's tcgen05.mma
+//                (kind::f16, M=256, N=256, K=16; A from tensor memory, B from
+//                shared memory, fp32 accumulator in tensor memory) once both
+//                CTAs' transforms of a stage are in, frees the stage in both
+//                CTAs with a multicast tcgen05.commit, and starts a tile only
+//                once both CTAs' epilogues have released the accumulator;
+//   warps 10..17 epilogue: tcgen05.ld of the CTA's accumulator rows (two
+//                warps per lane quarter, 128 token columns each), released as
+//                soon as it is in registers (bf16 output), then the stores.
 // So W_eff never goes through shared memory: per k-step the shared memory
 // sees the W and x tiles written once by TMA, W read once by the transform
 // and x read once by the tensor cores.
@@ -47,6 +51,8 @@
 // role of the CTA at its next wait (the other CTA of the pair then times out
 // on its own waits), drains the copies in flight, waits for the issued MMAs,
 // and the pair frees its tensor memory together.
+#include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "bd_device.cuh"
@@ -65,7 +71,8 @@ constexpr int kXBytes = BNH * BK * 2;                     // 16384
 constexpr int kWBytes = BM * BK * 2;                      // 16384
 constexpr int kSBytes = BM * 16;                          // 4 sign words per row (128 columns)
 constexpr int kStageBytes = kXBytes + kWBytes + kSBytes;  // 34816 (multiple of 1024)
-constexpr int kThreads = 320;                             // 10 warps
+constexpr int kThreads = 576;                             // 18 warps
+constexpr int kEpilogueWarp0 = 10;                        // warps 10..17: epilogue
 constexpr int kTmemCols = 512;                            // D: 256 columns; A ring: 6 x 32 columns
 constexpr int kDCol = 0;
 constexpr int kACol = 256;
@@ -81,6 +88,7 @@ struct PrefillParams {
     uint32_t* err;
     int64_t T, d_out, d_in;
     int per_row, out_f32;
+    int ntb;  // 256-token blocks (grouped: plan entries, some past the plan)
 };
 
 // Multi-variant prefill: the single-variant fields describe the gathered x
@@ -97,7 +105,9 @@ struct PrefillShared {
     uint64_t full[kStages];   // this CTA's TMA landed
     uint64_t afull[kStages];  // even CTA: both CTAs' transforms wrote the A stage (16 warp arrivals)
     uint64_t empty[kStages];  // the pair MMAs reading the stage finished (multicast tcgen05.commit)
-    uint64_t accum;           // all pair MMAs finished (multicast tcgen05.commit)
+    uint64_t accum;           // a tile's pair MMAs finished (multicast tcgen05.commit; one phase per tile)
+    uint64_t dfree;           // even CTA: both CTAs' epilogues read the accumulator (16 warp arrivals)
+    uint64_t mma_done;        // even CTA: every MMA it issued finished (teardown)
     uint32_t tmem_base;
     volatile int abort;
 };
@@ -121,41 +131,61 @@ __device__ __forceinline__ bool pwait(PrefillShared& sh, uint64_t* bar, uint32_t
     return true;
 }
 
+// The tile a CTA pair works on: tokens [tok0, tok_end) of a 256-token block
+// (MMA N = nmma), this CTA's 128 rows from row0, its x rows from xtok, and
+// the key's sign map and alpha.  Tiles are numbered row pair major, token
+// block minor, so the clusters in flight share W_base rows in L2.
+struct TileInfo {
+    int64_t tok0, tok_end, xtok, row0;
+    const CUtensorMap* s_map;
+    const float* alpha;
+    int nmma;
+    bool valid;
+};
+
+template <class P>
+__device__ __forceinline__ TileInfo tile_info(const P& p, int t, uint32_t rank)
+{
+    constexpr bool kGrouped = std::is_same<P, GroupedPrefillParams>::value;
+    TileInfo ti;
+    const int tb = t % p.ntb, rp = t / p.ntb;
+    ti.row0 = (2 * static_cast<int64_t>(rp) + rank) * BM;
+    ti.tok0 = static_cast<int64_t>(tb) * BN;
+    ti.tok_end = p.T;
+    ti.s_map = &p.s_map;
+    ti.alpha = p.alpha;
+    ti.nmma = BN;
+    ti.valid = true;
+    if constexpr (kGrouped) {
+        const int4 b = p.plan[tb];
+        ti.valid = b.w != 0;  // past the plan
+        ti.tok0 = b.x;
+        ti.tok_end = b.y;
+        ti.s_map = &p.s_maps[b.z >= 1 ? b.z - 1 : 0];
+        ti.alpha = b.z >= 1 ? p.alphas[b.z - 1] : nullptr;  // key 0: alpha = 0, W_eff = W_base
+        // a segment's tail: N = its token count rounded up to 16
+        const int n = ti.tok_end - ti.tok0 < BN ? static_cast<int>(ti.tok_end - ti.tok0) : BN;
+        ti.nmma = (n + 15) / 16 * 16;
+    }
+    // this CTA stages tokens tok0 + rank * N/2 .. + N/2 - 1 (rows past N/2 of
+    // the 128-token box are loaded but not multiplied)
+    ti.xtok = ti.tok0 + static_cast<int64_t>(rank) * (ti.nmma / 2);
+    return ti;
+}
+
 template <class P>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefill_kernel(const __grid_constant__ P p)
 {
-    constexpr bool kGrouped = std::is_same<P, GroupedPrefillParams>::value;
     extern __shared__ uint8_t dyn_raw[];
     __shared__ PrefillShared sh;
     uint8_t* dyn = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // grid x = 2 * token block + rank in the pair (pairs lie along the
-    // cluster's x dimension), grid y = row pair: consecutive clusters share
-    // W_base rows and walk the token blocks
     const uint32_t rank = cluster_ctarank();  // 0: even CTA (rows 0..127 of the pair, issues the MMAs)
-    const int tblk = static_cast<int>(blockIdx.x >> 1);
-    int64_t tok0 = static_cast<int64_t>(tblk) * BN, tok_end = p.T;
-    const CUtensorMap* s_map = &p.s_map;
-    const float* alpha = p.alpha;
-    if constexpr (kGrouped) {
-        const int4 b = p.plan[tblk];
-        if (b.w == 0) return;  // past the plan: both CTAs of the pair leave before any setup
-        tok0 = b.x;
-        tok_end = b.y;
-        s_map = &p.s_maps[b.z >= 1 ? b.z - 1 : 0];
-        alpha = b.z >= 1 ? p.alphas[b.z - 1] : nullptr;  // key 0: alpha = 0, W_eff = W_base
-    }
-    // MMA N: the whole tile, or a grouped tail's token count rounded up to 16;
-    // this CTA stages tokens tok0 + rank * N/2 .. + N/2 - 1 (rows past N/2 of
-    // the 128-token box are loaded but not multiplied)
-    int nmma = BN;
-    if constexpr (kGrouped) {
-        const int n = tok_end - tok0 < BN ? static_cast<int>(tok_end - tok0) : BN;
-        nmma = (n + 15) / 16 * 16;
-    }
-    const int64_t xtok = tok0 + static_cast<int64_t>(rank) * (nmma / 2);
-    const int64_t row0 = (2 * static_cast<int64_t>(blockIdx.y) + rank) * BM;
+    // persistent pairs: cluster c takes tiles c, c + C, c + 2C, ... (pairs lie
+    // along the cluster's x dimension: grid x = 2 * C)
+    const int cid = static_cast<int>(blockIdx.x >> 1), ncl = static_cast<int>(gridDim.x >> 1);
+    const int ntiles = p.ntb * static_cast<int>((p.d_out + 2 * BM - 1) / (2 * BM));
     const int nk = static_cast<int>(p.d_in / BK);
 
     if (tid == 0) {
@@ -165,6 +195,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefill
             mbar_init(&sh.empty[s], 1);
         }
         mbar_init(&sh.accum, 1);
+        mbar_init(&sh.dfree, 16);
+        mbar_init(&sh.mma_done, 1);
         sh.abort = 0;
         fence_mbarrier_init();
     }
@@ -175,125 +207,203 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefill
     tc_fence_after();
     const uint32_t tmem = sh.tmem_base;
 
+    // Every role walks the same tiles and k-steps; g counts k-steps over all
+    // of them (ring slot g % kStages, phase g / kStages), j counts tiles
+    // (accumulator phase j).
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % kStages;
-                if (i >= kStages && !pwait(sh, &sh.empty[s], static_cast<uint32_t>(i / kStages - 1) & 1u, p.err))
-                    break;
-                uint8_t* st = dyn + s * kStageBytes;
-                mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
-                tma_load_2d(st, &p.x_map, i * BK, static_cast<int>(xtok), &sh.full[s]);
-                tma_load_2d(st + kXBytes, &p.w_map, i * BK, static_cast<int>(row0), &sh.full[s]);
-                tma_load_2d(st + kXBytes + kWBytes, s_map, 4 * (i / 2), static_cast<int>(row0), &sh.full[s]);
-                ++issued;
+            uint32_t g = 0;
+            bool ok = true;
+            for (int t = cid; t < ntiles && ok; t += ncl) {
+                const TileInfo ti = tile_info(p, t, rank);
+                if (!ti.valid) continue;
+                for (int i = 0; i < nk; ++i, ++g) {
+                    const int s = static_cast<int>(g % kStages);
+                    if (g >= kStages && !pwait(sh, &sh.empty[s], (g / kStages - 1) & 1u, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = dyn + s * kStageBytes;
+                    mbar_arrive_expect_tx(&sh.full[s], kStageBytes);
+                    tma_load_2d(st, &p.x_map, i * BK, static_cast<int>(ti.xtok), &sh.full[s]);
+                    tma_load_2d(st + kXBytes, &p.w_map, i * BK, static_cast<int>(ti.row0), &sh.full[s]);
+                    tma_load_2d(st + kXBytes + kWBytes, ti.s_map, 4 * (i / 2), static_cast<int>(ti.row0),
+                                &sh.full[s]);
+                }
             }
             // copies still in flight must land before the CTA ends
-            for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i) {
-                const int s = i % kStages;
-                const uint32_t par = static_cast<uint32_t>(i / kStages) & 1u;
+            for (uint32_t u = g > kStages ? g - kStages : 0; u < g; ++u) {
                 const uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(&sh.full[s], par) && global_timer_ns() - t0 < kWaitLimitNs) {
+                while (!mbar_try_wait(&sh.full[u % kStages], (u / kStages) & 1u) &&
+                       global_timer_ns() - t0 < kWaitLimitNs) {
                 }
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (even CTA)
         if (lane == 0 && rank == 0) {
-            const uint32_t idesc = idesc_bf16_f32(2 * BM, nmma);
-            int done = 0;
-            for (int i = 0; i < nk; ++i) {
-                const int s = i % kStages;
-                if (!pwait<true>(sh, &sh.afull[s], static_cast<uint32_t>(i / kStages) & 1u, p.err)) break;
+            uint32_t g = 0, j = 0;
+            bool ok = true;
+            for (int t = cid; t < ntiles && ok; t += ncl) {
+                const TileInfo ti = tile_info(p, t, rank);
+                if (!ti.valid) continue;
+                // the accumulator is free once both CTAs' epilogues have read the previous tile
+                if (j > 0 && !pwait<true>(sh, &sh.dfree, (j - 1) & 1u, p.err)) break;
                 tc_fence_after();
-                const uint64_t bdesc = smem_desc_sw128(smem_u32(dyn + s * kStageBytes));
+                const uint32_t idesc = idesc_bf16_f32(2 * BM, ti.nmma);
+                for (int i = 0; i < nk; ++i, ++g) {
+                    const int s = static_cast<int>(g % kStages);
+                    if (!pwait<true>(sh, &sh.afull[s], (g / kStages) & 1u, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t bdesc = smem_desc_sw128(smem_u32(dyn + s * kStageBytes));
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_ts_pair(tmem + kDCol, tmem + kACol + 32 * s + 8 * kk, bdesc + static_cast<uint64_t>(2 * kk),
-                                idesc, (i | kk) != 0 ? 1u : 0u);
-                mma_commit_pair(&sh.empty[s], kPairMask);
-                ++done;
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_ts_pair(tmem + kDCol, tmem + kACol + 32 * s + 8 * kk,
+                                    bdesc + static_cast<uint64_t>(2 * kk), idesc, (i | kk) != 0 ? 1u : 0u);
+                    mma_commit_pair(&sh.empty[s], kPairMask);
+                }
+                if (ok) {
+                    mma_commit_pair(&sh.accum, kPairMask);  // the tile's accumulator is complete
+                    ++j;
+                }
             }
-            mma_commit_pair(&sh.accum, kPairMask);  // fires once every MMA issued above has completed
-            // tensor memory is freed below only after those MMAs are done
+            // tensor memory is freed below only after every MMA issued above is done
+            mma_commit_pair(&sh.mma_done, 0x1);
             const uint64_t t0 = global_timer_ns();
-            while (done > 0 && !mbar_try_wait(&sh.accum, 0u) && global_timer_ns() - t0 < kWaitLimitNs) {
+            while (!mbar_try_wait(&sh.mma_done, 0u) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
-    } else {
-        // ------------------------------------------------------------ transform, then epilogue
+    } else if (warp < kEpilogueWarp0) {
+        // ------------------------------------------------------------ transform
         const int quarter = warp & 3;     // TMEM lanes 32*quarter .. +31
         const int ch = (warp - 2) >> 2;   // column half of the k-step (warps 2..5 -> 0, 6..9 -> 1)
         const int rl = 32 * quarter + lane;
-        const int64_t row = row0 + rl;
-        float a = 0.0f;
-        if (alpha && row < p.d_out) a = alpha[p.per_row ? row : 0];
-        const uint32_t ab = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a)));
-        const uint32_t neg = ((ab << 16) | ab) ^ 0x80008000u;  // (-alpha, -alpha) as bf16x2
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+        uint32_t g = 0;
         bool ok = true;
-        for (int i = 0; i < nk; ++i) {
-            const int s = i % kStages;
-            if (!__all_sync(0xffffffffu, pwait(sh, &sh.full[s], static_cast<uint32_t>(i / kStages) & 1u, p.err))) {
-                ok = false;
-                break;
-            }
-            const uint8_t* st = dyn + s * kStageBytes;
-            const uint8_t* wrow = st + kXBytes + rl * 128;
-            const uint32_t* srow = reinterpret_cast<const uint32_t*>(st + kXBytes + kWBytes + rl * 16);
-            const uint32_t word = srow[2 * (i & 1) + ch];  // sign bits of this warp's 32 columns
-            uint32_t v[16];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                const int cc = 4 * ch + c;  // 16-byte chunk within the 128-byte row
-                const uint4 u = *reinterpret_cast<const uint4*>(wrow + ((cc ^ (rl & 7)) << 4));
-                v[4 * c + 0] = u.x;
-                v[4 * c + 1] = u.y;
-                v[4 * c + 2] = u.z;
-                v[4 * c + 3] = u.w;
-            }
-#pragma unroll
-            for (int hw = 0; hw < 2; ++hw) {  // 16 columns per sign half-word
-                const uint32_t h = (word >> (16 * hw)) & 0xFFFFu;
-                const uint32_t z = (h | (h << 15)) & 0x55555555u;
-#pragma unroll
-                for (int pp = 0; pp < 8; ++pp) {
-                    const uint32_t add = neg ^ ((z << (15 - 2 * pp)) & 0x80008000u);  // +alpha where bit = 1
-                    __nv_bfloat162 w2 = *reinterpret_cast<__nv_bfloat162*>(&v[8 * hw + pp]);
-                    const __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(&add);
-                    w2 = __hadd2(w2, a2);
-                    v[8 * hw + pp] = *reinterpret_cast<uint32_t*>(&w2);
+        for (int t = cid; t < ntiles && ok; t += ncl) {
+            const TileInfo ti = tile_info(p, t, rank);
+            if (!ti.valid) continue;
+            const int64_t row = ti.row0 + rl;
+            float a = 0.0f;
+            if (ti.alpha && row < p.d_out) a = ti.alpha[p.per_row ? row : 0];
+            const uint32_t ab = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a)));
+            const uint32_t neg = ((ab << 16) | ab) ^ 0x80008000u;  // (-alpha, -alpha) as bf16x2
+            for (int i = 0; i < nk; ++i, ++g) {
+                const int s = static_cast<int>(g % kStages);
+                if (!__all_sync(0xffffffffu, pwait(sh, &sh.full[s], (g / kStages) & 1u, p.err))) {
+                    ok = false;
+                    break;
                 }
-            }
-            tmem_st16(lane_addr + kACol + 32 * s + 16 * ch, v);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(&sh.afull[s], 0);
-        }
-        // epilogue
-        if (ok && __all_sync(0xffffffffu, pwait(sh, &sh.accum, 0u, p.err))) {
-            tc_fence_after();
-            for (int cb = ch * (BN / 64); cb < (ch + 1) * (BN / 64); ++cb) {
-                if (32 * cb >= nmma) break;
-                uint32_t d[32];
-                tmem_ld32(lane_addr + kDCol + 32 * cb, d);
-                if (row < p.d_out) {
+                const uint8_t* st = dyn + s * kStageBytes;
+                const uint8_t* wrow = st + kXBytes + rl * 128;
+                const uint32_t* srow = reinterpret_cast<const uint32_t*>(st + kXBytes + kWBytes + rl * 16);
+                const uint32_t word = srow[2 * (i & 1) + ch];  // sign bits of this warp's 32 columns
+                uint32_t v[16];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        int64_t t = tok0 + 32 * cb + j;
-                        if (t < tok_end) {
-                            if constexpr (kGrouped) t = p.perm[t];
-                            const float val = __uint_as_float(d[j]);
-                            if (p.out_f32)
-                                static_cast<float*>(p.y)[t * p.d_out + row] = val;
-                            else
-                                static_cast<__nv_bfloat16*>(p.y)[t * p.d_out + row] = __float2bfloat16_rn(val);
+                for (int c = 0; c < 4; ++c) {
+                    const int cc = 4 * ch + c;  // 16-byte chunk within the 128-byte row
+                    const uint4 u = *reinterpret_cast<const uint4*>(wrow + ((cc ^ (rl & 7)) << 4));
+                    v[4 * c + 0] = u.x;
+                    v[4 * c + 1] = u.y;
+                    v[4 * c + 2] = u.z;
+                    v[4 * c + 3] = u.w;
+                }
+#pragma unroll
+                for (int hw = 0; hw < 2; ++hw) {  // 16 columns per sign half-word
+                    const uint32_t h = (word >> (16 * hw)) & 0xFFFFu;
+                    const uint32_t z = (h | (h << 15)) & 0x55555555u;
+#pragma unroll
+                    for (int pp = 0; pp < 8; ++pp) {
+                        const uint32_t add = neg ^ ((z << (15 - 2 * pp)) & 0x80008000u);  // +alpha where bit = 1
+                        __nv_bfloat162 w2 = *reinterpret_cast<__nv_bfloat162*>(&v[8 * hw + pp]);
+                        const __nv_bfloat162 a2 = *reinterpret_cast<const __nv_bfloat162*>(&add);
+                        w2 = __hadd2(w2, a2);
+                        v[8 * hw + pp] = *reinterpret_cast<uint32_t*>(&w2);
+                    }
+                }
+                tmem_st16(lane_addr + kACol + 32 * s + 16 * ch, v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(&sh.afull[s], 0);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        // warps 10..17: lane quarter warp % 4, token columns 128 * half ..
+        // +127 of the accumulator.  bf16 output: the columns are read into
+        // registers as packed bf16 and the accumulator is released before
+        // the stores, which then overlap the next tile's MMAs; fp32 output
+        // releases it after the stores.
+        const int quarter = warp & 3;
+        const int half = (warp - kEpilogueWarp0) >> 2;
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * quarter) << 16);
+        uint32_t j = 0;
+        for (int t = cid; t < ntiles; t += ncl) {
+            const TileInfo ti = tile_info(p, t, rank);
+            if (!ti.valid) continue;
+            if (!__all_sync(0xffffffffu, pwait(sh, &sh.accum, j & 1u, p.err))) break;
+            tc_fence_after();
+            const int64_t row = ti.row0 + 32 * quarter + lane;
+            const int c0 = 128 * half;
+            auto store = [&](int col, float val) {
+                int64_t tk = ti.tok0 + col;
+                if (tk >= ti.tok_end || row >= p.d_out) return;
+                if constexpr (std::is_same<P, GroupedPrefillParams>::value) tk = p.perm[tk];
+                if (p.out_f32)
+                    static_cast<float*>(p.y)[tk * p.d_out + row] = val;
+                else
+                    static_cast<__nv_bfloat16*>(p.y)[tk * p.d_out + row] = __float2bfloat16_rn(val);
+            };
+            if (p.out_f32) {
+                for (int cb = 0; cb < 4 && c0 + 32 * cb < ti.nmma; ++cb) {
+                    uint32_t d[32];
+                    tmem_ld32(lane_addr + kDCol + c0 + 32 * cb, d);
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) store(c0 + 32 * cb + jj, __uint_as_float(d[jj]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(&sh.dfree, 0);
+            } else {
+                uint32_t pk[64];  // bf16 pairs of columns c0 + 2q, c0 + 2q + 1
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    pk[8 * c] = pk[8 * c + 1] = pk[8 * c + 2] = pk[8 * c + 3] = 0u;
+                    pk[8 * c + 4] = pk[8 * c + 5] = pk[8 * c + 6] = pk[8 * c + 7] = 0u;
+                    if (c0 + 16 * c < ti.nmma) {
+                        uint32_t d[16];
+                        tmem_ld16(lane_addr + kDCol + c0 + 16 * c, d);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const __nv_bfloat162 h2 =
+                                __floats2bfloat162_rn(__uint_as_float(d[2 * q]), __uint_as_float(d[2 * q + 1]));
+                            pk[8 * c + q] = *reinterpret_cast<const uint32_t*>(&h2);
+                        }
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(&sh.dfree, 0);
+                const int64_t nvalid = ti.tok_end - ti.tok0 - c0;  // columns of this half with a token
+                uint16_t* yb = static_cast<uint16_t*>(p.y);
+#pragma unroll
+                for (int q = 0; q < 64; ++q) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        if (row < p.d_out && 2 * q + e < nvalid) {
+                            int64_t tk = ti.tok0 + c0 + 2 * q + e;
+                            if constexpr (std::is_same<P, GroupedPrefillParams>::value) tk = p.perm[tk];
+                            yb[tk * p.d_out + row] = static_cast<uint16_t>(e ? (pk[q] >> 16) : (pk[q] & 0xFFFFu));
                         }
                     }
                 }
             }
+            ++j;
         }
     }
 
@@ -308,6 +418,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefill
         tmem_dealloc_pair(tmem, kTmemCols);
     }
 }
+
+// Clusters of prefill_kernel<P> resident on the current device at once with
+// this shared-memory size (cached per device): the persistent grid.
+template <class P>
+int resident_clusters(size_t smem)
+{
+    static std::atomic<int> cached[kHostMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kHostMaxDevices) return 1;
+    int n = cached[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    if (cudaOccupancyMaxActiveClusters(&n, prefill_kernel<P>, &cfg) != cudaSuccess || n < 1) {
+        (void)cudaGetLastError();
+        int sms = 0;
+        (void)cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        n = sms >= 4 ? sms / 2 : 1;
+    }
+    cached[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+int row_pairs(int64_t d_out) { return static_cast<int>((d_out + 2 * BM - 1) / (2 * BM)); }
 
 }  // namespace
 
@@ -334,13 +470,14 @@ cudaError_t launch_prefill(const PrefillArgs& a, int /*sm_count*/, cudaStream_t 
     prm.d_in = a.d_in;
     prm.per_row = a.per_row;
     prm.out_f32 = a.out_f32;
+    prm.ntb = static_cast<int>((a.T + BN - 1) / BN);
     const size_t smem = static_cast<size_t>(kStages) * kStageBytes + 1024;
     static std::atomic<size_t> smem_set[kHostMaxDevices];
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel<PrefillParams>), smem, smem_set);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(2 * ((a.T + BN - 1) / BN)),
-                    static_cast<unsigned>((a.d_out + 2 * BM - 1) / (2 * BM)));
-    prefill_kernel<PrefillParams><<<grid, kThreads, smem, stream>>>(prm);
+    const int64_t tiles = static_cast<int64_t>(prm.ntb) * row_pairs(a.d_out);
+    const int64_t ncl = std::min<int64_t>(tiles, resident_clusters<PrefillParams>(smem));
+    prefill_kernel<PrefillParams><<<dim3(static_cast<unsigned>(2 * ncl)), kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }
 
@@ -404,6 +541,7 @@ cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t str
     prm.plan = a.plan;
     prm.perm = a.perm;
     const int nblk = grouped_prefill_blocks(a.T, a.V);
+    prm.ntb = nblk;
     prefill_plan_kernel<<<1, 32, 0, stream>>>(a.seg_off, a.V, nblk, a.plan);
     gather_rows_kernel<<<static_cast<unsigned>(a.T), 256, 0, stream>>>(a.x, a.perm, a.d_in, a.xs);
     cudaError_t e = cudaGetLastError();
@@ -412,8 +550,9 @@ cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t str
     static std::atomic<size_t> smem_set[kHostMaxDevices];
     e = ensure_dynamic_smem(reinterpret_cast<const void*>(prefill_kernel<GroupedPrefillParams>), smem, smem_set);
     if (e != cudaSuccess) return e;
-    const dim3 grid(static_cast<unsigned>(2 * nblk), static_cast<unsigned>((a.d_out + 2 * BM - 1) / (2 * BM)));
-    prefill_kernel<GroupedPrefillParams><<<grid, kThreads, smem, stream>>>(prm);
+    const int64_t tiles = static_cast<int64_t>(nblk) * row_pairs(a.d_out);
+    const int64_t ncl = std::min<int64_t>(tiles, resident_clusters<GroupedPrefillParams>(smem));
+    prefill_kernel<GroupedPrefillParams><<<dim3(static_cast<unsigned>(2 * ncl)), kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }
 
