@@ -50,6 +50,7 @@ EXPORTS = (
     "bd_debug_reconstruct", "bd_check_async", "bd_compress_noalloc",
     "bd_cache_create", "bd_cache_destroy", "bd_cache_set_source", "bd_cache_step", "bd_cache_release",
     "bd_cache_get_stats", "bd_cache_query", "bd_materialize",
+    "bd_monosoup_workspace_size", "bd_monosoup_merge",
 )
 BD_CACHE_SERVED = 0
 BD_CACHE_BASE = 1
@@ -107,6 +108,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "bd_check_async": ([_vp, _vp], _int),
             "bd_compress_noalloc": ([_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp], _int),
             "bd_materialize": ([_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp], _int),
+            "bd_monosoup_workspace_size": ([_i64, _i64, _i32, _i32, _i32], _sz),
+            "bd_monosoup_merge": ([_vp, _vp, _i32, _i64, _i64, _i32, _i32, _i32, _vp, _vp, _int, _vp, _sz, _vp],
+                                  _int),
             "bd_cache_create": ([_vp, _sz, _sz, _i32, ctypes.c_double, _vp, ctypes.POINTER(_vp)], _int),
             "bd_cache_destroy": ([_vp], None),
             "bd_cache_set_source": ([_vp, _i32, _vp, _sz], _int),
@@ -251,6 +255,24 @@ def bd_materialize(w_base, signs, alpha, alpha_mode, w_eff, stream=None) -> None
     _check(load().bd_materialize(_ptr(w_base, "w_base", _BF16_LIKE), _ptr(signs, "signs", (torch.int32, torch.uint32)),
                                  _ptr(alpha, "alpha", (torch.float32,)), int(alpha_mode), d_out, d_in,
                                  _ptr(w_eff, "w_eff", _BF16_LIKE), _stream(stream)), "bd_materialize")
+
+
+def bd_monosoup_workspace_size(d_out: int, d_in: int, k: int, rank: int, l: int) -> int:
+    return int(load().bd_monosoup_workspace_size(d_out, d_in, k, rank, l))
+
+
+def bd_monosoup_merge(w_base, w_ft_list, rank, l, power_iters, omega, w_merged, ws, stream=None) -> None:
+    """W_merged = W_base + (1/k) sum_i truncated_SVD_rank(W_i - W_base); omega [d_in][l] fp32 Gaussian."""
+    d_out, d_in = w_base.shape
+    k = len(w_ft_list)
+    tab = (ctypes.c_void_p * max(k, 1))(*[_ptr(w, "w_ft", _BF16_LIKE) for w in w_ft_list])
+    out_dtype = BD_OUT_F32 if w_merged.dtype == torch.float32 else BD_OUT_BF16
+    wsp, wsn = _ws(ws)
+    _check(load().bd_monosoup_merge(_ptr(w_base, "w_base", _BF16_LIKE), ctypes.addressof(tab), k, d_out, d_in,
+                                    int(rank), int(l), int(power_iters),
+                                    _ptr(omega, "omega", (torch.float32,), allow_none=True),
+                                    _ptr(w_merged, "w_merged", _BF16_LIKE + (torch.float32,)), out_dtype, wsp, wsn,
+                                    _stream(stream)), "bd_monosoup_merge")
 
 
 def bd_route(vid, V, perm, seg_off, ws, stream=None) -> None:

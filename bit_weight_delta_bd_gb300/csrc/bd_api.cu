@@ -175,6 +175,56 @@ bd_status bd_materialize(const uint16_t* w_base, const uint32_t* signs, const fl
                                            sms, static_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------------ MonoSoup merge
+
+size_t bd_monosoup_workspace_size(int64_t d_out, int64_t d_in, int32_t k, int32_t rank, int32_t l)
+{
+    if (d_out < 0 || d_in < 0 || k < 1 || rank < 0 || l < 1) return 0;
+    return bd::monosoup_workspace_size(d_out, d_in, k, rank, l);
+}
+
+bd_status bd_monosoup_merge(const uint16_t* w_base, const uint16_t* const* w_ft, int32_t k, int64_t d_out,
+                            int64_t d_in, int32_t rank, int32_t l, int32_t power_iters, const float* omega,
+                            void* w_merged, int out_dtype, void* ws, size_t ws_bytes, void* stream)
+{
+    if (out_dtype != BD_OUT_BF16 && out_dtype != BD_OUT_F32) return BD_ERR_INVALID_ARG;
+    if (k < 1 || k > BD_MAX_VARIANTS || rank < 0 || l < 1 || l > bd::monosoup_max_l() || rank > l ||
+        power_iters < 0 || power_iters > 16)
+        return BD_ERR_INVALID_ARG;
+    if (d_out < 0) return BD_ERR_UNSUPPORTED_SHAPE;
+    if (bd_status s = check_d_in(d_in)) return s;
+    if (d_out == 0) return BD_OK;
+    if (!w_base || !w_ft || !w_merged || (rank > 0 && !omega)) return BD_ERR_INVALID_ARG;
+    const size_t wbytes = static_cast<size_t>(d_out) * static_cast<size_t>(d_in) * 2;
+    const size_t obytes = wbytes * (out_dtype == BD_OUT_F32 ? 2 : 1);
+    if (!aligned(w_base, 16) || !aligned(w_merged, 16) || (omega && !aligned(omega, 4))) return BD_ERR_MISALIGNED;
+    if (overlaps(w_merged, obytes, w_base, wbytes)) return BD_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < k; ++i) {
+        if (!w_ft[i]) return BD_ERR_INVALID_ARG;
+        if (!aligned(w_ft[i], 16)) return BD_ERR_MISALIGNED;
+        if (overlaps(w_merged, obytes, w_ft[i], wbytes)) return BD_ERR_INVALID_ARG;
+    }
+    if (omega && overlaps(w_merged, obytes, omega, static_cast<size_t>(d_in) * l * 4)) return BD_ERR_INVALID_ARG;
+    if (bd_status s = check_ws(ws, ws_bytes, bd::monosoup_workspace_size(d_out, d_in, k, rank, l))) return s;
+    if (overlaps(ws, ws_bytes, w_merged, obytes)) return BD_ERR_INVALID_ARG;
+    int sms = 0;
+    if (bd_status s = device_info(&sms)) return s;
+    bd::MonoSoupArgs a{};
+    a.w_base = w_base;
+    a.w_ft = w_ft;
+    a.k = k;
+    a.d_out = d_out;
+    a.d_in = d_in;
+    a.rank = rank;
+    a.l = l;
+    a.power_iters = power_iters;
+    a.omega = omega;
+    a.out = w_merged;
+    a.out_f32 = out_dtype == BD_OUT_F32;
+    a.ws = ws;
+    return launched(bd::launch_monosoup(a, static_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------------ linear
 
 size_t bd_linear_workspace_size(int64_t /*T*/, int64_t /*d_out*/, int64_t /*d_in*/) { return kWsHeader; }

@@ -124,6 +124,24 @@ struct GroupedPrefillArgs {
 
 // Upper bound of the 256-token blocks of a grouped prefill: ceil(T / 256) + V + 1.
 int grouped_prefill_blocks(int64_t T, int V);
+
+// ---- MonoSoup merge (bd_monosoup.cu) ---------------------------------------------------------
+
+struct MonoSoupArgs {
+    const uint16_t* w_base;        // [d_out][d_in] bf16 bits
+    const uint16_t* const* w_ft;   // host array of k device pointers, each [d_out][d_in]
+    int k;
+    int64_t d_out, d_in;
+    int rank, l, power_iters;
+    const float* omega;            // [d_in][l] Gaussian test matrix (rank > 0)
+    void* out;                     // [d_out][d_in] bf16 or fp32
+    int out_f32;
+    void* ws;                      // monosoup_workspace_size bytes
+};
+
+int monosoup_max_l();
+size_t monosoup_workspace_size(int64_t d_out, int64_t d_in, int k, int r, int l);
+cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t stream);
 
 }  // namespace bd

@@ -1,0 +1,524 @@
+// MonoSoup merge of k fine-tuned checkpoints of one base matrix (section
+// "MonoSoup" of the BitDelta post):
+//
+//   Delta_i = W_i - W_base,  tau_i = rank-r truncated SVD of Delta_i,
+//   W_merged = W_base + (1/k) * sum_i tau_i.
+//
+// The truncated SVD is computed by randomized subspace iteration (Halko,
+// Martinsson and Tropp, "Finding structure with randomness", 2011: the range
+// finder with power iterations, then the SVD of the small projected matrix):
+//   Y = Delta * Omega          (Omega [d_in][l], Gaussian, given by the caller)
+//   Q = orth(Y); q times: Z = orth(Delta^T Q), Q = orth(Delta Z)
+//   B^T = Delta^T Q            ([d_in][l])
+//   B B^T = U_B Lambda U_B^T   (l x l symmetric eigenproblem, Jacobi)
+//   tau = (Q U_r) (U_r^T B)    (U_r: the r leading eigenvectors)
+// which is U_r S_r V_r^T of the rank-l approximation Q Q^T Delta.  Every pass
+// over Delta reads W_i and W_base (bf16) and forms Delta in fp32 on the fly.
+// Orthonormalisation is CholeskyQR2: the Gram matrix is accumulated in fp64,
+// factored in one CTA, and Y <- Y R^-1 applied twice; directions whose pivot
+// falls below 1e-12 of the largest are dropped (rank-deficient sketches).
+// The merge is one pass: W_base + (1/k) [L_1 .. L_k][R_1 .. R_k]^T with
+// L_i = Q_i U_r, R_i = B_i^T U_r, rounded once to the output type.
+//
+// All arithmetic is fp32 on the CUDA cores except the Gram matrices, the
+// Cholesky factor and the eigenproblem (fp64).  No kernel waits on another
+// CTA; the passes are plain stream-ordered launches.
+#include <cuda_bf16.h>
+
+#include <cmath>
+
+#include <atomic>
+
+#include "bd_device.cuh"
+#include "bd_tma.h"
+
+namespace bd {
+namespace {
+
+constexpr int kMaxL = 64;        // sketch width l (columns of Y, Q, B^T)
+constexpr int kGramBlocks = 64;  // CTAs of one Gram pass (fixed-order fp64 partials)
+// dynamic shared memory of the one-CTA kernels: two fp64 [64][65] matrices
+constexpr size_t kSmallSmem = 2 * sizeof(double) * kMaxL * (kMaxL + 1);
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+// Delta for 8 consecutive columns from two 16-byte loads of bf16 bits.
+__device__ __forceinline__ void delta8(const uint16_t* w, const uint16_t* wb, float* out)
+{
+    const uint4 a = *reinterpret_cast<const uint4*>(w);
+    const uint4 b = *reinterpret_cast<const uint4*>(wb);
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        out[2 * q] = bf16_bits_to_float(av[q] & 0xFFFFu) - bf16_bits_to_float(bv[q] & 0xFFFFu);
+        out[2 * q + 1] = bf16_bits_to_float(av[q] >> 16) - bf16_bits_to_float(bv[q] >> 16);
+    }
+}
+
+// Y[row][c] = sum_j Delta[row][j] * Om[j][c]  (c < l).  32 rows per CTA,
+// d_in in 64-column chunks; each thread holds 2 rows x 4 columns.
+__global__ void __launch_bounds__(256) sketch_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ wb,
+                                                     int64_t d_out, int64_t d_in, const float* __restrict__ om, int l,
+                                                     float* __restrict__ y)
+{
+    __shared__ float sd[32][65];
+    __shared__ __align__(16) float so[64][kMaxL];
+    const int tid = threadIdx.x;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int tr = (tid >> 4) * 2, tc = (tid & 15) * 4;
+    float acc[2][4] = {};
+    for (int64_t j0 = 0; j0 < d_in; j0 += 64) {
+        {
+            const int rr = tid >> 3, cc = (tid & 7) * 8;
+            const int64_t row = r0 + rr;
+            float d[8] = {};
+            if (row < d_out) delta8(w + row * d_in + j0 + cc, wb + row * d_in + j0 + cc, d);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) sd[rr][cc + q] = d[q];
+        }
+        for (int e = tid; e < 64 * kMaxL; e += 256) {
+            const int jj = e / kMaxL, c = e % kMaxL;
+            so[jj][c] = c < l ? om[(j0 + jj) * l + c] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int jj = 0; jj < 64; ++jj) {
+            const float a0 = sd[tr][jj], a1 = sd[tr + 1][jj];
+            const float4 o = *reinterpret_cast<const float4*>(&so[jj][tc]);
+            acc[0][0] = fmaf(a0, o.x, acc[0][0]);
+            acc[0][1] = fmaf(a0, o.y, acc[0][1]);
+            acc[0][2] = fmaf(a0, o.z, acc[0][2]);
+            acc[0][3] = fmaf(a0, o.w, acc[0][3]);
+            acc[1][0] = fmaf(a1, o.x, acc[1][0]);
+            acc[1][1] = fmaf(a1, o.y, acc[1][1]);
+            acc[1][2] = fmaf(a1, o.z, acc[1][2]);
+            acc[1][3] = fmaf(a1, o.w, acc[1][3]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x) {
+        const int64_t row = r0 + tr + x;
+        if (row >= d_out) continue;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            if (tc + q < l) y[row * l + tc + q] = acc[x][q];
+    }
+}
+
+// Bt[j][c] = sum_row Delta[row][j] * Q[row][c]  (c < l).  32 columns of
+// Delta per CTA, all rows in 64-row chunks; each thread holds 2 columns x 4.
+__global__ void __launch_bounds__(256) left_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ wb,
+                                                   int64_t d_out, int64_t d_in, const float* __restrict__ q, int l,
+                                                   float* __restrict__ bt)
+{
+    __shared__ float sd[64][33];
+    __shared__ __align__(16) float sq[64][kMaxL];
+    const int tid = threadIdx.x;
+    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 32;
+    const int tj = (tid >> 4) * 2, tc = (tid & 15) * 4;
+    float acc[2][4] = {};
+    for (int64_t r0 = 0; r0 < d_out; r0 += 64) {
+        {
+            const int rr = tid >> 2, cc = (tid & 3) * 8;
+            const int64_t row = r0 + rr;
+            float d[8] = {};
+            if (row < d_out) delta8(w + row * d_in + j0 + cc, wb + row * d_in + j0 + cc, d);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) sd[rr][cc + e] = d[e];
+        }
+        for (int e = tid; e < 64 * kMaxL; e += 256) {
+            const int rr = e / kMaxL, c = e % kMaxL;
+            const int64_t row = r0 + rr;
+            sq[rr][c] = (c < l && row < d_out) ? q[row * l + c] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 8
+        for (int rr = 0; rr < 64; ++rr) {
+            const float a0 = sd[rr][tj], a1 = sd[rr][tj + 1];
+            const float4 o = *reinterpret_cast<const float4*>(&sq[rr][tc]);
+            acc[0][0] = fmaf(a0, o.x, acc[0][0]);
+            acc[0][1] = fmaf(a0, o.y, acc[0][1]);
+            acc[0][2] = fmaf(a0, o.z, acc[0][2]);
+            acc[0][3] = fmaf(a0, o.w, acc[0][3]);
+            acc[1][0] = fmaf(a1, o.x, acc[1][0]);
+            acc[1][1] = fmaf(a1, o.y, acc[1][1]);
+            acc[1][2] = fmaf(a1, o.z, acc[1][2]);
+            acc[1][3] = fmaf(a1, o.w, acc[1][3]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int x = 0; x < 2; ++x)
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq)
+            if (tc + qq < l) bt[(j0 + tj + x) * l + tc + qq] = acc[x][qq];
+}
+
+// Partial Gram matrices of A [n][l]: CTA b sums A^T A over its contiguous row
+// range in fp64 into part[b][64][64] (entries past l are zero).
+__global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, int64_t n, int l,
+                                                   double* __restrict__ part)
+{
+    __shared__ float sa[32][kMaxL + 1];
+    const int tid = threadIdx.x;
+    const int64_t per = (n + kGramBlocks - 1) / kGramBlocks;
+    const int64_t b0 = static_cast<int64_t>(blockIdx.x) * per;
+    const int64_t b1 = b0 + per < n ? b0 + per : n;
+    double acc[16];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) acc[m] = 0.0;
+    for (int64_t r0 = b0; r0 < b1; r0 += 32) {
+        for (int e = tid; e < 32 * kMaxL; e += 256) {
+            const int rr = e / kMaxL, c = e % kMaxL;
+            const int64_t row = r0 + rr;
+            sa[rr][c] = (row < b1 && c < l) ? a[row * l + c] : 0.0f;
+        }
+        __syncthreads();
+        for (int rr = 0; rr < 32; ++rr) {
+#pragma unroll
+            for (int m = 0; m < 16; ++m) {
+                const int p = tid + 256 * m;
+                acc[m] = fma(static_cast<double>(sa[rr][p >> 6]), static_cast<double>(sa[rr][p & 63]), acc[m]);
+            }
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int m = 0; m < 16; ++m) part[static_cast<int64_t>(blockIdx.x) * 4096 + tid + 256 * m] = acc[m];
+}
+
+// Sums the Gram partials (fixed order) into g[64][65] (one CTA, 256 threads).
+__device__ __forceinline__ void sum_partials(const double* __restrict__ part, int l, double (*g)[kMaxL + 1])
+{
+    for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
+        const int i = e >> 6, j = e & 63;
+        double s = 0.0;
+        if (i < l && j < l)
+            for (int b = 0; b < kGramBlocks; ++b) s += part[b * 4096 + e];
+        g[i][j] = s;
+    }
+}
+
+// One CTA: G = sum of the partials; G = R^T R (Cholesky, R upper); minv = R^-1
+// as fp32 [l][l].  A pivot below 1e-12 of the largest diagonal entry drops
+// its direction (its row and column of R^-1 are zero).
+__global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict__ part, int l,
+                                                       float* __restrict__ minv)
+{
+    extern __shared__ double dsm[];  // kSmallSmem bytes: g, then ri
+    double (*g)[kMaxL + 1] = reinterpret_cast<double (*)[kMaxL + 1]>(dsm);
+    double (*ri)[kMaxL + 1] = reinterpret_cast<double (*)[kMaxL + 1]>(dsm + kMaxL * (kMaxL + 1));
+    __shared__ double dmax;
+    __shared__ int dead[kMaxL];
+    const int tid = threadIdx.x;
+    sum_partials(part, l, g);
+    __syncthreads();
+    if (tid == 0) {
+        double m = 0.0;
+        for (int i = 0; i < l; ++i) m = fmax(m, g[i][i]);
+        dmax = m;
+    }
+    __syncthreads();
+    const double tol = 1e-12 * dmax;
+    for (int k = 0; k < l; ++k) {
+        // g holds the trailing Schur complement; row k of R replaces row k of g
+        const double d = g[k][k];
+        const bool live = d > tol && d > 0.0;
+        __syncthreads();
+        if (tid == 0) dead[k] = live ? 0 : 1;
+        const double rkk = live ? sqrt(d) : 0.0;
+        for (int j = k + tid; j < l; j += blockDim.x) g[k][j] = live ? (j == k ? rkk : g[k][j] / rkk) : 0.0;
+        __syncthreads();
+        for (int e = tid; e < l * l; e += blockDim.x) {
+            const int i = e / l, j = e % l;
+            if (i > k && j >= i) g[i][j] -= g[k][i] * g[k][j];
+        }
+        __syncthreads();
+    }
+    // R^-1 (upper triangular) by back substitution, one column per thread
+    for (int j = tid; j < l; j += blockDim.x) {
+        for (int i = 0; i < l; ++i) ri[i][j] = 0.0;
+        if (!dead[j]) {
+            ri[j][j] = 1.0 / g[j][j];
+            for (int i = j - 1; i >= 0; --i) {
+                if (dead[i]) continue;
+                double s = 0.0;
+                for (int m = i + 1; m <= j; ++m) s += g[i][m] * ri[m][j];
+                ri[i][j] = -s / g[i][i];
+            }
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < l * l; e += blockDim.x) minv[e] = static_cast<float>(ri[e / l][e % l]);
+}
+
+// One CTA: the symmetric eigenproblem of G = sum of the partials by cyclic
+// Jacobi with the round-robin pair order (l/2 disjoint rotations per round,
+// at most 40 sweeps); ur[i][m] = the eigenvector of the m-th largest
+// eigenvalue, m < r.
+__global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ part, int l, int r,
+                                                     float* __restrict__ ur)
+{
+    extern __shared__ double dsm[];  // kSmallSmem bytes: A, then V
+    double (*A)[kMaxL + 1] = reinterpret_cast<double (*)[kMaxL + 1]>(dsm);
+    double (*V)[kMaxL + 1] = reinterpret_cast<double (*)[kMaxL + 1]>(dsm + kMaxL * (kMaxL + 1));
+    __shared__ double cs[kMaxL / 2], sn[kMaxL / 2];
+    __shared__ int pp[kMaxL / 2], qq[kMaxL / 2];
+    __shared__ double red[2][256];
+    __shared__ int idx[kMaxL];
+    const int tid = threadIdx.x;
+    sum_partials(part, l, A);
+    for (int e = tid; e < kMaxL * kMaxL; e += blockDim.x) V[e >> 6][e & 63] = (e >> 6) == (e & 63) ? 1.0 : 0.0;
+    __syncthreads();
+    const int n = l + (l & 1);  // even number of players; index l is a dummy when l is odd
+    for (int sweep = 0; sweep < 40; ++sweep) {
+        double off = 0.0, dia = 0.0;
+        for (int e = tid; e < l * l; e += blockDim.x) {
+            const double v = A[e / l][e % l];
+            if (e / l == e % l)
+                dia += v * v;
+            else
+                off += v * v;
+        }
+        red[0][tid] = off;
+        red[1][tid] = dia;
+        __syncthreads();
+        for (int s = 128; s > 0; s >>= 1) {
+            if (tid < s) {
+                red[0][tid] += red[0][tid + s];
+                red[1][tid] += red[1][tid + s];
+            }
+            __syncthreads();
+        }
+        const bool done = !(red[0][0] > 1e-30 * red[1][0]);
+        __syncthreads();
+        if (done) break;
+        for (int t = 0; t + 1 < n; ++t) {
+            if (tid < n / 2) {
+                const int a = tid == 0 ? 0 : 1 + (tid - 1 + t) % (n - 1);
+                const int b = 1 + (n - 2 - tid + t) % (n - 1);
+                const int p = a < b ? a : b, q = a < b ? b : a;
+                double c = 1.0, s = 0.0;
+                if (q < l) {
+                    const double apq = A[p][q];
+                    if (fabs(apq) > 1e-300) {
+                        const double th = (A[q][q] - A[p][p]) / (2.0 * apq);
+                        const double tt = (th >= 0.0 ? 1.0 : -1.0) / (fabs(th) + sqrt(th * th + 1.0));
+                        c = 1.0 / sqrt(tt * tt + 1.0);
+                        s = tt * c;
+                    }
+                }
+                cs[tid] = c;
+                sn[tid] = s;
+                pp[tid] = p;
+                qq[tid] = q;
+            }
+            __syncthreads();
+            // A <- A P and V <- V P (columns p, q of every disjoint pair)
+            for (int e = tid; e < (n / 2) * l; e += blockDim.x) {
+                const int i = e / l, row = e % l;
+                const int p = pp[i], q = qq[i];
+                if (q >= l) continue;
+                const double c = cs[i], s = sn[i];
+                const double ap = A[row][p], aq = A[row][q];
+                A[row][p] = c * ap - s * aq;
+                A[row][q] = s * ap + c * aq;
+                const double vp = V[row][p], vq = V[row][q];
+                V[row][p] = c * vp - s * vq;
+                V[row][q] = s * vp + c * vq;
+            }
+            __syncthreads();
+            // A <- P^T A (rows p, q)
+            for (int e = tid; e < (n / 2) * l; e += blockDim.x) {
+                const int i = e / l, col = e % l;
+                const int p = pp[i], q = qq[i];
+                if (q >= l) continue;
+                const double c = cs[i], s = sn[i];
+                const double ap = A[p][col], aq = A[q][col];
+                A[p][col] = c * ap - s * aq;
+                A[q][col] = s * ap + c * aq;
+            }
+            __syncthreads();
+        }
+    }
+    if (tid == 0) {
+        for (int i = 0; i < l; ++i) idx[i] = i;
+        for (int i = 0; i < l; ++i) {  // selection sort, largest eigenvalue first (ties: lower index)
+            int best = i;
+            for (int j = i + 1; j < l; ++j)
+                if (A[idx[j]][idx[j]] > A[idx[best]][idx[best]]) best = j;
+            const int tmp = idx[i];
+            idx[i] = idx[best];
+            idx[best] = tmp;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < l * r; e += blockDim.x) ur[e] = static_cast<float>(V[e / r][idx[e % r]]);
+}
+
+// dst[row][j] = sum_c src[row][c] * M[c][j]  (c < l, j < m); one row per
+// thread, read whole before any write, so dst may be src when m == l.
+__global__ void __launch_bounds__(256) apply_kernel(const float* src, int64_t n, int l, const float* __restrict__ M,
+                                                    int m, float* dst)
+{
+    __shared__ float sm[kMaxL][kMaxL];
+    for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
+        const int c = e >> 6, j = e & 63;
+        sm[c][j] = (c < l && j < m) ? M[c * m + j] : 0.0f;
+    }
+    __syncthreads();
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (row >= n) return;
+    float v[kMaxL];
+#pragma unroll
+    for (int c = 0; c < kMaxL; ++c) v[c] = c < l ? src[row * l + c] : 0.0f;
+    for (int j = 0; j < m; ++j) {
+        float s = 0.0f;
+#pragma unroll
+        for (int c = 0; c < kMaxL; ++c) s = fmaf(v[c], sm[c][j], s);
+        dst[row * m + j] = s;
+    }
+}
+
+// out[row][j] = W_base[row][j] + inv_k * sum_e L[e][row] Rt[e][j], e over the
+// k * r factor columns (L [k][d_out][r], Rt [k][d_in][r]); 64 x 64 outputs per
+// CTA, 4 x 4 per thread, factor columns in chunks of 32.
+__global__ void __launch_bounds__(256) merge_kernel(const uint16_t* __restrict__ wb, int64_t d_out, int64_t d_in,
+                                                    const float* __restrict__ L, const float* __restrict__ Rt, int k,
+                                                    int r, float inv_k, void* __restrict__ out, int out_f32)
+{
+    __shared__ float sl[64][33];
+    __shared__ float sr[64][33];
+    const int tid = threadIdx.x;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, j0 = static_cast<int64_t>(blockIdx.x) * 64;
+    const int tr = (tid >> 4) * 4, tc = (tid & 15) * 4;
+    float acc[4][4] = {};
+    const int K = k * r;
+    for (int e0 = 0; e0 < K; e0 += 32) {
+        for (int e = tid; e < 64 * 32; e += 256) {
+            const int rr = e >> 5, ee = e & 31, f = e0 + ee;
+            const int fi = f / (r > 0 ? r : 1), fc = f - fi * r;
+            const int64_t row = r0 + rr, col = j0 + rr;
+            sl[rr][ee] = (f < K && row < d_out) ? L[(static_cast<int64_t>(fi) * d_out + row) * r + fc] : 0.0f;
+            sr[rr][ee] = (f < K && col < d_in) ? Rt[(static_cast<int64_t>(fi) * d_in + col) * r + fc] : 0.0f;
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int ee = 0; ee < 32; ++ee) {
+            float a[4], b[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                a[x] = sl[tr + x][ee];
+                b[x] = sr[tc + x][ee];
+            }
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+#pragma unroll
+                for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x], b[y], acc[x][y]);
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int x = 0; x < 4; ++x) {
+        const int64_t row = r0 + tr + x;
+        if (row >= d_out) continue;
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            const int64_t col = j0 + tc + y;
+            const float v = bf16_bits_to_float(wb[row * d_in + col]) + inv_k * acc[x][y];
+            if (out_f32)
+                static_cast<float*>(out)[row * d_in + col] = v;
+            else
+                static_cast<__nv_bfloat16*>(out)[row * d_in + col] = __float2bfloat16_rn(v);
+        }
+    }
+}
+
+size_t up256(size_t b) { return (b + 255) / 256 * 256; }
+
+struct MonoSoupWs {
+    size_t y, z, part, m, L, Rt, total;
+};
+
+MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
+{
+    MonoSoupWs w{};
+    size_t off = 256;  // error word area (unused by these kernels, kept for the common layout)
+    w.y = off;
+    off += up256(static_cast<size_t>(d_out) * l * 4);
+    w.z = off;
+    off += up256(static_cast<size_t>(d_in) * l * 4);
+    w.part = off;
+    off += up256(static_cast<size_t>(kGramBlocks) * 4096 * 8);
+    w.m = off;
+    off += up256(static_cast<size_t>(kMaxL) * kMaxL * 4);
+    w.L = off;
+    off += up256(static_cast<size_t>(k) * d_out * (r > 0 ? r : 1) * 4);
+    w.Rt = off;
+    off += up256(static_cast<size_t>(k) * d_in * (r > 0 ? r : 1) * 4);
+    w.total = off;
+    return w;
+}
+
+}  // namespace
+
+int monosoup_max_l() { return kMaxL; }
+
+size_t monosoup_workspace_size(int64_t d_out, int64_t d_in, int k, int r, int l)
+{
+    return ws_layout(d_out, d_in, k, r, l).total;
+}
+
+cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
+{
+    static std::atomic<size_t> chol_set[kHostMaxDevices], jacobi_set[kHostMaxDevices];
+    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(chol_inv_kernel), kSmallSmem, chol_set);
+    if (e == cudaSuccess)
+        e = ensure_dynamic_smem(reinterpret_cast<const void*>(jacobi_kernel), kSmallSmem, jacobi_set);
+    if (e != cudaSuccess) return e;
+    const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
+    char* w = static_cast<char*>(a.ws);
+    float* Y = reinterpret_cast<float*>(w + lay.y);
+    float* Z = reinterpret_cast<float*>(w + lay.z);
+    double* part = reinterpret_cast<double*>(w + lay.part);
+    float* M = reinterpret_cast<float*>(w + lay.m);
+    float* L = reinterpret_cast<float*>(w + lay.L);
+    float* Rt = reinterpret_cast<float*>(w + lay.Rt);
+    const int l = a.l, r = a.rank;
+    const unsigned gy = static_cast<unsigned>((a.d_out + 31) / 32);
+    const unsigned gl = static_cast<unsigned>(a.d_in / 32);
+    auto orth = [&](float* A, int64_t n) {  // CholeskyQR2: A <- A R^-1, twice
+        for (int pass = 0; pass < 2; ++pass) {
+            gram_kernel<<<kGramBlocks, 256, 0, st>>>(A, n, l, part);
+            chol_inv_kernel<<<1, 256, kSmallSmem, st>>>(part, l, M);
+            apply_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(A, n, l, M, l, A);
+        }
+    };
+    if (r > 0) {
+        for (int i = 0; i < a.k; ++i) {
+            const uint16_t* wi = a.w_ft[i];
+            sketch_kernel<<<gy, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, a.omega, l, Y);
+            orth(Y, a.d_out);
+            for (int it = 0; it < a.power_iters; ++it) {
+                left_kernel<<<gl, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, Z);
+                orth(Z, a.d_in);
+                sketch_kernel<<<gy, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Z, l, Y);
+                orth(Y, a.d_out);
+            }
+            left_kernel<<<gl, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, Z);  // Z = B^T
+            gram_kernel<<<kGramBlocks, 256, 0, st>>>(Z, a.d_in, l, part);               // B B^T
+            jacobi_kernel<<<1, 256, kSmallSmem, st>>>(part, l, r, M);                  // U_r [l][r]
+            apply_kernel<<<static_cast<unsigned>((a.d_out + 255) / 256), 256, 0, st>>>(
+                Y, a.d_out, l, M, r, L + static_cast<size_t>(i) * a.d_out * r);
+            apply_kernel<<<static_cast<unsigned>((a.d_in + 255) / 256), 256, 0, st>>>(
+                Z, a.d_in, l, M, r, Rt + static_cast<size_t>(i) * a.d_in * r);
+        }
+    }
+    const dim3 grid(static_cast<unsigned>(a.d_in / 64), static_cast<unsigned>((a.d_out + 63) / 64));
+    merge_kernel<<<grid, 256, 0, st>>>(a.w_base, a.d_out, a.d_in, L, Rt, r > 0 ? a.k : 0, r,
+                                       1.0f / static_cast<float>(a.k), a.out, a.out_f32);
+    return cudaGetLastError();
+}
+
+}  // namespace bd

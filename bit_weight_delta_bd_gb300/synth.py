@@ -139,3 +139,31 @@ def device_finetuned_weight(seed: int, w_base, b: float):
 
 def slice_variant_scales(seed: int, V: int, b_lo: float = 5e-4, b_hi: float = 2e-3) -> np.ndarray:
     return np.random.default_rng(seed).uniform(b_lo, b_hi, size=V)
+
+
+def monosoup_checkpoints(seed: int, d_out: int, d_in: int, k: int, rank_signal: int,
+                         sigma_hi: float = 4.0, sigma_lo: float = 1.0):
+    """Inputs of a MonoSoup merge (section "MonoSoup" of the BitDelta post):
+    W_base as ``base_weight`` and k fine-tuned checkpoints
+    W_i = bf16(W_base + U_i diag(s) V_i^T), U_i [d_out][rank_signal] and
+    V_i [d_in][rank_signal] standard normal scaled by 1/sqrt(rows) (nearly
+    orthonormal columns), s log-spaced from sigma_hi down to sigma_lo: the
+    few high-variance directions the post says fine-tuning moves a weight
+    along, plus the bf16 rounding of W_i as the small remainder.  Draw order:
+    W_base, then U_i, V_i per checkpoint.  Returns (w_base_bits, [w_i_bits])."""
+    rng = np.random.default_rng(seed)
+    wb = base_weight(rng, d_out, d_in)
+    s = np.geomspace(sigma_hi, sigma_lo, rank_signal) if rank_signal > 0 else np.zeros(0)
+    wb64 = bf16_bits_to_f32(wb).astype(np.float64)
+    out = []
+    for _ in range(k):
+        u = rng.standard_normal((d_out, rank_signal)) / np.sqrt(d_out)
+        v = rng.standard_normal((d_in, rank_signal)) / np.sqrt(d_in)
+        out.append(f32_to_bf16_bits((wb64 + (u * s) @ v.T).astype(np.float32)))
+    return wb, out
+
+
+def gaussian_test_matrix(seed: int, d_in: int, l: int) -> np.ndarray:
+    """Standard normal fp32 [d_in][l]: the random test matrix a randomized
+    range finder draws (here an input, so both sides see the same one)."""
+    return np.random.default_rng(seed).standard_normal((d_in, l), dtype=np.float32)

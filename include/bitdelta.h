@@ -197,6 +197,39 @@ bd_status bd_materialize(const uint16_t* w_base, const uint32_t* signs, const fl
                          int64_t d_out, int64_t d_in, uint16_t* w_eff, void* stream);
 
 /* ------------------------------------------------------------------------
+ * MonoSoup merge -- section "MonoSoup" of the BitDelta post: for k
+ * fine-tuned checkpoints W_1..W_k of one base matrix,
+ *   Delta_i = W_i - W_base,  tau_i = the rank-`rank` truncated SVD of Delta_i,
+ *   W_merged = W_base + (1/k) * sum_i tau_i.
+ * The truncated SVD is computed by randomized subspace iteration (Halko,
+ * Martinsson & Tropp 2011): a sketch Delta_i * omega with the caller's
+ * Gaussian test matrix `omega` (device fp32 [d_in][l], rank <= l <= 64; the
+ * same matrix for every checkpoint), `power_iters` power iterations with
+ * re-orthonormalisation, then the exact SVD of the l x d_in projection.  It
+ * equals the exact truncated SVD when Delta_i has rank <= l; otherwise its
+ * error is governed by the singular values past l (more power iterations and
+ * a larger l reduce it).  fp32 arithmetic with fp64 Gram matrices; the result
+ * is rounded once to `out_dtype`.
+ *   w_base    device bf16 [d_out][d_in], 16-byte aligned
+ *   w_ft      HOST array of k device pointers, each bf16 [d_out][d_in],
+ *             16-byte aligned; 1 <= k <= BD_MAX_VARIANTS
+ *   rank      0 (W_merged = W_base) .. l
+ *   omega     device fp32 [d_in][l], 4-byte aligned (may be NULL if rank = 0)
+ *   w_merged  device [d_out][d_in], bf16 or fp32 by out_dtype, 16-byte
+ *             aligned, overlapping no input and not the workspace
+ *   ws        bd_monosoup_workspace_size(d_out, d_in, k, rank, l) bytes,
+ *             256-byte aligned (scratch: the sketches, Gram partials and the
+ *             rank-`rank` factors of every checkpoint)
+ * d_in must be a positive multiple of 128 (BD_ERR_UNSUPPORTED_SHAPE);
+ * out-of-range k, rank, l or power_iters (0..16) give BD_ERR_INVALID_ARG.
+ * Stream-ordered; the inputs must stay valid until the work completes.
+ * ------------------------------------------------------------------------ */
+size_t bd_monosoup_workspace_size(int64_t d_out, int64_t d_in, int32_t k, int32_t rank, int32_t l);
+bd_status bd_monosoup_merge(const uint16_t* w_base, const uint16_t* const* w_ft, int32_t k, int64_t d_out,
+                            int64_t d_in, int32_t rank, int32_t l, int32_t power_iters, const float* omega,
+                            void* w_merged, int out_dtype, void* ws, size_t ws_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Compression that allocates nothing (the BitDelta post has no counterpart
  * for this entry point; it exists for callers of this library).
  * Some callers cannot call cudaMalloc or hand the library a workspace: code

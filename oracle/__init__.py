@@ -9,7 +9,8 @@ What it follows: "BitDelta: Tek bir GPU kumesinden 14 Zen modeli sunmak"
 (Hanzo blog, 2026-02-28), sections "Matematiksel temel" (eqs. (1)-(3)),
 "Sunum mimarisi" (the conceptual fused_bitdelta_linear listing and the serving
 pipeline) and "Altyapi ayrintilari" (the packed int8 sign storage and float32
-alpha per output dimension).
+alpha per output dimension), and section "MonoSoup" (the rank-r truncated-SVD
+merge of several fine-tuned checkpoints of one base).
 
 Parity status: every function here is pinned by ``tests/test_oracle_*.py``
 (closed forms, brute force, hand-built bit patterns, special cases that reduce
@@ -222,6 +223,31 @@ def linear_multi(x_bits, vid, signs_list, alpha_list, per_row: bool, w_base_bits
     if rc != 0:
         raise ValueError("oracle_linear_multi_rows: bad arguments")
     return y
+
+
+def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
+    """fp64 values of bf16 bit patterns (the upper 16 bits of an fp32)."""
+    return (np.ascontiguousarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def monosoup_merge_f64(w_base: np.ndarray, w_ft_list, rank: int) -> np.ndarray:
+    """MonoSoup merge, section "MonoSoup" of the BitDelta post, in fp64: for
+    each checkpoint the task vector Delta_i = W_i - W_base, its rank-`rank`
+    truncated SVD tau_i = U_i[:, :r] diag(S_i[:r]) Vh_i[:r] (numpy's SVD as
+    the library step), and W_merged = W_base + (1/k) * sum_i tau_i."""
+    w_base = np.asarray(w_base, np.float64)
+    acc = np.zeros_like(w_base)
+    for w in w_ft_list:
+        d = np.asarray(w, np.float64) - w_base
+        if rank > 0:
+            u, sv, vh = np.linalg.svd(d, full_matrices=False)
+            acc += (u[:, :rank] * sv[:rank]) @ vh[:rank]
+    return w_base + acc / len(w_ft_list)
+
+
+def monosoup_merge(w_base_bits: np.ndarray, w_ft_bits_list, rank: int) -> np.ndarray:
+    """``monosoup_merge_f64`` on bf16 weights (Delta_i is exact in fp64)."""
+    return monosoup_merge_f64(bf16_to_f64(w_base_bits), [bf16_to_f64(w) for w in w_ft_bits_list], rank)
 
 
 def compressed_bytes(d_out: int, d_in: int, n_alpha: int) -> int:

@@ -130,3 +130,31 @@ def test_multi_and_route_argument_checks(lib):
     assert lib.bd_route(A, 10, -1, A + (1 << 30), A + (2 << 30), A + (5 << 30), 4096, None) == bd.BD_ERR_INVALID_ARG
     assert lib.bd_route(A, 10, 3, A, A + (2 << 30), A + (5 << 30), 4096, None) == bd.BD_ERR_INVALID_ARG  # perm = vid
     assert lib.bd_check_async(0, None) == bd.BD_ERR_WORKSPACE
+
+
+def test_monosoup_argument_checks(lib):
+    tab = (ctypes.c_void_p * 2)(A + (1 << 30), A + (2 << 30))
+    ws = A + (5 << 30)
+    need = lib.bd_monosoup_workspace_size(16, 256, 2, 4, 8)
+    assert need >= 256 + 16 * 8 * 4 + 256 * 8 * 4
+
+    def m(k=2, d_out=16, d_in=256, rank=4, l=8, q=1, om=A + (3 << 30), out=A + (4 << 30), t=tab, wsb=need,
+          dtype=0):
+        return lib.bd_monosoup_merge(A, ctypes.addressof(t), k, d_out, d_in, rank, l, q, om, out, dtype, ws, wsb,
+                                     None)
+
+    assert m(k=0) == bd.BD_ERR_INVALID_ARG
+    assert m(l=65) == bd.BD_ERR_INVALID_ARG
+    assert m(rank=9) == bd.BD_ERR_INVALID_ARG  # rank > l
+    assert m(rank=-1) == bd.BD_ERR_INVALID_ARG
+    assert m(q=17) == bd.BD_ERR_INVALID_ARG
+    assert m(dtype=3) == bd.BD_ERR_INVALID_ARG
+    assert m(d_in=100) == bd.BD_ERR_UNSUPPORTED_SHAPE
+    assert m(d_out=-1) == bd.BD_ERR_UNSUPPORTED_SHAPE
+    assert m(om=0) == bd.BD_ERR_INVALID_ARG  # rank > 0 needs the test matrix
+    assert m(out=A + (4 << 30) + 8) == bd.BD_ERR_MISALIGNED
+    bad = (ctypes.c_void_p * 2)(A + (1 << 30), A + (2 << 30) + 2)
+    assert m(t=bad) == bd.BD_ERR_MISALIGNED
+    assert m(out=A + (2 << 30)) == bd.BD_ERR_INVALID_ARG  # output overlaps a checkpoint
+    assert m(wsb=need - 1) == bd.BD_ERR_WORKSPACE
+    assert m(d_out=0) == bd.BD_OK

@@ -1,0 +1,111 @@
+"""MonoSoup merge on the GPU (bd_monosoup_merge) against the fp64 oracle:
+section "MonoSoup" of the BitDelta post, tau_i = the rank-r truncated SVD of
+Delta_i = W_i - W_base and W_merged = W_base + (1/k) sum_i tau_i.
+
+The GPU computes the truncated SVD by randomized subspace iteration, the
+oracle by a full SVD.  The inputs have rank-r task vectors (log-spaced
+singular values 4..1) plus the bf16 rounding of the checkpoints, so the
+spectral gap at r is about 1e-3 and after one power iteration the two agree
+to fp32 accuracy (the subspace error falls like the gap cubed)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_weight_delta_bd_gb300 import bitdelta as bd
+from bit_weight_delta_bd_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def dev():
+    assert torch.cuda.is_available()
+    import __graft_entry__
+
+    __graft_entry__.build()
+    return torch.device("cuda:0")
+
+
+def to_dev(a, dev):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
+
+
+def run_gpu(dev, wb, ws, om, rank, l, q, out_dtype):
+    d_out, d_in = wb.shape
+    wb_d = to_dev(wb, dev)
+    ws_d = [to_dev(w, dev) for w in ws]
+    om_d = torch.from_numpy(om).to(dev) if om is not None else None
+    out = torch.empty((d_out, d_in), dtype=out_dtype, device=dev)
+    wsp = bd.new_workspace(bd.bd_monosoup_workspace_size(d_out, d_in, len(ws), rank, l), dev)
+    bd.bd_monosoup_merge(wb_d, ws_d, rank, l, q, om_d, out, wsp)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def bf16_ulp(v):
+    """Spacing of bf16 numbers at |v| (8 significant bits)."""
+    e = np.floor(np.log2(np.maximum(np.abs(v), 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+@pytest.mark.parametrize("d_out,d_in,k,r,l,q", [
+    (256, 384, 3, 8, 16, 1),     # several tiles of every pass
+    (300, 256, 2, 16, 24, 1),    # ragged rows
+    (1000, 512, 4, 12, 32, 2),   # two power iterations, k = 4
+    (8, 128, 2, 4, 16, 1),       # fewer rows than sketch columns (rank-deficient sketch)
+    (512, 640, 1, 32, 64, 1),    # the widest sketch
+])
+def test_monosoup_matches_exact_truncated_svd(dev, d_out, d_in, k, r, l, q):
+    wb, ws = synth.monosoup_checkpoints(7 + d_out, d_out, d_in, k, min(r, d_out))
+    om = synth.gaussian_test_matrix(11 + d_in, d_in, l)
+    ref = oracle.monosoup_merge(wb, ws, r)
+    base = oracle.bf16_to_f64(wb)
+    upd_ref = ref - base
+    got = run_gpu(dev, wb, ws, om, r, l, q, torch.float32).double().numpy()
+    rel = np.linalg.norm((got - base) - upd_ref) / np.linalg.norm(upd_ref)
+    assert rel <= 1e-4, f"relative error of the merged update {rel:.3e}"
+    # bf16 output: one rounding of a value this close to the oracle's lands
+    # on one of the two bf16 neighbours of the exact result; near zero the
+    # fp32 error of the update (about 1e-7 of its largest entry) dominates
+    gb = run_gpu(dev, wb, ws, om, r, l, q, torch.bfloat16).float().double().numpy()
+    assert np.all(np.abs(gb - ref) <= bf16_ulp(ref) + 1e-6 * np.abs(upd_ref).max())
+
+
+def test_monosoup_without_power_iteration(dev):
+    """q = 0: the range finder alone; the error is set by the spectral gap
+    (about 1e-3 here), not by the arithmetic."""
+    wb, ws = synth.monosoup_checkpoints(3, 256, 256, 2, 8)
+    om = synth.gaussian_test_matrix(4, 256, 24)
+    ref = oracle.monosoup_merge(wb, ws, 8)
+    base = oracle.bf16_to_f64(wb)
+    got = run_gpu(dev, wb, ws, om, 8, 24, 0, torch.float32).double().numpy()
+    rel = np.linalg.norm((got - base) - (ref - base)) / np.linalg.norm(ref - base)
+    assert rel <= 1e-2
+
+
+def test_monosoup_rank_zero_is_the_base(dev):
+    wb, ws = synth.monosoup_checkpoints(5, 64, 256, 3, 4)
+    got = run_gpu(dev, wb, ws, None, 0, 8, 1, torch.bfloat16)
+    assert np.array_equal(got.view(torch.int16).numpy().view(np.uint16), wb)
+
+
+def test_monosoup_full_rank_one_checkpoint(dev):
+    """k = 1 and rank = d_out <= l: the sketch spans every row direction, so
+    the merge returns the checkpoint itself (to fp32 accuracy)."""
+    wb, ws = synth.monosoup_checkpoints(6, 16, 256, 1, 16)
+    om = synth.gaussian_test_matrix(8, 256, 32)
+    got = run_gpu(dev, wb, ws, om, 16, 32, 1, torch.float32).double().numpy()
+    np.testing.assert_allclose(got, oracle.bf16_to_f64(ws[0]), rtol=0, atol=2e-6)
+
+
+def test_monosoup_ffn_sized(dev):
+    """2048 x 2048, 3 checkpoints, rank 16: the oracle's full SVD still runs
+    in seconds; the same bound as the small cases."""
+    wb, ws = synth.monosoup_checkpoints(9, 2048, 2048, 3, 16)
+    om = synth.gaussian_test_matrix(10, 2048, 32)
+    ref = oracle.monosoup_merge(wb, ws, 16)
+    base = oracle.bf16_to_f64(wb)
+    got = run_gpu(dev, wb, ws, om, 16, 32, 1, torch.float32).double().numpy()
+    rel = np.linalg.norm((got - base) - (ref - base)) / np.linalg.norm(ref - base)
+    assert rel <= 1e-4, rel

@@ -382,3 +382,72 @@ def test_materialize_is_the_rounded_reconstruction():
     dec = synth.bf16_bits_to_f32(bits).astype(np.float64)
     ulp = 2.0 ** (np.floor(np.log2(np.abs(exact))) - 7)
     assert np.all(np.abs(dec - exact) <= ulp / 2)
+
+
+# ---------------------------------------------------------------- MonoSoup
+# Section "MonoSoup" of the BitDelta post: tau_i = rank-r truncated SVD of
+# Delta_i = W_i - W_base, W_merged = W_base + (1/k) sum_i tau_i.
+
+
+def _orthonormal(rng, n, m):
+    q, _ = np.linalg.qr(rng.standard_normal((n, m)))
+    return q
+
+
+def test_monosoup_truncation_closed_form():
+    """Delta_i = U diag(s) V^T built from orthonormal U, V and decreasing s
+    without any SVD: the rank-r truncation keeps exactly the r leading terms,
+    so the merge is W_base + mean_i U_i[:, :r] diag(s_i[:r]) V_i[:, :r]^T.
+    A dropped 1/k, an off-by-one rank, a transposed factor or a sign slip all
+    fail this (non-square, k = 3)."""
+    rng = np.random.default_rng(0)
+    d_out, d_in, k, r = 24, 40, 3, 4
+    wb = rng.standard_normal((d_out, d_in))
+    ws, expect = [], np.zeros((d_out, d_in))
+    for _ in range(k):
+        u, v = _orthonormal(rng, d_out, 10), _orthonormal(rng, d_in, 10)
+        s = np.sort(rng.uniform(0.5, 5.0, 10))[::-1]
+        ws.append(wb + (u * s) @ v.T)
+        expect += (u[:, :r] * s[:r]) @ v[:, :r].T
+    got = oracle.monosoup_merge_f64(wb, ws, r)
+    np.testing.assert_allclose(got, wb + expect / k, rtol=0, atol=1e-12)
+
+
+def test_monosoup_special_cases():
+    rng = np.random.default_rng(1)
+    wb = rng.standard_normal((12, 16))
+    w1, w2 = wb + rng.standard_normal((12, 16)), wb + rng.standard_normal((12, 16))
+    # rank 0: the base itself
+    np.testing.assert_array_equal(oracle.monosoup_merge_f64(wb, [w1, w2], 0), wb)
+    # full rank, one checkpoint: the checkpoint itself
+    np.testing.assert_allclose(oracle.monosoup_merge_f64(wb, [w1], 12), w1, atol=1e-12)
+    # full rank, several: the plain average of the checkpoints
+    np.testing.assert_allclose(oracle.monosoup_merge_f64(wb, [w1, w2], 12), (w1 + w2) / 2, atol=1e-12)
+    # k copies of one checkpoint merge like that checkpoint alone
+    np.testing.assert_allclose(oracle.monosoup_merge_f64(wb, [w1, w1, w1], 5),
+                               oracle.monosoup_merge_f64(wb, [w1], 5), atol=1e-12)
+
+
+def test_monosoup_eckart_young():
+    """The truncation error ||Delta - tau||_F^2 equals the sum of the
+    eigenvalues of Delta^T Delta past the r largest (eigvalsh, a different
+    routine from the SVD the oracle calls), and projecting Delta on random
+    r-dimensional subspaces never does better (rank-r optimality)."""
+    rng = np.random.default_rng(2)
+    d = rng.standard_normal((30, 20))
+    r = 6
+    tau = oracle.monosoup_merge_f64(np.zeros_like(d), [d], r)
+    assert np.linalg.matrix_rank(tau) == r
+    err = np.sum((d - tau) ** 2)
+    lam = np.sort(np.linalg.eigvalsh(d.T @ d))[::-1]
+    assert abs(err - lam[r:].sum()) <= 1e-9 * lam.sum()
+    for _ in range(20):
+        q = _orthonormal(rng, 30, r)
+        assert np.sum((d - q @ (q.T @ d)) ** 2) >= err * (1 - 1e-12)
+
+
+def test_bf16_to_f64_patterns():
+    bits = np.array([0x3F80, 0xC000, 0x0000, 0x8000, 0x3C23, 0x7F7F], np.uint16)
+    got = oracle.bf16_to_f64(bits)
+    assert got[0] == 1.0 and got[1] == -2.0 and got[2] == 0.0 and np.signbit(got[3])
+    assert got[4] == float.fromhex("0x1.46p-7") and got[5] == float.fromhex("0x1.FEp127")
