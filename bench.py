@@ -68,9 +68,15 @@ NCU_TRAFFIC = {
 
 # kernels each timed call launches: multi = prepare + fused kernel; multi_prefill =
 # router + plan + gather + grouped prefill; slice = 56 multi calls
-LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4}
+LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4, "monosoup": 88}
 # workloads whose own figure is tensor throughput (TFLOP/s) rather than GB/s
 TENSOR_WORKLOADS = ("prefill", "multi_prefill")
+# workloads bound by fp32 CUDA-core arithmetic: their figure is fp32 TFLOP/s
+ALU_WORKLOADS = ("monosoup",)
+# fp32 FMA peak of the GB300 from unit counts: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# MonoSoup workload: k checkpoints, rank r, sketch width l, power iterations q
+MONOSOUP = {"d": 8192, "k": 3, "rank": 16, "l": 32, "q": 1}
 
 
 def parse_args():
@@ -79,7 +85,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill", "multi_prefill", "materialize",
+    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill", "multi_prefill", "materialize", "monosoup",
                                           "slice"], default="decode")
     p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement of the decode line")
     p.add_argument("--seed", type=int, default=0)
@@ -109,6 +115,19 @@ def load_peaks():
 def materialize_bytes(d_out, d_in, n_alpha):
     """W_base read, W_eff written (2 bytes each per weight), bits and alpha read."""
     return 4 * d_out * d_in + d_out * d_in // 8 + 4 * n_alpha
+
+
+def monosoup_bytes(d, k, q):
+    """Each pass over a task vector reads W_i and W_base (2 + 2q + ... passes:
+    sketch, 2q power-iteration products, B^T), plus the merge's W_base read
+    and W_merged write."""
+    return k * (2 + 2 * q) * 4 * d * d + 4 * d * d
+
+
+def monosoup_flops(d, k, rank, l, q):
+    """fp32 FLOPs of the products with the task vectors (2 d^2 l each) and of
+    the rank-(k r) merge (2 d^2 k r)."""
+    return k * (2 + 2 * q) * 2 * d * d * l + 2 * d * d * k * rank
 
 
 def linear_bytes(T, d_out, d_in, n_alpha, y_bytes=2):
@@ -151,6 +170,14 @@ class Workload:
             self.per_row = True
             self.wb, wf, _ = synth.single_problem(seed, d_out, d_in, 1)
             self.wf = [wf]
+            self.xs = []
+            self.vid = None
+        elif name == "monosoup":
+            d_out = d_in = MONOSOUP["d"]
+            self.tokens = []
+            self.per_row = True
+            self.wb, self.wf = synth.monosoup_checkpoints(seed, d_out, d_in, MONOSOUP["k"], MONOSOUP["rank"])
+            self.omega = synth.gaussian_test_matrix(seed + 1, d_in, MONOSOUP["l"])
             self.xs = []
             self.vid = None
         elif name == "prefill":
@@ -199,6 +226,12 @@ class Workload:
             c["workload"] = "materialize_ffn_28672x8192"
             c["step"] = "bd_materialize: W_eff = RN_bf16(W_base + alpha s) written to HBM (variant compressed once, untimed)"
             c["l2"] = "inputs larger than L2 (W_base 470 MB in, W_eff 470 MB out vs 126.5 MB L2)"
+        elif self.name == "monosoup":
+            c = {"workload": f"monosoup_{self.d_out}x{self.d_in}_k{MONOSOUP['k']}_r{MONOSOUP['rank']}",
+                 "d_out": self.d_out, "d_in": self.d_in, **{k: v for k, v in MONOSOUP.items() if k != "d"},
+                 "step": ("bd_monosoup_merge: randomized rank-16 truncated SVD of 3 task vectors (sketch width 32, "
+                          "one power iteration) and the merge W_base + mean tau_i, bf16 out"),
+                 "l2": "inputs larger than L2 (4 x 134 MB of bf16 weights)"}
         elif self.name == "tiny":
             c["workload"] = "tiny_256x256_T4"
             c["step"] = "bd_compress + bd_linear at T=4"
@@ -241,6 +274,11 @@ class GpuRun:
         self.flush = None
         if wl.name == "materialize":
             self.w_eff = torch.empty((wl.d_out, wl.d_in), dtype=torch.int16, device=dev)
+        if wl.name == "monosoup":
+            self.omega = torch.from_numpy(wl.omega).to(dev)
+            self.w_merged = torch.empty((wl.d_out, wl.d_in), dtype=torch.bfloat16, device=dev)
+            self.ws_ms = bd.new_workspace(bd.bd_monosoup_workspace_size(wl.d_out, wl.d_in, len(wl.wf),
+                                                                        MONOSOUP["rank"], MONOSOUP["l"]), dev)
         if wl.name in ("multi", "prefill", "multi_prefill", "materialize"):
             for v in range(len(wl.wf)):  # variants are compressed once, before timing
                 bd.bd_compress(self.wb, self.wf[v], PR, self.signs[v], self.alpha[v], self.ws)
@@ -265,6 +303,14 @@ class GpuRun:
             out.append((f"linear_multi_T{T}", kname, nbytes, flops,
                         lambda: bd.bd_linear_multi(self.xs[0], self.vid, self.signs, self.alpha, self.mode, self.wb,
                                                    self.ys[0], self.ws)))
+            return out
+        if wl.name == "monosoup":
+            m = MONOSOUP
+            out.append(("monosoup_merge", "bd_monosoup_merge (sketch, transpose-product, Gram, merge kernels)",
+                        monosoup_bytes(wl.d_out, len(wl.wf), m["q"]),
+                        monosoup_flops(wl.d_out, len(wl.wf), m["rank"], m["l"], m["q"]),
+                        lambda: bd.bd_monosoup_merge(self.wb, self.wf, m["rank"], m["l"], m["q"], self.omega,
+                                                     self.w_merged, self.ws_ms)))
             return out
         if wl.name == "materialize":
             out.append(("materialize", "materialize_kernel", materialize_bytes(wl.d_out, wl.d_in, wl.n_alpha), 0,
@@ -427,6 +473,23 @@ def oracle_time(wl: Workload, budget_s: float = 12.0, threads: int = 0):
     cores = oracle.set_threads(threads)
     d_out, d_in = wl.d_out, wl.d_in
     step_bytes = sum(c[2] for c in _step_bytes_rows(wl))
+    if wl.name == "monosoup":
+        # the oracle's full SVD on the leading n x n block of each checkpoint,
+        # n doubled while the budget allows, scaled to the full size by the
+        # SVD's n^3 cost
+        n, t_used, t_last = 256, 0.0, 0.0
+        while n <= min(d_out, d_in):
+            t0 = time.perf_counter()
+            oracle.monosoup_merge(wl.wb[:n, :n], [w[:n, :n] for w in wl.wf], MONOSOUP["rank"])
+            t_last = time.perf_counter() - t0
+            t_used += t_last
+            if t_used > budget_s / 4 or 2 * n > min(d_out, d_in):
+                break
+            n *= 2
+        t_full = t_last * (d_out / n) * (d_in / n) * (min(d_out, d_in) / n)
+        return (step_bytes / t_full / 1e9, cores,
+                f"oracle merge of {len(wl.wf)} checkpoints on the leading {n}x{n} block ({t_last:.2f} s, numpy "
+                f"SVD threads), scaled by n^3 to {d_out}x{d_in} ({t_full:.1f} s)")
     if d_out * d_in <= (1 << 20):  # small: whole steps
         n, t_used = 0, 0.0
         while t_used < budget_s or n == 0:
@@ -475,6 +538,8 @@ def _step_bytes_rows(wl: Workload):
         return out
     if wl.name == "materialize":
         return [("materialize", "", materialize_bytes(wl.d_out, wl.d_in, wl.n_alpha))]
+    if wl.name == "monosoup":
+        return [("monosoup", "", monosoup_bytes(wl.d_out, len(wl.wf), MONOSOUP["q"]))]
     if wl.name != "prefill":
         out.append(("compress", "", compress_bytes(wl.d_out, wl.d_in, wl.n_alpha)))
     for T in wl.tokens:
@@ -492,7 +557,10 @@ def dist_setup():
 
 
 def _step_flops(wl: Workload) -> int:
-    """Useful FLOPs of one step of a tensor-bound workload: 2 T d_out d_in per call."""
+    """Useful FLOPs of one step of a tensor- or ALU-bound workload: 2 T d_out
+    d_in per linear call; the MonoSoup merge's fp32 products."""
+    if wl.name == "monosoup":
+        return monosoup_flops(wl.d_out, len(wl.wf), MONOSOUP["rank"], MONOSOUP["l"], MONOSOUP["q"])
     return sum(2 * T * wl.d_out * wl.d_in for T in wl.tokens)
 
 
@@ -514,7 +582,7 @@ def run_reference(args):
     value = statistics.median(vals)
     ms_per_step = step_bytes / (value * 1e9) * 1e3
     unit = "GB/s"
-    if wl.name in TENSOR_WORKLOADS:  # the same unit as the GPU arm's line
+    if wl.name in TENSOR_WORKLOADS or wl.name in ALU_WORKLOADS:  # the same unit as the GPU arm's line
         value = _step_flops(wl) / (ms_per_step * 1e-3) / 1e12
         unit = "TFLOP/s"
     line = {"metric": METRIC, "value": value, "unit": unit, "impl": "reference", "n_gpus": args.gpus,
@@ -623,6 +691,14 @@ def run_gpu(args):
         roofline = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
                     "frac": tf / bf16_peak, "traffic": traffic, "peak_source": f"{peak_src} (bf16_tflops, burst)",
                     "flops_per_launch": flops_per_launch, "avg_launch_us": avg_ms * 1e3}
+    elif wl.name in ALU_WORKLOADS:
+        flops_per_launch = calls[0][3]
+        tf = flops_per_launch / (avg_ms * 1e-3) / 1e12
+        roofline = {"bound": "alu", "kernel": dom, "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                    "frac": tf / FP32_PEAK_TFLOPS, "traffic": traffic,
+                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (fp32 FMA)",
+                    "flops_per_launch": flops_per_launch, "avg_launch_us": avg_ms * 1e3,
+                    "hbm_achieved_gbs": achieved, "hbm_frac": achieved / hbm_peak}
     else:
         roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                     "frac": achieved / hbm_peak, "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)",
@@ -641,7 +717,7 @@ def run_gpu(args):
             dist.all_reduce(t, op=dist.ReduceOp.MAX)
             e2e["ms_per_step"] = float(t.item())
         e2e["value"] = world * step_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9
-        if wl.name in TENSOR_WORKLOADS:
+        if wl.name in TENSOR_WORKLOADS or wl.name in ALU_WORKLOADS:
             e2e["value"] = world * calls[0][3] / (e2e["ms_per_step"] * 1e-3) / 1e12
             e2e["unit"] = "TFLOP/s"
 
@@ -659,18 +735,18 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu and wl.name != "slice":
         gbs, cores, sample = oracle_time(wl)
         cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
-        if wl.name in TENSOR_WORKLOADS:  # in the line's own unit
+        if wl.name in TENSOR_WORKLOADS or wl.name in ALU_WORKLOADS:  # in the line's own unit
             cpu["value"] = _step_flops(wl) / (step_bytes / (gbs * 1e9)) / 1e12
             cpu["unit"] = "TFLOP/s"
 
     if rank == 0:
         unit = "GB/s"
-        if wl.name in TENSOR_WORKLOADS:  # this workload's own figure is tensor throughput
+        if wl.name in TENSOR_WORKLOADS or wl.name in ALU_WORKLOADS:  # this workload's own figure is FLOP/s
             value = world * calls[0][3] / (ms_per_step * 1e-3) / 1e12
             unit = "TFLOP/s"
         line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "bf16", "accumulate": "f32",
+                "vs_baseline": None, "dtype": "f32" if wl.name in ALU_WORKLOADS else "bf16", "accumulate": "f32",
                 "data": "synthetic (seeded numpy; shapes and distributions of the BitDelta serving setup)",
                 "config": {**wl.config(), "parallelism": f"replicas x{world} (no exchange step)"},
                 "tokens_per_s": world * tokens / (ms_per_step * 1e-3),
@@ -725,6 +801,9 @@ def run_e2e(run: GpuRun, calls, wl: Workload, steps: int, stream):
     elif wl.name == "materialize":
         h_in = [(pin(run.wb), run.wb), (pin(run.signs[0]), run.signs[0]), (pin(run.alpha[0]), run.alpha[0])]
         h_out = [(pin(run.w_eff), run.w_eff)]
+    elif wl.name == "monosoup":
+        h_in = [(pin(run.wb), run.wb)] + [(pin(w), w) for w in run.wf] + [(pin(run.omega), run.omega)]
+        h_out = [(pin(run.w_merged), run.w_merged)]
     elif wl.name == "prefill":
         h_in = [(pin(run.xs[0]), run.xs[0])]
         h_out = [(pin(run.ys[0]), run.ys[0])]

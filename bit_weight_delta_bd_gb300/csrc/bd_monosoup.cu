@@ -14,14 +14,15 @@
 //   tau = (Q U_r) (U_r^T B)    (U_r: the r leading eigenvectors)
 // which is U_r S_r V_r^T of the rank-l approximation Q Q^T Delta.  Every pass
 // over Delta reads W_i and W_base (bf16) and forms Delta in fp32 on the fly.
-// Orthonormalisation is CholeskyQR2: the Gram matrix is accumulated in fp64,
-// factored in one CTA, and Y <- Y R^-1 applied twice; directions whose pivot
-// falls below 1e-12 of the largest are dropped (rank-deficient sketches).
+// Orthonormalisation is CholeskyQR: the Gram matrix is accumulated in fp64,
+// factored in one CTA, and Y <- Y R^-1 applied (twice, CholeskyQR2, for the
+// final basis); directions whose pivot falls below 1e-12 of the largest are
+// dropped (rank-deficient sketches).
 // The merge is one pass: W_base + (1/k) [L_1 .. L_k][R_1 .. R_k]^T with
 // L_i = Q_i U_r, R_i = B_i^T U_r, rounded once to the output type.
 //
-// All arithmetic is fp32 on the CUDA cores except the Gram matrices, the
-// Cholesky factor and the eigenproblem (fp64).  No kernel waits on another
+// All arithmetic is fp32 on the CUDA cores except the Gram matrices and the
+// Cholesky factor (fp64).  No kernel waits on another
 // CTA; the passes are plain stream-ordered launches.
 #include <cuda_bf16.h>
 
@@ -36,8 +37,9 @@ namespace bd {
 namespace {
 
 constexpr int kMaxL = 64;        // sketch width l (columns of Y, Q, B^T)
-constexpr int kGramBlocks = 64;  // CTAs of one Gram pass (fixed-order fp64 partials)
-// dynamic shared memory of the one-CTA kernels: two fp64 [64][65] matrices
+constexpr int kGramBlocks = 152;  // CTAs of one Gram pass (fixed-order fp64 partials)
+constexpr int kSlices = 16;       // split of the long dimension in the two products with Delta
+// dynamic shared memory of the Cholesky kernel: two fp64 [64][65] matrices
 constexpr size_t kSmallSmem = 2 * sizeof(double) * kMaxL * (kMaxL + 1);
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
@@ -55,19 +57,23 @@ __device__ __forceinline__ void delta8(const uint16_t* w, const uint16_t* wb, fl
     }
 }
 
-// Y[row][c] = sum_j Delta[row][j] * Om[j][c]  (c < l).  32 rows per CTA,
-// d_in in 64-column chunks; each thread holds 2 rows x 4 columns.
+// ypart[s][row][c] = sum over slice s of the columns j of Delta[row][j] *
+// Om[j][c]  (c < l).  32 rows per CTA, blockIdx.y = slice (cols_per columns,
+// a multiple of 64), 64-column chunks; each thread holds 2 rows x 4 columns.
 __global__ void __launch_bounds__(256) sketch_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ wb,
                                                      int64_t d_out, int64_t d_in, const float* __restrict__ om, int l,
-                                                     float* __restrict__ y)
+                                                     int64_t cols_per, float* __restrict__ ypart)
 {
+    const int64_t jbeg = static_cast<int64_t>(blockIdx.y) * cols_per;
+    const int64_t jend = jbeg + cols_per < d_in ? jbeg + cols_per : d_in;
+    float* y = ypart + static_cast<int64_t>(blockIdx.y) * d_out * l;
     __shared__ float sd[32][65];
     __shared__ __align__(16) float so[64][kMaxL];
     const int tid = threadIdx.x;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
     const int tr = (tid >> 4) * 2, tc = (tid & 15) * 4;
     float acc[2][4] = {};
-    for (int64_t j0 = 0; j0 < d_in; j0 += 64) {
+    for (int64_t j0 = jbeg; j0 < jend; j0 += 64) {
         {
             const int rr = tid >> 3, cc = (tid & 7) * 8;
             const int64_t row = r0 + rr;
@@ -106,31 +112,36 @@ __global__ void __launch_bounds__(256) sketch_kernel(const uint16_t* __restrict_
     }
 }
 
-// Bt[j][c] = sum_row Delta[row][j] * Q[row][c]  (c < l).  32 columns of
-// Delta per CTA, all rows in 64-row chunks; each thread holds 2 columns x 4.
+// btpart[s][j][c] = sum over slice s of the rows of Delta[row][j] *
+// Q[row][c]  (c < l).  32 columns of Delta per CTA, blockIdx.y = slice
+// (rows_per rows, a multiple of 64), 64-row chunks; each thread holds 2
+// columns x 4.
 __global__ void __launch_bounds__(256) left_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ wb,
                                                    int64_t d_out, int64_t d_in, const float* __restrict__ q, int l,
-                                                   float* __restrict__ bt)
+                                                   int64_t rows_per, float* __restrict__ btpart)
 {
+    const int64_t rbeg = static_cast<int64_t>(blockIdx.y) * rows_per;
+    const int64_t rend = rbeg + rows_per < d_out ? rbeg + rows_per : d_out;
+    float* bt = btpart + static_cast<int64_t>(blockIdx.y) * d_in * l;
     __shared__ float sd[64][33];
     __shared__ __align__(16) float sq[64][kMaxL];
     const int tid = threadIdx.x;
     const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 32;
     const int tj = (tid >> 4) * 2, tc = (tid & 15) * 4;
     float acc[2][4] = {};
-    for (int64_t r0 = 0; r0 < d_out; r0 += 64) {
+    for (int64_t r0 = rbeg; r0 < rend; r0 += 64) {
         {
             const int rr = tid >> 2, cc = (tid & 3) * 8;
             const int64_t row = r0 + rr;
             float d[8] = {};
-            if (row < d_out) delta8(w + row * d_in + j0 + cc, wb + row * d_in + j0 + cc, d);
+            if (row < rend) delta8(w + row * d_in + j0 + cc, wb + row * d_in + j0 + cc, d);
 #pragma unroll
             for (int e = 0; e < 8; ++e) sd[rr][cc + e] = d[e];
         }
         for (int e = tid; e < 64 * kMaxL; e += 256) {
             const int rr = e / kMaxL, c = e % kMaxL;
             const int64_t row = r0 + rr;
-            sq[rr][c] = (c < l && row < d_out) ? q[row * l + c] : 0.0f;
+            sq[rr][c] = (c < l && row < rend) ? q[row * l + c] : 0.0f;
         }
         __syncthreads();
 #pragma unroll 8
@@ -155,8 +166,19 @@ __global__ void __launch_bounds__(256) left_kernel(const uint16_t* __restrict__ 
             if (tc + qq < l) bt[(j0 + tj + x) * l + tc + qq] = acc[x][qq];
 }
 
+// out[e] = sum_s part[s][e], e < n (fixed order).
+__global__ void __launch_bounds__(256) sum_slices_kernel(const float* __restrict__ part, int nslice, int64_t n,
+                                                         float* __restrict__ out)
+{
+    const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (e >= n) return;
+    float s = part[e];
+    for (int k = 1; k < nslice; ++k) s += part[k * n + e];
+    out[e] = s;
+}
+
 // Partial Gram matrices of A [n][l]: CTA b sums A^T A over its contiguous row
-// range in fp64 into part[b][64][64] (entries past l are zero).
+// range in fp64 into part[b][l * l] (entry i * l + j).
 __global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, int64_t n, int l,
                                                    double* __restrict__ part)
 {
@@ -165,6 +187,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, 
     const int64_t per = (n + kGramBlocks - 1) / kGramBlocks;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * per;
     const int64_t b1 = b0 + per < n ? b0 + per : n;
+    const int ll = l * l;
     double acc[16];
 #pragma unroll
     for (int m = 0; m < 16; ++m) acc[m] = 0.0;
@@ -179,31 +202,42 @@ __global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, 
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const int p = tid + 256 * m;
-                acc[m] = fma(static_cast<double>(sa[rr][p >> 6]), static_cast<double>(sa[rr][p & 63]), acc[m]);
+                if (p < ll) acc[m] = fma(static_cast<double>(sa[rr][p / l]), static_cast<double>(sa[rr][p % l]), acc[m]);
             }
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int m = 0; m < 16; ++m) part[static_cast<int64_t>(blockIdx.x) * 4096 + tid + 256 * m] = acc[m];
-}
-
-// Sums the Gram partials (fixed order) into g[64][65] (one CTA, 256 threads).
-__device__ __forceinline__ void sum_partials(const double* __restrict__ part, int l, double (*g)[kMaxL + 1])
-{
-    for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
-        const int i = e >> 6, j = e & 63;
-        double s = 0.0;
-        if (i < l && j < l)
-            for (int b = 0; b < kGramBlocks; ++b) s += part[b * 4096 + e];
-        g[i][j] = s;
+    for (int m = 0; m < 16; ++m) {
+        const int p = tid + 256 * m;
+        if (p < ll) part[static_cast<int64_t>(blockIdx.x) * ll + p] = acc[m];
     }
 }
 
-// One CTA: G = sum of the partials; G = R^T R (Cholesky, R upper); minv = R^-1
+// g[e] = sum_b part[b][e], e < l * l (fixed order, one thread per entry).
+__global__ void __launch_bounds__(256) gram_sum_kernel(const double* __restrict__ part, int l, double* __restrict__ g)
+{
+    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int ll = l * l;
+    if (e >= ll) return;
+    double s = 0.0;
+    for (int b = 0; b < kGramBlocks; ++b) s += part[static_cast<int64_t>(b) * ll + e];
+    g[e] = s;
+}
+
+// Loads the summed Gram matrix G [l][l] into g[64][65], zero past l.
+__device__ __forceinline__ void load_gram(const double* __restrict__ G, int l, double (*g)[kMaxL + 1])
+{
+    for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
+        const int i = e >> 6, j = e & 63;
+        g[i][j] = (i < l && j < l) ? G[i * l + j] : 0.0;
+    }
+}
+
+// One CTA: G = R^T R (Cholesky, R upper); minv = R^-1
 // as fp32 [l][l].  A pivot below 1e-12 of the largest diagonal entry drops
 // its direction (its row and column of R^-1 are zero).
-__global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict__ part, int l,
+__global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict__ G, int l,
                                                        float* __restrict__ minv)
 {
     extern __shared__ double dsm[];  // kSmallSmem bytes: g, then ri
@@ -212,7 +246,7 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict_
     __shared__ double dmax;
     __shared__ int dead[kMaxL];
     const int tid = threadIdx.x;
-    sum_partials(part, l, g);
+    load_gram(G, l, g);
     __syncthreads();
     if (tid == 0) {
         double m = 0.0;
@@ -253,29 +287,34 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict_
     for (int e = tid; e < l * l; e += blockDim.x) minv[e] = static_cast<float>(ri[e / l][e % l]);
 }
 
-// One CTA: the symmetric eigenproblem of G = sum of the partials by cyclic
-// Jacobi with the round-robin pair order (l/2 disjoint rotations per round,
-// at most 40 sweeps); ur[i][m] = the eigenvector of the m-th largest
-// eigenvalue, m < r.
-__global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ part, int l, int r,
+// One CTA: the symmetric eigenproblem of G by cyclic Jacobi in fp32 with the
+// round-robin pair order (l/2 disjoint rotations per round) until the
+// off-diagonal mass is below 1e-12 of the diagonal's (at most 40 sweeps);
+// ur[i][m] = the eigenvector of the m-th largest eigenvalue, m < r.  Only
+// the r leading eigenvectors are used, and they are set apart by the
+// spectral gap, so fp32 (fp64 rotations are slow on this GPU's few fp64
+// units) costs about 1e-6 of them.
+__global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ G, int l, int r,
                                                      float* __restrict__ ur)
 {
-    extern __shared__ double dsm[];  // kSmallSmem bytes: A, then V
-    double (*A)[kMaxL + 1] = reinterpret_cast<double (*)[kMaxL + 1]>(dsm);
-    double (*V)[kMaxL + 1] = reinterpret_cast<double (*)[kMaxL + 1]>(dsm + kMaxL * (kMaxL + 1));
-    __shared__ double cs[kMaxL / 2], sn[kMaxL / 2];
+    __shared__ float A[kMaxL][kMaxL + 1];
+    __shared__ float V[kMaxL][kMaxL + 1];
+    __shared__ float cs[kMaxL / 2], sn[kMaxL / 2];
     __shared__ int pp[kMaxL / 2], qq[kMaxL / 2];
-    __shared__ double red[2][256];
+    __shared__ float red[2][256];
     __shared__ int idx[kMaxL];
     const int tid = threadIdx.x;
-    sum_partials(part, l, A);
-    for (int e = tid; e < kMaxL * kMaxL; e += blockDim.x) V[e >> 6][e & 63] = (e >> 6) == (e & 63) ? 1.0 : 0.0;
+    for (int e = tid; e < kMaxL * kMaxL; e += blockDim.x) {
+        const int i = e >> 6, j = e & 63;
+        A[i][j] = (i < l && j < l) ? static_cast<float>(G[i * l + j]) : 0.0f;
+        V[i][j] = i == j ? 1.0f : 0.0f;
+    }
     __syncthreads();
     const int n = l + (l & 1);  // even number of players; index l is a dummy when l is odd
     for (int sweep = 0; sweep < 40; ++sweep) {
-        double off = 0.0, dia = 0.0;
+        float off = 0.0f, dia = 0.0f;
         for (int e = tid; e < l * l; e += blockDim.x) {
-            const double v = A[e / l][e % l];
+            const float v = A[e / l][e % l];
             if (e / l == e % l)
                 dia += v * v;
             else
@@ -291,7 +330,7 @@ __global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ 
             }
             __syncthreads();
         }
-        const bool done = !(red[0][0] > 1e-30 * red[1][0]);
+        const bool done = !(red[0][0] > 1e-12f * red[1][0]);
         __syncthreads();
         if (done) break;
         for (int t = 0; t + 1 < n; ++t) {
@@ -299,13 +338,13 @@ __global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ 
                 const int a = tid == 0 ? 0 : 1 + (tid - 1 + t) % (n - 1);
                 const int b = 1 + (n - 2 - tid + t) % (n - 1);
                 const int p = a < b ? a : b, q = a < b ? b : a;
-                double c = 1.0, s = 0.0;
+                float c = 1.0f, s = 0.0f;
                 if (q < l) {
-                    const double apq = A[p][q];
-                    if (fabs(apq) > 1e-300) {
-                        const double th = (A[q][q] - A[p][p]) / (2.0 * apq);
-                        const double tt = (th >= 0.0 ? 1.0 : -1.0) / (fabs(th) + sqrt(th * th + 1.0));
-                        c = 1.0 / sqrt(tt * tt + 1.0);
+                    const float apq = A[p][q];
+                    if (fabsf(apq) > 1e-30f) {
+                        const float th = (A[q][q] - A[p][p]) / (2.0f * apq);
+                        const float tt = (th >= 0.0f ? 1.0f : -1.0f) / (fabsf(th) + sqrtf(th * th + 1.0f));
+                        c = 1.0f / sqrtf(tt * tt + 1.0f);
                         s = tt * c;
                     }
                 }
@@ -320,11 +359,11 @@ __global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ 
                 const int i = e / l, row = e % l;
                 const int p = pp[i], q = qq[i];
                 if (q >= l) continue;
-                const double c = cs[i], s = sn[i];
-                const double ap = A[row][p], aq = A[row][q];
+                const float c = cs[i], s = sn[i];
+                const float ap = A[row][p], aq = A[row][q];
                 A[row][p] = c * ap - s * aq;
                 A[row][q] = s * ap + c * aq;
-                const double vp = V[row][p], vq = V[row][q];
+                const float vp = V[row][p], vq = V[row][q];
                 V[row][p] = c * vp - s * vq;
                 V[row][q] = s * vp + c * vq;
             }
@@ -334,8 +373,8 @@ __global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ 
                 const int i = e / l, col = e % l;
                 const int p = pp[i], q = qq[i];
                 if (q >= l) continue;
-                const double c = cs[i], s = sn[i];
-                const double ap = A[p][col], aq = A[q][col];
+                const float c = cs[i], s = sn[i];
+                const float ap = A[p][col], aq = A[q][col];
                 A[p][col] = c * ap - s * aq;
                 A[q][col] = s * ap + c * aq;
             }
@@ -354,7 +393,7 @@ __global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ 
         }
     }
     __syncthreads();
-    for (int e = tid; e < l * r; e += blockDim.x) ur[e] = static_cast<float>(V[e / r][idx[e % r]]);
+    for (int e = tid; e < l * r; e += blockDim.x) ur[e] = V[e / r][idx[e % r]];
 }
 
 // dst[row][j] = sum_c src[row][c] * M[c][j]  (c < l, j < m); one row per
@@ -438,28 +477,32 @@ __global__ void __launch_bounds__(256) merge_kernel(const uint16_t* __restrict__
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct MonoSoupWs {
-    size_t y, z, part, m, L, Rt, total;
+    size_t y, z, ypart, zpart, part, g, m, L, Rt, total;
 };
 
 MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
 {
     MonoSoupWs w{};
     size_t off = 256;  // error word area (unused by these kernels, kept for the common layout)
-    w.y = off;
-    off += up256(static_cast<size_t>(d_out) * l * 4);
-    w.z = off;
-    off += up256(static_cast<size_t>(d_in) * l * 4);
-    w.part = off;
-    off += up256(static_cast<size_t>(kGramBlocks) * 4096 * 8);
-    w.m = off;
-    off += up256(static_cast<size_t>(kMaxL) * kMaxL * 4);
-    w.L = off;
-    off += up256(static_cast<size_t>(k) * d_out * (r > 0 ? r : 1) * 4);
-    w.Rt = off;
-    off += up256(static_cast<size_t>(k) * d_in * (r > 0 ? r : 1) * 4);
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off += up256(bytes);
+        return at;
+    };
+    w.y = take(static_cast<size_t>(d_out) * l * 4);
+    w.z = take(static_cast<size_t>(d_in) * l * 4);
+    w.ypart = take(static_cast<size_t>(kSlices) * d_out * l * 4);
+    w.zpart = take(static_cast<size_t>(kSlices) * d_in * l * 4);
+    w.part = take(static_cast<size_t>(kGramBlocks) * l * l * 8);
+    w.g = take(static_cast<size_t>(l) * l * 8);
+    w.m = take(static_cast<size_t>(kMaxL) * kMaxL * 4);
+    w.L = take(static_cast<size_t>(k) * d_out * (r > 0 ? r : 1) * 4);
+    w.Rt = take(static_cast<size_t>(k) * d_in * (r > 0 ? r : 1) * 4);
     w.total = off;
     return w;
 }
+
+unsigned blocks_for(int64_t n) { return static_cast<unsigned>((n + 255) / 256); }
 
 }  // namespace
 
@@ -472,47 +515,67 @@ size_t monosoup_workspace_size(int64_t d_out, int64_t d_in, int k, int r, int l)
 
 cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
 {
-    static std::atomic<size_t> chol_set[kHostMaxDevices], jacobi_set[kHostMaxDevices];
-    cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(chol_inv_kernel), kSmallSmem, chol_set);
-    if (e == cudaSuccess)
-        e = ensure_dynamic_smem(reinterpret_cast<const void*>(jacobi_kernel), kSmallSmem, jacobi_set);
+    static std::atomic<size_t> chol_set[kHostMaxDevices];
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(chol_inv_kernel), kSmallSmem, chol_set);
     if (e != cudaSuccess) return e;
     const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
     char* w = static_cast<char*>(a.ws);
     float* Y = reinterpret_cast<float*>(w + lay.y);
     float* Z = reinterpret_cast<float*>(w + lay.z);
+    float* Yp = reinterpret_cast<float*>(w + lay.ypart);
+    float* Zp = reinterpret_cast<float*>(w + lay.zpart);
     double* part = reinterpret_cast<double*>(w + lay.part);
+    double* G = reinterpret_cast<double*>(w + lay.g);
     float* M = reinterpret_cast<float*>(w + lay.m);
     float* L = reinterpret_cast<float*>(w + lay.L);
     float* Rt = reinterpret_cast<float*>(w + lay.Rt);
     const int l = a.l, r = a.rank;
-    const unsigned gy = static_cast<unsigned>((a.d_out + 31) / 32);
-    const unsigned gl = static_cast<unsigned>(a.d_in / 32);
-    auto orth = [&](float* A, int64_t n) {  // CholeskyQR2: A <- A R^-1, twice
-        for (int pass = 0; pass < 2; ++pass) {
-            gram_kernel<<<kGramBlocks, 256, 0, st>>>(A, n, l, part);
-            chol_inv_kernel<<<1, 256, kSmallSmem, st>>>(part, l, M);
-            apply_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, st>>>(A, n, l, M, l, A);
+    // the two products with Delta, each split in kSlices along its long
+    // dimension and summed in slice order
+    const int64_t ncol = a.d_in / 64, nrow = (a.d_out + 63) / 64;
+    const int64_t cs = (ncol + kSlices - 1) / kSlices, rs = (nrow + kSlices - 1) / kSlices;
+    const dim3 gsk(static_cast<unsigned>((a.d_out + 31) / 32), static_cast<unsigned>((ncol + cs - 1) / cs));
+    const dim3 glf(static_cast<unsigned>(a.d_in / 32), static_cast<unsigned>((nrow + rs - 1) / rs));
+    auto sketch = [&](const uint16_t* wi, const float* om) {  // Y = Delta om
+        sketch_kernel<<<gsk, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, om, l, 64 * cs, Yp);
+        sum_slices_kernel<<<blocks_for(a.d_out * l), 256, 0, st>>>(Yp, static_cast<int>(gsk.y), a.d_out * l, Y);
+    };
+    auto left = [&](const uint16_t* wi) {  // Z = Delta^T Y
+        left_kernel<<<glf, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, 64 * rs, Zp);
+        sum_slices_kernel<<<blocks_for(a.d_in * l), 256, 0, st>>>(Zp, static_cast<int>(glf.y), a.d_in * l, Z);
+    };
+    auto gram = [&](const float* A, int64_t n) {  // G = A^T A
+        gram_kernel<<<kGramBlocks, 256, 0, st>>>(A, n, l, part);
+        gram_sum_kernel<<<blocks_for(static_cast<int64_t>(l) * l), 256, 0, st>>>(part, l, G);
+    };
+    // A <- A R^-1 (CholeskyQR), `passes` times: two (CholeskyQR2) for the Q
+    // that B is projected on, one for the intermediate bases of the power
+    // iterations, where only the spanned subspace matters
+    auto orth = [&](float* A, int64_t n, int passes) {
+        for (int pass = 0; pass < passes; ++pass) {
+            gram(A, n);
+            chol_inv_kernel<<<1, 256, kSmallSmem, st>>>(G, l, M);
+            apply_kernel<<<blocks_for(n), 256, 0, st>>>(A, n, l, M, l, A);
         }
     };
     if (r > 0) {
         for (int i = 0; i < a.k; ++i) {
             const uint16_t* wi = a.w_ft[i];
-            sketch_kernel<<<gy, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, a.omega, l, Y);
-            orth(Y, a.d_out);
+            sketch(wi, a.omega);
+            orth(Y, a.d_out, a.power_iters > 0 ? 1 : 2);
             for (int it = 0; it < a.power_iters; ++it) {
-                left_kernel<<<gl, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, Z);
-                orth(Z, a.d_in);
-                sketch_kernel<<<gy, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Z, l, Y);
-                orth(Y, a.d_out);
+                left(wi);
+                orth(Z, a.d_in, 1);
+                sketch(wi, Z);
+                orth(Y, a.d_out, it + 1 == a.power_iters ? 2 : 1);
             }
-            left_kernel<<<gl, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, Z);  // Z = B^T
-            gram_kernel<<<kGramBlocks, 256, 0, st>>>(Z, a.d_in, l, part);               // B B^T
-            jacobi_kernel<<<1, 256, kSmallSmem, st>>>(part, l, r, M);                  // U_r [l][r]
-            apply_kernel<<<static_cast<unsigned>((a.d_out + 255) / 256), 256, 0, st>>>(
-                Y, a.d_out, l, M, r, L + static_cast<size_t>(i) * a.d_out * r);
-            apply_kernel<<<static_cast<unsigned>((a.d_in + 255) / 256), 256, 0, st>>>(
-                Z, a.d_in, l, M, r, Rt + static_cast<size_t>(i) * a.d_in * r);
+            left(wi);  // Z = B^T
+            gram(Z, a.d_in);                                        // B B^T
+            jacobi_kernel<<<1, 256, 0, st>>>(G, l, r, M);  // U_r [l][r]
+            apply_kernel<<<blocks_for(a.d_out), 256, 0, st>>>(Y, a.d_out, l, M, r,
+                                                              L + static_cast<size_t>(i) * a.d_out * r);
+            apply_kernel<<<blocks_for(a.d_in), 256, 0, st>>>(Z, a.d_in, l, M, r,
+                                                             Rt + static_cast<size_t>(i) * a.d_in * r);
         }
     }
     const dim3 grid(static_cast<unsigned>(a.d_in / 64), static_cast<unsigned>((a.d_out + 63) / 64));
