@@ -59,20 +59,23 @@ __device__ __forceinline__ void delta8(const uint16_t* w, const uint16_t* wb, fl
 
 // ypart[s][row][c] = sum over slice s of the columns j of Delta[row][j] *
 // Om[j][c]  (c < l).  32 rows per CTA, blockIdx.y = slice (cols_per columns,
-// a multiple of 64), 64-column chunks; each thread holds 2 rows x 4 columns.
+// a multiple of 64), 64-column chunks; each thread holds 2 rows x NC columns.
+// NC = output columns per thread (kW = 16 NC columns per CTA, kW >= l).
+template <int NC>
 __global__ void __launch_bounds__(256) sketch_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ wb,
                                                      int64_t d_out, int64_t d_in, const float* __restrict__ om, int l,
                                                      int64_t cols_per, float* __restrict__ ypart)
 {
+    constexpr int kW = 16 * NC;
     const int64_t jbeg = static_cast<int64_t>(blockIdx.y) * cols_per;
     const int64_t jend = jbeg + cols_per < d_in ? jbeg + cols_per : d_in;
     float* y = ypart + static_cast<int64_t>(blockIdx.y) * d_out * l;
     __shared__ float sd[32][65];
-    __shared__ __align__(16) float so[64][kMaxL];
+    __shared__ __align__(16) float so[64][kW];
     const int tid = threadIdx.x;
     const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
-    const int tr = (tid >> 4) * 2, tc = (tid & 15) * 4;
-    float acc[2][4] = {};
+    const int tr = (tid >> 4) * 2, tc = (tid & 15) * NC;
+    float acc[2][NC] = {};
     for (int64_t j0 = jbeg; j0 < jend; j0 += 64) {
         {
             const int rr = tid >> 3, cc = (tid & 7) * 8;
@@ -82,23 +85,22 @@ __global__ void __launch_bounds__(256) sketch_kernel(const uint16_t* __restrict_
 #pragma unroll
             for (int q = 0; q < 8; ++q) sd[rr][cc + q] = d[q];
         }
-        for (int e = tid; e < 64 * kMaxL; e += 256) {
-            const int jj = e / kMaxL, c = e % kMaxL;
+        for (int e = tid; e < 64 * kW; e += 256) {
+            const int jj = e / kW, c = e % kW;
             so[jj][c] = c < l ? om[(j0 + jj) * l + c] : 0.0f;
         }
         __syncthreads();
 #pragma unroll 8
         for (int jj = 0; jj < 64; ++jj) {
             const float a0 = sd[tr][jj], a1 = sd[tr + 1][jj];
-            const float4 o = *reinterpret_cast<const float4*>(&so[jj][tc]);
-            acc[0][0] = fmaf(a0, o.x, acc[0][0]);
-            acc[0][1] = fmaf(a0, o.y, acc[0][1]);
-            acc[0][2] = fmaf(a0, o.z, acc[0][2]);
-            acc[0][3] = fmaf(a0, o.w, acc[0][3]);
-            acc[1][0] = fmaf(a1, o.x, acc[1][0]);
-            acc[1][1] = fmaf(a1, o.y, acc[1][1]);
-            acc[1][2] = fmaf(a1, o.z, acc[1][2]);
-            acc[1][3] = fmaf(a1, o.w, acc[1][3]);
+            float o[NC];
+#pragma unroll
+            for (int q = 0; q < NC; ++q) o[q] = so[jj][tc + q];
+#pragma unroll
+            for (int q = 0; q < NC; ++q) {
+                acc[0][q] = fmaf(a0, o[q], acc[0][q]);
+                acc[1][q] = fmaf(a1, o[q], acc[1][q]);
+            }
         }
         __syncthreads();
     }
@@ -107,7 +109,7 @@ __global__ void __launch_bounds__(256) sketch_kernel(const uint16_t* __restrict_
         const int64_t row = r0 + tr + x;
         if (row >= d_out) continue;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < NC; ++q)
             if (tc + q < l) y[row * l + tc + q] = acc[x][q];
     }
 }
@@ -115,20 +117,22 @@ __global__ void __launch_bounds__(256) sketch_kernel(const uint16_t* __restrict_
 // btpart[s][j][c] = sum over slice s of the rows of Delta[row][j] *
 // Q[row][c]  (c < l).  32 columns of Delta per CTA, blockIdx.y = slice
 // (rows_per rows, a multiple of 64), 64-row chunks; each thread holds 2
-// columns x 4.
+// columns x NC.
+template <int NC>
 __global__ void __launch_bounds__(256) left_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ wb,
                                                    int64_t d_out, int64_t d_in, const float* __restrict__ q, int l,
                                                    int64_t rows_per, float* __restrict__ btpart)
 {
+    constexpr int kW = 16 * NC;
     const int64_t rbeg = static_cast<int64_t>(blockIdx.y) * rows_per;
     const int64_t rend = rbeg + rows_per < d_out ? rbeg + rows_per : d_out;
     float* bt = btpart + static_cast<int64_t>(blockIdx.y) * d_in * l;
     __shared__ float sd[64][33];
-    __shared__ __align__(16) float sq[64][kMaxL];
+    __shared__ __align__(16) float sq[64][kW];
     const int tid = threadIdx.x;
     const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 32;
-    const int tj = (tid >> 4) * 2, tc = (tid & 15) * 4;
-    float acc[2][4] = {};
+    const int tj = (tid >> 4) * 2, tc = (tid & 15) * NC;
+    float acc[2][NC] = {};
     for (int64_t r0 = rbeg; r0 < rend; r0 += 64) {
         {
             const int rr = tid >> 2, cc = (tid & 3) * 8;
@@ -138,8 +142,8 @@ __global__ void __launch_bounds__(256) left_kernel(const uint16_t* __restrict__ 
 #pragma unroll
             for (int e = 0; e < 8; ++e) sd[rr][cc + e] = d[e];
         }
-        for (int e = tid; e < 64 * kMaxL; e += 256) {
-            const int rr = e / kMaxL, c = e % kMaxL;
+        for (int e = tid; e < 64 * kW; e += 256) {
+            const int rr = e / kW, c = e % kW;
             const int64_t row = r0 + rr;
             sq[rr][c] = (c < l && row < rend) ? q[row * l + c] : 0.0f;
         }
@@ -147,22 +151,21 @@ __global__ void __launch_bounds__(256) left_kernel(const uint16_t* __restrict__ 
 #pragma unroll 8
         for (int rr = 0; rr < 64; ++rr) {
             const float a0 = sd[rr][tj], a1 = sd[rr][tj + 1];
-            const float4 o = *reinterpret_cast<const float4*>(&sq[rr][tc]);
-            acc[0][0] = fmaf(a0, o.x, acc[0][0]);
-            acc[0][1] = fmaf(a0, o.y, acc[0][1]);
-            acc[0][2] = fmaf(a0, o.z, acc[0][2]);
-            acc[0][3] = fmaf(a0, o.w, acc[0][3]);
-            acc[1][0] = fmaf(a1, o.x, acc[1][0]);
-            acc[1][1] = fmaf(a1, o.y, acc[1][1]);
-            acc[1][2] = fmaf(a1, o.z, acc[1][2]);
-            acc[1][3] = fmaf(a1, o.w, acc[1][3]);
+            float o[NC];
+#pragma unroll
+            for (int qq = 0; qq < NC; ++qq) o[qq] = sq[rr][tc + qq];
+#pragma unroll
+            for (int qq = 0; qq < NC; ++qq) {
+                acc[0][qq] = fmaf(a0, o[qq], acc[0][qq]);
+                acc[1][qq] = fmaf(a1, o[qq], acc[1][qq]);
+            }
         }
         __syncthreads();
     }
 #pragma unroll
     for (int x = 0; x < 2; ++x)
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq)
+        for (int qq = 0; qq < NC; ++qq)
             if (tc + qq < l) bt[(j0 + tj + x) * l + tc + qq] = acc[x][qq];
 }
 
@@ -536,12 +539,19 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     const int64_t cs = (ncol + kSlices - 1) / kSlices, rs = (nrow + kSlices - 1) / kSlices;
     const dim3 gsk(static_cast<unsigned>((a.d_out + 31) / 32), static_cast<unsigned>((ncol + cs - 1) / cs));
     const dim3 glf(static_cast<unsigned>(a.d_in / 32), static_cast<unsigned>((nrow + rs - 1) / rs));
+    // tiles as wide as l needs: 32 columns (2 per thread) up to l = 32, else 64
     auto sketch = [&](const uint16_t* wi, const float* om) {  // Y = Delta om
-        sketch_kernel<<<gsk, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, om, l, 64 * cs, Yp);
+        if (l <= 32)
+            sketch_kernel<2><<<gsk, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, om, l, 64 * cs, Yp);
+        else
+            sketch_kernel<4><<<gsk, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, om, l, 64 * cs, Yp);
         sum_slices_kernel<<<blocks_for(a.d_out * l), 256, 0, st>>>(Yp, static_cast<int>(gsk.y), a.d_out * l, Y);
     };
     auto left = [&](const uint16_t* wi) {  // Z = Delta^T Y
-        left_kernel<<<glf, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, 64 * rs, Zp);
+        if (l <= 32)
+            left_kernel<2><<<glf, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, 64 * rs, Zp);
+        else
+            left_kernel<4><<<glf, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, 64 * rs, Zp);
         sum_slices_kernel<<<blocks_for(a.d_in * l), 256, 0, st>>>(Zp, static_cast<int>(glf.y), a.d_in * l, Z);
     };
     auto gram = [&](const float* A, int64_t n) {  // G = A^T A
