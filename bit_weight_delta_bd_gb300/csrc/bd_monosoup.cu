@@ -185,7 +185,7 @@ __global__ void __launch_bounds__(256) sum_slices_kernel(const float* __restrict
 __global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, int64_t n, int l,
                                                    double* __restrict__ part)
 {
-    __shared__ float sa[32][kMaxL + 1];
+    __shared__ double sa[32][kMaxL + 1];  // converted once per element, not once per product
     const int tid = threadIdx.x;
     const int64_t per = (n + kGramBlocks - 1) / kGramBlocks;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * per;
@@ -198,14 +198,14 @@ __global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, 
         for (int e = tid; e < 32 * kMaxL; e += 256) {
             const int rr = e / kMaxL, c = e % kMaxL;
             const int64_t row = r0 + rr;
-            sa[rr][c] = (row < b1 && c < l) ? a[row * l + c] : 0.0f;
+            sa[rr][c] = (row < b1 && c < l) ? static_cast<double>(a[row * l + c]) : 0.0;
         }
         __syncthreads();
         for (int rr = 0; rr < 32; ++rr) {
 #pragma unroll
             for (int m = 0; m < 16; ++m) {
                 const int p = tid + 256 * m;
-                if (p < ll) acc[m] = fma(static_cast<double>(sa[rr][p / l]), static_cast<double>(sa[rr][p % l]), acc[m]);
+                if (p < ll) acc[m] = fma(sa[rr][p / l], sa[rr][p % l], acc[m]);
             }
         }
         __syncthreads();
@@ -265,7 +265,8 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict_
         __syncthreads();
         if (tid == 0) dead[k] = live ? 0 : 1;
         const double rkk = live ? sqrt(d) : 0.0;
-        for (int j = k + tid; j < l; j += blockDim.x) g[k][j] = live ? (j == k ? rkk : g[k][j] / rkk) : 0.0;
+        const double inv = live ? 1.0 / rkk : 0.0;
+        for (int j = k + tid; j < l; j += blockDim.x) g[k][j] = live ? (j == k ? rkk : g[k][j] * inv) : 0.0;
         __syncthreads();
         for (int e = tid; e < l * l; e += blockDim.x) {
             const int i = e / l, j = e % l;
@@ -273,16 +274,20 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict_
         }
         __syncthreads();
     }
-    // R^-1 (upper triangular) by back substitution, one column per thread
+    // R^-1 (upper triangular) by back substitution, one column per thread,
+    // with the diagonal's reciprocals taken once
+    __shared__ double dinv[kMaxL];
+    for (int i = tid; i < l; i += blockDim.x) dinv[i] = dead[i] ? 0.0 : 1.0 / g[i][i];
+    __syncthreads();
     for (int j = tid; j < l; j += blockDim.x) {
         for (int i = 0; i < l; ++i) ri[i][j] = 0.0;
         if (!dead[j]) {
-            ri[j][j] = 1.0 / g[j][j];
+            ri[j][j] = dinv[j];
             for (int i = j - 1; i >= 0; --i) {
                 if (dead[i]) continue;
                 double s = 0.0;
                 for (int m = i + 1; m <= j; ++m) s += g[i][m] * ri[m][j];
-                ri[i][j] = -s / g[i][i];
+                ri[i][j] = -s * dinv[i];
             }
         }
     }
