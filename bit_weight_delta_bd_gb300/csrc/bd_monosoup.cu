@@ -22,8 +22,8 @@
 // L_i = Q_i U_r, R_i = B_i^T U_r, rounded once to the output type.
 //
 // All arithmetic is fp32 on the CUDA cores except the Gram matrices and the
-// Cholesky factor (fp64).  No kernel waits on another
-// CTA; the passes are plain stream-ordered launches.
+// Cholesky factor (fp64).  No kernel waits on another CTA; the passes are
+// plain stream-ordered launches.
 #include <cuda_bf16.h>
 
 #include <cmath>
@@ -300,8 +300,8 @@ __global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict_
 // off-diagonal mass is below 1e-12 of the diagonal's (at most 40 sweeps);
 // ur[i][m] = the eigenvector of the m-th largest eigenvalue, m < r.  Only
 // the r leading eigenvectors are used, and they are set apart by the
-// spectral gap, so fp32 (fp64 rotations are slow on this GPU's few fp64
-// units) costs about 1e-6 of them.
+// spectral gap, so fp32 (fp64 rotations are slow on GB300's few fp64 units)
+// costs about 1e-6 of them.
 __global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ G, int l, int r,
                                                      float* __restrict__ ur)
 {
