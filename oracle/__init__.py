@@ -155,14 +155,20 @@ def reconstruct(w_base_bits, signs, alpha, per_row: bool) -> np.ndarray:
 
 def round_to_bf16(v: np.ndarray) -> np.ndarray:
     """bf16 bit patterns of fp64 values rounded to nearest, ties to even, in
-    one rounding: v = m 2^e with 0.5 <= |m| < 1, the 8 significant bits are
-    rint(256 m) (numpy's rint rounds halves to even), and the result, exact
-    in fp64 and fp32 for values in bf16's normal range, is read back through
-    fp32 whose upper 16 bits it occupies."""
+    one rounding.  bf16 keeps 8 significant bits down to 2^-126 and a fixed
+    spacing of 2^-133 below it (its subnormals), so the rounding quantum of
+    v = m 2^e (0.5 <= |m| < 1) is q = 2^max(e - 8, -133) and the result is
+    rint(v / q) q (numpy's rint rounds halves to even; both steps are exact
+    in fp64).  That value is a bf16 number, hence exact in fp32, whose upper
+    16 bits are its pattern; magnitudes past the largest bf16 become inf
+    through the same fp32 read-back."""
     v = np.asarray(v, np.float64)
-    m, e = np.frexp(v)
-    r = np.ldexp(np.rint(m * 256.0), e - 8)
-    return (r.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    _, e = np.frexp(v)
+    q = np.ldexp(1.0, np.maximum(e - 8, -133))
+    r = np.rint(v / q) * q
+    with np.errstate(over="ignore"):
+        f = r.astype(np.float32)
+    return (f.view(np.uint32) >> 16).astype(np.uint16)
 
 
 def materialize(w_base_bits, signs, alpha, per_row: bool) -> np.ndarray:

@@ -335,6 +335,37 @@ def test_multi_routes_each_token_to_its_variant():
         np.testing.assert_allclose(y[t], expect, rtol=1e-12, atol=1e-15)
 
 
+def test_multi_out_of_range_ids_are_base_model_tokens():
+    """The reading for ids outside [-1, V): such a token is computed with
+    W_base alone.  With W_base = 0 its output is exactly 0; with a random
+    W_base it equals numpy's fp64 product x W_base^T (the Delta = 0 GEMM),
+    while the in-range tokens keep their variant's alpha * sum_j x_j."""
+    rng = np.random.default_rng(15)
+    V, d_out, d_in, T = 3, 6, 64, 10
+    signs_l, alpha_l = [], []
+    wb0 = np.zeros((d_out, d_in), np.float32)
+    for v in range(V):
+        wf = np.full((d_out, d_in), 2.0 ** -(v + 2), np.float32)
+        s, a = oracle.compress(_bits(wb0), _bits(wf), per_row=True)
+        signs_l.append(s)
+        alpha_l.append(a)
+    vid = np.array([V, 0, -2, 2, V + 7, -1, 1, -9, 0, 2 ** 30], np.int32)
+    bad = (vid < -1) | (vid >= V)
+    x = synth.activations(rng, T, d_in)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    y = oracle.linear_multi(x, vid, signs_l, alpha_l, True, _bits(wb0))
+    assert np.all(y[bad] == 0.0) and np.all(y[vid == -1] == 0.0)
+    for t in np.flatnonzero((vid >= 0) & (vid < V)):
+        np.testing.assert_allclose(y[t], 2.0 ** -(vid[t] + 2) * xf[t].sum(), rtol=1e-12)
+    wb = synth.base_weight(rng, d_out, d_in)
+    y2 = oracle.linear_multi(x, vid, signs_l, alpha_l, True, wb)
+    gemm = xf @ synth.bf16_bits_to_f32(wb).astype(np.float64).T
+    np.testing.assert_allclose(y2[bad], gemm[bad], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(y2[vid == -1], gemm[vid == -1], rtol=1e-12, atol=1e-15)
+    _, _, n_bad = oracle.route(vid, V)
+    assert n_bad == int(bad.sum())
+
+
 def test_synth_zipf_ids_in_range_and_skewed():
     rng = np.random.default_rng(0)
     vid = synth.zipf_variant_ids(rng, 20000, 14)
@@ -370,6 +401,46 @@ def test_round_to_bf16_matches_the_fp32_rounding_of_the_input_module():
     rng = np.random.default_rng(3)
     v = (rng.standard_normal(20000) * 2.0 ** rng.integers(-20, 20, 20000)).astype(np.float32)
     assert np.array_equal(oracle.round_to_bf16(v.astype(np.float64)), synth.f32_to_bf16_bits(v))
+
+
+def _all_finite_bf16():
+    """(values, patterns) of every finite non-negative bf16 number, ascending."""
+    pats = np.arange(0, 0x7F80, dtype=np.uint16)
+    return synth.bf16_bits_to_f32(pats).astype(np.float64), pats
+
+
+def _nearest_bf16_brute_force(v: np.ndarray) -> np.ndarray:
+    """The definition of round-to-nearest-even, by search over every finite
+    bf16 value: the closest one, the one with an even last significand bit
+    on a tie; the sign is carried over (so -0.0 stays -0.0)."""
+    vals, pats = _all_finite_bf16()
+    out = np.zeros(v.shape, np.uint16)
+    for i, x in enumerate(v):
+        a = abs(float(x))
+        k = int(np.searchsorted(vals, a))  # vals[k-1] < a <= vals[k]
+        cand = [j for j in (k - 1, k) if 0 <= j < len(vals)]
+        d = [abs(vals[j] - a) for j in cand]
+        best = min(d)
+        ties = [cand[n] for n in range(len(cand)) if d[n] == best]
+        j = ties[0] if len(ties) == 1 else next(t for t in ties if int(pats[t]) % 2 == 0)
+        out[i] = int(pats[j]) | (0x8000 if math.copysign(1.0, float(x)) < 0 else 0)
+    return out
+
+
+def test_round_to_bf16_brute_force_normal_and_subnormal():
+    """Against the brute-force nearest-even search: random values from bf16's
+    subnormal range (below 2^-126, spacing 2^-133) up through its normal
+    range, the exact midpoints between neighbouring bf16 values (ties) and a
+    hair either side of them, both signs, zeros."""
+    rng = np.random.default_rng(41)
+    vals, _ = _all_finite_bf16()
+    sub = rng.uniform(0, 2.0 ** -126, 400)
+    normal = rng.standard_normal(400) * 2.0 ** rng.integers(-126, 120, 400)
+    k = rng.integers(0, len(vals) - 1, 400)
+    mid = (vals[k] + vals[k + 1]) / 2
+    near = np.concatenate([mid, mid * (1 + 2.0 ** -40), mid * (1 - 2.0 ** -40)])
+    v = np.concatenate([sub, -sub[:100], normal, near, -near[:200], [0.0, -0.0, 2.0 ** -134, 3 * 2.0 ** -134]])
+    assert np.array_equal(oracle.round_to_bf16(v), _nearest_bf16_brute_force(v))
 
 
 def test_materialize_is_the_rounded_reconstruction():
