@@ -49,7 +49,7 @@ EXPORTS = (
     "bd_route_workspace_size", "bd_route",
     "bd_debug_reconstruct", "bd_check_async", "bd_compress_noalloc",
     "bd_cache_create", "bd_cache_destroy", "bd_cache_set_source", "bd_cache_step", "bd_cache_release",
-    "bd_cache_get_stats", "bd_cache_query", "bd_materialize",
+    "bd_cache_get_stats", "bd_cache_query", "bd_cache_debug_fail_load", "bd_materialize",
     "bd_monosoup_workspace_size", "bd_monosoup_merge",
 )
 BD_CACHE_SERVED = 0
@@ -117,6 +117,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "bd_cache_step": ([_vp, _vp, _i64, _vp, _vp, _vp], _int),
             "bd_cache_release": ([_vp, _vp], _int),
             "bd_cache_get_stats": ([_vp, ctypes.POINTER(CacheStats)], _int),
+            "bd_cache_debug_fail_load": ([_vp, _i64], _int),
             "bd_cache_query": ([_vp, _i32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                 ctypes.POINTER(ctypes.c_double)], _int),
         }
@@ -357,6 +358,10 @@ class DeltaCache:
         _check(self._lib.bd_cache_query(self._h, int(variant), ctypes.byref(r), ctypes.byref(pn), ctypes.byref(rate)),
                "bd_cache_query")
         return bool(r.value), bool(pn.value), rate.value
+
+    def debug_fail_load(self, n: int) -> None:
+        """Test aid: the n-th load from now fails like a failed copy (bd_cache_debug_fail_load)."""
+        _check(self._lib.bd_cache_debug_fail_load(self._h, int(n)), "bd_cache_debug_fail_load")
 
     def close(self) -> None:
         if self._h:

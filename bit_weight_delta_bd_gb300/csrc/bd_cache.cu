@@ -57,6 +57,7 @@ struct bd_cache {
     std::unordered_map<int32_t, int> slot_of;  // resident variant -> slot
     std::vector<int32_t> pinned;               // current pinned set
     std::vector<int> acquired;                 // slots handed out by the pending step
+    int64_t fail_countdown = 0;                // test aid: the n-th load from now fails (0: never)
     uint64_t tick = 0;
     bd_cache_stats st{};
 };
@@ -202,14 +203,23 @@ bd_status bd_cache_step(bd_cache* c, const int32_t* vid, int64_t n, void* stream
                 ++c->st.evictions;
             }
             const bd_cache::Source& so = c->src[v];
-            if (c->arena && so.bytes > 0) {
+            cudaError_t e = cudaSuccess;
+            if (c->fail_countdown > 0 && --c->fail_countdown == 0) e = cudaErrorUnknown;  // injected (test aid)
+            if (e == cudaSuccess && c->arena && so.bytes > 0) {
                 // the copy overwrites the slot only after the last step using it finished
-                cudaError_t e = sl.released_recorded ? cudaStreamWaitEvent(c->copy, sl.released, 0) : cudaSuccess;
+                e = sl.released_recorded ? cudaStreamWaitEvent(c->copy, sl.released, 0) : cudaSuccess;
                 if (e == cudaSuccess)
                     e = cudaMemcpyAsync(c->arena + static_cast<size_t>(s) * c->slot_bytes, so.host, so.bytes,
                                         cudaMemcpyHostToDevice, c->copy);
                 if (e == cudaSuccess) e = cudaEventRecord(sl.ready, c->copy);
-                if (e != cudaSuccess) return static_cast<bd_status>(bd::cuda_status(e));
+            }
+            if (e != cudaSuccess) {
+                // the slot's old contents are gone (evicted above, perhaps partly overwritten): leave it
+                // empty; hand out nothing, so the failed step needs no release
+                sl.variant = -1;
+                sl.last_use = 0;
+                c->acquired.clear();
+                return static_cast<bd_status>(bd::cuda_status(e));
             }
             sl.variant = v;
             c->slot_of[v] = s;
@@ -221,8 +231,10 @@ bd_status bd_cache_step(bd_cache* c, const int32_t* vid, int64_t n, void* stream
         c->acquired.push_back(s);
         granted[v] = s;
         if (c->arena)
-            if (const int cs_ = bd::cuda_status(cudaStreamWaitEvent(st, c->slots[s].ready, 0)))
+            if (const int cs_ = bd::cuda_status(cudaStreamWaitEvent(st, c->slots[s].ready, 0))) {
+                c->acquired.clear();  // nothing handed out (the slot keeps its loaded variant)
                 return static_cast<bd_status>(cs_);
+            }
     }
     for (int64_t i = 0; i < n; ++i) {
         const int32_t v = vid[i];
@@ -257,6 +269,14 @@ bd_status bd_cache_release(bd_cache* c, void* stream)
         }
     }
     c->acquired.clear();
+    return BD_OK;
+}
+
+bd_status bd_cache_debug_fail_load(bd_cache* c, int64_t n)
+{
+    if (!c || n < 0) return BD_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lk(c->mu);
+    c->fail_countdown = n;
     return BD_OK;
 }
 

@@ -12,10 +12,12 @@
 namespace {
 
 constexpr int64_t kMaxRows = BD_NOALLOC_MAX_ROWS;
+static_assert(kMaxRows % bd::kCompressRowsPerCta == 0, "whole compression CTAs");
 constexpr size_t kPartials = static_cast<size_t>(kMaxRows / bd::kCompressRowsPerCta);
 
-// One fp64 partial sum per compression CTA (8 rows).  Every GPU that loads
-// the library holds these 256 KiB until the process exits.
+// One fp64 partial sum per compression CTA (kCompressRowsPerCta = 4 rows):
+// 65536 doubles.  Every GPU that loads the library holds these 512 KiB until
+// the process exits.
 static __device__ __align__(256) double g_noalloc_partials[kPartials];
 
 constexpr int kMaxDevices = 64;

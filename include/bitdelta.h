@@ -20,8 +20,10 @@
  *  - alpha: float32, one per output row (BD_ALPHA_PER_ROW) or one per matrix
  *    (BD_ALPHA_PER_MATRIX).
  *  - Shapes: d_in must be a positive multiple of 128 (every packed sign row
- *    then starts on a 16-byte boundary, which the bulk copies need);
- *    d_out >= 0 and T >= 0 are otherwise free (zero sizes are a no-op).
+ *    then starts on a 16-byte boundary, which the bulk copies need; the bit
+ *    packing alone would only need a multiple of 32, so this is the stricter
+ *    rule of this library); d_out >= 0 and T >= 0 are otherwise free (zero
+ *    sizes are a no-op).
  *  - Alignment: bf16 and sign buffers and y must be 16-byte aligned; alpha,
  *    vid, perm, seg_off 4-byte aligned; workspaces 256-byte aligned.
  *  - Asynchrony: all work is enqueued on `stream` (a cudaStream_t; NULL is
@@ -34,9 +36,12 @@
  *    non-finite delta, a wait that timed out) set bits there; read and clear
  *    them with bd_check_async.  Calls that share a workspace must be ordered
  *    on one stream.
- *  - No exceptions cross this boundary.  The library keeps no mutable global
- *    state other than a per-device attribute cache, so it may be called from
- *    several host threads.
+ *  - No exceptions cross this boundary.  Mutable global state: a per-device
+ *    cache of device attributes and kernel settings (filled once, under a
+ *    lock or with atomics), the thread_local launch
+ *    parameter blocks of the multi-variant and prefill launches (one per
+ *    host thread), and the fixed scratch array of bd_compress_noalloc.  The
+ *    library may be called from several host threads.
  */
 #ifndef BITDELTA_H
 #define BITDELTA_H
@@ -114,8 +119,8 @@ bd_status bd_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_ou
  *         must not overlap any input.
  * Accumulation is fp32.  T <= 64 runs the decode kernel (the base and the
  * sign contraction are kept apart, so W_eff is never rounded); larger T runs
- * the prefill GEMM, which rounds W_eff to bf16 in shared memory before the
- * tensor-core contraction.  For a given (T, d_in) the result of a row does
+ * the prefill GEMM, which rounds W_eff to bf16 in tensor memory (the A
+ * operand of the tensor-core contraction) before multiplying.  For a given (T, d_in) the result of a row does
  * not depend on d_out, so a row-sharded call reproduces the unsharded one
  * bit for bit.
  * ------------------------------------------------------------------------ */
@@ -133,6 +138,9 @@ bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const 
  * x        : device bf16 [T][d_in];  vid: device int32 [T]
  * signs_tab: host array of V device pointers, each uint32 [d_out][d_in/32]
  * alpha_tab: host array of V device pointers, each float32 [d_out] or [1]
+ *            (host arrays, read during the call: the library builds each
+ *            variant's tensor map from them; the pointed-to data is read by
+ *            the kernels in stream order)
  * y        : device [T][d_out] in the caller's token order.
  * 1 <= V <= BD_MAX_VARIANTS.  An id outside [-1, V) sets BD_ERR_BAD_VARIANT
  * in the error word and that token is computed as a base-model token.
@@ -161,7 +169,10 @@ bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int3
                           size_t ws_bytes, void* stream);
 
 /* ------------------------------------------------------------------------
- * Router on its own (the grouping that bd_linear_multi does internally).
+ * Router on its own -- section "Sunum mimarisi", serving steps 1-3: a request
+ * names its variant, the router looks that variant's delta up and sends the
+ * request to the fused kernel with it.  This is the grouping that
+ * bd_linear_multi does internally, exposed so that it can be checked.
  * perm   : device int32 [T]   -- token indices, stably sorted by vid+1
  * seg_off: device int32 [V+2] -- seg_off[k] = number of tokens with
  *          vid+1 < k; segment 0 holds the base-model tokens.
@@ -237,8 +248,9 @@ bd_status bd_monosoup_merge(const uint16_t* w_base, const uint16_t* const* w_ft,
  * code that must not allocate while a stream is being captured, or plain C
  * hosts with no device allocator of their own.  This variant computes
  * exactly what bd_compress computes, but keeps the per-matrix partial sums
- * in a fixed device array of the library (256 KiB per GPU that loads the
- * library, held until the process exits) instead of in `ws`.
+ * in a fixed device array of the library (one fp64 sum per 4-row block of
+ * BD_NOALLOC_MAX_ROWS rows: 512 KiB on every GPU that loads the library,
+ * held until the process exits) instead of in `ws`.
  *  - d_out may be at most BD_NOALLOC_MAX_ROWS, else BD_ERR_UNSUPPORTED_SHAPE.
  *  - The first call on a device looks up that array's device address (once
  *    per device, with the device current); make that first call before any
@@ -292,9 +304,11 @@ bd_status bd_compress_noalloc(const uint16_t* w_base, const uint16_t* w_ft, int6
  *   into them wait for that point on the copy stream.
  * bd_cache_destroy: frees the cache object and its events; copies already
  *   issued may still be writing the arena, so the caller keeps the arena and
- *   the host sources alive until the copy stream has drained.  A step that
- *   fails with BD_ERR_CUDA may have handed out some slots: call
- *   bd_cache_release before the next step.
+ *   the host sources alive until the copy stream has drained.
+ * A step that fails with BD_ERR_CUDA hands out no slot (the next step needs
+ *   no bd_cache_release first).  Loads it issued before the failure stay
+ *   valid and resident; the slot whose load failed is left empty (its former
+ *   variant was evicted); its rate and statistics updates stand.
  * ------------------------------------------------------------------------ */
 typedef struct bd_cache bd_cache;
 
@@ -324,6 +338,11 @@ bd_status bd_cache_release(bd_cache* cache, void* stream);
 bd_status bd_cache_get_stats(bd_cache* cache, bd_cache_stats* out);
 /* resident / pinned (0 or 1) and current request rate of one variant */
 bd_status bd_cache_query(bd_cache* cache, int32_t variant, int32_t* resident, int32_t* pinned, double* rate);
+/* Test aid, not for serving: the n-th load issued from now on (n >= 1; 0
+ * cancels) fails as if its copy had returned a CUDA error, before any copy
+ * is enqueued, so that the failure path above can be exercised on the host
+ * (also by a dry-run cache, which makes no CUDA call). */
+bd_status bd_cache_debug_fail_load(bd_cache* cache, int64_t n);
 
 /* Waits for `stream`, then reads and clears the error word in `ws`.
  * Returns BD_OK, or the first asynchronous error found (in the order

@@ -133,6 +133,26 @@ def test_step_needs_release_and_rejects_bad_ids():
     assert c.stats() == before  # a rejected step changes nothing
 
 
+def test_failed_load_hands_out_nothing_and_needs_no_release():
+    """A copy that fails (a host-side fake of the failing call) ends the
+    step with BD_ERR_CUDA: nothing is handed out, so the next step runs
+    without a release; the load issued before the failure stays resident,
+    the slot whose load failed is empty, later variants were not loaded."""
+    c = make_cache(4, 0, range(8))
+    step(c, [0, 1])
+    c.debug_fail_load(2)
+    with pytest.raises(bd.BitDeltaError) as ei:
+        c.step([2, 2, 3, 4])  # 2 loads, 3 fails, 4 is never reached
+    assert ei.value.status == bd.BD_ERR_CUDA
+    assert resident(c, range(8)) == {0, 1, 2}
+    st = c.stats()
+    assert st["loads"] == 3 and st["resident"] == 3
+    d, s = step(c, [3, 0])  # no release needed; the empty slot takes 3
+    assert list(s) == [bd.BD_CACHE_SERVED, bd.BD_CACHE_SERVED]
+    assert resident(c, range(8)) == {0, 1, 2, 3}
+    assert c.stats()["loads"] == 4
+
+
 def test_create_and_source_errors():
     with pytest.raises(bd.BitDeltaError):
         bd.DeltaCache(None, 0, 0, n_slots=4)
@@ -146,15 +166,32 @@ def test_create_and_source_errors():
         c.set_source(0, torch.zeros(16, dtype=torch.uint8))  # resident
 
 
+def _dyadic_variants(seed, V, d_out, d_in):
+    """W_base in {k/64 : |k| <= 8} and W_v = W_base +- 2^-(3 + v mod 6): with
+    integer activations every partial sum of the fused linear is exact in
+    fp32, so the GPU result must equal the fp64 oracle bit for bit."""
+    from bit_weight_delta_bd_gb300 import synth
+
+    rng = np.random.default_rng(seed)
+    wb = rng.integers(-8, 9, size=(d_out, d_in)).astype(np.float32) / 64.0
+    wfs = []
+    for v in range(V):
+        s = np.where(rng.random((d_out, d_in)) < 0.5, -1.0, 1.0).astype(np.float32)
+        wfs.append(synth.f32_to_bf16_bits(wb + s * 2.0 ** -(3 + v % 6)))
+    return synth.f32_to_bf16_bits(wb), wfs
+
+
 @pytest.mark.gpu
 def test_cache_serves_bd_linear_multi_bit_identical():
     """Real arena (8 slots, 6 pinned) in front of bd_linear_multi: 14
     variants' packed signs and alphas live in pinned host memory and are
-    loaded on demand on a copy stream; every step's output equals the same
-    call on device-resident deltas bit for bit; queued requests are served
-    by a later step."""
+    loaded on demand on a copy stream.  Every step's output equals the fp64
+    oracle on the same tokens bit for bit (exact dyadic inputs) and the same
+    call on device-resident deltas; queued requests are served by a later
+    step."""
     import ctypes
 
+    import oracle
     from bit_weight_delta_bd_gb300 import synth
 
     assert torch.cuda.is_available()
@@ -163,7 +200,8 @@ def test_cache_serves_bd_linear_multi_bit_identical():
     __graft_entry__.build()
     dev = torch.device("cuda:0")
     V, d_out, d_in, T = 14, 512, 1024, 32
-    wb, wfs, _, _, _ = synth.multi_problem(5, d_out, d_in, T, V)
+    wb, wfs = _dyadic_variants(5, V, d_out, d_in)
+    refs = [oracle.compress(wb, wf, per_row=True) for wf in wfs]
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)  # noqa: E731
     wb_d = to(wb)
     ws = bd.new_workspace(max(bd.bd_compress_workspace_size(d_out, d_in, bd.BD_ALPHA_PER_ROW),
@@ -172,6 +210,10 @@ def test_cache_serves_bd_linear_multi_bit_identical():
     alphas = [torch.empty(d_out, dtype=torch.float32, device=dev) for _ in range(V)]
     for v in range(V):
         bd.bd_compress(wb_d, to(wfs[v]), bd.BD_ALPHA_PER_ROW, signs[v], alphas[v], ws)
+    assert bd.bd_check_async(ws) == bd.BD_OK
+    for v in range(V):
+        assert np.array_equal(signs[v].cpu().numpy().view(np.uint32), refs[v][0])
+        assert np.array_equal(alphas[v].cpu().numpy(), refs[v][1])
     sbytes = d_out * d_in // 8
     slot = (sbytes + 4 * d_out + 255) // 256 * 256
     blobs = []
@@ -192,7 +234,7 @@ def test_cache_serves_bd_linear_multi_bit_identical():
     for k in range(30):
         new_vid = synth.zipf_variant_ids(rng, T, V)
         new_vid[rng.random(T) < 0.1] = -1
-        new_x = synth.activations(rng, T, d_in)
+        new_x = synth.f32_to_bf16_bits(rng.integers(-4, 5, size=(T, d_in)).astype(np.float32))
         vids = np.concatenate([np.array([p[0] for p in pending], np.int32), new_vid]) if pending else new_vid
         xs = np.concatenate([np.stack([p[1] for p in pending]), new_x]) if pending else new_x
         ptr, state = cache.step(vids)
@@ -217,7 +259,10 @@ def test_cache_serves_bd_linear_multi_bit_identical():
         y_ref = torch.empty_like(y)
         bd.bd_linear_multi(x_d, v_d, signs, alphas, bd.BD_ALPHA_PER_ROW, wb_d, y_ref, ws)
         assert bd.bd_check_async(ws) == bd.BD_OK
-        assert torch.equal(y, y_ref), f"step {k}"
+        y_host = y.cpu().numpy().astype(np.float64)
+        y_oracle = oracle.linear_multi(sx, sv, [r[0] for r in refs], [r[1] for r in refs], True, wb)
+        assert np.array_equal(y_host, y_oracle), f"step {k}: differs from the oracle"
+        assert torch.equal(y, y_ref), f"step {k}: differs from the resident-delta call"
     st = cache.stats()
     assert st["pinned"] == 6 and st["resident"] <= 8 and st["loads"] >= 6
     assert served_total + len(pending) == 30 * T

@@ -9,6 +9,7 @@ variants and 64 Zipf-routed tokens; plus ragged shapes, exact dyadic inputs
 sharding, canary guards, determinism and argument errors.
 """
 import ctypes
+import os
 
 import numpy as np
 import pytest
@@ -116,6 +117,86 @@ def test_compress_nonfinite_is_flagged(dev):
     assert bd.bd_check_async(ws) == bd.BD_OK  # cleared
     s_ref, _ = oracle.compress(wb, wf, per_row=True)
     assert np.array_equal(u32(signs), s_ref)  # bits still written
+
+
+def _golden_hand_rows():
+    """Rows of tests/golden/hand_bits.txt: (name, W_ft values [64], expected words [2]).
+    W_base = 0 everywhere; W_ft = -1.0 except the listed columns."""
+    rows = []
+    with open(os.path.join(os.path.dirname(__file__), "golden", "hand_bits.txt")) as fh:
+        for line in fh:
+            if not line.strip() or line.startswith("#"):
+                continue
+            name, cols, words = [p.strip() for p in line.split("|")]
+            wf = np.full(64, -1.0, np.float32)
+            for item in filter(None, cols.split(",")):
+                c, v = item.split("=")
+                wf[int(c)] = np.float32(float(v))
+            rows.append((name, wf, [int(w, 16) for w in words.split()]))
+    return rows
+
+
+@pytest.mark.parametrize("mode", [PR, PM])
+def test_compress_golden_hand_rows_on_device(dev, mode):
+    """The hand-built sign rows (sign(0) = +1 for +0.0 and -0.0, the bit of
+    each column at its place) through bd_compress, checked against the words
+    the golden file prints, not against the oracle.  Each 64-column pattern
+    is placed at every 64-column offset of a 1024-column row and at several
+    row positions of a 37-row matrix (different lanes, warps and CTAs); the
+    rest of the matrix is -1.0 (all bits 0)."""
+    rows = _golden_hand_rows()
+    assert any(r[0] == "negzero_col9" for r in rows) and any(r[0] == "zero_col5" for r in rows)
+    d_out, d_in = 37, 1024
+    wf = np.full((d_out, d_in), -1.0, np.float32)
+    expect = np.zeros((d_out, d_in // 32), np.uint32)
+    placed = 0
+    for k, (name, pat, words) in enumerate(rows):
+        for r in (k, k + 8, k + 29) if k + 29 < d_out else (k, k + 8):
+            off = 64 * ((r * 5 + k) % (d_in // 64))
+            wf[r, off:off + 64] = pat
+            expect[r, off // 32:off // 32 + 2] = words
+            placed += 1
+    assert placed >= 16
+    wb = np.zeros_like(wf)
+    wf_bits = synth.f32_to_bf16_bits(wf)
+    assert np.any(wf_bits == 0x8000), "-0.0 must reach the device as its own bit pattern"
+    s, a = gpu_compress(to_dev(synth.f32_to_bf16_bits(wb), dev), to_dev(wf_bits, dev), mode, dev)
+    got = u32(s)
+    for r in range(d_out):
+        assert np.array_equal(got[r], expect[r]), f"row {r}: {[hex(w) for w in got[r]]}"
+    absd = np.abs(wf.astype(np.float64))  # |Delta| = |W_ft| with W_base = 0
+    a_ref = absd.mean(axis=1) if mode == PR else np.array([absd.mean()])
+    assert_alpha(a.cpu().numpy(), a_ref.astype(np.float32))
+
+
+def test_compress_row_blocks_per_matrix_alpha(dev):
+    """Row sharding of a per-matrix alpha through the library: bd_compress on
+    pointer-offset row blocks (one of them empty, whose alpha buffer keeps
+    its NaN), alphas combined with the fp64 row weighting of the sharded
+    all-reduce, against the unsharded bd_compress and the oracle; the
+    stacked signs equal the unsharded ones bit for bit."""
+    from bit_weight_delta_bd_gb300 import shard
+
+    d_out, d_in = 1000, 1024
+    wb, wf, _ = synth.single_problem(901, d_out, d_in, 1)
+    wb_d, wf_d = to_dev(wb, dev), to_dev(wf, dev)
+    s_all, a_all = gpu_compress(wb_d, wf_d, PM, dev)
+    _, a_ref = oracle.compress(wb, wf, per_row=False)
+    for bounds in ([0, 333, 334, 1000], [0, 500, 500, 1000], [0, 1, 999, 1000]):
+        shares = torch.zeros(1, dtype=torch.float64, device=dev)
+        parts = []
+        for r0, r1 in zip(bounds[:-1], bounds[1:]):
+            s = torch.empty((r1 - r0, d_in // 32), dtype=torch.int32, device=dev)
+            a = torch.full((1,), float("nan"), dtype=torch.float32, device=dev)
+            ws = bd.new_workspace(bd.bd_compress_workspace_size(r1 - r0, d_in, PM), dev)
+            bd.bd_compress(wb_d[r0:r1], wf_d[r0:r1], PM, s, a, ws)
+            assert bd.bd_check_async(ws) == bd.BD_OK
+            shares += shard.alpha_share(a, r1 - r0)
+            parts.append(s)
+        alpha = shard.combine_alpha(shares, d_out)
+        assert torch.equal(torch.cat(parts, dim=0), s_all)
+        assert_alpha(alpha.cpu().numpy(), a_ref)
+        assert_alpha(alpha.cpu().numpy(), a_all.cpu().numpy())
 
 
 # ============================================================================ linear

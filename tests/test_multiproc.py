@@ -7,7 +7,8 @@ exactly.  The benchmark's multi-GPU timing reduction (slowest rank wins) is
 checked the same way.  A per-matrix alpha under row sharding is the one
 exchange (``shard.per_matrix_alpha_allreduce``): it must match the unsharded
 alpha within the 1e-6 relative bound, and a rank that never reaches it must
-turn into BD_ERR_TIMEOUT on the others, not a hang.
+turn into BD_ERR_TIMEOUT on the others, not a hang (gloo; under NCCL the
+watchdog handles a timed-out collective instead).
 """
 import os
 import socket
@@ -69,7 +70,7 @@ def test_row_sharding_two_gloo_ranks():
     assert [r[2] for r in res] == [11.0, 11.0]
 
 
-def _alpha_rank(rank, world, port, q):
+def _alpha_rank(rank, world, port, q, d_out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     dist.init_process_group("gloo", rank=rank, world_size=world)
     try:
@@ -77,10 +78,13 @@ def _alpha_rank(rank, world, port, q):
         from bit_weight_delta_bd_gb300 import shard, synth
 
         oracle.set_threads(1)
-        d_out, d_in = 70, 256
+        d_in = 256
         wb, wf, _ = synth.single_problem(7, d_out, d_in, 1)
         r0, r1 = shard.row_bounds(d_out, world, rank)
-        _, a = oracle.compress(wb[r0:r1], wf[r0:r1], per_row=False)
+        if r1 > r0:
+            _, a = oracle.compress(wb[r0:r1], wf[r0:r1], per_row=False)
+        else:  # no rows: the compression writes no alpha, so the buffer holds whatever it held
+            a = np.array([np.nan], np.float32)
         alpha = shard.per_matrix_alpha_allreduce(torch.from_numpy(a), r1 - r0, d_out)
         _, a_all = oracle.compress(wb, wf, per_row=False)
         q.put((rank, float(alpha.item()), float(a_all[0]), r1 - r0))
@@ -89,19 +93,22 @@ def _alpha_rank(rank, world, port, q):
 
 
 @pytest.mark.timeout(300)
-@pytest.mark.parametrize("world", [2, 3])
-def test_per_matrix_alpha_under_row_sharding(world):
+@pytest.mark.parametrize("world,d_out", [(2, 70), (3, 70), (3, 2)])
+def test_per_matrix_alpha_under_row_sharding(world, d_out):
+    """d_out = 2 over 3 ranks leaves one rank without rows; its NaN alpha
+    buffer must not reach the others."""
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
     port = _free_port()
-    procs = [ctx.Process(target=_alpha_rank, args=(r, world, port, q)) for r in range(world)]
+    procs = [ctx.Process(target=_alpha_rank, args=(r, world, port, q, d_out)) for r in range(world)]
     for p in procs:
         p.start()
     res = sorted(q.get(timeout=240) for _ in procs)
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    assert sum(r[3] for r in res) == 70
+    assert sum(r[3] for r in res) == d_out
+    assert all(np.isfinite(r[1]) for r in res)
     alphas = {r[1] for r in res}
     assert len(alphas) == 1  # every rank holds the same alpha
     got, ref = alphas.pop(), res[0][2]
