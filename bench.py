@@ -6,23 +6,32 @@ one step is the whole path over one batch: bd_compress (Delta, sign bits,
 alpha) followed by the fused linear for 1, 4 and 16 tokens.  The metric is
 HBM GB/s of algorithmic bytes per step; the JSON line also carries tokens/s,
 the roofline of the dominant kernel (CUDA-event timed inside the timed
-region), the CPU oracle timed on the host cores, an end-to-end number with
-host buffers, and the SM clocks sampled during the timed region.
+region), the CPU oracle timed on the host cores (all of them and one), an
+end-to-end number with host buffers (the full step, and a serving step in
+which the weights stay resident), and the SM clocks sampled during the timed
+region.
 
-Other workloads (--workload): tiny (256x256, T=4, per-matrix alpha), multi
-(8192x8192 shared W_base, 14 variants, 64 Zipf-routed tokens) and prefill
-(4096 tokens x 8192x8192, the tensor-core path, reported in TFLOP/s).  The
-default decode line also carries a short prefill measurement under
-"prefill", since the metric names prefill TFLOP/s.  slice: the 8-layer slice of
-a 70B-shaped stack (56 linears, 14 variants compressed on the GPU, 32 decode
-tokens routed by Zipf), one step = the 56 multi-variant linears.
+The default line also carries one sub-measurement per other workload of the
+serving setup, each timed in its own region with its own roofline, clocks
+and CPU oracle baseline: "tiny" (256 x 256, T = 4, per-matrix alpha; L2-
+resident, latency only), "multi" (8192 x 8192 shared W_base, 14 variants,
+64 Zipf-routed tokens), "prefill" (4096 tokens x 8192 x 8192, tensor cores,
+TFLOP/s) and "slice" (8 layers of a 70B-shaped stack, 56 multi-variant
+linears, 14 variants compressed on the GPU, 32 decode tokens).
 
-`python bench.py --impl reference` times the CPU oracle instead (the
-reference arm), on bounded samples of the same workload.
+--workload runs any of them (and materialize, multi_prefill, monosoup) as the
+main line instead.  `python bench.py --impl reference` times the CPU oracle
+instead (the reference arm), on bounded samples of the same workload.
 
-Multi-GPU: one process per GPU (torchrun); every rank runs its own copy of
-the workload (the path has no exchange step), the timed region is bracketed
-by barriers and the slowest rank's time is reported (weak scaling).
+Multi-GPU (--gpus N): one process per GPU.  Without a torchrun environment
+the script relaunches itself under torch.distributed.run with N ranks.  Every
+matrix is partitioned by output rows (rank r owns rows [r d_out / N,
+(r + 1) d_out / N)); x is replicated; per-row alpha needs no exchange; a
+per-matrix alpha takes one fp64 all-reduce; each rank's kernels read only
+its own rows.  The timed region is bracketed by barriers and the slowest
+rank's time is reported; value = the whole matrices' bytes / that time
+(strong scaling).  The all-gather of y that a following layer would need is
+timed separately ("exchange").
 """
 from __future__ import annotations
 
@@ -30,10 +39,11 @@ import argparse
 import hashlib
 import json
 import os
+import socket
 import statistics
 import subprocess
-import threading
 import sys
+import threading
 import time
 
 import numpy as np
@@ -44,6 +54,7 @@ sys.path.insert(0, ROOT)
 METRIC = "fused BitDelta linear HBM GB/s (% of peak), tokens/s; prefill TFLOP/s (% peak)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+DATA = "synthetic (seeded numpy / torch generators; shapes and distributions of the BitDelta serving setup)"
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
 # one ncu capture, keyed by kernel; each entry records the sha256 of the
@@ -65,9 +76,8 @@ NCU_TRAFFIC = {
     ("materialize_kernel", "materialize"): ("fae23fcd0ba90d9b", "bd_materialize.cu", 499_370_496 + 426_232_320),
 }
 
-
-# kernels each timed call launches: multi = prepare + fused kernel; multi_prefill =
-# router + plan + gather + grouped prefill; slice = 56 multi calls
+# kernels each call launches: multi = prepare + fused kernel; multi_prefill =
+# router + plan + gather + grouped prefill; monosoup = the merge's launches
 LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4, "monosoup": 88}
 # workloads whose own figure is tensor throughput (TFLOP/s) rather than GB/s
 TENSOR_WORKLOADS = ("prefill", "multi_prefill")
@@ -77,21 +87,24 @@ ALU_WORKLOADS = ("monosoup",)
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 # MonoSoup workload: k checkpoints, rank r, sketch width l, power iterations q
 MONOSOUP = {"d": 8192, "k": 3, "rank": 16, "l": 32, "q": 1}
+# sub-measurements of the default line: (name, timed steps, warm-up steps)
+SUBS = (("tiny", 200, 10), ("multi", 20, 5), ("prefill", 20, 3), ("slice", 10, 3))
+WORKLOADS = ("decode", "tiny", "multi", "prefill", "multi_prefill", "materialize", "monosoup", "slice")
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
-    p.add_argument("--workload", choices=["decode", "tiny", "multi", "prefill", "multi_prefill", "materialize", "monosoup",
-                                          "slice"], default="decode")
-    p.add_argument("--no-prefill", action="store_true", help="skip the prefill sub-measurement of the decode line")
+    p.add_argument("--workload", choices=WORKLOADS, default="decode")
+    p.add_argument("--no-sub", action="store_true", help="skip the sub-measurements of the default line")
+    p.add_argument("--sub", default="", help="comma-separated subset of the sub-measurements (default: all)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def _src_sha(name: str) -> str:
@@ -110,7 +123,12 @@ def load_peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, "fallback"
 
 
-# ----------------------------------------------------------------------------- workloads
+def row_span(d_out: int, world: int, rank: int) -> tuple[int, int]:
+    """Rows [r0, r1) of `rank` under the output-row partition (sizes differ by at most one)."""
+    return d_out * rank // world, d_out * (rank + 1) // world
+
+
+# ----------------------------------------------------------------------------- algorithmic bytes and FLOPs
 
 def materialize_bytes(d_out, d_in, n_alpha):
     """W_base read, W_eff written (2 bytes each per weight), bits and alpha read."""
@@ -118,7 +136,7 @@ def materialize_bytes(d_out, d_in, n_alpha):
 
 
 def monosoup_bytes(d, k, q):
-    """Each pass over a task vector reads W_i and W_base (2 + 2q + ... passes:
+    """Each pass over a task vector reads W_i and W_base (2 + 2q passes:
     sketch, 2q power-iteration products, B^T), plus the merge's W_base read
     and W_merged write."""
     return k * (2 + 2 * q) * 4 * d * d + 4 * d * d
@@ -135,82 +153,109 @@ def linear_bytes(T, d_out, d_in, n_alpha, y_bytes=2):
     return 2 * d_out * d_in + d_out * d_in // 8 + 4 * n_alpha + 2 * T * d_in + y_bytes * T * d_out
 
 
+def multi_bytes(T, d_out, d_in, n_active, per_row=True):
+    """Multi-variant linear: W_base once + bits and alpha of every active
+    variant + x + y + variant ids."""
+    n_alpha = d_out if per_row else 1
+    return 2 * d_out * d_in + n_active * (d_out * d_in // 8 + 4 * n_alpha) + 2 * T * d_in + 2 * T * d_out + 4 * T
+
+
 def compress_bytes(d_out, d_in, n_alpha):
     """Algorithmic bytes of one compression: W_base + W_ft read, bits + alpha written."""
     return 4 * d_out * d_in + d_out * d_in // 8 + 4 * n_alpha
 
 
-class Workload:
-    """Host inputs (numpy bf16 bits) plus the list of calls of one step."""
+# ----------------------------------------------------------------------------- workloads
 
-    def __init__(self, name, seed):
+class Workload:
+    """Host inputs (numpy bf16 bits) of one workload, restricted to the output
+    rows [r0, r1) a rank owns (all rows for one GPU), plus its description."""
+
+    def __init__(self, name, seed, world=1, rank=0):
         from bit_weight_delta_bd_gb300 import synth
 
-        self.name = name
+        self.name, self.seed, self.world, self.rank = name, seed, world, rank
+        self.wb, self.wf, self.xs, self.vid = None, [], [], None
         if name == "slice":  # weights are drawn on the device by SliceRun
             self.tokens = [32]
             self.per_row = True
             self.vid = synth.zipf_variant_ids(np.random.default_rng(seed), 32, 14)
-            self.d_out = self.d_in = 0
-            self.wf, self.xs, self.wb = [None] * 14, [], None
+            self.d_out_full = self.d_out = self.d_in = 0
             self.n_alpha = 0
+            self.r0 = self.r1 = 0
             return
         if name in ("decode", "tiny"):
             d_out, d_in = (28672, 8192) if name == "decode" else (256, 256)
             self.tokens = [1, 4, 16] if name == "decode" else [4]
             self.per_row = name == "decode"
             rng = np.random.default_rng(seed)
-            self.wb = synth.base_weight(rng, d_out, d_in)
-            self.wf = [synth.finetuned_weight(rng, self.wb, 1e-3)]
+            wb = synth.base_weight(rng, d_out, d_in)
+            wfs = [synth.finetuned_weight(rng, wb, 1e-3)]
             self.xs = [synth.activations(rng, T, d_in) for T in self.tokens]
-            self.vid = None
         elif name == "materialize":
             d_out, d_in = 28672, 8192
             self.tokens = []
             self.per_row = True
-            self.wb, wf, _ = synth.single_problem(seed, d_out, d_in, 1)
-            self.wf = [wf]
-            self.xs = []
-            self.vid = None
+            wb, wf, _ = synth.single_problem(seed, d_out, d_in, 1)
+            wfs = [wf]
         elif name == "monosoup":
             d_out = d_in = MONOSOUP["d"]
             self.tokens = []
             self.per_row = True
-            self.wb, self.wf = synth.monosoup_checkpoints(seed, d_out, d_in, MONOSOUP["k"], MONOSOUP["rank"])
+            wb, wfs = synth.monosoup_checkpoints(seed, d_out, d_in, MONOSOUP["k"], MONOSOUP["rank"])
             self.omega = synth.gaussian_test_matrix(seed + 1, d_in, MONOSOUP["l"])
-            self.xs = []
-            self.vid = None
         elif name == "prefill":
             d_out, d_in = 8192, 8192
             self.tokens = [4096]
             self.per_row = True
-            self.wb, wf, x = synth.single_problem(seed + 3, d_out, d_in, 4096)
-            self.wf = [wf]
+            wb, wf, x = synth.single_problem(seed + 3, d_out, d_in, 4096)
+            wfs = [wf]
             self.xs = [x]
-            self.vid = None
         else:  # multi (64 tokens, decode kernel) or multi_prefill (4096 tokens, tensor cores)
             d_out, d_in = 8192, 8192
             self.tokens = [4096 if name == "multi_prefill" else 64]
             self.per_row = True
-            self.wb, self.wf, x, self.vid, _ = synth.multi_problem(seed, d_out, d_in, self.tokens[0], 14)
+            wb, wfs, x, self.vid, _ = synth.multi_problem(seed, d_out, d_in, self.tokens[0], 14)
             self.xs = [x]
-        self.d_out, self.d_in = d_out, d_in
-        self.n_alpha = d_out if self.per_row else 1
+        self.d_out_full, self.d_in = d_out, d_in
+        if name == "monosoup" and world > 1:
+            raise SystemExit("monosoup: the merge is not row-partitioned (its subspace spans every row); use --gpus 1")
+        self.r0, self.r1 = row_span(d_out, world, rank)
+        self.wb = np.ascontiguousarray(wb[self.r0:self.r1])
+        self.wf = [np.ascontiguousarray(w[self.r0:self.r1]) for w in wfs]
+        self.d_out = self.r1 - self.r0
+        self.n_alpha = self.d_out if self.per_row else 1
+
+    def active(self) -> int:
+        return 0 if self.vid is None else len(set(int(v) for v in self.vid if v >= 0))
+
+    def step_bytes_full(self) -> int:
+        """Algorithmic bytes of one step over the whole matrices (all ranks' rows)."""
+        return _step_bytes(self.name, self.d_out_full, self.d_in, self.tokens, self.per_row, self.active(),
+                           len(self.wf))
+
+    def step_flops_full(self) -> int:
+        if self.name == "monosoup":
+            return monosoup_flops(self.d_out_full, len(self.wf), MONOSOUP["rank"], MONOSOUP["l"], MONOSOUP["q"])
+        if self.name == "slice":
+            return sum(2 * 32 * d_out * d_in for _, d_out, d_in in _slice_linears()) * 8
+        return sum(2 * T * self.d_out_full * self.d_in for T in self.tokens)
 
     def config(self):
-        c = {"workload": self.name, "d_out": self.d_out, "d_in": self.d_in, "tokens": self.tokens,
+        par = ("single GPU" if self.world == 1 else
+               f"rows{self.world}: output rows of every matrix split over {self.world} GPUs, x replicated")
+        if self.name == "slice":
+            return {"workload": "slice_8_layers_70b_shapes_V14_T32", "layers": 8,
+                    "linears": "q/o 8192x8192, k/v 8192->1024, gate/up 8192->28672, down 28672->8192",
+                    "variants": 14, "active_variants": self.active(), "tokens": [32], "alpha": "per_row",
+                    "step": "56 bd_linear_multi calls (variants compressed on the GPU once, untimed)",
+                    "l2": "inputs larger than L2 (13.7 GB of W_base per step)", "parallelism": par}
+        c = {"workload": self.name, "d_out": self.d_out_full, "d_in": self.d_in, "tokens": self.tokens,
              "alpha": "per_row" if self.per_row else "per_matrix"}
         if self.name == "decode":
             c["workload"] = "decode_ffn_28672x8192_T1_4_16"
             c["step"] = "bd_compress + bd_linear at T=1, 4, 16 (one variant)"
             c["l2"] = "inputs larger than L2 (W_base 470 MB, W_ft 470 MB vs 126.5 MB L2)"
-        elif self.name == "slice":
-            c = {"workload": "slice_8_layers_70b_shapes_V14_T32", "layers": 8,
-                 "linears": "q/o 8192x8192, k/v 8192->1024, gate/up 8192->28672, down 28672->8192",
-                 "variants": 14, "active_variants": int(len(set(int(v) for v in self.vid))), "tokens": [32],
-                 "alpha": "per_row",
-                 "step": "56 bd_linear_multi calls (variants compressed on the GPU once, untimed)",
-                 "l2": "inputs larger than L2 (13.7 GB of W_base per step)"}
         elif self.name == "prefill":
             c["workload"] = "prefill_4096x8192x8192"
             c["step"] = "bd_linear at T=4096, one variant (compressed once, untimed); tensor-core path"
@@ -218,7 +263,7 @@ class Workload:
         elif self.name == "multi_prefill":
             c["workload"] = "multi_prefill_8192x8192_V14_T4096"
             c["variants"] = len(self.wf)
-            c["active_variants"] = int(len(set(int(v) for v in self.vid)))
+            c["active_variants"] = self.active()
             c["step"] = ("bd_linear_multi over 4096 Zipf(1.1)-routed tokens: router, gather, grouped tensor-core "
                          "prefill (variants compressed once, untimed)")
             c["l2"] = "inputs larger than L2 (W_base 134 MB + x 67 MB + y 67 MB vs 126.5 MB L2)"
@@ -239,14 +284,35 @@ class Workload:
         else:
             c["workload"] = "multi_tenant_8192x8192_V14_T64"
             c["variants"] = len(self.wf)
-            c["active_variants"] = int(len(set(int(v) for v in self.vid)))
+            c["active_variants"] = self.active()
             c["step"] = "bd_linear_multi over 64 Zipf(1.1)-routed tokens (variants compressed once, untimed)"
             c["l2"] = "L2 flushed (256 MB write) before each step; flush excluded from kernel events"
+        c["parallelism"] = par
         return c
 
 
+def _slice_linears():
+    from bit_weight_delta_bd_gb300 import synth
+
+    return synth.SLICE_LINEARS
+
+
+def _step_bytes(name, d_out, d_in, tokens, per_row, n_active, n_ckpt):
+    n_alpha = d_out if per_row else 1
+    if name == "slice":
+        return 8 * sum(multi_bytes(32, o, i, n_active) for _, o, i in _slice_linears())
+    if name in ("multi", "multi_prefill"):
+        return multi_bytes(tokens[0], d_out, d_in, n_active, per_row)
+    if name == "materialize":
+        return materialize_bytes(d_out, d_in, n_alpha)
+    if name == "monosoup":
+        return monosoup_bytes(d_out, n_ckpt, MONOSOUP["q"])
+    out = 0 if name == "prefill" else compress_bytes(d_out, d_in, n_alpha)
+    return out + sum(linear_bytes(T, d_out, d_in, n_alpha) for T in tokens)
+
+
 class GpuRun:
-    """Device copies of a workload and the calls of one step."""
+    """Device copies of a workload (this rank's rows) and the calls of one step."""
 
     def __init__(self, wl: Workload, dev):
         import torch
@@ -254,8 +320,8 @@ class GpuRun:
         from bit_weight_delta_bd_gb300 import bitdelta as bd
 
         self.bd, self.torch, self.wl, self.dev = bd, torch, wl, dev
-        PR = bd.BD_ALPHA_PER_ROW if wl.per_row else bd.BD_ALPHA_PER_MATRIX
-        self.mode = PR
+        self.mode = bd.BD_ALPHA_PER_ROW if wl.per_row else bd.BD_ALPHA_PER_MATRIX
+        rows, d_in = max(wl.d_out, 0), wl.d_in
 
         def d(a):
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev)
@@ -263,43 +329,50 @@ class GpuRun:
         self.wb = d(wl.wb)
         self.wf = [d(w) for w in wl.wf]
         self.xs = [d(x) for x in wl.xs]
-        self.signs = [torch.empty((wl.d_out, wl.d_in // 32), dtype=torch.int32, device=dev) for _ in wl.wf]
-        self.alpha = [torch.empty(wl.n_alpha, dtype=torch.float32, device=dev) for _ in wl.wf]
-        self.ys = [torch.empty((T, wl.d_out), dtype=torch.bfloat16, device=dev) for T in wl.tokens]
-        self.ws = bd.new_workspace(max(bd.bd_compress_workspace_size(wl.d_out, wl.d_in, PR),
-                                       bd.bd_linear_workspace_size(64, wl.d_out, wl.d_in),
-                                       bd.bd_linear_multi_workspace_size(max(64, max(wl.tokens, default=0)), max(len(wl.wf), 1),
-                                                                         wl.d_out, wl.d_in)), dev)
+        self.signs = [torch.empty((rows, d_in // 32), dtype=torch.int32, device=dev) for _ in wl.wf]
+        self.alpha = [torch.full((wl.n_alpha,), float("nan"), dtype=torch.float32, device=dev) for _ in wl.wf]
+        self.ys = [torch.empty((T, rows), dtype=torch.bfloat16, device=dev) for T in wl.tokens]
+        self.ws = bd.new_workspace(max(bd.bd_compress_workspace_size(rows, d_in, self.mode),
+                                       bd.bd_linear_workspace_size(64, rows, d_in),
+                                       bd.bd_linear_multi_workspace_size(max(64, max(wl.tokens, default=0)),
+                                                                         max(len(wl.wf), 1), rows, d_in)), dev)
         self.vid = None if wl.vid is None else torch.from_numpy(wl.vid).to(dev)
         self.flush = None
+        self.alpha_exchange = None  # per-matrix alpha over row partitions: the one collective of a step
         if wl.name == "materialize":
-            self.w_eff = torch.empty((wl.d_out, wl.d_in), dtype=torch.int16, device=dev)
+            self.w_eff = torch.empty((rows, d_in), dtype=torch.int16, device=dev)
         if wl.name == "monosoup":
             self.omega = torch.from_numpy(wl.omega).to(dev)
-            self.w_merged = torch.empty((wl.d_out, wl.d_in), dtype=torch.bfloat16, device=dev)
-            self.ws_ms = bd.new_workspace(bd.bd_monosoup_workspace_size(wl.d_out, wl.d_in, len(wl.wf),
+            self.w_merged = torch.empty((rows, d_in), dtype=torch.bfloat16, device=dev)
+            self.ws_ms = bd.new_workspace(bd.bd_monosoup_workspace_size(rows, d_in, len(wl.wf),
                                                                         MONOSOUP["rank"], MONOSOUP["l"]), dev)
         if wl.name in ("multi", "prefill", "multi_prefill", "materialize"):
             for v in range(len(wl.wf)):  # variants are compressed once, before timing
-                bd.bd_compress(self.wb, self.wf[v], PR, self.signs[v], self.alpha[v], self.ws)
+                bd.bd_compress(self.wb, self.wf[v], self.mode, self.signs[v], self.alpha[v], self.ws)
             torch.cuda.synchronize()
             self.wf = []  # W_ft is not needed any more
             torch.cuda.empty_cache()
         if wl.name == "multi":
             self.flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        if wl.world > 1 and not wl.per_row:
+            from bit_weight_delta_bd_gb300 import shard
+
+            def exchange():
+                a = shard.per_matrix_alpha_allreduce(self.alpha[0].cpu() if _backend() == "gloo" else self.alpha[0],
+                                                     wl.d_out, wl.d_out_full)
+                self.alpha[0].copy_(a)
+            self.alpha_exchange = exchange
 
     def calls(self):
-        """[(label, kernel name, algorithmic bytes, flops, fn)] of one step."""
+        """[(label, kernel name, algorithmic bytes (this rank), flops, fn)] of one step."""
         bd, wl = self.bd, self.wl
         out = []
         if wl.name in ("multi", "multi_prefill"):
-            active = sorted(set(int(v) for v in wl.vid if v >= 0))
             T = wl.tokens[0]
-            nbytes = (2 * wl.d_out * wl.d_in + len(active) * (wl.d_out * wl.d_in // 8 + 4 * wl.n_alpha) +
-                      2 * T * wl.d_in + 2 * T * wl.d_out + 4 * T)
+            nbytes = multi_bytes(T, wl.d_out, wl.d_in, wl.active(), wl.per_row)
             kname = ("route + gather + prefill_kernel (grouped)" if wl.name == "multi_prefill"
                      else "multi_prepare + multi_kernel<8>")
-            flops = 2 * T * wl.d_out * wl.d_in if wl.name == "multi_prefill" else 4 * T * wl.d_out * wl.d_in
+            flops = 2 * T * wl.d_out * wl.d_in
             out.append((f"linear_multi_T{T}", kname, nbytes, flops,
                         lambda: bd.bd_linear_multi(self.xs[0], self.vid, self.signs, self.alpha, self.mode, self.wb,
                                                    self.ys[0], self.ws)))
@@ -323,23 +396,34 @@ class GpuRun:
                         lambda: bd.bd_linear(self.xs[0], self.wb, self.signs[0], self.alpha[0], self.mode, self.ys[0],
                                              self.ws)))
             return out
-        out.append(("compress", "compress_kernel", compress_bytes(wl.d_out, wl.d_in, wl.n_alpha), 0,
-                    lambda: bd.bd_compress(self.wb, self.wf[0], self.mode, self.signs[0], self.alpha[0], self.ws)))
+
+        def compress():
+            bd.bd_compress(self.wb, self.wf[0], self.mode, self.signs[0], self.alpha[0], self.ws)
+            if self.alpha_exchange is not None:
+                self.alpha_exchange()
+        out.append(("compress", "compress_kernel", compress_bytes(wl.d_out, wl.d_in, wl.n_alpha), 0, compress))
         for i, T in enumerate(wl.tokens):
             nt = 1 if T <= 8 else 2 if T <= 16 else 4 if T <= 32 else 8
             out.append((f"linear_T{T}", f"skinny_kernel<{nt}>", linear_bytes(T, wl.d_out, wl.d_in, wl.n_alpha),
-                        4 * T * wl.d_out * wl.d_in,
+                        2 * T * wl.d_out * wl.d_in,
                         (lambda i=i: bd.bd_linear(self.xs[i], self.wb, self.signs[0], self.alpha[0], self.mode,
                                                   self.ys[i], self.ws))))
         return out
+
+    def serving_calls(self):
+        """The linears alone (weights, signs and alpha resident): the steady-state serving step."""
+        return [c for c in self.calls() if c[0] != "compress"]
 
 
 class SliceRun:
     """The 8-layer slice resident on the device: per linear W_base and the 14
     variants' packed signs and alpha (compressed here, on the GPU, from
-    on-device seeded draws), plus that linear's 32-token input."""
+    on-device seeded draws), plus that linear's 32-token input.  With
+    world > 1 each matrix keeps only this rank's rows.  `sample_rows` rows of
+    every matrix are also kept on the host (W_base and every W_ft) for the
+    CPU oracle baseline."""
 
-    def __init__(self, wl: Workload, dev, seed: int, layers: int = 8):
+    def __init__(self, wl: Workload, dev, seed: int, layers: int = 8, sample_rows: int = 0):
         import torch
 
         from bit_weight_delta_bd_gb300 import bitdelta as bd
@@ -354,40 +438,65 @@ class SliceRun:
         self.ws = bd.new_workspace(ws_bytes, dev)
         self.vid = torch.from_numpy(wl.vid).to(dev)
         rng = np.random.default_rng(seed + 17)
-        self.mats = []
+        self.mats, self.samples = [], []
         for layer in range(layers):
             for m, (name, d_out, d_in) in enumerate(synth.SLICE_LINEARS):
-                wb = synth.device_base_weight(synth.slice_seed(seed, layer, m), d_out, d_in, dev)
+                r0, r1 = row_span(d_out, wl.world, wl.rank)
+                wb_full = synth.device_base_weight(synth.slice_seed(seed, layer, m), d_out, d_in, dev)
+                wb = wb_full[r0:r1].contiguous()
+                smp = None
+                if sample_rows:
+                    rows = synth.sample_rows(layer * 7 + m, r1 - r0, sample_rows)
+                    ridx = torch.from_numpy(rows + r0).to(dev)
+                    smp = {"rows": rows, "d_out": r1 - r0, "d_in": d_in, "wb": _bits16(wb_full[ridx]), "wf": []}
                 signs, alphas = [], []
                 for v in range(V):
-                    wf = synth.device_finetuned_weight(synth.slice_seed(seed, layer, m, v), wb, float(scales[v]))
-                    sg = torch.empty((d_out, d_in // 32), dtype=torch.int32, device=dev)
-                    al = torch.empty(d_out, dtype=torch.float32, device=dev)
+                    wf_full = synth.device_finetuned_weight(synth.slice_seed(seed, layer, m, v), wb_full,
+                                                            float(scales[v]))
+                    wf = wf_full[r0:r1].contiguous()
+                    if smp is not None:
+                        smp["wf"].append(_bits16(wf_full[ridx]))
+                    del wf_full
+                    sg = torch.empty((r1 - r0, d_in // 32), dtype=torch.int32, device=dev)
+                    al = torch.empty(r1 - r0, dtype=torch.float32, device=dev)
                     bd.bd_compress(wb, wf, bd.BD_ALPHA_PER_ROW, sg, al, self.ws)
                     del wf
                     signs.append(sg)
                     alphas.append(al)
-                x = torch.from_numpy(synth.activations(rng, T, d_in).view(np.int16)).to(dev)
-                y = torch.empty((T, d_out), dtype=torch.bfloat16, device=dev)
-                self.mats.append((f"L{layer}.{name}", d_out, d_in, wb, signs, alphas, x, y))
+                del wb_full
+                x_host = synth.activations(rng, T, d_in)
+                x = torch.from_numpy(x_host.view(np.int16)).to(dev)
+                y = torch.empty((T, r1 - r0), dtype=torch.bfloat16, device=dev)
+                self.mats.append((f"L{layer}.{name}", r1 - r0, d_in, wb, signs, alphas, x, y))
+                if smp is not None:
+                    smp["x"] = x_host
+                    self.samples.append(smp)
         torch.cuda.synchronize()
         if bd.bd_check_async(self.ws) != bd.BD_OK:
             raise RuntimeError("asynchronous error while compressing the slice")
         self.flush = None
+        self.alpha_exchange = None
         self.xs = [mt[6] for mt in self.mats]
         self.ys = [mt[7] for mt in self.mats]
 
     def calls(self):
         bd, wl = self.bd, self.wl
-        active = len(set(int(v) for v in wl.vid if v >= 0))
+        active = wl.active()
         T = 32
         out = []
         for label, d_out, d_in, wb, signs, alphas, x, y in self.mats:
-            nbytes = 2 * d_out * d_in + active * (d_out * d_in // 8 + 4 * d_out) + 2 * T * d_in + 2 * T * d_out + 4 * T
-            out.append((label, "multi_prepare + multi_kernel<4>", nbytes, 4 * T * d_out * d_in,
+            out.append((label, "multi_prepare + multi_kernel<4>", multi_bytes(T, d_out, d_in, active),
+                        2 * T * d_out * d_in,
                         (lambda wb=wb, signs=signs, alphas=alphas, x=x, y=y:
                          bd.bd_linear_multi(x, self.vid, signs, alphas, bd.BD_ALPHA_PER_ROW, wb, y, self.ws))))
         return out
+
+    def serving_calls(self):
+        return self.calls()
+
+
+def _bits16(t) -> np.ndarray:
+    return t.contiguous().view(__import__("torch").int16).cpu().numpy().view(np.uint16)
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -463,16 +572,25 @@ def _smi_id(local: int) -> str:
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_time(wl: Workload, budget_s: float = 12.0, threads: int = 0):
+def _cpu_cores() -> int:
+    return os.cpu_count() or 1
+
+
+def oracle_time(wl: Workload, budget_s: float = 12.0, threads: int = 0, slice_samples=None):
     """Times the CPU oracle (as it stands) on a bounded sample of one step:
     whole steps for a small matrix, growing row blocks of one step for a large
-    one, until `budget_s` of wall time is spent.  Returns (GB/s of algorithmic
-    bytes, threads used, sample description)."""
+    one, until `budget_s` of wall time is spent.  Work the GPU step does not
+    time (compressing variants that are resident before the step) is done
+    before the clock starts.  Returns (GB/s of algorithmic bytes, threads
+    used, sample description)."""
     import oracle
 
-    cores = oracle.set_threads(threads)
+    cores = oracle.set_threads(threads if threads > 0 else _cpu_cores())
+    step_bytes = wl.step_bytes_full()
+    if wl.name == "slice":
+        return _oracle_time_slice(wl, slice_samples, cores, step_bytes)
     d_out, d_in = wl.d_out, wl.d_in
-    step_bytes = sum(c[2] for c in _step_bytes_rows(wl))
+    scale = wl.d_out_full / max(d_out, 1)  # this rank's rows stand for the whole matrices
     if wl.name == "monosoup":
         # the oracle's full SVD on the leading n x n block of each checkpoint,
         # n doubled while the budget allows, scaled to the full size by the
@@ -490,6 +608,7 @@ def oracle_time(wl: Workload, budget_s: float = 12.0, threads: int = 0):
         return (step_bytes / t_full / 1e9, cores,
                 f"oracle merge of {len(wl.wf)} checkpoints on the leading {n}x{n} block ({t_last:.2f} s, numpy "
                 f"SVD threads), scaled by n^3 to {d_out}x{d_in} ({t_full:.1f} s)")
+    compress_in_step = wl.name in ("decode", "tiny")
     if d_out * d_in <= (1 << 20):  # small: whole steps
         n, t_used = 0, 0.0
         while t_used < budget_s or n == 0:
@@ -499,11 +618,11 @@ def oracle_time(wl: Workload, budget_s: float = 12.0, threads: int = 0):
                 oracle.linear(x, wl.wb, s, a, wl.per_row)
             t_used += time.perf_counter() - t0
             n += 1
-        return step_bytes * n / t_used / 1e9, cores, f"{n} whole steps ({t_used:.2f} s on {cores} threads)"
+        return step_bytes * n / (t_used * scale) / 1e9, cores, f"{n} whole steps ({t_used:.2f} s on {cores} threads)"
     rows_done, t_used, chunk = 0, 0.0, 16
     while (t_used < budget_s or rows_done == 0) and rows_done < d_out:
         r = np.arange(rows_done, min(d_out, rows_done + chunk), dtype=np.int64)
-        t0 = time.perf_counter()
+        t_prep = time.perf_counter()
         sfs, afs = [], []
         for wf in wl.wf:
             s, a = oracle.compress_rows(wl.wb, wf, r)
@@ -512,6 +631,7 @@ def oracle_time(wl: Workload, budget_s: float = 12.0, threads: int = 0):
             sf[r], af[r] = s, a
             sfs.append(sf)
             afs.append(af)
+        t0 = time.perf_counter()
         if wl.name == "materialize":
             oracle.materialize(wl.wb[r], sfs[0][r], afs[0][r], True)
         elif wl.vid is None:
@@ -519,35 +639,65 @@ def oracle_time(wl: Workload, budget_s: float = 12.0, threads: int = 0):
                 oracle.linear(x, wl.wb, sfs[0], afs[0], True, rows=r)
         else:
             oracle.linear_multi(wl.xs[0], wl.vid, sfs, afs, True, wl.wb, rows=r)
-        t_used += time.perf_counter() - t0
+        t_end = time.perf_counter()
+        t_used += t_end - (t_prep if compress_in_step else t0)
         rows_done += len(r)
         chunk = min(chunk * 2, 4096)
-    gbs = step_bytes * rows_done / d_out / t_used / 1e9
-    sample = f"{rows_done} of {d_out} rows of one step ({t_used:.2f} s on {cores} threads)"
+    gbs = step_bytes * rows_done / (d_out * scale) / t_used / 1e9
+    what = "compression and linears" if compress_in_step else "linears (variants compressed before the clock)"
+    sample = f"{rows_done} of {d_out} rows of one step, {what} ({t_used:.2f} s on {cores} threads)"
     return gbs, cores, sample
 
 
-def _step_bytes_rows(wl: Workload):
-    """(label, kernel, bytes) of one step, computable without a GPU."""
-    out = []
-    if wl.vid is not None:
-        active = sorted(set(int(v) for v in wl.vid if v >= 0))
-        T = wl.tokens[0]
-        out.append(("linear_multi", "", 2 * wl.d_out * wl.d_in + len(active) * (wl.d_out * wl.d_in // 8 + 4 * wl.n_alpha)
-                    + 2 * T * wl.d_in + 2 * T * wl.d_out + 4 * T))
-        return out
-    if wl.name == "materialize":
-        return [("materialize", "", materialize_bytes(wl.d_out, wl.d_in, wl.n_alpha))]
-    if wl.name == "monosoup":
-        return [("monosoup", "", monosoup_bytes(wl.d_out, len(wl.wf), MONOSOUP["q"]))]
-    if wl.name != "prefill":
-        out.append(("compress", "", compress_bytes(wl.d_out, wl.d_in, wl.n_alpha)))
-    for T in wl.tokens:
-        out.append((f"linear_T{T}", "", linear_bytes(T, wl.d_out, wl.d_in, wl.n_alpha)))
-    return out
+def _oracle_time_slice(wl: Workload, samples, cores: int, step_bytes: int):
+    """The slice step on the CPU: for every one of the 56 linears, the oracle
+    multi-variant linear of the 32 tokens over a seeded sample of its rows
+    (W_base and each variant's W_ft rows drawn by the same generators as the
+    GPU's inputs, compressed by the oracle before the clock starts); the time
+    of each linear is scaled by its rows / sampled rows."""
+    import oracle
+
+    if not samples:
+        raise RuntimeError("the slice CPU baseline needs the sampled rows")
+    t_full, t_used, n_rows = 0.0, 0.0, 0
+    vid = wl.vid
+    for smp in samples:
+        loc = np.arange(len(smp["rows"]), dtype=np.int64)
+        refs = [oracle.compress_rows(smp["wb"], wf, loc) for wf in smp["wf"]]
+        t0 = time.perf_counter()
+        oracle.linear_multi(smp["x"], vid, [r[0] for r in refs], [r[1] for r in refs], True, smp["wb"])
+        dt = time.perf_counter() - t0
+        t_used += dt
+        n_rows += len(loc)
+        t_full += dt * smp["d_out"] / len(loc)
+    total_rows = sum(s["d_out"] for s in samples)
+    t_full *= wl.world  # this rank's rows stand for the whole matrices
+    return (step_bytes / t_full / 1e9, cores,
+            f"{n_rows} of {total_rows} rows (a seeded sample of every one of the {len(samples)} linears; "
+            f"{t_used:.2f} s on {cores} threads), scaled per linear to a full step ({t_full:.1f} s)")
 
 
-# ----------------------------------------------------------------------------- arms
+def cpu_baseline(wl: Workload, unit: str, budget_s: float = 10.0, slice_samples=None) -> dict:
+    """The oracle on all host cores and on one core, in the line's unit."""
+    out = {}
+    for key, thr in (("all", 0), ("one", 1)):
+        gbs, cores, sample = oracle_time(wl, budget_s=budget_s if thr == 0 else budget_s / 2, threads=thr,
+                                         slice_samples=slice_samples)
+        value = gbs
+        if unit == "TFLOP/s":
+            value = wl.step_flops_full() / (wl.step_bytes_full() / (gbs * 1e9)) / 1e12
+        elif unit == "tokens/s":
+            value = sum(wl.tokens) / (wl.step_bytes_full() / (gbs * 1e9))
+        out[key] = {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+    import oracle
+
+    oracle.set_threads(_cpu_cores())
+    line = dict(out["all"])
+    line["single_thread"] = {k: out["one"][k] for k in ("value", "cores", "sample")}
+    return line
+
+
+# ----------------------------------------------------------------------------- distributed
 
 def dist_setup():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -556,40 +706,268 @@ def dist_setup():
     return world, rank, local
 
 
-def _step_flops(wl: Workload) -> int:
-    """Useful FLOPs of one step of a tensor- or ALU-bound workload: 2 T d_out
-    d_in per linear call; the MonoSoup merge's fp32 products."""
-    if wl.name == "monosoup":
-        return monosoup_flops(wl.d_out, len(wl.wf), MONOSOUP["rank"], MONOSOUP["l"], MONOSOUP["q"])
-    return sum(2 * T * wl.d_out * wl.d_in for T in wl.tokens)
+def _backend() -> str:
+    import torch.distributed as dist
 
+    return dist.get_backend() if dist.is_initialized() else "none"
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """Relaunches this script under torch.distributed.run with n ranks on
+    this node (127.0.0.1 rendezvous) and returns its exit code."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(_free_port()), os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd, cwd=ROOT).returncode
+
+
+def gather_rows(y_local, d_out: int, world: int, rank: int, group=None):
+    """All-gather of a row-partitioned output: y_local [T][rows of `rank`]
+    -> y [T][d_out] on every rank (shards padded to the largest row count,
+    so that every rank sends one equal-sized buffer)."""
+    import torch
+    import torch.distributed as dist
+
+    spans = [row_span(d_out, world, r) for r in range(world)]
+    width = max(b - a for a, b in spans)
+    T = y_local.shape[0]
+    send = torch.zeros((width, T), dtype=y_local.dtype, device=y_local.device)
+    send[:y_local.shape[1]] = y_local.t()
+    recv = [torch.empty_like(send) for _ in range(world)]
+    dist.all_gather(recv, send, group=group)
+    return torch.cat([recv[r][:b - a] for r, (a, b) in enumerate(spans)], dim=0).t().contiguous()
+
+
+def _max_over_ranks(v: float, dev, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([v], dtype=torch.float64, device=dev if _backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- timing
+
+def time_steps(run, calls, steps: int, warmup: int, world: int, dev, local: int):
+    """W warm-up steps, then exactly `steps` timed steps bracketed by a barrier
+    and a device synchronize on both sides, CUDA events around every call on
+    the launching stream, clocks sampled during the region.  Returns
+    (ms per step of this rank, per-call event times [steps][calls] in ms,
+    clock summary)."""
+    import torch
+
+    stream = torch.cuda.current_stream()
+
+    def one_step(evs=None):
+        if run.flush is not None:
+            run.flush.fill_(1)
+        for i, c in enumerate(calls):
+            if evs is not None:
+                evs[i][0].record(stream)
+            c[4]()
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(max(warmup, 3)):
+        one_step()
+    if run.bd.bd_check_async(run.ws) != run.bd.BD_OK:
+        raise RuntimeError("asynchronous error during warm-up")
+    torch.cuda.synchronize()
+    events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in calls]
+              for _ in range(steps)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(_smi_id(local))
+    t_start.record(stream)
+    for k in range(steps):
+        one_step(events[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    if run.bd.bd_check_async(run.ws) != run.bd.BD_OK:
+        raise RuntimeError("asynchronous error during the timed region")
+    ev_ms = [[events[k][i][0].elapsed_time(events[k][i][1]) for i in range(len(calls))] for k in range(steps)]
+    elapsed = t_start.elapsed_time(t_end)
+    if run.flush is not None:  # the L2 flush is not part of the path: count kernel time only
+        elapsed = sum(sum(r) for r in ev_ms)
+    return elapsed / steps, ev_ms, clk
+
+
+def roofline_of(wl: Workload, calls, ev_ms, hbm_peak, bf16_peak, peak_src):
+    """Roofline of the dominant kernel (largest share of the events' time):
+    achieved = algorithmic bytes (or FLOPs) per launch / its average
+    CUDA-event duration; plus the per-kernel table."""
+    per_kernel = {}
+    for i, (label, kname, nbytes, flops, _) in enumerate(calls):
+        ms = [row[i] for row in ev_ms]
+        e = per_kernel.setdefault(kname, {"launches": 0, "total_ms": 0.0, "bytes": 0, "flops": 0, "labels": []})
+        e["launches"] += len(ms)
+        e["total_ms"] += sum(ms)
+        e["bytes"] += nbytes * len(ms)
+        e["flops"] += flops * len(ms)
+        e["labels"].append(label)
+    dom = max(per_kernel, key=lambda k: per_kernel[k]["total_ms"])
+    d = per_kernel[dom]
+    avg_ms = d["total_ms"] / d["launches"]
+    bytes_per_launch = d["bytes"] / d["launches"]
+    flops_per_launch = d["flops"] / d["launches"]
+    achieved = bytes_per_launch / (avg_ms * 1e-3) / 1e9
+    traffic = None
+    tr = NCU_TRAFFIC.get((dom, wl.name))
+    if tr is not None and tr[0] == _src_sha(tr[1]) and wl.world == 1:
+        traffic = tr[2] * bytes_per_launch if isinstance(tr[2], float) else tr[2]
+    if wl.name in TENSOR_WORKLOADS:
+        tf = flops_per_launch / (avg_ms * 1e-3) / 1e12
+        roof = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
+                "frac": tf / bf16_peak, "traffic": traffic, "peak_source": f"{peak_src} (bf16_tflops, burst)",
+                "flops_per_launch": flops_per_launch, "avg_launch_us": avg_ms * 1e3}
+    elif wl.name in ALU_WORKLOADS:
+        tf = flops_per_launch / (avg_ms * 1e-3) / 1e12
+        roof = {"bound": "alu", "kernel": dom, "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
+                "frac": tf / FP32_PEAK_TFLOPS, "traffic": traffic,
+                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (fp32 FMA)",
+                "flops_per_launch": flops_per_launch, "avg_launch_us": avg_ms * 1e3,
+                "hbm_achieved_gbs": achieved, "hbm_frac": achieved / hbm_peak}
+    else:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)",
+                "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_ms * 1e3}
+    tot = sum(x["total_ms"] for x in per_kernel.values())
+    kernels = {k: {"launches": v["launches"], "avg_us": v["total_ms"] / v["launches"] * 1e3,
+                   "share": v["total_ms"] / tot, "GBps": v["bytes"] / (v["total_ms"] * 1e-3) / 1e9,
+                   "frac_hbm": v["bytes"] / (v["total_ms"] * 1e-3) / 1e9 / hbm_peak,
+                   "calls": v["labels"] if len(v["labels"]) <= 4 else f"{len(v['labels'])} calls"}
+               for k, v in per_kernel.items()}
+    return roof, kernels
+
+
+def _unit_of(name: str) -> str:
+    return "TFLOP/s" if name in TENSOR_WORKLOADS or name in ALU_WORKLOADS else "GB/s"
+
+
+def _value(wl: Workload, ms_per_step: float) -> float:
+    """Whole-job figure of one step that took ms_per_step (all ranks' rows)."""
+    if _unit_of(wl.name) == "TFLOP/s":
+        return wl.step_flops_full() / (ms_per_step * 1e-3) / 1e12
+    return wl.step_bytes_full() / (ms_per_step * 1e-3) / 1e9
+
+
+def make_run(wl: Workload, dev, sample_rows: int = 0):
+    if wl.name == "slice":
+        return SliceRun(wl, dev, wl.seed, sample_rows=sample_rows)
+    return GpuRun(wl, dev)
+
+
+def measure(name, args, steps, warmup, world, rank, local, dev, peaks, want_cpu):
+    """One workload in its own timed region: the line fields for it."""
+    import torch
+
+    hbm_peak, bf16_peak, peak_src = peaks
+    wl = Workload(name, args.seed, world, rank)
+    run = make_run(wl, dev, sample_rows=128 if (want_cpu and rank == 0) else 0)
+    calls = run.calls()
+    ms_local, ev_ms, clk = time_steps(run, calls, steps, warmup, world, dev, local)
+    ms = _max_over_ranks(ms_local, dev, world)
+    roof, kernels = roofline_of(wl, calls, ev_ms, hbm_peak, bf16_peak, peak_src)
+    unit = _unit_of(name)
+    out = {"workload": wl.config()["workload"], "config": wl.config(), "value": _value(wl, ms), "unit": unit,
+           "ms_per_step": ms, "steps": steps, "warmup": warmup,
+           "tokens_per_s": sum(wl.tokens) / (ms * 1e-3) if wl.tokens else None,
+           "roofline": roof, "kernels": kernels, "clocks": clk,
+           "gpu_launches": LAUNCHES_PER_CALL.get(name, 1) * len(calls) * steps + (steps if not wl.per_row else 0)}
+    if name == "tiny":
+        out["roofline"] = None  # 139 KB stay in L2: latency only
+        out["latency_us"] = ms * 1e3
+        out["kernels"] = kernels
+    out["cpu_baseline"] = None
+    if want_cpu and rank == 0:
+        out["cpu_baseline"] = cpu_baseline(wl, unit, slice_samples=getattr(run, "samples", None))
+    del run
+    torch.cuda.empty_cache()
+    return out
+
+
+def measure_exchange(run, wl: Workload, dev, world: int, reps: int = 20):
+    """The all-gather of every linear's y that a following layer would need
+    (row-partitioned outputs to full rows on every rank), timed on its own."""
+    import torch
+
+    if world == 1 or not getattr(run, "ys", None):
+        return None
+    full = [wl.d_out_full] * len(run.ys) if wl.name != "slice" else [None] * len(run.ys)
+    if wl.name == "slice":
+        full = [d for _ in range(8) for _, d, _ in _slice_linears()]
+
+    def step():
+        for y, d_out in zip(run.ys, full):
+            gather_rows(y, d_out, world, wl.rank)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    _barrier(world)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    ms = _max_over_ranks(a.elapsed_time(b) / reps, dev, world)
+    nbytes = sum(y.shape[0] * d * y.element_size() for y, d in zip(run.ys, full))
+    return {"collective": "all_gather of y per linear (NCCL)", "ms_per_step": ms, "bytes_per_step": nbytes,
+            "GBps": nbytes / (ms * 1e-3) / 1e9}
+
+
+# ----------------------------------------------------------------------------- arms
 
 def run_reference(args):
     world, rank, _ = dist_setup()
     if rank != 0:
         return 0
-    wl = Workload(args.workload, args.seed)
-    step_bytes = sum(c[2] for c in _step_bytes_rows(wl))
+    wl = Workload(args.workload, args.seed, world, 0)
+    unit = _unit_of(wl.name)
+    slice_samples = None
+    if wl.name == "slice":
+        import torch
+
+        if not torch.cuda.is_available():
+            print(json.dumps({"impl": "reference", "unavailable": "the slice inputs are drawn by torch's CUDA "
+                              "generator; no GPU here to draw them"}), flush=True)
+            return 0
+        slice_samples = SliceRun(wl, torch.device("cuda", 0), args.seed, sample_rows=128).samples
     # each step is a bounded sample so that the whole run stays near 90 s of oracle time
     budget = max(0.01, min(12.0, 90.0 / max(args.steps + args.warmup, 1)))
     for _ in range(args.warmup):
-        oracle_time(wl, budget_s=budget / 4)
+        oracle_time(wl, budget_s=budget / 4, slice_samples=slice_samples)
     vals = []
     cores, sample = 0, ""
     for _ in range(args.steps):
-        gbs, cores, sample = oracle_time(wl, budget_s=budget)
+        gbs, cores, sample = oracle_time(wl, budget_s=budget, slice_samples=slice_samples)
         vals.append(gbs)
-    value = statistics.median(vals)
-    ms_per_step = step_bytes / (value * 1e9) * 1e3
-    unit = "GB/s"
-    if wl.name in TENSOR_WORKLOADS or wl.name in ALU_WORKLOADS:  # the same unit as the GPU arm's line
-        value = _step_flops(wl) / (ms_per_step * 1e-3) / 1e12
-        unit = "TFLOP/s"
+    gbs = statistics.median(vals)
+    ms_per_step = wl.step_bytes_full() / (gbs * 1e9) * 1e3
+    value = _value(wl, ms_per_step)
     line = {"metric": METRIC, "value": value, "unit": unit, "impl": "reference", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic (seeded numpy; shapes and distributions of the BitDelta serving setup)",
-            "config": wl.config(),
+            "higher_is_better": True, "scaling": "strong" if world > 1 else "weak", "vs_baseline": None,
+            "dtype": "f64", "data": DATA, "config": wl.config(),
             "cpu_baseline": {"value": value, "unit": unit, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -607,196 +985,73 @@ def run_gpu(args):
     dev = torch.device("cuda", local)
     import __graft_entry__
 
-    if rank == 0 or world == 1:
+    if rank == 0:
         __graft_entry__.build()
-    if world > 1:
-        dist.barrier()
+    _barrier(world)
     __graft_entry__.build()  # no-op once built; loads the library on every rank
-    from bit_weight_delta_bd_gb300 import bitdelta as bd
+    peaks = load_peaks()
+    hbm_peak, bf16_peak, peak_src = peaks
 
-    wl = Workload(args.workload, args.seed + rank)
-    run = SliceRun(wl, dev, args.seed + rank) if wl.name == "slice" else GpuRun(wl, dev)
+    wl = Workload(args.workload, args.seed, world, rank)
+    run = make_run(wl, dev, sample_rows=128 if (rank == 0 and not args.no_cpu) else 0)
     calls = run.calls()
-    stream = torch.cuda.current_stream()
+    ms_local, ev_ms, clk = time_steps(run, calls, args.steps, args.warmup, world, dev, local)
+    ms_per_step = _max_over_ranks(ms_local, dev, world)
+    roofline, kernels = roofline_of(wl, calls, ev_ms, hbm_peak, bf16_peak, peak_src)
+    unit = _unit_of(wl.name)
+    value = _value(wl, ms_per_step)
+    step_bytes = wl.step_bytes_full()
 
-    def one_step(evs=None):
-        if run.flush is not None:
-            run.flush.fill_(1)
-        for i, (_, _, _, _, fn) in enumerate(calls):
-            if evs is not None:
-                evs[i][0].record(stream)
-            fn()
-            if evs is not None:
-                evs[i][1].record(stream)
-
-    for _ in range(max(args.warmup, 3)):
-        one_step()
-    if bd.bd_check_async(run.ws) != bd.BD_OK:
-        raise RuntimeError("asynchronous error during warm-up")
-    torch.cuda.synchronize()
-
-    events = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in calls]
-              for _ in range(args.steps)]
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(_smi_id(local))
-    t_start.record(stream)
-    for k in range(args.steps):
-        one_step(events[k])
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    clk = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if run.flush is not None:  # the L2 flush is not part of the path: count kernel time only
-        elapsed_ms = sum(events[k][i][0].elapsed_time(events[k][i][1]) for k in range(args.steps)
-                         for i in range(len(calls)))
-    if bd.bd_check_async(run.ws) != bd.BD_OK:
-        raise RuntimeError("asynchronous error during the timed region")
-    if world > 1:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-
-    step_bytes = sum(c[2] for c in calls)
-    ms_per_step = elapsed_ms / args.steps
-    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
-    tokens = sum(wl.tokens)
-    hbm_peak, bf16_peak, peak_src = load_peaks()
-
-    # per-kernel averages from the events
-    per_kernel = {}
-    for i, (label, kname, nbytes, flops, _) in enumerate(calls):
-        ms = [events[k][i][0].elapsed_time(events[k][i][1]) for k in range(args.steps)]
-        e = per_kernel.setdefault(kname, {"launches": 0, "total_ms": 0.0, "bytes": 0, "labels": []})
-        e["launches"] += len(ms)
-        e["total_ms"] += sum(ms)
-        e["bytes"] += nbytes * len(ms)
-        e["labels"].append(label)
-    dom = max(per_kernel, key=lambda k: per_kernel[k]["total_ms"])
-    d = per_kernel[dom]
-    avg_ms = d["total_ms"] / d["launches"]
-    bytes_per_launch = d["bytes"] / d["launches"]
-    achieved = bytes_per_launch / (avg_ms * 1e-3) / 1e9
-    traffic = None
-    tr = NCU_TRAFFIC.get((dom, wl.name))
-    if tr is not None and tr[0] == _src_sha(tr[1]):
-        traffic = tr[2] * bytes_per_launch if isinstance(tr[2], float) else tr[2]
-    if wl.name in TENSOR_WORKLOADS:
-        flops_per_launch = calls[0][3]
-        tf = flops_per_launch / (avg_ms * 1e-3) / 1e12
-        roofline = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
-                    "frac": tf / bf16_peak, "traffic": traffic, "peak_source": f"{peak_src} (bf16_tflops, burst)",
-                    "flops_per_launch": flops_per_launch, "avg_launch_us": avg_ms * 1e3}
-    elif wl.name in ALU_WORKLOADS:
-        flops_per_launch = calls[0][3]
-        tf = flops_per_launch / (avg_ms * 1e-3) / 1e12
-        roofline = {"bound": "alu", "kernel": dom, "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                    "frac": tf / FP32_PEAK_TFLOPS, "traffic": traffic,
-                    "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (fp32 FMA)",
-                    "flops_per_launch": flops_per_launch, "avg_launch_us": avg_ms * 1e3,
-                    "hbm_achieved_gbs": achieved, "hbm_frac": achieved / hbm_peak}
-    else:
-        roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": achieved / hbm_peak, "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)",
-                    "bytes_per_launch": bytes_per_launch, "avg_launch_us": avg_ms * 1e3}
-    kernels = {k: {"launches": v["launches"], "avg_us": v["total_ms"] / v["launches"] * 1e3,
-                   "share": v["total_ms"] / sum(x["total_ms"] for x in per_kernel.values()),
-                   "GBps": v["bytes"] / (v["total_ms"] * 1e-3) / 1e9,
-                   "frac_hbm": v["bytes"] / (v["total_ms"] * 1e-3) / 1e9 / hbm_peak, "calls": v["labels"]}
-               for k, v in per_kernel.items()}
-
-    e2e = None
+    e2e = e2e_serving = None
     if not args.no_e2e:
-        e2e = run_e2e(run, calls, wl, max(3, min(args.steps, 20)), stream)
-        if world > 1:
-            t = torch.tensor([e2e["ms_per_step"]], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e["ms_per_step"] = float(t.item())
-        e2e["value"] = world * step_bytes / (e2e["ms_per_step"] * 1e-3) / 1e9
-        if wl.name in TENSOR_WORKLOADS or wl.name in ALU_WORKLOADS:
-            e2e["value"] = world * calls[0][3] / (e2e["ms_per_step"] * 1e-3) / 1e12
-            e2e["unit"] = "TFLOP/s"
-
-    prefill = None
-    if wl.name == "decode" and not args.no_prefill:
-        prefill = measure_prefill(dev, args.seed + rank, bf16_peak, peak_src)
-        if world > 1:
-            t = torch.tensor([prefill["avg_us"]], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            prefill["avg_us"] = float(t.item())
-            prefill["tflops"] = world * prefill["flops_per_launch"] / (prefill["avg_us"] * 1e-6) / 1e12
-            prefill["frac"] = prefill["tflops"] / world / bf16_peak
-
+        e2e = run_e2e(run, calls, wl, max(3, min(args.steps, 20)), world, dev)
+        if wl.name in ("decode", "tiny"):
+            e2e_serving = run_e2e(run, run.serving_calls(), wl, max(3, min(args.steps, 20)), world, dev,
+                                  serving=True)
+    exchange = measure_exchange(run, wl, dev, world)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu and wl.name != "slice":
-        gbs, cores, sample = oracle_time(wl)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
-        if wl.name in TENSOR_WORKLOADS or wl.name in ALU_WORKLOADS:  # in the line's own unit
-            cpu["value"] = _step_flops(wl) / (step_bytes / (gbs * 1e9)) / 1e12
-            cpu["unit"] = "TFLOP/s"
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(wl, unit, budget_s=12.0, slice_samples=getattr(run, "samples", None))
+    launches = LAUNCHES_PER_CALL.get(wl.name, 1) * len(calls) * args.steps
+    if not wl.per_row:
+        launches += args.steps  # the per-matrix alpha's finalize pass
+    del run, calls
+    torch.cuda.empty_cache()
+
+    subs = {}
+    if wl.name == "decode" and not args.no_sub:
+        want = [s for s in args.sub.split(",") if s] or [s[0] for s in SUBS]
+        for name, steps, warmup in SUBS:
+            if name in want:
+                subs[name] = measure(name, args, steps, warmup, world, rank, local, dev, peaks,
+                                     want_cpu=not args.no_cpu)
 
     if rank == 0:
-        unit = "GB/s"
-        if wl.name in TENSOR_WORKLOADS or wl.name in ALU_WORKLOADS:  # this workload's own figure is FLOP/s
-            value = world * calls[0][3] / (ms_per_step * 1e-3) / 1e12
-            unit = "TFLOP/s"
         line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": "f32" if wl.name in ALU_WORKLOADS else "bf16", "accumulate": "f32",
-                "data": "synthetic (seeded numpy; shapes and distributions of the BitDelta serving setup)",
-                "config": {**wl.config(), "parallelism": f"replicas x{world} (no exchange step)"},
-                "tokens_per_s": world * tokens / (ms_per_step * 1e-3),
-                "frac_hbm_step": value / world / hbm_peak,
-                "roofline": roofline, "kernels": kernels, "prefill": prefill, "cpu_baseline": cpu, "e2e": e2e,
-                "clocks": clk, "gpu_launches": LAUNCHES_PER_CALL.get(wl.name, 1) * len(calls) * args.steps}
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "strong" if world > 1 else "weak", "vs_baseline": None,
+                "dtype": "f32" if wl.name in ALU_WORKLOADS else "bf16", "accumulate": "f32", "data": DATA,
+                "config": wl.config(),
+                "tokens_per_s": sum(wl.tokens) / (ms_per_step * 1e-3) if wl.tokens else None,
+                "frac_hbm_step": step_bytes / (ms_per_step * 1e-3) / 1e9 / world / hbm_peak,
+                "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+                "e2e_serving": e2e_serving, "exchange": exchange, "clocks": clk, "gpu_launches": launches}
+        line.update(subs)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()
     return 0
 
 
-def measure_prefill(dev, seed, bf16_peak, peak_src, reps=20):
-    """Tensor-core prefill on its own: 4096 tokens x W_base [8192 x 8192], one
-    variant; median of `reps` CUDA-event-timed calls."""
-    import torch
-
-    wl = Workload("prefill", seed)
-    run = GpuRun(wl, dev)
-    fn = run.calls()[0][4]
-    for _ in range(3):
-        fn()
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
-    stream = torch.cuda.current_stream()
-    for a, b in ev:
-        a.record(stream)
-        fn()
-        b.record(stream)
-    torch.cuda.synchronize()
-    if run.bd.bd_check_async(run.ws) != run.bd.BD_OK:
-        raise RuntimeError("asynchronous error in the prefill measurement")
-    us = statistics.median(a.elapsed_time(b) for a, b in ev) * 1e3
-    flops = 2 * 4096 * 8192 * 8192
-    tf = flops / (us * 1e-6) / 1e12
-    return {"workload": "prefill_4096x8192x8192", "kernel": "prefill_kernel", "bound": "tensor", "avg_us": us,
-            "flops_per_launch": flops, "tflops": tf, "peak": bf16_peak, "frac": tf / bf16_peak,
-            "peak_source": f"{peak_src} (bf16_tflops, burst)", "reps": reps}
-
-
-def run_e2e(run: GpuRun, calls, wl: Workload, steps: int, stream):
-    """The same step through the public API with pinned host buffers: inputs
-    are copied host -> device and results device -> host inside the timing."""
+def run_e2e(run, calls, wl: Workload, steps: int, world: int, dev, serving: bool = False):
+    """The same step through the public API with pinned host buffers: this
+    step's inputs are copied host -> device and its results device -> host
+    inside the timing.  serving=True: the steady-state serving step, in which
+    W_base, the signs and alpha stay resident and only x and y cross."""
     torch = run.torch
     pin = lambda t: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)  # noqa: E731
-    if wl.name in ("multi", "multi_prefill"):
-        h_in = [(pin(run.xs[0]), run.xs[0]), (pin(run.vid), run.vid)]
-        h_out = [(pin(run.ys[0]), run.ys[0])]
-    elif wl.name == "slice":
-        h_in = [(pin(x), x) for x in run.xs] + [(pin(run.vid), run.vid)]
+    if serving or wl.name in ("multi", "multi_prefill", "prefill", "slice"):
+        h_in = [(pin(x), x) for x in run.xs] + ([(pin(run.vid), run.vid)] if run.vid is not None else [])
         h_out = [(pin(y), y) for y in run.ys]
     elif wl.name == "materialize":
         h_in = [(pin(run.wb), run.wb), (pin(run.signs[0]), run.signs[0]), (pin(run.alpha[0]), run.alpha[0])]
@@ -804,9 +1059,6 @@ def run_e2e(run: GpuRun, calls, wl: Workload, steps: int, stream):
     elif wl.name == "monosoup":
         h_in = [(pin(run.wb), run.wb)] + [(pin(w), w) for w in run.wf] + [(pin(run.omega), run.omega)]
         h_out = [(pin(run.w_merged), run.w_merged)]
-    elif wl.name == "prefill":
-        h_in = [(pin(run.xs[0]), run.xs[0])]
-        h_out = [(pin(run.ys[0]), run.ys[0])]
     else:
         h_in = [(pin(run.wb), run.wb), (pin(run.wf[0]), run.wf[0])] + [(pin(x), x) for x in run.xs]
         h_out = [(pin(run.signs[0]), run.signs[0]), (pin(run.alpha[0]), run.alpha[0])] + \
@@ -827,19 +1079,44 @@ def run_e2e(run: GpuRun, calls, wl: Workload, steps: int, stream):
     for _ in range(2):
         step()
     torch.cuda.synchronize()
+    _barrier(world)
+    stream = torch.cuda.current_stream()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(steps):
         step()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b) / steps
-    return {"value": None, "unit": "GB/s", "ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "steps": steps, "path": "pinned host -> device copies, bd_* calls, device -> host copies"}
+    ms = _max_over_ranks(a.elapsed_time(b) / steps, dev, world)
+    if serving:
+        nbytes = world * sum(c[2] for c in calls)
+        if world > 1:
+            nbytes = sum(linear_bytes(T, wl.d_out_full, wl.d_in, wl.d_out_full if wl.per_row else 1)
+                         for T in wl.tokens)
+        unit, value = "GB/s", nbytes / (ms * 1e-3) / 1e9
+        path = ("pinned host -> device copies of x, bd_linear calls on resident W_base / signs / alpha, "
+                "device -> host copies of y")
+    else:
+        unit = _unit_of(wl.name)
+        value = _value(wl, ms)
+        path = "pinned host -> device copies, bd_* calls, device -> host copies"
+    out = {"value": value, "unit": unit, "ms_per_step": ms, "h2d_bytes_per_step": h2d * world,
+           "d2h_bytes_per_step": d2h * world, "steps": steps, "path": path}
+    if serving:
+        out["tokens_per_s"] = sum(wl.tokens) / (ms * 1e-3)
+    return out
 
 
-def main():
-    args = parse_args()
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else argv
+    args = parse_args(argv)
+    if args.gpus < 1:
+        raise SystemExit("--gpus must be >= 1")
+    if "WORLD_SIZE" not in os.environ and args.gpus > 1:
+        return spawn_ranks(args.gpus, argv)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but the launcher started {world} ranks (WORLD_SIZE)")
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -167,3 +167,37 @@ def test_row_bounds_partition():
             assert max(sizes) - min(sizes) <= 1
     with pytest.raises(ValueError):
         shard.row_bounds(10, 2, 2)
+
+
+def _gather_rank(rank, world, port, q, d_out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        import bench
+
+        T = 3
+        y_full = torch.arange(T * d_out, dtype=torch.float32).reshape(T, d_out)
+        r0, r1 = bench.row_span(d_out, world, rank)
+        y = bench.gather_rows(y_full[:, r0:r1].contiguous(), d_out, world, rank)
+        q.put((rank, bool(torch.equal(y, y_full))))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.timeout(300)
+@pytest.mark.parametrize("world,d_out", [(2, 8), (3, 7), (3, 2)])
+def test_benchmark_row_gather_reassembles_y(world, d_out):
+    """The benchmark's exchange step under the output-row partition: each
+    rank's y columns, gathered (shards padded to equal size), give the full y
+    on every rank, also for ragged and empty shards."""
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_gather_rank, args=(r, world, port, q, d_out)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=240) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [True] * world
