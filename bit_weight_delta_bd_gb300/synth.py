@@ -163,6 +163,27 @@ def monosoup_checkpoints(seed: int, d_out: int, d_in: int, k: int, rank_signal: 
     return wb, out
 
 
+def monosoup_noisy_checkpoints(seed: int, d_out: int, d_in: int, k: int, rank_signal: int, b: float = 1e-3,
+                               sigma_hi: float = 4.0, sigma_lo: float = 1.0):
+    """MonoSoup inputs whose task vectors carry a noise floor of real size:
+    W_i = bf16(W_base + U_i diag(s) V_i^T + L_i), the low-rank part as in
+    ``monosoup_checkpoints`` and L_i ~ Laplace(0, b) elementwise (the delta
+    model of section "Matematiksel temel"), which the post's truncation is
+    meant to remove as noise.  Draw order: W_base, then U_i, V_i, L_i per
+    checkpoint.  Returns (w_base_bits, [w_i_bits])."""
+    rng = np.random.default_rng(seed)
+    wb = base_weight(rng, d_out, d_in)
+    s = np.geomspace(sigma_hi, sigma_lo, rank_signal) if rank_signal > 0 else np.zeros(0)
+    wb64 = bf16_bits_to_f32(wb).astype(np.float64)
+    out = []
+    for _ in range(k):
+        u = rng.standard_normal((d_out, rank_signal)) / np.sqrt(d_out)
+        v = rng.standard_normal((d_in, rank_signal)) / np.sqrt(d_in)
+        noise = rng.laplace(0.0, b, size=(d_out, d_in))
+        out.append(f32_to_bf16_bits((wb64 + (u * s) @ v.T + noise).astype(np.float32)))
+    return wb, out
+
+
 def gaussian_test_matrix(seed: int, d_in: int, l: int) -> np.ndarray:
     """Standard normal fp32 [d_in][l]: the random test matrix a randomized
     range finder draws (here an input, so both sides see the same one)."""
