@@ -8,18 +8,25 @@
 // base and the sign contraction are separate bf16 MMAs (s in {-1,+1} is exact
 // in bf16) that share the x operand, accumulated in fp32.
 //
-// Work split.  A CTA owns a block of 16*kConsumers output rows and one of CK
-// equal slices of d_in; the CK CTAs of a thread-block cluster cover all of
-// d_in and reduce their partial sums through distributed shared memory, in
-// rank order (CK depends on d_in only, never on d_out, so a row's arithmetic
-// does not change when the rows are sharded).  Inside the CTA one producer
-// thread streams 128-column stages into a ring of shared-memory buffers with
-// a handful of 2-D TMA boxes per stage and the consumer warps (16 rows each)
-// run the MMAs:
+// Work split.  A thread-block cluster of CK CTAs covers all of d_in (CTA
+// rank k takes the k-th of CK equal slices; CK depends on d_in only, never on
+// d_out, so a row's arithmetic does not change when the rows are sharded) and
+// is persistent: it takes the blocks of 16*kConsumers output rows numbered
+// c, c + C, c + 2C, ... (C clusters resident), reducing each block's partial
+// sums through distributed shared memory, in rank order.  Inside the CTA one
+// producer thread streams 128-column stages into a ring of shared-memory
+// buffers with a handful of 2-D TMA boxes per stage, one running stage count
+// across the blocks, and the consumer warps (16 rows each) run the MMAs:
 //   - W_base: two boxes [block rows x 64 columns], 128-byte swizzle;
 //   - x: two boxes [8*NT tokens x 64 columns], 128-byte swizzle;
 //   - sign bits: one box [block rows x 4 words];
 //   - full/empty mbarriers between producer and consumers, all waits bounded.
+// Between two row blocks the producer first fills the ring with the next
+// block's stages and then joins the block's cluster barrier, so the stream
+// from device memory does not stop while the consumers reduce and store the
+// finished block.  The reduction buffers are double-buffered by block parity
+// (one cluster barrier per block: a CTA reuses a buffer only after its peers
+// passed the next block's barrier, i.e. after they read it).
 // The swizzle puts 16-byte chunk c of a 128-byte row r at chunk c ^ (r % 8),
 // so the fragment loads below are bank-conflict free.
 //
@@ -48,7 +55,7 @@ constexpr int kMaxStages = 4;
 constexpr int kConsumers = 4;      // 64 rows per CTA, up to three CTAs per SM
 constexpr int kRows = 16 * kConsumers;
 constexpr int kThreads = 32 * (kConsumers + 1);
-constexpr size_t kSmemBudget = 66u * 1024u;  // three CTAs per SM (measured best on GB300)
+constexpr size_t kSmemBudget = 74u * 1024u;  // three CTAs per SM
 
 struct SkinnyParams {
     CUtensorMap sign_map;   // [d_out][d_in/32] uint32, box 4 x 64 rows
@@ -60,6 +67,8 @@ struct SkinnyParams {
     int64_t T, d_out, d_in;
     int per_row, out_f32;
     int CK, stages;
+    int n_blocks;     // row blocks of kRows rows
+    int n_clusters;   // clusters launched (each takes every n_clusters-th block)
 };
 
 struct SkinnyShared {
@@ -121,8 +130,7 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
     const int CK = p.CK;
     cg::cluster_group cluster = cg::this_cluster();
     const int rank = static_cast<int>(cluster.block_rank());
-    const int64_t row0 = static_cast<int64_t>(blockIdx.x / CK) * kRows;
-    const int valid_rows = static_cast<int>(p.d_out - row0 < kRows ? p.d_out - row0 : kRows);
+    const int cl = static_cast<int>(blockIdx.x) / CK;  // cluster index
 
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
@@ -135,154 +143,176 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
     __syncthreads();
 
     // ---------------------------------------------------------------- pipeline
-    // stage layout: [W half 0 | W half 1 | x half 0 | x half 1 | sign tile], 1024-byte aligned
+    // stage layout: [W half 0 | W half 1 | x half 0 | x half 1 | sign tile], 1024-byte aligned;
+    // after the ring: two reduction buffers (base and sign partials, [kRows][Tpad] fp32 each)
     const int stages = p.stages;
     constexpr int kWHalf = kRows * kHalfRowBytes;
     constexpr int kXHalf = Tpad * kHalfRowBytes;
     constexpr int kSignOff = 2 * kWHalf + 2 * kXHalf;
     constexpr int kSignTile = kRows * kSignRowBytes;
     constexpr int kStageBytes = (kSignOff + kSignTile + 1023) & ~1023;
+    constexpr int kRedFloats = 2 * kRows * Tpad;  // one buffer: base then sign partials
+    float* red_all = reinterpret_cast<float*>(dyn + static_cast<size_t>(stages) * kStageBytes);
     const int nc = static_cast<int>(d_in / kChunk);
     const int c_begin = static_cast<int>(static_cast<int64_t>(rank) * nc / CK);
     const int c_end = static_cast<int>(static_cast<int64_t>(rank + 1) * nc / CK);
     const int n_chunks = c_end - c_begin;
+    const int n_mine = cl < p.n_blocks ? (p.n_blocks - 1 - cl) / p.n_clusters + 1 : 0;  // blocks of this cluster
+    const uint32_t tx = static_cast<uint32_t>(2 * kWHalf + 2 * kXHalf + kSignTile);
 
-    float accb[NT][4], accs[NT][4];
-#pragma unroll
-    for (int j = 0; j < NT; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) accb[j][e] = accs[j][e] = 0.0f;
-
-    if (warp == kConsumers) {
-        // ------------------------------------------------------------ producer warp
-        const uint32_t tx = static_cast<uint32_t>(2 * kWHalf + 2 * kXHalf + kSignTile);
-        int issued = 0;
-        for (int i = 0; i < n_chunks; ++i) {
-            const int s = i % stages;
-            if (i >= stages &&
-                !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty[s], static_cast<uint32_t>(i / stages - 1) & 1u,
+    // Producer: stage k (running count over this cluster's blocks) is chunk
+    // k % n_chunks of the block k / n_chunks.  Issues stages up to `target`;
+    // waits only for ring slots whose previous stage precedes `target` - the
+    // stages slots back, which the consumers release without waiting for
+    // anything the producer does later.
+    int pk = 0;
+    auto produce_until = [&](int target) {
+        for (; pk < target; ++pk) {
+            const int s = pk % stages;
+            if (pk >= stages &&
+                !__all_sync(0xffffffffu, wait_or_abort(sh, &sh.empty[s], static_cast<uint32_t>(pk / stages - 1) & 1u,
                                                        p.err)))
-                break;
+                return false;
             uint8_t* st = dyn + static_cast<size_t>(s) * kStageBytes;
-            const int col = (c_begin + i) * kChunk;
+            const int col = (c_begin + pk % n_chunks) * kChunk;
+            const int rb = (cl + (pk / n_chunks) * p.n_clusters) * kRows;
             if (lane == 0) {
                 mbar_arrive_expect_tx(&sh.full[s], tx);
-                tma_load_2d(st, &p.w_map, col, static_cast<int>(row0), &sh.full[s]);
-                tma_load_2d(st + kWHalf, &p.w_map, col + 64, static_cast<int>(row0), &sh.full[s]);
+                tma_load_2d(st, &p.w_map, col, rb, &sh.full[s]);
+                tma_load_2d(st + kWHalf, &p.w_map, col + 64, rb, &sh.full[s]);
                 tma_load_2d(st + 2 * kWHalf, &p.x_map, col, 0, &sh.full[s]);
                 tma_load_2d(st + 2 * kWHalf + kXHalf, &p.x_map, col + 64, 0, &sh.full[s]);
-                tma_load_2d(st + kSignOff, &p.sign_map, col / 32, static_cast<int>(row0), &sh.full[s]);
+                tma_load_2d(st + kSignOff, &p.sign_map, col / 32, rb, &sh.full[s]);
             }
             __syncwarp();
-            ++issued;
         }
-        // every issued stage must have landed before the CTA reuses or frees the memory
-        for (int i = (issued > stages ? issued - stages : 0); i < issued; ++i) {
+        return true;
+    };
+    bool p_ok = true;
+    const int rl0 = 16 * warp + g;  // consumer rows rl0 and rl0 + 8 (both = g mod 8)
+    const int c0 = ((2 * q) ^ g) << 4, c1 = ((2 * q + 1) ^ g) << 4;  // swizzled chunk offsets
+
+    for (int u = 0; u < n_mine; ++u) {
+        const int64_t row0 = static_cast<int64_t>(cl + u * p.n_clusters) * kRows;
+        const int valid_rows = static_cast<int>(p.d_out - row0 < kRows ? p.d_out - row0 : kRows);
+        float* red_b = red_all + (u & 1) * kRedFloats;
+        float* red_s = red_b + kRows * Tpad;
+        if (warp == kConsumers) {
+            // ------------------------------------------------------------ producer warp
+            // the rest of this block, then the first `stages` stages of the next one (their slots
+            // held this block's last stages), before the block's cluster barrier
+            int target = (u + 1) * n_chunks;
+            if (u + 1 < n_mine) target += n_chunks < stages ? n_chunks : stages;
+            if (p_ok && !sh.abort) p_ok = produce_until(target);
+        } else {
+            // ------------------------------------------------------------ consumer warps
+            float accb[NT][4], accs[NT][4];
+#pragma unroll
+            for (int j = 0; j < NT; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) accb[j][e] = accs[j][e] = 0.0f;
+            for (int i = 0; i < n_chunks; ++i) {
+                const int kst = u * n_chunks + i;
+                const int s = kst % stages;
+                if (!__all_sync(0xffffffffu, wait_or_abort(sh, &sh.full[s], static_cast<uint32_t>(kst / stages) & 1u,
+                                                           p.err)))
+                    break;
+                const uint8_t* st = dyn + static_cast<size_t>(s) * kStageBytes;
+                const uint32_t* sgn = reinterpret_cast<const uint32_t*>(st + kSignOff);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint8_t* wst = st + h * kWHalf;
+                    const uint8_t* xst = st + 2 * kWHalf + h * kXHalf;
+                    uint32_t W0[8], W1[8];
+                    {
+                        const uint8_t* r0p = wst + rl0 * kHalfRowBytes;
+                        const uint8_t* r1p = wst + (rl0 + 8) * kHalfRowBytes;
+                        const uint4 u0 = *reinterpret_cast<const uint4*>(r0p + c0);
+                        const uint4 u1 = *reinterpret_cast<const uint4*>(r0p + c1);
+                        const uint4 v0 = *reinterpret_cast<const uint4*>(r1p + c0);
+                        const uint4 v1 = *reinterpret_cast<const uint4*>(r1p + c1);
+                        W0[0] = u0.x; W0[1] = u0.y; W0[2] = u0.z; W0[3] = u0.w;
+                        W0[4] = u1.x; W0[5] = u1.y; W0[6] = u1.z; W0[7] = u1.w;
+                        W1[0] = v0.x; W1[1] = v0.y; W1[2] = v0.z; W1[3] = v0.w;
+                        W1[4] = v1.x; W1[5] = v1.y; W1[6] = v1.z; W1[7] = v1.w;
+                    }
+                    const int sign_word = 2 * h + (q >> 1);
+                    const uint32_t sign_shift = 16u * (q & 1);
+                    uint32_t S0[8], S1[8];
+                    expand_signs((sgn[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
+                    expand_signs((sgn[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
+#pragma unroll
+                    for (int j = 0; j < NT; ++j) {
+                        const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
+                        const uint4 xa = *reinterpret_cast<const uint4*>(xr + c0);
+                        const uint4 xb = *reinterpret_cast<const uint4*>(xr + c1);
+                        mma4(accb[j], W0, W1, xa, xb);
+                        mma4(accs[j], S0, S1, xa, xb);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.empty[s]);
+            }
+            // this block's partial sums into this CTA's reduction buffer of the block's parity
+#pragma unroll
+            for (int j = 0; j < NT; ++j) {
+                const int pos = 8 * j + 2 * q;
+                red_b[rl0 * Tpad + pos] = accb[j][0];
+                red_b[rl0 * Tpad + pos + 1] = accb[j][1];
+                red_b[(rl0 + 8) * Tpad + pos] = accb[j][2];
+                red_b[(rl0 + 8) * Tpad + pos + 1] = accb[j][3];
+                red_s[rl0 * Tpad + pos] = accs[j][0];
+                red_s[rl0 * Tpad + pos + 1] = accs[j][1];
+                red_s[(rl0 + 8) * Tpad + pos] = accs[j][2];
+                red_s[(rl0 + 8) * Tpad + pos + 1] = accs[j][3];
+            }
+        }
+        // ---------------------------------------------------------------- cluster K reduction of block u
+        cluster.sync();
+        if (warp < kConsumers) {
+            const int r_lo = rank * kRows / CK, r_hi = (rank + 1) * kRows / CK;
+            const int nr = r_hi - r_lo;
+            for (int o = tid; o < nr * T; o += 32 * kConsumers) {
+                const int t = o / nr, r = r_lo + o % nr;
+                if (r >= valid_rows) continue;
+                float b = 0.0f, sg = 0.0f;
+                for (int k = 0; k < CK; ++k) {
+                    const float* pb = cluster.map_shared_rank(red_b, k);
+                    const float* ps = cluster.map_shared_rank(red_s, k);
+                    b += pb[r * Tpad + t];
+                    sg += ps[r * Tpad + t];
+                }
+                const int64_t row = row0 + r;
+                const float y = fmaf(p.alpha[p.per_row ? row : 0], sg, b);
+                const int64_t idx = static_cast<int64_t>(t) * p.d_out + row;
+                if (p.out_f32)
+                    static_cast<float*>(p.y)[idx] = y;
+                else
+                    static_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(y);
+            }
+        }
+    }
+    if (warp == kConsumers) {
+        // every issued stage must have landed before the CTA exits
+        for (int i = (pk > stages ? pk - stages : 0); i < pk; ++i) {
             const int s = i % stages;
             const uint32_t par = static_cast<uint32_t>(i / stages) & 1u;
             const uint64_t t0 = global_timer_ns();
             while (!mbar_try_wait(&sh.full[s], par) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
-    } else {
-        // ------------------------------------------------------------ consumer warps
-        const int rl0 = 16 * warp + g;  // local rows rl0 and rl0 + 8 (both = g mod 8)
-        const int c0 = ((2 * q) ^ g) << 4, c1 = ((2 * q + 1) ^ g) << 4;  // swizzled chunk offsets
-        for (int i = 0; i < n_chunks; ++i) {
-            const int s = i % stages;
-            if (!__all_sync(0xffffffffu,
-                            wait_or_abort(sh, &sh.full[s], static_cast<uint32_t>(i / stages) & 1u, p.err)))
-                break;
-            const uint8_t* st = dyn + static_cast<size_t>(s) * kStageBytes;
-            const uint32_t* sgn = reinterpret_cast<const uint32_t*>(st + kSignOff);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint8_t* wst = st + h * kWHalf;
-                const uint8_t* xst = st + 2 * kWHalf + h * kXHalf;
-                uint32_t W0[8], W1[8];
-                {
-                    const uint8_t* r0p = wst + rl0 * kHalfRowBytes;
-                    const uint8_t* r1p = wst + (rl0 + 8) * kHalfRowBytes;
-                    const uint4 u0 = *reinterpret_cast<const uint4*>(r0p + c0);
-                    const uint4 u1 = *reinterpret_cast<const uint4*>(r0p + c1);
-                    const uint4 v0 = *reinterpret_cast<const uint4*>(r1p + c0);
-                    const uint4 v1 = *reinterpret_cast<const uint4*>(r1p + c1);
-                    W0[0] = u0.x; W0[1] = u0.y; W0[2] = u0.z; W0[3] = u0.w;
-                    W0[4] = u1.x; W0[5] = u1.y; W0[6] = u1.z; W0[7] = u1.w;
-                    W1[0] = v0.x; W1[1] = v0.y; W1[2] = v0.z; W1[3] = v0.w;
-                    W1[4] = v1.x; W1[5] = v1.y; W1[6] = v1.z; W1[7] = v1.w;
-                }
-                const int sign_word = 2 * h + (q >> 1);
-                const uint32_t sign_shift = 16u * (q & 1);
-                uint32_t S0[8], S1[8];
-                expand_signs((sgn[rl0 * 4 + sign_word] >> sign_shift) & 0xFFFFu, S0);
-                expand_signs((sgn[(rl0 + 8) * 4 + sign_word] >> sign_shift) & 0xFFFFu, S1);
-#pragma unroll
-                for (int j = 0; j < NT; ++j) {
-                    const uint8_t* xr = xst + (8 * j + g) * kHalfRowBytes;
-                    const uint4 xa = *reinterpret_cast<const uint4*>(xr + c0);
-                    const uint4 xb = *reinterpret_cast<const uint4*>(xr + c1);
-                    mma4(accb[j], W0, W1, xa, xb);
-                    mma4(accs[j], S0, S1, xa, xb);
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sh.empty[s]);
-        }
     }
-
-    // ---------------------------------------------------------------- cluster K reduction
-    __syncthreads();  // pipeline drained: the stage memory becomes the reduction buffer
-    float* red_b = reinterpret_cast<float*>(dyn);
-    float* red_s = red_b + kRows * Tpad;
-    if (warp < kConsumers) {
-        const int r0 = 16 * warp + g;
-#pragma unroll
-        for (int j = 0; j < NT; ++j) {
-            const int pos = 8 * j + 2 * q;
-            red_b[r0 * Tpad + pos] = accb[j][0];
-            red_b[r0 * Tpad + pos + 1] = accb[j][1];
-            red_b[(r0 + 8) * Tpad + pos] = accb[j][2];
-            red_b[(r0 + 8) * Tpad + pos + 1] = accb[j][3];
-            red_s[r0 * Tpad + pos] = accs[j][0];
-            red_s[r0 * Tpad + pos + 1] = accs[j][1];
-            red_s[(r0 + 8) * Tpad + pos] = accs[j][2];
-            red_s[(r0 + 8) * Tpad + pos + 1] = accs[j][3];
-        }
-    }
-    cluster.sync();
-    const int r_lo = rank * kRows / CK, r_hi = (rank + 1) * kRows / CK;
-    const int nr = r_hi - r_lo;
-    for (int o = tid; o < nr * T; o += kThreads) {
-        const int t = o / nr, r = r_lo + o % nr;
-        if (r >= valid_rows) continue;
-        float b = 0.0f, sg = 0.0f;
-        for (int k = 0; k < CK; ++k) {
-            const float* pb = cluster.map_shared_rank(red_b, k);
-            const float* ps = cluster.map_shared_rank(red_s, k);
-            b += pb[r * Tpad + t];
-            sg += ps[r * Tpad + t];
-        }
-        const int64_t row = row0 + r;
-        const float y = fmaf(p.alpha[p.per_row ? row : 0], sg, b);
-        const int64_t idx = static_cast<int64_t>(t) * p.d_out + row;
-        if (p.out_f32)
-            static_cast<float*>(p.y)[idx] = y;
-        else
-            static_cast<__nv_bfloat16*>(p.y)[idx] = __float2bfloat16_rn(y);
-    }
-    cluster.sync();  // peers may still read this CTA's partials until here
+    cluster.sync();  // peers may still read this CTA's last reduction buffer until here
 }
 
 template <int NT>
-cudaError_t launch_nt(const SkinnyParams& prm, size_t smem, cudaStream_t stream)
+cudaError_t launch_nt(SkinnyParams& prm, size_t smem, cudaStream_t stream)
 {
     auto kern = skinny_kernel<NT>;
     static std::atomic<size_t> smem_set[kHostMaxDevices];
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(kern), smem, smem_set);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(static_cast<unsigned>((prm.d_out + kRows - 1) / kRows * prm.CK));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -293,6 +323,24 @@ cudaError_t launch_nt(const SkinnyParams& prm, size_t smem, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    // persistent clusters: as many as can be resident at once (cached per device,
+    // cluster size and shared-memory size), each taking every n-th row block
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= kHostMaxDevices) return cudaErrorInvalidDevice;
+    static std::atomic<int> resident[kHostMaxDevices][4];
+    static std::atomic<size_t> resident_smem[kHostMaxDevices][4];
+    const int ci = prm.CK == 1 ? 0 : prm.CK == 2 ? 1 : prm.CK == 4 ? 2 : 3;
+    int n_res = resident[dev][ci].load(std::memory_order_relaxed);
+    if (n_res <= 0 || resident_smem[dev][ci].load(std::memory_order_relaxed) != smem) {
+        cfg.gridDim = dim3(static_cast<unsigned>(prm.CK));
+        if ((e = cudaOccupancyMaxActiveClusters(&n_res, kern, &cfg)) != cudaSuccess) return e;
+        if (n_res < 1) n_res = 1;
+        resident[dev][ci].store(n_res, std::memory_order_relaxed);
+        resident_smem[dev][ci].store(smem, std::memory_order_relaxed);
+    }
+    prm.n_clusters = prm.n_blocks < n_res ? prm.n_blocks : n_res;
+    cfg.gridDim = dim3(static_cast<unsigned>(prm.n_clusters * prm.CK));
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
@@ -338,12 +386,12 @@ cudaError_t launch_skinny(const SkinnyArgs& a, cudaStream_t stream)
     ck = ck < 1 ? 1 : ck > 4 ? 4 : ck;
     prm.CK = ck;
     const size_t stage_bytes = stage_bytes_for(nt);
+    const size_t red = 2u * (2u * kRows * (8u * nt) * sizeof(float));  // two buffers of base + sign partials
     int stages = kMaxStages;
-    while (stages > 2 && stages * stage_bytes + 1024 > kSmemBudget) --stages;
+    while (stages > 2 && stages * stage_bytes + red + 1024 > kSmemBudget) --stages;
     prm.stages = stages;
-    const size_t red = 2u * kRows * (8u * nt) * sizeof(float);
-    size_t smem = stages * stage_bytes;
-    smem = (smem > red ? smem : red) + 1024;
+    prm.n_blocks = static_cast<int>((a.d_out + kRows - 1) / kRows);
+    const size_t smem = stages * stage_bytes + red + 1024;
     if (smem > 227u * 1024u) return cudaErrorInvalidConfiguration;
     switch (nt) {
         case 1: return launch_nt<1>(prm, smem, stream);
