@@ -188,7 +188,7 @@ bd_status bd_monosoup_merge(const uint16_t* w_base, const uint16_t* const* w_ft,
                             void* w_merged, int out_dtype, void* ws, size_t ws_bytes, void* stream)
 {
     if (out_dtype != BD_OUT_BF16 && out_dtype != BD_OUT_F32) return BD_ERR_INVALID_ARG;
-    if (k < 1 || k > BD_MAX_VARIANTS || rank < 0 || l < 1 || l > bd::monosoup_max_l() || rank > l ||
+    if (k < 1 || k > BD_MAX_VARIANTS || rank < 0 || l < 4 || l > bd::monosoup_max_l() || l % 4 != 0 || rank > l ||
         power_iters < 0 || power_iters > 16)
         return BD_ERR_INVALID_ARG;
     if (d_out < 0) return BD_ERR_UNSUPPORTED_SHAPE;
@@ -197,7 +197,7 @@ bd_status bd_monosoup_merge(const uint16_t* w_base, const uint16_t* const* w_ft,
     if (!w_base || !w_ft || !w_merged || (rank > 0 && !omega)) return BD_ERR_INVALID_ARG;
     const size_t wbytes = static_cast<size_t>(d_out) * static_cast<size_t>(d_in) * 2;
     const size_t obytes = wbytes * (out_dtype == BD_OUT_F32 ? 2 : 1);
-    if (!aligned(w_base, 16) || !aligned(w_merged, 16) || (omega && !aligned(omega, 4))) return BD_ERR_MISALIGNED;
+    if (!aligned(w_base, 16) || !aligned(w_merged, 16) || (omega && !aligned(omega, 16))) return BD_ERR_MISALIGNED;
     if (overlaps(w_merged, obytes, w_base, wbytes)) return BD_ERR_INVALID_ARG;
     for (int32_t i = 0; i < k; ++i) {
         if (!w_ft[i]) return BD_ERR_INVALID_ARG;
@@ -222,6 +222,7 @@ bd_status bd_monosoup_merge(const uint16_t* w_base, const uint16_t* const* w_ft,
     a.out = w_merged;
     a.out_f32 = out_dtype == BD_OUT_F32;
     a.ws = ws;
+    a.sm_count = sms;
     return launched(bd::launch_monosoup(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -137,6 +137,7 @@ struct MonoSoupArgs {
     void* out;                     // [d_out][d_in] bf16 or fp32
     int out_f32;
     void* ws;                      // monosoup_workspace_size bytes
+    int sm_count;                  // SMs of the current device
 };
 
 int monosoup_max_l();

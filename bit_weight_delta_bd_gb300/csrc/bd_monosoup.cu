@@ -14,18 +14,20 @@
 //   tau = (Q U_r) (U_r^T B)    (U_r: the r leading eigenvectors)
 // which is U_r S_r V_r^T of the rank-l approximation Q Q^T Delta.  Every pass
 // over Delta reads W_i and W_base (bf16) and forms Delta in fp32 on the fly.
-// Orthonormalisation is CholeskyQR: the Gram matrix is accumulated in fp64,
-// factored in one CTA, and Y <- Y R^-1 applied (twice, CholeskyQR2, for the
-// final basis); directions whose pivot falls below 1e-12 of the largest are
-// dropped (rank-deficient sketches).
+// Orthonormalisation is CholeskyQR: the Gram matrix is accumulated in
+// float-float, factored in fp64 in one CTA, and Y <- Y R^-1 applied by
+// forward substitution (twice, CholeskyQR2, for the final basis); directions
+// whose pivot falls below 1e-12 of the largest are dropped (rank-deficient
+// sketches).
 // The merge is one pass: W_base + (1/k) [L_1 .. L_k][R_1 .. R_k]^T with
 // L_i = Q_i U_r, R_i = B_i^T U_r, rounded once to the output type.
 //
-// All arithmetic is fp32 on the CUDA cores except the Gram matrices and the
-// Cholesky factor (fp64).  No kernel waits on another CTA; the passes are
+// All arithmetic is fp32 on the CUDA cores except the Gram matrices
+// (float-float) and the Cholesky factor (fp64).  No kernel waits on another CTA; the passes are
 // plain stream-ordered launches.
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <cmath>
 
 #include <atomic>
@@ -37,136 +39,244 @@ namespace bd {
 namespace {
 
 constexpr int kMaxL = 64;        // sketch width l (columns of Y, Q, B^T)
-constexpr int kGramBlocks = 152;  // CTAs of one Gram pass (fixed-order fp64 partials)
+constexpr int kGramBlocks = 608;  // CTAs of one Gram pass (fixed-order float-float partials)
 constexpr int kSlices = 16;       // split of the long dimension in the two products with Delta
-// dynamic shared memory of the Cholesky kernel: two fp64 [64][65] matrices
-constexpr size_t kSmallSmem = 2 * sizeof(double) * kMaxL * (kMaxL + 1);
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
-// Delta for 8 consecutive columns from two 16-byte loads of bf16 bits.
-__device__ __forceinline__ void delta8(const uint16_t* w, const uint16_t* wb, float* out)
-{
-    const uint4 a = *reinterpret_cast<const uint4*>(w);
-    const uint4 b = *reinterpret_cast<const uint4*>(wb);
-    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        out[2 * q] = bf16_bits_to_float(av[q] & 0xFFFFu) - bf16_bits_to_float(bv[q] & 0xFFFFu);
-        out[2 * q + 1] = bf16_bits_to_float(av[q] >> 16) - bf16_bits_to_float(bv[q] >> 16);
-    }
-}
+// The two products with Delta on the CUDA cores (fp32 FMA).  Products
+// accurate to fp32 are needed (the subspace of the final basis moves with
+// the products' relative error, amplified by the spectral spread): a bf16
+// tensor-core form accurate to fp32 takes six bf16 MMAs per 256 products
+// (three pieces of each operand), which at GB300's legacy MMA rate equals its
+// fp32 FMA rate, and tcgen05 MMAs with N = l <= 64 are bound by their issue
+// rate.  Both products stream the same tiles through one kernel:
+//   - a producer warp issues, per 64 x 64 tile of Delta's index space, TMA
+//     loads of W_i and W_base (128-byte swizzle) and a bulk copy of the 64
+//     rows of the small operand that the tile meets (Omega / Z for the
+//     sketch: rows = Delta's columns; Q for the transpose product: rows =
+//     Delta's rows) into a ring of kPStages stages;
+//   - eight FMA warps, as four pairs that split each stage 4 ways along its
+//     reduction index; every lane owns RPL rows (sketch) or 2 columns
+//     (transpose product) of Delta, the two warps of a pair one half each of
+//     the l output columns; Delta values come from the swizzled tile
+//     (conflict-free), the small operand as broadcasts (every lane of a warp
+//     reads the same row).
+// The warps' partial sums are added in warp order at the end and written as
+// one of gridDim.y partial results (summed in order by sum_slices_kernel).
 
-// ypart[s][row][c] = sum over slice s of the columns j of Delta[row][j] *
-// Om[j][c]  (c < l).  32 rows per CTA, blockIdx.y = slice (cols_per columns,
-// a multiple of 64), 64-column chunks; each thread holds 2 rows x NC columns.
-// NC = output columns per thread (kW = 16 NC columns per CTA, kW >= l).
-template <int NC>
-__global__ void __launch_bounds__(256) sketch_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ wb,
-                                                     int64_t d_out, int64_t d_in, const float* __restrict__ om, int l,
-                                                     int64_t cols_per, float* __restrict__ ypart)
+constexpr int kPWarps = 8;       // FMA warps per product CTA
+constexpr int kPTile = 64;       // Delta tile per stage: 64 x 64
+constexpr int kPStages = 4;
+constexpr int kPThreads = 32 * (kPWarps + 1);
+
+struct ProdParams {
+    CUtensorMap w_map;   // W_i  [d_out][d_in] bf16, box 64 x 64, 128-byte swizzle
+    CUtensorMap b_map;   // W_base, same
+    const float* small;  // Omega / Z [d_in][l] (sketch) or Q [d_out][l] (transpose product)
+    float* part;         // [gridDim.y][out rows][l]
+    uint32_t* err;
+    int64_t d_out, d_in;
+    int l;
+    int64_t k_per;       // reduction indices per slice (a multiple of 64)
+};
+
+// MODE 0: part[s][row][c] = sum over slice s of j of Delta[row][j] small[j][c]
+//         (CTA: 32 RPL rows of Delta; lane: rows lane + 32 h, h < RPL; warp
+//         pair cg = warp / 2 takes columns 16 cg .. 16 cg + 15 of each tile)
+// MODE 1: part[s][j][c] = sum over slice s of rows of Delta[row][j] small[row][c]
+//         (CTA: 64 columns of Delta; lane: columns 2 lane, 2 lane + 1; warp
+//         pair rg = warp / 2 takes rows 16 rg .. 16 rg + 15 of each tile)
+// The two warps of a pair hold the two halves of the l output columns
+// (LH = L4 / 2 float4 each), so that a lane keeps 2 x 4 LH accumulators.
+template <int MODE, int L4>
+__global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_constant__ ProdParams p)
 {
-    constexpr int kW = 16 * NC;
-    const int64_t jbeg = static_cast<int64_t>(blockIdx.y) * cols_per;
-    const int64_t jend = jbeg + cols_per < d_in ? jbeg + cols_per : d_in;
-    float* y = ypart + static_cast<int64_t>(blockIdx.y) * d_out * l;
-    __shared__ float sd[32][65];
-    __shared__ __align__(16) float so[64][kW];
-    const int tid = threadIdx.x;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * 32;
-    const int tr = (tid >> 4) * 2, tc = (tid & 15) * NC;
-    float acc[2][NC] = {};
-    for (int64_t j0 = jbeg; j0 < jend; j0 += 64) {
-        {
-            const int rr = tid >> 3, cc = (tid & 7) * 8;
-            const int64_t row = r0 + rr;
-            float d[8] = {};
-            if (row < d_out) delta8(w + row * d_in + j0 + cc, wb + row * d_in + j0 + cc, d);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) sd[rr][cc + q] = d[q];
+    constexpr int LH = L4 / 2;                                // float4 output columns per warp
+    constexpr int RPL = MODE == 0 ? (L4 <= 8 ? 2 : 1) : 2;  // Delta rows (columns) per lane
+    constexpr int kOut = MODE == 0 ? 32 * RPL : kPTile;      // output rows of one CTA
+    constexpr int kBoxRows = MODE == 0 ? 32 * RPL : kPTile;  // Delta rows per tile
+    constexpr int kWTile = kBoxRows * 128;                  // one bf16 tile: kBoxRows x 64
+    constexpr int kSTile = kPTile * 4 * L4 * 4;              // 64 rows of the small operand (fp32)
+    constexpr int kStage = 2 * kWTile + kSTile;
+    extern __shared__ uint8_t dyn_raw[];
+    __shared__ uint64_t full[kPStages], empty[kPStages];
+    __shared__ volatile int abort;
+    uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int l = p.l;
+    const int grp = warp >> 1, half = warp & 1;
+    const int c0 = half * LH;  // first float4 output column of this warp
+    const int64_t o0 = static_cast<int64_t>(blockIdx.x) * kOut;  // first output row of this CTA
+    const int64_t kb = static_cast<int64_t>(blockIdx.y) * p.k_per;
+    const int64_t klen = MODE == 0 ? p.d_in : p.d_out;
+    const int64_t ke = kb + p.k_per < klen ? kb + p.k_per : klen;
+    const int nt = static_cast<int>((ke - kb + kPTile - 1) / kPTile);  // tiles of this CTA
+    if (tid == 0) {
+        for (int s = 0; s < kPStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kPWarps);
         }
-        for (int e = tid; e < 64 * kW; e += 256) {
-            const int jj = e / kW, c = e % kW;
-            so[jj][c] = c < l ? om[(j0 + jj) * l + c] : 0.0f;
+        abort = 0;
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (mbar_try_wait(bar, par)) return true;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar, par)) {
+            if (abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                abort = 1;
+                raise_error(p.err, kErrTimeout);
+                return false;
+            }
         }
-        __syncthreads();
-#pragma unroll 8
-        for (int jj = 0; jj < 64; ++jj) {
-            const float a0 = sd[tr][jj], a1 = sd[tr + 1][jj];
-            float o[NC];
+        return true;
+    };
+    float4 acc[RPL][LH];
 #pragma unroll
-            for (int q = 0; q < NC; ++q) o[q] = so[jj][tc + q];
+    for (int h = 0; h < RPL; ++h)
 #pragma unroll
-            for (int q = 0; q < NC; ++q) {
-                acc[0][q] = fmaf(a0, o[q], acc[0][q]);
-                acc[1][q] = fmaf(a1, o[q], acc[1][q]);
+        for (int c = 0; c < LH; ++c) acc[h][c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    // acc += d[h] * small row (float4 columns c0 .. c0 + LH of it)
+    auto fma_row = [&](const float* row, const float (&d)[RPL]) {
+#pragma unroll
+        for (int c = 0; c < LH; ++c) {
+            if (4 * (c0 + c) >= l) break;
+            const float4 m = *reinterpret_cast<const float4*>(row + 4 * (c0 + c));
+#pragma unroll
+            for (int h = 0; h < RPL; ++h) {
+                acc[h][c].x = fmaf(d[h], m.x, acc[h][c].x);
+                acc[h][c].y = fmaf(d[h], m.y, acc[h][c].y);
+                acc[h][c].z = fmaf(d[h], m.z, acc[h][c].z);
+                acc[h][c].w = fmaf(d[h], m.w, acc[h][c].w);
+            }
+        }
+    };
+
+    if (warp == kPWarps) {
+        // ---------------------------------------------------------------- producer
+        int t = 0;
+        for (; t < nt; ++t) {
+            const int s = t % kPStages;
+            if (t >= kPStages && !__all_sync(0xffffffffu, wait(&empty[s], static_cast<uint32_t>(t / kPStages - 1) & 1u)))
+                break;
+            uint8_t* st = ring + static_cast<size_t>(s) * kStage;
+            const int64_t k0 = kb + static_cast<int64_t>(t) * kPTile;  // first reduction index of the tile
+            const int64_t kn = ke - k0 < kPTile ? ke - k0 : kPTile;     // valid rows of the small operand
+            if (lane == 0) {
+                const uint32_t sbytes = static_cast<uint32_t>(kn * l * 4);
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * kWTile) + sbytes);
+                const int cx = static_cast<int>(MODE == 0 ? k0 : o0), cy = static_cast<int>(MODE == 0 ? o0 : k0);
+                tma_load_2d(st, &p.w_map, cx, cy, &full[s]);
+                tma_load_2d(st + kWTile, &p.b_map, cx, cy, &full[s]);
+                bulk_g2s(st + 2 * kWTile, p.small + k0 * l, sbytes, &full[s]);
+            }
+            __syncwarp();
+        }
+        for (int i = (t > kPStages ? t - kPStages : 0); i < t; ++i) {  // every issued copy lands before exit
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(&full[i % kPStages], static_cast<uint32_t>(i / kPStages) & 1u) &&
+                   global_timer_ns() - t0 < kWaitLimitNs) {
+            }
+        }
+    } else {
+        // ---------------------------------------------------------------- FMA warps
+        for (int t = 0; t < nt; ++t) {
+            const int s = t % kPStages;
+            if (!__all_sync(0xffffffffu, wait(&full[s], static_cast<uint32_t>(t / kPStages) & 1u))) break;
+            const uint8_t* st = ring + static_cast<size_t>(s) * kStage;
+            const int64_t k0 = kb + static_cast<int64_t>(t) * kPTile;
+            const int kn = static_cast<int>(ke - k0 < kPTile ? ke - k0 : kPTile);
+            const float* sm = reinterpret_cast<const float*>(st + 2 * kWTile);  // [kn][l] as copied
+            if (MODE == 0) {
+                // pair grp: columns 16 grp .. 16 grp + 15 of the tile (16-byte chunks 2 grp, 2 grp + 1)
+#pragma unroll
+                for (int ch = 0; ch < 2; ++ch) {
+                    const int chunk = 2 * grp + ch, jj0 = 8 * chunk;
+                    if (jj0 >= kn) break;
+                    float d[RPL][8];
+#pragma unroll
+                    for (int h = 0; h < RPL; ++h) {
+                        const int r = lane + 32 * h;
+                        const int off = r * 128 + ((chunk ^ (r & 7)) << 4);
+                        const uint4 a = *reinterpret_cast<const uint4*>(st + off);
+                        const uint4 b = *reinterpret_cast<const uint4*>(st + kWTile + off);
+                        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            d[h][2 * q] = bf16_bits_to_float(av[q] & 0xFFFFu) - bf16_bits_to_float(bv[q] & 0xFFFFu);
+                            d[h][2 * q + 1] = bf16_bits_to_float(av[q] >> 16) - bf16_bits_to_float(bv[q] >> 16);
+                        }
+                    }
+                    const int qn = kn - jj0 < 8 ? kn - jj0 : 8;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        if (q >= qn) break;
+                        float dq[RPL];
+#pragma unroll
+                        for (int h = 0; h < RPL; ++h) dq[h] = d[h][q];
+                        fma_row(sm + (jj0 + q) * l, dq);
+                    }
+                }
+            } else {
+                // pair grp: rows 16 grp .. 16 grp + 15 of the tile; lane: columns 2 lane, 2 lane + 1
+#pragma unroll 4
+                for (int q = 0; q < 16; ++q) {
+                    const int r = 16 * grp + q;
+                    if (r >= kn) break;
+                    const int off = r * 128 + (((lane >> 2) ^ (r & 7)) << 4) + ((lane & 3) << 2);
+                    const uint32_t a = *reinterpret_cast<const uint32_t*>(st + off);
+                    const uint32_t b = *reinterpret_cast<const uint32_t*>(st + kWTile + off);
+                    float d[RPL];
+                    d[0] = bf16_bits_to_float(a & 0xFFFFu) - bf16_bits_to_float(b & 0xFFFFu);
+                    d[RPL - 1] = bf16_bits_to_float(a >> 16) - bf16_bits_to_float(b >> 16);
+                    fma_row(sm + r * l, d);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+    }
+    // ---------------------------------------------------------------- the warps' partials, in warp order
+    __syncthreads();  // the ring is drained: it becomes the reduction buffer [kOut][4 L4 + 1]
+    float* red = reinterpret_cast<float*>(ring);
+    constexpr int kRS = 4 * L4 + 1;
+    for (int wv = 0; wv < kPWarps; ++wv) {
+        if (warp == wv) {
+#pragma unroll
+            for (int h = 0; h < RPL; ++h) {
+                const int row = MODE == 0 ? lane + 32 * h : 2 * lane + h;
+#pragma unroll
+                for (int c = 0; c < LH; ++c) {
+                    const float v[4] = {acc[h][c].x, acc[h][c].y, acc[h][c].z, acc[h][c].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        float* dst = &red[row * kRS + 4 * (c0 + c) + e];
+                        *dst = wv < 2 ? v[e] : *dst + v[e];  // warps 0 and 1 start the two halves
+                    }
+                }
             }
         }
         __syncthreads();
     }
-#pragma unroll
-    for (int x = 0; x < 2; ++x) {
-        const int64_t row = r0 + tr + x;
-        if (row >= d_out) continue;
-#pragma unroll
-        for (int q = 0; q < NC; ++q)
-            if (tc + q < l) y[row * l + tc + q] = acc[x][q];
+    const int64_t nrows = MODE == 0 ? p.d_out : p.d_in;
+    float* out = p.part + static_cast<int64_t>(blockIdx.y) * nrows * l;
+    for (int e = tid; e < kOut * l; e += kPThreads) {
+        const int rr = e / l, c = e - rr * l;
+        if (o0 + rr < nrows) out[(o0 + rr) * l + c] = red[rr * kRS + c];
     }
 }
 
-// btpart[s][j][c] = sum over slice s of the rows of Delta[row][j] *
-// Q[row][c]  (c < l).  32 columns of Delta per CTA, blockIdx.y = slice
-// (rows_per rows, a multiple of 64), 64-row chunks; each thread holds 2
-// columns x NC.
-template <int NC>
-__global__ void __launch_bounds__(256) left_kernel(const uint16_t* __restrict__ w, const uint16_t* __restrict__ wb,
-                                                   int64_t d_out, int64_t d_in, const float* __restrict__ q, int l,
-                                                   int64_t rows_per, float* __restrict__ btpart)
+template <int MODE, int L4>
+size_t dprod_smem()
 {
-    constexpr int kW = 16 * NC;
-    const int64_t rbeg = static_cast<int64_t>(blockIdx.y) * rows_per;
-    const int64_t rend = rbeg + rows_per < d_out ? rbeg + rows_per : d_out;
-    float* bt = btpart + static_cast<int64_t>(blockIdx.y) * d_in * l;
-    __shared__ float sd[64][33];
-    __shared__ __align__(16) float sq[64][kW];
-    const int tid = threadIdx.x;
-    const int64_t j0 = static_cast<int64_t>(blockIdx.x) * 32;
-    const int tj = (tid >> 4) * 2, tc = (tid & 15) * NC;
-    float acc[2][NC] = {};
-    for (int64_t r0 = rbeg; r0 < rend; r0 += 64) {
-        {
-            const int rr = tid >> 2, cc = (tid & 3) * 8;
-            const int64_t row = r0 + rr;
-            float d[8] = {};
-            if (row < rend) delta8(w + row * d_in + j0 + cc, wb + row * d_in + j0 + cc, d);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) sd[rr][cc + e] = d[e];
-        }
-        for (int e = tid; e < 64 * kW; e += 256) {
-            const int rr = e / kW, c = e % kW;
-            const int64_t row = r0 + rr;
-            sq[rr][c] = (c < l && row < rend) ? q[row * l + c] : 0.0f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int rr = 0; rr < 64; ++rr) {
-            const float a0 = sd[rr][tj], a1 = sd[rr][tj + 1];
-            float o[NC];
-#pragma unroll
-            for (int qq = 0; qq < NC; ++qq) o[qq] = sq[rr][tc + qq];
-#pragma unroll
-            for (int qq = 0; qq < NC; ++qq) {
-                acc[0][qq] = fmaf(a0, o[qq], acc[0][qq]);
-                acc[1][qq] = fmaf(a1, o[qq], acc[1][qq]);
-            }
-        }
-        __syncthreads();
-    }
-#pragma unroll
-    for (int x = 0; x < 2; ++x)
-#pragma unroll
-        for (int qq = 0; qq < NC; ++qq)
-            if (tc + qq < l) bt[(j0 + tj + x) * l + tc + qq] = acc[x][qq];
+    constexpr int RPL = MODE == 0 ? (L4 <= 8 ? 2 : 1) : 2;
+    constexpr int kBoxRows = MODE == 0 ? 32 * RPL : kPTile;
+    const size_t stage = 2u * kBoxRows * 128 + static_cast<size_t>(kPTile) * 4 * L4 * 4;
+    const size_t red = static_cast<size_t>(MODE == 0 ? 32 * RPL : kPTile) * (4 * L4 + 1) * 4;
+    return (kPStages * stage > red ? kPStages * stage : red) + 1024;
 }
 
 // out[e] = sum_s part[s][e], e < n (fixed order).
@@ -180,211 +290,279 @@ __global__ void __launch_bounds__(256) sum_slices_kernel(const float* __restrict
     out[e] = s;
 }
 
-// Partial Gram matrices of A [n][l]: CTA b sums A^T A over its contiguous row
-// range in fp64 into part[b][l * l] (entry i * l + j).
-__global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, int64_t n, int l,
-                                                   double* __restrict__ part)
+// ---------------------------------------------------------------- small-matrix steps
+// GB300 has few fp64 units (about 2 fp64 FMAs per cycle per SM), so the Gram
+// matrices are accumulated in float-float arithmetic on the fp32 units (each
+// product split exactly with an FMA, each sum with TwoSum; about 2^-44
+// relative, like fp64 for this purpose), and only the l x l Cholesky factor
+// is computed in fp64.
+
+// s + t = a + b exactly (Knuth's TwoSum; explicit _rn intrinsics so that no
+// operation is contracted or reordered).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& t)
 {
-    __shared__ double sa[32][kMaxL + 1];  // converted once per element, not once per product
+    s = __fadd_rn(a, b);
+    const float z = __fsub_rn(s, a);
+    t = __fadd_rn(__fsub_rn(a, __fsub_rn(s, z)), __fsub_rn(b, z));
+}
+
+// (s, c) += a * b in float-float: the rounded product and its exact error
+// (fma), the sum by TwoSum, the errors gathered in c.
+__device__ __forceinline__ void ff_madd(float& s, float& c, float a, float b)
+{
+    const float p = __fmul_rn(a, b);
+    const float pe = __fmaf_rn(a, b, -p);
+    float t, e;
+    two_sum(s, p, t, e);
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(e, pe));
+}
+
+// (s, c) += (x, y) in float-float.
+__device__ __forceinline__ void ff_add(float& s, float& c, float x, float y)
+{
+    float t, e;
+    two_sum(s, x, t, e);
+    s = t;
+    c = __fadd_rn(c, __fadd_rn(e, y));
+}
+
+// Partial Gram matrices of A [n][l]: CTA b sums A^T A over its contiguous row
+// range in float-float into part[b][l * l] (entry i * l + j as (hi, lo));
+// ENT = entries per thread (l * l <= 256 ENT).
+template <int ENT>
+__global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, int64_t n, int l,
+                                                   float2* __restrict__ part)
+{
+    __shared__ float sa[32][kMaxL + 1];
     const int tid = threadIdx.x;
     const int64_t per = (n + kGramBlocks - 1) / kGramBlocks;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * per;
     const int64_t b1 = b0 + per < n ? b0 + per : n;
     const int ll = l * l;
-    double acc[16];
+    int pi[ENT], pj[ENT];
+    float s[ENT], c[ENT];
 #pragma unroll
-    for (int m = 0; m < 16; ++m) acc[m] = 0.0;
+    for (int m = 0; m < ENT; ++m) {
+        const int p = tid + 256 * m;
+        pi[m] = p < ll ? p / l : 0;  // past l * l: a dummy entry, never stored
+        pj[m] = p < ll ? p % l : 0;
+        s[m] = c[m] = 0.0f;
+    }
     for (int64_t r0 = b0; r0 < b1; r0 += 32) {
         for (int e = tid; e < 32 * kMaxL; e += 256) {
-            const int rr = e / kMaxL, c = e % kMaxL;
+            const int rr = e >> 6, cc = e & 63;
             const int64_t row = r0 + rr;
-            sa[rr][c] = (row < b1 && c < l) ? static_cast<double>(a[row * l + c]) : 0.0;
+            sa[rr][cc] = (row < b1 && cc < l) ? a[row * l + cc] : 0.0f;
         }
         __syncthreads();
-        for (int rr = 0; rr < 32; ++rr) {
+        const int nr = b1 - r0 < 32 ? static_cast<int>(b1 - r0) : 32;
+        for (int rr = 0; rr < nr; ++rr) {
 #pragma unroll
-            for (int m = 0; m < 16; ++m) {
-                const int p = tid + 256 * m;
-                if (p < ll) acc[m] = fma(sa[rr][p / l], sa[rr][p % l], acc[m]);
-            }
+            for (int m = 0; m < ENT; ++m) ff_madd(s[m], c[m], sa[rr][pi[m]], sa[rr][pj[m]]);
         }
         __syncthreads();
     }
 #pragma unroll
-    for (int m = 0; m < 16; ++m) {
+    for (int m = 0; m < ENT; ++m) {
         const int p = tid + 256 * m;
-        if (p < ll) part[static_cast<int64_t>(blockIdx.x) * ll + p] = acc[m];
+        if (p < ll) {
+            float hi, lo;
+            two_sum(s[m], c[m], hi, lo);
+            part[static_cast<int64_t>(blockIdx.x) * ll + p] = make_float2(hi, lo);
+        }
     }
 }
 
-// g[e] = sum_b part[b][e], e < l * l (fixed order, one thread per entry).
-__global__ void __launch_bounds__(256) gram_sum_kernel(const double* __restrict__ part, int l, double* __restrict__ g)
+// G[e] = sum_b part[b][e] (float-float, then exactly to fp64), one warp per
+// entry: lane L takes partials L, L + 32, ... in order, then a fixed
+// butterfly; the result does not depend on timing.
+__global__ void __launch_bounds__(256) gram_sum_kernel(const float2* __restrict__ part, int l, double* __restrict__ G)
 {
-    const int e = blockIdx.x * blockDim.x + threadIdx.x;
+    const int e = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
     const int ll = l * l;
     if (e >= ll) return;
-    double s = 0.0;
-    for (int b = 0; b < kGramBlocks; ++b) s += part[static_cast<int64_t>(b) * ll + e];
-    g[e] = s;
-}
-
-// Loads the summed Gram matrix G [l][l] into g[64][65], zero past l.
-__device__ __forceinline__ void load_gram(const double* __restrict__ G, int l, double (*g)[kMaxL + 1])
-{
-    for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
-        const int i = e >> 6, j = e & 63;
-        g[i][j] = (i < l && j < l) ? G[i * l + j] : 0.0;
+    // four independent float-float chains per lane (partials lane + 32 (4 i + u)), then fixed combines
+    float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int b = lane; b < kGramBlocks; b += 128) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int bb = b + 32 * u;
+            if (bb < kGramBlocks) {
+                const float2 v = part[static_cast<int64_t>(bb) * ll + e];
+                ff_add(s[u], c[u], v.x, v.y);
+            }
+        }
     }
+    ff_add(s[0], c[0], s[1], c[1]);
+    ff_add(s[2], c[2], s[3], c[3]);
+    ff_add(s[0], c[0], s[2], c[2]);
+    float sv = s[0], cv = c[0];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, sv, o), oc = __shfl_xor_sync(0xffffffffu, cv, o);
+        ff_add(sv, cv, os, oc);  // fixed butterfly: lane 0's sum does not depend on timing
+    }
+    if (lane == 0) G[e] = static_cast<double>(sv) + static_cast<double>(cv);
 }
 
-// One CTA: G = R^T R (Cholesky, R upper); minv = R^-1
-// as fp32 [l][l].  A pivot below 1e-12 of the largest diagonal entry drops
-// its direction (its row and column of R^-1 are zero).
-__global__ void __launch_bounds__(256) chol_inv_kernel(const double* __restrict__ G, int l,
-                                                       float* __restrict__ minv)
+// One CTA: G = R^T R (Cholesky, R upper) in fp64; R written as fp32 [l][l]
+// (zero below the diagonal) with the reciprocals of its diagonal in rinv.
+// 1/sqrt(d) comes from the fp32 rsqrt and two Newton steps in fp64 (about
+// 2^-46; fp64 square roots and divisions are long sequences on GB300's few
+// fp64 units).  A pivot below 1e-12 of the largest diagonal entry drops its
+// direction (its row of R and its reciprocal are zero).
+__global__ void __launch_bounds__(256) chol_kernel(const double* __restrict__ G, int l, float* __restrict__ Rf,
+                                                   float* __restrict__ rinv)
 {
-    extern __shared__ double dsm[];  // kSmallSmem bytes: g, then ri
-    double (*g)[kMaxL + 1] = reinterpret_cast<double (*)[kMaxL + 1]>(dsm);
-    double (*ri)[kMaxL + 1] = reinterpret_cast<double (*)[kMaxL + 1]>(dsm + kMaxL * (kMaxL + 1));
-    __shared__ double dmax;
-    __shared__ int dead[kMaxL];
+    __shared__ double g[kMaxL][kMaxL + 1];
+    __shared__ double dmax, s_inv;
+    __shared__ double rdiag[kMaxL];
+    __shared__ int live[kMaxL];
     const int tid = threadIdx.x;
-    load_gram(G, l, g);
+    const int ti = tid >> 4, tj = tid & 15;
+    for (int i = ti; i < kMaxL; i += 16)
+        for (int j = tj; j < kMaxL; j += 16) g[i][j] = (i < l && j < l) ? G[i * l + j] : 0.0;
     __syncthreads();
-    if (tid == 0) {
+    if (tid < 32) {
         double m = 0.0;
-        for (int i = 0; i < l; ++i) m = fmax(m, g[i][i]);
-        dmax = m;
+        for (int i = tid; i < l; i += 32) m = fmax(m, g[i][i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (tid == 0) dmax = m;
     }
     __syncthreads();
     const double tol = 1e-12 * dmax;
     for (int k = 0; k < l; ++k) {
-        // g holds the trailing Schur complement; row k of R replaces row k of g
-        const double d = g[k][k];
-        const bool live = d > tol && d > 0.0;
-        __syncthreads();
-        if (tid == 0) dead[k] = live ? 0 : 1;
-        const double rkk = live ? sqrt(d) : 0.0;
-        const double inv = live ? 1.0 / rkk : 0.0;
-        for (int j = k + tid; j < l; j += blockDim.x) g[k][j] = live ? (j == k ? rkk : g[k][j] * inv) : 0.0;
-        __syncthreads();
-        for (int e = tid; e < l * l; e += blockDim.x) {
-            const int i = e / l, j = e % l;
-            if (i > k && j >= i) g[i][j] -= g[k][i] * g[k][j];
+        if (tid == 0) {
+            const double d = g[k][k];
+            const bool ok = d > tol && d > 0.0;
+            double y = ok ? static_cast<double>(rsqrtf(static_cast<float>(d))) : 0.0;
+            y = y * fma(-0.5 * d * y, y, 1.5);
+            y = y * fma(-0.5 * d * y, y, 1.5);
+            g[k][k] = ok ? d * y : 0.0;
+            s_inv = ok ? y : 0.0;
+            rdiag[k] = s_inv;
+            live[k] = ok ? 1 : 0;
         }
         __syncthreads();
+        for (int j = k + 1 + tid; j < l; j += 256) g[k][j] *= s_inv;
+        __syncthreads();
+        for (int i = k + 1 + ti; i < l; i += 16)
+            for (int j = i + ((tj - i) & 15); j < l; j += 16) g[i][j] = fma(-g[k][i], g[k][j], g[i][j]);
+        __syncthreads();
     }
-    // R^-1 (upper triangular) by back substitution, one column per thread,
-    // with the diagonal's reciprocals taken once
-    __shared__ double dinv[kMaxL];
-    for (int i = tid; i < l; i += blockDim.x) dinv[i] = dead[i] ? 0.0 : 1.0 / g[i][i];
-    __syncthreads();
-    for (int j = tid; j < l; j += blockDim.x) {
-        for (int i = 0; i < l; ++i) ri[i][j] = 0.0;
-        if (!dead[j]) {
-            ri[j][j] = dinv[j];
-            for (int i = j - 1; i >= 0; --i) {
-                if (dead[i]) continue;
-                double s = 0.0;
-                for (int m = i + 1; m <= j; ++m) s += g[i][m] * ri[m][j];
-                ri[i][j] = -s * dinv[i];
-            }
-        }
-    }
-    __syncthreads();
-    for (int e = tid; e < l * l; e += blockDim.x) minv[e] = static_cast<float>(ri[e / l][e % l]);
+    for (int i = ti; i < l; i += 16)
+        for (int j = tj; j < l; j += 16) Rf[i * l + j] = (j >= i && live[i]) ? static_cast<float>(g[i][j]) : 0.0f;
+    for (int i = tid; i < l; i += 256) rinv[i] = live[i] ? static_cast<float>(rdiag[i]) : 0.0f;
 }
 
-// One CTA: the symmetric eigenproblem of G by cyclic Jacobi in fp32 with the
-// round-robin pair order (l/2 disjoint rotations per round) until the
-// off-diagonal mass is below 1e-12 of the diagonal's (at most 40 sweeps);
-// ur[i][m] = the eigenvector of the m-th largest eigenvalue, m < r.  Only
-// the r leading eigenvectors are used, and they are set apart by the
-// spectral gap, so fp32 (fp64 rotations are slow on GB300's few fp64 units)
-// costs about 1e-6 of them.
-__global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ G, int l, int r,
-                                                     float* __restrict__ ur)
+// One CTA of 1024 threads: the symmetric eigenproblem of G by cyclic Jacobi
+// in fp32 with the round-robin pair order (n/2 disjoint rotations per round,
+// n = l rounded up to even, index l a dummy when l is odd) until the
+// off-diagonal mass is below 1e-12 of the diagonal's (at most 40 sweeps).
+// A round is A <- P^T A P and V <- V P for the rotations P of its n/2 pairs:
+// every 2 x 2 block of A at (row pair, column pair) and every (row, column
+// pair) of V is updated in place by one thread, so a round needs two
+// barriers.  ur[i][m] = the eigenvector of the m-th largest eigenvalue,
+// m < r.  Only the r leading eigenvectors are used, and they are set apart
+// by the spectral gap, so fp32 costs about 1e-6 of them.
+constexpr int kJacobiThreads = 1024;
+
+__global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const double* __restrict__ G_all, int l, int r,
+                                                                float* __restrict__ ur_all)
 {
+    // one eigenproblem per CTA (checkpoint blockIdx.x)
+    const double* G = G_all + static_cast<size_t>(blockIdx.x) * l * l;
+    float* ur = ur_all + static_cast<size_t>(blockIdx.x) * l * r;
     __shared__ float A[kMaxL][kMaxL + 1];
     __shared__ float V[kMaxL][kMaxL + 1];
     __shared__ float cs[kMaxL / 2], sn[kMaxL / 2];
     __shared__ int pp[kMaxL / 2], qq[kMaxL / 2];
-    __shared__ float red[2][256];
+    __shared__ float red[2][32];
     __shared__ int idx[kMaxL];
-    const int tid = threadIdx.x;
-    for (int e = tid; e < kMaxL * kMaxL; e += blockDim.x) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int e = tid; e < kMaxL * kMaxL; e += kJacobiThreads) {
         const int i = e >> 6, j = e & 63;
         A[i][j] = (i < l && j < l) ? static_cast<float>(G[i * l + j]) : 0.0f;
         V[i][j] = i == j ? 1.0f : 0.0f;
     }
     __syncthreads();
-    const int n = l + (l & 1);  // even number of players; index l is a dummy when l is odd
+    const int n = l + (l & 1);
+    const int h = n / 2;
     for (int sweep = 0; sweep < 40; ++sweep) {
         float off = 0.0f, dia = 0.0f;
-        for (int e = tid; e < l * l; e += blockDim.x) {
-            const float v = A[e / l][e % l];
-            if (e / l == e % l)
-                dia += v * v;
+        for (int e = tid; e < kMaxL * kMaxL; e += kJacobiThreads) {
+            const int i = e >> 6, j = e & 63;
+            const float v = A[i][j];
+            if (i == j)
+                dia = fmaf(v, v, dia);
             else
-                off += v * v;
+                off = fmaf(v, v, off);
         }
-        red[0][tid] = off;
-        red[1][tid] = dia;
-        __syncthreads();
-        for (int s = 128; s > 0; s >>= 1) {
-            if (tid < s) {
-                red[0][tid] += red[0][tid + s];
-                red[1][tid] += red[1][tid + s];
-            }
-            __syncthreads();
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            off += __shfl_xor_sync(0xffffffffu, off, o);
+            dia += __shfl_xor_sync(0xffffffffu, dia, o);
         }
-        const bool done = !(red[0][0] > 1e-12f * red[1][0]);
+        if (lane == 0) {
+            red[0][warp] = off;
+            red[1][warp] = dia;
+        }
         __syncthreads();
-        if (done) break;
+        float toff = 0.0f, tdia = 0.0f;
+        for (int w = 0; w < kJacobiThreads / 32; ++w) {
+            toff += red[0][w];
+            tdia += red[1][w];
+        }
+        __syncthreads();
+        if (!(toff > 1e-12f * tdia)) break;
         for (int t = 0; t + 1 < n; ++t) {
-            if (tid < n / 2) {
+            if (tid < h) {
                 const int a = tid == 0 ? 0 : 1 + (tid - 1 + t) % (n - 1);
                 const int b = 1 + (n - 2 - tid + t) % (n - 1);
                 const int p = a < b ? a : b, q = a < b ? b : a;
-                float c = 1.0f, s = 0.0f;
+                float c = 1.0f, sv = 0.0f;
                 if (q < l) {
                     const float apq = A[p][q];
                     if (fabsf(apq) > 1e-30f) {
                         const float th = (A[q][q] - A[p][p]) / (2.0f * apq);
                         const float tt = (th >= 0.0f ? 1.0f : -1.0f) / (fabsf(th) + sqrtf(th * th + 1.0f));
                         c = 1.0f / sqrtf(tt * tt + 1.0f);
-                        s = tt * c;
+                        sv = tt * c;
                     }
                 }
                 cs[tid] = c;
-                sn[tid] = s;
+                sn[tid] = sv;
                 pp[tid] = p;
                 qq[tid] = q;
             }
             __syncthreads();
-            // A <- A P and V <- V P (columns p, q of every disjoint pair)
-            for (int e = tid; e < (n / 2) * l; e += blockDim.x) {
-                const int i = e / l, row = e % l;
-                const int p = pp[i], q = qq[i];
-                if (q >= l) continue;
-                const float c = cs[i], s = sn[i];
-                const float ap = A[row][p], aq = A[row][q];
-                A[row][p] = c * ap - s * aq;
-                A[row][q] = s * ap + c * aq;
-                const float vp = V[row][p], vq = V[row][q];
-                V[row][p] = c * vp - s * vq;
-                V[row][q] = s * vp + c * vq;
+            // A: block (pair bi rows, pair bj columns); columns first (A P), then rows (P^T .)
+            for (int e = tid; e < h * h; e += kJacobiThreads) {
+                const int bi = e / h, bj = e - (e / h) * h;
+                const int p = pp[bi], q = qq[bi], p2 = pp[bj], q2 = qq[bj];
+                const float ci = cs[bi], si = sn[bi], cj = cs[bj], sj = sn[bj];
+                const bool rq = q < l, cq = q2 < l;
+                const float a_pp = A[p][p2], a_pq = cq ? A[p][q2] : 0.0f;
+                const float a_qp = rq ? A[q][p2] : 0.0f, a_qq = (rq && cq) ? A[q][q2] : 0.0f;
+                const float x_pp = cj * a_pp - sj * a_pq, x_pq = sj * a_pp + cj * a_pq;
+                const float x_qp = cj * a_qp - sj * a_qq, x_qq = sj * a_qp + cj * a_qq;
+                A[p][p2] = ci * x_pp - si * x_qp;
+                if (cq) A[p][q2] = ci * x_pq - si * x_qq;
+                if (rq) A[q][p2] = si * x_pp + ci * x_qp;
+                if (rq && cq) A[q][q2] = si * x_pq + ci * x_qq;
             }
-            __syncthreads();
-            // A <- P^T A (rows p, q)
-            for (int e = tid; e < (n / 2) * l; e += blockDim.x) {
-                const int i = e / l, col = e % l;
-                const int p = pp[i], q = qq[i];
-                if (q >= l) continue;
-                const float c = cs[i], s = sn[i];
-                const float ap = A[p][col], aq = A[q][col];
-                A[p][col] = c * ap - s * aq;
-                A[q][col] = s * ap + c * aq;
+            // V: (row, column pair bj)
+            for (int e = tid; e < l * h; e += kJacobiThreads) {
+                const int row = e / h, bj = e - (e / h) * h;
+                const int p2 = pp[bj], q2 = qq[bj];
+                if (q2 >= l) continue;
+                const float cj = cs[bj], sj = sn[bj];
+                const float vp = V[row][p2], vq = V[row][q2];
+                V[row][p2] = cj * vp - sj * vq;
+                V[row][q2] = sj * vp + cj * vq;
             }
             __syncthreads();
         }
@@ -401,13 +579,45 @@ __global__ void __launch_bounds__(256) jacobi_kernel(const double* __restrict__ 
         }
     }
     __syncthreads();
-    for (int e = tid; e < l * r; e += blockDim.x) ur[e] = V[e / r][idx[e % r]];
+    for (int e = tid; e < l * r; e += kJacobiThreads) ur[e] = V[e / r][idx[e % r]];
 }
 
-// dst[row][j] = sum_c src[row][c] * M[c][j]  (c < l, j < m); one row per
-// thread, read whole before any write, so dst may be src when m == l.
-__global__ void __launch_bounds__(256) apply_kernel(const float* src, int64_t n, int l, const float* __restrict__ M,
-                                                    int m, float* dst)
+// A <- A R^-1 in place (R from chol_kernel): per row the forward substitution
+// x_j = (a_j - sum_{m<j} x_m R[m][j]) / R[j][j], a dropped direction giving
+// x_j = 0; one row per thread.
+__global__ void __launch_bounds__(64) tri_solve_kernel(float* a, int64_t n, int l, const float* __restrict__ Rf,
+                                                       const float* __restrict__ rinv)
+{
+    __shared__ float sr[kMaxL][kMaxL + 1];
+    __shared__ float sd[kMaxL];
+    for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
+        const int i = e >> 6, j = e & 63;
+        sr[i][j] = (i < l && j < l) ? Rf[i * l + j] : 0.0f;
+    }
+    for (int i = threadIdx.x; i < kMaxL; i += blockDim.x) sd[i] = i < l ? rinv[i] : 0.0f;
+    __syncthreads();
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (row >= n) return;
+    float x[kMaxL];
+#pragma unroll
+    for (int j = 0; j < kMaxL; ++j) x[j] = j < l ? a[row * l + j] : 0.0f;
+#pragma unroll
+    for (int j = 0; j < kMaxL; ++j) {
+        if (j >= l) break;
+        float s = x[j];
+#pragma unroll
+        for (int m = 0; m < j; ++m) s = fmaf(-x[m], sr[m][j], s);
+        x[j] = s * sd[j];
+    }
+#pragma unroll
+    for (int j = 0; j < kMaxL; ++j)
+        if (j < l) a[row * l + j] = x[j];
+}
+
+// dst[row][j] = sum_c src[row][c] * M[c][j]  (c < l, j < m): one output
+// element per thread (src and dst distinct).
+__global__ void __launch_bounds__(256) apply_kernel(const float* __restrict__ src, int64_t n, int l,
+                                                    const float* __restrict__ M, int m, float* __restrict__ dst)
 {
     __shared__ float sm[kMaxL][kMaxL];
     for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
@@ -415,17 +625,14 @@ __global__ void __launch_bounds__(256) apply_kernel(const float* src, int64_t n,
         sm[c][j] = (c < l && j < m) ? M[c * m + j] : 0.0f;
     }
     __syncthreads();
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= n) return;
-    float v[kMaxL];
-#pragma unroll
-    for (int c = 0; c < kMaxL; ++c) v[c] = c < l ? src[row * l + c] : 0.0f;
-    for (int j = 0; j < m; ++j) {
-        float s = 0.0f;
-#pragma unroll
-        for (int c = 0; c < kMaxL; ++c) s = fmaf(v[c], sm[c][j], s);
-        dst[row * m + j] = s;
-    }
+    const int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (o >= n * m) return;
+    const int64_t row = o / m;
+    const int j = static_cast<int>(o - row * m);
+    const float* s = src + row * l;
+    float acc = 0.0f;
+    for (int c = 0; c < l; ++c) acc = fmaf(s[c], sm[c][j], acc);
+    dst[o] = acc;
 }
 
 // out[row][j] = W_base[row][j] + inv_k * sum_e L[e][row] Rt[e][j], e over the
@@ -485,7 +692,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const uint16_t* __restrict__
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct MonoSoupWs {
-    size_t y, z, ypart, zpart, part, g, m, L, Rt, total;
+    size_t y, z, ypart, zpart, part, g, gk, m, uk, L, Rt, total;
 };
 
 MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
@@ -497,13 +704,15 @@ MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
         off += up256(bytes);
         return at;
     };
-    w.y = take(static_cast<size_t>(d_out) * l * 4);
-    w.z = take(static_cast<size_t>(d_in) * l * 4);
+    w.y = take(static_cast<size_t>(k) * d_out * l * 4);  // Q_i of every checkpoint
+    w.z = take(static_cast<size_t>(k) * d_in * l * 4);   // B_i^T of every checkpoint
     w.ypart = take(static_cast<size_t>(kSlices) * d_out * l * 4);
     w.zpart = take(static_cast<size_t>(kSlices) * d_in * l * 4);
     w.part = take(static_cast<size_t>(kGramBlocks) * l * l * 8);
     w.g = take(static_cast<size_t>(l) * l * 8);
-    w.m = take(static_cast<size_t>(kMaxL) * kMaxL * 4);
+    w.gk = take(static_cast<size_t>(k) * l * l * 8);     // B_i B_i^T of every checkpoint
+    w.m = take(static_cast<size_t>(kMaxL) * kMaxL * 4 + kMaxL * 4);
+    w.uk = take(static_cast<size_t>(k) * l * (r > 0 ? r : 1) * 4);
     w.L = take(static_cast<size_t>(k) * d_out * (r > 0 ? r : 1) * 4);
     w.Rt = take(static_cast<size_t>(k) * d_in * (r > 0 ? r : 1) * 4);
     w.total = off;
@@ -523,59 +732,124 @@ size_t monosoup_workspace_size(int64_t d_out, int64_t d_in, int k, int r, int l)
 
 cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
 {
-    static std::atomic<size_t> chol_set[kHostMaxDevices];
-    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(chol_inv_kernel), kSmallSmem, chol_set);
-    if (e != cudaSuccess) return e;
+    static std::atomic<size_t> s00[kHostMaxDevices], s01[kHostMaxDevices], s10[kHostMaxDevices], s11[kHostMaxDevices];
+    cudaError_t e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(dprod_kernel<0, 8>), dprod_smem<0, 8>(), s00);
+    if (e0 == cudaSuccess)
+        e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(dprod_kernel<0, 16>), dprod_smem<0, 16>(), s01);
+    if (e0 == cudaSuccess)
+        e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(dprod_kernel<1, 8>), dprod_smem<1, 8>(), s10);
+    if (e0 == cudaSuccess)
+        e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(dprod_kernel<1, 16>), dprod_smem<1, 16>(), s11);
+    if (e0 != cudaSuccess) return e0;
     const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
     char* w = static_cast<char*>(a.ws);
-    float* Y = reinterpret_cast<float*>(w + lay.y);
-    float* Z = reinterpret_cast<float*>(w + lay.z);
+    float* Yall = reinterpret_cast<float*>(w + lay.y);
+    float* Zall = reinterpret_cast<float*>(w + lay.z);
+    double* Gk = reinterpret_cast<double*>(w + lay.gk);
+    float* Uk = reinterpret_cast<float*>(w + lay.uk);
+    float* Y = Yall;
+    float* Z = Zall;
     float* Yp = reinterpret_cast<float*>(w + lay.ypart);
     float* Zp = reinterpret_cast<float*>(w + lay.zpart);
-    double* part = reinterpret_cast<double*>(w + lay.part);
+    float2* part = reinterpret_cast<float2*>(w + lay.part);
     double* G = reinterpret_cast<double*>(w + lay.g);
     float* M = reinterpret_cast<float*>(w + lay.m);
     float* L = reinterpret_cast<float*>(w + lay.L);
     float* Rt = reinterpret_cast<float*>(w + lay.Rt);
     const int l = a.l, r = a.rank;
-    // the two products with Delta, each split in kSlices along its long
-    // dimension and summed in slice order
-    const int64_t ncol = a.d_in / 64, nrow = (a.d_out + 63) / 64;
-    const int64_t cs = (ncol + kSlices - 1) / kSlices, rs = (nrow + kSlices - 1) / kSlices;
-    const dim3 gsk(static_cast<unsigned>((a.d_out + 31) / 32), static_cast<unsigned>((ncol + cs - 1) / cs));
-    const dim3 glf(static_cast<unsigned>(a.d_in / 32), static_cast<unsigned>((nrow + rs - 1) / rs));
-    // tiles as wide as l needs: 32 columns (2 per thread) up to l = 32, else 64
+    // the two products with Delta: CTAs of 64 rows (or 32, l > 32) / 64
+    // columns of Delta, the reduction dimension split in gridDim.y slices (so
+    // that every SM gets about two CTAs), the slices summed in order
+    const int sms = a.sm_count > 0 ? a.sm_count : 152;
+    static thread_local ProdParams pp_sk, pp_lf;
+    const int sk_rows = l <= 32 ? 64 : 32;
+    const int64_t rblocks = (a.d_out + sk_rows - 1) / sk_rows, cblocks = a.d_in / kPTile;
+    // slices: the smallest count whose CTAs fill whole waves of two CTAs per SM
+    // to within an eighth (else the count nearest three waves), at most kSlices
+    auto slices = [&](int64_t blocks, int64_t klen, int64_t* per) {
+        const int64_t wave = 2 * static_cast<int64_t>(sms);
+        int ns = 1;
+        for (int c = 1; c <= kSlices; ++c) {
+            const int64_t ctas = blocks * c;
+            const int64_t full = (ctas + wave - 1) / wave;
+            if (ctas * 8 >= full * wave * 7 && ctas >= wave) {
+                ns = c;
+                break;
+            }
+            if (std::llabs(ctas - 3 * wave) < std::llabs(blocks * ns - 3 * wave)) ns = c;
+        }
+        *per = ((klen + ns - 1) / ns + kPTile - 1) / kPTile * kPTile;
+        return static_cast<int>((klen + *per - 1) / *per);
+    };
+    int64_t cper = 0, rper = 0;
+    const int ssk = slices(rblocks, a.d_in, &cper), slf = slices(cblocks, a.d_out, &rper);
+    const dim3 gsk(static_cast<unsigned>(rblocks), static_cast<unsigned>(ssk));
+    const dim3 glf(static_cast<unsigned>(cblocks), static_cast<unsigned>(slf));
+    auto prep = [&](ProdParams& pr, const uint16_t* wi, const float* small, float* part, int64_t per, int box_rows) {
+        if (!encode_tma_2d(&pr.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wi, static_cast<uint64_t>(a.d_in),
+                           static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, kPTile,
+                           static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+        if (!encode_tma_2d(&pr.b_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
+                           static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, kPTile,
+                           static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B))
+            return false;
+        pr.small = small;
+        pr.part = part;
+        pr.err = nullptr;
+        pr.d_out = a.d_out;
+        pr.d_in = a.d_in;
+        pr.l = l;
+        pr.k_per = per;
+        return true;
+    };
+    cudaError_t perr = cudaSuccess;
     auto sketch = [&](const uint16_t* wi, const float* om) {  // Y = Delta om
+        if (perr != cudaSuccess) return;
+        if (!prep(pp_sk, wi, om, Yp, cper, sk_rows)) {
+            perr = cudaErrorInvalidValue;
+            return;
+        }
         if (l <= 32)
-            sketch_kernel<2><<<gsk, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, om, l, 64 * cs, Yp);
+            dprod_kernel<0, 8><<<gsk, kPThreads, dprod_smem<0, 8>(), st>>>(pp_sk);
         else
-            sketch_kernel<4><<<gsk, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, om, l, 64 * cs, Yp);
-        sum_slices_kernel<<<blocks_for(a.d_out * l), 256, 0, st>>>(Yp, static_cast<int>(gsk.y), a.d_out * l, Y);
+            dprod_kernel<0, 16><<<gsk, kPThreads, dprod_smem<0, 16>(), st>>>(pp_sk);
+        sum_slices_kernel<<<blocks_for(a.d_out * l), 256, 0, st>>>(Yp, ssk, a.d_out * l, Y);
     };
     auto left = [&](const uint16_t* wi) {  // Z = Delta^T Y
+        if (perr != cudaSuccess) return;
+        if (!prep(pp_lf, wi, Y, Zp, rper, kPTile)) {
+            perr = cudaErrorInvalidValue;
+            return;
+        }
         if (l <= 32)
-            left_kernel<2><<<glf, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, 64 * rs, Zp);
+            dprod_kernel<1, 8><<<glf, kPThreads, dprod_smem<1, 8>(), st>>>(pp_lf);
         else
-            left_kernel<4><<<glf, 256, 0, st>>>(wi, a.w_base, a.d_out, a.d_in, Y, l, 64 * rs, Zp);
-        sum_slices_kernel<<<blocks_for(a.d_in * l), 256, 0, st>>>(Zp, static_cast<int>(glf.y), a.d_in * l, Z);
+            dprod_kernel<1, 16><<<glf, kPThreads, dprod_smem<1, 16>(), st>>>(pp_lf);
+        sum_slices_kernel<<<blocks_for(a.d_in * l), 256, 0, st>>>(Zp, slf, a.d_in * l, Z);
     };
-    auto gram = [&](const float* A, int64_t n) {  // G = A^T A
-        gram_kernel<<<kGramBlocks, 256, 0, st>>>(A, n, l, part);
-        gram_sum_kernel<<<blocks_for(static_cast<int64_t>(l) * l), 256, 0, st>>>(part, l, G);
+    auto gram = [&](const float* A, int64_t n, double* out) {  // out = A^T A
+        if (l * l <= 1024)
+            gram_kernel<4><<<kGramBlocks, 256, 0, st>>>(A, n, l, part);
+        else
+            gram_kernel<16><<<kGramBlocks, 256, 0, st>>>(A, n, l, part);
+        gram_sum_kernel<<<blocks_for(32 * static_cast<int64_t>(l) * l), 256, 0, st>>>(part, l, out);
     };
     // A <- A R^-1 (CholeskyQR), `passes` times: two (CholeskyQR2) for the Q
     // that B is projected on, one for the intermediate bases of the power
     // iterations, where only the spanned subspace matters
     auto orth = [&](float* A, int64_t n, int passes) {
         for (int pass = 0; pass < passes; ++pass) {
-            gram(A, n);
-            chol_inv_kernel<<<1, 256, kSmallSmem, st>>>(G, l, M);
-            apply_kernel<<<blocks_for(n), 256, 0, st>>>(A, n, l, M, l, A);
+            gram(A, n, G);
+            chol_kernel<<<1, 256, 0, st>>>(G, l, M, M + kMaxL * kMaxL);
+            tri_solve_kernel<<<static_cast<unsigned>((n + 63) / 64), 64, 0, st>>>(A, n, l, M, M + kMaxL * kMaxL);
         }
     };
     if (r > 0) {
         for (int i = 0; i < a.k; ++i) {
             const uint16_t* wi = a.w_ft[i];
+            Y = Yall + static_cast<size_t>(i) * a.d_out * l;
+            Z = Zall + static_cast<size_t>(i) * a.d_in * l;
             sketch(wi, a.omega);
             orth(Y, a.d_out, a.power_iters > 0 ? 1 : 2);
             for (int it = 0; it < a.power_iters; ++it) {
@@ -584,15 +858,20 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                 sketch(wi, Z);
                 orth(Y, a.d_out, it + 1 == a.power_iters ? 2 : 1);
             }
-            left(wi);  // Z = B^T
-            gram(Z, a.d_in);                                        // B B^T
-            jacobi_kernel<<<1, 256, 0, st>>>(G, l, r, M);  // U_r [l][r]
-            apply_kernel<<<blocks_for(a.d_out), 256, 0, st>>>(Y, a.d_out, l, M, r,
-                                                              L + static_cast<size_t>(i) * a.d_out * r);
-            apply_kernel<<<blocks_for(a.d_in), 256, 0, st>>>(Z, a.d_in, l, M, r,
-                                                             Rt + static_cast<size_t>(i) * a.d_in * r);
+            left(wi);                                                    // Z = B^T
+            gram(Z, a.d_in, Gk + static_cast<size_t>(i) * l * l);        // B B^T
+        }
+        // the k projected eigenproblems at once, one CTA each
+        jacobi_kernel<<<static_cast<unsigned>(a.k), kJacobiThreads, 0, st>>>(Gk, l, r, Uk);  // U_r [l][r]
+        for (int i = 0; i < a.k; ++i) {
+            const float* Ui = Uk + static_cast<size_t>(i) * l * r;
+            apply_kernel<<<blocks_for(a.d_out * r), 256, 0, st>>>(Yall + static_cast<size_t>(i) * a.d_out * l, a.d_out,
+                                                                  l, Ui, r, L + static_cast<size_t>(i) * a.d_out * r);
+            apply_kernel<<<blocks_for(a.d_in * r), 256, 0, st>>>(Zall + static_cast<size_t>(i) * a.d_in * l, a.d_in, l,
+                                                                 Ui, r, Rt + static_cast<size_t>(i) * a.d_in * r);
         }
     }
+    if (perr != cudaSuccess) return perr;
     const dim3 grid(static_cast<unsigned>(a.d_in / 64), static_cast<unsigned>((a.d_out + 63) / 64));
     merge_kernel<<<grid, 256, 0, st>>>(a.w_base, a.d_out, a.d_in, L, Rt, r > 0 ? a.k : 0, r,
                                        1.0f / static_cast<float>(a.k), a.out, a.out_f32);

@@ -225,14 +225,16 @@ bd_status bd_materialize(const uint16_t* w_base, const uint32_t* signs, const fl
  *   w_ft      HOST array of k device pointers, each bf16 [d_out][d_in],
  *             16-byte aligned; 1 <= k <= BD_MAX_VARIANTS
  *   rank      0 (W_merged = W_base) .. l
- *   omega     device fp32 [d_in][l], 4-byte aligned (may be NULL if rank = 0)
+ *   omega     device fp32 [d_in][l], 16-byte aligned (may be NULL if rank = 0)
  *   w_merged  device [d_out][d_in], bf16 or fp32 by out_dtype, 16-byte
  *             aligned, overlapping no input and not the workspace
  *   ws        bd_monosoup_workspace_size(d_out, d_in, k, rank, l) bytes,
  *             256-byte aligned (scratch: the sketches, Gram partials and the
  *             rank-`rank` factors of every checkpoint)
- * d_in must be a positive multiple of 128 (BD_ERR_UNSUPPORTED_SHAPE);
- * out-of-range k, rank, l or power_iters (0..16) give BD_ERR_INVALID_ARG.
+ * d_in must be a positive multiple of 128 (BD_ERR_UNSUPPORTED_SHAPE); l
+ * must be a multiple of 4 (rows of the l-column operands move as 16-byte
+ * units); out-of-range k, rank, l or power_iters (0..16) give
+ * BD_ERR_INVALID_ARG.
  * Stream-ordered; the inputs must stay valid until the work completes.
  * ------------------------------------------------------------------------ */
 size_t bd_monosoup_workspace_size(int64_t d_out, int64_t d_in, int32_t k, int32_t rank, int32_t l);

@@ -145,6 +145,8 @@ def test_monosoup_argument_checks(lib):
 
     assert m(k=0) == bd.BD_ERR_INVALID_ARG
     assert m(l=65) == bd.BD_ERR_INVALID_ARG
+    assert m(l=6) == bd.BD_ERR_INVALID_ARG  # l must be a multiple of 4
+    assert m(om=A + (3 << 30) + 4) == bd.BD_ERR_MISALIGNED  # omega 16-byte aligned
     assert m(rank=9) == bd.BD_ERR_INVALID_ARG  # rank > l
     assert m(rank=-1) == bd.BD_ERR_INVALID_ARG
     assert m(q=17) == bd.BD_ERR_INVALID_ARG
