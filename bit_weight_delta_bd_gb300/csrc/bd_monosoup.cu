@@ -44,6 +44,19 @@ constexpr int kSlices = 16;       // split of the long dimension in the two prod
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
+// acc += (a, a) * m on a pair of fp32 lanes: one paired FMA instruction
+// (two independent fma.rn, the same results as two fmaf calls) issues two
+// FMAs in one instruction slot.
+__device__ __forceinline__ void ffma2(float2& acc, float a, float mx, float my)
+{
+    uint64_t ac, aa, mm;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(ac) : "f"(acc.x), "f"(acc.y));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(aa) : "f"(a));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(mm) : "f"(mx), "f"(my));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(ac) : "l"(aa), "l"(mm));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(acc.x), "=f"(acc.y) : "l"(ac));
+}
+
 // The two products with Delta on the CUDA cores (fp32 FMA).  Products
 // accurate to fp32 are needed (the subspace of the final basis moves with
 // the products' relative error, amplified by the spectral spread): a bf16
@@ -73,7 +86,8 @@ constexpr int kPThreads = 32 * (kPWarps + 1);
 struct ProdParams {
     CUtensorMap w_map;   // W_i  [d_out][d_in] bf16, box 64 x 64, 128-byte swizzle
     CUtensorMap b_map;   // W_base, same
-    const float* small;  // Omega / Z [d_in][l] (sketch) or Q [d_out][l] (transpose product)
+    CUtensorMap s_map;   // the small operand, fp32 [rows][l], box 4 L4 x 64 (zero past l and past the rows):
+                         // Omega / Z [d_in][l] (sketch) or Q [d_out][l] (transpose product)
     float* part;         // [gridDim.y][out rows][l]
     uint32_t* err;
     int64_t d_out, d_in;
@@ -97,7 +111,7 @@ __global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_consta
     constexpr int kOut = MODE == 0 ? 32 * RPL : kPTile;      // output rows of one CTA
     constexpr int kBoxRows = MODE == 0 ? 32 * RPL : kPTile;  // Delta rows per tile
     constexpr int kWTile = kBoxRows * 128;                  // one bf16 tile: kBoxRows x 64
-    constexpr int kSTile = kPTile * 4 * L4 * 4;              // 64 rows of the small operand (fp32)
+    constexpr int kSTile = kPTile * 4 * L4 * 4;              // 64 rows of the small operand (fp32, 4 L4 wide)
     constexpr int kStage = 2 * kWTile + kSTile;
     extern __shared__ uint8_t dyn_raw[];
     __shared__ uint64_t full[kPStages], empty[kPStages];
@@ -134,23 +148,22 @@ __global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_consta
         }
         return true;
     };
-    float4 acc[RPL][LH];
+    float2 acc[RPL][2 * LH];
 #pragma unroll
     for (int h = 0; h < RPL; ++h)
 #pragma unroll
-        for (int c = 0; c < LH; ++c) acc[h][c] = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    // acc += d[h] * small row (float4 columns c0 .. c0 + LH of it)
+        for (int c = 0; c < 2 * LH; ++c) acc[h][c] = make_float2(0.0f, 0.0f);
+    // acc += d[h] * small row (this warp's float4 columns c0 .. c0 + LH; the
+    // staged rows are 4 L4 floats, zero past l)
     auto fma_row = [&](const float* row, const float (&d)[RPL]) {
+        const float4* r4 = reinterpret_cast<const float4*>(row) + c0;
 #pragma unroll
         for (int c = 0; c < LH; ++c) {
-            if (4 * (c0 + c) >= l) break;
-            const float4 m = *reinterpret_cast<const float4*>(row + 4 * (c0 + c));
+            const float4 m = r4[c];
 #pragma unroll
             for (int h = 0; h < RPL; ++h) {
-                acc[h][c].x = fmaf(d[h], m.x, acc[h][c].x);
-                acc[h][c].y = fmaf(d[h], m.y, acc[h][c].y);
-                acc[h][c].z = fmaf(d[h], m.z, acc[h][c].z);
-                acc[h][c].w = fmaf(d[h], m.w, acc[h][c].w);
+                ffma2(acc[h][2 * c], d[h], m.x, m.y);
+                ffma2(acc[h][2 * c + 1], d[h], m.z, m.w);
             }
         }
     };
@@ -164,14 +177,12 @@ __global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_consta
                 break;
             uint8_t* st = ring + static_cast<size_t>(s) * kStage;
             const int64_t k0 = kb + static_cast<int64_t>(t) * kPTile;  // first reduction index of the tile
-            const int64_t kn = ke - k0 < kPTile ? ke - k0 : kPTile;     // valid rows of the small operand
             if (lane == 0) {
-                const uint32_t sbytes = static_cast<uint32_t>(kn * l * 4);
-                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(2 * kWTile) + sbytes);
+                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(kStage));
                 const int cx = static_cast<int>(MODE == 0 ? k0 : o0), cy = static_cast<int>(MODE == 0 ? o0 : k0);
                 tma_load_2d(st, &p.w_map, cx, cy, &full[s]);
                 tma_load_2d(st + kWTile, &p.b_map, cx, cy, &full[s]);
-                bulk_g2s(st + 2 * kWTile, p.small + k0 * l, sbytes, &full[s]);
+                tma_load_2d(st + 2 * kWTile, &p.s_map, 0, static_cast<int>(k0), &full[s]);
             }
             __syncwarp();
         }
@@ -189,7 +200,7 @@ __global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_consta
             const uint8_t* st = ring + static_cast<size_t>(s) * kStage;
             const int64_t k0 = kb + static_cast<int64_t>(t) * kPTile;
             const int kn = static_cast<int>(ke - k0 < kPTile ? ke - k0 : kPTile);
-            const float* sm = reinterpret_cast<const float*>(st + 2 * kWTile);  // [kn][l] as copied
+            const float* sm = reinterpret_cast<const float*>(st + 2 * kWTile);  // [64][4 L4]
             if (MODE == 0) {
                 // pair grp: columns 16 grp .. 16 grp + 15 of the tile (16-byte chunks 2 grp, 2 grp + 1)
 #pragma unroll
@@ -217,7 +228,7 @@ __global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_consta
                         float dq[RPL];
 #pragma unroll
                         for (int h = 0; h < RPL; ++h) dq[h] = d[h][q];
-                        fma_row(sm + (jj0 + q) * l, dq);
+                        fma_row(sm + (jj0 + q) * 4 * L4, dq);
                     }
                 }
             } else {
@@ -232,7 +243,7 @@ __global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_consta
                     float d[RPL];
                     d[0] = bf16_bits_to_float(a & 0xFFFFu) - bf16_bits_to_float(b & 0xFFFFu);
                     d[RPL - 1] = bf16_bits_to_float(a >> 16) - bf16_bits_to_float(b >> 16);
-                    fma_row(sm + r * l, d);
+                    fma_row(sm + r * 4 * L4, d);
                 }
             }
             __syncwarp();
@@ -249,11 +260,11 @@ __global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_consta
             for (int h = 0; h < RPL; ++h) {
                 const int row = MODE == 0 ? lane + 32 * h : 2 * lane + h;
 #pragma unroll
-                for (int c = 0; c < LH; ++c) {
-                    const float v[4] = {acc[h][c].x, acc[h][c].y, acc[h][c].z, acc[h][c].w};
+                for (int c = 0; c < 2 * LH; ++c) {
+                    const float v[2] = {acc[h][c].x, acc[h][c].y};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        float* dst = &red[row * kRS + 4 * (c0 + c) + e];
+                    for (int e = 0; e < 2; ++e) {
+                        float* dst = &red[row * kRS + 4 * c0 + 2 * c + e];
                         *dst = wv < 2 ? v[e] : *dst + v[e];  // warps 0 and 1 start the two halves
                     }
                 }
@@ -785,7 +796,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     const int ssk = slices(rblocks, a.d_in, &cper), slf = slices(cblocks, a.d_out, &rper);
     const dim3 gsk(static_cast<unsigned>(rblocks), static_cast<unsigned>(ssk));
     const dim3 glf(static_cast<unsigned>(cblocks), static_cast<unsigned>(slf));
-    auto prep = [&](ProdParams& pr, const uint16_t* wi, const float* small, float* part, int64_t per, int box_rows) {
+    auto prep = [&](ProdParams& pr, const uint16_t* wi, const float* small, int64_t small_rows, float* part, int64_t per,
+                    int box_rows) {
         if (!encode_tma_2d(&pr.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wi, static_cast<uint64_t>(a.d_in),
                            static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, kPTile,
                            static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B))
@@ -794,7 +806,10 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                            static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, kPTile,
                            static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B))
             return false;
-        pr.small = small;
+        if (!encode_tma_2d(&pr.s_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, small, static_cast<uint64_t>(l),
+                           static_cast<uint64_t>(small_rows), static_cast<uint64_t>(l) * 4, static_cast<uint32_t>(l <= 32 ? 32 : 64),
+                           kPTile, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return false;
         pr.part = part;
         pr.err = nullptr;
         pr.d_out = a.d_out;
@@ -806,7 +821,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     cudaError_t perr = cudaSuccess;
     auto sketch = [&](const uint16_t* wi, const float* om) {  // Y = Delta om
         if (perr != cudaSuccess) return;
-        if (!prep(pp_sk, wi, om, Yp, cper, sk_rows)) {
+        if (!prep(pp_sk, wi, om, a.d_in, Yp, cper, sk_rows)) {
             perr = cudaErrorInvalidValue;
             return;
         }
@@ -818,7 +833,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     };
     auto left = [&](const uint16_t* wi) {  // Z = Delta^T Y
         if (perr != cudaSuccess) return;
-        if (!prep(pp_lf, wi, Y, Zp, rper, kPTile)) {
+        if (!prep(pp_lf, wi, Y, a.d_out, Zp, rper, kPTile)) {
             perr = cudaErrorInvalidValue;
             return;
         }
