@@ -39,7 +39,8 @@ namespace bd {
 namespace {
 
 constexpr int kMaxL = 64;        // sketch width l (columns of Y, Q, B^T)
-constexpr int kGramBlocks = 608;  // CTAs of one Gram pass (fixed-order float-float partials)
+constexpr int kGramBlocks = 152;  // CTAs of one Gram pass (fixed-order float-float partials)
+constexpr int kGramThreads = 1024;
 constexpr int kSlices = 16;       // split of the long dimension in the two products with Delta
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
@@ -68,7 +69,7 @@ __device__ __forceinline__ void ffma2(float2& acc, float a, float mx, float my)
 //     loads of W_i and W_base (128-byte swizzle) and a bulk copy of the 64
 //     rows of the small operand that the tile meets (Omega / Z for the
 //     sketch: rows = Delta's columns; Q for the transpose product: rows =
-//     Delta's rows) into a ring of kPStages stages;
+//     Delta's rows) into a ring of prod_stages<L4>() stages;
 //   - eight FMA warps, as four pairs that split each stage 4 ways along its
 //     reduction index; every lane owns RPL rows (sketch) or 2 columns
 //     (transpose product) of Delta, the two warps of a pair one half each of
@@ -80,7 +81,12 @@ __device__ __forceinline__ void ffma2(float2& acc, float a, float mx, float my)
 
 constexpr int kPWarps = 8;       // FMA warps per product CTA
 constexpr int kPTile = 64;       // Delta tile per stage: 64 x 64
-constexpr int kPStages = 4;
+// ring stages and resident CTAs per SM: l <= 32 takes three CTAs of three
+// stages (six FMA warps per scheduler), l <= 64 two CTAs of four stages
+template <int L4>
+constexpr int prod_stages() { return L4 <= 8 ? 3 : 4; }
+template <int L4>
+constexpr int prod_ctas() { return L4 <= 8 ? 3 : 2; }
 constexpr int kPThreads = 32 * (kPWarps + 1);
 
 struct ProdParams {
@@ -104,7 +110,7 @@ struct ProdParams {
 // The two warps of a pair hold the two halves of the l output columns
 // (LH = L4 / 2 float4 each), so that a lane keeps 2 x 4 LH accumulators.
 template <int MODE, int L4>
-__global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_constant__ ProdParams p)
+__global__ void __launch_bounds__(kPThreads, prod_ctas<L4>()) dprod_kernel(const __grid_constant__ ProdParams p)
 {
     constexpr int LH = L4 / 2;                                // float4 output columns per warp
     constexpr int RPL = MODE == 0 ? (L4 <= 8 ? 2 : 1) : 2;  // Delta rows (columns) per lane
@@ -113,6 +119,7 @@ __global__ void __launch_bounds__(kPThreads, 2) dprod_kernel(const __grid_consta
     constexpr int kWTile = kBoxRows * 128;                  // one bf16 tile: kBoxRows x 64
     constexpr int kSTile = kPTile * 4 * L4 * 4;              // 64 rows of the small operand (fp32, 4 L4 wide)
     constexpr int kStage = 2 * kWTile + kSTile;
+    constexpr int kPStages = prod_stages<L4>();
     extern __shared__ uint8_t dyn_raw[];
     __shared__ uint64_t full[kPStages], empty[kPStages];
     __shared__ volatile int abort;
@@ -287,6 +294,7 @@ size_t dprod_smem()
     constexpr int kBoxRows = MODE == 0 ? 32 * RPL : kPTile;
     const size_t stage = 2u * kBoxRows * 128 + static_cast<size_t>(kPTile) * 4 * L4 * 4;
     const size_t red = static_cast<size_t>(MODE == 0 ? 32 * RPL : kPTile) * (4 * L4 + 1) * 4;
+    constexpr int kPStages = prod_stages<L4>();
     return (kPStages * stage > red ? kPStages * stage : red) + 1024;
 }
 
@@ -340,10 +348,10 @@ __device__ __forceinline__ void ff_add(float& s, float& c, float x, float y)
 
 // Partial Gram matrices of A [n][l]: CTA b sums A^T A over its contiguous row
 // range in float-float into part[b][l * l] (entry i * l + j as (hi, lo));
-// ENT = entries per thread (l * l <= 256 ENT).
+// ENT = entries per thread (l * l <= 1024 ENT).
 template <int ENT>
-__global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, int64_t n, int l,
-                                                   float2* __restrict__ part)
+__global__ void __launch_bounds__(kGramThreads) gram_kernel(const float* __restrict__ a, int64_t n, int l,
+                                                            float2* __restrict__ part)
 {
     __shared__ float sa[32][kMaxL + 1];
     const int tid = threadIdx.x;
@@ -355,13 +363,13 @@ __global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, 
     float s[ENT], c[ENT];
 #pragma unroll
     for (int m = 0; m < ENT; ++m) {
-        const int p = tid + 256 * m;
+        const int p = tid + kGramThreads * m;
         pi[m] = p < ll ? p / l : 0;  // past l * l: a dummy entry, never stored
         pj[m] = p < ll ? p % l : 0;
         s[m] = c[m] = 0.0f;
     }
     for (int64_t r0 = b0; r0 < b1; r0 += 32) {
-        for (int e = tid; e < 32 * kMaxL; e += 256) {
+        for (int e = tid; e < 32 * kMaxL; e += kGramThreads) {
             const int rr = e >> 6, cc = e & 63;
             const int64_t row = r0 + rr;
             sa[rr][cc] = (row < b1 && cc < l) ? a[row * l + cc] : 0.0f;
@@ -376,7 +384,7 @@ __global__ void __launch_bounds__(256) gram_kernel(const float* __restrict__ a, 
     }
 #pragma unroll
     for (int m = 0; m < ENT; ++m) {
-        const int p = tid + 256 * m;
+        const int p = tid + kGramThreads * m;
         if (p < ll) {
             float hi, lo;
             two_sum(s[m], c[m], hi, lo);
@@ -491,6 +499,7 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const double* __
     __shared__ float V[kMaxL][kMaxL + 1];
     __shared__ float cs[kMaxL / 2], sn[kMaxL / 2];
     __shared__ int pp[kMaxL / 2], qq[kMaxL / 2];
+    __shared__ unsigned char tp[kMaxL][kMaxL / 2], tq[kMaxL][kMaxL / 2];  // round-robin pairs of every round
     __shared__ float red[2][32];
     __shared__ int idx[kMaxL];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -502,6 +511,20 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const double* __
     __syncthreads();
     const int n = l + (l & 1);
     const int h = n / 2;
+    for (int e = tid; e < (n - 1) * h; e += kJacobiThreads) {  // the pair schedule, once
+        const int t = e / h, i = e - t * h;
+        const int a = i == 0 ? 0 : 1 + (i - 1 + t) % (n - 1);
+        const int b = 1 + (n - 2 - i + t) % (n - 1);
+        tp[t][i] = static_cast<unsigned char>(a < b ? a : b);
+        tq[t][i] = static_cast<unsigned char>(a < b ? b : a);
+    }
+    // this thread's 2 x 2 blocks (bi, bj) and V items (row, bj), fixed for the kernel
+    const int nb = h * h, nv = l * h;
+    const int ab = tid < nb ? tid / h : 0, bb = tid < nb ? tid - ab * h : 0;
+    const int av0 = tid < nv ? tid / h : 0, bv0 = tid < nv ? tid - av0 * h : 0;
+    const int e1 = tid + kJacobiThreads;
+    const int av1 = e1 < nv ? e1 / h : 0, bv1 = e1 < nv ? e1 - av1 * h : 0;
+    __syncthreads();
     for (int sweep = 0; sweep < 40; ++sweep) {
         float off = 0.0f, dia = 0.0f;
         for (int e = tid; e < kMaxL * kMaxL; e += kJacobiThreads) {
@@ -531,9 +554,7 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const double* __
         if (!(toff > 1e-12f * tdia)) break;
         for (int t = 0; t + 1 < n; ++t) {
             if (tid < h) {
-                const int a = tid == 0 ? 0 : 1 + (tid - 1 + t) % (n - 1);
-                const int b = 1 + (n - 2 - tid + t) % (n - 1);
-                const int p = a < b ? a : b, q = a < b ? b : a;
+                const int p = tp[t][tid], q = tq[t][tid];
                 float c = 1.0f, sv = 0.0f;
                 if (q < l) {
                     const float apq = A[p][q];
@@ -551,8 +572,8 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const double* __
             }
             __syncthreads();
             // A: block (pair bi rows, pair bj columns); columns first (A P), then rows (P^T .)
-            for (int e = tid; e < h * h; e += kJacobiThreads) {
-                const int bi = e / h, bj = e - (e / h) * h;
+            if (tid < nb) {
+                const int bi = ab, bj = bb;
                 const int p = pp[bi], q = qq[bi], p2 = pp[bj], q2 = qq[bj];
                 const float ci = cs[bi], si = sn[bi], cj = cs[bj], sj = sn[bj];
                 const bool rq = q < l, cq = q2 < l;
@@ -565,9 +586,12 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const double* __
                 if (rq) A[q][p2] = si * x_pp + ci * x_qp;
                 if (rq && cq) A[q][q2] = si * x_pq + ci * x_qq;
             }
-            // V: (row, column pair bj)
-            for (int e = tid; e < l * h; e += kJacobiThreads) {
-                const int row = e / h, bj = e - (e / h) * h;
+            // V: (row, column pair bj), at most two items per thread
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int e = tid + u * kJacobiThreads;
+                if (e >= nv) break;
+                const int row = u == 0 ? av0 : av1, bj = u == 0 ? bv0 : bv1;
                 const int p2 = pp[bj], q2 = qq[bj];
                 if (q2 >= l) continue;
                 const float cj = cs[bj], sj = sn[bj];
@@ -625,77 +649,115 @@ __global__ void __launch_bounds__(64) tri_solve_kernel(float* a, int64_t n, int 
         if (j < l) a[row * l + j] = x[j];
 }
 
-// dst[row][j] = sum_c src[row][c] * M[c][j]  (c < l, j < m): one output
-// element per thread (src and dst distinct).
-__global__ void __launch_bounds__(256) apply_kernel(const float* __restrict__ src, int64_t n, int l,
-                                                    const float* __restrict__ M, int m, float* __restrict__ dst)
+// dst[j][row] = sum_c src[row][c] * M[c][j]  (c < l, j < m), written
+// transposed (the merge reads the factors of consecutive rows contiguously).
+// One thread per row and group of four outputs j: it reads its row with
+// 16-byte loads (l is a multiple of 4) and writes four coalesced columns.
+__global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ src, int64_t n, int l,
+                                                      const float* __restrict__ M, int m, float* __restrict__ dst)
 {
-    __shared__ float sm[kMaxL][kMaxL];
+    __shared__ __align__(16) float sm[kMaxL][kMaxL];
     for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
         const int c = e >> 6, j = e & 63;
         sm[c][j] = (c < l && j < m) ? M[c * m + j] : 0.0f;
     }
     __syncthreads();
     const int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (o >= n * m) return;
-    const int64_t row = o / m;
-    const int j = static_cast<int>(o - row * m);
-    const float* s = src + row * l;
-    float acc = 0.0f;
-    for (int c = 0; c < l; ++c) acc = fmaf(s[c], sm[c][j], acc);
-    dst[o] = acc;
+    const int jg = static_cast<int>(o / n);
+    const int64_t row = o - static_cast<int64_t>(jg) * n;
+    if (4 * jg >= m) return;
+    const float4* s = reinterpret_cast<const float4*>(src + row * l);
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    for (int c4 = 0; c4 < l / 4; ++c4) {
+        const float4 v = s[c4];
+        const float sv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            const float4 mv = *reinterpret_cast<const float4*>(&sm[4 * c4 + cc][4 * jg]);
+            acc[0] = fmaf(sv[cc], mv.x, acc[0]);
+            acc[1] = fmaf(sv[cc], mv.y, acc[1]);
+            acc[2] = fmaf(sv[cc], mv.z, acc[2]);
+            acc[3] = fmaf(sv[cc], mv.w, acc[3]);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+        if (4 * jg + t < m) dst[static_cast<int64_t>(4 * jg + t) * n + row] = acc[t];
 }
 
 // out[row][j] = W_base[row][j] + inv_k * sum_e L[e][row] Rt[e][j], e over the
-// k * r factor columns (L [k][d_out][r], Rt [k][d_in][r]); 64 x 64 outputs per
-// CTA, 4 x 4 per thread, factor columns in chunks of 32.
-__global__ void __launch_bounds__(256) merge_kernel(const uint16_t* __restrict__ wb, int64_t d_out, int64_t d_in,
-                                                    const float* __restrict__ L, const float* __restrict__ Rt, int k,
-                                                    int r, float inv_k, void* __restrict__ out, int out_f32)
+// k * r factor columns (L [k r][d_out], Rt [k r][d_in]).  CTA: 128 x 128
+// outputs, 8 x 8 per thread: rows 8 ty .. 8 ty + 7, columns 4 tx .. 4 tx + 3
+// and 64 + 4 tx .. (so that the 16-byte reads of a quarter warp cover the 32
+// banks once).  The factors of its rows and columns are staged in shared
+// memory k-major with coalesced loads, in chunks of 48 factor columns;
+// paired FMAs.  The sum runs over e in order; the result is rounded once to
+// the output type.
+constexpr int kMergeTile = 128;
+constexpr int kMergeK = 48;
+
+__global__ void __launch_bounds__(256, 2) merge_kernel(const uint16_t* __restrict__ wb, int64_t d_out, int64_t d_in,
+                                                       const float* __restrict__ L, const float* __restrict__ Rt, int k,
+                                                       int r, float inv_k, void* __restrict__ out, int out_f32)
 {
-    __shared__ float sl[64][33];
-    __shared__ float sr[64][33];
-    const int tid = threadIdx.x;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * 64, j0 = static_cast<int64_t>(blockIdx.x) * 64;
-    const int tr = (tid >> 4) * 4, tc = (tid & 15) * 4;
-    float acc[4][4] = {};
+    __shared__ __align__(16) float sl[kMergeK][kMergeTile];
+    __shared__ __align__(16) float sr[kMergeK][kMergeTile];
+    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kMergeTile, j0 = static_cast<int64_t>(blockIdx.x) * kMergeTile;
+    float2 acc[8][4];
+#pragma unroll
+    for (int x = 0; x < 8; ++x)
+#pragma unroll
+        for (int y = 0; y < 4; ++y) acc[x][y] = make_float2(0.0f, 0.0f);
     const int K = k * r;
-    for (int e0 = 0; e0 < K; e0 += 32) {
-        for (int e = tid; e < 64 * 32; e += 256) {
-            const int rr = e >> 5, ee = e & 31, f = e0 + ee;
-            const int fi = f / (r > 0 ? r : 1), fc = f - fi * r;
-            const int64_t row = r0 + rr, col = j0 + rr;
-            sl[rr][ee] = (f < K && row < d_out) ? L[(static_cast<int64_t>(fi) * d_out + row) * r + fc] : 0.0f;
-            sr[rr][ee] = (f < K && col < d_in) ? Rt[(static_cast<int64_t>(fi) * d_in + col) * r + fc] : 0.0f;
-        }
+    const int rr = tid & (kMergeTile - 1), e_lo = tid >> 7;
+    for (int e0 = 0; e0 < K; e0 += kMergeK) {
         __syncthreads();
+        const int64_t row = r0 + rr, col = j0 + rr;
 #pragma unroll 4
-        for (int ee = 0; ee < 32; ++ee) {
-            float a[4], b[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-                a[x] = sl[tr + x][ee];
-                b[x] = sr[tc + x][ee];
-            }
-#pragma unroll
-            for (int x = 0; x < 4; ++x)
-#pragma unroll
-                for (int y = 0; y < 4; ++y) acc[x][y] = fmaf(a[x], b[y], acc[x][y]);
+        for (int ee = e_lo; ee < kMergeK; ee += 2) {
+            const int f = e0 + ee;
+            sl[ee][rr] = (f < K && row < d_out) ? L[static_cast<int64_t>(f) * d_out + row] : 0.0f;
+            sr[ee][rr] = (f < K && col < d_in) ? Rt[static_cast<int64_t>(f) * d_in + col] : 0.0f;
         }
         __syncthreads();
+        const int ne = K - e0 < kMergeK ? K - e0 : kMergeK;
+        for (int ee = 0; ee < ne; ++ee) {
+            const float4 a0 = *reinterpret_cast<const float4*>(&sl[ee][8 * ty]);
+            const float4 a1 = *reinterpret_cast<const float4*>(&sl[ee][8 * ty + 4]);
+            const float4 b0 = *reinterpret_cast<const float4*>(&sr[ee][4 * tx]);
+            const float4 b1 = *reinterpret_cast<const float4*>(&sr[ee][64 + 4 * tx]);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int x = 0; x < 8; ++x) {
+                ffma2(acc[x][0], av[x], b0.x, b0.y);
+                ffma2(acc[x][1], av[x], b0.z, b0.w);
+                ffma2(acc[x][2], av[x], b1.x, b1.y);
+                ffma2(acc[x][3], av[x], b1.z, b1.w);
+            }
+        }
     }
 #pragma unroll
-    for (int x = 0; x < 4; ++x) {
-        const int64_t row = r0 + tr + x;
+    for (int x = 0; x < 8; ++x) {
+        const int64_t row = r0 + 8 * ty + x;
         if (row >= d_out) continue;
 #pragma unroll
-        for (int y = 0; y < 4; ++y) {
-            const int64_t col = j0 + tc + y;
-            const float v = bf16_bits_to_float(wb[row * d_in + col]) + inv_k * acc[x][y];
-            if (out_f32)
-                static_cast<float*>(out)[row * d_in + col] = v;
-            else
-                static_cast<__nv_bfloat16*>(out)[row * d_in + col] = __float2bfloat16_rn(v);
+        for (int h = 0; h < 2; ++h) {
+            const int64_t col = j0 + 64 * h + 4 * tx;
+            const uint2 w = *reinterpret_cast<const uint2*>(wb + row * d_in + col);
+            const float v0 = bf16_bits_to_float(w.x & 0xFFFFu) + inv_k * acc[x][2 * h].x;
+            const float v1 = bf16_bits_to_float(w.x >> 16) + inv_k * acc[x][2 * h].y;
+            const float v2 = bf16_bits_to_float(w.y & 0xFFFFu) + inv_k * acc[x][2 * h + 1].x;
+            const float v3 = bf16_bits_to_float(w.y >> 16) + inv_k * acc[x][2 * h + 1].y;
+            if (out_f32) {
+                *reinterpret_cast<float4*>(static_cast<float*>(out) + row * d_in + col) = make_float4(v0, v1, v2, v3);
+            } else {
+                const uint32_t o0 = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v0))) |
+                                    (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v1))) << 16);
+                const uint32_t o1 = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v2))) |
+                                    (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v3))) << 16);
+                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + row * d_in + col) = make_uint2(o0, o1);
+            }
         }
     }
 }
@@ -770,15 +832,15 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     const int l = a.l, r = a.rank;
     // the two products with Delta: CTAs of 64 rows (or 32, l > 32) / 64
     // columns of Delta, the reduction dimension split in gridDim.y slices (so
-    // that every SM gets about two CTAs), the slices summed in order
+    // that every SM gets its resident CTAs), the slices summed in order
     const int sms = a.sm_count > 0 ? a.sm_count : 152;
     static thread_local ProdParams pp_sk, pp_lf;
     const int sk_rows = l <= 32 ? 64 : 32;
     const int64_t rblocks = (a.d_out + sk_rows - 1) / sk_rows, cblocks = a.d_in / kPTile;
-    // slices: the smallest count whose CTAs fill whole waves of two CTAs per SM
+    // slices: the smallest count whose CTAs fill whole waves of resident CTAs
     // to within an eighth (else the count nearest three waves), at most kSlices
     auto slices = [&](int64_t blocks, int64_t klen, int64_t* per) {
-        const int64_t wave = 2 * static_cast<int64_t>(sms);
+        const int64_t wave = static_cast<int64_t>(l <= 32 ? prod_ctas<8>() : prod_ctas<16>()) * sms;
         int ns = 1;
         for (int c = 1; c <= kSlices; ++c) {
             const int64_t ctas = blocks * c;
@@ -844,10 +906,10 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         sum_slices_kernel<<<blocks_for(a.d_in * l), 256, 0, st>>>(Zp, slf, a.d_in * l, Z);
     };
     auto gram = [&](const float* A, int64_t n, double* out) {  // out = A^T A
-        if (l * l <= 1024)
-            gram_kernel<4><<<kGramBlocks, 256, 0, st>>>(A, n, l, part);
+        if (l * l <= kGramThreads)
+            gram_kernel<1><<<kGramBlocks, kGramThreads, 0, st>>>(A, n, l, part);
         else
-            gram_kernel<16><<<kGramBlocks, 256, 0, st>>>(A, n, l, part);
+            gram_kernel<4><<<kGramBlocks, kGramThreads, 0, st>>>(A, n, l, part);
         gram_sum_kernel<<<blocks_for(32 * static_cast<int64_t>(l) * l), 256, 0, st>>>(part, l, out);
     };
     // A <- A R^-1 (CholeskyQR), `passes` times: two (CholeskyQR2) for the Q
@@ -880,14 +942,16 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         jacobi_kernel<<<static_cast<unsigned>(a.k), kJacobiThreads, 0, st>>>(Gk, l, r, Uk);  // U_r [l][r]
         for (int i = 0; i < a.k; ++i) {
             const float* Ui = Uk + static_cast<size_t>(i) * l * r;
-            apply_kernel<<<blocks_for(a.d_out * r), 256, 0, st>>>(Yall + static_cast<size_t>(i) * a.d_out * l, a.d_out,
-                                                                  l, Ui, r, L + static_cast<size_t>(i) * a.d_out * r);
-            apply_kernel<<<blocks_for(a.d_in * r), 256, 0, st>>>(Zall + static_cast<size_t>(i) * a.d_in * l, a.d_in, l,
-                                                                 Ui, r, Rt + static_cast<size_t>(i) * a.d_in * r);
+            apply_t_kernel<<<blocks_for(a.d_out * ((r + 3) / 4)), 256, 0, st>>>(Yall + static_cast<size_t>(i) * a.d_out * l,
+                                                                    a.d_out, l, Ui, r,
+                                                                    L + static_cast<size_t>(i) * a.d_out * r);
+            apply_t_kernel<<<blocks_for(a.d_in * ((r + 3) / 4)), 256, 0, st>>>(Zall + static_cast<size_t>(i) * a.d_in * l, a.d_in,
+                                                                   l, Ui, r, Rt + static_cast<size_t>(i) * a.d_in * r);
         }
     }
     if (perr != cudaSuccess) return perr;
-    const dim3 grid(static_cast<unsigned>(a.d_in / 64), static_cast<unsigned>((a.d_out + 63) / 64));
+    const dim3 grid(static_cast<unsigned>((a.d_in + kMergeTile - 1) / kMergeTile),
+                    static_cast<unsigned>((a.d_out + kMergeTile - 1) / kMergeTile));
     merge_kernel<<<grid, 256, 0, st>>>(a.w_base, a.d_out, a.d_in, L, Rt, r > 0 ? a.k : 0, r,
                                        1.0f / static_cast<float>(a.k), a.out, a.out_f32);
     return cudaGetLastError();
