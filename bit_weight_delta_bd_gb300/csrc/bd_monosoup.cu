@@ -14,17 +14,19 @@
 //   tau = (Q U_r) (U_r^T B)    (U_r: the r leading eigenvectors)
 // which is U_r S_r V_r^T of the rank-l approximation Q Q^T Delta.  Every pass
 // over Delta reads W_i and W_base (bf16) and forms Delta in fp32 on the fly.
-// Orthonormalisation is CholeskyQR: the Gram matrix is accumulated in
-// float-float, factored in fp64 in one CTA, and Y <- Y R^-1 applied by
+// Orthonormalisation is CholeskyQR: the Gram matrix is accumulated and
+// factored in float-float (one CTA per checkpoint), and Y <- Y R^-1 applied by
 // forward substitution (twice, CholeskyQR2, for the final basis); directions
 // whose pivot falls below 1e-12 of the largest are dropped (rank-deficient
 // sketches).
 // The merge is one pass: W_base + (1/k) [L_1 .. L_k][R_1 .. R_k]^T with
 // L_i = Q_i U_r, R_i = B_i^T U_r, rounded once to the output type.
 //
-// All arithmetic is fp32 on the CUDA cores except the Gram matrices
-// (float-float) and the Cholesky factor (fp64).  No kernel waits on another CTA; the passes are
-// plain stream-ordered launches.
+// All arithmetic is fp32 on the CUDA cores except the Gram matrices and the
+// Cholesky factor (float-float, on the same fp32 units).  Up to kMaxBatch
+// checkpoints go through every step together (one launch per step, the
+// checkpoint in the last grid dimension).  No kernel waits on another CTA;
+// the passes are plain stream-ordered launches.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -41,7 +43,8 @@ namespace {
 constexpr int kMaxL = 64;        // sketch width l (columns of Y, Q, B^T)
 constexpr int kGramBlocks = 152;  // CTAs of one Gram pass (fixed-order float-float partials)
 constexpr int kGramThreads = 1024;
-constexpr int kSlices = 16;       // split of the long dimension in the two products with Delta
+constexpr int kSlices = 16;       // partial results of one product pass (over the checkpoints of a batch)
+constexpr int kMaxBatch = 8;      // checkpoints that go through the steps together
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
@@ -90,21 +93,22 @@ constexpr int prod_ctas() { return L4 <= 8 ? 3 : 2; }
 constexpr int kPThreads = 32 * (kPWarps + 1);
 
 struct ProdParams {
-    CUtensorMap w_map;   // W_i  [d_out][d_in] bf16, box 64 x 64, 128-byte swizzle
-    CUtensorMap b_map;   // W_base, same
-    CUtensorMap s_map;   // the small operand, fp32 [rows][l], box 4 L4 x 64 (zero past l and past the rows):
-                         // Omega / Z [d_in][l] (sketch) or Q [d_out][l] (transpose product)
-    float* part;         // [gridDim.y][out rows][l]
+    CUtensorMap b_map;               // W_base [d_out][d_in] bf16, box 64 x 64, 128-byte swizzle
+    CUtensorMap w_map[kMaxBatch];    // W_i of checkpoint blockIdx.z, same
+    CUtensorMap s_map[kMaxBatch];    // its small operand, fp32 [rows][l], box 4 L4 x 64 (zero past l and
+                                     // past the rows): Omega / Z [d_in][l] (sketch) or Q [d_out][l]
+    float* part;         // [gridDim.z][gridDim.y][out rows][l]
     uint32_t* err;
     int64_t d_out, d_in;
     int l;
     int64_t k_per;       // reduction indices per slice (a multiple of 64)
 };
 
-// MODE 0: part[s][row][c] = sum over slice s of j of Delta[row][j] small[j][c]
+// Checkpoint z = blockIdx.z of the batch:
+// MODE 0: part[z][s][row][c] = sum over slice s of j of Delta[row][j] small[j][c]
 //         (CTA: 32 RPL rows of Delta; lane: rows lane + 32 h, h < RPL; warp
 //         pair cg = warp / 2 takes columns 16 cg .. 16 cg + 15 of each tile)
-// MODE 1: part[s][j][c] = sum over slice s of rows of Delta[row][j] small[row][c]
+// MODE 1: part[z][s][j][c] = sum over slice s of rows of Delta[row][j] small[row][c]
 //         (CTA: 64 columns of Delta; lane: columns 2 lane, 2 lane + 1; warp
 //         pair rg = warp / 2 takes rows 16 rg .. 16 rg + 15 of each tile)
 // The two warps of a pair hold the two halves of the l output columns
@@ -187,9 +191,9 @@ __global__ void __launch_bounds__(kPThreads, prod_ctas<L4>()) dprod_kernel(const
             if (lane == 0) {
                 mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(kStage));
                 const int cx = static_cast<int>(MODE == 0 ? k0 : o0), cy = static_cast<int>(MODE == 0 ? o0 : k0);
-                tma_load_2d(st, &p.w_map, cx, cy, &full[s]);
+                tma_load_2d(st, &p.w_map[blockIdx.z], cx, cy, &full[s]);
                 tma_load_2d(st + kWTile, &p.b_map, cx, cy, &full[s]);
-                tma_load_2d(st + 2 * kWTile, &p.s_map, 0, static_cast<int>(k0), &full[s]);
+                tma_load_2d(st + 2 * kWTile, &p.s_map[blockIdx.z], 0, static_cast<int>(k0), &full[s]);
             }
             __syncwarp();
         }
@@ -280,7 +284,7 @@ __global__ void __launch_bounds__(kPThreads, prod_ctas<L4>()) dprod_kernel(const
         __syncthreads();
     }
     const int64_t nrows = MODE == 0 ? p.d_out : p.d_in;
-    float* out = p.part + static_cast<int64_t>(blockIdx.y) * nrows * l;
+    float* out = p.part + (static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * nrows * l;
     for (int e = tid; e < kOut * l; e += kPThreads) {
         const int rr = e / l, c = e - rr * l;
         if (o0 + rr < nrows) out[(o0 + rr) * l + c] = red[rr * kRS + c];
@@ -298,23 +302,25 @@ size_t dprod_smem()
     return (kPStages * stage > red ? kPStages * stage : red) + 1024;
 }
 
-// out[e] = sum_s part[s][e], e < n (fixed order).
+// out[z][e] = sum_s part[z][s][e], e < n, for the gridDim.y checkpoints z
+// (fixed order).
 __global__ void __launch_bounds__(256) sum_slices_kernel(const float* __restrict__ part, int nslice, int64_t n,
                                                          float* __restrict__ out)
 {
     const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (e >= n) return;
-    float s = part[e];
-    for (int k = 1; k < nslice; ++k) s += part[k * n + e];
-    out[e] = s;
+    const float* pz = part + static_cast<int64_t>(blockIdx.y) * nslice * n;
+    float s = pz[e];
+    for (int k = 1; k < nslice; ++k) s += pz[k * n + e];
+    out[static_cast<int64_t>(blockIdx.y) * n + e] = s;
 }
 
 // ---------------------------------------------------------------- small-matrix steps
-// GB300 has few fp64 units (about 2 fp64 FMAs per cycle per SM), so the Gram
-// matrices are accumulated in float-float arithmetic on the fp32 units (each
-// product split exactly with an FMA, each sum with TwoSum; about 2^-44
-// relative, like fp64 for this purpose), and only the l x l Cholesky factor
-// is computed in fp64.
+// GB300 has few fp64 units (about 2 fp64 FMAs per cycle per SM, with long
+// latencies), so the Gram matrices and their Cholesky factors are computed in
+// float-float arithmetic on the fp32 units (each product split exactly with
+// an FMA, each sum with TwoSum; about 2^-44 relative, like fp64 for this
+// purpose).
 
 // s + t = a + b exactly (Knuth's TwoSum; explicit _rn intrinsics so that no
 // operation is contracted or reordered).
@@ -346,16 +352,19 @@ __device__ __forceinline__ void ff_add(float& s, float& c, float x, float y)
     c = __fadd_rn(c, __fadd_rn(e, y));
 }
 
-// Partial Gram matrices of A [n][l]: CTA b sums A^T A over its contiguous row
-// range in float-float into part[b][l * l] (entry i * l + j as (hi, lo));
-// ENT = entries per thread (l * l <= 1024 ENT).
+// Partial Gram matrices of A_z [n][l] (checkpoint z = blockIdx.y, the A_z
+// consecutive): CTA b sums A_z^T A_z over its contiguous row range in
+// float-float into part[z][b][l * l] (entry i * l + j as (hi, lo)); ENT =
+// entries per thread (l * l <= 1024 ENT).
 template <int ENT>
-__global__ void __launch_bounds__(kGramThreads) gram_kernel(const float* __restrict__ a, int64_t n, int l,
-                                                            float2* __restrict__ part)
+__global__ void __launch_bounds__(kGramThreads) gram_kernel(const float* __restrict__ a_all, int64_t n, int l,
+                                                            float2* __restrict__ part_all)
 {
     __shared__ float sa[32][kMaxL + 1];
     const int tid = threadIdx.x;
-    const int64_t per = (n + kGramBlocks - 1) / kGramBlocks;
+    const float* a = a_all + static_cast<int64_t>(blockIdx.y) * n * l;
+    float2* part = part_all + static_cast<int64_t>(blockIdx.y) * gridDim.x * l * l;
+    const int64_t per = (n + gridDim.x - 1) / gridDim.x;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * per;
     const int64_t b1 = b0 + per < n ? b0 + per : n;
     const int ll = l * l;
@@ -393,22 +402,25 @@ __global__ void __launch_bounds__(kGramThreads) gram_kernel(const float* __restr
     }
 }
 
-// G[e] = sum_b part[b][e] (float-float, then exactly to fp64), one warp per
+// G[z][e] = sum_b part[z][b][e], b < nb (float-float, normalised to
+// (hi, lo) with |lo| <= ulp(hi) / 2), checkpoint z = blockIdx.y, one warp per
 // entry: lane L takes partials L, L + 32, ... in order, then a fixed
 // butterfly; the result does not depend on timing.
-__global__ void __launch_bounds__(256) gram_sum_kernel(const float2* __restrict__ part, int l, double* __restrict__ G)
+__global__ void __launch_bounds__(256) gram_sum_kernel(const float2* __restrict__ part_all, int nb, int l,
+                                                       float2* __restrict__ G_all)
 {
     const int e = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     const int ll = l * l;
     if (e >= ll) return;
+    const float2* part = part_all + static_cast<int64_t>(blockIdx.y) * nb * ll;
     // four independent float-float chains per lane (partials lane + 32 (4 i + u)), then fixed combines
     float s[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int b = lane; b < kGramBlocks; b += 128) {
+    for (int b = lane; b < nb; b += 128) {
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
             const int bb = b + 32 * u;
-            if (bb < kGramBlocks) {
+            if (bb < nb) {
                 const float2 v = part[static_cast<int64_t>(bb) * ll + e];
                 ff_add(s[u], c[u], v.x, v.y);
             }
@@ -423,92 +435,162 @@ __global__ void __launch_bounds__(256) gram_sum_kernel(const float2* __restrict_
         const float os = __shfl_xor_sync(0xffffffffu, sv, o), oc = __shfl_xor_sync(0xffffffffu, cv, o);
         ff_add(sv, cv, os, oc);  // fixed butterfly: lane 0's sum does not depend on timing
     }
-    if (lane == 0) G[e] = static_cast<double>(sv) + static_cast<double>(cv);
+    if (lane == 0) {
+        float hi, lo;
+        two_sum(sv, cv, hi, lo);
+        G_all[static_cast<int64_t>(blockIdx.y) * ll + e] = make_float2(hi, lo);
+    }
 }
 
-// One CTA: G = R^T R (Cholesky, R upper) in fp64; R written as fp32 [l][l]
-// (zero below the diagonal) with the reciprocals of its diagonal in rinv.
-// 1/sqrt(d) comes from the fp32 rsqrt and two Newton steps in fp64 (about
-// 2^-46; fp64 square roots and divisions are long sequences on GB300's few
-// fp64 units).  A pivot below 1e-12 of the largest diagonal entry drops its
-// direction (its row of R and its reciprocal are zero).
-__global__ void __launch_bounds__(256) chol_kernel(const double* __restrict__ G, int l, float* __restrict__ Rf,
-                                                   float* __restrict__ rinv)
+// s + t = a + b exactly when |a| >= |b| or a = 0 (Dekker's Fast2Sum).
+__device__ __forceinline__ void fast_two_sum(float a, float b, float& s, float& t)
 {
-    __shared__ double g[kMaxL][kMaxL + 1];
-    __shared__ double dmax, s_inv;
-    __shared__ double rdiag[kMaxL];
+    s = __fadd_rn(a, b);
+    t = __fsub_rn(b, __fsub_rn(s, a));
+}
+
+// (ph, pl) = (ah + al) (bh + bl) in float-float (the al bl term, below
+// 2^-48 of the product, is left out), normalised.
+__device__ __forceinline__ void ff_mul(float ah, float al, float bh, float bl, float& ph, float& pl)
+{
+    const float p = __fmul_rn(ah, bh);
+    float e = __fmaf_rn(ah, bh, -p);
+    e = __fmaf_rn(ah, bl, e);
+    e = __fmaf_rn(al, bh, e);
+    fast_two_sum(p, e, ph, pl);
+}
+
+// (h, l) += (xh, xl) in float-float, normalised.
+__device__ __forceinline__ void ff_add_norm(float& h, float& l, float xh, float xl)
+{
+    float s, e;
+    two_sum(h, xh, s, e);
+    fast_two_sum(s, __fadd_rn(e, __fadd_rn(l, xl)), h, l);
+}
+
+// One CTA per checkpoint (blockIdx.x): G = R^T R (Cholesky, R upper) in
+// float-float, right-looking; R written as fp32 [l][l] (zero below the
+// diagonal) with the reciprocals of its diagonal in rinv (Rf of checkpoint z
+// at Rf_all + z (kMaxL^2 + kMaxL), rinv right after its kMaxL^2 floats).
+// Pivot d: y = rsqrt(d_hi) (fp32, about 2^-22), s0 = d_hi y, one Newton step
+// s = s0 + (d - s0^2) y / 2 with d - s0^2 formed exactly (Sterbenz and an
+// FMA), then 1/s by one Newton step from y; both within about 2^-42.  Warp 0 takes the pivot (every lane the same
+// values) and scales row k by 1/s; the CTA then updates the trailing upper
+// triangle.  A pivot below 1e-12 of the largest diagonal entry drops its
+// direction (its row of R and its reciprocal are zero).
+__global__ void __launch_bounds__(256) chol_kernel(const float2* __restrict__ G_all, int l, float* __restrict__ Rf_all)
+{
+    __shared__ float2 g[kMaxL][kMaxL + 1];
+    __shared__ float rdiag[kMaxL];
     __shared__ int live[kMaxL];
-    const int tid = threadIdx.x;
+    __shared__ float dmax;
+    const float2* G = G_all + static_cast<int64_t>(blockIdx.x) * l * l;
+    float* Rf = Rf_all + static_cast<int64_t>(blockIdx.x) * (kMaxL * kMaxL + kMaxL);
+    float* rinv = Rf + kMaxL * kMaxL;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ti = tid >> 4, tj = tid & 15;
-    for (int i = ti; i < kMaxL; i += 16)
-        for (int j = tj; j < kMaxL; j += 16) g[i][j] = (i < l && j < l) ? G[i * l + j] : 0.0;
+    for (int e = tid; e < l * l; e += 256) g[e / l][e % l] = G[e];
     __syncthreads();
-    if (tid < 32) {
-        double m = 0.0;
-        for (int i = tid; i < l; i += 32) m = fmax(m, g[i][i]);
+    if (warp == 0) {
+        float m = 0.0f;
+        for (int i = lane; i < l; i += 32) m = fmaxf(m, g[i][i].x);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (tid == 0) dmax = m;
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) dmax = m;
     }
     __syncthreads();
-    const double tol = 1e-12 * dmax;
+    const float tol = 1e-12f * dmax;
     for (int k = 0; k < l; ++k) {
-        if (tid == 0) {
-            const double d = g[k][k];
-            const bool ok = d > tol && d > 0.0;
-            double y = ok ? static_cast<double>(rsqrtf(static_cast<float>(d))) : 0.0;
-            y = y * fma(-0.5 * d * y, y, 1.5);
-            y = y * fma(-0.5 * d * y, y, 1.5);
-            g[k][k] = ok ? d * y : 0.0;
-            s_inv = ok ? y : 0.0;
-            rdiag[k] = s_inv;
-            live[k] = ok ? 1 : 0;
+        if (warp == 0) {
+            const float dh = g[k][k].x, dl = g[k][k].y;
+            const bool ok = dh > tol && dh > 0.0f;
+            float sh = 0.0f, sl = 0.0f, ih = 0.0f, il = 0.0f;
+            if (ok) {
+                const float y = rsqrtf(dh);
+                const float s0 = __fmul_rn(dh, y);
+                const float p = __fmul_rn(s0, s0), pe = __fmaf_rn(s0, s0, -p);
+                const float res = __fadd_rn(__fsub_rn(__fsub_rn(dh, p), pe), dl);  // d - s0^2
+                fast_two_sum(s0, __fmul_rn(__fmul_rn(0.5f, res), y), sh, sl);
+                float t = __fmaf_rn(-sh, y, 1.0f);  // 1 - s y
+                t = __fmaf_rn(-sl, y, t);
+                fast_two_sum(y, __fmul_rn(y, t), ih, il);
+            }
+            for (int j = k + 1 + lane; j < l; j += 32) {
+                float2 v = g[k][j];
+                ff_mul(v.x, v.y, ih, il, v.x, v.y);
+                g[k][j] = v;
+            }
+            if (lane == 0) {
+                g[k][k] = make_float2(sh, sl);
+                rdiag[k] = ih;
+                live[k] = ok ? 1 : 0;
+            }
         }
         __syncthreads();
-        for (int j = k + 1 + tid; j < l; j += 256) g[k][j] *= s_inv;
-        __syncthreads();
-        for (int i = k + 1 + ti; i < l; i += 16)
-            for (int j = i + ((tj - i) & 15); j < l; j += 16) g[i][j] = fma(-g[k][i], g[k][j], g[i][j]);
+        for (int i = k + 1 + ti; i < l; i += 16) {
+            const float2 a = g[k][i];
+            for (int j = i + ((tj - i) & 15); j < l; j += 16) {
+                const float2 b = g[k][j];
+                float ph, pl;
+                ff_mul(a.x, a.y, b.x, b.y, ph, pl);
+                float2 v = g[i][j];
+                ff_add_norm(v.x, v.y, -ph, -pl);
+                g[i][j] = v;
+            }
+        }
         __syncthreads();
     }
-    for (int i = ti; i < l; i += 16)
-        for (int j = tj; j < l; j += 16) Rf[i * l + j] = (j >= i && live[i]) ? static_cast<float>(g[i][j]) : 0.0f;
-    for (int i = tid; i < l; i += 256) rinv[i] = live[i] ? static_cast<float>(rdiag[i]) : 0.0f;
+    for (int e = tid; e < l * l; e += 256) {
+        const int i = e / l, j = e % l;
+        Rf[e] = (j >= i && live[i]) ? g[i][j].x : 0.0f;
+    }
+    for (int i = tid; i < l; i += 256) rinv[i] = live[i] ? rdiag[i] : 0.0f;
 }
 
-// One CTA of 1024 threads: the symmetric eigenproblem of G by cyclic Jacobi
-// in fp32 with the round-robin pair order (n/2 disjoint rotations per round,
-// n = l rounded up to even, index l a dummy when l is odd) until the
-// off-diagonal mass is below 1e-12 of the diagonal's (at most 40 sweeps).
-// A round is A <- P^T A P and V <- V P for the rotations P of its n/2 pairs:
-// every 2 x 2 block of A at (row pair, column pair) and every (row, column
-// pair) of V is updated in place by one thread, so a round needs two
-// barriers.  ur[i][m] = the eigenvector of the m-th largest eigenvalue,
-// m < r.  Only the r leading eigenvectors are used, and they are set apart
-// by the spectral gap, so fp32 costs about 1e-6 of them.
-constexpr int kJacobiThreads = 1024;
+// One CTA of 256 threads per checkpoint: the symmetric eigenproblem of G by
+// cyclic Jacobi in fp32 with the round-robin pair order (n/2 disjoint
+// rotations per round, n = l rounded up to even, index l a dummy when l is
+// odd).  A pair is rotated only when |a_pq| exceeds both 2^-22
+// sqrt(|a_pp| |a_qq|) and 2^-24 of the largest initial diagonal entry (below
+// either, the rotation would move nothing above fp32 rounding: the relative
+// threshold rule of Demmel and Veselic, "Jacobi's method is more accurate
+// than QR", 1992, with an absolute floor for the null space of a
+// rank-deficient sketch); the iteration stops after a sweep without a
+// rotation (at most 40 sweeps).  The rotation of a pair: theta = (a_qq -
+// a_pp) / (2 a_pq), t = sign(theta) / (|theta| + sqrt(theta^2 + 1)), c = 1 /
+// sqrt(1 + t^2) (rsqrt and one Newton step), s = t c; a_pq becomes exactly 0
+// and the diagonal moves by -/+ t a_pq.  A round is A <- P^T A P and
+// V <- V P for the rotations P of its n/2 pairs: every 2 x 2 block of A at
+// (row pair, column pair) and every (row, column pair) of V is updated in
+// place by one thread, so a round needs two barriers.  ur[i][m] = the
+// eigenvector of the m-th largest eigenvalue, m < r, normalised.  Only the r
+// leading eigenvectors are used, and they are set apart by the spectral gap,
+// so fp32 costs about 1e-6 of them.
+constexpr int kJacobiThreads = 256;
+constexpr int kJacobiBlocks = (kMaxL / 2) * (kMaxL / 2) / kJacobiThreads;  // 2 x 2 blocks per thread
+constexpr int kJacobiVItems = kMaxL * (kMaxL / 2) / kJacobiThreads;        // V items per thread
 
-__global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const double* __restrict__ G_all, int l, int r,
+__global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __restrict__ G_all, int l, int r,
                                                                 float* __restrict__ ur_all)
 {
     // one eigenproblem per CTA (checkpoint blockIdx.x)
-    const double* G = G_all + static_cast<size_t>(blockIdx.x) * l * l;
+    const float2* G = G_all + static_cast<size_t>(blockIdx.x) * l * l;
     float* ur = ur_all + static_cast<size_t>(blockIdx.x) * l * r;
     __shared__ float A[kMaxL][kMaxL + 1];
     __shared__ float V[kMaxL][kMaxL + 1];
-    __shared__ float cs[kMaxL / 2], sn[kMaxL / 2];
+    __shared__ float cs[kMaxL / 2], sn[kMaxL / 2], tn[kMaxL / 2];
     __shared__ int pp[kMaxL / 2], qq[kMaxL / 2];
     __shared__ unsigned char tp[kMaxL][kMaxL / 2], tq[kMaxL][kMaxL / 2];  // round-robin pairs of every round
-    __shared__ float red[2][32];
     __shared__ int idx[kMaxL];
+    __shared__ float vnorm[kMaxL];
+    __shared__ int rotated[2];  // rotations in sweeps of even / odd parity
+    __shared__ float athr;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e < kMaxL * kMaxL; e += kJacobiThreads) {
         const int i = e >> 6, j = e & 63;
-        A[i][j] = (i < l && j < l) ? static_cast<float>(G[i * l + j]) : 0.0f;
+        A[i][j] = (i < l && j < l) ? __fadd_rn(G[i * l + j].x, G[i * l + j].y) : 0.0f;
         V[i][j] = i == j ? 1.0f : 0.0f;
     }
-    __syncthreads();
     const int n = l + (l & 1);
     const int h = n / 2;
     for (int e = tid; e < (n - 1) * h; e += kJacobiThreads) {  // the pair schedule, once
@@ -520,78 +602,91 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const double* __
     }
     // this thread's 2 x 2 blocks (bi, bj) and V items (row, bj), fixed for the kernel
     const int nb = h * h, nv = l * h;
-    const int ab = tid < nb ? tid / h : 0, bb = tid < nb ? tid - ab * h : 0;
-    const int av0 = tid < nv ? tid / h : 0, bv0 = tid < nv ? tid - av0 * h : 0;
-    const int e1 = tid + kJacobiThreads;
-    const int av1 = e1 < nv ? e1 / h : 0, bv1 = e1 < nv ? e1 - av1 * h : 0;
+    int bi_[kJacobiBlocks], bj_[kJacobiBlocks], vr_[kJacobiVItems], vb_[kJacobiVItems];
+#pragma unroll
+    for (int u = 0; u < kJacobiBlocks; ++u) {
+        const int e = tid + u * kJacobiThreads;
+        bi_[u] = e < nb ? e / h : -1;
+        bj_[u] = e < nb ? e - (e / h) * h : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < kJacobiVItems; ++u) {
+        const int e = tid + u * kJacobiThreads;
+        vr_[u] = e < nv ? e / h : -1;
+        vb_[u] = e < nv ? e - (e / h) * h : 0;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        float m = 0.0f;
+        for (int i = lane; i < l; i += 32) m = fmaxf(m, fabsf(A[i][i]));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) {
+            athr = 0x1p-24f * m;
+            rotated[0] = 0;
+        }
+    }
     __syncthreads();
     for (int sweep = 0; sweep < 40; ++sweep) {
-        float off = 0.0f, dia = 0.0f;
-        for (int e = tid; e < kMaxL * kMaxL; e += kJacobiThreads) {
-            const int i = e >> 6, j = e & 63;
-            const float v = A[i][j];
-            if (i == j)
-                dia = fmaf(v, v, dia);
-            else
-                off = fmaf(v, v, off);
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            off += __shfl_xor_sync(0xffffffffu, off, o);
-            dia += __shfl_xor_sync(0xffffffffu, dia, o);
-        }
-        if (lane == 0) {
-            red[0][warp] = off;
-            red[1][warp] = dia;
-        }
-        __syncthreads();
-        float toff = 0.0f, tdia = 0.0f;
-        for (int w = 0; w < kJacobiThreads / 32; ++w) {
-            toff += red[0][w];
-            tdia += red[1][w];
-        }
-        __syncthreads();
-        if (!(toff > 1e-12f * tdia)) break;
+        const int par = sweep & 1;
         for (int t = 0; t + 1 < n; ++t) {
             if (tid < h) {
                 const int p = tp[t][tid], q = tq[t][tid];
-                float c = 1.0f, sv = 0.0f;
+                float c = 1.0f, sv = 0.0f, tt = 0.0f;
                 if (q < l) {
-                    const float apq = A[p][q];
-                    if (fabsf(apq) > 1e-30f) {
-                        const float th = (A[q][q] - A[p][p]) / (2.0f * apq);
-                        const float tt = (th >= 0.0f ? 1.0f : -1.0f) / (fabsf(th) + sqrtf(th * th + 1.0f));
-                        c = 1.0f / sqrtf(tt * tt + 1.0f);
-                        sv = tt * c;
+                    const float apq = A[p][q], app = A[p][p], aqq = A[q][q];
+                    if (fabsf(apq) > athr && fabsf(apq) > 0x1p-22f * sqrtf(fabsf(app)) * sqrtf(fabsf(aqq))) {
+                        rotated[par] = 1;
+                        const float th = __fdividef(aqq - app, 2.0f * apq);
+                        tt = copysignf(__fdividef(1.0f, fabsf(th) + sqrtf(fmaf(th, th, 1.0f))), th);
+                        const float x = fmaf(tt, tt, 1.0f);
+                        float y = rsqrtf(x);
+                        y = y * fmaf(-0.5f * x * y, y, 1.5f);
+                        c = y;
+                        sv = tt * y;
                     }
                 }
                 cs[tid] = c;
                 sn[tid] = sv;
+                tn[tid] = tt;
                 pp[tid] = p;
                 qq[tid] = q;
             }
             __syncthreads();
+            // every thread has read the previous sweep's flag: clear it for the next sweep
+            if (t == 0 && tid == 0) rotated[par ^ 1] = 0;
             // A: block (pair bi rows, pair bj columns); columns first (A P), then rows (P^T .)
-            if (tid < nb) {
-                const int bi = ab, bj = bb;
+#pragma unroll
+            for (int u = 0; u < kJacobiBlocks; ++u) {
+                const int bi = bi_[u], bj = bj_[u];
+                if (bi < 0) break;
                 const int p = pp[bi], q = qq[bi], p2 = pp[bj], q2 = qq[bj];
                 const float ci = cs[bi], si = sn[bi], cj = cs[bj], sj = sn[bj];
                 const bool rq = q < l, cq = q2 < l;
                 const float a_pp = A[p][p2], a_pq = cq ? A[p][q2] : 0.0f;
                 const float a_qp = rq ? A[q][p2] : 0.0f, a_qq = (rq && cq) ? A[q][q2] : 0.0f;
-                const float x_pp = cj * a_pp - sj * a_pq, x_pq = sj * a_pp + cj * a_pq;
-                const float x_qp = cj * a_qp - sj * a_qq, x_qq = sj * a_qp + cj * a_qq;
-                A[p][p2] = ci * x_pp - si * x_qp;
-                if (cq) A[p][q2] = ci * x_pq - si * x_qq;
-                if (rq) A[q][p2] = si * x_pp + ci * x_qp;
-                if (rq && cq) A[q][q2] = si * x_pq + ci * x_qq;
+                if (bi == bj && si != 0.0f) {
+                    // the rotated pair itself: a_pq is annihilated exactly and
+                    // the diagonal moves by t a_pq
+                    const float ta = tn[bi] * a_pq;
+                    A[p][p] = a_pp - ta;
+                    A[q][q] = a_qq + ta;
+                    A[p][q] = 0.0f;
+                    A[q][p] = 0.0f;
+                } else {
+                    const float x_pp = cj * a_pp - sj * a_pq, x_pq = sj * a_pp + cj * a_pq;
+                    const float x_qp = cj * a_qp - sj * a_qq, x_qq = sj * a_qp + cj * a_qq;
+                    A[p][p2] = ci * x_pp - si * x_qp;
+                    if (cq) A[p][q2] = ci * x_pq - si * x_qq;
+                    if (rq) A[q][p2] = si * x_pp + ci * x_qp;
+                    if (rq && cq) A[q][q2] = si * x_pq + ci * x_qq;
+                }
             }
-            // V: (row, column pair bj), at most two items per thread
+            // V: (row, column pair bj)
 #pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int e = tid + u * kJacobiThreads;
-                if (e >= nv) break;
-                const int row = u == 0 ? av0 : av1, bj = u == 0 ? bv0 : bv1;
+            for (int u = 0; u < kJacobiVItems; ++u) {
+                const int row = vr_[u], bj = vb_[u];
+                if (row < 0) break;
                 const int p2 = pp[bj], q2 = qq[bj];
                 if (q2 >= l) continue;
                 const float cj = cs[bj], sj = sn[bj];
@@ -601,28 +696,37 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const double* __
             }
             __syncthreads();
         }
+        if (!rotated[par]) break;
     }
-    if (tid == 0) {
-        for (int i = 0; i < l; ++i) idx[i] = i;
-        for (int i = 0; i < l; ++i) {  // selection sort, largest eigenvalue first (ties: lower index)
-            int best = i;
-            for (int j = i + 1; j < l; ++j)
-                if (A[idx[j]][idx[j]] > A[idx[best]][idx[best]]) best = j;
-            const int tmp = idx[i];
-            idx[i] = idx[best];
-            idx[best] = tmp;
+    if (tid < l) {  // rank of eigenvalue tid: largest first, ties by lower index (NaN as -inf: a permutation)
+        const float d = isnan(A[tid][tid]) ? -INFINITY : A[tid][tid];
+        int rank = 0;
+        for (int j = 0; j < l; ++j) {
+            const float dj = isnan(A[j][j]) ? -INFINITY : A[j][j];
+            rank += (dj > d || (dj == d && j < tid)) ? 1 : 0;
         }
+        idx[rank] = tid;
+        float ss = 0.0f;
+        for (int i = 0; i < l; ++i) ss = fmaf(V[i][tid], V[i][tid], ss);
+        float y = ss > 0.0f ? rsqrtf(ss) : 0.0f;
+        y = y * fmaf(-0.5f * ss * y, y, 1.5f);  // one Newton step
+        vnorm[tid] = y;
     }
     __syncthreads();
-    for (int e = tid; e < l * r; e += kJacobiThreads) ur[e] = V[e / r][idx[e % r]];
+    for (int e = tid; e < l * r; e += kJacobiThreads) {
+        const int c = idx[e % r];
+        ur[e] = V[e / r][c] * vnorm[c];
+    }
 }
 
-// A <- A R^-1 in place (R from chol_kernel): per row the forward substitution
-// x_j = (a_j - sum_{m<j} x_m R[m][j]) / R[j][j], a dropped direction giving
-// x_j = 0; one row per thread.
-__global__ void __launch_bounds__(64) tri_solve_kernel(float* a, int64_t n, int l, const float* __restrict__ Rf,
-                                                       const float* __restrict__ rinv)
+// A_z <- A_z R_z^-1 in place (R_z from chol_kernel, checkpoint z =
+// blockIdx.y): per row the forward substitution x_j = (a_j - sum_{m<j} x_m
+// R[m][j]) / R[j][j], a dropped direction giving x_j = 0; one row per thread.
+__global__ void __launch_bounds__(64) tri_solve_kernel(float* a_all, int64_t n, int l, const float* __restrict__ Rf_all)
 {
+    float* a = a_all + static_cast<int64_t>(blockIdx.y) * n * l;
+    const float* Rf = Rf_all + static_cast<int64_t>(blockIdx.y) * (kMaxL * kMaxL + kMaxL);
+    const float* rinv = Rf + kMaxL * kMaxL;
     __shared__ float sr[kMaxL][kMaxL + 1];
     __shared__ float sd[kMaxL];
     for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
@@ -653,9 +757,13 @@ __global__ void __launch_bounds__(64) tri_solve_kernel(float* a, int64_t n, int 
 // transposed (the merge reads the factors of consecutive rows contiguously).
 // One thread per row and group of four outputs j: it reads its row with
 // 16-byte loads (l is a multiple of 4) and writes four coalesced columns.
-__global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ src, int64_t n, int l,
-                                                      const float* __restrict__ M, int m, float* __restrict__ dst)
+__global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ src_all, int64_t n, int l,
+                                                      const float* __restrict__ M_all, int m, float* __restrict__ dst_all)
 {
+    // checkpoint z = blockIdx.y: src_z [n][l], M_z [l][m], dst_z [m][n], each set consecutive
+    const float* src = src_all + static_cast<int64_t>(blockIdx.y) * n * l;
+    const float* M = M_all + static_cast<int64_t>(blockIdx.y) * l * m;
+    float* dst = dst_all + static_cast<int64_t>(blockIdx.y) * n * m;
     __shared__ __align__(16) float sm[kMaxL][kMaxL];
     for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
         const int c = e >> 6, j = e & 63;
@@ -781,10 +889,10 @@ MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
     w.z = take(static_cast<size_t>(k) * d_in * l * 4);   // B_i^T of every checkpoint
     w.ypart = take(static_cast<size_t>(kSlices) * d_out * l * 4);
     w.zpart = take(static_cast<size_t>(kSlices) * d_in * l * 4);
-    w.part = take(static_cast<size_t>(kGramBlocks) * l * l * 8);
-    w.g = take(static_cast<size_t>(l) * l * 8);
-    w.gk = take(static_cast<size_t>(k) * l * l * 8);     // B_i B_i^T of every checkpoint
-    w.m = take(static_cast<size_t>(kMaxL) * kMaxL * 4 + kMaxL * 4);
+    w.part = take(static_cast<size_t>(kGramBlocks) * l * l * 8);  // Gram partials of a batch (float2)
+    w.g = take(static_cast<size_t>(kMaxBatch) * l * l * 8);       // Gram matrices of a batch (float2)
+    w.gk = take(static_cast<size_t>(k) * l * l * 8);              // B_i B_i^T of every checkpoint (float2)
+    w.m = take(static_cast<size_t>(kMaxBatch) * (kMaxL * kMaxL + kMaxL) * 4);  // R and 1/diag(R) of a batch
     w.uk = take(static_cast<size_t>(k) * l * (r > 0 ? r : 1) * 4);
     w.L = take(static_cast<size_t>(k) * d_out * (r > 0 ? r : 1) * 4);
     w.Rt = take(static_cast<size_t>(k) * d_in * (r > 0 ? r : 1) * 4);
@@ -818,60 +926,61 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     char* w = static_cast<char*>(a.ws);
     float* Yall = reinterpret_cast<float*>(w + lay.y);
     float* Zall = reinterpret_cast<float*>(w + lay.z);
-    double* Gk = reinterpret_cast<double*>(w + lay.gk);
+    float2* Gk = reinterpret_cast<float2*>(w + lay.gk);
     float* Uk = reinterpret_cast<float*>(w + lay.uk);
-    float* Y = Yall;
-    float* Z = Zall;
     float* Yp = reinterpret_cast<float*>(w + lay.ypart);
     float* Zp = reinterpret_cast<float*>(w + lay.zpart);
     float2* part = reinterpret_cast<float2*>(w + lay.part);
-    double* G = reinterpret_cast<double*>(w + lay.g);
+    float2* G = reinterpret_cast<float2*>(w + lay.g);
     float* M = reinterpret_cast<float*>(w + lay.m);
     float* L = reinterpret_cast<float*>(w + lay.L);
     float* Rt = reinterpret_cast<float*>(w + lay.Rt);
     const int l = a.l, r = a.rank;
+    const int64_t ll = static_cast<int64_t>(l) * l;
     // the two products with Delta: CTAs of 64 rows (or 32, l > 32) / 64
-    // columns of Delta, the reduction dimension split in gridDim.y slices (so
-    // that every SM gets its resident CTAs), the slices summed in order
+    // columns of Delta for each checkpoint of the batch, the reduction
+    // dimension split in gridDim.y slices (so that every SM gets its resident
+    // CTAs), the slices summed in order
     const int sms = a.sm_count > 0 ? a.sm_count : 152;
     static thread_local ProdParams pp_sk, pp_lf;
     const int sk_rows = l <= 32 ? 64 : 32;
     const int64_t rblocks = (a.d_out + sk_rows - 1) / sk_rows, cblocks = a.d_in / kPTile;
     // slices: the smallest count whose CTAs fill whole waves of resident CTAs
-    // to within an eighth (else the count nearest three waves), at most kSlices
-    auto slices = [&](int64_t blocks, int64_t klen, int64_t* per) {
+    // to within an eighth (else the count nearest three waves), at most
+    // kSlices / nb over the nb checkpoints of a batch
+    auto slices = [&](int64_t blocks, int64_t klen, int nb, int64_t* per) {
         const int64_t wave = static_cast<int64_t>(l <= 32 ? prod_ctas<8>() : prod_ctas<16>()) * sms;
+        const int cap = kSlices / nb;
         int ns = 1;
-        for (int c = 1; c <= kSlices; ++c) {
-            const int64_t ctas = blocks * c;
+        for (int c = 1; c <= cap; ++c) {
+            const int64_t ctas = blocks * nb * c;
             const int64_t full = (ctas + wave - 1) / wave;
             if (ctas * 8 >= full * wave * 7 && ctas >= wave) {
                 ns = c;
                 break;
             }
-            if (std::llabs(ctas - 3 * wave) < std::llabs(blocks * ns - 3 * wave)) ns = c;
+            if (std::llabs(ctas - 3 * wave) < std::llabs(blocks * nb * ns - 3 * wave)) ns = c;
         }
         *per = ((klen + ns - 1) / ns + kPTile - 1) / kPTile * kPTile;
         return static_cast<int>((klen + *per - 1) / *per);
     };
-    int64_t cper = 0, rper = 0;
-    const int ssk = slices(rblocks, a.d_in, &cper), slf = slices(cblocks, a.d_out, &rper);
-    const dim3 gsk(static_cast<unsigned>(rblocks), static_cast<unsigned>(ssk));
-    const dim3 glf(static_cast<unsigned>(cblocks), static_cast<unsigned>(slf));
-    auto prep = [&](ProdParams& pr, const uint16_t* wi, const float* small, int64_t small_rows, float* part, int64_t per,
+    cudaError_t perr = cudaSuccess;
+    // tensor maps of checkpoints i0 .. i0 + nb - 1; small(z) = the small operand of checkpoint z
+    auto prep = [&](ProdParams& pr, int i0, int nb, auto small, int64_t small_rows, float* part, int64_t per,
                     int box_rows) {
-        if (!encode_tma_2d(&pr.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, wi, static_cast<uint64_t>(a.d_in),
-                           static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, kPTile,
-                           static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B))
-            return false;
-        if (!encode_tma_2d(&pr.b_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
-                           static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, kPTile,
-                           static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B))
-            return false;
-        if (!encode_tma_2d(&pr.s_map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, small, static_cast<uint64_t>(l),
-                           static_cast<uint64_t>(small_rows), static_cast<uint64_t>(l) * 4, static_cast<uint32_t>(l <= 32 ? 32 : 64),
-                           kPTile, CU_TENSOR_MAP_SWIZZLE_NONE))
-            return false;
+        auto enc_w = [&](CUtensorMap* m, const uint16_t* src) {
+            return encode_tma_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, static_cast<uint64_t>(a.d_in),
+                                 static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, kPTile,
+                                 static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B);
+        };
+        if (!enc_w(&pr.b_map, a.w_base)) return false;
+        for (int z = 0; z < nb; ++z) {
+            if (!enc_w(&pr.w_map[z], a.w_ft[i0 + z])) return false;
+            if (!encode_tma_2d(&pr.s_map[z], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, small(z), static_cast<uint64_t>(l),
+                               static_cast<uint64_t>(small_rows), static_cast<uint64_t>(l) * 4,
+                               static_cast<uint32_t>(l <= 32 ? 32 : 64), kPTile, CU_TENSOR_MAP_SWIZZLE_NONE))
+                return false;
+        }
         pr.part = part;
         pr.err = nullptr;
         pr.d_out = a.d_out;
@@ -880,74 +989,88 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         pr.k_per = per;
         return true;
     };
-    cudaError_t perr = cudaSuccess;
-    auto sketch = [&](const uint16_t* wi, const float* om) {  // Y = Delta om
+    // Y_z = Delta_z S_z for the batch (S_z = Omega, or Z_z with zs)
+    auto sketch = [&](int i0, int nb, bool zs) {
         if (perr != cudaSuccess) return;
-        if (!prep(pp_sk, wi, om, a.d_in, Yp, cper, sk_rows)) {
+        int64_t per = 0;
+        const int ns = slices(rblocks, a.d_in, nb, &per);
+        auto small = [&](int z) -> const float* {
+            return zs ? Zall + static_cast<size_t>(i0 + z) * a.d_in * l : a.omega;
+        };
+        if (!prep(pp_sk, i0, nb, small, a.d_in, Yp, per, sk_rows)) {
             perr = cudaErrorInvalidValue;
             return;
         }
+        const dim3 g(static_cast<unsigned>(rblocks), static_cast<unsigned>(ns), static_cast<unsigned>(nb));
         if (l <= 32)
-            dprod_kernel<0, 8><<<gsk, kPThreads, dprod_smem<0, 8>(), st>>>(pp_sk);
+            dprod_kernel<0, 8><<<g, kPThreads, dprod_smem<0, 8>(), st>>>(pp_sk);
         else
-            dprod_kernel<0, 16><<<gsk, kPThreads, dprod_smem<0, 16>(), st>>>(pp_sk);
-        sum_slices_kernel<<<blocks_for(a.d_out * l), 256, 0, st>>>(Yp, ssk, a.d_out * l, Y);
+            dprod_kernel<0, 16><<<g, kPThreads, dprod_smem<0, 16>(), st>>>(pp_sk);
+        sum_slices_kernel<<<dim3(blocks_for(a.d_out * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
+            Yp, ns, a.d_out * l, Yall + static_cast<size_t>(i0) * a.d_out * l);
     };
-    auto left = [&](const uint16_t* wi) {  // Z = Delta^T Y
+    // Z_z = Delta_z^T Y_z for the batch
+    auto left = [&](int i0, int nb) {
         if (perr != cudaSuccess) return;
-        if (!prep(pp_lf, wi, Y, a.d_out, Zp, rper, kPTile)) {
+        int64_t per = 0;
+        const int ns = slices(cblocks, a.d_out, nb, &per);
+        auto small = [&](int z) -> const float* { return Yall + static_cast<size_t>(i0 + z) * a.d_out * l; };
+        if (!prep(pp_lf, i0, nb, small, a.d_out, Zp, per, kPTile)) {
             perr = cudaErrorInvalidValue;
             return;
         }
+        const dim3 g(static_cast<unsigned>(cblocks), static_cast<unsigned>(ns), static_cast<unsigned>(nb));
         if (l <= 32)
-            dprod_kernel<1, 8><<<glf, kPThreads, dprod_smem<1, 8>(), st>>>(pp_lf);
+            dprod_kernel<1, 8><<<g, kPThreads, dprod_smem<1, 8>(), st>>>(pp_lf);
         else
-            dprod_kernel<1, 16><<<glf, kPThreads, dprod_smem<1, 16>(), st>>>(pp_lf);
-        sum_slices_kernel<<<blocks_for(a.d_in * l), 256, 0, st>>>(Zp, slf, a.d_in * l, Z);
+            dprod_kernel<1, 16><<<g, kPThreads, dprod_smem<1, 16>(), st>>>(pp_lf);
+        sum_slices_kernel<<<dim3(blocks_for(a.d_in * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
+            Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
     };
-    auto gram = [&](const float* A, int64_t n, double* out) {  // out = A^T A
-        if (l * l <= kGramThreads)
-            gram_kernel<1><<<kGramBlocks, kGramThreads, 0, st>>>(A, n, l, part);
+    // out_z = A_z^T A_z for the nb consecutive A_z [n][l]
+    auto gram = [&](const float* A, int64_t n, int nb, float2* out) {
+        const int gb = kGramBlocks / nb;
+        const dim3 g(static_cast<unsigned>(gb), static_cast<unsigned>(nb));
+        if (ll <= kGramThreads)
+            gram_kernel<1><<<g, kGramThreads, 0, st>>>(A, n, l, part);
         else
-            gram_kernel<4><<<kGramBlocks, kGramThreads, 0, st>>>(A, n, l, part);
-        gram_sum_kernel<<<blocks_for(32 * static_cast<int64_t>(l) * l), 256, 0, st>>>(part, l, out);
+            gram_kernel<4><<<g, kGramThreads, 0, st>>>(A, n, l, part);
+        gram_sum_kernel<<<dim3(blocks_for(32 * ll), static_cast<unsigned>(nb)), 256, 0, st>>>(part, gb, l, out);
     };
-    // A <- A R^-1 (CholeskyQR), `passes` times: two (CholeskyQR2) for the Q
-    // that B is projected on, one for the intermediate bases of the power
-    // iterations, where only the spanned subspace matters
-    auto orth = [&](float* A, int64_t n, int passes) {
+    // A_z <- A_z R_z^-1 (CholeskyQR), `passes` times: two (CholeskyQR2) for
+    // the Q that B is projected on, one for the intermediate bases of the
+    // power iterations, where only the spanned subspace matters
+    auto orth = [&](float* A, int64_t n, int nb, int passes) {
         for (int pass = 0; pass < passes; ++pass) {
-            gram(A, n, G);
-            chol_kernel<<<1, 256, 0, st>>>(G, l, M, M + kMaxL * kMaxL);
-            tri_solve_kernel<<<static_cast<unsigned>((n + 63) / 64), 64, 0, st>>>(A, n, l, M, M + kMaxL * kMaxL);
+            gram(A, n, nb, G);
+            chol_kernel<<<static_cast<unsigned>(nb), 256, 0, st>>>(G, l, M);
+            tri_solve_kernel<<<dim3(static_cast<unsigned>((n + 63) / 64), static_cast<unsigned>(nb)), 64, 0, st>>>(
+                A, n, l, M);
         }
     };
     if (r > 0) {
-        for (int i = 0; i < a.k; ++i) {
-            const uint16_t* wi = a.w_ft[i];
-            Y = Yall + static_cast<size_t>(i) * a.d_out * l;
-            Z = Zall + static_cast<size_t>(i) * a.d_in * l;
-            sketch(wi, a.omega);
-            orth(Y, a.d_out, a.power_iters > 0 ? 1 : 2);
+        for (int i0 = 0; i0 < a.k; i0 += kMaxBatch) {
+            const int nb = a.k - i0 < kMaxBatch ? a.k - i0 : kMaxBatch;
+            float* Y = Yall + static_cast<size_t>(i0) * a.d_out * l;
+            float* Z = Zall + static_cast<size_t>(i0) * a.d_in * l;
+            sketch(i0, nb, false);
+            orth(Y, a.d_out, nb, a.power_iters > 0 ? 1 : 2);
             for (int it = 0; it < a.power_iters; ++it) {
-                left(wi);
-                orth(Z, a.d_in, 1);
-                sketch(wi, Z);
-                orth(Y, a.d_out, it + 1 == a.power_iters ? 2 : 1);
+                left(i0, nb);
+                orth(Z, a.d_in, nb, 1);
+                sketch(i0, nb, true);
+                orth(Y, a.d_out, nb, it + 1 == a.power_iters ? 2 : 1);
             }
-            left(wi);                                                    // Z = B^T
-            gram(Z, a.d_in, Gk + static_cast<size_t>(i) * l * l);        // B B^T
+            left(i0, nb);                                          // Z = B^T
+            gram(Z, a.d_in, nb, Gk + static_cast<size_t>(i0) * ll);  // B B^T
         }
         // the k projected eigenproblems at once, one CTA each
         jacobi_kernel<<<static_cast<unsigned>(a.k), kJacobiThreads, 0, st>>>(Gk, l, r, Uk);  // U_r [l][r]
-        for (int i = 0; i < a.k; ++i) {
-            const float* Ui = Uk + static_cast<size_t>(i) * l * r;
-            apply_t_kernel<<<blocks_for(a.d_out * ((r + 3) / 4)), 256, 0, st>>>(Yall + static_cast<size_t>(i) * a.d_out * l,
-                                                                    a.d_out, l, Ui, r,
-                                                                    L + static_cast<size_t>(i) * a.d_out * r);
-            apply_t_kernel<<<blocks_for(a.d_in * ((r + 3) / 4)), 256, 0, st>>>(Zall + static_cast<size_t>(i) * a.d_in * l, a.d_in,
-                                                                   l, Ui, r, Rt + static_cast<size_t>(i) * a.d_in * r);
-        }
+        const unsigned rq = static_cast<unsigned>((r + 3) / 4);
+        apply_t_kernel<<<dim3(blocks_for(a.d_out * rq), static_cast<unsigned>(a.k)), 256, 0, st>>>(Yall, a.d_out, l,
+                                                                                                  Uk, r, L);
+        apply_t_kernel<<<dim3(blocks_for(a.d_in * rq), static_cast<unsigned>(a.k)), 256, 0, st>>>(Zall, a.d_in, l, Uk,
+                                                                                                 r, Rt);
     }
     if (perr != cudaSuccess) return perr;
     const dim3 grid(static_cast<unsigned>((a.d_in + kMergeTile - 1) / kMergeTile),
