@@ -35,6 +35,7 @@
 #include <atomic>
 
 #include "bd_device.cuh"
+#include "bd_tcgen05.cuh"
 #include "bd_tma.h"
 
 namespace bd {
@@ -300,6 +301,264 @@ size_t dprod_smem()
     const size_t red = static_cast<size_t>(MODE == 0 ? 32 * RPL : kPTile) * (4 * L4 + 1) * 4;
     constexpr int kPStages = prod_stages<L4>();
     return (kPStages * stage > red ? kPStages * stage : red) + 1024;
+}
+
+// ---------------------------------------------------------------- tensor-core products (l <= 32)
+// The same two products on the tcgen05 tensor cores with exact splits: an
+// fp32 value v is v1 + v2 + v3 with v1 = v with the low 16 bits of its
+// encoding cleared, v2 the same of v - v1 and v3 = v - v1 - v2 (each
+// subtraction exact, each piece a bf16 value), so that Delta S is the sum of
+// the nine products of pieces, each bf16 x bf16 product exact and the sums
+// in fp32 in the tensor core.
+//   A = the pieces of the small operand stacked: row 32 b + c = piece b of
+//       column c (rows past 3 x 32 and columns past l zero), [128][K] bf16,
+//       K-major (split_small_kernel);
+//   B = the pieces of Delta, formed in shared memory from the W_i and W_base
+//       tiles in place: the three pieces of an element sit at the same offset
+//       of three tiles, so the tiles keep the TMA's 128-byte swizzle;
+//   D[32 b + c][n] (+)= sum over the k-step of A B^T, three MMAs (one per
+//       piece of Delta) of M = 128, N = 128, K = 16, in tensor memory; the
+//       result is D[c][n] + D[32 + c][n] + D[64 + c][n].
+// MODE 0 (Y = Delta S): n = 128 rows of Delta, K = its columns (K-major, as
+// loaded).  MODE 1 (Z = Delta^T S): n = 128 columns of Delta, K = its rows:
+// MN-major, two 64-column boxes per tile, 8 KB apart.  Warp 0 issues the TMA
+// loads, warp 1 allocates tensor memory and issues the MMAs, warps 2..9 form
+// the pieces; warps 2..5 (one per lane quarter) then read the accumulator.
+constexpr int kTN = 128;                 // MMA N: Delta rows (MODE 0) or columns (MODE 1) of a CTA
+constexpr int kTK = 64;                  // reduction indices per stage
+constexpr int kTStages = 3;
+constexpr int kTTile = kTN * kTK * 2;    // one bf16 tile: 16 KB
+constexpr int kTStage = 4 * kTTile;      // W_i -> piece 1, W_base -> piece 2, piece 3, A
+constexpr int kTConvWarps = 8;
+constexpr int kTThreads = 32 * (2 + kTConvWarps);
+constexpr uint32_t kTTmemCols = kTN;
+
+struct TProdParams {
+    CUtensorMap b_map;             // W_base [d_out][d_in] bf16, box 64 x 128 (MODE 0) or 64 x 64 (MODE 1), 128-byte swizzle
+    CUtensorMap w_map[kMaxBatch];  // W_i of checkpoint blockIdx.z, same
+    CUtensorMap a_map[kMaxBatch];  // its split small operand [128][K] bf16, box 64 x 128, 128-byte swizzle
+    float* part;                   // [gridDim.z][gridDim.y][out rows][l]
+    int64_t d_out, d_in;
+    int l;
+    int64_t k_per;                 // reduction indices per slice (a multiple of 64)
+};
+
+// Shared-memory matrix descriptor of an MN-major operand with 128-byte
+// swizzle: 64-element (128-byte) blocks along M/N lbo bytes apart, 8-row
+// groups along K 1024 bytes apart (tile base 1024-byte aligned).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo)
+{
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    d |= static_cast<uint64_t>(2) << 61;
+    return d;
+}
+
+// The three pieces of the two Delta values of a bf16 pair (W_i word wi,
+// W_base word wb), each packed as a bf16 pair.
+__device__ __forceinline__ void split_pair(uint32_t wi, uint32_t wb, uint32_t& o1, uint32_t& o2, uint32_t& o3)
+{
+    const float dl = __fsub_rn(__uint_as_float(wi << 16), __uint_as_float(wb << 16));
+    const float dh = __fsub_rn(__uint_as_float(wi & 0xFFFF0000u), __uint_as_float(wb & 0xFFFF0000u));
+    const uint32_t l1 = __float_as_uint(dl) & 0xFFFF0000u, h1 = __float_as_uint(dh) & 0xFFFF0000u;
+    const float rl = __fsub_rn(dl, __uint_as_float(l1)), rh = __fsub_rn(dh, __uint_as_float(h1));
+    const uint32_t l2 = __float_as_uint(rl) & 0xFFFF0000u, h2 = __float_as_uint(rh) & 0xFFFF0000u;
+    const float sl = __fsub_rn(rl, __uint_as_float(l2)), sh = __fsub_rn(rh, __uint_as_float(h2));
+    o1 = __byte_perm(l1, h1, 0x7632);
+    o2 = __byte_perm(l2, h2, 0x7632);
+    o3 = __byte_perm(__float_as_uint(sl), __float_as_uint(sh), 0x7632);
+}
+
+// Sp[z][32 b + c][k] = piece b of S_z[k][c] (c < l, b < 3, k < K), zero in
+// the other rows and in the columns K .. Kp - 1 (rows of Kp elements, Kp = K
+// rounded up to 64); S_z = S + z zstride ([K][l] fp32), z = blockIdx.y.
+__global__ void __launch_bounds__(256) split_small_kernel(const float* __restrict__ S, int64_t zstride, int64_t K,
+                                                          int64_t Kp, int l, uint16_t* __restrict__ Sp)
+{
+    const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (k >= Kp) return;
+    const float* src = S + blockIdx.y * zstride + k * l;
+    uint16_t* o = Sp + static_cast<int64_t>(blockIdx.y) * 128 * Kp + k;
+    for (int c = 0; c < 32; ++c) {
+        const float v = (c < l && k < K) ? src[c] : 0.0f;
+        const uint32_t b1 = __float_as_uint(v) & 0xFFFF0000u;
+        const float r1 = __fsub_rn(v, __uint_as_float(b1));
+        const uint32_t b2 = __float_as_uint(r1) & 0xFFFF0000u;
+        const float r2 = __fsub_rn(r1, __uint_as_float(b2));
+        o[c * Kp] = static_cast<uint16_t>(b1 >> 16);
+        o[(32 + c) * Kp] = static_cast<uint16_t>(b2 >> 16);
+        o[(64 + c) * Kp] = static_cast<uint16_t>(__float_as_uint(r2) >> 16);
+        o[(96 + c) * Kp] = 0;
+    }
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_constant__ TProdParams p)
+{
+    extern __shared__ uint8_t dyn_raw[];
+    __shared__ uint64_t full[kTStages], conv[kTStages], empty[kTStages];
+    __shared__ uint64_t done;
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int abort;
+    uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int z = static_cast<int>(blockIdx.z);
+    const int64_t o0 = static_cast<int64_t>(blockIdx.x) * kTN;  // first output row of this CTA
+    const int64_t klen = MODE == 0 ? p.d_in : p.d_out;
+    const int64_t kb = static_cast<int64_t>(blockIdx.y) * p.k_per;
+    const int64_t ke = kb + p.k_per < klen ? kb + p.k_per : klen;
+    const int nt = ke > kb ? static_cast<int>((ke - kb + kTK - 1) / kTK) : 0;
+    if (tid == 0) {
+        for (int st = 0; st < kTStages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&conv[st], kTConvWarps);
+            mbar_init(&empty[st], 1);
+        }
+        mbar_init(&done, 1);
+        abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_base, kTTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (mbar_try_wait(bar, par)) return true;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar, par)) {
+            if (abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                abort = 1;
+                return false;
+            }
+        }
+        return true;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int t = 0;
+            for (; t < nt; ++t) {
+                const int st = t % kTStages;
+                if (t >= kTStages && !wait(&empty[st], static_cast<uint32_t>(t / kTStages - 1) & 1u)) break;
+                uint8_t* sb = ring + static_cast<size_t>(st) * kTStage;
+                const int k0 = static_cast<int>(kb + static_cast<int64_t>(t) * kTK);
+                mbar_arrive_expect_tx(&full[st], 3u * kTTile);
+                if (MODE == 0) {
+                    tma_load_2d(sb, &p.w_map[z], k0, static_cast<int>(o0), &full[st]);
+                    tma_load_2d(sb + kTTile, &p.b_map, k0, static_cast<int>(o0), &full[st]);
+                } else {
+#pragma unroll
+                    for (int hb = 0; hb < 2; ++hb) {
+                        const int cx = static_cast<int>(o0) + 64 * hb;
+                        tma_load_2d(sb + hb * (kTTile / 2), &p.w_map[z], cx, k0, &full[st]);
+                        tma_load_2d(sb + kTTile + hb * (kTTile / 2), &p.b_map, cx, k0, &full[st]);
+                    }
+                }
+                tma_load_2d(sb + 3 * kTTile, &p.a_map[z], k0, 0, &full[st]);
+            }
+            for (int i = (t > kTStages ? t - kTStages : 0); i < t; ++i) {  // every issued copy lands before exit
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&full[i % kTStages], static_cast<uint32_t>(i / kTStages) & 1u) &&
+                       global_timer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, kTN) | (MODE == 1 ? (1u << 16) : 0u);
+            for (int t = 0; t < nt; ++t) {
+                const int st = t % kTStages;
+                if (!wait(&conv[st], static_cast<uint32_t>(t / kTStages) & 1u)) break;
+                tc_fence_after();
+                const uint32_t sb = smem_u32(ring + static_cast<size_t>(st) * kTStage);
+                const uint64_t adesc = smem_desc_sw128(sb + 3 * kTTile);
+#pragma unroll
+                for (int kk = 0; kk < kTK / 16; ++kk) {
+#pragma unroll
+                    for (int a = 0; a < 3; ++a) {
+                        const uint64_t bdesc =
+                            MODE == 0 ? smem_desc_sw128(sb + a * kTTile) + static_cast<uint64_t>(2 * kk)
+                                      : smem_desc_mn_sw128(sb + a * kTTile, kTTile / 2) + static_cast<uint64_t>(128 * kk);
+                        mma_ss(tmem, adesc + static_cast<uint64_t>(2 * kk), bdesc, idesc, (t | kk | a) != 0 ? 1u : 0u);
+                    }
+                }
+                mma_commit(&empty[st]);
+            }
+            mma_commit(&done);  // every MMA issued above has finished when this arrives
+        }
+    } else {
+        // ------------------------------------------------------------ pieces of Delta
+        const int ct = tid - 64;  // 0 .. 255
+        for (int t = 0; t < nt; ++t) {
+            const int st = t % kTStages;
+            if (!__all_sync(0xffffffffu, wait(&full[st], static_cast<uint32_t>(t / kTStages) & 1u))) break;
+            uint4* t1 = reinterpret_cast<uint4*>(ring + static_cast<size_t>(st) * kTStage);
+            uint4* t2 = t1 + kTTile / 16;
+            uint4* t3 = t2 + kTTile / 16;
+#pragma unroll
+            for (int c = ct; c < kTTile / 16; c += 32 * kTConvWarps) {
+                const uint4 a = t1[c], b = t2[c];
+                uint4 r1, r2, r3;
+                split_pair(a.x, b.x, r1.x, r2.x, r3.x);
+                split_pair(a.y, b.y, r1.y, r2.y, r3.y);
+                split_pair(a.z, b.z, r1.z, r2.z, r3.z);
+                split_pair(a.w, b.w, r1.w, r2.w, r3.w);
+                t1[c] = r1;
+                t2[c] = r2;
+                t3[c] = r3;
+            }
+            fence_proxy_async_smem();  // the pieces are read by the tensor core (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&conv[st]);
+        }
+    }
+    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    if (warp >= 2 && warp < 6) {
+        const int q = warp & 3;  // tensor-memory lanes 32 q .. 32 q + 31: piece q of the small operand
+        const bool ok = __all_sync(0xffffffffu, wait(&done, 0u)) && !abort;
+        tc_fence_after();
+        float* red = reinterpret_cast<float*>(ring);  // [2][kTN][33]: pieces 1 and 2
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
+        if (ok && (q == 1 || q == 2)) {
+#pragma unroll 1
+            for (int j0 = 0; j0 < kTN; j0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(taddr + j0, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) red[((q - 1) * kTN + j0 + j) * 33 + lane] = __uint_as_float(v[j]);
+            }
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");
+        if (ok && q == 0) {
+            const int64_t nrows = MODE == 0 ? p.d_out : p.d_in;
+            float* out = p.part + (static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * nrows * p.l;
+#pragma unroll 1
+            for (int j0 = 0; j0 < kTN; j0 += 32) {
+                uint32_t v[32];
+                tmem_ld32(taddr + j0, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int n = j0 + j;
+                    const float y = nt > 0 ? (__uint_as_float(v[j]) + red[n * 33 + lane]) + red[(kTN + n) * 33 + lane]
+                                           : 0.0f;
+                    if (lane < p.l && o0 + n < nrows) out[(o0 + n) * p.l + lane] = y;
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTTmemCols);
+    }
 }
 
 // out[z][e] = sum_s part[z][s][e], e < n, for the gridDim.y checkpoints z
@@ -873,7 +1132,7 @@ __global__ void __launch_bounds__(256, 2) merge_kernel(const uint16_t* __restric
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct MonoSoupWs {
-    size_t y, z, ypart, zpart, part, g, gk, m, uk, L, Rt, total;
+    size_t y, z, ypart, zpart, part, g, gk, m, uk, L, Rt, sp, total;
 };
 
 MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
@@ -896,6 +1155,9 @@ MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
     w.uk = take(static_cast<size_t>(k) * l * (r > 0 ? r : 1) * 4);
     w.L = take(static_cast<size_t>(k) * d_out * (r > 0 ? r : 1) * 4);
     w.Rt = take(static_cast<size_t>(k) * d_in * (r > 0 ? r : 1) * 4);
+    // split small operands of a batch for the tensor-core products (l <= 32)
+    const size_t kp = static_cast<size_t>(((d_in > d_out ? d_in : d_out) + 63) / 64 * 64);
+    w.sp = take(l <= 32 ? static_cast<size_t>(kMaxBatch) * 128 * kp * 2 : 0);
     w.total = off;
     return w;
 }
@@ -921,6 +1183,10 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(dprod_kernel<1, 8>), dprod_smem<1, 8>(), s10);
     if (e0 == cudaSuccess)
         e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(dprod_kernel<1, 16>), dprod_smem<1, 16>(), s11);
+    static std::atomic<size_t> t0c[kHostMaxDevices], t1c[kHostMaxDevices];
+    constexpr size_t kTSmem = static_cast<size_t>(kTStages) * kTStage + 1024;
+    if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<0>), kTSmem, t0c);
+    if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<1>), kTSmem, t1c);
     if (e0 != cudaSuccess) return e0;
     const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
     char* w = static_cast<char*>(a.ws);
@@ -935,7 +1201,9 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     float* M = reinterpret_cast<float*>(w + lay.m);
     float* L = reinterpret_cast<float*>(w + lay.L);
     float* Rt = reinterpret_cast<float*>(w + lay.Rt);
+    uint16_t* Sp = reinterpret_cast<uint16_t*>(w + lay.sp);
     const int l = a.l, r = a.rank;
+    const bool tc = l <= 32;  // tensor-core products
     const int64_t ll = static_cast<int64_t>(l) * l;
     // the two products with Delta: CTAs of 64 rows (or 32, l > 32) / 64
     // columns of Delta for each checkpoint of the batch, the reduction
@@ -949,7 +1217,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     // to within an eighth (else the count nearest three waves), at most
     // kSlices / nb over the nb checkpoints of a batch
     auto slices = [&](int64_t blocks, int64_t klen, int nb, int64_t* per) {
-        const int64_t wave = static_cast<int64_t>(l <= 32 ? prod_ctas<8>() : prod_ctas<16>()) * sms;
+        const int64_t wave = tc ? static_cast<int64_t>(sms) : static_cast<int64_t>(prod_ctas<16>()) * sms;
         const int cap = kSlices / nb;
         int ns = 1;
         for (int c = 1; c <= cap; ++c) {
@@ -989,10 +1257,51 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         pr.k_per = per;
         return true;
     };
+    // tensor-core form: A = the split small operands (Sp), B = the pieces of Delta
+    static thread_local TProdParams tp_sk, tp_lf;
+    auto tprep = [&](TProdParams& pr, int i0, int nb, int64_t Kp, float* part, int64_t per, int box_rows) {
+        auto enc_w = [&](CUtensorMap* m, const uint16_t* src) {
+            return encode_tma_2d(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, src, static_cast<uint64_t>(a.d_in),
+                                 static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, kTK,
+                                 static_cast<uint32_t>(box_rows), CU_TENSOR_MAP_SWIZZLE_128B);
+        };
+        if (!enc_w(&pr.b_map, a.w_base)) return false;
+        for (int z = 0; z < nb; ++z) {
+            if (!enc_w(&pr.w_map[z], a.w_ft[i0 + z])) return false;
+            if (!encode_tma_2d(&pr.a_map[z], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Sp + static_cast<size_t>(z) * 128 * Kp,
+                               static_cast<uint64_t>(Kp), 128, static_cast<uint64_t>(Kp) * 2, kTK, 128,
+                               CU_TENSOR_MAP_SWIZZLE_128B))
+                return false;
+        }
+        pr.part = part;
+        pr.d_out = a.d_out;
+        pr.d_in = a.d_in;
+        pr.l = l;
+        pr.k_per = per;
+        return true;
+    };
+    const int64_t tr_blocks = (a.d_out + kTN - 1) / kTN, tc_blocks = a.d_in / kTN;
     // Y_z = Delta_z S_z for the batch (S_z = Omega, or Z_z with zs)
     auto sketch = [&](int i0, int nb, bool zs) {
         if (perr != cudaSuccess) return;
         int64_t per = 0;
+        if (tc) {
+            const int ns = slices(tr_blocks, a.d_in, nb, &per);
+            const int64_t kp = (a.d_in + 63) / 64 * 64;
+            split_small_kernel<<<dim3(blocks_for(kp), static_cast<unsigned>(nb)), 256, 0, st>>>(
+                zs ? Zall + static_cast<size_t>(i0) * a.d_in * l : a.omega,
+                zs ? static_cast<int64_t>(a.d_in) * l : 0, a.d_in, kp, l, Sp);
+            if (!tprep(tp_sk, i0, nb, kp, Yp, per, kTN)) {
+                perr = cudaErrorInvalidValue;
+                return;
+            }
+            tprod_kernel<0><<<dim3(static_cast<unsigned>(tr_blocks), static_cast<unsigned>(ns),
+                                   static_cast<unsigned>(nb)),
+                              kTThreads, kTSmem, st>>>(tp_sk);
+            sum_slices_kernel<<<dim3(blocks_for(a.d_out * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
+                Yp, ns, a.d_out * l, Yall + static_cast<size_t>(i0) * a.d_out * l);
+            return;
+        }
         const int ns = slices(rblocks, a.d_in, nb, &per);
         auto small = [&](int z) -> const float* {
             return zs ? Zall + static_cast<size_t>(i0 + z) * a.d_in * l : a.omega;
@@ -1013,6 +1322,22 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     auto left = [&](int i0, int nb) {
         if (perr != cudaSuccess) return;
         int64_t per = 0;
+        if (tc) {
+            const int ns = slices(tc_blocks, a.d_out, nb, &per);
+            const int64_t kp = (a.d_out + 63) / 64 * 64;
+            split_small_kernel<<<dim3(blocks_for(kp), static_cast<unsigned>(nb)), 256, 0, st>>>(
+                Yall + static_cast<size_t>(i0) * a.d_out * l, static_cast<int64_t>(a.d_out) * l, a.d_out, kp, l, Sp);
+            if (!tprep(tp_lf, i0, nb, kp, Zp, per, 64)) {
+                perr = cudaErrorInvalidValue;
+                return;
+            }
+            tprod_kernel<1><<<dim3(static_cast<unsigned>(tc_blocks), static_cast<unsigned>(ns),
+                                   static_cast<unsigned>(nb)),
+                              kTThreads, kTSmem, st>>>(tp_lf);
+            sum_slices_kernel<<<dim3(blocks_for(a.d_in * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
+                Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
+            return;
+        }
         const int ns = slices(cblocks, a.d_out, nb, &per);
         auto small = [&](int z) -> const float* { return Yall + static_cast<size_t>(i0 + z) * a.d_out * l; };
         if (!prep(pp_lf, i0, nb, small, a.d_out, Zp, per, kPTile)) {
