@@ -310,52 +310,45 @@ size_t dprod_smem()
 // subtraction exact, each piece a bf16 value), so that Delta S is the sum of
 // the nine products of pieces, each bf16 x bf16 product exact and the sums
 // in fp32 in the tensor core.
-//   A = the pieces of the small operand stacked: row 32 b + c = piece b of
-//       column c (rows past 3 x 32 and columns past l zero), [128][K] bf16,
-//       K-major (split_small_kernel);
-//   B = the pieces of Delta, formed in shared memory from the W_i and W_base
-//       tiles in place: the three pieces of an element sit at the same offset
-//       of three tiles, so the tiles keep the TMA's 128-byte swizzle;
-//   D[32 b + c][n] (+)= sum over the k-step of A B^T, three MMAs (one per
-//       piece of Delta) of M = 128, N = 128, K = 16, in tensor memory; the
-//       result is D[c][n] + D[32 + c][n] + D[64 + c][n].
-// MODE 0 (Y = Delta S): n = 128 rows of Delta, K = its columns (K-major, as
-// loaded).  MODE 1 (Z = Delta^T S): n = 128 columns of Delta, K = its rows:
-// MN-major, two 64-column boxes per tile, 8 KB apart.  Warp 0 issues the TMA
+//   A = a piece of Delta (M = 128 rows of Delta for the sketch, 128 columns
+//       for the transpose product; K = its other index), formed by the
+//       piece warps from the W_i and W_base tiles and written to tensor
+//       memory (one lane per row of A, a bf16 pair per column);
+//   B = the pieces of the small operand stacked along N: row 32 b + c =
+//       piece b of column c (N = 96, rows c >= l zero), K-major in shared
+//       memory (split_small_kernel writes them, a TMA box brings 64 K);
+//   D[m][32 b + c] (+)= sum over the k-step of A_a B^T for the three pieces
+//       a of Delta (three MMAs of M = 128, N = 96, K = 16 per k-step) in
+//       tensor memory; the result is D[m][c] + D[m][32 + c] + D[m][64 + c].
+// A stage holds only the W_i and W_base tiles and the B tile (44 KB), so four
+// stages keep four tiles of Delta in flight per SM.  Warp 0 issues the TMA
 // loads, warp 1 allocates tensor memory and issues the MMAs, warps 2..9 form
-// the pieces; warps 2..5 (one per lane quarter) then read the accumulator.
-constexpr int kTN = 128;                 // MMA N: Delta rows (MODE 0) or columns (MODE 1) of a CTA
-constexpr int kTK = 64;                  // reduction indices per stage
-constexpr int kTStages = 3;
-constexpr int kTTile = kTN * kTK * 2;    // one bf16 tile: 16 KB
-constexpr int kTStage = 4 * kTTile;      // W_i -> piece 1, W_base -> piece 2, piece 3, A
+// the pieces (lane quarter warp % 4, K half (warp - 2) / 4); warps 2..5 then
+// read the accumulator, one row per thread.
+constexpr int kTM = 128;                     // MMA M: Delta rows (MODE 0) or columns (MODE 1) of a CTA
+constexpr int kTK = 64;                      // reduction indices per stage
+constexpr int kTNB = 96;                     // MMA N: three pieces x 32 columns of the small operand
+constexpr int kTStages = 4;
+constexpr int kTWTile = kTM * kTK * 2;       // one bf16 tile of W: 16 KB
+constexpr int kTBTile = kTNB * kTK * 2;      // the B tile: 12 KB
+constexpr int kTStage = 2 * kTWTile + kTBTile;
 constexpr int kTConvWarps = 8;
 constexpr int kTThreads = 32 * (2 + kTConvWarps);
-constexpr uint32_t kTTmemCols = kTN;
+constexpr uint32_t kTTmemCols = 512;
+constexpr uint32_t kTDCol = 0;                // D: 96 columns
+constexpr uint32_t kTACol = 128;              // A ring: 3 pieces x 32 columns per stage
+static_assert(kTACol + 3 * 32 * kTStages <= kTTmemCols, "tensor-memory columns");
+static_assert(kTStage % 1024 == 0, "1024-byte aligned stages");
 
 struct TProdParams {
     CUtensorMap b_map;             // W_base [d_out][d_in] bf16, box 64 x 128 (MODE 0) or 64 x 64 (MODE 1), 128-byte swizzle
     CUtensorMap w_map[kMaxBatch];  // W_i of checkpoint blockIdx.z, same
-    CUtensorMap a_map[kMaxBatch];  // its split small operand [128][K] bf16, box 64 x 128, 128-byte swizzle
+    CUtensorMap s_map[kMaxBatch];  // its split small operand [128][Kp] bf16, box 64 x 96, 128-byte swizzle
     float* part;                   // [gridDim.z][gridDim.y][out rows][l]
     int64_t d_out, d_in;
     int l;
     int64_t k_per;                 // reduction indices per slice (a multiple of 64)
 };
-
-// Shared-memory matrix descriptor of an MN-major operand with 128-byte
-// swizzle: 64-element (128-byte) blocks along M/N lbo bytes apart, 8-row
-// groups along K 1024 bytes apart (tile base 1024-byte aligned).
-__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t lbo)
-{
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>(1024 >> 4) << 32;
-    d |= static_cast<uint64_t>(1) << 46;
-    d |= static_cast<uint64_t>(2) << 61;
-    return d;
-}
 
 // The three pieces of the two Delta values of a bf16 pair (W_i word wi,
 // W_base word wb), each packed as a bf16 pair.
@@ -395,18 +388,28 @@ __global__ void __launch_bounds__(256) split_small_kernel(const float* __restric
     }
 }
 
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&v)[16])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+        : "memory");
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_constant__ TProdParams p)
 {
     extern __shared__ uint8_t dyn_raw[];
-    __shared__ uint64_t full[kTStages], conv[kTStages], empty[kTStages];
+    __shared__ uint64_t full[kTStages], afull[kTStages], empty[kTStages];
     __shared__ uint64_t done;
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort;
     uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int z = static_cast<int>(blockIdx.z);
-    const int64_t o0 = static_cast<int64_t>(blockIdx.x) * kTN;  // first output row of this CTA
+    const int64_t o0 = static_cast<int64_t>(blockIdx.x) * kTM;  // first output row of this CTA
     const int64_t klen = MODE == 0 ? p.d_in : p.d_out;
     const int64_t kb = static_cast<int64_t>(blockIdx.y) * p.k_per;
     const int64_t ke = kb + p.k_per < klen ? kb + p.k_per : klen;
@@ -414,7 +417,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
     if (tid == 0) {
         for (int st = 0; st < kTStages; ++st) {
             mbar_init(&full[st], 1);
-            mbar_init(&conv[st], kTConvWarps);
+            mbar_init(&afull[st], kTConvWarps);
             mbar_init(&empty[st], 1);
         }
         mbar_init(&done, 1);
@@ -448,19 +451,19 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
                 if (t >= kTStages && !wait(&empty[st], static_cast<uint32_t>(t / kTStages - 1) & 1u)) break;
                 uint8_t* sb = ring + static_cast<size_t>(st) * kTStage;
                 const int k0 = static_cast<int>(kb + static_cast<int64_t>(t) * kTK);
-                mbar_arrive_expect_tx(&full[st], 3u * kTTile);
+                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kTStage));
                 if (MODE == 0) {
                     tma_load_2d(sb, &p.w_map[z], k0, static_cast<int>(o0), &full[st]);
-                    tma_load_2d(sb + kTTile, &p.b_map, k0, static_cast<int>(o0), &full[st]);
+                    tma_load_2d(sb + kTWTile, &p.b_map, k0, static_cast<int>(o0), &full[st]);
                 } else {
 #pragma unroll
                     for (int hb = 0; hb < 2; ++hb) {
                         const int cx = static_cast<int>(o0) + 64 * hb;
-                        tma_load_2d(sb + hb * (kTTile / 2), &p.w_map[z], cx, k0, &full[st]);
-                        tma_load_2d(sb + kTTile + hb * (kTTile / 2), &p.b_map, cx, k0, &full[st]);
+                        tma_load_2d(sb + hb * (kTWTile / 2), &p.w_map[z], cx, k0, &full[st]);
+                        tma_load_2d(sb + kTWTile + hb * (kTWTile / 2), &p.b_map, cx, k0, &full[st]);
                     }
                 }
-                tma_load_2d(sb + 3 * kTTile, &p.a_map[z], k0, 0, &full[st]);
+                tma_load_2d(sb + 2 * kTWTile, &p.s_map[z], k0, 0, &full[st]);
             }
             for (int i = (t > kTStages ? t - kTStages : 0); i < t; ++i) {  // every issued copy lands before exit
                 const uint64_t t0 = global_timer_ns();
@@ -472,83 +475,102 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(128, kTN) | (MODE == 1 ? (1u << 16) : 0u);
+            const uint32_t idesc = idesc_bf16_f32(kTM, kTNB);
             for (int t = 0; t < nt; ++t) {
                 const int st = t % kTStages;
-                if (!wait(&conv[st], static_cast<uint32_t>(t / kTStages) & 1u)) break;
+                if (!wait(&afull[st], static_cast<uint32_t>(t / kTStages) & 1u)) break;
                 tc_fence_after();
-                const uint32_t sb = smem_u32(ring + static_cast<size_t>(st) * kTStage);
-                const uint64_t adesc = smem_desc_sw128(sb + 3 * kTTile);
+                const uint64_t bdesc = smem_desc_sw128(smem_u32(ring + static_cast<size_t>(st) * kTStage + 2 * kTWTile));
+                const uint32_t acol = tmem + kTACol + 96u * static_cast<uint32_t>(st);
 #pragma unroll
                 for (int kk = 0; kk < kTK / 16; ++kk) {
 #pragma unroll
-                    for (int a = 0; a < 3; ++a) {
-                        const uint64_t bdesc =
-                            MODE == 0 ? smem_desc_sw128(sb + a * kTTile) + static_cast<uint64_t>(2 * kk)
-                                      : smem_desc_mn_sw128(sb + a * kTTile, kTTile / 2) + static_cast<uint64_t>(128 * kk);
-                        mma_ss(tmem, adesc + static_cast<uint64_t>(2 * kk), bdesc, idesc, (t | kk | a) != 0 ? 1u : 0u);
-                    }
+                    for (int a = 0; a < 3; ++a)
+                        mma_ts(tmem + kTDCol, acol + 32u * a + 8u * kk, bdesc + static_cast<uint64_t>(2 * kk), idesc,
+                               (t | kk | a) != 0 ? 1u : 0u);
                 }
                 mma_commit(&empty[st]);
             }
             mma_commit(&done);  // every MMA issued above has finished when this arrives
         }
     } else {
-        // ------------------------------------------------------------ pieces of Delta
-        const int ct = tid - 64;  // 0 .. 255
+        // ------------------------------------------------------------ pieces of Delta -> tensor memory
+        const int q = warp & 3;                  // lane quarter: rows 32 q .. 32 q + 31 of A
+        const int kh = (warp - 2) >> 2;          // K half: 32 reduction indices (16 columns) of each stage
+        const int rl = 32 * q + lane;            // this thread's row of A
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
         for (int t = 0; t < nt; ++t) {
             const int st = t % kTStages;
             if (!__all_sync(0xffffffffu, wait(&full[st], static_cast<uint32_t>(t / kTStages) & 1u))) break;
-            uint4* t1 = reinterpret_cast<uint4*>(ring + static_cast<size_t>(st) * kTStage);
-            uint4* t2 = t1 + kTTile / 16;
-            uint4* t3 = t2 + kTTile / 16;
+            const uint8_t* sb = ring + static_cast<size_t>(st) * kTStage;
+            uint32_t v1[16], v2[16], v3[16];
+            if (MODE == 0) {
+                // row rl of the tiles, 16-byte chunks 4 kh .. 4 kh + 3 (swizzled)
 #pragma unroll
-            for (int c = ct; c < kTTile / 16; c += 32 * kTConvWarps) {
-                const uint4 a = t1[c], b = t2[c];
-                uint4 r1, r2, r3;
-                split_pair(a.x, b.x, r1.x, r2.x, r3.x);
-                split_pair(a.y, b.y, r1.y, r2.y, r3.y);
-                split_pair(a.z, b.z, r1.z, r2.z, r3.z);
-                split_pair(a.w, b.w, r1.w, r2.w, r3.w);
-                t1[c] = r1;
-                t2[c] = r2;
-                t3[c] = r3;
+                for (int c = 0; c < 4; ++c) {
+                    const int off = rl * 128 + (((4 * kh + c) ^ (rl & 7)) << 4);
+                    const uint4 wi = *reinterpret_cast<const uint4*>(sb + off);
+                    const uint4 wb = *reinterpret_cast<const uint4*>(sb + kTWTile + off);
+                    split_pair(wi.x, wb.x, v1[4 * c + 0], v2[4 * c + 0], v3[4 * c + 0]);
+                    split_pair(wi.y, wb.y, v1[4 * c + 1], v2[4 * c + 1], v3[4 * c + 1]);
+                    split_pair(wi.z, wb.z, v1[4 * c + 2], v2[4 * c + 2], v3[4 * c + 2]);
+                    split_pair(wi.w, wb.w, v1[4 * c + 3], v2[4 * c + 3], v3[4 * c + 3]);
+                }
+            } else {
+                // column rl of the tile (box rl / 64, column rl % 64), rows 32 kh .. 32 kh + 31
+                const int bx = rl >> 6, cb = rl & 63;
+                const uint8_t* base = sb + bx * (kTWTile / 2) + (cb & 7) * 2;
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const int r0 = 32 * kh + 2 * j, r1 = r0 + 1;
+                    const int off0 = r0 * 128 + (((cb >> 3) ^ (r0 & 7)) << 4);
+                    const int off1 = r1 * 128 + (((cb >> 3) ^ (r1 & 7)) << 4);
+                    const uint32_t wi = static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(base + off0)) |
+                                        (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(base + off1)) << 16);
+                    const uint32_t wb =
+                        static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(base + kTWTile + off0)) |
+                        (static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(base + kTWTile + off1)) << 16);
+                    split_pair(wi, wb, v1[j], v2[j], v3[j]);
+                }
             }
-            fence_proxy_async_smem();  // the pieces are read by the tensor core (async proxy)
+            const uint32_t acol = lane_addr + kTACol + 96u * static_cast<uint32_t>(st) + 16u * kh;
+            tmem_st16_nowait(acol, v1);
+            tmem_st16_nowait(acol + 32, v2);
+            tmem_st16_nowait(acol + 64, v3);
+            tmem_wait_st();
+            tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&conv[st]);
+            if (lane == 0) mbar_arrive(&afull[st]);
         }
     }
-    // ---------------------------------------------------------------- epilogue (warps 2..5)
+    // ---------------------------------------------------------------- epilogue (warps 2..5): one row of D per thread
     if (warp >= 2 && warp < 6) {
-        const int q = warp & 3;  // tensor-memory lanes 32 q .. 32 q + 31: piece q of the small operand
+        const int q = warp & 3;
         const bool ok = __all_sync(0xffffffffu, wait(&done, 0u)) && !abort;
         tc_fence_after();
-        float* red = reinterpret_cast<float*>(ring);  // [2][kTN][33]: pieces 1 and 2
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        if (ok && (q == 1 || q == 2)) {
-#pragma unroll 1
-            for (int j0 = 0; j0 < kTN; j0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(taddr + j0, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) red[((q - 1) * kTN + j0 + j) * 33 + lane] = __uint_as_float(v[j]);
-            }
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (ok && q == 0) {
+        if (ok) {
+            const int rl = 32 * q + lane;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kTDCol;
+            uint32_t d0[32], d1[32], d2[32];
+            tmem_ld32(taddr, d0);
+            tmem_ld32(taddr + 32, d1);
+            tmem_ld32(taddr + 64, d2);
             const int64_t nrows = MODE == 0 ? p.d_out : p.d_in;
-            float* out = p.part + (static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * nrows * p.l;
-#pragma unroll 1
-            for (int j0 = 0; j0 < kTN; j0 += 32) {
-                uint32_t v[32];
-                tmem_ld32(taddr + j0, v);
+            const int64_t row = o0 + rl;
+            if (row < nrows) {
+                float* out = p.part + ((static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * nrows + row) * p.l;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int n = j0 + j;
-                    const float y = nt > 0 ? (__uint_as_float(v[j]) + red[n * 33 + lane]) + red[(kTN + n) * 33 + lane]
-                                           : 0.0f;
-                    if (lane < p.l && o0 + n < nrows) out[(o0 + n) * p.l + lane] = y;
+                for (int c = 0; c < 32; c += 4) {
+                    if (c >= p.l) break;
+                    float4 y;
+                    y.x = nt > 0 ? (__uint_as_float(d0[c]) + __uint_as_float(d1[c])) + __uint_as_float(d2[c]) : 0.0f;
+                    y.y = nt > 0 ? (__uint_as_float(d0[c + 1]) + __uint_as_float(d1[c + 1])) + __uint_as_float(d2[c + 1])
+                                 : 0.0f;
+                    y.z = nt > 0 ? (__uint_as_float(d0[c + 2]) + __uint_as_float(d1[c + 2])) + __uint_as_float(d2[c + 2])
+                                 : 0.0f;
+                    y.w = nt > 0 ? (__uint_as_float(d0[c + 3]) + __uint_as_float(d1[c + 3])) + __uint_as_float(d2[c + 3])
+                                 : 0.0f;
+                    *reinterpret_cast<float4*>(out + c) = y;
                 }
             }
         }
@@ -1268,8 +1290,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         if (!enc_w(&pr.b_map, a.w_base)) return false;
         for (int z = 0; z < nb; ++z) {
             if (!enc_w(&pr.w_map[z], a.w_ft[i0 + z])) return false;
-            if (!encode_tma_2d(&pr.a_map[z], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Sp + static_cast<size_t>(z) * 128 * Kp,
-                               static_cast<uint64_t>(Kp), 128, static_cast<uint64_t>(Kp) * 2, kTK, 128,
+            if (!encode_tma_2d(&pr.s_map[z], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Sp + static_cast<size_t>(z) * 128 * Kp,
+                               static_cast<uint64_t>(Kp), 128, static_cast<uint64_t>(Kp) * 2, kTK, kTNB,
                                CU_TENSOR_MAP_SWIZZLE_128B))
                 return false;
         }
@@ -1280,7 +1302,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         pr.k_per = per;
         return true;
     };
-    const int64_t tr_blocks = (a.d_out + kTN - 1) / kTN, tc_blocks = a.d_in / kTN;
+    const int64_t tr_blocks = (a.d_out + kTM - 1) / kTM, tc_blocks = a.d_in / kTM;
     // Y_z = Delta_z S_z for the batch (S_z = Omega, or Z_z with zs)
     auto sketch = [&](int i0, int nb, bool zs) {
         if (perr != cudaSuccess) return;
@@ -1291,7 +1313,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             split_small_kernel<<<dim3(blocks_for(kp), static_cast<unsigned>(nb)), 256, 0, st>>>(
                 zs ? Zall + static_cast<size_t>(i0) * a.d_in * l : a.omega,
                 zs ? static_cast<int64_t>(a.d_in) * l : 0, a.d_in, kp, l, Sp);
-            if (!tprep(tp_sk, i0, nb, kp, Yp, per, kTN)) {
+            if (!tprep(tp_sk, i0, nb, kp, Yp, per, kTM)) {
                 perr = cudaErrorInvalidValue;
                 return;
             }
