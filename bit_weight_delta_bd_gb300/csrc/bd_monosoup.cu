@@ -1074,87 +1074,224 @@ __global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ 
         if (4 * jg + t < m) dst[static_cast<int64_t>(4 * jg + t) * n + row] = acc[t];
 }
 
-// out[row][j] = W_base[row][j] + inv_k * sum_e L[e][row] Rt[e][j], e over the
-// k * r factor columns (L [k r][d_out], Rt [k r][d_in]).  CTA: 128 x 128
-// outputs, 8 x 8 per thread: rows 8 ty .. 8 ty + 7, columns 4 tx .. 4 tx + 3
-// and 64 + 4 tx .. (so that the 16-byte reads of a quarter warp cover the 32
-// banks once).  The factors of its rows and columns are staged in shared
-// memory k-major with coalesced loads, in chunks of 48 factor columns;
-// paired FMAs.  The sum runs over e in order; the result is rounded once to
-// the output type.
-constexpr int kMergeTile = 128;
-constexpr int kMergeK = 48;
+// ---------------------------------------------------------------- the merge on the tensor cores
+// out[row][j] = W_base[row][j] + inv_k * sum_e L[e][row] R[e][j], e over the
+// K = k r factor columns (L [K][d_out], R [K][d_in] as written by
+// apply_t_kernel), rounded once to the output type.  Every factor value is
+// split into three bf16 pieces (as for the products) and the six piece pairs
+// (1,1), (1,2), (2,1), (1,3), (2,2), (3,1) are stacked along the reduction:
+// Ls[row][p K + e] = piece a_p of L[e][row], Rs[j][p K + e] = piece b_p of
+// R[e][j] (split_factors_kernel; a piece after the first is below 2^-7 of the
+// value's magnitude and the third below 2^-15, so the three pairs left out
+// add up to less than 2^-21 |L[e][row] R[e][j]|), zero-padded to Kp = 6 K
+// rounded up to 64.  A CTA
+// computes 128 rows x 256 columns: D = Ls Rs^T in tensor memory (M = 128,
+// N = 256, K = 16 MMAs; A and B K-major in shared memory, two 48 KB stages),
+// then warps 2..9 add W_base row by row (lane quarter warp % 4, column half
+// (warp - 2) / 4; the W_base loads of the next 32 columns are issued before
+// the current ones are used).  Two CTAs per SM.
+constexpr int kMgM = 128;
+constexpr int kMgN = 256;
+constexpr int kMgStages = 2;
+constexpr int kMgATile = kMgM * 128;          // 64 reduction indices x 128 rows, bf16: 16 KB
+constexpr int kMgBTile = kMgN * 128;          // 64 x 256: 32 KB
+constexpr int kMgStage = kMgATile + kMgBTile;
+constexpr int kMgThreads = 320;               // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr uint32_t kMgTmemCols = kMgN;
+constexpr int kMgPairs = 6;
 
-__global__ void __launch_bounds__(256, 2) merge_kernel(const uint16_t* __restrict__ wb, int64_t d_out, int64_t d_in,
-                                                       const float* __restrict__ L, const float* __restrict__ Rt, int k,
-                                                       int r, float inv_k, void* __restrict__ out, int out_f32)
+__device__ __forceinline__ int merge_piece(int p, int side)
 {
-    __shared__ __align__(16) float sl[kMergeK][kMergeTile];
-    __shared__ __align__(16) float sr[kMergeK][kMergeTile];
-    const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * kMergeTile, j0 = static_cast<int64_t>(blockIdx.x) * kMergeTile;
-    float2 acc[8][4];
+    // piece index (0, 1, 2) of the L side (side 0) or the R side (side 1) in pair p
+    const int a = p == 2 ? 1 : (p == 4 ? 1 : (p == 5 ? 2 : 0));
+    const int b = p == 1 ? 1 : (p == 3 ? 2 : (p == 4 ? 1 : 0));
+    return side == 0 ? a : b;
+}
+
+// dst[n][kk] (kk < Kp; n < rows) = piece merge_piece(kk / K, side) of
+// src[kk % K][n] for kk < 6 K, else 0.  Thread: one row and 8 consecutive kk
+// (one 16-byte store); rows vary fastest, so the reads of src are coalesced.
+__global__ void __launch_bounds__(256) split_factors_kernel(const float* __restrict__ src, int64_t rows, int K, int Kp,
+                                                            int side, uint16_t* __restrict__ dst)
+{
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t g = idx / rows, n = idx - g * rows;
+    if (g >= Kp / 8) return;
+    uint32_t w[4];
 #pragma unroll
-    for (int x = 0; x < 8; ++x)
-#pragma unroll
-        for (int y = 0; y < 4; ++y) acc[x][y] = make_float2(0.0f, 0.0f);
-    const int K = k * r;
-    const int rr = tid & (kMergeTile - 1), e_lo = tid >> 7;
-    for (int e0 = 0; e0 < K; e0 += kMergeK) {
-        __syncthreads();
-        const int64_t row = r0 + rr, col = j0 + rr;
-#pragma unroll 4
-        for (int ee = e_lo; ee < kMergeK; ee += 2) {
-            const int f = e0 + ee;
-            sl[ee][rr] = (f < K && row < d_out) ? L[static_cast<int64_t>(f) * d_out + row] : 0.0f;
-            sr[ee][rr] = (f < K && col < d_in) ? Rt[static_cast<int64_t>(f) * d_in + col] : 0.0f;
+    for (int j = 0; j < 8; ++j) {
+        const int kk = static_cast<int>(8 * g) + j;
+        const int pr = kk / K, e = kk - pr * K;
+        uint32_t h = 0;
+        if (pr < kMgPairs) {
+            const float v = src[static_cast<int64_t>(e) * rows + n];
+            const int pc = merge_piece(pr, side);
+            const uint32_t b1 = __float_as_uint(v) & 0xFFFF0000u;
+            const float r1 = __fsub_rn(v, __uint_as_float(b1));
+            const uint32_t b2 = __float_as_uint(r1) & 0xFFFF0000u;
+            const float r2 = __fsub_rn(r1, __uint_as_float(b2));
+            h = (pc == 0 ? b1 : (pc == 1 ? b2 : __float_as_uint(r2))) >> 16;
         }
-        __syncthreads();
-        const int ne = K - e0 < kMergeK ? K - e0 : kMergeK;
-        for (int ee = 0; ee < ne; ++ee) {
-            const float4 a0 = *reinterpret_cast<const float4*>(&sl[ee][8 * ty]);
-            const float4 a1 = *reinterpret_cast<const float4*>(&sl[ee][8 * ty + 4]);
-            const float4 b0 = *reinterpret_cast<const float4*>(&sr[ee][4 * tx]);
-            const float4 b1 = *reinterpret_cast<const float4*>(&sr[ee][64 + 4 * tx]);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+        if (j & 1)
+            w[j >> 1] |= h << 16;
+        else
+            w[j >> 1] = h;
+    }
+    *reinterpret_cast<uint4*>(dst + n * Kp + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+struct MergeParams {
+    CUtensorMap a_map;  // Ls [d_out][Kp] bf16, box 64 x 128, 128-byte swizzle
+    CUtensorMap b_map;  // Rs [d_in][Kp] bf16, box 64 x 256, 128-byte swizzle
+    const uint16_t* wb;
+    void* out;
+    int64_t d_out, d_in;
+    int nk;             // Kp / 64 (0: rank 0, out = W_base)
+    float inv_k;
+    int out_f32;
+};
+
+__global__ void __launch_bounds__(kMgThreads, 2) merge_tc_kernel(const __grid_constant__ MergeParams p)
+{
+    extern __shared__ uint8_t dyn_raw[];
+    __shared__ uint64_t full[kMgStages], empty[kMgStages];
+    __shared__ uint64_t done;
+    __shared__ uint32_t tmem_base;
+    __shared__ volatile int abort;
+    uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row0 = static_cast<int64_t>(blockIdx.y) * kMgM, col0 = static_cast<int64_t>(blockIdx.x) * kMgN;
+    const int nk = p.nk;
+    if (tid == 0) {
+        for (int st = 0; st < kMgStages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], 1);
+        }
+        mbar_init(&done, 1);
+        abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == 1) tmem_alloc(&tmem_base, kMgTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base;
+    auto wait = [&](uint64_t* bar, uint32_t par) {
+        if (mbar_try_wait(bar, par)) return true;
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(bar, par)) {
+            if (abort) return false;
+            if (global_timer_ns() - t0 > kWaitLimitNs) {
+                abort = 1;
+                return false;
+            }
+        }
+        return true;
+    };
+    if (warp == 0) {
+        if (lane == 0) {
+            int t = 0;
+            for (; t < nk; ++t) {
+                const int st = t % kMgStages;
+                if (t >= kMgStages && !wait(&empty[st], static_cast<uint32_t>(t / kMgStages - 1) & 1u)) break;
+                uint8_t* sb = ring + static_cast<size_t>(st) * kMgStage;
+                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kMgStage));
+                tma_load_2d(sb, &p.a_map, 64 * t, static_cast<int>(row0), &full[st]);
+                tma_load_2d(sb + kMgATile, &p.b_map, 64 * t, static_cast<int>(col0), &full[st]);
+            }
+            for (int i = (t > kMgStages ? t - kMgStages : 0); i < t; ++i) {  // every issued copy lands before exit
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&full[i % kMgStages], static_cast<uint32_t>(i / kMgStages) & 1u) &&
+                       global_timer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kMgM, kMgN);
+            for (int t = 0; t < nk; ++t) {
+                const int st = t % kMgStages;
+                if (!wait(&full[st], static_cast<uint32_t>(t / kMgStages) & 1u)) break;
+                tc_fence_after();
+                const uint32_t sb = smem_u32(ring + static_cast<size_t>(st) * kMgStage);
+                const uint64_t adesc = smem_desc_sw128(sb), bdesc = smem_desc_sw128(sb + kMgATile);
 #pragma unroll
-            for (int x = 0; x < 8; ++x) {
-                ffma2(acc[x][0], av[x], b0.x, b0.y);
-                ffma2(acc[x][1], av[x], b0.z, b0.w);
-                ffma2(acc[x][2], av[x], b1.x, b1.y);
-                ffma2(acc[x][3], av[x], b1.z, b1.w);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_ss(tmem, adesc + static_cast<uint64_t>(2 * kk), bdesc + static_cast<uint64_t>(2 * kk), idesc,
+                           (t | kk) != 0 ? 1u : 0u);
+                mma_commit(&empty[st]);
+            }
+            mma_commit(&done);
+        }
+    } else {
+        // epilogue: one row per thread (lane quarter warp % 4), columns
+        // 128 hc .. 128 hc + 127 in chunks of 32
+        const int q = warp & 3, hc = (warp - 2) >> 2;
+        const bool ok = __all_sync(0xffffffffu, wait(&done, 0u)) && !abort;
+        tc_fence_after();
+        const int64_t row = row0 + 32 * q + lane;
+        const bool live = row < p.d_out;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128u * hc;
+        const int64_t cbase = col0 + 128 * hc;
+        const int nch = cbase >= p.d_in ? 0 : static_cast<int>((p.d_in - cbase < 128 ? p.d_in - cbase : 128) / 32);
+        uint4 wn[4];
+        auto load_w = [&](int ch) {
+            if (live && ch < nch) {
+                const uint4* wr = reinterpret_cast<const uint4*>(p.wb + row * p.d_in + cbase + 32 * ch);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) wn[c] = wr[c];
+            }
+        };
+        if (ok) {
+            load_w(0);
+#pragma unroll 1
+            for (int ch = 0; ch < nch; ++ch) {
+                const uint4 wcur[4] = {wn[0], wn[1], wn[2], wn[3]};
+                load_w(ch + 1);
+                uint32_t v[32];
+                tmem_ld32(taddr + 32 * ch, v);
+                if (!live) continue;
+                const int64_t col = cbase + 32 * ch;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const uint32_t wv[4] = {wcur[c].x, wcur[c].y, wcur[c].z, wcur[c].w};
+                    float o[8];
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float a0 = nk > 0 ? __uint_as_float(v[8 * c + 2 * u]) : 0.0f;
+                        const float a1 = nk > 0 ? __uint_as_float(v[8 * c + 2 * u + 1]) : 0.0f;
+                        o[2 * u] = bf16_bits_to_float(wv[u] & 0xFFFFu) + p.inv_k * a0;
+                        o[2 * u + 1] = bf16_bits_to_float(wv[u] >> 16) + p.inv_k * a1;
+                    }
+                    if (p.out_f32) {
+                        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * p.d_in + col + 8 * c);
+                        dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+                        dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+                    } else {
+                        uint32_t ob[4];
+#pragma unroll
+                        for (int u = 0; u < 4; ++u)
+                            ob[u] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o[2 * u]))) |
+                                    (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o[2 * u + 1]))) << 16);
+                        *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.d_in + col + 8 * c) =
+                            make_uint4(ob[0], ob[1], ob[2], ob[3]);
+                    }
+                }
             }
         }
     }
-#pragma unroll
-    for (int x = 0; x < 8; ++x) {
-        const int64_t row = r0 + 8 * ty + x;
-        if (row >= d_out) continue;
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int64_t col = j0 + 64 * h + 4 * tx;
-            const uint2 w = *reinterpret_cast<const uint2*>(wb + row * d_in + col);
-            const float v0 = bf16_bits_to_float(w.x & 0xFFFFu) + inv_k * acc[x][2 * h].x;
-            const float v1 = bf16_bits_to_float(w.x >> 16) + inv_k * acc[x][2 * h].y;
-            const float v2 = bf16_bits_to_float(w.y & 0xFFFFu) + inv_k * acc[x][2 * h + 1].x;
-            const float v3 = bf16_bits_to_float(w.y >> 16) + inv_k * acc[x][2 * h + 1].y;
-            if (out_f32) {
-                *reinterpret_cast<float4*>(static_cast<float*>(out) + row * d_in + col) = make_float4(v0, v1, v2, v3);
-            } else {
-                const uint32_t o0 = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v0))) |
-                                    (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v1))) << 16);
-                const uint32_t o1 = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v2))) |
-                                    (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(v3))) << 16);
-                *reinterpret_cast<uint2*>(static_cast<uint16_t*>(out) + row * d_in + col) = make_uint2(o0, o1);
-            }
-        }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kMgTmemCols);
     }
 }
 
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 
 struct MonoSoupWs {
-    size_t y, z, ypart, zpart, part, g, gk, m, uk, L, Rt, sp, total;
+    size_t y, z, ypart, zpart, part, g, gk, m, uk, L, Rt, sp, ls, rs, total;
 };
 
 MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
@@ -1180,6 +1317,10 @@ MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
     // split small operands of a batch for the tensor-core products (l <= 32)
     const size_t kp = static_cast<size_t>(((d_in > d_out ? d_in : d_out) + 63) / 64 * 64);
     w.sp = take(l <= 32 ? static_cast<size_t>(kMaxBatch) * 128 * kp * 2 : 0);
+    // the split factors of the merge: [rows][Kp] bf16, Kp = 6 k r rounded up to 64
+    const size_t kpm = static_cast<size_t>((kMgPairs * k * (r > 0 ? r : 1) + 63) / 64 * 64);
+    w.ls = take(static_cast<size_t>(d_out) * kpm * 2);
+    w.rs = take(static_cast<size_t>(d_in) * kpm * 2);
     w.total = off;
     return w;
 }
@@ -1209,6 +1350,9 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     constexpr size_t kTSmem = static_cast<size_t>(kTStages) * kTStage + 1024;
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<0>), kTSmem, t0c);
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<1>), kTSmem, t1c);
+    static std::atomic<size_t> mgc[kHostMaxDevices];
+    constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + 1024;
+    if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(merge_tc_kernel), kMgSmem, mgc);
     if (e0 != cudaSuccess) return e0;
     const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
     char* w = static_cast<char*>(a.ws);
@@ -1420,10 +1564,32 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                                                                                                  r, Rt);
     }
     if (perr != cudaSuccess) return perr;
-    const dim3 grid(static_cast<unsigned>((a.d_in + kMergeTile - 1) / kMergeTile),
-                    static_cast<unsigned>((a.d_out + kMergeTile - 1) / kMergeTile));
-    merge_kernel<<<grid, 256, 0, st>>>(a.w_base, a.d_out, a.d_in, L, Rt, r > 0 ? a.k : 0, r,
-                                       1.0f / static_cast<float>(a.k), a.out, a.out_f32);
+    // the merge: split factors, then D = Ls Rs^T + W_base on the tensor cores
+    const int K = r > 0 ? a.k * r : 0;
+    const int Kp = (kMgPairs * (K > 0 ? K : 1) + 63) / 64 * 64;
+    uint16_t* Ls = reinterpret_cast<uint16_t*>(w + lay.ls);
+    uint16_t* Rs = reinterpret_cast<uint16_t*>(w + lay.rs);
+    static thread_local MergeParams mp;
+    if (K > 0) {
+        split_factors_kernel<<<blocks_for(a.d_out * (Kp / 8)), 256, 0, st>>>(L, a.d_out, K, Kp, 0, Ls);
+        split_factors_kernel<<<blocks_for(a.d_in * (Kp / 8)), 256, 0, st>>>(Rt, a.d_in, K, Kp, 1, Rs);
+    }
+    if (!encode_tma_2d(&mp.a_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ls, static_cast<uint64_t>(Kp),
+                       static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(Kp) * 2, 64, kMgM,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tma_2d(&mp.b_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Rs, static_cast<uint64_t>(Kp),
+                       static_cast<uint64_t>(a.d_in), static_cast<uint64_t>(Kp) * 2, 64, kMgN,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    mp.wb = a.w_base;
+    mp.out = a.out;
+    mp.d_out = a.d_out;
+    mp.d_in = a.d_in;
+    mp.nk = K > 0 ? Kp / 64 : 0;
+    mp.inv_k = 1.0f / static_cast<float>(a.k);
+    mp.out_f32 = a.out_f32;
+    const dim3 grid(static_cast<unsigned>((a.d_in + kMgN - 1) / kMgN), static_cast<unsigned>((a.d_out + kMgM - 1) / kMgM));
+    merge_tc_kernel<<<grid, kMgThreads, kMgSmem, st>>>(mp);
     return cudaGetLastError();
 }
 
