@@ -42,7 +42,7 @@ namespace bd {
 namespace {
 
 constexpr int kMaxL = 64;        // sketch width l (columns of Y, Q, B^T)
-constexpr int kGramBlocks = 152;  // CTAs of one Gram pass (fixed-order float-float partials)
+constexpr int kGramParts = 304;   // CTAs of one Gram pass (fixed-order float-float partials)
 constexpr int kGramThreads = 1024;
 constexpr int kSlices = 16;       // partial results of one product pass (over the checkpoints of a batch)
 constexpr int kMaxBatch = 8;      // checkpoints that go through the steps together
@@ -365,26 +365,58 @@ __device__ __forceinline__ void split_pair(uint32_t wi, uint32_t wb, uint32_t& o
     o3 = __byte_perm(__float_as_uint(sl), __float_as_uint(sh), 0x7632);
 }
 
-// Sp[z][32 b + c][k] = piece b of S_z[k][c] (c < l, b < 3, k < K), zero in
-// the other rows and in the columns K .. Kp - 1 (rows of Kp elements, Kp = K
-// rounded up to 64); S_z = S + z zstride ([K][l] fp32), z = blockIdx.y.
+// Sp[z][32 b + c][k] = piece b of S_z[k][c] (c < l, b < 3, k < K), zero for
+// c >= l and in the columns K .. Kp - 1 (rows of Kp elements, Kp = K rounded
+// up to 64; rows 96 .. 127 are not read); S_z = S + z zstride ([K][l] fp32,
+// l a multiple of 4), z = blockIdx.y.  Thread: 8 consecutive k (lane: k
+// group 32 blockIdx.x + lane) and 4 columns (warp w: columns 4 w .. 4 w + 3),
+// one 16-byte store per row; 256 threads.
 __global__ void __launch_bounds__(256) split_small_kernel(const float* __restrict__ S, int64_t zstride, int64_t K,
                                                           int64_t Kp, int l, uint16_t* __restrict__ Sp)
 {
-    const int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (k >= Kp) return;
-    const float* src = S + blockIdx.y * zstride + k * l;
-    uint16_t* o = Sp + static_cast<int64_t>(blockIdx.y) * 128 * Kp + k;
-    for (int c = 0; c < 32; ++c) {
-        const float v = (c < l && k < K) ? src[c] : 0.0f;
-        const uint32_t b1 = __float_as_uint(v) & 0xFFFF0000u;
-        const float r1 = __fsub_rn(v, __uint_as_float(b1));
-        const uint32_t b2 = __float_as_uint(r1) & 0xFFFF0000u;
-        const float r2 = __fsub_rn(r1, __uint_as_float(b2));
-        o[c * Kp] = static_cast<uint16_t>(b1 >> 16);
-        o[(32 + c) * Kp] = static_cast<uint16_t>(b2 >> 16);
-        o[(64 + c) * Kp] = static_cast<uint16_t>(__float_as_uint(r2) >> 16);
-        o[(96 + c) * Kp] = 0;
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * 32 + (threadIdx.x & 31);
+    if (8 * g >= Kp) return;
+    const float* src = S + blockIdx.y * zstride;
+    uint16_t* o = Sp + static_cast<int64_t>(blockIdx.y) * 128 * Kp + 8 * g;
+    {
+        const int c0 = 4 * static_cast<int>(threadIdx.x >> 5);
+        float v[8][4];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int64_t k = 8 * g + j;
+            const float4 f = (k < K && c0 < l) ? *reinterpret_cast<const float4*>(src + k * l + c0)
+                                               : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            v[j][0] = f.x;
+            v[j][1] = f.y;
+            v[j][2] = f.z;
+            v[j][3] = f.w;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t w1[4], w2[4], w3[4];
+#pragma unroll
+            for (int j = 0; j < 8; j += 2) {
+                uint32_t p1[2], p2[2], p3[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const float x = v[j + e][cc];
+                    const uint32_t b1 = __float_as_uint(x) & 0xFFFF0000u;
+                    const float r1 = __fsub_rn(x, __uint_as_float(b1));
+                    const uint32_t b2 = __float_as_uint(r1) & 0xFFFF0000u;
+                    const float r2 = __fsub_rn(r1, __uint_as_float(b2));
+                    p1[e] = b1;
+                    p2[e] = b2;
+                    p3[e] = __float_as_uint(r2);
+                }
+                w1[j / 2] = __byte_perm(p1[0], p1[1], 0x7632);
+                w2[j / 2] = __byte_perm(p2[0], p2[1], 0x7632);
+                w3[j / 2] = __byte_perm(p3[0], p3[1], 0x7632);
+            }
+            const int c = c0 + cc;
+            *reinterpret_cast<uint4*>(o + static_cast<int64_t>(c) * Kp) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
+            *reinterpret_cast<uint4*>(o + static_cast<int64_t>(32 + c) * Kp) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
+            *reinterpret_cast<uint4*>(o + static_cast<int64_t>(64 + c) * Kp) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
+        }
     }
 }
 
@@ -635,31 +667,41 @@ __device__ __forceinline__ void ff_add(float& s, float& c, float x, float y)
 
 // Partial Gram matrices of A_z [n][l] (checkpoint z = blockIdx.y, the A_z
 // consecutive): CTA b sums A_z^T A_z over its contiguous row range in
-// float-float into part[z][b][l * l] (entry i * l + j as (hi, lo)); ENT =
-// entries per thread (l * l <= 1024 ENT).
+// float-float into part[z][b][l * l] (entry i * l + j as (hi, lo)).  Only the
+// l (l + 1) / 2 entries i <= j are summed (ENT per thread, blockDim.x threads
+// of consecutive entries; ENT = 1 takes at most kGramThreads1 threads and
+// runs two CTAs per SM); each is stored at (i, j) and (j, i).
+constexpr int kGramThreads1 = 576;
 template <int ENT>
-__global__ void __launch_bounds__(kGramThreads) gram_kernel(const float* __restrict__ a_all, int64_t n, int l,
+__global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT == 1 ? 2 : 1) gram_kernel(const float* __restrict__ a_all, int64_t n, int l,
                                                             float2* __restrict__ part_all)
 {
     __shared__ float sa[32][kMaxL + 1];
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, nt = blockDim.x;
     const float* a = a_all + static_cast<int64_t>(blockIdx.y) * n * l;
     float2* part = part_all + static_cast<int64_t>(blockIdx.y) * gridDim.x * l * l;
     const int64_t per = (n + gridDim.x - 1) / gridDim.x;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * per;
     const int64_t b1 = b0 + per < n ? b0 + per : n;
-    const int ll = l * l;
+    const int np = l * (l + 1) / 2;
     int pi[ENT], pj[ENT];
     float s[ENT], c[ENT];
 #pragma unroll
     for (int m = 0; m < ENT; ++m) {
-        const int p = tid + kGramThreads * m;
-        pi[m] = p < ll ? p / l : 0;  // past l * l: a dummy entry, never stored
-        pj[m] = p < ll ? p % l : 0;
+        int u = tid + nt * m;
+        int i = 0;
+        if (u < np) {
+            while (u >= l - i) {  // u -> (i, j), i <= j, row-major over the upper triangle
+                u -= l - i;
+                ++i;
+            }
+        }
+        pi[m] = u < np ? i : 0;  // past the triangle: a dummy entry, never stored
+        pj[m] = u < np ? i + u : 0;
         s[m] = c[m] = 0.0f;
     }
     for (int64_t r0 = b0; r0 < b1; r0 += 32) {
-        for (int e = tid; e < 32 * kMaxL; e += kGramThreads) {
+        for (int e = tid; e < 32 * kMaxL; e += nt) {
             const int rr = e >> 6, cc = e & 63;
             const int64_t row = r0 + rr;
             sa[rr][cc] = (row < b1 && cc < l) ? a[row * l + cc] : 0.0f;
@@ -674,11 +716,12 @@ __global__ void __launch_bounds__(kGramThreads) gram_kernel(const float* __restr
     }
 #pragma unroll
     for (int m = 0; m < ENT; ++m) {
-        const int p = tid + kGramThreads * m;
-        if (p < ll) {
+        if (tid + nt * m < np) {
             float hi, lo;
             two_sum(s[m], c[m], hi, lo);
-            part[static_cast<int64_t>(blockIdx.x) * ll + p] = make_float2(hi, lo);
+            const int64_t pb = static_cast<int64_t>(blockIdx.x) * l * l;
+            part[pb + pi[m] * l + pj[m]] = make_float2(hi, lo);
+            part[pb + pj[m] * l + pi[m]] = make_float2(hi, lo);
         }
     }
 }
@@ -838,9 +881,13 @@ __global__ void __launch_bounds__(256) chol_kernel(const float2* __restrict__ G_
 // than QR", 1992, with an absolute floor for the null space of a
 // rank-deficient sketch); the iteration stops after a sweep without a
 // rotation (at most 40 sweeps).  The rotation of a pair: theta = (a_qq -
-// a_pp) / (2 a_pq), t = sign(theta) / (|theta| + sqrt(theta^2 + 1)), c = 1 /
-// sqrt(1 + t^2) (rsqrt and one Newton step), s = t c; a_pq becomes exactly 0
-// and the diagonal moves by -/+ t a_pq.  A round is A <- P^T A P and
+// a_pp) / (2 a_pq), t = sign(theta) / (|theta| + sqrt(theta^2 + 1)) (from the
+// approximate reciprocal and reciprocal square root: an angle off by about
+// 2^-21 only leaves a residue of that size of a_pq), c = 1 / sqrt(1 + t^2)
+// (rsqrt and one Newton step, so that c^2 + s^2 = 1 to fp32 accuracy),
+// s = t c; a_pq becomes exactly 0 and the diagonal moves by -/+ t a_pq.  The
+// parameters of a round's pairs sit in one float4 each (c, s, t, p | q << 8)
+// so that an update reads them with one load.  A round is A <- P^T A P and
 // V <- V P for the rotations P of its n/2 pairs: every 2 x 2 block of A at
 // (row pair, column pair) and every (row, column pair) of V is updated in
 // place by one thread, so a round needs two barriers.  ur[i][m] = the
@@ -859,8 +906,7 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __
     float* ur = ur_all + static_cast<size_t>(blockIdx.x) * l * r;
     __shared__ float A[kMaxL][kMaxL + 1];
     __shared__ float V[kMaxL][kMaxL + 1];
-    __shared__ float cs[kMaxL / 2], sn[kMaxL / 2], tn[kMaxL / 2];
-    __shared__ int pp[kMaxL / 2], qq[kMaxL / 2];
+    __shared__ float4 prm[kMaxL / 2];  // this round's pairs: c, s, t, p | q << 8
     __shared__ unsigned char tp[kMaxL][kMaxL / 2], tq[kMaxL][kMaxL / 2];  // round-robin pairs of every round
     __shared__ int idx[kMaxL];
     __shared__ float vnorm[kMaxL];
@@ -916,10 +962,15 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __
                 float c = 1.0f, sv = 0.0f, tt = 0.0f;
                 if (q < l) {
                     const float apq = A[p][q], app = A[p][p], aqq = A[q][q];
-                    if (fabsf(apq) > athr && fabsf(apq) > 0x1p-22f * sqrtf(fabsf(app)) * sqrtf(fabsf(aqq))) {
+                    if (fabsf(apq) > athr && apq * apq > 0x1p-44f * fabsf(app * aqq)) {
                         rotated[par] = 1;
-                        const float th = __fdividef(aqq - app, 2.0f * apq);
-                        tt = copysignf(__fdividef(1.0f, fabsf(th) + sqrtf(fmaf(th, th, 1.0f))), th);
+                        float rc, rs, rd;
+                        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(2.0f * apq));
+                        const float th = (aqq - app) * rc;
+                        const float w = fmaf(th, th, 1.0f);
+                        asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(rs) : "f"(w));
+                        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rd) : "f"(fabsf(th) + w * rs));
+                        tt = copysignf(rd, th);
                         const float x = fmaf(tt, tt, 1.0f);
                         float y = rsqrtf(x);
                         y = y * fmaf(-0.5f * x * y, y, 1.5f);
@@ -927,11 +978,7 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __
                         sv = tt * y;
                     }
                 }
-                cs[tid] = c;
-                sn[tid] = sv;
-                tn[tid] = tt;
-                pp[tid] = p;
-                qq[tid] = q;
+                prm[tid] = make_float4(c, sv, tt, __int_as_float(p | (q << 8)));
             }
             __syncthreads();
             // every thread has read the previous sweep's flag: clear it for the next sweep
@@ -941,15 +988,17 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __
             for (int u = 0; u < kJacobiBlocks; ++u) {
                 const int bi = bi_[u], bj = bj_[u];
                 if (bi < 0) break;
-                const int p = pp[bi], q = qq[bi], p2 = pp[bj], q2 = qq[bj];
-                const float ci = cs[bi], si = sn[bi], cj = cs[bj], sj = sn[bj];
+                const float4 fi = prm[bi], fj = prm[bj];
+                const int pqi = __float_as_int(fi.w), pqj = __float_as_int(fj.w);
+                const int p = pqi & 255, q = pqi >> 8, p2 = pqj & 255, q2 = pqj >> 8;
+                const float ci = fi.x, si = fi.y, cj = fj.x, sj = fj.y;
                 const bool rq = q < l, cq = q2 < l;
                 const float a_pp = A[p][p2], a_pq = cq ? A[p][q2] : 0.0f;
                 const float a_qp = rq ? A[q][p2] : 0.0f, a_qq = (rq && cq) ? A[q][q2] : 0.0f;
                 if (bi == bj && si != 0.0f) {
                     // the rotated pair itself: a_pq is annihilated exactly and
                     // the diagonal moves by t a_pq
-                    const float ta = tn[bi] * a_pq;
+                    const float ta = fi.z * a_pq;
                     A[p][p] = a_pp - ta;
                     A[q][q] = a_qq + ta;
                     A[p][q] = 0.0f;
@@ -968,9 +1017,10 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __
             for (int u = 0; u < kJacobiVItems; ++u) {
                 const int row = vr_[u], bj = vb_[u];
                 if (row < 0) break;
-                const int p2 = pp[bj], q2 = qq[bj];
-                if (q2 >= l) continue;
-                const float cj = cs[bj], sj = sn[bj];
+                const float4 fj = prm[bj];
+                const int p2 = __float_as_int(fj.w) & 255, q2 = __float_as_int(fj.w) >> 8;
+                if (q2 >= l || fj.y == 0.0f) continue;
+                const float cj = fj.x, sj = fj.y;
                 const float vp = V[row][p2], vq = V[row][q2];
                 V[row][p2] = cj * vp - sj * vq;
                 V[row][q2] = sj * vp + cj * vq;
@@ -1307,7 +1357,7 @@ MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
     w.z = take(static_cast<size_t>(k) * d_in * l * 4);   // B_i^T of every checkpoint
     w.ypart = take(static_cast<size_t>(kSlices) * d_out * l * 4);
     w.zpart = take(static_cast<size_t>(kSlices) * d_in * l * 4);
-    w.part = take(static_cast<size_t>(kGramBlocks) * l * l * 8);  // Gram partials of a batch (float2)
+    w.part = take(static_cast<size_t>(kGramParts) * l * l * 8);   // Gram partials of a batch (float2)
     w.g = take(static_cast<size_t>(kMaxBatch) * l * l * 8);       // Gram matrices of a batch (float2)
     w.gk = take(static_cast<size_t>(k) * l * l * 8);              // B_i B_i^T of every checkpoint (float2)
     w.m = take(static_cast<size_t>(kMaxBatch) * (kMaxL * kMaxL + kMaxL) * 4);  // R and 1/diag(R) of a batch
@@ -1454,7 +1504,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         if (tc) {
             const int ns = slices(tr_blocks, a.d_in, nb, &per);
             const int64_t kp = (a.d_in + 63) / 64 * 64;
-            split_small_kernel<<<dim3(blocks_for(kp), static_cast<unsigned>(nb)), 256, 0, st>>>(
+            split_small_kernel<<<dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st>>>(
                 zs ? Zall + static_cast<size_t>(i0) * a.d_in * l : a.omega,
                 zs ? static_cast<int64_t>(a.d_in) * l : 0, a.d_in, kp, l, Sp);
             if (!tprep(tp_sk, i0, nb, kp, Yp, per, kTM)) {
@@ -1491,7 +1541,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         if (tc) {
             const int ns = slices(tc_blocks, a.d_out, nb, &per);
             const int64_t kp = (a.d_out + 63) / 64 * 64;
-            split_small_kernel<<<dim3(blocks_for(kp), static_cast<unsigned>(nb)), 256, 0, st>>>(
+            split_small_kernel<<<dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st>>>(
                 Yall + static_cast<size_t>(i0) * a.d_out * l, static_cast<int64_t>(a.d_out) * l, a.d_out, kp, l, Sp);
             if (!tprep(tp_lf, i0, nb, kp, Zp, per, 64)) {
                 perr = cudaErrorInvalidValue;
@@ -1519,13 +1569,20 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
     };
     // out_z = A_z^T A_z for the nb consecutive A_z [n][l]
+    // the upper triangle's l (l + 1) / 2 entries: one per thread up to
+    // kGramThreads1 threads (two CTAs per SM), else 2 or 3 per thread
+    const int npairs = l * (l + 1) / 2;
+    const int gent = npairs <= kGramThreads1 ? 1 : (npairs <= 2 * kGramThreads ? 2 : 3);
+    const int gthreads = ((npairs + gent - 1) / gent + 31) / 32 * 32;
     auto gram = [&](const float* A, int64_t n, int nb, float2* out) {
-        const int gb = kGramBlocks / nb;
+        const int gb = kGramParts / nb;
         const dim3 g(static_cast<unsigned>(gb), static_cast<unsigned>(nb));
-        if (ll <= kGramThreads)
-            gram_kernel<1><<<g, kGramThreads, 0, st>>>(A, n, l, part);
+        if (gent == 1)
+            gram_kernel<1><<<g, gthreads, 0, st>>>(A, n, l, part);
+        else if (gent == 2)
+            gram_kernel<2><<<g, gthreads, 0, st>>>(A, n, l, part);
         else
-            gram_kernel<4><<<g, kGramThreads, 0, st>>>(A, n, l, part);
+            gram_kernel<3><<<g, gthreads, 0, st>>>(A, n, l, part);
         gram_sum_kernel<<<dim3(blocks_for(32 * ll), static_cast<unsigned>(nb)), 256, 0, st>>>(part, gb, l, out);
     };
     // A_z <- A_z R_z^-1 (CholeskyQR), `passes` times: two (CholeskyQR2) for
