@@ -78,13 +78,14 @@ NCU_TRAFFIC = {
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =
 # router + plan + gather + grouped prefill; monosoup = the merge's launches
-LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4, "monosoup": 88}
+LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4, "monosoup": 36}
 # workloads whose own figure is tensor throughput (TFLOP/s) rather than GB/s
 TENSOR_WORKLOADS = ("prefill", "multi_prefill")
-# workloads bound by fp32 CUDA-core arithmetic: their figure is fp32 TFLOP/s
-ALU_WORKLOADS = ("monosoup",)
-# fp32 FMA peak of the GB300 from unit counts: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz
-FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+# the arithmetic type each workload computes in (the MonoSoup products and
+# merge multiply exact three-piece bf16 splits of fp32 operands on the tensor
+# cores with fp32 accumulation; Gram matrices and Cholesky factors in
+# float-float)
+DTYPES = {"monosoup": "bf16 pieces of fp32 (exact splits), f32 accumulate"}
 # MonoSoup workload: k checkpoints, rank r, sketch width l, power iterations q
 MONOSOUP = {"d": 8192, "k": 3, "rank": 16, "l": 32, "q": 1}
 # sub-measurements of the default line: (name, timed steps, warm-up steps)
@@ -143,8 +144,10 @@ def monosoup_bytes(d, k, q):
 
 
 def monosoup_flops(d, k, rank, l, q):
-    """fp32 FLOPs of the products with the task vectors (2 d^2 l each) and of
-    the rank-(k r) merge (2 d^2 k r)."""
+    """Algorithmic FLOPs of the products with the task vectors (2 d^2 l each)
+    and of the rank-(k r) merge (2 d^2 k r), counted once per product (the
+    tensor cores multiply exact bf16 pieces of the fp32 operands, several
+    piece products per algorithmic one)."""
     return k * (2 + 2 * q) * 2 * d * d * l + 2 * d * d * k * rank
 
 
@@ -838,13 +841,6 @@ def roofline_of(wl: Workload, calls, ev_ms, hbm_peak, bf16_peak, peak_src):
         roof = {"bound": "tensor", "kernel": dom, "achieved": tf, "peak": bf16_peak, "unit": "TFLOP/s",
                 "frac": tf / bf16_peak, "traffic": traffic, "peak_source": f"{peak_src} (bf16_tflops, burst)",
                 "flops_per_launch": flops_per_launch, "avg_launch_us": avg_ms * 1e3}
-    elif wl.name in ALU_WORKLOADS:
-        tf = flops_per_launch / (avg_ms * 1e-3) / 1e12
-        roof = {"bound": "alu", "kernel": dom, "achieved": tf, "peak": FP32_PEAK_TFLOPS, "unit": "TFLOP/s",
-                "frac": tf / FP32_PEAK_TFLOPS, "traffic": traffic,
-                "peak_source": "derived: 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (fp32 FMA)",
-                "flops_per_launch": flops_per_launch, "avg_launch_us": avg_ms * 1e3,
-                "hbm_achieved_gbs": achieved, "hbm_frac": achieved / hbm_peak}
     else:
         roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                 "frac": achieved / hbm_peak, "traffic": traffic, "peak_source": f"{peak_src} (hbm_gbs)",
@@ -859,7 +855,7 @@ def roofline_of(wl: Workload, calls, ev_ms, hbm_peak, bf16_peak, peak_src):
 
 
 def _unit_of(name: str) -> str:
-    return "TFLOP/s" if name in TENSOR_WORKLOADS or name in ALU_WORKLOADS else "GB/s"
+    return "TFLOP/s" if name in TENSOR_WORKLOADS else "GB/s"
 
 
 def _value(wl: Workload, ms_per_step: float) -> float:
@@ -1030,7 +1026,7 @@ def run_gpu(args):
         line = {"metric": METRIC, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "strong" if world > 1 else "weak", "vs_baseline": None,
-                "dtype": "f32" if wl.name in ALU_WORKLOADS else "bf16", "accumulate": "f32", "data": DATA,
+                "dtype": DTYPES.get(wl.name, "bf16"), "accumulate": "f32", "data": DATA,
                 "config": wl.config(),
                 "tokens_per_s": sum(wl.tokens) / (ms_per_step * 1e-3) if wl.tokens else None,
                 "frac_hbm_step": step_bytes / (ms_per_step * 1e-3) / 1e9 / world / hbm_peak,
