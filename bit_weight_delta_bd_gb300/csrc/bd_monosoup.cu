@@ -1136,16 +1136,18 @@ __global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ 
 // add up to less than 2^-21 |L[e][row] R[e][j]|), zero-padded to Kp = 6 K
 // rounded up to 64.  A CTA
 // computes 128 rows x 256 columns: D = Ls Rs^T in tensor memory (M = 128,
-// N = 256, K = 16 MMAs; A and B K-major in shared memory, two 48 KB stages),
+// N = 256, K = 16 MMAs; A and B K-major in shared memory, three 48 KB stages),
 // then warps 2..9 add W_base row by row (lane quarter warp % 4, column half
-// (warp - 2) / 4; the W_base loads of the next 32 columns are issued before
-// the current ones are used).  Two CTAs per SM.
+// (warp - 2) / 4).  The CTA's W_base tile comes in by TMA at the start (four
+// 64-column boxes, 128-byte swizzle, 64 KB), so that it lands while the
+// MMAs run and the epilogue reads it from shared memory.
 constexpr int kMgM = 128;
 constexpr int kMgN = 256;
-constexpr int kMgStages = 2;
+constexpr int kMgStages = 3;
 constexpr int kMgATile = kMgM * 128;          // 64 reduction indices x 128 rows, bf16: 16 KB
 constexpr int kMgBTile = kMgN * 128;          // 64 x 256: 32 KB
 constexpr int kMgStage = kMgATile + kMgBTile;
+constexpr int kMgWTile = kMgM * kMgN * 2;       // the W_base tile: 64 KB
 constexpr int kMgThreads = 320;               // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
 constexpr uint32_t kMgTmemCols = kMgN;
 constexpr int kMgPairs = 6;
@@ -1193,6 +1195,7 @@ __global__ void __launch_bounds__(256) split_factors_kernel(const float* __restr
 struct MergeParams {
     CUtensorMap a_map;  // Ls [d_out][Kp] bf16, box 64 x 128, 128-byte swizzle
     CUtensorMap b_map;  // Rs [d_in][Kp] bf16, box 64 x 256, 128-byte swizzle
+    CUtensorMap w_map;  // W_base [d_out][d_in] bf16, box 64 x 128, 128-byte swizzle
     const uint16_t* wb;
     void* out;
     int64_t d_out, d_in;
@@ -1201,11 +1204,11 @@ struct MergeParams {
     int out_f32;
 };
 
-__global__ void __launch_bounds__(kMgThreads, 2) merge_tc_kernel(const __grid_constant__ MergeParams p)
+__global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_constant__ MergeParams p)
 {
     extern __shared__ uint8_t dyn_raw[];
     __shared__ uint64_t full[kMgStages], empty[kMgStages];
-    __shared__ uint64_t done;
+    __shared__ uint64_t done, wfull;
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort;
     uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
@@ -1218,10 +1221,12 @@ __global__ void __launch_bounds__(kMgThreads, 2) merge_tc_kernel(const __grid_co
             mbar_init(&empty[st], 1);
         }
         mbar_init(&done, 1);
+        mbar_init(&wfull, 1);
         abort = 0;
         fence_mbarrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, kMgTmemCols);
+    uint8_t* wtile = ring + static_cast<size_t>(kMgStages) * kMgStage;  // [4 boxes][128 rows][128 B]
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1240,6 +1245,12 @@ __global__ void __launch_bounds__(kMgThreads, 2) merge_tc_kernel(const __grid_co
     };
     if (warp == 0) {
         if (lane == 0) {
+            // the W_base tile first (columns past d_in are zero-filled and never stored)
+            mbar_arrive_expect_tx(&wfull, static_cast<uint32_t>(kMgWTile));
+#pragma unroll
+            for (int bx = 0; bx < kMgN / 64; ++bx)
+                tma_load_2d(wtile + bx * (kMgWTile / 4), &p.w_map, static_cast<int>(col0) + 64 * bx,
+                            static_cast<int>(row0), &wfull);
             int t = 0;
             for (; t < nk; ++t) {
                 const int st = t % kMgStages;
@@ -1254,6 +1265,9 @@ __global__ void __launch_bounds__(kMgThreads, 2) merge_tc_kernel(const __grid_co
                 while (!mbar_try_wait(&full[i % kMgStages], static_cast<uint32_t>(i / kMgStages) & 1u) &&
                        global_timer_ns() - t0 < kWaitLimitNs) {
                 }
+            }
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(&wfull, 0u) && global_timer_ns() - t0 < kWaitLimitNs) {
             }
         }
     } else if (warp == 1) {
@@ -1277,34 +1291,28 @@ __global__ void __launch_bounds__(kMgThreads, 2) merge_tc_kernel(const __grid_co
         // epilogue: one row per thread (lane quarter warp % 4), columns
         // 128 hc .. 128 hc + 127 in chunks of 32
         const int q = warp & 3, hc = (warp - 2) >> 2;
-        const bool ok = __all_sync(0xffffffffu, wait(&done, 0u)) && !abort;
+        const bool ok = __all_sync(0xffffffffu, wait(&done, 0u) && wait(&wfull, 0u)) && !abort;
         tc_fence_after();
-        const int64_t row = row0 + 32 * q + lane;
+        const int rl = 32 * q + lane;
+        const int64_t row = row0 + rl;
         const bool live = row < p.d_out;
         const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128u * hc;
         const int64_t cbase = col0 + 128 * hc;
         const int nch = cbase >= p.d_in ? 0 : static_cast<int>((p.d_in - cbase < 128 ? p.d_in - cbase : 128) / 32);
-        uint4 wn[4];
-        auto load_w = [&](int ch) {
-            if (live && ch < nch) {
-                const uint4* wr = reinterpret_cast<const uint4*>(p.wb + row * p.d_in + cbase + 32 * ch);
-#pragma unroll
-                for (int c = 0; c < 4; ++c) wn[c] = wr[c];
-            }
-        };
         if (ok) {
-            load_w(0);
 #pragma unroll 1
             for (int ch = 0; ch < nch; ++ch) {
-                const uint4 wcur[4] = {wn[0], wn[1], wn[2], wn[3]};
-                load_w(ch + 1);
                 uint32_t v[32];
                 tmem_ld32(taddr + 32 * ch, v);
                 if (!live) continue;
                 const int64_t col = cbase + 32 * ch;
+                const int cl = 128 * hc + 32 * ch;  // column within the tile
+                const uint8_t* wbox = wtile + (cl >> 6) * (kMgWTile / 4) + rl * 128;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint32_t wv[4] = {wcur[c].x, wcur[c].y, wcur[c].z, wcur[c].w};
+                    const int chunk = ((cl & 63) >> 3) + c;  // 16-byte chunk of the 128-byte box row
+                    const uint4 w = *reinterpret_cast<const uint4*>(wbox + ((chunk ^ (rl & 7)) << 4));
+                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
                     float o[8];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -1401,7 +1409,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<0>), kTSmem, t0c);
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<1>), kTSmem, t1c);
     static std::atomic<size_t> mgc[kHostMaxDevices];
-    constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + 1024;
+    constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + kMgWTile + 1024;
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(merge_tc_kernel), kMgSmem, mgc);
     if (e0 != cudaSuccess) return e0;
     const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
@@ -1636,6 +1644,9 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tma_2d(&mp.b_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Rs, static_cast<uint64_t>(Kp),
                        static_cast<uint64_t>(a.d_in), static_cast<uint64_t>(Kp) * 2, 64, kMgN,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tma_2d(&mp.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
+                       static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, 64, kMgM,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     mp.wb = a.w_base;
