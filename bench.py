@@ -62,9 +62,10 @@ DATA = "synthetic (seeded numpy / torch generators; shapes and distributions of 
 # changed.  Summaries of the captures are in profiles/.  An entry whose value
 # is a float is a ratio (traffic / algorithmic bytes) taken on one launch of a
 # smaller call of the same kernel and applied to the average launch.
+MONOSOUP_CALL = "bd_monosoup_merge (tensor-core products, Gram / Cholesky / Jacobi, tensor-core merge)"
 NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
-    ("skinny_kernel<1>", "decode"): ("60707ad3c65224a0", "bd_skinny.cu", 499_405_056 + 3_889_920),
+    ("skinny_kernel<1>", "decode"): ("20d4bf1c25e2a4b4", "bd_skinny.cu", 499_405_824 + 3_356_416),
     # 4 rows per CTA (kCompressRowsPerCta in bd_internal.h)
     ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_566_080 + 7_655_936),
     ("prefill_kernel", "prefill"): ("705a6fbf4f52e879", "bd_prefill.cu", 591_238_912 + 67_592_704),
@@ -74,6 +75,8 @@ NCU_TRAFFIC = {
     ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("705a6fbf4f52e879", "bd_prefill.cu",
                                                                       1_097_012_736 + 64_569_088),
     ("materialize_kernel", "materialize"): ("fae23fcd0ba90d9b", "bd_materialize.cu", 499_370_496 + 426_232_320),
+    # all 36 launches of one merge (launch list with DRAM counters, one pass)
+    (MONOSOUP_CALL, "monosoup"): ("483ce878dc4c59c2", "bd_monosoup.cu", 3_488_855_296 + 114_338_048),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =
@@ -382,7 +385,7 @@ class GpuRun:
             return out
         if wl.name == "monosoup":
             m = MONOSOUP
-            out.append(("monosoup_merge", "bd_monosoup_merge (sketch, transpose-product, Gram, merge kernels)",
+            out.append(("monosoup_merge", MONOSOUP_CALL,
                         monosoup_bytes(wl.d_out, len(wl.wf), m["q"]),
                         monosoup_flops(wl.d_out, len(wl.wf), m["rank"], m["l"], m["q"]),
                         lambda: bd.bd_monosoup_merge(self.wb, self.wf, m["rank"], m["l"], m["q"], self.omega,
