@@ -222,6 +222,7 @@ bd_status bd_monosoup_merge(const uint16_t* w_base, const uint16_t* const* w_ft,
     a.out = w_merged;
     a.out_f32 = out_dtype == BD_OUT_F32;
     a.ws = ws;
+    a.err = err_word(ws);
     a.sm_count = sms;
     return launched(bd::launch_monosoup(a, static_cast<cudaStream_t>(stream)));
 }

@@ -137,6 +137,7 @@ struct MonoSoupArgs {
     void* out;                     // [d_out][d_in] bf16 or fp32
     int out_f32;
     void* ws;                      // monosoup_workspace_size bytes
+    uint32_t* err;                 // the asynchronous error word (start of ws)
     int sm_count;                  // SMs of the current device
 };
 

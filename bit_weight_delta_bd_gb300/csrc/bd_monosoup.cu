@@ -345,6 +345,7 @@ struct TProdParams {
     CUtensorMap w_map[kMaxBatch];  // W_i of checkpoint blockIdx.z, same
     CUtensorMap s_map[kMaxBatch];  // its split small operand [128][Kp] bf16, box 64 x 96, 128-byte swizzle
     float* part;                   // [gridDim.z][gridDim.y][out rows][l]
+    uint32_t* err;                 // the error word: a wait that timed out sets kErrTimeout
     int64_t d_out, d_in;
     int l;
     int64_t k_per;                 // reduction indices per slice (a multiple of 64)
@@ -468,6 +469,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
             if (abort) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 abort = 1;
+                raise_error(p.err, kErrTimeout);
                 return false;
             }
         }
@@ -1198,6 +1200,7 @@ struct MergeParams {
     CUtensorMap w_map;  // W_base [d_out][d_in] bf16, box 64 x 128, 128-byte swizzle
     const uint16_t* wb;
     void* out;
+    uint32_t* err;      // the error word: a wait that timed out sets kErrTimeout
     int64_t d_out, d_in;
     int nk;             // Kp / 64 (0: rank 0, out = W_base)
     float inv_k;
@@ -1238,6 +1241,7 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
             if (abort) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 abort = 1;
+                raise_error(p.err, kErrTimeout);
                 return false;
             }
         }
@@ -1355,7 +1359,7 @@ struct MonoSoupWs {
 MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
 {
     MonoSoupWs w{};
-    size_t off = 256;  // error word area (unused by these kernels, kept for the common layout)
+    size_t off = 256;  // the asynchronous error word (a product or merge wait that timed out)
     auto take = [&](size_t bytes) {
         const size_t at = off;
         off += up256(bytes);
@@ -1474,7 +1478,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                 return false;
         }
         pr.part = part;
-        pr.err = nullptr;
+        pr.err = a.err;
         pr.d_out = a.d_out;
         pr.d_in = a.d_in;
         pr.l = l;
@@ -1498,6 +1502,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                 return false;
         }
         pr.part = part;
+        pr.err = a.err;
         pr.d_out = a.d_out;
         pr.d_in = a.d_in;
         pr.l = l;
@@ -1651,6 +1656,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         return cudaErrorInvalidValue;
     mp.wb = a.w_base;
     mp.out = a.out;
+    mp.err = a.err;
     mp.d_out = a.d_out;
     mp.d_in = a.d_in;
     mp.nk = K > 0 ? Kp / 64 : 0;

@@ -219,8 +219,12 @@ bd_status bd_materialize(const uint16_t* w_base, const uint32_t* signs, const fl
  * re-orthonormalisation, then the exact SVD of the l x d_in projection.  It
  * equals the exact truncated SVD when Delta_i has rank <= l; otherwise its
  * error is governed by the singular values past l (more power iterations and
- * a larger l reduce it).  fp32 arithmetic with fp64 Gram matrices; the result
- * is rounded once to `out_dtype`.
+ * a larger l reduce it).  The products with Delta_i and the final merge run
+ * on the tensor cores on exact three-piece bf16 splits of their fp32
+ * operands (fp32 accumulation; l <= 32 -- wider sketches use fp32 CUDA-core
+ * products); the Gram matrices and their Cholesky factors are float-float,
+ * the l x l eigenproblem fp32 Jacobi.  The result is rounded once to
+ * `out_dtype`.
  *   w_base    device bf16 [d_out][d_in], 16-byte aligned
  *   w_ft      HOST array of k device pointers, each bf16 [d_out][d_in],
  *             16-byte aligned; 1 <= k <= BD_MAX_VARIANTS
@@ -229,8 +233,11 @@ bd_status bd_materialize(const uint16_t* w_base, const uint32_t* signs, const fl
  *   w_merged  device [d_out][d_in], bf16 or fp32 by out_dtype, 16-byte
  *             aligned, overlapping no input and not the workspace
  *   ws        bd_monosoup_workspace_size(d_out, d_in, k, rank, l) bytes,
- *             256-byte aligned (scratch: the sketches, Gram partials and the
- *             rank-`rank` factors of every checkpoint)
+ *             256-byte aligned: the asynchronous error word at its start (a
+ *             bounded wait of a product or merge kernel that timed out sets
+ *             BD_ERR_TIMEOUT; read it with bd_check_async), then scratch (the
+ *             sketches, Gram partials, split operands and the rank-`rank`
+ *             factors of every checkpoint)
  * d_in must be a positive multiple of 128 (BD_ERR_UNSUPPORTED_SHAPE); l
  * must be a multiple of 4 (rows of the l-column operands move as 16-byte
  * units); out-of-range k, rank, l or power_iters (0..16) give

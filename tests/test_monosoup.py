@@ -43,7 +43,7 @@ def run_gpu(dev, wb, ws, om, rank, l, q, out_dtype):
     out = torch.empty((d_out, d_in), dtype=out_dtype, device=dev)
     wsp = bd.new_workspace(bd.bd_monosoup_workspace_size(d_out, d_in, len(ws), rank, l), dev)
     bd.bd_monosoup_merge(wb_d, ws_d, rank, l, q, om_d, out, wsp)
-    torch.cuda.synchronize()
+    assert bd.bd_check_async(wsp) == bd.BD_OK  # no bounded wait gave up
     return out.cpu()
 
 
