@@ -140,10 +140,10 @@ def materialize_bytes(d_out, d_in, n_alpha):
 
 
 def monosoup_bytes(d, k, q):
-    """Each pass over a task vector reads W_i and W_base (2 + 2q passes:
-    sketch, 2q power-iteration products, B^T), plus the merge's W_base read
-    and W_merged write."""
-    return k * (2 + 2 * q) * 4 * d * d + 4 * d * d
+    """Each of the 2 + 2q passes (sketch, 2q power-iteration products, B^T)
+    reads every W_i and W_base once (the k products of a pass share the
+    W_base tiles), plus the merge's W_base read and W_merged write."""
+    return (2 + 2 * q) * (k + 1) * 2 * d * d + 4 * d * d
 
 
 def monosoup_flops(d, k, rank, l, q):

@@ -321,7 +321,11 @@ size_t dprod_smem()
 //       a of Delta (three MMAs of M = 128, N = 96, K = 16 per k-step) in
 //       tensor memory; the result is D[m][c] + D[m][32 + c] + D[m][64 + c].
 // A stage holds only the W_i and W_base tiles and the B tile (44 KB), so four
-// stages keep four tiles of Delta in flight per SM.  Warp 0 issues the TMA
+// stages keep four tiles of Delta in flight per SM.  The W tiles of a stage
+// are free as soon as the piece warps hold their values (wfree), the B tile
+// when the stage's MMAs finish (empty).  The checkpoint varies fastest along
+// grid x (blockIdx.x = block * checkpoints + checkpoint), so the CTAs that
+// read the same W_base tiles run side by side and share them in L2.  Warp 0 issues the TMA
 // loads, warp 1 allocates tensor memory and issues the MMAs, warps 2..9 form
 // the pieces (lane quarter warp % 4, K half (warp - 2) / 4); warps 2..5 then
 // read the accumulator, one row per thread.
@@ -342,12 +346,13 @@ static_assert(kTStage % 1024 == 0, "1024-byte aligned stages");
 
 struct TProdParams {
     CUtensorMap b_map;             // W_base [d_out][d_in] bf16, box 64 x 128 (MODE 0) or 64 x 64 (MODE 1), 128-byte swizzle
-    CUtensorMap w_map[kMaxBatch];  // W_i of checkpoint blockIdx.z, same
+    CUtensorMap w_map[kMaxBatch];  // W_i of checkpoint blockIdx.x % nz, same
     CUtensorMap s_map[kMaxBatch];  // its split small operand [128][Kp] bf16, box 64 x 96, 128-byte swizzle
-    float* part;                   // [gridDim.z][gridDim.y][out rows][l]
+    float* part;                   // [checkpoints][gridDim.y][out rows][l]
     uint32_t* err;                 // the error word: a wait that timed out sets kErrTimeout
     int64_t d_out, d_in;
     int l;
+    int nz;                        // checkpoints of the batch (grid x = blocks * nz)
     int64_t k_per;                 // reduction indices per slice (a multiple of 64)
 };
 
@@ -436,13 +441,15 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
 {
     extern __shared__ uint8_t dyn_raw[];
     __shared__ uint64_t full[kTStages], afull[kTStages], empty[kTStages];
+    __shared__ uint64_t wfree[kTStages];  // the piece warps hold the stage's W values (W slots free)
     __shared__ uint64_t done;
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort;
     uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int z = static_cast<int>(blockIdx.z);
-    const int64_t o0 = static_cast<int64_t>(blockIdx.x) * kTM;  // first output row of this CTA
+    const int nz = p.nz;
+    const int z = static_cast<int>(blockIdx.x % nz);                        // checkpoint of the batch
+    const int64_t o0 = static_cast<int64_t>(blockIdx.x / nz) * kTM;  // first output row of this CTA
     const int64_t klen = MODE == 0 ? p.d_in : p.d_out;
     const int64_t kb = static_cast<int64_t>(blockIdx.y) * p.k_per;
     const int64_t ke = kb + p.k_per < klen ? kb + p.k_per : klen;
@@ -452,6 +459,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
             mbar_init(&full[st], 1);
             mbar_init(&afull[st], kTConvWarps);
             mbar_init(&empty[st], 1);
+            mbar_init(&wfree[st], kTConvWarps);
         }
         mbar_init(&done, 1);
         abort = 0;
@@ -482,7 +490,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
             int t = 0;
             for (; t < nt; ++t) {
                 const int st = t % kTStages;
-                if (t >= kTStages && !wait(&empty[st], static_cast<uint32_t>(t / kTStages - 1) & 1u)) break;
+                const uint32_t prev = static_cast<uint32_t>(t / kTStages - 1) & 1u;
+                if (t >= kTStages && !wait(&wfree[st], prev)) break;
                 uint8_t* sb = ring + static_cast<size_t>(st) * kTStage;
                 const int k0 = static_cast<int>(kb + static_cast<int64_t>(t) * kTK);
                 mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kTStage));
@@ -497,6 +506,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
                         tma_load_2d(sb + kTWTile + hb * (kTWTile / 2), &p.b_map, cx, k0, &full[st]);
                     }
                 }
+                // the B tile once the stage's MMAs are done with it
+                if (t >= kTStages && !wait(&empty[st], prev)) break;
                 tma_load_2d(sb + 2 * kTWTile, &p.s_map[z], k0, 0, &full[st]);
             }
             for (int i = (t > kTStages ? t - kTStages : 0); i < t; ++i) {  // every issued copy lands before exit
@@ -567,6 +578,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
                     split_pair(wi, wb, v1[j], v2[j], v3[j]);
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&wfree[st]);  // the W values are in registers
             const uint32_t acol = lane_addr + kTACol + 96u * static_cast<uint32_t>(st) + 16u * kh;
             tmem_st16_nowait(acol, v1);
             tmem_st16_nowait(acol + 32, v2);
@@ -592,7 +605,7 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
             const int64_t nrows = MODE == 0 ? p.d_out : p.d_in;
             const int64_t row = o0 + rl;
             if (row < nrows) {
-                float* out = p.part + ((static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * nrows + row) * p.l;
+                float* out = p.part + ((static_cast<int64_t>(z) * gridDim.y + blockIdx.y) * nrows + row) * p.l;
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
                     if (c >= p.l) break;
@@ -1524,9 +1537,9 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                 perr = cudaErrorInvalidValue;
                 return;
             }
-            tprod_kernel<0><<<dim3(static_cast<unsigned>(tr_blocks), static_cast<unsigned>(ns),
-                                   static_cast<unsigned>(nb)),
-                              kTThreads, kTSmem, st>>>(tp_sk);
+            tp_sk.nz = nb;
+            tprod_kernel<0><<<dim3(static_cast<unsigned>(tr_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem,
+                              st>>>(tp_sk);
             sum_slices_kernel<<<dim3(blocks_for(a.d_out * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
                 Yp, ns, a.d_out * l, Yall + static_cast<size_t>(i0) * a.d_out * l);
             return;
@@ -1560,9 +1573,9 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                 perr = cudaErrorInvalidValue;
                 return;
             }
-            tprod_kernel<1><<<dim3(static_cast<unsigned>(tc_blocks), static_cast<unsigned>(ns),
-                                   static_cast<unsigned>(nb)),
-                              kTThreads, kTSmem, st>>>(tp_lf);
+            tp_lf.nz = nb;
+            tprod_kernel<1><<<dim3(static_cast<unsigned>(tc_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem,
+                              st>>>(tp_lf);
             sum_slices_kernel<<<dim3(blocks_for(a.d_in * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
                 Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
             return;
