@@ -1149,22 +1149,22 @@ __global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ 
 // R[e][j] (split_factors_kernel; a piece after the first is below 2^-7 of the
 // value's magnitude and the third below 2^-15, so the three pairs left out
 // add up to less than 2^-21 |L[e][row] R[e][j]|), zero-padded to Kp = 6 K
-// rounded up to 64.  A CTA
-// computes 128 rows x 256 columns: D = Ls Rs^T in tensor memory (M = 128,
-// N = 256, K = 16 MMAs; A and B K-major in shared memory, three 48 KB stages),
-// then warps 2..9 add W_base row by row (lane quarter warp % 4, column half
-// (warp - 2) / 4).  The CTA's W_base tile comes in by TMA at the start (four
-// 64-column boxes, 128-byte swizzle, 64 KB), so that it lands while the
-// MMAs run and the epilogue reads it from shared memory.
+// rounded up to 64.  Persistent CTAs (one per SM) walk the 128-row x
+// 256-column output tiles c, c + G, c + 2G, ... (row-major tile order): per
+// tile D = Ls Rs^T in tensor memory (M = 128, N = 256, K = 16 MMAs; A and B
+// K-major in shared memory, a ring of three 48 KB stages shared by all the
+// CTA's tiles), with two accumulators of 256 columns, so that the MMAs of
+// the next tile run while warps 2..9 add W_base to this one row by row (lane
+// quarter warp % 4, column half (warp - 2) / 4; the W_base loads of the next
+// 32 columns are issued before the current ones are used).
 constexpr int kMgM = 128;
 constexpr int kMgN = 256;
 constexpr int kMgStages = 3;
 constexpr int kMgATile = kMgM * 128;          // 64 reduction indices x 128 rows, bf16: 16 KB
 constexpr int kMgBTile = kMgN * 128;          // 64 x 256: 32 KB
 constexpr int kMgStage = kMgATile + kMgBTile;
-constexpr int kMgWTile = kMgM * kMgN * 2;       // the W_base tile: 64 KB
 constexpr int kMgThreads = 320;               // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
-constexpr uint32_t kMgTmemCols = kMgN;
+constexpr uint32_t kMgTmemCols = 2 * kMgN;    // two accumulators
 constexpr int kMgPairs = 6;
 
 __device__ __forceinline__ int merge_piece(int p, int side)
@@ -1210,12 +1210,12 @@ __global__ void __launch_bounds__(256) split_factors_kernel(const float* __restr
 struct MergeParams {
     CUtensorMap a_map;  // Ls [d_out][Kp] bf16, box 64 x 128, 128-byte swizzle
     CUtensorMap b_map;  // Rs [d_in][Kp] bf16, box 64 x 256, 128-byte swizzle
-    CUtensorMap w_map;  // W_base [d_out][d_in] bf16, box 64 x 128, 128-byte swizzle
     const uint16_t* wb;
     void* out;
     uint32_t* err;      // the error word: a wait that timed out sets kErrTimeout
     int64_t d_out, d_in;
     int nk;             // Kp / 64 (0: rank 0, out = W_base)
+    int ncb, ntiles;    // column tiles, tiles
     float inv_k;
     int out_f32;
 };
@@ -1224,25 +1224,27 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
 {
     extern __shared__ uint8_t dyn_raw[];
     __shared__ uint64_t full[kMgStages], empty[kMgStages];
-    __shared__ uint64_t done, wfull;
+    __shared__ uint64_t accfull[2], accempty[2], done;
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort;
     uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int64_t row0 = static_cast<int64_t>(blockIdx.y) * kMgM, col0 = static_cast<int64_t>(blockIdx.x) * kMgN;
     const int nk = p.nk;
+    const int c0 = static_cast<int>(blockIdx.x), G = static_cast<int>(gridDim.x);
     if (tid == 0) {
         for (int st = 0; st < kMgStages; ++st) {
             mbar_init(&full[st], 1);
             mbar_init(&empty[st], 1);
         }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&accfull[b], 1);
+            mbar_init(&accempty[b], 8);  // the eight epilogue warps
+        }
         mbar_init(&done, 1);
-        mbar_init(&wfull, 1);
         abort = 0;
         fence_mbarrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, kMgTmemCols);
-    uint8_t* wtile = ring + static_cast<size_t>(kMgStages) * kMgStage;  // [4 boxes][128 rows][128 B]
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1261,75 +1263,99 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
         return true;
     };
     if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (one k-step counter g over all tiles)
         if (lane == 0) {
-            // the W_base tile first (columns past d_in are zero-filled and never stored)
-            mbar_arrive_expect_tx(&wfull, static_cast<uint32_t>(kMgWTile));
-#pragma unroll
-            for (int bx = 0; bx < kMgN / 64; ++bx)
-                tma_load_2d(wtile + bx * (kMgWTile / 4), &p.w_map, static_cast<int>(col0) + 64 * bx,
-                            static_cast<int>(row0), &wfull);
-            int t = 0;
-            for (; t < nk; ++t) {
-                const int st = t % kMgStages;
-                if (t >= kMgStages && !wait(&empty[st], static_cast<uint32_t>(t / kMgStages - 1) & 1u)) break;
-                uint8_t* sb = ring + static_cast<size_t>(st) * kMgStage;
-                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kMgStage));
-                tma_load_2d(sb, &p.a_map, 64 * t, static_cast<int>(row0), &full[st]);
-                tma_load_2d(sb + kMgATile, &p.b_map, 64 * t, static_cast<int>(col0), &full[st]);
+            int g = 0;
+            bool ok = true;
+            for (int tile = c0; tile < p.ntiles && ok; tile += G) {
+                const int rb = tile / p.ncb, cb = tile - rb * p.ncb;
+                for (int t = 0; t < nk; ++t, ++g) {
+                    const int st = g % kMgStages;
+                    if (g >= kMgStages && !wait(&empty[st], static_cast<uint32_t>(g / kMgStages - 1) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sb = ring + static_cast<size_t>(st) * kMgStage;
+                    mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kMgStage));
+                    tma_load_2d(sb, &p.a_map, 64 * t, rb * kMgM, &full[st]);
+                    tma_load_2d(sb + kMgATile, &p.b_map, 64 * t, cb * kMgN, &full[st]);
+                }
             }
-            for (int i = (t > kMgStages ? t - kMgStages : 0); i < t; ++i) {  // every issued copy lands before exit
+            for (int i = (g > kMgStages ? g - kMgStages : 0); i < g; ++i) {  // every issued copy lands before exit
                 const uint64_t t0 = global_timer_ns();
                 while (!mbar_try_wait(&full[i % kMgStages], static_cast<uint32_t>(i / kMgStages) & 1u) &&
                        global_timer_ns() - t0 < kWaitLimitNs) {
                 }
             }
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(&wfull, 0u) && global_timer_ns() - t0 < kWaitLimitNs) {
-            }
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(kMgM, kMgN);
-            for (int t = 0; t < nk; ++t) {
-                const int st = t % kMgStages;
-                if (!wait(&full[st], static_cast<uint32_t>(t / kMgStages) & 1u)) break;
+            int g = 0, j = 0;
+            bool ok = true;
+            for (int tile = c0; tile < p.ntiles && ok; tile += G, ++j) {
+                const int b = j & 1;
+                // accumulator b is free once the epilogue has read tile j - 2
+                if (j >= 2 && !wait(&accempty[b], static_cast<uint32_t>(j / 2 - 1) & 1u)) break;
                 tc_fence_after();
-                const uint32_t sb = smem_u32(ring + static_cast<size_t>(st) * kMgStage);
-                const uint64_t adesc = smem_desc_sw128(sb), bdesc = smem_desc_sw128(sb + kMgATile);
+                const uint32_t d = tmem + static_cast<uint32_t>(b * kMgN);
+                for (int t = 0; t < nk; ++t, ++g) {
+                    const int st = g % kMgStages;
+                    if (!wait(&full[st], static_cast<uint32_t>(g / kMgStages) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sb = smem_u32(ring + static_cast<size_t>(st) * kMgStage);
+                    const uint64_t adesc = smem_desc_sw128(sb), bdesc = smem_desc_sw128(sb + kMgATile);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_ss(tmem, adesc + static_cast<uint64_t>(2 * kk), bdesc + static_cast<uint64_t>(2 * kk), idesc,
-                           (t | kk) != 0 ? 1u : 0u);
-                mma_commit(&empty[st]);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_ss(d, adesc + static_cast<uint64_t>(2 * kk), bdesc + static_cast<uint64_t>(2 * kk), idesc,
+                               (t | kk) != 0 ? 1u : 0u);
+                    mma_commit(&empty[st]);
+                }
+                if (ok) mma_commit(&accfull[b]);  // tile j's accumulator is complete
             }
-            mma_commit(&done);
+            mma_commit(&done);  // every MMA issued above has finished when this arrives
         }
     } else {
-        // epilogue: one row per thread (lane quarter warp % 4), columns
-        // 128 hc .. 128 hc + 127 in chunks of 32
+        // ------------------------------------------------------------ epilogue: one row per thread, columns
+        // 128 hc .. 128 hc + 127 of the tile in chunks of 32
         const int q = warp & 3, hc = (warp - 2) >> 2;
-        const bool ok = __all_sync(0xffffffffu, wait(&done, 0u) && wait(&wfull, 0u)) && !abort;
-        tc_fence_after();
-        const int rl = 32 * q + lane;
-        const int64_t row = row0 + rl;
-        const bool live = row < p.d_out;
-        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + 128u * hc;
-        const int64_t cbase = col0 + 128 * hc;
-        const int nch = cbase >= p.d_in ? 0 : static_cast<int>((p.d_in - cbase < 128 ? p.d_in - cbase : 128) / 32);
-        if (ok) {
+        int j = 0;
+        for (int tile = c0; tile < p.ntiles; tile += G, ++j) {
+            const int b = j & 1;
+            if (!__all_sync(0xffffffffu, wait(&accfull[b], static_cast<uint32_t>(j / 2) & 1u))) break;
+            tc_fence_after();
+            const int rb = tile / p.ncb, cb = tile - rb * p.ncb;
+            const int64_t row = static_cast<int64_t>(rb) * kMgM + 32 * q + lane;
+            const bool live = row < p.d_out;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * kMgN) +
+                                   128u * hc;
+            const int64_t cbase = static_cast<int64_t>(cb) * kMgN + 128 * hc;
+            const int nch =
+                cbase >= p.d_in ? 0 : static_cast<int>((p.d_in - cbase < 128 ? p.d_in - cbase : 128) / 32);
+            uint4 wn[4];
+            auto load_w = [&](int ch) {
+                if (live && ch < nch) {
+                    const uint4* wr = reinterpret_cast<const uint4*>(p.wb + row * p.d_in + cbase + 32 * ch);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) wn[c] = wr[c];
+                }
+            };
+            load_w(0);
 #pragma unroll 1
             for (int ch = 0; ch < nch; ++ch) {
+                const uint4 wcur[4] = {wn[0], wn[1], wn[2], wn[3]};
+                load_w(ch + 1);
                 uint32_t v[32];
                 tmem_ld32(taddr + 32 * ch, v);
                 if (!live) continue;
                 const int64_t col = cbase + 32 * ch;
-                const int cl = 128 * hc + 32 * ch;  // column within the tile
-                const uint8_t* wbox = wtile + (cl >> 6) * (kMgWTile / 4) + rl * 128;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const int chunk = ((cl & 63) >> 3) + c;  // 16-byte chunk of the 128-byte box row
-                    const uint4 w = *reinterpret_cast<const uint4*>(wbox + ((chunk ^ (rl & 7)) << 4));
-                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+                    const uint32_t wv[4] = {wcur[c].x, wcur[c].y, wcur[c].z, wcur[c].w};
                     float o[8];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -1353,6 +1379,16 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
                     }
                 }
             }
+            // this warp has read its part of accumulator b
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty[b]);
+        }
+    }
+    // tensor memory is freed only after every MMA issued has finished
+    if (warp == 1 && lane == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(&done, 0u) && global_timer_ns() - t0 < kWaitLimitNs) {
         }
     }
     tc_fence_before();
@@ -1426,7 +1462,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<0>), kTSmem, t0c);
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<1>), kTSmem, t1c);
     static std::atomic<size_t> mgc[kHostMaxDevices];
-    constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + kMgWTile + 1024;
+    constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + 1024;
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(merge_tc_kernel), kMgSmem, mgc);
     if (e0 != cudaSuccess) return e0;
     const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
@@ -1662,9 +1698,6 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tma_2d(&mp.b_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Rs, static_cast<uint64_t>(Kp),
                        static_cast<uint64_t>(a.d_in), static_cast<uint64_t>(Kp) * 2, 64, kMgN,
-                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !encode_tma_2d(&mp.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
-                       static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, 64, kMgM,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     mp.wb = a.w_base;
@@ -1675,8 +1708,10 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     mp.nk = K > 0 ? Kp / 64 : 0;
     mp.inv_k = 1.0f / static_cast<float>(a.k);
     mp.out_f32 = a.out_f32;
-    const dim3 grid(static_cast<unsigned>((a.d_in + kMgN - 1) / kMgN), static_cast<unsigned>((a.d_out + kMgM - 1) / kMgM));
-    merge_tc_kernel<<<grid, kMgThreads, kMgSmem, st>>>(mp);
+    mp.ncb = static_cast<int>((a.d_in + kMgN - 1) / kMgN);
+    mp.ntiles = mp.ncb * static_cast<int>((a.d_out + kMgM - 1) / kMgM);
+    const int mg_grid = mp.ntiles < sms ? mp.ntiles : sms;  // persistent: one CTA per SM
+    merge_tc_kernel<<<mg_grid, kMgThreads, kMgSmem, st>>>(mp);
     return cudaGetLastError();
 }
 
