@@ -76,6 +76,22 @@ def test_monosoup_matches_exact_truncated_svd(dev, d_out, d_in, k, r, l, q):
     assert np.all(np.abs(gb - ref) <= bf16_ulp(ref) + 1e-6 * np.abs(upd_ref).max())
 
 
+@pytest.mark.parametrize("d_out,d_in,k,r,l,q", [
+    (256, 384, 10, 4, 16, 1),    # two batches of checkpoints (8 + 2)
+    (200, 256, 17, 4, 8, 1),     # three batches (8 + 8 + 1), ragged rows
+    (512, 640, 3, 24, 64, 1),    # l = 64: CUDA-core products, three checkpoints in one batch
+])
+def test_monosoup_batches_and_wide_sketches(dev, d_out, d_in, k, r, l, q):
+    wb, ws = synth.monosoup_checkpoints(23 + k, d_out, d_in, k, min(r, d_out))
+    om = synth.gaussian_test_matrix(29 + l, d_in, l)
+    ref = oracle.monosoup_merge(wb, ws, r)
+    base = oracle.bf16_to_f64(wb)
+    upd_ref = ref - base
+    got = run_gpu(dev, wb, ws, om, r, l, q, torch.float32).double().numpy()
+    rel = np.linalg.norm((got - base) - upd_ref) / np.linalg.norm(upd_ref)
+    assert rel <= 1e-4, f"relative error of the merged update {rel:.3e}"
+
+
 def subspace_bound(delta: np.ndarray, omega: np.ndarray, r: int, q: int) -> float:
     """Elementwise bound on |tau_randomized - tau_exact| for one task vector,
     in exact arithmetic.  With sigma_j the singular values of Delta, V its
