@@ -76,7 +76,7 @@ NCU_TRAFFIC = {
                                                                       1_097_012_736 + 64_569_088),
     ("materialize_kernel", "materialize"): ("fae23fcd0ba90d9b", "bd_materialize.cu", 499_370_496 + 426_232_320),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("6b746641d7b4d4b3", "bd_monosoup.cu", 2_434_467_328 + 113_571_328),
+    (MONOSOUP_CALL, "monosoup"): ("d8d297141b5a4e7e", "bd_monosoup.cu", 2_434_400_768 + 115_017_216),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =

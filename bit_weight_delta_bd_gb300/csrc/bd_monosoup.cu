@@ -1067,36 +1067,56 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __
 
 // A_z <- A_z R_z^-1 in place (R_z from chol_kernel, checkpoint z =
 // blockIdx.y): per row the forward substitution x_j = (a_j - sum_{m<j} x_m
-// R[m][j]) / R[j][j], a dropped direction giving x_j = 0; one row per thread.
-__global__ void __launch_bounds__(64) tri_solve_kernel(float* a_all, int64_t n, int l, const float* __restrict__ Rf_all)
+// R[m][j]) / R[j][j] (the sum in order m = 0, 1, ...), a dropped direction
+// giving x_j = 0; one row per thread (16-byte row loads and stores), R
+// staged transposed so that four coefficients of column j come with one
+// 16-byte broadcast load.
+constexpr int kTriThreads = 128;
+constexpr int kTriStride = kMaxL + 4;  // floats per row of R^T in shared memory (16-byte multiple)
+
+__global__ void __launch_bounds__(kTriThreads) tri_solve_kernel(float* a_all, int64_t n, int l,
+                                                                const float* __restrict__ Rf_all)
 {
     float* a = a_all + static_cast<int64_t>(blockIdx.y) * n * l;
     const float* Rf = Rf_all + static_cast<int64_t>(blockIdx.y) * (kMaxL * kMaxL + kMaxL);
     const float* rinv = Rf + kMaxL * kMaxL;
-    __shared__ float sr[kMaxL][kMaxL + 1];
+    __shared__ __align__(16) float srt[kMaxL][kTriStride];  // srt[j][m] = R[m][j]
     __shared__ float sd[kMaxL];
-    for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
-        const int i = e >> 6, j = e & 63;
-        sr[i][j] = (i < l && j < l) ? Rf[i * l + j] : 0.0f;
+    for (int e = threadIdx.x; e < kMaxL * kTriStride; e += blockDim.x) {
+        const int j = e / kTriStride, m = e - j * kTriStride;
+        srt[j][m] = (j < l && m < l) ? Rf[m * l + j] : 0.0f;
     }
     for (int i = threadIdx.x; i < kMaxL; i += blockDim.x) sd[i] = i < l ? rinv[i] : 0.0f;
     __syncthreads();
     const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (row >= n) return;
     float x[kMaxL];
+    float4* ar = reinterpret_cast<float4*>(a + row * l);  // l is a multiple of 4
 #pragma unroll
-    for (int j = 0; j < kMaxL; ++j) x[j] = j < l ? a[row * l + j] : 0.0f;
+    for (int j4 = 0; j4 < kMaxL / 4; ++j4) {
+        const float4 v = 4 * j4 < l ? ar[j4] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        x[4 * j4] = v.x;
+        x[4 * j4 + 1] = v.y;
+        x[4 * j4 + 2] = v.z;
+        x[4 * j4 + 3] = v.w;
+    }
 #pragma unroll
     for (int j = 0; j < kMaxL; ++j) {
         if (j >= l) break;
         float s = x[j];
 #pragma unroll
-        for (int m = 0; m < j; ++m) s = fmaf(-x[m], sr[m][j], s);
+        for (int m4 = 0; m4 < (j + 3) / 4; ++m4) {
+            const float4 r = *reinterpret_cast<const float4*>(&srt[j][4 * m4]);
+            const float rv[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (4 * m4 + u < j) s = fmaf(-x[4 * m4 + u], rv[u], s);
+        }
         x[j] = s * sd[j];
     }
 #pragma unroll
-    for (int j = 0; j < kMaxL; ++j)
-        if (j < l) a[row * l + j] = x[j];
+    for (int j4 = 0; j4 < kMaxL / 4; ++j4)
+        if (4 * j4 < l) ar[j4] = make_float4(x[4 * j4], x[4 * j4 + 1], x[4 * j4 + 2], x[4 * j4 + 3]);
 }
 
 // dst[j][row] = sum_c src[row][c] * M[c][j]  (c < l, j < m), written
@@ -1654,8 +1674,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         for (int pass = 0; pass < passes; ++pass) {
             gram(A, n, nb, G);
             chol_kernel<<<static_cast<unsigned>(nb), 256, 0, st>>>(G, l, M);
-            tri_solve_kernel<<<dim3(static_cast<unsigned>((n + 63) / 64), static_cast<unsigned>(nb)), 64, 0, st>>>(
-                A, n, l, M);
+            tri_solve_kernel<<<dim3(static_cast<unsigned>((n + kTriThreads - 1) / kTriThreads), static_cast<unsigned>(nb)),
+                               kTriThreads, 0, st>>>(A, n, l, M);
         }
     };
     if (r > 0) {
