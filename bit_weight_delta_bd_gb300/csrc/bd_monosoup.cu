@@ -22,11 +22,13 @@
 // The merge is one pass: W_base + (1/k) [L_1 .. L_k][R_1 .. R_k]^T with
 // L_i = Q_i U_r, R_i = B_i^T U_r, rounded once to the output type.
 //
-// All arithmetic is fp32 on the CUDA cores except the Gram matrices and the
-// Cholesky factor (float-float, on the same fp32 units).  Up to kMaxBatch
-// checkpoints go through every step together (one launch per step, the
-// checkpoint in the last grid dimension).  No kernel waits on another CTA;
-// the passes are plain stream-ordered launches.
+// The products with Delta (l <= 32) and the merge run on the tcgen05 tensor
+// cores on exact three-piece bf16 splits of their fp32 operands, with fp32
+// accumulation; wider sketches (l <= 64) use fp32 CUDA-core products.  The
+// Gram matrices and Cholesky factors are float-float on the fp32 units, the
+// eigenproblem fp32.  Up to kMaxBatch checkpoints go through every step
+// together (one launch per step, the checkpoint in a grid dimension).  No
+// kernel waits on another CTA; the passes are plain stream-ordered launches.
 #include <cuda_bf16.h>
 
 #include <algorithm>

@@ -127,9 +127,10 @@ def test_monosoup_noisy_task_vectors_elementwise(dev, d_out, d_in, k, r, l, q):
     """Task vectors = rank-r signal + Laplace(0, 1e-3) noise.  Elementwise:
     |W_gpu - W_oracle| <= (1/k) sum_i subspace_bound_i + an fp32 term of
     2^-16 sigma_1 (the sketches and projections are fp32 sums of at most
-    d_in or d_out terms, the bases are orthonormalised through fp64 Gram
-    matrices; 256 fp32 roundings of the largest singular value cover them
-    with room to spare).  bf16 output: the same plus half a bf16 ulp."""
+    d_in or d_out exact products, the bases are orthonormalised through
+    float-float Gram matrices and Cholesky factors; 256 fp32 roundings of the
+    largest singular value cover them with room to spare).  bf16 output: the
+    same plus half a bf16 ulp."""
     wb, ws = synth.monosoup_noisy_checkpoints(17 + d_out, d_out, d_in, k, r)
     om = synth.gaussian_test_matrix(19 + d_in, d_in, l)
     ref = oracle.monosoup_merge(wb, ws, r)
