@@ -143,12 +143,24 @@ struct TileInfo {
     bool valid;
 };
 
+constexpr int kRasterPairs = 8;  // grouped prefill: row pairs per raster group
+
 template <class P>
 __device__ __forceinline__ TileInfo tile_info(const P& p, int t, uint32_t rank)
 {
     constexpr bool kGrouped = std::is_same<P, GroupedPrefillParams>::value;
     TileInfo ti;
-    const int tb = t % p.ntb, rp = t / p.ntb;
+    int tb = t % p.ntb, rp = t / p.ntb;
+    if constexpr (kGrouped) {
+        // groups of kRasterPairs row pairs x every block, block-major inside
+        // a group: the group's W_base rows and the blocks' x stay in L2
+        const int nrp = static_cast<int>((p.d_out + 2 * BM - 1) / (2 * BM));
+        const int per = kRasterPairs * p.ntb;
+        const int g = t / per, loc = t - g * per;
+        const int gp = nrp - g * kRasterPairs < kRasterPairs ? nrp - g * kRasterPairs : kRasterPairs;
+        tb = loc / gp;
+        rp = g * kRasterPairs + (loc - tb * gp);
+    }
     ti.row0 = (2 * static_cast<int64_t>(rp) + rank) * BM;
     ti.tok0 = static_cast<int64_t>(tb) * BN;
     ti.tok_end = p.T;
