@@ -68,15 +68,15 @@ NCU_TRAFFIC = {
     ("skinny_kernel<1>", "decode"): ("20d4bf1c25e2a4b4", "bd_skinny.cu", 499_405_824 + 3_356_416),
     # 4 rows per CTA (kCompressRowsPerCta in bd_internal.h)
     ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_566_080 + 7_655_936),
-    ("prefill_kernel", "prefill"): ("705a6fbf4f52e879", "bd_prefill.cu", 591_238_912 + 67_592_704),
+    ("prefill_kernel", "prefill"): ("e4118a0ff3103961", "bd_prefill.cu", 619_106_816 + 68_359_936),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
     ("multi_prepare + multi_kernel<8>", "multi"): ("d89f83fcd4e67914", "bd_multi.cu", 255_770_880 + 3_986_432),
     # the grouped prefill_kernel only (router, plan and gather add about 134 MB of x copies)
-    ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("705a6fbf4f52e879", "bd_prefill.cu",
-                                                                      1_097_012_736 + 64_569_088),
+    ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("e4118a0ff3103961", "bd_prefill.cu",
+                                                                      935_756_288 + 63_227_904),
     ("materialize_kernel", "materialize"): ("fae23fcd0ba90d9b", "bd_materialize.cu", 499_370_496 + 426_232_320),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("d8d297141b5a4e7e", "bd_monosoup.cu", 2_434_400_768 + 115_017_216),
+    (MONOSOUP_CALL, "monosoup"): ("bf30a84f010b9947", "bd_monosoup.cu", 2_434_392_832 + 114_479_360),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =
