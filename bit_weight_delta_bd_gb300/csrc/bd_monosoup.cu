@@ -1177,15 +1177,18 @@ __global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ 
 // K-major in shared memory, a ring of three 48 KB stages shared by all the
 // CTA's tiles), with two accumulators of 256 columns, so that the MMAs of
 // the next tile run while warps 2..9 add W_base to this one row by row (lane
-// quarter warp % 4, column half (warp - 2) / 4; the W_base loads of the next
-// 32 columns are issued before the current ones are used).
+// quarter warp % 4, column half (warp - 2) / 4).  Warp 10 loads each tile's
+// W_base block by TMA (four 64-column boxes, 128-byte swizzle, 64 KB) as soon
+// as the epilogue has finished with the previous one, so the epilogue reads
+// W_base from shared memory.
 constexpr int kMgM = 128;
 constexpr int kMgN = 256;
 constexpr int kMgStages = 3;
 constexpr int kMgATile = kMgM * 128;          // 64 reduction indices x 128 rows, bf16: 16 KB
 constexpr int kMgBTile = kMgN * 128;          // 64 x 256: 32 KB
 constexpr int kMgStage = kMgATile + kMgBTile;
-constexpr int kMgThreads = 320;               // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue
+constexpr int kMgWTile = kMgM * kMgN * 2;     // a tile's W_base block: 64 KB
+constexpr int kMgThreads = 352;               // warp 0 TMA, warp 1 MMA, warps 2..9 epilogue, warp 10 W_base
 constexpr uint32_t kMgTmemCols = 2 * kMgN;    // two accumulators
 constexpr int kMgPairs = 6;
 
@@ -1232,6 +1235,7 @@ __global__ void __launch_bounds__(256) split_factors_kernel(const float* __restr
 struct MergeParams {
     CUtensorMap a_map;  // Ls [d_out][Kp] bf16, box 64 x 128, 128-byte swizzle
     CUtensorMap b_map;  // Rs [d_in][Kp] bf16, box 64 x 256, 128-byte swizzle
+    CUtensorMap w_map;  // W_base [d_out][d_in] bf16, box 64 x 128, 128-byte swizzle
     const uint16_t* wb;
     void* out;
     uint32_t* err;      // the error word: a wait that timed out sets kErrTimeout
@@ -1247,6 +1251,7 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
     extern __shared__ uint8_t dyn_raw[];
     __shared__ uint64_t full[kMgStages], empty[kMgStages];
     __shared__ uint64_t accfull[2], accempty[2], done;
+    __shared__ uint64_t wfull, wfree;  // the W_base block of a tile landed / the epilogue is done with it
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort;
     uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
@@ -1263,10 +1268,13 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
             mbar_init(&accempty[b], 8);  // the eight epilogue warps
         }
         mbar_init(&done, 1);
+        mbar_init(&wfull, 1);
+        mbar_init(&wfree, 8);  // the eight epilogue warps
         abort = 0;
         fence_mbarrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, kMgTmemCols);
+    uint8_t* wtile = ring + static_cast<size_t>(kMgStages) * kMgStage;  // [4 boxes][128 rows][128 B]
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1284,7 +1292,26 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
         }
         return true;
     };
-    if (warp == 0) {
+    if (warp == 10) {
+        // ------------------------------------------------------------ W_base blocks, one tile at a time
+        if (lane == 0) {
+            int j = 0;
+            for (int tile = c0; tile < p.ntiles; tile += G, ++j) {
+                if (j > 0 && !wait(&wfree, static_cast<uint32_t>(j - 1) & 1u)) break;
+                const int rb = tile / p.ncb, cb = tile - rb * p.ncb;
+                mbar_arrive_expect_tx(&wfull, static_cast<uint32_t>(kMgWTile));
+#pragma unroll
+                for (int bx = 0; bx < kMgN / 64; ++bx)  // columns past d_in read the fill value, never stored
+                    tma_load_2d(wtile + bx * (kMgWTile / 4), &p.w_map, cb * kMgN + 64 * bx, rb * kMgM, &wfull);
+            }
+            if (j > 0) {  // the last block lands before the CTA ends
+                const uint64_t t0 = global_timer_ns();
+                while (!mbar_try_wait(&wfull, static_cast<uint32_t>(j - 1) & 1u) &&
+                       global_timer_ns() - t0 < kWaitLimitNs) {
+                }
+            }
+        }
+    } else if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (one k-step counter g over all tiles)
         if (lane == 0) {
             int g = 0;
@@ -1341,43 +1368,39 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
             }
             mma_commit(&done);  // every MMA issued above has finished when this arrives
         }
-    } else {
+    } else if (warp < 10) {
         // ------------------------------------------------------------ epilogue: one row per thread, columns
         // 128 hc .. 128 hc + 127 of the tile in chunks of 32
         const int q = warp & 3, hc = (warp - 2) >> 2;
+        const int rl = 32 * q + lane;
         int j = 0;
         for (int tile = c0; tile < p.ntiles; tile += G, ++j) {
             const int b = j & 1;
-            if (!__all_sync(0xffffffffu, wait(&accfull[b], static_cast<uint32_t>(j / 2) & 1u))) break;
+            if (!__all_sync(0xffffffffu, wait(&accfull[b], static_cast<uint32_t>(j / 2) & 1u) &&
+                                             wait(&wfull, static_cast<uint32_t>(j) & 1u)))
+                break;
             tc_fence_after();
             const int rb = tile / p.ncb, cb = tile - rb * p.ncb;
-            const int64_t row = static_cast<int64_t>(rb) * kMgM + 32 * q + lane;
+            const int64_t row = static_cast<int64_t>(rb) * kMgM + rl;
             const bool live = row < p.d_out;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * kMgN) +
                                    128u * hc;
             const int64_t cbase = static_cast<int64_t>(cb) * kMgN + 128 * hc;
             const int nch =
                 cbase >= p.d_in ? 0 : static_cast<int>((p.d_in - cbase < 128 ? p.d_in - cbase : 128) / 32);
-            uint4 wn[4];
-            auto load_w = [&](int ch) {
-                if (live && ch < nch) {
-                    const uint4* wr = reinterpret_cast<const uint4*>(p.wb + row * p.d_in + cbase + 32 * ch);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) wn[c] = wr[c];
-                }
-            };
-            load_w(0);
 #pragma unroll 1
             for (int ch = 0; ch < nch; ++ch) {
-                const uint4 wcur[4] = {wn[0], wn[1], wn[2], wn[3]};
-                load_w(ch + 1);
                 uint32_t v[32];
                 tmem_ld32(taddr + 32 * ch, v);
                 if (!live) continue;
                 const int64_t col = cbase + 32 * ch;
+                const int cl = 128 * hc + 32 * ch;  // column within the tile
+                const uint8_t* wbox = wtile + (cl >> 6) * (kMgWTile / 4) + rl * 128;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const uint32_t wv[4] = {wcur[c].x, wcur[c].y, wcur[c].z, wcur[c].w};
+                    const int chunk = ((cl & 63) >> 3) + c;  // 16-byte chunk of the 128-byte box row
+                    const uint4 w = *reinterpret_cast<const uint4*>(wbox + ((chunk ^ (rl & 7)) << 4));
+                    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
                     float o[8];
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -1401,10 +1424,13 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
                     }
                 }
             }
-            // this warp has read its part of accumulator b
+            // this warp has read its part of accumulator b and of the W_base block
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&accempty[b]);
+            if (lane == 0) {
+                mbar_arrive(&accempty[b]);
+                mbar_arrive(&wfree);
+            }
         }
     }
     // tensor memory is freed only after every MMA issued has finished
@@ -1484,7 +1510,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<0>), kTSmem, t0c);
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<1>), kTSmem, t1c);
     static std::atomic<size_t> mgc[kHostMaxDevices];
-    constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + 1024;
+    constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + kMgWTile + 1024;
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(merge_tc_kernel), kMgSmem, mgc);
     if (e0 != cudaSuccess) return e0;
     const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
@@ -1720,6 +1746,9 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                        CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_tma_2d(&mp.b_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Rs, static_cast<uint64_t>(Kp),
                        static_cast<uint64_t>(a.d_in), static_cast<uint64_t>(Kp) * 2, 64, kMgN,
+                       CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_tma_2d(&mp.w_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a.w_base, static_cast<uint64_t>(a.d_in),
+                       static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(a.d_in) * 2, 64, kMgM,
                        CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     mp.wb = a.w_base;
