@@ -76,7 +76,7 @@ NCU_TRAFFIC = {
                                                                       935_756_288 + 63_227_904),
     ("materialize_kernel", "materialize"): ("fae23fcd0ba90d9b", "bd_materialize.cu", 499_370_496 + 426_232_320),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("bf30a84f010b9947", "bd_monosoup.cu", 2_434_392_832 + 114_479_360),
+    (MONOSOUP_CALL, "monosoup"): ("a57f3d4296061505", "bd_monosoup.cu", 2_434_355_456 + 112_421_888),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =
