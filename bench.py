@@ -17,10 +17,13 @@ and CPU oracle baseline: "tiny" (256 x 256, T = 4, per-matrix alpha; L2-
 resident, latency only), "multi" (8192 x 8192 shared W_base, 14 variants,
 64 Zipf-routed tokens), "prefill" (4096 tokens x 8192 x 8192, tensor cores,
 TFLOP/s) and "slice" (8 layers of a 70B-shaped stack, 56 multi-variant
-linears, 14 variants compressed on the GPU, 32 decode tokens).
+linears, 14 variants compressed on the GPU, 32 decode tokens).  On one GPU it
+also carries the rows past the serving setup: "materialize" (W_eff written
+once, 28672 x 8192), "multi_prefill" (4096 Zipf-routed tokens over 14
+variants, tensor cores) and "monosoup" (the merge of 3 task vectors of
+8192 x 8192 at rank 16).
 
---workload runs any of them (and materialize, multi_prefill, monosoup) as the
-main line instead.  `python bench.py --impl reference` times the CPU oracle
+--workload runs any of them as the main line instead.  `python bench.py --impl reference` times the CPU oracle
 instead (the reference arm), on bounded samples of the same workload.
 
 Multi-GPU (--gpus N): one process per GPU.  Without a torchrun environment
@@ -93,6 +96,9 @@ DTYPES = {"monosoup": "bf16 pieces of fp32 (exact splits), f32 accumulate"}
 MONOSOUP = {"d": 8192, "k": 3, "rank": 16, "l": 32, "q": 1}
 # sub-measurements of the default line: (name, timed steps, warm-up steps)
 SUBS = (("tiny", 200, 10), ("multi", 20, 5), ("prefill", 20, 3), ("slice", 10, 3))
+# the rows past the serving configurations (materialised variant, mixed-variant
+# prefill, MonoSoup merge), measured in the default line on one GPU
+SUBS_NEXT = (("materialize", 20, 3), ("multi_prefill", 20, 3), ("monosoup", 10, 3))
 WORKLOADS = ("decode", "tiny", "multi", "prefill", "multi_prefill", "materialize", "monosoup", "slice")
 
 
@@ -1019,8 +1025,9 @@ def run_gpu(args):
 
     subs = {}
     if wl.name == "decode" and not args.no_sub:
-        want = [s for s in args.sub.split(",") if s] or [s[0] for s in SUBS]
-        for name, steps, warmup in SUBS:
+        subs_all = SUBS + (SUBS_NEXT if world == 1 else ())
+        want = [s for s in args.sub.split(",") if s] or [s[0] for s in subs_all]
+        for name, steps, warmup in subs_all:
             if name in want:
                 subs[name] = measure(name, args, steps, warmup, world, rank, local, dev, peaks,
                                      want_cpu=not args.no_cpu)
