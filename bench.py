@@ -60,26 +60,26 @@ FALLBACK_BF16_TFLOPS = 1900.0
 DATA = "synthetic (seeded numpy / torch generators; shapes and distributions of the BitDelta serving setup)"
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from
-# one ncu capture, keyed by kernel; each entry records the sha256 of the
-# kernel's source file at capture time and is ignored once that source has
-# changed.  Summaries of the captures are in profiles/.  An entry whose value
+# one ncu capture (mean over the captured launches), keyed by kernel; each
+# entry records the sha256 of the kernel's source file at capture time and is
+# ignored once that source has changed.  Summaries of the captures are in profiles/.  An entry whose value
 # is a float is a ratio (traffic / algorithmic bytes) taken on one launch of a
 # smaller call of the same kernel and applied to the average launch.
 MONOSOUP_CALL = "bd_monosoup_merge (tensor-core products, Gram / Cholesky / Jacobi, tensor-core merge)"
 NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
-    ("skinny_kernel<1>", "decode"): ("20d4bf1c25e2a4b4", "bd_skinny.cu", 499_405_824 + 3_356_416),
+    ("skinny_kernel<1>", "decode"): ("12c3e9046774fa1a", "bd_skinny.cu", 499_377_365 + 259_541),
     # 4 rows per CTA (kCompressRowsPerCta in bd_internal.h)
-    ("compress_kernel", "decode"): ("364b9a156a18e55b", "bd_compress.cu", 939_566_080 + 7_655_936),
-    ("prefill_kernel", "prefill"): ("e4118a0ff3103961", "bd_prefill.cu", 619_106_816 + 68_359_936),
+    ("compress_kernel", "decode"): ("157f94bb54f54bb5", "bd_compress.cu", 939_564_117 + 6_540_587),
+    ("prefill_kernel", "prefill"): ("384ee679f294ff5d", "bd_prefill.cu", 621_643_264 + 65_396_267),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
-    ("multi_prepare + multi_kernel<8>", "multi"): ("d89f83fcd4e67914", "bd_multi.cu", 255_770_880 + 3_986_432),
+    ("multi_prepare + multi_kernel<8>", "multi"): ("a3057edfbaaadd8d", "bd_multi.cu", 255_719_211 + 114_603),
     # the grouped prefill_kernel only (router, plan and gather add about 134 MB of x copies)
-    ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("e4118a0ff3103961", "bd_prefill.cu",
-                                                                      935_756_288 + 63_227_904),
-    ("materialize_kernel", "materialize"): ("fae23fcd0ba90d9b", "bd_materialize.cu", 499_370_496 + 426_232_320),
+    ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("384ee679f294ff5d", "bd_prefill.cu",
+                                                                      936_756_779 + 60_209_195),
+    ("materialize_kernel", "materialize"): ("6b6adea86f0f4408", "bd_materialize.cu", 499_315_883 + 422_566_528),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("a57f3d4296061505", "bd_monosoup.cu", 2_434_355_456 + 112_421_888),
+    (MONOSOUP_CALL, "monosoup"): ("e1fe4e4aab152919", "bd_monosoup.cu", 2_434_349_312 + 112_774_656),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =

@@ -20,7 +20,9 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libbitdelta.so")
+# BD_LIBRARY selects another build of the library (the bounds-checked one,
+# libbitdelta_bounds.so, in its test)
+LIB_PATH = os.environ.get("BD_LIBRARY") or os.path.join(_HERE, "libbitdelta.so")
 
 BD_OK = 0
 BD_ERR_INVALID_ARG = 1
@@ -32,6 +34,7 @@ BD_ERR_CUDA = 6
 BD_ERR_TIMEOUT = 7
 BD_ERR_WORKSPACE = 8
 BD_ERR_DEVICE = 9
+BD_ERR_BOUNDS = 10
 
 BD_ALPHA_PER_MATRIX = 0
 BD_ALPHA_PER_ROW = 1
@@ -47,7 +50,8 @@ EXPORTS = (
     "bd_linear_workspace_size", "bd_linear",
     "bd_linear_multi_workspace_size", "bd_linear_multi",
     "bd_route_workspace_size", "bd_route",
-    "bd_debug_reconstruct", "bd_check_async", "bd_compress_noalloc",
+    "bd_debug_reconstruct", "bd_check_async", "bd_compress_noalloc", "bd_debug_bounds_check",
+    "bd_debug_bounds_enabled",
     "bd_cache_create", "bd_cache_destroy", "bd_cache_set_source", "bd_cache_step", "bd_cache_release",
     "bd_cache_get_stats", "bd_cache_query", "bd_cache_debug_fail_load", "bd_materialize",
     "bd_monosoup_workspace_size", "bd_monosoup_merge",
@@ -106,6 +110,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
             "bd_route": ([_vp, _i64, _i32, _vp, _vp, _vp, _sz, _vp], _int),
             "bd_debug_reconstruct": ([_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp], _int),
             "bd_check_async": ([_vp, _vp], _int),
+            "bd_debug_bounds_check": ([_vp], _int),
+            "bd_debug_bounds_enabled": ([], _int),
             "bd_compress_noalloc": ([_vp, _vp, _i64, _i64, _int, _vp, _vp, _vp], _int),
             "bd_materialize": ([_vp, _vp, _vp, _int, _i64, _i64, _vp, _vp], _int),
             "bd_monosoup_workspace_size": ([_i64, _i64, _i32, _i32, _i32], _sz),
@@ -290,6 +296,19 @@ def bd_debug_reconstruct(w_base, signs, alpha, alpha_mode, w_eff, stream=None) -
                                        _ptr(alpha, "alpha", (torch.float32,)), int(alpha_mode), d_out, d_in,
                                        _ptr(w_eff, "w_eff", (torch.float32,)), _stream(stream)),
            "bd_debug_reconstruct")
+
+
+def bd_debug_bounds_check() -> tuple[int, int]:
+    """(status, kernel bits): BD_ERR_BOUNDS if a kernel of a bounds-checked
+    build met an index outside its buffer since the last call; synchronises
+    the device."""
+    bits = ctypes.c_uint32(0)
+    st = int(load().bd_debug_bounds_check(ctypes.byref(bits)))
+    return st, int(bits.value)
+
+
+def bd_debug_bounds_enabled() -> bool:
+    return bool(load().bd_debug_bounds_enabled())
 
 
 def bd_check_async(ws, stream=None) -> int:

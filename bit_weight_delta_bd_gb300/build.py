@@ -1,6 +1,8 @@
 """Builds libbitdelta.so in-tree for sm_103a with nvcc (no cmake, no torch
 extension machinery): every csrc/*.cu file is compiled in parallel, then
-linked into one shared library next to this file."""
+linked into one shared library next to this file.  build(debug_bounds=True)
+builds the bounds-checked variant, libbitdelta_bounds.so (-DBD_DEBUG_BOUNDS,
+its own object directory)."""
 from __future__ import annotations
 
 import concurrent.futures as cf
@@ -15,6 +17,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbitdelta.so")
+OBJ_DIR_BOUNDS = os.path.join(HERE, "_build_bounds")
+LIB_BOUNDS = os.path.join(HERE, "libbitdelta_bounds.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -39,22 +43,26 @@ def _deps():
         os.path.join(ROOT, "include", "bitdelta.h"), __file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OBJ_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False, debug_bounds: bool = False) -> str:
+    lib = LIB_BOUNDS if debug_bounds else LIB
+    obj_dir = OBJ_DIR_BOUNDS if debug_bounds else OBJ_DIR
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(obj_dir, exist_ok=True)
     exe = nvcc()
     extra = ["-Xptxas", "-v"] if ptxas_info else []
+    if debug_bounds:
+        extra.append("-DBD_DEBUG_BOUNDS")
 
     def compile_one(src):
-        obj = os.path.join(OBJ_DIR, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [exe, *_flags(extra), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -67,15 +75,16 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
         for _, log in results:
             if log:
                 sys.stderr.write(log)
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [exe, "-shared", *ARCH, "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
-           "-Xlinker", "-rpath,/usr/local/cuda/lib64"]
+           "-Xlinker", "-rpath,/usr/local/cuda/lib64", "-ldl"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv,
+                debug_bounds="--debug-bounds" in sys.argv))

@@ -97,6 +97,7 @@ const char* bd_status_string(bd_status s)
         case BD_ERR_TIMEOUT: return "BD_ERR_TIMEOUT: an in-kernel wait timed out";
         case BD_ERR_WORKSPACE: return "BD_ERR_WORKSPACE: workspace missing or too small";
         case BD_ERR_DEVICE: return "BD_ERR_DEVICE: current device is not compute capability 10.3";
+        case BD_ERR_BOUNDS: return "BD_ERR_BOUNDS: a kernel met an index outside its buffer (bounds-checked build)";
     }
     return "BD_ERR_UNKNOWN";
 }
@@ -117,6 +118,7 @@ size_t bd_compress_workspace_size(int64_t d_out, int64_t /*d_in*/, int alpha_mod
 bd_status bd_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out, int64_t d_in, int alpha_mode,
                       uint32_t* signs, float* alpha, void* ws, size_t ws_bytes, void* stream)
 {
+    BD_NVTX_RANGE("bd_compress");
     if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
     if (d_out < 0) return BD_ERR_UNSUPPORTED_SHAPE;
     if (bd_status s = check_d_in(d_in)) return s;
@@ -143,6 +145,7 @@ bd_status bd_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_ou
 bd_status bd_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, const float* alpha, int alpha_mode,
                                int64_t d_out, int64_t d_in, float* w_eff, void* stream)
 {
+    BD_NVTX_RANGE("bd_debug_reconstruct");
     if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
     if (d_out < 0) return BD_ERR_UNSUPPORTED_SHAPE;
     if (bd_status s = check_d_in(d_in)) return s;
@@ -157,6 +160,7 @@ bd_status bd_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, co
 bd_status bd_materialize(const uint16_t* w_base, const uint32_t* signs, const float* alpha, int alpha_mode,
                          int64_t d_out, int64_t d_in, uint16_t* w_eff, void* stream)
 {
+    BD_NVTX_RANGE("bd_materialize");
     if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
     if (d_out < 0) return BD_ERR_UNSUPPORTED_SHAPE;
     if (bd_status s = check_d_in(d_in)) return s;
@@ -187,6 +191,7 @@ bd_status bd_monosoup_merge(const uint16_t* w_base, const uint16_t* const* w_ft,
                             int64_t d_in, int32_t rank, int32_t l, int32_t power_iters, const float* omega,
                             void* w_merged, int out_dtype, void* ws, size_t ws_bytes, void* stream)
 {
+    BD_NVTX_RANGE("bd_monosoup_merge");
     if (out_dtype != BD_OUT_BF16 && out_dtype != BD_OUT_F32) return BD_ERR_INVALID_ARG;
     if (k < 1 || k > BD_MAX_VARIANTS || rank < 0 || l < 4 || l > bd::monosoup_max_l() || l % 4 != 0 || rank > l ||
         power_iters < 0 || power_iters > 16)
@@ -252,6 +257,7 @@ bd_status bd_linear(const uint16_t* x, int64_t T, const uint16_t* w_base, const 
                     int alpha_mode, int64_t d_out, int64_t d_in, void* y, int out_dtype, void* ws, size_t ws_bytes,
                     void* stream)
 {
+    BD_NVTX_RANGE("bd_linear");
     if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
     if (bd_status s = check_linear_common(x, T, w_base, d_out, d_in, y, out_dtype, ws, ws_bytes,
                                           bd_linear_workspace_size(T, d_out, d_in)))
@@ -357,6 +363,7 @@ bd_status bd_linear_multi(const uint16_t* x, int64_t T, const int32_t* vid, int3
                           const uint16_t* w_base, int64_t d_out, int64_t d_in, void* y, int out_dtype, void* ws,
                           size_t ws_bytes, void* stream)
 {
+    BD_NVTX_RANGE("bd_linear_multi");
     if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
     if (V < 1 || V > BD_MAX_VARIANTS) return BD_ERR_INVALID_ARG;
     if (bd_status s = check_linear_common(x, T, w_base, d_out, d_in, y, out_dtype, ws, ws_bytes,
@@ -438,6 +445,7 @@ size_t bd_route_workspace_size(int64_t /*T*/, int32_t /*V*/) { return kWsHeader;
 bd_status bd_route(const int32_t* vid, int64_t T, int32_t V, int32_t* perm, int32_t* seg_off, void* ws,
                    size_t ws_bytes, void* stream)
 {
+    BD_NVTX_RANGE("bd_route");
     if (V < 0 || V > BD_MAX_VARIANTS) return BD_ERR_INVALID_ARG;
     if (T < 0 || T > INT32_MAX) return BD_ERR_UNSUPPORTED_SHAPE;
     if (bd_status s = check_ws(ws, ws_bytes, bd_route_workspace_size(T, V))) return s;
@@ -453,6 +461,25 @@ bd_status bd_route(const int32_t* vid, int64_t T, int32_t V, int32_t* perm, int3
 }
 
 // ------------------------------------------------------------------ async errors
+
+int bd_debug_bounds_check(uint32_t* kernels)
+{
+    const uint32_t f = bd::bounds_take_compress() | bd::bounds_take_skinny() | bd::bounds_take_multi() |
+                       bd::bounds_take_prefill() | bd::bounds_take_route() | bd::bounds_take_materialize() |
+                       bd::bounds_take_monosoup();
+    if (kernels) *kernels = f;
+    if (f == ~0u) return BD_ERR_CUDA;
+    return f ? BD_ERR_BOUNDS : BD_OK;
+}
+
+int bd_debug_bounds_enabled(void)
+{
+#ifdef BD_DEBUG_BOUNDS
+    return 1;
+#else
+    return 0;
+#endif
+}
 
 bd_status bd_check_async(void* ws, void* stream)
 {

@@ -161,6 +161,7 @@ bd_status bd_cache_set_source(bd_cache* c, int32_t variant, const void* host_src
 
 bd_status bd_cache_step(bd_cache* c, const int32_t* vid, int64_t n, void* stream, const void** delta, int32_t* state)
 {
+    BD_NVTX_RANGE("bd_cache_step");
     if (!c || n < 0 || (n > 0 && (!vid || !delta || !state))) return BD_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lk(c->mu);
     if (!c->acquired.empty()) return BD_ERR_INVALID_ARG;  // the previous step was not released

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(32 * kCompressRowsPerCta)
 #pragma unroll
             for (int u = 0; u < kUnroll; ++u) {
                 const int64_t col = (s0 + u) * kStripe + lane * 8;
-                if (s0 + u < n_stripes && col < d_in) {
+                if (s0 + u < n_stripes && col < d_in && bd_in_range(kBkCompress, row * d_in + col, 8, d_out * d_in)) {
                     vb[u] = ld_stream_v4(pb + col);
                     vf[u] = ld_stream_v4(pf + col);
                 } else {
@@ -82,7 +82,9 @@ __global__ void __launch_bounds__(32 * kCompressRowsPerCta)
                 uint32_t word = byte << (8 * (lane & 3));
                 word |= __shfl_xor_sync(0xffffffffu, word, 1);
                 word |= __shfl_xor_sync(0xffffffffu, word, 2);
-                if ((lane & 3) == 0 && valid) ps[s * (kStripe / 32) + (lane >> 2)] = word;
+                const int64_t wi = s * (kStripe / 32) + (lane >> 2);
+                if ((lane & 3) == 0 && valid && bd_in(kBkCompress, row * (d_in / 32) + wi, d_out * (d_in / 32)))
+                    ps[wi] = word;
             }
         }
     }
@@ -93,7 +95,7 @@ __global__ void __launch_bounds__(32 * kCompressRowsPerCta)
     if (per_row) {
         if (lane == 0 && row < d_out) {
             if (!isfinite(acc)) raise_error(err, kErrNonFinite);
-            alpha[row] = static_cast<float>(acc / static_cast<double>(d_in));
+            if (bd_in(kBkCompress, row, d_out)) alpha[row] = static_cast<float>(acc / static_cast<double>(d_in));
         }
         return;
     }
@@ -103,7 +105,8 @@ __global__ void __launch_bounds__(32 * kCompressRowsPerCta)
         double total = 0.0;
         for (int w = 0; w < kCompressRowsPerCta; ++w) total += warp_sum[w];
         if (!isfinite(total)) raise_error(err, kErrNonFinite);
-        partials[blockIdx.x] = total;
+        if (bd_in(kBkCompress, blockIdx.x, (d_out + kCompressRowsPerCta - 1) / kCompressRowsPerCta))
+            partials[blockIdx.x] = total;
     }
 }
 
@@ -113,7 +116,8 @@ __global__ void __launch_bounds__(1024)
 {
     __shared__ double sm[1024];
     double s = 0.0;
-    for (int64_t i = threadIdx.x; i < n_parts; i += 1024) s += partials[i];
+    for (int64_t i = threadIdx.x; i < n_parts; i += 1024)
+        if (bd_in(kBkAlphaFinalize, i, n_parts)) s += partials[i];
     sm[threadIdx.x] = s;
     __syncthreads();
     for (int o = 512; o > 0; o >>= 1) {
@@ -131,6 +135,9 @@ __global__ void debug_reconstruct_kernel(const uint16_t* __restrict__ w_base, co
     for (int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; e < n;
          e += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t r = e / d_in, c = e % d_in;
+        if (!bd_in(kBkReconstruct, e, n) || !bd_in(kBkReconstruct, r * (d_in / 32) + c / 32, d_out * (d_in / 32)) ||
+            !bd_in(kBkReconstruct, per_row ? r : 0, per_row ? d_out : 1))
+            continue;
         const float w = __uint_as_float(static_cast<uint32_t>(w_base[e]) << 16);
         const uint32_t bit = (signs[r * (d_in / 32) + c / 32] >> (c % 32)) & 1u;
         const float a = per_row ? alpha[r] : alpha[0];
@@ -162,5 +169,7 @@ cudaError_t launch_debug_reconstruct(const uint16_t* w_base, const uint32_t* sig
                                                                                  per_row ? 1 : 0, d_out, d_in, w_eff);
     return cudaGetLastError();
 }
+
+BD_BOUNDS_TAKE(bounds_take_compress)
 
 }  // namespace bd

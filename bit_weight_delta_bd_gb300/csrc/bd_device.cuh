@@ -25,6 +25,52 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bits)
     if (err) atomicOr(err, bits);
 }
 
+// ---------------------------------------------------------------- bounds-checked builds
+// With -DBD_DEBUG_BOUNDS the plain global loads and stores of the kernels are
+// preceded by bd_in(kernel, i, n): true when 0 <= i < n; otherwise bit
+// `kernel` of the translation unit's flag word is set and the caller skips
+// the access (no trap).  bd_debug_bounds_check() reads and clears the flag
+// words of every translation unit.  TMA copies need no check: the hardware
+// fills the out-of-range elements of a load and drops them from a store.  In
+// normal builds bd_in is the constant true.
+enum BoundsKernel : uint32_t {
+    kBkCompress = 0, kBkAlphaFinalize, kBkReconstruct, kBkSkinny, kBkMultiPrepare, kBkMulti, kBkPrefill,
+    kBkPrefillPlan, kBkGather, kBkRoute, kBkMaterialize, kBkMsProd, kBkMsSplit, kBkMsSlices, kBkMsGram,
+    kBkMsGramSum, kBkMsChol, kBkMsJacobi, kBkMsTri, kBkMsApply, kBkMsMerge
+};
+#ifdef BD_DEBUG_BOUNDS
+namespace {
+__device__ uint32_t g_bounds_flags = 0;  // one word per translation unit
+}
+__device__ __forceinline__ bool bd_in(uint32_t kernel, int64_t i, int64_t n)
+{
+    if (i >= 0 && i < n) return true;
+    atomicOr(&g_bounds_flags, 1u << kernel);
+    return false;
+}
+// the range [i, i + len) lies in [0, n)
+__device__ __forceinline__ bool bd_in_range(uint32_t kernel, int64_t i, int64_t len, int64_t n)
+{
+    if (i >= 0 && len >= 0 && i + len <= n) return true;
+    atomicOr(&g_bounds_flags, 1u << kernel);
+    return false;
+}
+// host: the flags of this translation unit, cleared (synchronises the device)
+#define BD_BOUNDS_TAKE(fn)                                                \
+    uint32_t fn()                                                         \
+    {                                                                     \
+        uint32_t v = 0, z = 0;                                            \
+        if (cudaMemcpyFromSymbol(&v, g_bounds_flags, sizeof v) != cudaSuccess) return ~0u; \
+        if (cudaMemcpyToSymbol(g_bounds_flags, &z, sizeof z) != cudaSuccess) return ~0u;   \
+        return v;                                                         \
+    }
+#else
+__device__ __forceinline__ constexpr bool bd_in(uint32_t, int64_t, int64_t) { return true; }
+__device__ __forceinline__ constexpr bool bd_in_range(uint32_t, int64_t, int64_t, int64_t) { return true; }
+#define BD_BOUNDS_TAKE(fn) \
+    uint32_t fn() { return 0; }
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p)
 {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -5,9 +5,30 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#ifndef BD_NO_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace bd {
 
 constexpr int kMaxVariants = 64;
+
+// An NVTX range around each compute entry point of the C ABI, named after
+// the entry point, so that a profiler's timeline (or ncu --nvtx-include)
+// groups the launches of one call.  NVTX v3 is header-only: with no tool
+// attached a push or a pop tests one function pointer.  -DBD_NO_NVTX leaves
+// the ranges out.
+#ifndef BD_NO_NVTX
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define BD_NVTX_RANGE(name) const ::bd::NvtxRange bd_nvtx_range_(name)
+#else
+#define BD_NVTX_RANGE(name) static_cast<void>(0)
+#endif
 
 // Maps a CUDA runtime result to a library status: cudaSuccess -> 0
 // (BD_OK), anything else -> BD_ERR_CUDA, with the code kept as the calling
@@ -140,6 +161,16 @@ struct MonoSoupArgs {
     uint32_t* err;                 // the asynchronous error word (start of ws)
     int sm_count;                  // SMs of the current device
 };
+
+// bounds-checked builds: the flag words of each translation unit, read and
+// cleared (0 in normal builds)
+uint32_t bounds_take_compress();
+uint32_t bounds_take_skinny();
+uint32_t bounds_take_multi();
+uint32_t bounds_take_prefill();
+uint32_t bounds_take_route();
+uint32_t bounds_take_materialize();
+uint32_t bounds_take_monosoup();
 
 int monosoup_max_l();
 size_t monosoup_workspace_size(int64_t d_out, int64_t d_in, int k, int r, int l);

@@ -54,12 +54,17 @@ __global__ void __launch_bounds__(256) materialize_kernel(const uint16_t* __rest
 {
     const int64_t gpr = d_in / 8;  // groups of 8 weights per row (a multiple of 16)
     for (int64_t r = blockIdx.x; r < d_out; r += gridDim.x) {
+        if (!bd_in(kBkMaterialize, per_row ? r : 0, per_row ? d_out : 1)) continue;
         const uint32_t ab = __float_as_uint(alpha[per_row ? r : 0]);
         const uint16_t* wr = w + r * d_in;
         const uint8_t* sr = reinterpret_cast<const uint8_t*>(signs + r * (d_in / 32));  // byte g: bits of group g
         uint16_t* orow = out + r * d_in;
         int64_t g = threadIdx.x;
+        const int64_t nw = d_out * d_in, nb = d_out * (d_in / 8);  // weights, sign bytes
         for (; g + 3 * 256 < gpr; g += 4 * 256) {
+            if (!bd_in_range(kBkMaterialize, r * d_in + 8 * g, 8 * (3 * 256 + 1), nw) ||
+                !bd_in_range(kBkMaterialize, r * (d_in / 8) + g, 3 * 256 + 1, nb))
+                continue;
             uint4 u[4];
             uint32_t bits[4];
 #pragma unroll
@@ -72,7 +77,8 @@ __global__ void __launch_bounds__(256) materialize_kernel(const uint16_t* __rest
                 *reinterpret_cast<uint4*>(orow + 8 * (g + 256 * k)) = materialize8(u[k], bits[k], ab);
         }
         for (; g < gpr; g += 256)
-            *reinterpret_cast<uint4*>(orow + 8 * g) = materialize8(ld_nc_v4(wr + 8 * g), __ldg(sr + g), ab);
+            if (bd_in_range(kBkMaterialize, r * d_in + 8 * g, 8, nw) && bd_in(kBkMaterialize, r * (d_in / 8) + g, nb))
+                *reinterpret_cast<uint4*>(orow + 8 * g) = materialize8(ld_nc_v4(wr + 8 * g), __ldg(sr + g), ab);
     }
 }
 
@@ -87,5 +93,7 @@ cudaError_t launch_materialize(const uint16_t* w_base, const uint32_t* signs, co
     materialize_kernel<<<grid, 256, 0, stream>>>(w_base, signs, alpha, per_row, d_out, d_in, w_eff);
     return cudaGetLastError();
 }
+
+BD_BOUNDS_TAKE(bounds_take_materialize)
 
 }  // namespace bd

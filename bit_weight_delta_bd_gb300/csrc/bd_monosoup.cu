@@ -290,7 +290,10 @@ __global__ void __launch_bounds__(kPThreads, prod_ctas<L4>()) dprod_kernel(const
     float* out = p.part + (static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * nrows * l;
     for (int e = tid; e < kOut * l; e += kPThreads) {
         const int rr = e / l, c = e - rr * l;
-        if (o0 + rr < nrows) out[(o0 + rr) * l + c] = red[rr * kRS + c];
+        if (o0 + rr < nrows &&
+            bd_in(kBkMsProd, (static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * nrows * l + (o0 + rr) * l + c,
+                  static_cast<int64_t>(gridDim.z) * gridDim.y * nrows * l))
+            out[(o0 + rr) * l + c] = red[rr * kRS + c];
     }
 }
 
@@ -392,7 +395,10 @@ __global__ void __launch_bounds__(256) split_small_kernel(const float* __restric
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int64_t k = 8 * g + j;
-            const float4 f = (k < K && c0 < l) ? *reinterpret_cast<const float4*>(src + k * l + c0)
+            const float4 f = (k < K && c0 < l &&
+                              bd_in_range(kBkMsSplit, blockIdx.y * zstride + k * l + c0, 4,
+                                          (gridDim.y - 1) * zstride + K * l))
+                                 ? *reinterpret_cast<const float4*>(src + k * l + c0)
                                                : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
             v[j][0] = f.x;
             v[j][1] = f.y;
@@ -421,6 +427,9 @@ __global__ void __launch_bounds__(256) split_small_kernel(const float* __restric
                 w3[j / 2] = __byte_perm(p3[0], p3[1], 0x7632);
             }
             const int c = c0 + cc;
+            const int64_t ob = static_cast<int64_t>(blockIdx.y) * 128 * Kp + 8 * g, on = gridDim.y * 128 * Kp;
+            if (!bd_in_range(kBkMsSplit, ob + c * Kp, 8, on) || !bd_in_range(kBkMsSplit, ob + (64 + c) * Kp, 8, on))
+                continue;
             *reinterpret_cast<uint4*>(o + static_cast<int64_t>(c) * Kp) = make_uint4(w1[0], w1[1], w1[2], w1[3]);
             *reinterpret_cast<uint4*>(o + static_cast<int64_t>(32 + c) * Kp) = make_uint4(w2[0], w2[1], w2[2], w2[3]);
             *reinterpret_cast<uint4*>(o + static_cast<int64_t>(64 + c) * Kp) = make_uint4(w3[0], w3[1], w3[2], w3[3]);
@@ -619,7 +628,9 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
                                  : 0.0f;
                     y.w = nt > 0 ? (__uint_as_float(d0[c + 3]) + __uint_as_float(d1[c + 3])) + __uint_as_float(d2[c + 3])
                                  : 0.0f;
-                    *reinterpret_cast<float4*>(out + c) = y;
+                    if (bd_in_range(kBkMsProd, ((static_cast<int64_t>(z) * gridDim.y + blockIdx.y) * nrows + row) * p.l + c,
+                                    4, static_cast<int64_t>(nz) * gridDim.y * nrows * p.l))
+                        *reinterpret_cast<float4*>(out + c) = y;
                 }
             }
         }
@@ -640,9 +651,13 @@ __global__ void __launch_bounds__(256) sum_slices_kernel(const float* __restrict
     const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (e >= n) return;
     const float* pz = part + static_cast<int64_t>(blockIdx.y) * nslice * n;
-    float s = pz[e];
-    for (int k = 1; k < nslice; ++k) s += pz[k * n + e];
-    out[static_cast<int64_t>(blockIdx.y) * n + e] = s;
+    const int64_t np = static_cast<int64_t>(gridDim.y) * nslice * n;
+    const int64_t zb = static_cast<int64_t>(blockIdx.y) * nslice * n;
+    float s = bd_in(kBkMsSlices, zb + e, np) ? pz[e] : 0.0f;
+    for (int k = 1; k < nslice; ++k)
+        if (bd_in(kBkMsSlices, zb + k * n + e, np)) s += pz[k * n + e];
+    if (bd_in(kBkMsSlices, static_cast<int64_t>(blockIdx.y) * n + e, static_cast<int64_t>(gridDim.y) * n))
+        out[static_cast<int64_t>(blockIdx.y) * n + e] = s;
 }
 
 // ---------------------------------------------------------------- small-matrix steps
@@ -721,7 +736,10 @@ __global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT =
         for (int e = tid; e < 32 * kMaxL; e += nt) {
             const int rr = e >> 6, cc = e & 63;
             const int64_t row = r0 + rr;
-            sa[rr][cc] = (row < b1 && cc < l) ? a[row * l + cc] : 0.0f;
+            sa[rr][cc] = (row < b1 && cc < l &&
+                          bd_in(kBkMsGram, blockIdx.y * n * l + row * l + cc, static_cast<int64_t>(gridDim.y) * n * l))
+                             ? a[row * l + cc]
+                             : 0.0f;
         }
         __syncthreads();
         const int nr = b1 - r0 < 32 ? static_cast<int>(b1 - r0) : 32;
@@ -737,8 +755,12 @@ __global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT =
             float hi, lo;
             two_sum(s[m], c[m], hi, lo);
             const int64_t pb = static_cast<int64_t>(blockIdx.x) * l * l;
-            part[pb + pi[m] * l + pj[m]] = make_float2(hi, lo);
-            part[pb + pj[m] * l + pi[m]] = make_float2(hi, lo);
+            const int64_t zb = static_cast<int64_t>(blockIdx.y) * gridDim.x * l * l,
+                          np = static_cast<int64_t>(gridDim.y) * gridDim.x * l * l;
+            if (bd_in(kBkMsGram, zb + pb + pi[m] * l + pj[m], np) && bd_in(kBkMsGram, zb + pb + pj[m] * l + pi[m], np)) {
+                part[pb + pi[m] * l + pj[m]] = make_float2(hi, lo);
+                part[pb + pj[m] * l + pi[m]] = make_float2(hi, lo);
+            }
         }
     }
 }
@@ -762,6 +784,9 @@ __global__ void __launch_bounds__(256) gram_sum_kernel(const float2* __restrict_
         for (int u = 0; u < 4; ++u) {
             const int bb = b + 32 * u;
             if (bb < nb) {
+                if (!bd_in(kBkMsGramSum, (static_cast<int64_t>(blockIdx.y) * nb + bb) * ll + e,
+                           static_cast<int64_t>(gridDim.y) * nb * ll))
+                    continue;
                 const float2 v = part[static_cast<int64_t>(bb) * ll + e];
                 ff_add(s[u], c[u], v.x, v.y);
             }
@@ -779,7 +804,8 @@ __global__ void __launch_bounds__(256) gram_sum_kernel(const float2* __restrict_
     if (lane == 0) {
         float hi, lo;
         two_sum(sv, cv, hi, lo);
-        G_all[static_cast<int64_t>(blockIdx.y) * ll + e] = make_float2(hi, lo);
+        if (bd_in(kBkMsGramSum, static_cast<int64_t>(blockIdx.y) * ll + e, static_cast<int64_t>(gridDim.y) * ll))
+            G_all[static_cast<int64_t>(blockIdx.y) * ll + e] = make_float2(hi, lo);
     }
 }
 
@@ -830,7 +856,11 @@ __global__ void __launch_bounds__(256) chol_kernel(const float2* __restrict__ G_
     float* rinv = Rf + kMaxL * kMaxL;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ti = tid >> 4, tj = tid & 15;
-    for (int e = tid; e < l * l; e += 256) g[e / l][e % l] = G[e];
+    for (int e = tid; e < l * l; e += 256)
+        g[e / l][e % l] = bd_in(kBkMsChol, static_cast<int64_t>(blockIdx.x) * l * l + e,
+                                static_cast<int64_t>(gridDim.x) * l * l)
+                              ? G[e]
+                              : make_float2(0.0f, 0.0f);
     __syncthreads();
     if (warp == 0) {
         float m = 0.0f;
@@ -883,9 +913,10 @@ __global__ void __launch_bounds__(256) chol_kernel(const float2* __restrict__ G_
     }
     for (int e = tid; e < l * l; e += 256) {
         const int i = e / l, j = e % l;
-        Rf[e] = (j >= i && live[i]) ? g[i][j].x : 0.0f;
+        if (bd_in(kBkMsChol, e, kMaxL * kMaxL)) Rf[e] = (j >= i && live[i]) ? g[i][j].x : 0.0f;
     }
-    for (int i = tid; i < l; i += 256) rinv[i] = live[i] ? rdiag[i] : 0.0f;
+    for (int i = tid; i < l; i += 256)
+        if (bd_in(kBkMsChol, i, kMaxL)) rinv[i] = live[i] ? rdiag[i] : 0.0f;
 }
 
 // One CTA of 256 threads per checkpoint: the symmetric eigenproblem of G by
@@ -932,7 +963,9 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int e = tid; e < kMaxL * kMaxL; e += kJacobiThreads) {
         const int i = e >> 6, j = e & 63;
-        A[i][j] = (i < l && j < l) ? __fadd_rn(G[i * l + j].x, G[i * l + j].y) : 0.0f;
+        A[i][j] = (i < l && j < l && bd_in(kBkMsJacobi, blockIdx.x * l * l + i * l + j, gridDim.x * l * l))
+                      ? __fadd_rn(G[i * l + j].x, G[i * l + j].y)
+                      : 0.0f;
         V[i][j] = i == j ? 1.0f : 0.0f;
     }
     const int n = l + (l & 1);
@@ -1063,7 +1096,8 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __
     __syncthreads();
     for (int e = tid; e < l * r; e += kJacobiThreads) {
         const int c = idx[e % r];
-        ur[e] = V[e / r][c] * vnorm[c];
+        if (bd_in(kBkMsJacobi, static_cast<int64_t>(blockIdx.x) * l * r + e, static_cast<int64_t>(gridDim.x) * l * r))
+            ur[e] = V[e / r][c] * vnorm[c];
     }
 }
 
@@ -1086,12 +1120,13 @@ __global__ void __launch_bounds__(kTriThreads) tri_solve_kernel(float* a_all, in
     __shared__ float sd[kMaxL];
     for (int e = threadIdx.x; e < kMaxL * kTriStride; e += blockDim.x) {
         const int j = e / kTriStride, m = e - j * kTriStride;
-        srt[j][m] = (j < l && m < l) ? Rf[m * l + j] : 0.0f;
+        srt[j][m] = (j < l && m < l && bd_in(kBkMsTri, m * l + j, kMaxL * kMaxL)) ? Rf[m * l + j] : 0.0f;
     }
     for (int i = threadIdx.x; i < kMaxL; i += blockDim.x) sd[i] = i < l ? rinv[i] : 0.0f;
     __syncthreads();
     const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (row >= n) return;
+    if (!bd_in_range(kBkMsTri, blockIdx.y * n * l + row * l, l, static_cast<int64_t>(gridDim.y) * n * l)) return;
     float x[kMaxL];
     float4* ar = reinterpret_cast<float4*>(a + row * l);  // l is a multiple of 4
 #pragma unroll
@@ -1135,13 +1170,16 @@ __global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ 
     __shared__ __align__(16) float sm[kMaxL][kMaxL];
     for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
         const int c = e >> 6, j = e & 63;
-        sm[c][j] = (c < l && j < m) ? M[c * m + j] : 0.0f;
+        sm[c][j] = (c < l && j < m && bd_in(kBkMsApply, blockIdx.y * l * m + c * m + j, gridDim.y * l * m))
+                       ? M[c * m + j]
+                       : 0.0f;
     }
     __syncthreads();
     const int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int jg = static_cast<int>(o / n);
     const int64_t row = o - static_cast<int64_t>(jg) * n;
     if (4 * jg >= m) return;
+    if (!bd_in_range(kBkMsApply, blockIdx.y * n * l + row * l, l, static_cast<int64_t>(gridDim.y) * n * l)) return;
     const float4* s = reinterpret_cast<const float4*>(src + row * l);
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     for (int c4 = 0; c4 < l / 4; ++c4) {
@@ -1158,7 +1196,9 @@ __global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ 
     }
 #pragma unroll
     for (int t = 0; t < 4; ++t)
-        if (4 * jg + t < m) dst[static_cast<int64_t>(4 * jg + t) * n + row] = acc[t];
+        if (4 * jg + t < m && bd_in(kBkMsApply, blockIdx.y * n * m + static_cast<int64_t>(4 * jg + t) * n + row,
+                                    static_cast<int64_t>(gridDim.y) * n * m))
+            dst[static_cast<int64_t>(4 * jg + t) * n + row] = acc[t];
 }
 
 // ---------------------------------------------------------------- the merge on the tensor cores
@@ -1216,7 +1256,9 @@ __global__ void __launch_bounds__(256) split_factors_kernel(const float* __restr
         const int pr = kk / K, e = kk - pr * K;
         uint32_t h = 0;
         if (pr < kMgPairs) {
-            const float v = src[static_cast<int64_t>(e) * rows + n];
+            const float v = bd_in(kBkMsSplit, static_cast<int64_t>(e) * rows + n, static_cast<int64_t>(K) * rows)
+                                ? src[static_cast<int64_t>(e) * rows + n]
+                                : 0.0f;
             const int pc = merge_piece(pr, side);
             const uint32_t b1 = __float_as_uint(v) & 0xFFFF0000u;
             const float r1 = __fsub_rn(v, __uint_as_float(b1));
@@ -1229,7 +1271,8 @@ __global__ void __launch_bounds__(256) split_factors_kernel(const float* __restr
         else
             w[j >> 1] = h;
     }
-    *reinterpret_cast<uint4*>(dst + n * Kp + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
+    if (bd_in_range(kBkMsSplit, n * Kp + 8 * g, 8, rows * Kp))
+        *reinterpret_cast<uint4*>(dst + n * Kp + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 struct MergeParams {
@@ -1409,6 +1452,7 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
                         o[2 * u] = bf16_bits_to_float(wv[u] & 0xFFFFu) + p.inv_k * a0;
                         o[2 * u + 1] = bf16_bits_to_float(wv[u] >> 16) + p.inv_k * a1;
                     }
+                    if (!bd_in_range(kBkMsMerge, row * p.d_in + col + 8 * c, 8, p.d_out * p.d_in)) continue;
                     if (p.out_f32) {
                         float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + row * p.d_in + col + 8 * c);
                         dst[0] = make_float4(o[0], o[1], o[2], o[3]);
@@ -1765,5 +1809,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     merge_tc_kernel<<<mg_grid, kMgThreads, kMgSmem, st>>>(mp);
     return cudaGetLastError();
 }
+
+BD_BOUNDS_TAKE(bounds_take_monosoup)
 
 }  // namespace bd

@@ -115,6 +115,7 @@ struct MultiParams {
     CUtensorMap w_map;                   // [d_out][d_in] bf16, box 64 x 128 rows, 128B swizzle
     CUtensorMap x_map;                   // x [T][d_in] bf16 (caller order), box 64 x max(16, 8*NT), 128B swizzle
     const uint8_t* xp;                   // padded, permuted, scaled tiles of the variant phases
+    int64_t xp_bytes;                    // their extent (bounds-checked builds)
     const float* corr;                   // [T][nsplit] partial corrections C per sorted position
     const int32_t* vid;
     const float* alpha[kMaxVariants];
@@ -163,7 +164,7 @@ __device__ void route_group(Routing& rt, const int32_t* vid, int T, int V, uint3
     if (tid < kMaxTok) {
         int k = -1;
         if (tid < T) {
-            const int v = vid[tid];
+            const int v = bd_in(kBkMulti, tid, T) ? vid[tid] : -1;
             const bool ok = (v >= -1 && v < V);
             if (!ok && blockIdx.x == 0 && blockIdx.y == 0) raise_error(err, kErrBadVariant);
             k = ok ? v + 1 : 0;
@@ -271,7 +272,8 @@ __device__ __forceinline__ uint16_t scaled_bits(uint16_t xb, float sigma)
 __global__ void __launch_bounds__(kPrepThreads) multi_prepare_kernel(const uint16_t* __restrict__ x,
                                                                      const int32_t* __restrict__ vid, int T, int V,
                                                                      int64_t d_in, uint8_t* __restrict__ xp,
-                                                                     float* __restrict__ corr, int nsplit)
+                                                                     float* __restrict__ corr, int nsplit,
+                                                                     int64_t xp_bytes)
 {
     __shared__ Routing rt;
     __shared__ float part[kPrepThreads / 32];
@@ -310,7 +312,8 @@ __global__ void __launch_bounds__(kPrepThreads) multi_prepare_kernel(const uint1
     if (c < nc) {
         const int64_t col0 = static_cast<int64_t>(c) * kChunk + 32 * q;
         uint16_t v[32];
-        if (xrow) {
+        if (xrow && bd_in_range(kBkMultiPrepare, static_cast<int64_t>(rt.perm[pos]) * d_in + col0, 32,
+                                static_cast<int64_t>(T) * d_in)) {
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const uint4 w = ld_nc_v4(xrow + col0 + 8 * u);
@@ -339,7 +342,8 @@ __global__ void __launch_bounds__(kPrepThreads) multi_prepare_kernel(const uint1
                     o[k] = static_cast<uint32_t>(scaled_bits(v[lo], recode_sigma(k))) |
                            (static_cast<uint32_t>(scaled_bits(v[hi], recode_sigma(k))) << 16);
                 }
-                *reinterpret_cast<uint4*>(tile + ((i * 8 + g) * 4 + q) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+                if (bd_in_range(kBkMultiPrepare, (tile - xp) + ((i * 8 + g) * 4 + q) * 16, 16, xp_bytes))
+                    *reinterpret_cast<uint4*>(tile + ((i * 8 + g) * 4 + q) * 16) = make_uint4(o[0], o[1], o[2], o[3]);
             }
         }
     }
@@ -352,7 +356,8 @@ __global__ void __launch_bounds__(kPrepThreads) multi_prepare_kernel(const uint1
     if (tid == 0) {
         float s = 0.0f;
         for (int w = 0; w < kPrepThreads / 32; ++w) s += part[w];
-        corr[static_cast<int64_t>(pos) * nsplit + blockIdx.y] = s;
+        if (bd_in(kBkMultiPrepare, static_cast<int64_t>(pos) * nsplit + blockIdx.y, static_cast<int64_t>(T) * nsplit))
+            corr[static_cast<int64_t>(pos) * nsplit + blockIdx.y] = s;
     }
 }
 
@@ -444,8 +449,9 @@ __device__ __forceinline__ bool variant_phase(MultiShared& sh, const MultiParams
     const int v = rt.act[slot];
     const int64_t ra = row0 + rl0, rb = ra + 8;
     const float* al = p.alpha[v];
-    const float a2a = ra < p.d_out ? 2.0f * al[p.per_row ? ra : 0] : 0.0f;
-    const float a2b = rb < p.d_out ? 2.0f * al[p.per_row ? rb : 0] : 0.0f;
+    const int64_t na = p.per_row ? p.d_out : 1;
+    const float a2a = ra < p.d_out && bd_in(kBkMulti, p.per_row ? ra : 0, na) ? 2.0f * al[p.per_row ? ra : 0] : 0.0f;
+    const float a2b = rb < p.d_out && bd_in(kBkMulti, p.per_row ? rb : 0, na) ? 2.0f * al[p.per_row ? rb : 0] : 0.0f;
 #pragma unroll
     for (int r = 0; r < L; ++r) {
         float m[4];
@@ -625,9 +631,10 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
                             const int c = c_begin + c0 + cc;
                             tma_load_2d(st + cc * kSignChunk, &p.sign_map[v], 4 * c, static_cast<int>(row0),
                                         &sh.full[s]);
-                            bulk_g2s(st + cnt * kSignChunk + cc * L * kPadTile,
-                                     src + (static_cast<int64_t>(c) * len + t0) * kPadTile,
-                                     static_cast<uint32_t>(L * kPadTile), &sh.full[s]);
+                            const uint8_t* from = src + (static_cast<int64_t>(c) * len + t0) * kPadTile;
+                            if (bd_in_range(kBkMulti, from - p.xp, static_cast<int64_t>(L) * kPadTile, p.xp_bytes))
+                                bulk_g2s(st + cnt * kSignChunk + cc * L * kPadTile, from,
+                                         static_cast<uint32_t>(L * kPadTile), &sh.full[s]);
                         }
                     }
                     __syncwarp();
@@ -737,13 +744,17 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
     if (tid < T) {
         grid_dependency_wait();  // the corrections come from the prepare pass
         float c = 0.0f;
-        for (int sp = 0; sp < p.nsplit; ++sp) c += p.corr[static_cast<int64_t>(tid) * p.nsplit + sp];
+        for (int sp = 0; sp < p.nsplit; ++sp)
+            if (bd_in(kBkMulti, static_cast<int64_t>(tid) * p.nsplit + sp, p.T * p.nsplit))
+                c += p.corr[static_cast<int64_t>(tid) * p.nsplit + sp];
         corr_s[tid] = c;
     }
     for (int o = tid; o < n_act * nr; o += kThreads) {
         const int a = o >> lnr, r = o & (nr - 1);
         const int64_t row = row0 + rank * nr + r;
-        alpha_s[o] = row < p.d_out ? p.alpha[rt.act[a]][p.per_row ? row : 0] : 0.0f;
+        alpha_s[o] = row < p.d_out && bd_in(kBkMulti, p.per_row ? row : 0, p.per_row ? p.d_out : 1)
+                         ? p.alpha[rt.act[a]][p.per_row ? row : 0]
+                         : 0.0f;
     }
     cluster.sync();
     for (int o = tid; o < nr * T; o += kThreads) {
@@ -755,6 +766,7 @@ __global__ void __launch_bounds__(kThreads, 2) multi_kernel(const __grid_constan
         const int key = rt.keyp[pos];
         if (key >= 1) y = fmaf(-alpha_s[rt.slot_of_key[key] * nr + r], corr_s[pos], y);
         const int64_t idx = static_cast<int64_t>(rt.perm[pos]) * p.d_out + row;
+        if (!bd_in(kBkMulti, idx, p.T * p.d_out)) continue;
         if (p.out_f32)
             static_cast<float*>(p.y)[idx] = y;
         else
@@ -842,6 +854,7 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
     const int nsplit = multi_corr_splits(a.d_in);
     static thread_local MultiParams prm;  // ~9 KB: kept off the stack
     prm.xp = a.xp;
+    prm.xp_bytes = static_cast<int64_t>(multi_max_ptiles(T, a.V)) * 8 * a.d_in * 2;
     prm.corr = a.corr;
     prm.vid = a.vid;
     prm.y = a.y;
@@ -889,7 +902,8 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
     const size_t smem = kBaseStages * base_stage + kVarStages * static_cast<size_t>(kVarSlot) + 1024;
 
     const dim3 prep_grid(static_cast<unsigned>(T + 7 * (T < a.V ? T : a.V)), static_cast<unsigned>(nsplit));
-    multi_prepare_kernel<<<prep_grid, kPrepThreads, 0, stream>>>(a.x, a.vid, T, a.V, a.d_in, a.xp, a.corr, nsplit);
+    multi_prepare_kernel<<<prep_grid, kPrepThreads, 0, stream>>>(a.x, a.vid, T, a.V, a.d_in, a.xp, a.corr, nsplit,
+                                                                  prm.xp_bytes);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>((a.d_out + kRows - 1) / kRows * ck);
@@ -900,5 +914,7 @@ cudaError_t launch_multi(const MultiArgs& a, cudaStream_t stream)
         default: return launch_nt<8>(prm, smem, grid, stream);
     }
 }
+
+BD_BOUNDS_TAKE(bounds_take_multi)
 
 }  // namespace bd

@@ -62,6 +62,7 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb)
 extern "C" bd_status bd_compress_noalloc(const uint16_t* w_base, const uint16_t* w_ft, int64_t d_out, int64_t d_in,
                                          int alpha_mode, uint32_t* signs, float* alpha, void* stream)
 {
+    BD_NVTX_RANGE("bd_compress_noalloc");
     if (alpha_mode != BD_ALPHA_PER_MATRIX && alpha_mode != BD_ALPHA_PER_ROW) return BD_ERR_INVALID_ARG;
     if (d_out < 0 || d_out > kMaxRows) return BD_ERR_UNSUPPORTED_SHAPE;
     if (d_in <= 0 || d_in % 128 != 0) return BD_ERR_UNSUPPORTED_SHAPE;

@@ -169,8 +169,8 @@ __device__ __forceinline__ TileInfo tile_info(const P& p, int t, uint32_t rank)
     ti.nmma = BN;
     ti.valid = true;
     if constexpr (kGrouped) {
-        const int4 b = p.plan[tb];
-        ti.valid = b.w != 0;  // past the plan
+        const int4 b = bd_in(kBkPrefill, tb, p.ntb) ? p.plan[tb] : make_int4(0, 0, 0, 0);
+        ti.valid = b.w != 0 && bd_in(kBkPrefill, b.z, kMaxVariants + 1);  // past the plan
         ti.tok0 = b.x;
         ti.tok_end = b.y;
         ti.s_map = &p.s_maps[b.z >= 1 ? b.z - 1 : 0];
@@ -302,7 +302,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefill
             if (!ti.valid) continue;
             const int64_t row = ti.row0 + rl;
             float a = 0.0f;
-            if (ti.alpha && row < p.d_out) a = ti.alpha[p.per_row ? row : 0];
+            if (ti.alpha && row < p.d_out && bd_in(kBkPrefill, p.per_row ? row : 0, p.per_row ? p.d_out : 1))
+                a = ti.alpha[p.per_row ? row : 0];
             const uint32_t ab = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a)));
             const uint32_t neg = ((ab << 16) | ab) ^ 0x80008000u;  // (-alpha, -alpha) as bf16x2
             for (int i = 0; i < nk; ++i, ++g) {
@@ -365,7 +366,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefill
             auto store = [&](int col, float val) {
                 int64_t tk = ti.tok0 + col;
                 if (tk >= ti.tok_end || row >= p.d_out) return;
-                if constexpr (std::is_same<P, GroupedPrefillParams>::value) tk = p.perm[tk];
+                if constexpr (std::is_same<P, GroupedPrefillParams>::value) {
+                    if (!bd_in(kBkPrefill, tk, p.T)) return;
+                    tk = p.perm[tk];
+                }
+                if (!bd_in(kBkPrefill, tk * p.d_out + row, p.T * p.d_out)) return;
                 if (p.out_f32)
                     static_cast<float*>(p.y)[tk * p.d_out + row] = val;
                 else
@@ -409,8 +414,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefill
                     for (int e = 0; e < 2; ++e) {
                         if (row < p.d_out && 2 * q + e < nvalid) {
                             int64_t tk = ti.tok0 + c0 + 2 * q + e;
-                            if constexpr (std::is_same<P, GroupedPrefillParams>::value) tk = p.perm[tk];
-                            yb[tk * p.d_out + row] = static_cast<uint16_t>(e ? (pk[q] >> 16) : (pk[q] & 0xFFFFu));
+                            if constexpr (std::is_same<P, GroupedPrefillParams>::value) {
+                                if (!bd_in(kBkPrefill, tk, p.T)) continue;
+                                tk = p.perm[tk];
+                            }
+                            if (bd_in(kBkPrefill, tk * p.d_out + row, p.T * p.d_out))
+                                yb[tk * p.d_out + row] = static_cast<uint16_t>(e ? (pk[q] >> 16) : (pk[q] & 0xFFFFu));
                         }
                     }
                 }
@@ -503,6 +512,7 @@ __global__ void prefill_plan_kernel(const int32_t* __restrict__ seg_off, int V, 
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     int n = 0;
     for (int k = 0; k <= V; ++k) {
+        if (!bd_in(kBkPrefillPlan, k + 1, V + 2)) break;
         const int a = seg_off[k], e = seg_off[k + 1];
         for (int t = a; t < e && n < nblk; t += BN) plan[n++] = make_int4(t, e, k, 1);
     }
@@ -513,7 +523,8 @@ __global__ void prefill_plan_kernel(const int32_t* __restrict__ seg_off, int V, 
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int64_t d_in,
                                    uint16_t* __restrict__ xs)
 {
-    const int64_t i = blockIdx.x;
+    const int64_t i = blockIdx.x;  // grid = T rows
+    if (!bd_in(kBkGather, perm[i], gridDim.x)) return;
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(perm[i]) * d_in);
     uint4* dst = reinterpret_cast<uint4*>(xs + i * d_in);
     for (int64_t c = threadIdx.x; c < d_in / 8; c += blockDim.x) dst[c] = src[c];
@@ -567,5 +578,7 @@ cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t str
     prefill_kernel<GroupedPrefillParams><<<dim3(static_cast<unsigned>(2 * ncl)), kThreads, smem, stream>>>(prm);
     return cudaGetLastError();
 }
+
+BD_BOUNDS_TAKE(bounds_take_prefill)
 
 }  // namespace bd

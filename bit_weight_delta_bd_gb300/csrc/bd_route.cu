@@ -42,11 +42,11 @@ __global__ void __launch_bounds__(kRouteThreads)
     if (tid == 0) {
         int acc = 0;
         for (int k = 0; k < n_keys; ++k) {
-            seg_off[k] = acc;
+            if (bd_in(kBkRoute, k, n_keys + 1)) seg_off[k] = acc;
             running[k] = acc;
             acc += total[k];
         }
-        seg_off[n_keys] = acc;
+        if (bd_in(kBkRoute, n_keys, n_keys + 1)) seg_off[n_keys] = acc;
     }
     __syncthreads();
 
@@ -73,7 +73,8 @@ __global__ void __launch_bounds__(kRouteThreads)
             running[tid] = run;
         }
         __syncthreads();
-        if (key >= 0) perm[warp_cnt[warp][key] + rank] = static_cast<int32_t>(t);
+        if (key >= 0 && bd_in(kBkRoute, warp_cnt[warp][key] + rank, T))
+            perm[warp_cnt[warp][key] + rank] = static_cast<int32_t>(t);
         __syncthreads();
     }
 }
@@ -86,5 +87,7 @@ cudaError_t launch_route(const int32_t* vid, int64_t T, int V, int32_t* perm, in
     route_kernel<<<1, kRouteThreads, 0, stream>>>(vid, T, V, perm, seg_off, err);
     return cudaGetLastError();
 }
+
+BD_BOUNDS_TAKE(bounds_take_route)
 
 }  // namespace bd

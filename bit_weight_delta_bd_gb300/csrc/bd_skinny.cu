@@ -283,8 +283,11 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
                     sg += ps[r * Tpad + t];
                 }
                 const int64_t row = row0 + r;
-                const float y = fmaf(p.alpha[p.per_row ? row : 0], sg, b);
                 const int64_t idx = static_cast<int64_t>(t) * p.d_out + row;
+                if (!bd_in(kBkSkinny, p.per_row ? row : 0, p.per_row ? p.d_out : 1) ||
+                    !bd_in(kBkSkinny, idx, p.T * p.d_out))
+                    continue;
+                const float y = fmaf(p.alpha[p.per_row ? row : 0], sg, b);
                 if (p.out_f32)
                     static_cast<float*>(p.y)[idx] = y;
                 else
@@ -400,5 +403,7 @@ cudaError_t launch_skinny(const SkinnyArgs& a, cudaStream_t stream)
         default: return launch_nt<8>(prm, smem, stream);
     }
 }
+
+BD_BOUNDS_TAKE(bounds_take_skinny)
 
 }  // namespace bd

@@ -63,7 +63,8 @@ typedef enum bd_status {
     BD_ERR_CUDA = 6,              /* a CUDA runtime call or launch failed */
     BD_ERR_TIMEOUT = 7,           /* (async) a bounded in-kernel wait gave up */
     BD_ERR_WORKSPACE = 8,         /* workspace null or smaller than required */
-    BD_ERR_DEVICE = 9             /* current device is not a compute capability 10.3 GPU */
+    BD_ERR_DEVICE = 9,            /* current device is not a compute capability 10.3 GPU */
+    BD_ERR_BOUNDS = 10            /* (bounds-checked builds) a kernel met an index outside its buffer */
 } bd_status;
 
 typedef enum bd_alpha_mode { BD_ALPHA_PER_MATRIX = 0, BD_ALPHA_PER_ROW = 1 } bd_alpha_mode;
@@ -352,6 +353,25 @@ bd_status bd_cache_query(bd_cache* cache, int32_t variant, int32_t* resident, in
  * is enqueued, so that the failure path above can be exercised on the host
  * (also by a dry-run cache, which makes no CUDA call). */
 bd_status bd_cache_debug_fail_load(bd_cache* cache, int64_t n);
+
+/* Bounds-checked builds (compiled with -DBD_DEBUG_BOUNDS; the library
+ * built as libbitdelta_bounds.so): every plain global load and store of the
+ * kernels checks its index against its buffer and skips the access when it
+ * lies outside (TMA copies are bounded by the hardware).  This is a test
+ * aid, not part of the BitDelta post.  bd_debug_bounds_check synchronises the
+ * device, reads and clears the flags of every kernel and returns
+ * BD_ERR_BOUNDS if one met an out-of-range index since the last call (the
+ * kernels' bits in *kernels, if not NULL; bit numbers in the library
+ * source), BD_ERR_CUDA if the flags could not be read, else BD_OK (always
+ * BD_OK in normal builds).  bd_debug_bounds_enabled returns 1 in a
+ * bounds-checked build, 0 otherwise.
+ *
+ * Profiling: each compute entry point (compress, linear, multi, route,
+ * materialise, reconstruct, MonoSoup merge, cache step) pushes an NVTX range
+ * named after itself for the length of the call, so that a profiler can
+ * select one call's launches (unless built with -DBD_NO_NVTX). */
+int bd_debug_bounds_check(uint32_t* kernels);
+int bd_debug_bounds_enabled(void);
 
 /* Waits for `stream`, then reads and clears the error word in `ws`.
  * Returns BD_OK, or the first asynchronous error found (in the order

@@ -37,11 +37,25 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in range(10):
+    for code in range(11):
         s = bd.status_string(code)
         assert s.startswith("BD_")
     assert bd.status_string(999) == "BD_ERR_UNKNOWN"
     assert bd.bd_version() == 10000
+
+
+def test_bounds_checked_build_exports_every_declared_symbol(lib):
+    """The bounds-checked variant (-DBD_DEBUG_BOUNDS) builds, exports the
+    same functions and says it is that variant; the normal library says it is
+    not."""
+    from bit_weight_delta_bd_gb300 import build
+
+    path = build.build(debug_bounds=True)
+    blib = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(blib, name), name
+    assert blib.bd_debug_bounds_enabled() == 1
+    assert lib.bd_debug_bounds_enabled() == 0
 
 
 def test_cuda_error_names(lib):
