@@ -511,22 +511,30 @@ def _sized_vid(rng, sizes):
     return vid[rng.permutation(len(vid))]
 
 
-@pytest.mark.parametrize("case", ["random", "block_edges", "one_variant", "all_base"])
+@pytest.mark.parametrize("case", ["random", "block_edges", "many_tails", "mixed_sizes", "one_variant", "all_base"])
 def test_multi_prefill_exact(dev, case):
     """Grouped tensor-core prefill on dyadic inputs: exact against the oracle.
     Segments of 1, 255, 256 and 257 tokens (blocks ending at, before and after
-    a 256-token boundary), a single variant, and a batch of base-model tokens
-    only; ragged d_out."""
+    a 256-token boundary); 15 keys of 1 to 300 tokens (tails of every
+    16-column MMA width, bf16 output too); segments of 250, 10, 300 and 129
+    tokens after an empty base segment; a single variant, and a batch of
+    base-model tokens only; ragged d_out."""
     rng = np.random.default_rng(len(case))
     if case == "random":
         V, vid = 5, rng.integers(-1, 5, size=700).astype(np.int32)
     elif case == "block_edges":
         V, vid = 4, _sized_vid(rng, [331, 256, 257, 1, 255])
+    elif case == "many_tails":
+        V, vid = 14, _sized_vid(rng, [5, 1, 2, 3, 15, 16, 17, 31, 33, 63, 64, 65, 100, 7, 300])
+    elif case == "mixed_sizes":
+        V, vid = 4, _sized_vid(rng, [0, 250, 10, 300, 129])
     elif case == "one_variant":
         V, vid = 1, np.zeros(512, np.int32)
     else:
         V, vid = 14, np.full(600, -1, np.int32)
     _multi_case(dev, 400 + len(vid), V, 200, 512, vid.tolist())
+    if case == "many_tails":  # bf16 output as well
+        _multi_case(dev, 400 + len(vid), V, 200, 512, vid.tolist(), f32=False)
 
 
 def test_multi_wide_range_activations(dev):
