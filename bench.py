@@ -79,7 +79,7 @@ NCU_TRAFFIC = {
                                                                       936_756_779 + 60_209_195),
     ("materialize_kernel", "materialize"): ("6b6adea86f0f4408", "bd_materialize.cu", 499_315_883 + 422_566_528),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("e1fe4e4aab152919", "bd_monosoup.cu", 2_434_349_312 + 112_774_656),
+    (MONOSOUP_CALL, "monosoup"): ("fc477f7bc8f24ff5", "bd_monosoup.cu", 2_434_371_328 + 112_458_752),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =

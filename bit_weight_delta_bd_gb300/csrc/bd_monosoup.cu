@@ -313,8 +313,9 @@ size_t dprod_smem()
 // fp32 value v is v1 + v2 + v3 with v1 = v with the low 16 bits of its
 // encoding cleared, v2 the same of v - v1 and v3 = v - v1 - v2 (each
 // subtraction exact, each piece a bf16 value), so that Delta S is the sum of
-// the nine products of pieces, each bf16 x bf16 product exact and the sums
-// in fp32 in the tensor core.
+// the products of pieces, each bf16 x bf16 product exact and the sums in
+// fp32 in the tensor core; the six products of pieces a, b with a + b <= 2
+// are kept (the other three are below the fp32 rounding of the sums).
 //   A = a piece of Delta (M = 128 rows of Delta for the sketch, 128 columns
 //       for the transpose product; K = its other index), formed by the
 //       piece warps from the W_i and W_base tiles and written to tensor
@@ -322,9 +323,10 @@ size_t dprod_smem()
 //   B = the pieces of the small operand stacked along N: row 32 b + c =
 //       piece b of column c (N = 96, rows c >= l zero), K-major in shared
 //       memory (split_small_kernel writes them, a TMA box brings 64 K);
-//   D[m][32 b + c] (+)= sum over the k-step of A_a B^T for the three pieces
-//       a of Delta (three MMAs of M = 128, N = 96, K = 16 per k-step) in
-//       tensor memory; the result is D[m][c] + D[m][32 + c] + D[m][64 + c].
+//   D[m][32 b + c] (+)= sum over the k-step of A_a B_b^T, b < 3 - a, for the
+//       three pieces a of Delta (MMAs of M = 128, N = 96, 64 and 32, K = 16
+//       per k-step) in tensor memory; the result is
+//       D[m][c] + D[m][32 + c] + D[m][64 + c].
 // A stage holds only the W_i and W_base tiles and the B tile (44 KB), so four
 // stages keep four tiles of Delta in flight per SM.  The W tiles of a stage
 // are free as soon as the piece warps hold their values (wfree), the B tile
@@ -531,7 +533,13 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            const uint32_t idesc = idesc_bf16_f32(kTM, kTNB);
+            // piece a of Delta times the first 3 - a pieces of the small operand (B rows
+            // 0 .. 32 (3 - a) - 1): the products of pieces a, b with a + b <= 2, as in
+            // the merge.  Piece b + 1 is below 2^-7 of the value that piece b was cut
+            // from, so the dropped products (a + b >= 3) of one term add up to less
+            // than 2^-20 |Delta_j S_j|, below the fp32 accumulation error over K.
+            constexpr uint32_t idesc_a[3] = {idesc_bf16_f32(kTM, 96), idesc_bf16_f32(kTM, 64),
+                                             idesc_bf16_f32(kTM, 32)};
             for (int t = 0; t < nt; ++t) {
                 const int st = t % kTStages;
                 if (!wait(&afull[st], static_cast<uint32_t>(t / kTStages) & 1u)) break;
@@ -542,8 +550,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
                 for (int kk = 0; kk < kTK / 16; ++kk) {
 #pragma unroll
                     for (int a = 0; a < 3; ++a)
-                        mma_ts(tmem + kTDCol, acol + 32u * a + 8u * kk, bdesc + static_cast<uint64_t>(2 * kk), idesc,
-                               (t | kk | a) != 0 ? 1u : 0u);
+                        mma_ts(tmem + kTDCol, acol + 32u * a + 8u * kk, bdesc + static_cast<uint64_t>(2 * kk),
+                               idesc_a[a], (t | kk | a) != 0 ? 1u : 0u);
                 }
                 mma_commit(&empty[st]);
             }
