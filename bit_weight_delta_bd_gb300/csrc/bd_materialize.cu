@@ -28,18 +28,38 @@ __device__ __forceinline__ uint32_t add_round_bf16(float w, float d)
 }
 
 // 8 weights of one row: W_base bits in u, sign bits in the low byte of bits.
+// The fp32 sums are rounded to bf16 pairs by the conversion unless one of
+// them, in any lane of the warp, is a bf16 midpoint; then every lane takes
+// the exact path.
 __device__ __forceinline__ uint4 materialize8(uint4 u, uint32_t bits, uint32_t ab)
 {
     const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-    uint32_t o[4];
+    const uint32_t nb = ~bits;
+    float w[8], d[8], s[8];
+    uint32_t mid = 0;
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
-        // +alpha for a set bit, -alpha (sign bit flipped) for a clear one
-        const float d0 = __uint_as_float(ab ^ ((~bits >> (2 * h) & 1u) << 31));
-        const float d1 = __uint_as_float(ab ^ ((~bits >> (2 * h + 1) & 1u) << 31));
-        const uint32_t lo = add_round_bf16(__uint_as_float(in[h] << 16), d0);
-        const uint32_t hi = add_round_bf16(__uint_as_float(in[h] & 0xFFFF0000u), d1);
-        o[h] = (lo & 0xFFFFu) | (hi << 16);
+        w[2 * h] = __uint_as_float(in[h] << 16);
+        w[2 * h + 1] = __uint_as_float(in[h] & 0xFFFF0000u);
+        d[2 * h] = __uint_as_float(ab ^ ((nb << (31 - 2 * h)) & 0x80000000u));
+        d[2 * h + 1] = __uint_as_float(ab ^ ((nb << (30 - 2 * h)) & 0x80000000u));
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        s[k] = __fadd_rn(w[k], d[k]);
+        mid |= (__float_as_uint(s[k]) & 0xFFFFu) == 0x8000u ? 1u : 0u;
+    }
+    uint32_t o[4];
+    if (__any_sync(0xffffffffu, mid)) {
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+            o[h] = (add_round_bf16(w[2 * h], d[2 * h]) & 0xFFFFu) | (add_round_bf16(w[2 * h + 1], d[2 * h + 1]) << 16);
+    } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const __nv_bfloat162 r = __floats2bfloat162_rn(s[2 * h], s[2 * h + 1]);
+            o[h] = *reinterpret_cast<const uint32_t*>(&r);
+        }
     }
     return make_uint4(o[0], o[1], o[2], o[3]);
 }
