@@ -77,7 +77,7 @@ NCU_TRAFFIC = {
     # the grouped prefill_kernel only (router, plan and gather add about 134 MB of x copies)
     ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("384ee679f294ff5d", "bd_prefill.cu",
                                                                       936_756_779 + 60_209_195),
-    ("materialize_kernel", "materialize"): ("6b6adea86f0f4408", "bd_materialize.cu", 499_315_883 + 422_566_528),
+    ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
     (MONOSOUP_CALL, "monosoup"): ("fc477f7bc8f24ff5", "bd_monosoup.cu", 2_434_371_328 + 112_458_752),
 }
