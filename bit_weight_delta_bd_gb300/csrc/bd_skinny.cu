@@ -13,7 +13,9 @@
 // d_out, so a row's arithmetic does not change when the rows are sharded) and
 // is persistent: it takes the blocks of 16*kConsumers output rows numbered
 // c, c + C, c + 2C, ... (C clusters resident), reducing each block's partial
-// sums through distributed shared memory, in rank order.  Inside the CTA one
+// outputs (base + alpha * sign over the CTA's slice, one fma per value, so
+// that one buffer holds them) through distributed shared memory, in rank
+// order.  Inside the CTA one
 // producer thread streams 128-column stages into a ring of shared-memory
 // buffers with a handful of 2-D TMA boxes per stage, one running stage count
 // across the blocks, and the consumer warps (16 rows each) run the MMAs:
@@ -144,14 +146,15 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
 
     // ---------------------------------------------------------------- pipeline
     // stage layout: [W half 0 | W half 1 | x half 0 | x half 1 | sign tile], 1024-byte aligned;
-    // after the ring: two reduction buffers (base and sign partials, [kRows][Tpad] fp32 each)
+    // after the ring: two reduction buffers of the CTA's partial outputs
+    // base + alpha * sign, [kRows][Tpad] fp32 each
     const int stages = p.stages;
     constexpr int kWHalf = kRows * kHalfRowBytes;
     constexpr int kXHalf = Tpad * kHalfRowBytes;
     constexpr int kSignOff = 2 * kWHalf + 2 * kXHalf;
     constexpr int kSignTile = kRows * kSignRowBytes;
     constexpr int kStageBytes = (kSignOff + kSignTile + 1023) & ~1023;
-    constexpr int kRedFloats = 2 * kRows * Tpad;  // one buffer: base then sign partials
+    constexpr int kRedFloats = kRows * Tpad;  // one buffer
     float* red_all = reinterpret_cast<float*>(dyn + static_cast<size_t>(stages) * kStageBytes);
     const int nc = static_cast<int>(d_in / kChunk);
     const int c_begin = static_cast<int>(static_cast<int64_t>(rank) * nc / CK);
@@ -195,8 +198,7 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
     for (int u = 0; u < n_mine; ++u) {
         const int64_t row0 = static_cast<int64_t>(cl + u * p.n_clusters) * kRows;
         const int valid_rows = static_cast<int>(p.d_out - row0 < kRows ? p.d_out - row0 : kRows);
-        float* red_b = red_all + (u & 1) * kRedFloats;
-        float* red_s = red_b + kRows * Tpad;
+        float* red = red_all + (u & 1) * kRedFloats;
         if (warp == kConsumers) {
             // ------------------------------------------------------------ producer warp
             // the rest of this block, then the first `stages` stages of the next one (their slots
@@ -253,18 +255,20 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&sh.empty[s]);
             }
-            // this block's partial sums into this CTA's reduction buffer of the block's parity
+            // this block's partial outputs base + alpha * sign (alpha of the row) into
+            // this CTA's reduction buffer of the block's parity
+            float a0 = 0.0f, a1 = 0.0f;
+            if (rl0 < valid_rows && bd_in(kBkSkinny, p.per_row ? row0 + rl0 : 0, p.per_row ? p.d_out : 1))
+                a0 = p.alpha[p.per_row ? row0 + rl0 : 0];
+            if (rl0 + 8 < valid_rows && bd_in(kBkSkinny, p.per_row ? row0 + rl0 + 8 : 0, p.per_row ? p.d_out : 1))
+                a1 = p.alpha[p.per_row ? row0 + rl0 + 8 : 0];
 #pragma unroll
             for (int j = 0; j < NT; ++j) {
                 const int pos = 8 * j + 2 * q;
-                red_b[rl0 * Tpad + pos] = accb[j][0];
-                red_b[rl0 * Tpad + pos + 1] = accb[j][1];
-                red_b[(rl0 + 8) * Tpad + pos] = accb[j][2];
-                red_b[(rl0 + 8) * Tpad + pos + 1] = accb[j][3];
-                red_s[rl0 * Tpad + pos] = accs[j][0];
-                red_s[rl0 * Tpad + pos + 1] = accs[j][1];
-                red_s[(rl0 + 8) * Tpad + pos] = accs[j][2];
-                red_s[(rl0 + 8) * Tpad + pos + 1] = accs[j][3];
+                red[rl0 * Tpad + pos] = fmaf(a0, accs[j][0], accb[j][0]);
+                red[rl0 * Tpad + pos + 1] = fmaf(a0, accs[j][1], accb[j][1]);
+                red[(rl0 + 8) * Tpad + pos] = fmaf(a1, accs[j][2], accb[j][2]);
+                red[(rl0 + 8) * Tpad + pos + 1] = fmaf(a1, accs[j][3], accb[j][3]);
             }
         }
         // ---------------------------------------------------------------- cluster K reduction of block u
@@ -275,19 +279,11 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
             for (int o = tid; o < nr * T; o += 32 * kConsumers) {
                 const int t = o / nr, r = r_lo + o % nr;
                 if (r >= valid_rows) continue;
-                float b = 0.0f, sg = 0.0f;
-                for (int k = 0; k < CK; ++k) {
-                    const float* pb = cluster.map_shared_rank(red_b, k);
-                    const float* ps = cluster.map_shared_rank(red_s, k);
-                    b += pb[r * Tpad + t];
-                    sg += ps[r * Tpad + t];
-                }
+                float y = cluster.map_shared_rank(red, 0)[r * Tpad + t];
+                for (int k = 1; k < CK; ++k) y += cluster.map_shared_rank(red, k)[r * Tpad + t];
                 const int64_t row = row0 + r;
                 const int64_t idx = static_cast<int64_t>(t) * p.d_out + row;
-                if (!bd_in(kBkSkinny, p.per_row ? row : 0, p.per_row ? p.d_out : 1) ||
-                    !bd_in(kBkSkinny, idx, p.T * p.d_out))
-                    continue;
-                const float y = fmaf(p.alpha[p.per_row ? row : 0], sg, b);
+                if (!bd_in(kBkSkinny, idx, p.T * p.d_out)) continue;
                 if (p.out_f32)
                     static_cast<float*>(p.y)[idx] = y;
                 else
@@ -389,7 +385,7 @@ cudaError_t launch_skinny(const SkinnyArgs& a, cudaStream_t stream)
     ck = ck < 1 ? 1 : ck > 4 ? 4 : ck;
     prm.CK = ck;
     const size_t stage_bytes = stage_bytes_for(nt);
-    const size_t red = 2u * (2u * kRows * (8u * nt) * sizeof(float));  // two buffers of base + sign partials
+    const size_t red = 2u * (kRows * (8u * nt) * sizeof(float));  // two buffers of partial outputs
     int stages = kMaxStages;
     while (stages > 2 && stages * stage_bytes + red + 1024 > kSmemBudget) --stages;
     prm.stages = stages;
