@@ -1226,12 +1226,15 @@ __global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ 
 // CTA's tiles), with two accumulators of 256 columns, so that the MMAs of
 // the next tile run while warps 2..9 add W_base to this one row by row (lane
 // quarter warp % 4, column half (warp - 2) / 4).  Warp 10 loads each tile's
-// W_base block by TMA (four 64-column boxes, 128-byte swizzle, 64 KB) as soon
-// as the epilogue has finished with the previous one, so the epilogue reads
-// W_base from shared memory.
+// W_base block by TMA (four 64-column boxes, 128-byte swizzle, 64 KB) into
+// one of two buffers as soon as the epilogue has finished with the tile two
+// back, so the epilogue reads W_base from shared memory and the next block
+// is in flight while it works.  Two operand stages (48 KB each) leave room
+// for the two W_base buffers.
 constexpr int kMgM = 128;
 constexpr int kMgN = 256;
-constexpr int kMgStages = 3;
+constexpr int kMgStages = 2;
+constexpr int kMgWBufs = 2;                   // W_base blocks in flight
 constexpr int kMgATile = kMgM * 128;          // 64 reduction indices x 128 rows, bf16: 16 KB
 constexpr int kMgBTile = kMgN * 128;          // 64 x 256: 32 KB
 constexpr int kMgStage = kMgATile + kMgBTile;
@@ -1302,7 +1305,7 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
     extern __shared__ uint8_t dyn_raw[];
     __shared__ uint64_t full[kMgStages], empty[kMgStages];
     __shared__ uint64_t accfull[2], accempty[2], done;
-    __shared__ uint64_t wfull, wfree;  // the W_base block of a tile landed / the epilogue is done with it
+    __shared__ uint64_t wfull[kMgWBufs], wfree[kMgWBufs];  // a tile's W_base block landed / the epilogue is done with it
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort;
     uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
@@ -1319,13 +1322,15 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
             mbar_init(&accempty[b], 8);  // the eight epilogue warps
         }
         mbar_init(&done, 1);
-        mbar_init(&wfull, 1);
-        mbar_init(&wfree, 8);  // the eight epilogue warps
+        for (int b = 0; b < kMgWBufs; ++b) {
+            mbar_init(&wfull[b], 1);
+            mbar_init(&wfree[b], 8);  // the eight epilogue warps
+        }
         abort = 0;
         fence_mbarrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base, kMgTmemCols);
-    uint8_t* wtile = ring + static_cast<size_t>(kMgStages) * kMgStage;  // [4 boxes][128 rows][128 B]
+    uint8_t* wtiles = ring + static_cast<size_t>(kMgStages) * kMgStage;  // [kMgWBufs][4 boxes][128 rows][128 B]
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1344,20 +1349,23 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
         return true;
     };
     if (warp == 10) {
-        // ------------------------------------------------------------ W_base blocks, one tile at a time
+        // ------------------------------------------------------------ W_base blocks, two buffers
         if (lane == 0) {
             int j = 0;
             for (int tile = c0; tile < p.ntiles; tile += G, ++j) {
-                if (j > 0 && !wait(&wfree, static_cast<uint32_t>(j - 1) & 1u)) break;
+                const int wb = j % kMgWBufs;
+                // buffer wb is free once the epilogue is done with tile j - kMgWBufs
+                if (j >= kMgWBufs && !wait(&wfree[wb], static_cast<uint32_t>(j / kMgWBufs - 1) & 1u)) break;
                 const int rb = tile / p.ncb, cb = tile - rb * p.ncb;
-                mbar_arrive_expect_tx(&wfull, static_cast<uint32_t>(kMgWTile));
+                uint8_t* wt = wtiles + static_cast<size_t>(wb) * kMgWTile;
+                mbar_arrive_expect_tx(&wfull[wb], static_cast<uint32_t>(kMgWTile));
 #pragma unroll
                 for (int bx = 0; bx < kMgN / 64; ++bx)  // columns past d_in read the fill value, never stored
-                    tma_load_2d(wtile + bx * (kMgWTile / 4), &p.w_map, cb * kMgN + 64 * bx, rb * kMgM, &wfull);
+                    tma_load_2d(wt + bx * (kMgWTile / 4), &p.w_map, cb * kMgN + 64 * bx, rb * kMgM, &wfull[wb]);
             }
-            if (j > 0) {  // the last block lands before the CTA ends
+            for (int i = (j > kMgWBufs ? j - kMgWBufs : 0); i < j; ++i) {  // the last blocks land before the CTA ends
                 const uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(&wfull, static_cast<uint32_t>(j - 1) & 1u) &&
+                while (!mbar_try_wait(&wfull[i % kMgWBufs], static_cast<uint32_t>(i / kMgWBufs) & 1u) &&
                        global_timer_ns() - t0 < kWaitLimitNs) {
                 }
             }
@@ -1427,9 +1435,11 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
         int j = 0;
         for (int tile = c0; tile < p.ntiles; tile += G, ++j) {
             const int b = j & 1;
+            const int wb = j % kMgWBufs;
             if (!__all_sync(0xffffffffu, wait(&accfull[b], static_cast<uint32_t>(j / 2) & 1u) &&
-                                             wait(&wfull, static_cast<uint32_t>(j) & 1u)))
+                                             wait(&wfull[wb], static_cast<uint32_t>(j / kMgWBufs) & 1u)))
                 break;
+            const uint8_t* wtile = wtiles + static_cast<size_t>(wb) * kMgWTile;
             tc_fence_after();
             const int rb = tile / p.ncb, cb = tile - rb * p.ncb;
             const int64_t row = static_cast<int64_t>(rb) * kMgM + rl;
@@ -1468,9 +1478,10 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
                     } else {
                         uint32_t ob[4];
 #pragma unroll
-                        for (int u = 0; u < 4; ++u)
-                            ob[u] = static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o[2 * u]))) |
-                                    (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(o[2 * u + 1]))) << 16);
+                        for (int u = 0; u < 4; ++u) {
+                            const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * u], o[2 * u + 1]);
+                            ob[u] = *reinterpret_cast<const uint32_t*>(&h);
+                        }
                         *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * p.d_in + col + 8 * c) =
                             make_uint4(ob[0], ob[1], ob[2], ob[3]);
                     }
@@ -1481,7 +1492,7 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&accempty[b]);
-                mbar_arrive(&wfree);
+                mbar_arrive(&wfree[wb]);
             }
         }
     }
@@ -1562,7 +1573,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<0>), kTSmem, t0c);
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(tprod_kernel<1>), kTSmem, t1c);
     static std::atomic<size_t> mgc[kHostMaxDevices];
-    constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + kMgWTile + 1024;
+    constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + kMgWBufs * kMgWTile + 1024;
+    static_assert(kMgSmem <= 227 * 1024, "merge shared memory");
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(merge_tc_kernel), kMgSmem, mgc);
     if (e0 != cudaSuccess) return e0;
     const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
