@@ -79,7 +79,7 @@ NCU_TRAFFIC = {
                                                                       936_756_779 + 60_209_195),
     ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("af1cc86b53a1f516", "bd_monosoup.cu", 2_434_367_232 + 109_773_824),
+    (MONOSOUP_CALL, "monosoup"): ("bc0d131d4f9baba8", "bd_monosoup.cu", 2_434_450_688 + 108_814_592),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =

@@ -710,13 +710,16 @@ __device__ __forceinline__ void ff_add(float& s, float& c, float x, float y)
 // float-float into part[z][b][l * l] (entry i * l + j as (hi, lo)).  Only the
 // l (l + 1) / 2 entries i <= j are summed (ENT per thread, blockDim.x threads
 // of consecutive entries; ENT = 1 takes at most kGramThreads1 threads and
-// runs two CTAs per SM); each is stored at (i, j) and (j, i).
+// runs two CTAs per SM); each is stored at (i, j) and (j, i).  Rows come in
+// chunks of kGramRows (one chunk for the usual 8192-row operands over about
+// a hundred CTAs per checkpoint), l columns per row, coalesced.
 constexpr int kGramThreads1 = 576;
+constexpr int kGramRows = 96;
 template <int ENT>
 __global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT == 1 ? 2 : 1) gram_kernel(const float* __restrict__ a_all, int64_t n, int l,
                                                             float2* __restrict__ part_all)
 {
-    __shared__ float sa[32][kMaxL + 1];
+    __shared__ float sa[kGramRows][kMaxL + 1];
     const int tid = threadIdx.x, nt = blockDim.x;
     const float* a = a_all + static_cast<int64_t>(blockIdx.y) * n * l;
     float2* part = part_all + static_cast<int64_t>(blockIdx.y) * gridDim.x * l * l;
@@ -740,17 +743,16 @@ __global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT =
         pj[m] = u < np ? i + u : 0;
         s[m] = c[m] = 0.0f;
     }
-    for (int64_t r0 = b0; r0 < b1; r0 += 32) {
-        for (int e = tid; e < 32 * kMaxL; e += nt) {
-            const int rr = e >> 6, cc = e & 63;
+    for (int64_t r0 = b0; r0 < b1; r0 += kGramRows) {
+        const int nr = b1 - r0 < kGramRows ? static_cast<int>(b1 - r0) : kGramRows;
+        for (int e = tid; e < nr * l; e += nt) {
+            const int rr = e / l, cc = e - rr * l;
             const int64_t row = r0 + rr;
-            sa[rr][cc] = (row < b1 && cc < l &&
-                          bd_in(kBkMsGram, blockIdx.y * n * l + row * l + cc, static_cast<int64_t>(gridDim.y) * n * l))
+            sa[rr][cc] = bd_in(kBkMsGram, blockIdx.y * n * l + row * l + cc, static_cast<int64_t>(gridDim.y) * n * l)
                              ? a[row * l + cc]
                              : 0.0f;
         }
         __syncthreads();
-        const int nr = b1 - r0 < 32 ? static_cast<int>(b1 - r0) : 32;
         for (int rr = 0; rr < nr; ++rr) {
 #pragma unroll
             for (int m = 0; m < ENT; ++m) ff_madd(s[m], c[m], sa[rr][pi[m]], sa[rr][pj[m]]);
