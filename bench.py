@@ -68,9 +68,9 @@ DATA = "synthetic (seeded numpy / torch generators; shapes and distributions of 
 MONOSOUP_CALL = "bd_monosoup_merge (tensor-core products, Gram / Cholesky / Jacobi, tensor-core merge)"
 NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
-    ("skinny_kernel<1>", "decode"): ("12c3e9046774fa1a", "bd_skinny.cu", 499_377_365 + 259_541),
+    ("skinny_kernel<1>", "decode"): ("c133efac709bc60a", "bd_skinny.cu", 499_360_405 + 201_856),
     # 4 rows per CTA (kCompressRowsPerCta in bd_internal.h)
-    ("compress_kernel", "decode"): ("157f94bb54f54bb5", "bd_compress.cu", 939_564_117 + 6_540_587),
+    ("compress_kernel", "decode"): ("157f94bb54f54bb5", "bd_compress.cu", 939_588_267 + 6_411_563),
     ("prefill_kernel", "prefill"): ("384ee679f294ff5d", "bd_prefill.cu", 621_643_264 + 65_396_267),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
     ("multi_prepare + multi_kernel<8>", "multi"): ("a3057edfbaaadd8d", "bd_multi.cu", 255_719_211 + 114_603),
@@ -79,7 +79,7 @@ NCU_TRAFFIC = {
                                                                       936_756_779 + 60_209_195),
     ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("bc0d131d4f9baba8", "bd_monosoup.cu", 2_434_450_688 + 108_814_592),
+    (MONOSOUP_CALL, "monosoup"): ("bc0d131d4f9baba8", "bd_monosoup.cu", 2_434_325_248 + 109_545_728),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =
