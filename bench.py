@@ -79,7 +79,7 @@ NCU_TRAFFIC = {
                                                                       936_756_779 + 60_209_195),
     ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("bc0d131d4f9baba8", "bd_monosoup.cu", 2_434_325_248 + 109_545_728),
+    (MONOSOUP_CALL, "monosoup"): ("8aa774ab5fd362f8", "bd_monosoup.cu", 2_434_324_224 + 109_632_256),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =

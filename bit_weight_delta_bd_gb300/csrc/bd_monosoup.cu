@@ -36,6 +36,8 @@
 
 #include <atomic>
 
+#include <utility>
+
 #include "bd_device.cuh"
 #include "bd_tcgen05.cuh"
 #include "bd_tma.h"
@@ -119,6 +121,8 @@ struct ProdParams {
 template <int MODE, int L4>
 __global__ void __launch_bounds__(kPThreads, prod_ctas<L4>()) dprod_kernel(const __grid_constant__ ProdParams p)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     constexpr int LH = L4 / 2;                                // float4 output columns per warp
     constexpr int RPL = MODE == 0 ? (L4 <= 8 ? 2 : 1) : 2;  // Delta rows (columns) per lane
     constexpr int kOut = MODE == 0 ? 32 * RPL : kPTile;      // output rows of one CTA
@@ -387,6 +391,8 @@ __device__ __forceinline__ void split_pair(uint32_t wi, uint32_t wb, uint32_t& o
 __global__ void __launch_bounds__(256) split_small_kernel(const float* __restrict__ S, int64_t zstride, int64_t K,
                                                           int64_t Kp, int l, uint16_t* __restrict__ Sp)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     const int64_t g = static_cast<int64_t>(blockIdx.x) * 32 + (threadIdx.x & 31);
     if (8 * g >= Kp) return;
     const float* src = S + blockIdx.y * zstride;
@@ -482,6 +488,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     const uint32_t tmem = tmem_base;
     auto wait = [&](uint64_t* bar, uint32_t par) {
         if (mbar_try_wait(bar, par)) return true;
@@ -656,6 +664,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
 __global__ void __launch_bounds__(256) sum_slices_kernel(const float* __restrict__ part, int nslice, int64_t n,
                                                          float* __restrict__ out)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (e >= n) return;
     const float* pz = part + static_cast<int64_t>(blockIdx.y) * nslice * n;
@@ -719,6 +729,8 @@ template <int ENT>
 __global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT == 1 ? 2 : 1) gram_kernel(const float* __restrict__ a_all, int64_t n, int l,
                                                             float2* __restrict__ part_all)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     __shared__ float sa[kGramRows][kMaxL + 1];
     const int tid = threadIdx.x, nt = blockDim.x;
     const float* a = a_all + static_cast<int64_t>(blockIdx.y) * n * l;
@@ -782,6 +794,8 @@ __global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT =
 __global__ void __launch_bounds__(256) gram_sum_kernel(const float2* __restrict__ part_all, int nb, int l,
                                                        float2* __restrict__ G_all)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     const int e = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     const int ll = l * l;
@@ -857,6 +871,8 @@ __device__ __forceinline__ void ff_add_norm(float& h, float& l, float xh, float 
 // direction (its row of R and its reciprocal are zero).
 __global__ void __launch_bounds__(256) chol_kernel(const float2* __restrict__ G_all, int l, float* __restrict__ Rf_all)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     __shared__ float2 g[kMaxL][kMaxL + 1];
     __shared__ float rdiag[kMaxL];
     __shared__ int live[kMaxL];
@@ -959,6 +975,8 @@ constexpr int kJacobiVItems = kMaxL * (kMaxL / 2) / kJacobiThreads;        // V 
 __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __restrict__ G_all, int l, int r,
                                                                 float* __restrict__ ur_all)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     // one eigenproblem per CTA (checkpoint blockIdx.x)
     const float2* G = G_all + static_cast<size_t>(blockIdx.x) * l * l;
     float* ur = ur_all + static_cast<size_t>(blockIdx.x) * l * r;
@@ -1123,6 +1141,8 @@ constexpr int kTriStride = kMaxL + 4;  // floats per row of R^T in shared memory
 __global__ void __launch_bounds__(kTriThreads) tri_solve_kernel(float* a_all, int64_t n, int l,
                                                                 const float* __restrict__ Rf_all)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     float* a = a_all + static_cast<int64_t>(blockIdx.y) * n * l;
     const float* Rf = Rf_all + static_cast<int64_t>(blockIdx.y) * (kMaxL * kMaxL + kMaxL);
     const float* rinv = Rf + kMaxL * kMaxL;
@@ -1173,6 +1193,8 @@ __global__ void __launch_bounds__(kTriThreads) tri_solve_kernel(float* a_all, in
 __global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ src_all, int64_t n, int l,
                                                       const float* __restrict__ M_all, int m, float* __restrict__ dst_all)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     // checkpoint z = blockIdx.y: src_z [n][l], M_z [l][m], dst_z [m][n], each set consecutive
     const float* src = src_all + static_cast<int64_t>(blockIdx.y) * n * l;
     const float* M = M_all + static_cast<int64_t>(blockIdx.y) * l * m;
@@ -1259,6 +1281,8 @@ __device__ __forceinline__ int merge_piece(int p, int side)
 __global__ void __launch_bounds__(256) split_factors_kernel(const float* __restrict__ src, int64_t rows, int K, int Kp,
                                                             int side, uint16_t* __restrict__ dst)
 {
+    grid_launch_dependents();  // the next kernel of the merge may start launching
+    grid_dependency_wait();    // the previous kernel's results are visible
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t g = idx / rows, n = idx - g * rows;
     if (g >= Kp / 8) return;
@@ -1336,6 +1360,8 @@ __global__ void __launch_bounds__(kMgThreads, 1) merge_tc_kernel(const __grid_co
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    grid_launch_dependents();
+    grid_dependency_wait();    // the factors split by the previous kernels are visible
     const uint32_t tmem = tmem_base;
     auto wait = [&](uint64_t* bar, uint32_t par) {
         if (mbar_try_wait(bar, par)) return true;
@@ -1551,6 +1577,30 @@ MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
 
 unsigned blocks_for(int64_t n) { return static_cast<unsigned>((n + 255) / 256); }
 
+// Launches one kernel of the merge with programmatic dependent launch: it
+// may start launching while the previous kernel of the stream finishes (each
+// kernel lets its dependents launch at its start and waits for the previous
+// kernel's completion before touching device memory), so that the launch
+// latency of the merge's short kernels overlaps the kernel before them.  The
+// first error is kept in err and no later kernel is launched.
+template <typename... KArgs, typename... Args>
+void launch_dep(cudaError_t& err, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                Args&&... args)
+{
+    if (err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 }  // namespace
 
 int monosoup_max_l() { return kMaxL; }
@@ -1680,18 +1730,15 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         if (tc) {
             const int ns = slices(tr_blocks, a.d_in, nb, &per);
             const int64_t kp = (a.d_in + 63) / 64 * 64;
-            split_small_kernel<<<dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st>>>(
-                zs ? Zall + static_cast<size_t>(i0) * a.d_in * l : a.omega,
+            launch_dep(perr, split_small_kernel, dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st, zs ? Zall + static_cast<size_t>(i0) * a.d_in * l : a.omega,
                 zs ? static_cast<int64_t>(a.d_in) * l : 0, a.d_in, kp, l, Sp);
             if (!tprep(tp_sk, i0, nb, kp, Yp, per, kTM)) {
                 perr = cudaErrorInvalidValue;
                 return;
             }
             tp_sk.nz = nb;
-            tprod_kernel<0><<<dim3(static_cast<unsigned>(tr_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem,
-                              st>>>(tp_sk);
-            sum_slices_kernel<<<dim3(blocks_for(a.d_out * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
-                Yp, ns, a.d_out * l, Yall + static_cast<size_t>(i0) * a.d_out * l);
+            launch_dep(perr, tprod_kernel<0>, dim3(static_cast<unsigned>(tr_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem, st, tp_sk);
+            launch_dep(perr, sum_slices_kernel, dim3(blocks_for(a.d_out * l), static_cast<unsigned>(nb)), 256, 0, st, Yp, ns, a.d_out * l, Yall + static_cast<size_t>(i0) * a.d_out * l);
             return;
         }
         const int ns = slices(rblocks, a.d_in, nb, &per);
@@ -1704,11 +1751,10 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         }
         const dim3 g(static_cast<unsigned>(rblocks), static_cast<unsigned>(ns), static_cast<unsigned>(nb));
         if (l <= 32)
-            dprod_kernel<0, 8><<<g, kPThreads, dprod_smem<0, 8>(), st>>>(pp_sk);
+            launch_dep(perr, dprod_kernel<0, 8>, g, kPThreads, dprod_smem<0, 8>(), st, pp_sk);
         else
-            dprod_kernel<0, 16><<<g, kPThreads, dprod_smem<0, 16>(), st>>>(pp_sk);
-        sum_slices_kernel<<<dim3(blocks_for(a.d_out * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
-            Yp, ns, a.d_out * l, Yall + static_cast<size_t>(i0) * a.d_out * l);
+            launch_dep(perr, dprod_kernel<0, 16>, g, kPThreads, dprod_smem<0, 16>(), st, pp_sk);
+        launch_dep(perr, sum_slices_kernel, dim3(blocks_for(a.d_out * l), static_cast<unsigned>(nb)), 256, 0, st, Yp, ns, a.d_out * l, Yall + static_cast<size_t>(i0) * a.d_out * l);
     };
     // Z_z = Delta_z^T Y_z for the batch
     auto left = [&](int i0, int nb) {
@@ -1717,17 +1763,14 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         if (tc) {
             const int ns = slices(tc_blocks, a.d_out, nb, &per);
             const int64_t kp = (a.d_out + 63) / 64 * 64;
-            split_small_kernel<<<dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st>>>(
-                Yall + static_cast<size_t>(i0) * a.d_out * l, static_cast<int64_t>(a.d_out) * l, a.d_out, kp, l, Sp);
+            launch_dep(perr, split_small_kernel, dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st, Yall + static_cast<size_t>(i0) * a.d_out * l, static_cast<int64_t>(a.d_out) * l, a.d_out, kp, l, Sp);
             if (!tprep(tp_lf, i0, nb, kp, Zp, per, 64)) {
                 perr = cudaErrorInvalidValue;
                 return;
             }
             tp_lf.nz = nb;
-            tprod_kernel<1><<<dim3(static_cast<unsigned>(tc_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem,
-                              st>>>(tp_lf);
-            sum_slices_kernel<<<dim3(blocks_for(a.d_in * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
-                Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
+            launch_dep(perr, tprod_kernel<1>, dim3(static_cast<unsigned>(tc_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem, st, tp_lf);
+            launch_dep(perr, sum_slices_kernel, dim3(blocks_for(a.d_in * l), static_cast<unsigned>(nb)), 256, 0, st, Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
             return;
         }
         const int ns = slices(cblocks, a.d_out, nb, &per);
@@ -1738,11 +1781,10 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         }
         const dim3 g(static_cast<unsigned>(cblocks), static_cast<unsigned>(ns), static_cast<unsigned>(nb));
         if (l <= 32)
-            dprod_kernel<1, 8><<<g, kPThreads, dprod_smem<1, 8>(), st>>>(pp_lf);
+            launch_dep(perr, dprod_kernel<1, 8>, g, kPThreads, dprod_smem<1, 8>(), st, pp_lf);
         else
-            dprod_kernel<1, 16><<<g, kPThreads, dprod_smem<1, 16>(), st>>>(pp_lf);
-        sum_slices_kernel<<<dim3(blocks_for(a.d_in * l), static_cast<unsigned>(nb)), 256, 0, st>>>(
-            Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
+            launch_dep(perr, dprod_kernel<1, 16>, g, kPThreads, dprod_smem<1, 16>(), st, pp_lf);
+        launch_dep(perr, sum_slices_kernel, dim3(blocks_for(a.d_in * l), static_cast<unsigned>(nb)), 256, 0, st, Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
     };
     // out_z = A_z^T A_z for the nb consecutive A_z [n][l]
     // the upper triangle's l (l + 1) / 2 entries: one per thread up to
@@ -1754,12 +1796,12 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         const int gb = kGramParts / nb;
         const dim3 g(static_cast<unsigned>(gb), static_cast<unsigned>(nb));
         if (gent == 1)
-            gram_kernel<1><<<g, gthreads, 0, st>>>(A, n, l, part);
+            launch_dep(perr, gram_kernel<1>, g, gthreads, 0, st, A, n, l, part);
         else if (gent == 2)
-            gram_kernel<2><<<g, gthreads, 0, st>>>(A, n, l, part);
+            launch_dep(perr, gram_kernel<2>, g, gthreads, 0, st, A, n, l, part);
         else
-            gram_kernel<3><<<g, gthreads, 0, st>>>(A, n, l, part);
-        gram_sum_kernel<<<dim3(blocks_for(32 * ll), static_cast<unsigned>(nb)), 256, 0, st>>>(part, gb, l, out);
+            launch_dep(perr, gram_kernel<3>, g, gthreads, 0, st, A, n, l, part);
+        launch_dep(perr, gram_sum_kernel, dim3(blocks_for(32 * ll), static_cast<unsigned>(nb)), 256, 0, st, part, gb, l, out);
     };
     // A_z <- A_z R_z^-1 (CholeskyQR), `passes` times: two (CholeskyQR2) for
     // the Q that B is projected on, one for the intermediate bases of the
@@ -1767,9 +1809,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     auto orth = [&](float* A, int64_t n, int nb, int passes) {
         for (int pass = 0; pass < passes; ++pass) {
             gram(A, n, nb, G);
-            chol_kernel<<<static_cast<unsigned>(nb), 256, 0, st>>>(G, l, M);
-            tri_solve_kernel<<<dim3(static_cast<unsigned>((n + kTriThreads - 1) / kTriThreads), static_cast<unsigned>(nb)),
-                               kTriThreads, 0, st>>>(A, n, l, M);
+            launch_dep(perr, chol_kernel, static_cast<unsigned>(nb), 256, 0, st, G, l, M);
+            launch_dep(perr, tri_solve_kernel, dim3(static_cast<unsigned>((n + kTriThreads - 1) / kTriThreads), static_cast<unsigned>(nb)), kTriThreads, 0, st, A, n, l, M);
         }
     };
     if (r > 0) {
@@ -1789,11 +1830,11 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             gram(Z, a.d_in, nb, Gk + static_cast<size_t>(i0) * ll);  // B B^T
         }
         // the k projected eigenproblems at once, one CTA each
-        jacobi_kernel<<<static_cast<unsigned>(a.k), kJacobiThreads, 0, st>>>(Gk, l, r, Uk);  // U_r [l][r]
+        launch_dep(perr, jacobi_kernel, static_cast<unsigned>(a.k), kJacobiThreads, 0, st, Gk, l, r, Uk);  // U_r [l][r]
         const unsigned rq = static_cast<unsigned>((r + 3) / 4);
-        apply_t_kernel<<<dim3(blocks_for(a.d_out * rq), static_cast<unsigned>(a.k)), 256, 0, st>>>(Yall, a.d_out, l,
+        launch_dep(perr, apply_t_kernel, dim3(blocks_for(a.d_out * rq), static_cast<unsigned>(a.k)), 256, 0, st, Yall, a.d_out, l,
                                                                                                   Uk, r, L);
-        apply_t_kernel<<<dim3(blocks_for(a.d_in * rq), static_cast<unsigned>(a.k)), 256, 0, st>>>(Zall, a.d_in, l, Uk,
+        launch_dep(perr, apply_t_kernel, dim3(blocks_for(a.d_in * rq), static_cast<unsigned>(a.k)), 256, 0, st, Zall, a.d_in, l, Uk,
                                                                                                  r, Rt);
     }
     if (perr != cudaSuccess) return perr;
@@ -1804,8 +1845,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     uint16_t* Rs = reinterpret_cast<uint16_t*>(w + lay.rs);
     static thread_local MergeParams mp;
     if (K > 0) {
-        split_factors_kernel<<<blocks_for(a.d_out * (Kp / 8)), 256, 0, st>>>(L, a.d_out, K, Kp, 0, Ls);
-        split_factors_kernel<<<blocks_for(a.d_in * (Kp / 8)), 256, 0, st>>>(Rt, a.d_in, K, Kp, 1, Rs);
+        launch_dep(perr, split_factors_kernel, blocks_for(a.d_out * (Kp / 8)), 256, 0, st, L, a.d_out, K, Kp, 0, Ls);
+        launch_dep(perr, split_factors_kernel, blocks_for(a.d_in * (Kp / 8)), 256, 0, st, Rt, a.d_in, K, Kp, 1, Rs);
     }
     if (!encode_tma_2d(&mp.a_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ls, static_cast<uint64_t>(Kp),
                        static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(Kp) * 2, 64, kMgM,
@@ -1828,8 +1869,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     mp.ncb = static_cast<int>((a.d_in + kMgN - 1) / kMgN);
     mp.ntiles = mp.ncb * static_cast<int>((a.d_out + kMgM - 1) / kMgM);
     const int mg_grid = mp.ntiles < sms ? mp.ntiles : sms;  // persistent: one CTA per SM
-    merge_tc_kernel<<<mg_grid, kMgThreads, kMgSmem, st>>>(mp);
-    return cudaGetLastError();
+    launch_dep(perr, merge_tc_kernel, mg_grid, kMgThreads, kMgSmem, st, mp);
+    return perr != cudaSuccess ? perr : cudaGetLastError();
 }
 
 BD_BOUNDS_TAKE(bounds_take_monosoup)
