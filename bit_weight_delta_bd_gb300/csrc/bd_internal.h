@@ -5,6 +5,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <utility>
+
 #ifndef BD_NO_NVTX
 #include <nvtx3/nvToolsExt.h>
 #endif
@@ -12,6 +14,32 @@
 namespace bd {
 
 constexpr int kMaxVariants = 64;
+
+// Launches a kernel with programmatic dependent launch: it may start
+// launching while the previous kernel of the stream finishes.  The kernel
+// must wait for that kernel (griddepcontrol.wait) before it touches device
+// memory; kernels that also let their dependents launch at their start
+// (griddepcontrol.launch_dependents) overlap the launch latency of the next
+// kernel of a chain.  The first error is kept in err and no later kernel is
+// launched.
+template <typename... KArgs, typename... Args>
+void launch_dep(cudaError_t& err, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                Args&&... args)
+{
+    if (err != cudaSuccess) return;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 
 // An NVTX range around each compute entry point of the C ABI, named after
 // the entry point, so that a profiler's timeline (or ncu --nvtx-include)

@@ -36,8 +36,6 @@
 
 #include <atomic>
 
-#include <utility>
-
 #include "bd_device.cuh"
 #include "bd_tcgen05.cuh"
 #include "bd_tma.h"
@@ -1576,30 +1574,6 @@ MonoSoupWs ws_layout(int64_t d_out, int64_t d_in, int k, int r, int l)
 }
 
 unsigned blocks_for(int64_t n) { return static_cast<unsigned>((n + 255) / 256); }
-
-// Launches one kernel of the merge with programmatic dependent launch: it
-// may start launching while the previous kernel of the stream finishes (each
-// kernel lets its dependents launch at its start and waits for the previous
-// kernel's completion before touching device memory), so that the launch
-// latency of the merge's short kernels overlaps the kernel before them.  The
-// first error is kept in err and no later kernel is launched.
-template <typename... KArgs, typename... Args>
-void launch_dep(cudaError_t& err, void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
-                Args&&... args)
-{
-    if (err != cudaSuccess) return;
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
 
 }  // namespace
 

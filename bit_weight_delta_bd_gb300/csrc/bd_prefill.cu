@@ -191,6 +191,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1) prefill
     extern __shared__ uint8_t dyn_raw[];
     __shared__ PrefillShared sh;
     uint8_t* dyn = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
+    grid_dependency_wait();  // launched early (programmatic dependent launch): the previous kernel is done
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t rank = cluster_ctarank();  // 0: even CTA (rows 0..127 of the pair, issues the MMAs)
@@ -498,8 +499,9 @@ cudaError_t launch_prefill(const PrefillArgs& a, int /*sm_count*/, cudaStream_t 
     if (e != cudaSuccess) return e;
     const int64_t tiles = static_cast<int64_t>(prm.ntb) * row_pairs(a.d_out);
     const int64_t ncl = std::min<int64_t>(tiles, resident_clusters<PrefillParams>(smem));
-    prefill_kernel<PrefillParams><<<dim3(static_cast<unsigned>(2 * ncl)), kThreads, smem, stream>>>(prm);
-    return cudaGetLastError();
+    e = cudaSuccess;
+    launch_dep(e, prefill_kernel<PrefillParams>, dim3(static_cast<unsigned>(2 * ncl)), dim3(kThreads), smem, stream, prm);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 namespace {
@@ -509,6 +511,8 @@ namespace {
 // are marked invalid (their CTAs leave at once).
 __global__ void prefill_plan_kernel(const int32_t* __restrict__ seg_off, int V, int nblk, int4* __restrict__ plan)
 {
+    grid_launch_dependents();  // the gather may start launching
+    grid_dependency_wait();    // the router's seg_off is visible
     if (threadIdx.x != 0 || blockIdx.x != 0) return;
     int n = 0;
     for (int k = 0; k <= V; ++k) {
@@ -523,6 +527,8 @@ __global__ void prefill_plan_kernel(const int32_t* __restrict__ seg_off, int V, 
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm, int64_t d_in,
                                    uint16_t* __restrict__ xs)
 {
+    grid_launch_dependents();  // the prefill may start launching
+    grid_dependency_wait();    // the router's perm is visible (the plan kernel before this one waited for it)
     const int64_t i = blockIdx.x;  // grid = T rows
     if (!bd_in(kBkGather, perm[i], gridDim.x)) return;
     const uint4* src = reinterpret_cast<const uint4*>(x + static_cast<int64_t>(perm[i]) * d_in);
@@ -565,9 +571,10 @@ cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t str
     prm.perm = a.perm;
     const int nblk = grouped_prefill_blocks(a.T, a.V);
     prm.ntb = nblk;
-    prefill_plan_kernel<<<1, 32, 0, stream>>>(a.seg_off, a.V, nblk, a.plan);
-    gather_rows_kernel<<<static_cast<unsigned>(a.T), 256, 0, stream>>>(a.x, a.perm, a.d_in, a.xs);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaSuccess;
+    launch_dep(e, prefill_plan_kernel, dim3(1), dim3(32), 0, stream, a.seg_off, a.V, nblk, a.plan);
+    launch_dep(e, gather_rows_kernel, dim3(static_cast<unsigned>(a.T)), dim3(256), 0, stream, a.x, a.perm, a.d_in,
+               a.xs);
     if (e != cudaSuccess) return e;
     const size_t smem = static_cast<size_t>(kStages) * kStageBytes + 1024;
     static std::atomic<size_t> smem_set[kHostMaxDevices];
@@ -575,8 +582,9 @@ cudaError_t launch_prefill_grouped(const GroupedPrefillArgs& a, cudaStream_t str
     if (e != cudaSuccess) return e;
     const int64_t tiles = static_cast<int64_t>(nblk) * row_pairs(a.d_out);
     const int64_t ncl = std::min<int64_t>(tiles, resident_clusters<GroupedPrefillParams>(smem));
-    prefill_kernel<GroupedPrefillParams><<<dim3(static_cast<unsigned>(2 * ncl)), kThreads, smem, stream>>>(prm);
-    return cudaGetLastError();
+    launch_dep(e, prefill_kernel<GroupedPrefillParams>, dim3(static_cast<unsigned>(2 * ncl)), dim3(kThreads), smem,
+               stream, prm);
+    return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 BD_BOUNDS_TAKE(bounds_take_prefill)

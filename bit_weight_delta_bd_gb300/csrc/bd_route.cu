@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(kRouteThreads)
     __shared__ int warp_cnt[kRouteWarps][kKeys];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int n_keys = V + 1;
+    grid_launch_dependents();  // a kernel launched after this one with programmatic dependent launch may start
 
     for (int k = tid; k < kKeys; k += kRouteThreads) total[k] = 0;
     __syncthreads();
