@@ -71,12 +71,12 @@ NCU_TRAFFIC = {
     ("skinny_kernel<1>", "decode"): ("c133efac709bc60a", "bd_skinny.cu", 499_360_405 + 201_856),
     # 4 rows per CTA (kCompressRowsPerCta in bd_internal.h)
     ("compress_kernel", "decode"): ("157f94bb54f54bb5", "bd_compress.cu", 939_588_267 + 6_411_563),
-    ("prefill_kernel", "prefill"): ("384ee679f294ff5d", "bd_prefill.cu", 621_643_264 + 65_396_267),
+    ("prefill_kernel", "prefill"): ("4c65a422a15ad932", "bd_prefill.cu", 619_373_995 + 65_847_595),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
     ("multi_prepare + multi_kernel<8>", "multi"): ("a3057edfbaaadd8d", "bd_multi.cu", 255_719_211 + 114_603),
     # the grouped prefill_kernel only (router, plan and gather add about 134 MB of x copies)
-    ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("384ee679f294ff5d", "bd_prefill.cu",
-                                                                      936_756_779 + 60_209_195),
+    ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("4c65a422a15ad932", "bd_prefill.cu",
+                                                                      939_384_576 + 60_230_955),
     ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
     (MONOSOUP_CALL, "monosoup"): ("8aa774ab5fd362f8", "bd_monosoup.cu", 2_434_324_224 + 109_632_256),
