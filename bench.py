@@ -79,7 +79,7 @@ NCU_TRAFFIC = {
                                                                       939_384_576 + 60_230_955),
     ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
     # all 36 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("8aa774ab5fd362f8", "bd_monosoup.cu", 2_434_324_224 + 109_632_256),
+    (MONOSOUP_CALL, "monosoup"): ("d1793d678b04b918", "bd_monosoup.cu", 2_434_406_144 + 110_101_760),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =
