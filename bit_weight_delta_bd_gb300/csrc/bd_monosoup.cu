@@ -83,7 +83,8 @@ __device__ __forceinline__ void ffma2(float2& acc, float a, float mx, float my)
 //     (conflict-free), the small operand as broadcasts (every lane of a warp
 //     reads the same row).
 // The warps' partial sums are added in warp order at the end and written as
-// one of gridDim.y partial results (summed in order by sum_slices_kernel).
+// one of gridDim.y partial results (summed in slice order by the next Gram
+// pass, gram_kernel with nslice > 1).
 
 constexpr int kPWarps = 8;       // FMA warps per product CTA
 constexpr int kPTile = 64;       // Delta tile per stage: 64 x 64
@@ -657,25 +658,6 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
     }
 }
 
-// out[z][e] = sum_s part[z][s][e], e < n, for the gridDim.y checkpoints z
-// (fixed order).
-__global__ void __launch_bounds__(256) sum_slices_kernel(const float* __restrict__ part, int nslice, int64_t n,
-                                                         float* __restrict__ out)
-{
-    grid_launch_dependents();  // the next kernel of the merge may start launching
-    grid_dependency_wait();    // the previous kernel's results are visible
-    const int64_t e = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (e >= n) return;
-    const float* pz = part + static_cast<int64_t>(blockIdx.y) * nslice * n;
-    const int64_t np = static_cast<int64_t>(gridDim.y) * nslice * n;
-    const int64_t zb = static_cast<int64_t>(blockIdx.y) * nslice * n;
-    float s = bd_in(kBkMsSlices, zb + e, np) ? pz[e] : 0.0f;
-    for (int k = 1; k < nslice; ++k)
-        if (bd_in(kBkMsSlices, zb + k * n + e, np)) s += pz[k * n + e];
-    if (bd_in(kBkMsSlices, static_cast<int64_t>(blockIdx.y) * n + e, static_cast<int64_t>(gridDim.y) * n))
-        out[static_cast<int64_t>(blockIdx.y) * n + e] = s;
-}
-
 // ---------------------------------------------------------------- small-matrix steps
 // GB300 has few fp64 units (about 2 fp64 FMAs per cycle per SM, with long
 // latencies), so the Gram matrices and their Cholesky factors are computed in
@@ -720,18 +702,23 @@ __device__ __forceinline__ void ff_add(float& s, float& c, float x, float y)
 // of consecutive entries; ENT = 1 takes at most kGramThreads1 threads and
 // runs two CTAs per SM); each is stored at (i, j) and (j, i).  Rows come in
 // chunks of kGramRows (one chunk for the usual 8192-row operands over about
-// a hundred CTAs per checkpoint), l columns per row, coalesced.
+// a hundred CTAs per checkpoint), l columns per row, coalesced.  With
+// nslice > 1 the operand is the sum of a product's K slices (slice s of
+// checkpoint z at a_all + (z nslice + s) n l, added in slice order) and the
+// kernel also writes that sum to sum_all[z][n][l]: the CTAs' row ranges cover
+// every row once, so no separate pass sums the slices.
 constexpr int kGramThreads1 = 576;
 constexpr int kGramRows = 96;
 template <int ENT>
-__global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT == 1 ? 2 : 1) gram_kernel(const float* __restrict__ a_all, int64_t n, int l,
-                                                            float2* __restrict__ part_all)
+__global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT == 1 ? 2 : 1)
+    gram_kernel(const float* __restrict__ a_all, int nslice, int64_t n, int l, float2* __restrict__ part_all,
+                float* __restrict__ sum_all)
 {
     grid_launch_dependents();  // the next kernel of the merge may start launching
     grid_dependency_wait();    // the previous kernel's results are visible
     __shared__ float sa[kGramRows][kMaxL + 1];
     const int tid = threadIdx.x, nt = blockDim.x;
-    const float* a = a_all + static_cast<int64_t>(blockIdx.y) * n * l;
+    const float* a = a_all + static_cast<int64_t>(blockIdx.y) * nslice * n * l;
     float2* part = part_all + static_cast<int64_t>(blockIdx.y) * gridDim.x * l * l;
     const int64_t per = (n + gridDim.x - 1) / gridDim.x;
     const int64_t b0 = static_cast<int64_t>(blockIdx.x) * per;
@@ -758,9 +745,14 @@ __global__ void __launch_bounds__(ENT == 1 ? kGramThreads1 : kGramThreads, ENT =
         for (int e = tid; e < nr * l; e += nt) {
             const int rr = e / l, cc = e - rr * l;
             const int64_t row = r0 + rr;
-            sa[rr][cc] = bd_in(kBkMsGram, blockIdx.y * n * l + row * l + cc, static_cast<int64_t>(gridDim.y) * n * l)
-                             ? a[row * l + cc]
-                             : 0.0f;
+            const int64_t ext = static_cast<int64_t>(gridDim.y) * nslice * n * l;
+            const int64_t at = static_cast<int64_t>(blockIdx.y) * nslice * n * l + row * l + cc;
+            float v = bd_in(kBkMsGram, at, ext) ? a[row * l + cc] : 0.0f;
+            for (int sl = 1; sl < nslice; ++sl)
+                if (bd_in(kBkMsGram, at + sl * n * l, ext)) v += a[sl * n * l + row * l + cc];
+            sa[rr][cc] = v;
+            if (sum_all && bd_in(kBkMsGram, blockIdx.y * n * l + row * l + cc, static_cast<int64_t>(gridDim.y) * n * l))
+                sum_all[static_cast<int64_t>(blockIdx.y) * n * l + row * l + cc] = v;
         }
         __syncthreads();
         for (int rr = 0; rr < nr; ++rr) {
@@ -1696,6 +1688,12 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         pr.k_per = per;
         return true;
     };
+    // a product's output still in K slices, summed by the next Gram pass over dst
+    struct PendingSlices {
+        const float* src = nullptr;
+        int ns = 1;
+        float* dst = nullptr;
+    } pend;
     const int64_t tr_blocks = (a.d_out + kTM - 1) / kTM, tc_blocks = a.d_in / kTM;
     // Y_z = Delta_z S_z for the batch (S_z = Omega, or Z_z with zs)
     auto sketch = [&](int i0, int nb, bool zs) {
@@ -1712,7 +1710,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             }
             tp_sk.nz = nb;
             launch_dep(perr, tprod_kernel<0>, dim3(static_cast<unsigned>(tr_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem, st, tp_sk);
-            launch_dep(perr, sum_slices_kernel, dim3(blocks_for(a.d_out * l), static_cast<unsigned>(nb)), 256, 0, st, Yp, ns, a.d_out * l, Yall + static_cast<size_t>(i0) * a.d_out * l);
+            pend = {Yp, ns, Yall + static_cast<size_t>(i0) * a.d_out * l};  // summed by the next Gram pass
             return;
         }
         const int ns = slices(rblocks, a.d_in, nb, &per);
@@ -1728,7 +1726,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             launch_dep(perr, dprod_kernel<0, 8>, g, kPThreads, dprod_smem<0, 8>(), st, pp_sk);
         else
             launch_dep(perr, dprod_kernel<0, 16>, g, kPThreads, dprod_smem<0, 16>(), st, pp_sk);
-        launch_dep(perr, sum_slices_kernel, dim3(blocks_for(a.d_out * l), static_cast<unsigned>(nb)), 256, 0, st, Yp, ns, a.d_out * l, Yall + static_cast<size_t>(i0) * a.d_out * l);
+        pend = {Yp, ns, Yall + static_cast<size_t>(i0) * a.d_out * l};
     };
     // Z_z = Delta_z^T Y_z for the batch
     auto left = [&](int i0, int nb) {
@@ -1744,7 +1742,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             }
             tp_lf.nz = nb;
             launch_dep(perr, tprod_kernel<1>, dim3(static_cast<unsigned>(tc_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem, st, tp_lf);
-            launch_dep(perr, sum_slices_kernel, dim3(blocks_for(a.d_in * l), static_cast<unsigned>(nb)), 256, 0, st, Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
+            pend = {Zp, ns, Zall + static_cast<size_t>(i0) * a.d_in * l};
             return;
         }
         const int ns = slices(cblocks, a.d_out, nb, &per);
@@ -1758,7 +1756,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             launch_dep(perr, dprod_kernel<1, 8>, g, kPThreads, dprod_smem<1, 8>(), st, pp_lf);
         else
             launch_dep(perr, dprod_kernel<1, 16>, g, kPThreads, dprod_smem<1, 16>(), st, pp_lf);
-        launch_dep(perr, sum_slices_kernel, dim3(blocks_for(a.d_in * l), static_cast<unsigned>(nb)), 256, 0, st, Zp, ns, a.d_in * l, Zall + static_cast<size_t>(i0) * a.d_in * l);
+        pend = {Zp, ns, Zall + static_cast<size_t>(i0) * a.d_in * l};
     };
     // out_z = A_z^T A_z for the nb consecutive A_z [n][l]
     // the upper triangle's l (l + 1) / 2 entries: one per thread up to
@@ -1766,15 +1764,26 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     const int npairs = l * (l + 1) / 2;
     const int gent = npairs <= kGramThreads1 ? 1 : (npairs <= 2 * kGramThreads ? 2 : 3);
     const int gthreads = ((npairs + gent - 1) / gent + 31) / 32 * 32;
-    auto gram = [&](const float* A, int64_t n, int nb, float2* out) {
+    // (a product's output still in K slices is summed by its first Gram pass,
+    // which writes the sum to A)
+    auto gram = [&](float* A, int64_t n, int nb, float2* out) {
         const int gb = kGramParts / nb;
         const dim3 g(static_cast<unsigned>(gb), static_cast<unsigned>(nb));
+        const float* src = A;
+        int nsl = 1;
+        float* sum = nullptr;
+        if (pend.dst == A) {
+            src = pend.src;
+            nsl = pend.ns;
+            sum = A;
+            pend = {};
+        }
         if (gent == 1)
-            launch_dep(perr, gram_kernel<1>, g, gthreads, 0, st, A, n, l, part);
+            launch_dep(perr, gram_kernel<1>, g, gthreads, 0, st, src, nsl, n, l, part, sum);
         else if (gent == 2)
-            launch_dep(perr, gram_kernel<2>, g, gthreads, 0, st, A, n, l, part);
+            launch_dep(perr, gram_kernel<2>, g, gthreads, 0, st, src, nsl, n, l, part, sum);
         else
-            launch_dep(perr, gram_kernel<3>, g, gthreads, 0, st, A, n, l, part);
+            launch_dep(perr, gram_kernel<3>, g, gthreads, 0, st, src, nsl, n, l, part, sum);
         launch_dep(perr, gram_sum_kernel, dim3(blocks_for(32 * ll), static_cast<unsigned>(nb)), 256, 0, st, part, gb, l, out);
     };
     // A_z <- A_z R_z^-1 (CholeskyQR), `passes` times: two (CholeskyQR2) for
