@@ -78,13 +78,13 @@ NCU_TRAFFIC = {
     ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("4c65a422a15ad932", "bd_prefill.cu",
                                                                       939_384_576 + 60_230_955),
     ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
-    # all 32 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("3d3b5707b1fd4e6a", "bd_monosoup.cu", 2_421_907_200 + 110_191_616),
+    # all 29 launches of one merge (launch list with DRAM counters, one pass)
+    (MONOSOUP_CALL, "monosoup"): ("1d99e21301cc8b03", "bd_monosoup.cu", 2_412_529_152 + 109_030_656),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =
 # router + plan + gather + grouped prefill; monosoup = the merge's launches
-LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4, "monosoup": 32}
+LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4, "monosoup": 29}
 # workloads whose own figure is tensor throughput (TFLOP/s) rather than GB/s
 TENSOR_WORKLOADS = ("prefill", "multi_prefill")
 # the arithmetic type each workload computes in (the MonoSoup products and

@@ -1124,12 +1124,17 @@ __global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __
 // R[m][j]) / R[j][j] (the sum in order m = 0, 1, ...), a dropped direction
 // giving x_j = 0; one row per thread (16-byte row loads and stores), R
 // staged transposed so that four coefficients of column j come with one
-// 16-byte broadcast load.
+// 16-byte broadcast load.  With sp_all (l <= 32, the last CholeskyQR pass
+// before a tensor-core product) the kernel also writes the small operand's
+// bf16 pieces as split_small_kernel does, Sp[z][32 b + c][row] for every
+// row < kp (zero past n and for c >= l), so that pass needs no split
+// launch.
 constexpr int kTriThreads = 128;
 constexpr int kTriStride = kMaxL + 4;  // floats per row of R^T in shared memory (16-byte multiple)
 
 __global__ void __launch_bounds__(kTriThreads) tri_solve_kernel(float* a_all, int64_t n, int l,
-                                                                const float* __restrict__ Rf_all)
+                                                                const float* __restrict__ Rf_all,
+                                                                uint16_t* __restrict__ sp_all, int64_t kp)
 {
     grid_launch_dependents();  // the next kernel of the merge may start launching
     grid_dependency_wait();    // the previous kernel's results are visible
@@ -1145,13 +1150,14 @@ __global__ void __launch_bounds__(kTriThreads) tri_solve_kernel(float* a_all, in
     for (int i = threadIdx.x; i < kMaxL; i += blockDim.x) sd[i] = i < l ? rinv[i] : 0.0f;
     __syncthreads();
     const int64_t row = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (row >= n) return;
-    if (!bd_in_range(kBkMsTri, blockIdx.y * n * l + row * l, l, static_cast<int64_t>(gridDim.y) * n * l)) return;
+    const bool live = row < n &&
+                      bd_in_range(kBkMsTri, blockIdx.y * n * l + row * l, l, static_cast<int64_t>(gridDim.y) * n * l);
+    if (!live && (sp_all == nullptr || row >= kp)) return;
     float x[kMaxL];
     float4* ar = reinterpret_cast<float4*>(a + row * l);  // l is a multiple of 4
 #pragma unroll
     for (int j4 = 0; j4 < kMaxL / 4; ++j4) {
-        const float4 v = 4 * j4 < l ? ar[j4] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        const float4 v = live && 4 * j4 < l ? ar[j4] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
         x[4 * j4] = v.x;
         x[4 * j4 + 1] = v.y;
         x[4 * j4 + 2] = v.z;
@@ -1171,9 +1177,30 @@ __global__ void __launch_bounds__(kTriThreads) tri_solve_kernel(float* a_all, in
         }
         x[j] = s * sd[j];
     }
+    if (live) {
 #pragma unroll
-    for (int j4 = 0; j4 < kMaxL / 4; ++j4)
-        if (4 * j4 < l) ar[j4] = make_float4(x[4 * j4], x[4 * j4 + 1], x[4 * j4 + 2], x[4 * j4 + 3]);
+        for (int j4 = 0; j4 < kMaxL / 4; ++j4)
+            if (4 * j4 < l) ar[j4] = make_float4(x[4 * j4], x[4 * j4 + 1], x[4 * j4 + 2], x[4 * j4 + 3]);
+    }
+    if (sp_all != nullptr && row < kp) {
+        // the three bf16 pieces of each x_c (c < 32; zero for c >= l and past n)
+        uint16_t* o = sp_all + static_cast<int64_t>(blockIdx.y) * 128 * kp + row;
+        const int64_t ne = static_cast<int64_t>(gridDim.y) * 128 * kp;
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+            const float v = c < l ? x[c] : 0.0f;
+            const uint32_t b1 = __float_as_uint(v) & 0xFFFF0000u;
+            const float r1 = __fsub_rn(v, __uint_as_float(b1));
+            const uint32_t b2 = __float_as_uint(r1) & 0xFFFF0000u;
+            const float r2 = __fsub_rn(r1, __uint_as_float(b2));
+            const int64_t base = static_cast<int64_t>(blockIdx.y) * 128 * kp + row;
+            if (bd_in(kBkMsTri, base + static_cast<int64_t>(64 + c) * kp, ne)) {
+                o[static_cast<int64_t>(c) * kp] = static_cast<uint16_t>(b1 >> 16);
+                o[static_cast<int64_t>(32 + c) * kp] = static_cast<uint16_t>(b2 >> 16);
+                o[static_cast<int64_t>(64 + c) * kp] = static_cast<uint16_t>(__float_as_uint(r2) >> 16);
+            }
+        }
+    }
 }
 
 // dst[j][row] = sum_c src[row][c] * M[c][j]  (c < l, j < m), written
@@ -1694,6 +1721,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         int ns = 1;
         float* dst = nullptr;
     } pend;
+    bool sp_ready = false;  // the last CholeskyQR pass wrote the next product's split operand
     const int64_t tr_blocks = (a.d_out + kTM - 1) / kTM, tc_blocks = a.d_in / kTM;
     // Y_z = Delta_z S_z for the batch (S_z = Omega, or Z_z with zs)
     auto sketch = [&](int i0, int nb, bool zs) {
@@ -1702,7 +1730,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         if (tc) {
             const int ns = slices(tr_blocks, a.d_in, nb, &per);
             const int64_t kp = (a.d_in + 63) / 64 * 64;
-            launch_dep(perr, split_small_kernel, dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st, zs ? Zall + static_cast<size_t>(i0) * a.d_in * l : a.omega,
+            if (!zs || !sp_ready)  // after a CholeskyQR pass the split is already written
+                launch_dep(perr, split_small_kernel, dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st, zs ? Zall + static_cast<size_t>(i0) * a.d_in * l : a.omega,
                 zs ? static_cast<int64_t>(a.d_in) * l : 0, a.d_in, kp, l, Sp);
             if (!tprep(tp_sk, i0, nb, kp, Yp, per, kTM)) {
                 perr = cudaErrorInvalidValue;
@@ -1711,6 +1740,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             tp_sk.nz = nb;
             launch_dep(perr, tprod_kernel<0>, dim3(static_cast<unsigned>(tr_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem, st, tp_sk);
             pend = {Yp, ns, Yall + static_cast<size_t>(i0) * a.d_out * l};  // summed by the next Gram pass
+            sp_ready = false;
             return;
         }
         const int ns = slices(rblocks, a.d_in, nb, &per);
@@ -1735,7 +1765,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         if (tc) {
             const int ns = slices(tc_blocks, a.d_out, nb, &per);
             const int64_t kp = (a.d_out + 63) / 64 * 64;
-            launch_dep(perr, split_small_kernel, dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st, Yall + static_cast<size_t>(i0) * a.d_out * l, static_cast<int64_t>(a.d_out) * l, a.d_out, kp, l, Sp);
+            if (!sp_ready)  // after a CholeskyQR pass the split is already written
+                launch_dep(perr, split_small_kernel, dim3(static_cast<unsigned>((kp / 8 + 31) / 32), static_cast<unsigned>(nb)), 256, 0, st, Yall + static_cast<size_t>(i0) * a.d_out * l, static_cast<int64_t>(a.d_out) * l, a.d_out, kp, l, Sp);
             if (!tprep(tp_lf, i0, nb, kp, Zp, per, 64)) {
                 perr = cudaErrorInvalidValue;
                 return;
@@ -1743,6 +1774,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             tp_lf.nz = nb;
             launch_dep(perr, tprod_kernel<1>, dim3(static_cast<unsigned>(tc_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem, st, tp_lf);
             pend = {Zp, ns, Zall + static_cast<size_t>(i0) * a.d_in * l};
+            sp_ready = false;
             return;
         }
         const int ns = slices(cblocks, a.d_out, nb, &per);
@@ -1789,11 +1821,16 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     // A_z <- A_z R_z^-1 (CholeskyQR), `passes` times: two (CholeskyQR2) for
     // the Q that B is projected on, one for the intermediate bases of the
     // power iterations, where only the spanned subspace matters
+    // (on the tensor-core path the last pass also writes the split small
+    // operand of the product that follows it)
     auto orth = [&](float* A, int64_t n, int nb, int passes) {
         for (int pass = 0; pass < passes; ++pass) {
             gram(A, n, nb, G);
             launch_dep(perr, chol_kernel, static_cast<unsigned>(nb), 256, 0, st, G, l, M);
-            launch_dep(perr, tri_solve_kernel, dim3(static_cast<unsigned>((n + kTriThreads - 1) / kTriThreads), static_cast<unsigned>(nb)), kTriThreads, 0, st, A, n, l, M);
+            const bool split = tc && pass + 1 == passes;
+            const int64_t kp = (n + 63) / 64 * 64, rows = split ? kp : n;
+            launch_dep(perr, tri_solve_kernel, dim3(static_cast<unsigned>((rows + kTriThreads - 1) / kTriThreads), static_cast<unsigned>(nb)), kTriThreads, 0, st, A, n, l, static_cast<const float*>(M), split ? Sp : nullptr, kp);
+            sp_ready = split;
         }
     };
     if (r > 0) {
