@@ -65,7 +65,7 @@ DATA = "synthetic (seeded numpy / torch generators; shapes and distributions of 
 # ignored once that source has changed.  Summaries of the captures are in profiles/.  An entry whose value
 # is a float is a ratio (traffic / algorithmic bytes) taken on one launch of a
 # smaller call of the same kernel and applied to the average launch.
-MONOSOUP_CALL = "bd_monosoup_merge (tensor-core products, Gram / Cholesky / Jacobi, tensor-core merge)"
+MONOSOUP_CALL = "bd_monosoup_merge (tensor-core products, Gram / Cholesky / tridiagonal eigensolver, tensor-core merge)"
 NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
     ("skinny_kernel<1>", "decode"): ("c133efac709bc60a", "bd_skinny.cu", 499_360_405 + 201_856),
@@ -79,7 +79,7 @@ NCU_TRAFFIC = {
                                                                       939_384_576 + 60_230_955),
     ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
     # all 29 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("1d99e21301cc8b03", "bd_monosoup.cu", 2_412_529_152 + 109_030_656),
+    (MONOSOUP_CALL, "monosoup"): ("576ad9203fc86dca", "bd_monosoup.cu", 2_412_697_088 + 109_862_912),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =

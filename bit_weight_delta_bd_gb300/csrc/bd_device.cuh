@@ -36,7 +36,7 @@ __device__ __forceinline__ void raise_error(uint32_t* err, uint32_t bits)
 enum BoundsKernel : uint32_t {
     kBkCompress = 0, kBkAlphaFinalize, kBkReconstruct, kBkSkinny, kBkMultiPrepare, kBkMulti, kBkPrefill,
     kBkPrefillPlan, kBkGather, kBkRoute, kBkMaterialize, kBkMsProd, kBkMsSplit, kBkMsSlices, kBkMsGram,
-    kBkMsGramSum, kBkMsChol, kBkMsJacobi, kBkMsTri, kBkMsApply, kBkMsMerge
+    kBkMsGramSum, kBkMsChol, kBkMsEig, kBkMsTri, kBkMsApply, kBkMsMerge
 };
 #ifdef BD_DEBUG_BOUNDS
 namespace {

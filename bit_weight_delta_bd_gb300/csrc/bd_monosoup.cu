@@ -10,7 +10,8 @@
 //   Y = Delta * Omega          (Omega [d_in][l], Gaussian, given by the caller)
 //   Q = orth(Y); q times: Z = orth(Delta^T Q), Q = orth(Delta Z)
 //   B^T = Delta^T Q            ([d_in][l])
-//   B B^T = U_B Lambda U_B^T   (l x l symmetric eigenproblem, Jacobi)
+//   B B^T = U_B Lambda U_B^T   (l x l symmetric eigenproblem: tridiagonalisation,
+//                               bisection, inverse iteration)
 //   tau = (Q U_r) (U_r^T B)    (U_r: the r leading eigenvectors)
 // which is U_r S_r V_r^T of the rank-l approximation Q Q^T Delta.  Every pass
 // over Delta reads W_i and W_base (bf16) and forms Delta in fp32 on the fly.
@@ -28,7 +29,9 @@
 // Gram matrices and Cholesky factors are float-float on the fp32 units, the
 // eigenproblem fp32.  Up to kMaxBatch checkpoints go through every step
 // together (one launch per step, the checkpoint in a grid dimension).  No
-// kernel waits on another CTA; the passes are plain stream-ordered launches.
+// kernel waits on another CTA; the passes are stream-ordered launches, each
+// allowed to start launching while the kernel before it finishes
+// (programmatic dependent launch).
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -935,187 +938,288 @@ __global__ void __launch_bounds__(256) chol_kernel(const float2* __restrict__ G_
         if (bd_in(kBkMsChol, i, kMaxL)) rinv[i] = live[i] ? rdiag[i] : 0.0f;
 }
 
-// One CTA of 256 threads per checkpoint: the symmetric eigenproblem of G by
-// cyclic Jacobi in fp32 with the round-robin pair order (n/2 disjoint
-// rotations per round, n = l rounded up to even, index l a dummy when l is
-// odd).  A pair is rotated only when |a_pq| exceeds both 2^-22
-// sqrt(|a_pp| |a_qq|) and 2^-24 of the largest initial diagonal entry (below
-// either, the rotation would move nothing above fp32 rounding: the relative
-// threshold rule of Demmel and Veselic, "Jacobi's method is more accurate
-// than QR", 1992, with an absolute floor for the null space of a
-// rank-deficient sketch); the iteration stops after a sweep without a
-// rotation (at most 40 sweeps).  The rotation of a pair: theta = (a_qq -
-// a_pp) / (2 a_pq), t = sign(theta) / (|theta| + sqrt(theta^2 + 1)) (from the
-// approximate reciprocal and reciprocal square root: an angle off by about
-// 2^-21 only leaves a residue of that size of a_pq), c = 1 / sqrt(1 + t^2)
-// (rsqrt and one Newton step, so that c^2 + s^2 = 1 to fp32 accuracy),
-// s = t c; a_pq becomes exactly 0 and the diagonal moves by -/+ t a_pq.  The
-// parameters of a round's pairs sit in one float4 each (c, s, t, p | q << 8)
-// so that an update reads them with one load.  A round is A <- P^T A P and
-// V <- V P for the rotations P of its n/2 pairs: every 2 x 2 block of A at
-// (row pair, column pair) and every (row, column pair) of V is updated in
-// place by one thread, so a round needs two barriers.  ur[i][m] = the
-// eigenvector of the m-th largest eigenvalue, m < r, normalised.  Only the r
-// leading eigenvectors are used, and they are set apart by the spectral gap,
-// so fp32 costs about 1e-6 of them.
-constexpr int kJacobiThreads = 256;
-constexpr int kJacobiBlocks = (kMaxL / 2) * (kMaxL / 2) / kJacobiThreads;  // 2 x 2 blocks per thread
-constexpr int kJacobiVItems = kMaxL * (kMaxL / 2) / kJacobiThreads;        // V items per thread
+// The r leading eigenvectors of the symmetric l x l matrix G of each
+// checkpoint (one CTA of 256 threads per checkpoint, fp32; G arrives as
+// float-float pairs and is rounded to fp32):
+//   1. Householder tridiagonalisation Q^T G Q = T (reflector k, for
+//      k < l - 2, zeroes column k below the subdiagonal; its vector and 2 /
+//      (v^T v) are kept for step 4): per reflector one warp forms it, the CTA
+//      forms p = tau S v, w = p - (tau v^T p / 2) v and the rank-2 update of
+//      the trailing block S -= v w^T + w v^T;
+//   2. a half-warp finds the m-th largest eigenvalue of T (m < r) by
+//      multisection of the Gershgorin interval on the Sturm count (the number
+//      of negative pivots of T - x I): 16 points per round, at most 12 rounds
+//      or until the interval is two ulps wide;
+//   3. thread m then takes two steps of inverse iteration with T - lambda_m I
+//      (tridiagonal elimination, tiny pivots replaced by a floor) from a fixed
+//      start vector, and one warp orthonormalises the r vectors in order of
+//      decreasing eigenvalue (Gram-Schmidt, twice, within clusters of close
+//      eigenvalues), which keeps the vectors of close eigenvalues apart;
+//   4. each vector is carried back to G's basis by the reflectors in reverse
+//      order (one warp per vector, no barrier).
+// ur[i][m] = entry i of the unit eigenvector of the m-th largest eigenvalue,
+// m < r.  Standard dense symmetric eigensolver steps (Householder
+// tridiagonalisation, Sturm bisection, inverse iteration), as in Golub and
+// Van Loan, "Matrix Computations", sections 8.3-8.4.
+constexpr int kEigThreads = 256;
+constexpr int kEigLd = kMaxL + 1;  // row stride of A and of the vectors
+constexpr int kEigLuLd = 2 * kMaxL + 1;  // row stride of the per-vector pivots (odd: no bank conflicts)
+constexpr size_t kEigSmem =
+    static_cast<size_t>(kMaxL * kEigLd + kMaxL * kMaxL + kMaxL * kEigLuLd + kMaxL * kEigLd + 12 * kMaxL) * 4;
 
-__global__ void __launch_bounds__(kJacobiThreads) jacobi_kernel(const float2* __restrict__ G_all, int l, int r,
-                                                                float* __restrict__ ur_all)
+__global__ void __launch_bounds__(kEigThreads) eig_kernel(const float2* __restrict__ G_all, int l, int r,
+                                                          float* __restrict__ ur_all)
 {
     grid_launch_dependents();  // the next kernel of the merge may start launching
     grid_dependency_wait();    // the previous kernel's results are visible
-    // one eigenproblem per CTA (checkpoint blockIdx.x)
+    extern __shared__ float esm[];
+    float* A = esm;                                   // [kMaxL][kEigLd]
+    float* HV = A + kMaxL * kEigLd;                   // [kMaxL][kMaxL]: reflector k, entries 0 .. l - k - 2
+    float* LU = HV + kMaxL * kMaxL;                   // [kMaxL][kEigLuLd]: per vector m, u_i then l_i
+    float* Y = LU + kMaxL * kEigLuLd;                 // [kMaxL][kEigLd]: vector m, entry i
+    float* tau = Y + kMaxL * kEigLd;
+    float* dd = tau + kMaxL;
+    float* ee = dd + kMaxL;
+    float* e2 = ee + kMaxL;
+    float* pv = e2 + kMaxL;
+    float* wv = pv + kMaxL;
+    float* red = wv + kMaxL;  // 4 kMaxL floats of scratch
     const float2* G = G_all + static_cast<size_t>(blockIdx.x) * l * l;
     float* ur = ur_all + static_cast<size_t>(blockIdx.x) * l * r;
-    __shared__ float A[kMaxL][kMaxL + 1];
-    __shared__ float V[kMaxL][kMaxL + 1];
-    __shared__ float4 prm[kMaxL / 2];  // this round's pairs: c, s, t, p | q << 8
-    __shared__ unsigned char tp[kMaxL][kMaxL / 2], tq[kMaxL][kMaxL / 2];  // round-robin pairs of every round
-    __shared__ int idx[kMaxL];
-    __shared__ float vnorm[kMaxL];
-    __shared__ int rotated[2];  // rotations in sweeps of even / odd parity
-    __shared__ float athr;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int e = tid; e < kMaxL * kMaxL; e += kJacobiThreads) {
-        const int i = e >> 6, j = e & 63;
-        A[i][j] = (i < l && j < l && bd_in(kBkMsJacobi, blockIdx.x * l * l + i * l + j, gridDim.x * l * l))
-                      ? __fadd_rn(G[i * l + j].x, G[i * l + j].y)
-                      : 0.0f;
-        V[i][j] = i == j ? 1.0f : 0.0f;
-    }
-    const int n = l + (l & 1);
-    const int h = n / 2;
-    for (int e = tid; e < (n - 1) * h; e += kJacobiThreads) {  // the pair schedule, once
-        const int t = e / h, i = e - t * h;
-        const int a = i == 0 ? 0 : 1 + (i - 1 + t) % (n - 1);
-        const int b = 1 + (n - 2 - i + t) % (n - 1);
-        tp[t][i] = static_cast<unsigned char>(a < b ? a : b);
-        tq[t][i] = static_cast<unsigned char>(a < b ? b : a);
-    }
-    // this thread's 2 x 2 blocks (bi, bj) and V items (row, bj), fixed for the kernel
-    const int nb = h * h, nv = l * h;
-    int bi_[kJacobiBlocks], bj_[kJacobiBlocks], vr_[kJacobiVItems], vb_[kJacobiVItems];
+    for (int e = tid; e < l * l; e += kEigThreads)
+        A[(e / l) * kEigLd + e % l] =
+            bd_in(kBkMsEig, static_cast<int64_t>(blockIdx.x) * l * l + e, static_cast<int64_t>(gridDim.x) * l * l)
+                ? __fadd_rn(G[e].x, G[e].y)
+                : 0.0f;
+    __syncthreads();
+
+    // ---------------------------------------------------------------- 1. tridiagonalisation
+    // Every warp forms reflector k itself (its vector in registers: entries
+    // lane and lane + 32) and the p entries of its rows; after a barrier every
+    // warp forms K and w for itself and updates its rows of S; a second
+    // barrier ends the step.  Warp 0 keeps the reflectors for step 4.
+    for (int k = 0; k + 2 < l; ++k) {
+        const int m = l - k - 1;  // the trailing block S = A[k+1..][k+1..] is m x m
+        const float x0 = A[(k + 1) * kEigLd + k];
+        const float xa = lane < m ? A[(k + 1 + lane) * kEigLd + k] : 0.0f;
+        const float xb = lane + 32 < m ? A[(k + 33 + lane) * kEigLd + k] : 0.0f;
+        float sg = fmaf(xa, xa, xb * xb);
 #pragma unroll
-    for (int u = 0; u < kJacobiBlocks; ++u) {
-        const int e = tid + u * kJacobiThreads;
-        bi_[u] = e < nb ? e / h : -1;
-        bj_[u] = e < nb ? e - (e / h) * h : 0;
-    }
+        for (int o = 16; o > 0; o >>= 1) sg += __shfl_xor_sync(0xffffffffu, sg, o);
+        float alpha = 0.0f, t = 0.0f, v0 = x0;
+        if (sg > 0.0f) {
+            alpha = -copysignf(sqrtf(sg), x0);
+            v0 = x0 - alpha;
+            const float vtv = sg - x0 * x0 + v0 * v0;
+            t = vtv > 0.0f ? 2.0f / vtv : 0.0f;
+        }
+        const float va = lane == 0 ? v0 : xa, vb = xb;  // v_i, i = lane and lane + 32
+        if (warp == 0) {
+            if (lane < m) HV[k * kMaxL + lane] = va;
+            if (lane + 32 < m) HV[k * kMaxL + 32 + lane] = vb;
+            if (lane == 0) {
+                tau[k] = t;
+                ee[k] = t > 0.0f ? alpha : x0;  // the subdiagonal entry this reflector leaves
+            }
+        }
+        if (t != 0.0f) {
+            // p_i = tau (S v)_i for this warp's rows i = warp, warp + 8, ...
+            for (int i = warp; i < m; i += kEigThreads / 32) {
+                const float* srow = &A[(k + 1 + i) * kEigLd + k + 1];
+                float sv = (lane < m ? srow[lane] * va : 0.0f) + (lane + 32 < m ? srow[lane + 32] * vb : 0.0f);
 #pragma unroll
-    for (int u = 0; u < kJacobiVItems; ++u) {
-        const int e = tid + u * kJacobiThreads;
-        vr_[u] = e < nv ? e / h : -1;
-        vb_[u] = e < nv ? e - (e / h) * h : 0;
+                for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
+                if (lane == 0) pv[i] = t * sv;
+            }
+        }
+        __syncthreads();
+        if (t != 0.0f) {
+            const float pa = lane < m ? pv[lane] : 0.0f, pb = lane + 32 < m ? pv[lane + 32] : 0.0f;
+            float kp = fmaf(pa, va, pb * vb);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) kp += __shfl_xor_sync(0xffffffffu, kp, o);
+            const float K = 0.5f * t * kp;
+            const float wa = fmaf(-K, va, pa), wb = fmaf(-K, vb, pb);  // w_i, i = lane and lane + 32
+            for (int i = warp; i < m; i += kEigThreads / 32) {
+                // this warp's row i: S[i][j] -= v_i w_j + w_i v_j
+                const float vi = __shfl_sync(0xffffffffu, i < 32 ? va : vb, i & 31);
+                const float wi = __shfl_sync(0xffffffffu, i < 32 ? wa : wb, i & 31);
+                float* srow = &A[(k + 1 + i) * kEigLd + k + 1];
+                if (lane < m) srow[lane] = fmaf(-vi, wa, fmaf(-wi, va, srow[lane]));
+                if (lane + 32 < m) srow[lane + 32] = fmaf(-vi, wb, fmaf(-wi, vb, srow[lane + 32]));
+            }
+        }
+        __syncthreads();
+    }
+    for (int i = tid; i < l; i += kEigThreads) {
+        dd[i] = A[i * kEigLd + i];
+        if (i + 2 == l) ee[i] = A[(i + 1) * kEigLd + i];  // the last subdiagonal entry (no reflector)
     }
     __syncthreads();
+    for (int i = tid; i + 1 < l; i += kEigThreads) e2[i] = ee[i] * ee[i];
+    __syncthreads();
+
+    // ---------------------------------------------------------------- 2. eigenvalues by multisection
+    // A half-warp per eigenvalue (m = half-warp index, then + 16, ...): each of
+    // its 16 lanes counts the eigenvalues below one of 16 interior points of
+    // the interval, and the interval shrinks to the 1/17 that holds the
+    // eigenvalue; at most 12 rounds, or until the interval is two ulps wide.
+    float scale, pivmin, ufl;
+    {
+        float lo = dd[0], hi = dd[0], emax2 = 0.0f;
+        for (int i = 0; i < l; ++i) {
+            const float rad = (i > 0 ? fabsf(ee[i - 1]) : 0.0f) + (i + 1 < l ? fabsf(ee[i]) : 0.0f);
+            lo = fminf(lo, dd[i] - rad);
+            hi = fmaxf(hi, dd[i] + rad);
+            if (i + 1 < l) emax2 = fmaxf(emax2, e2[i]);
+        }
+        scale = fmaxf(fabsf(lo), fabsf(hi));
+        pivmin = fmaxf(1e-30f, 0x1p-60f * fmaxf(emax2, scale * scale));
+        ufl = fmaxf(pivmin, 0x1p-23f * scale);
+        const int hw = tid >> 4, g = tid & 15;
+        for (int mb = 0; mb < r; mb += kEigThreads / 16) {  // trip count uniform over the CTA
+            const int mm = mb + hw;
+            const bool act = mm < r;
+            float a = lo - (0x1p-22f * scale + pivmin), b = hi + (0x1p-22f * scale + pivmin);
+            const int target = act ? l - 1 - mm : 0;  // index of the eigenvalue in ascending order
+            for (int it = 0; it < 12; ++it) {
+                const float step = (b - a) * (1.0f / 17.0f);
+                const float x = g == 15 ? b - step : a + static_cast<float>(g + 1) * step;
+                int cnt = 0;
+                float q = dd[0] - x;
+                if (fabsf(q) < pivmin) q = -pivmin;
+                cnt += q < 0.0f ? 1 : 0;
+                for (int i = 1; i < l; ++i) {
+                    q = (dd[i] - x) - __fdividef(e2[i - 1], q);
+                    if (fabsf(q) < pivmin) q = -pivmin;
+                    cnt += q < 0.0f ? 1 : 0;
+                }
+                // the first point above the eigenvalue (count > target) bounds it from above
+                const unsigned above = __ballot_sync(0xffffffffu, cnt > target) >> (tid & 16);
+                const unsigned mine = above & 0xFFFFu;
+                const int gf = mine ? __ffs(mine) - 1 : 16;
+                const float xl = __shfl_sync(0xffffffffu, x, ((tid & 16) | (gf > 0 ? gf - 1 : 0)));
+                const float xh = __shfl_sync(0xffffffffu, x, ((tid & 16) | (gf < 16 ? gf : 15)));
+                const float na = gf > 0 ? xl : a, nb = gf < 16 ? xh : b;
+                const bool done = !(na < nb) || (nb - na) <= 2.0f * (fabsf(na) + fabsf(nb)) * 0x1p-24f;
+                a = na;
+                b = nb;
+                if (__all_sync(0xffffffffu, done)) break;
+            }
+            if (act && g == 0) red[mm] = 0.5f * (a + b);
+        }
+    }
+    __syncthreads();
+
+    // ---------------------------------------------------------------- 3. inverse iteration, then Gram-Schmidt
+    if (tid < r) {
+        const int mm = tid;
+        const float lam = red[mm];
+        // T - lam I = L U (no pivoting; a pivot below the floor is replaced by it)
+        float* U = LU + mm * kEigLuLd;
+        float* Lf = U + kMaxL;
+        float u = dd[0] - lam;
+        if (fabsf(u) < ufl) u = u < 0.0f ? -ufl : ufl;
+        U[0] = u;
+        for (int i = 1; i < l; ++i) {
+            const float lf = __fdividef(ee[i - 1], u);
+            u = (dd[i] - lam) - lf * ee[i - 1];
+            if (fabsf(u) < ufl) u = u < 0.0f ? -ufl : ufl;
+            Lf[i] = lf;
+            U[i] = u;
+        }
+        float* y = Y + mm * kEigLd;
+        for (int i = 0; i < l; ++i) y[i] = 1.0f + 0.125f * static_cast<float>((i * 7 + mm * 3) % 11);  // start vector
+        for (int pass = 0; pass < 2; ++pass) {
+            for (int i = 1; i < l; ++i) y[i] = fmaf(-Lf[i], y[i - 1], y[i]);
+            y[l - 1] = __fdividef(y[l - 1], U[l - 1]);
+            for (int i = l - 2; i >= 0; --i) y[i] = __fdividef(fmaf(-ee[i], y[i + 1], y[i]), U[i]);
+            // scale by the largest entry first (the solve can grow large), then normalise;
+            // a vector that is not finite or zero becomes the unit vector e_mm
+            float mx = 0.0f;
+            for (int i = 0; i < l; ++i) mx = fmaxf(mx, fabsf(y[i]));
+            if (!(mx > 0.0f) || !isfinite(mx)) {
+                for (int i = 0; i < l; ++i) y[i] = i == mm ? 1.0f : 0.0f;
+                continue;
+            }
+            const float inv = 1.0f / mx;
+            float nn = 0.0f;
+            for (int i = 0; i < l; ++i) {
+                y[i] *= inv;
+                nn = fmaf(y[i], y[i], nn);
+            }
+            const float sc = rsqrtf(nn);
+            for (int i = 0; i < l; ++i) y[i] *= sc;
+        }
+    }
+    __syncthreads();
+    // Gram-Schmidt in order of decreasing eigenvalue, twice, by warp 0 alone,
+    // within clusters: a vector is projected off the earlier vectors whose
+    // eigenvalues lie within 2^-10 of the spectrum's scale of its own (the
+    // vectors of eigenvalues further apart are orthogonal to about
+    // 2^-23 scale / gap after inverse iteration)
     if (warp == 0) {
-        float m = 0.0f;
-        for (int i = lane; i < l; i += 32) m = fmaxf(m, fabsf(A[i][i]));
+        for (int rep = 0; rep < 2; ++rep) {
+            int c0 = 0;  // first vector of the current cluster
+            for (int mm = 0; mm < r; ++mm) {
+                if (mm > 0 && red[c0] - red[mm] > 0x1p-10f * scale) {
+                    c0 = mm;
+                    while (c0 > 0 && red[c0 - 1] - red[mm] <= 0x1p-10f * scale) --c0;
+                }
+                float ya = lane < l ? Y[mm * kEigLd + lane] : 0.0f;
+                float yb = lane + 32 < l ? Y[mm * kEigLd + lane + 32] : 0.0f;
+                for (int i0 = c0; i0 < mm; ++i0) {
+                    const float ua = lane < l ? Y[i0 * kEigLd + lane] : 0.0f;
+                    const float ub = lane + 32 < l ? Y[i0 * kEigLd + lane + 32] : 0.0f;
+                    float d = fmaf(ua, ya, ub * yb);
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) {
-            athr = 0x1p-24f * m;
-            rotated[0] = 0;
+                    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+                    ya = fmaf(-d, ua, ya);
+                    yb = fmaf(-d, ub, yb);
+                }
+                float nn = fmaf(ya, ya, yb * yb);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) nn += __shfl_xor_sync(0xffffffffu, nn, o);
+                if (nn > 0x1p-40f) {
+                    const float sc = rsqrtf(nn);
+                    ya *= sc;
+                    yb *= sc;
+                } else {  // nothing left after the projection: a unit vector, orthogonalised by the next pass
+                    ya = lane == mm ? 1.0f : 0.0f;
+                    yb = lane + 32 == mm ? 1.0f : 0.0f;
+                }
+                if (lane < l) Y[mm * kEigLd + lane] = ya;
+                if (lane + 32 < l) Y[mm * kEigLd + lane + 32] = yb;
+                __syncwarp();
+            }
         }
     }
     __syncthreads();
-    for (int sweep = 0; sweep < 40; ++sweep) {
-        const int par = sweep & 1;
-        for (int t = 0; t + 1 < n; ++t) {
-            if (tid < h) {
-                const int p = tp[t][tid], q = tq[t][tid];
-                float c = 1.0f, sv = 0.0f, tt = 0.0f;
-                if (q < l) {
-                    const float apq = A[p][q], app = A[p][p], aqq = A[q][q];
-                    if (fabsf(apq) > athr && apq * apq > 0x1p-44f * fabsf(app * aqq)) {
-                        rotated[par] = 1;
-                        float rc, rs, rd;
-                        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rc) : "f"(2.0f * apq));
-                        const float th = (aqq - app) * rc;
-                        const float w = fmaf(th, th, 1.0f);
-                        asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(rs) : "f"(w));
-                        asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(rd) : "f"(fabsf(th) + w * rs));
-                        tt = copysignf(rd, th);
-                        const float x = fmaf(tt, tt, 1.0f);
-                        float y = rsqrtf(x);
-                        y = y * fmaf(-0.5f * x * y, y, 1.5f);
-                        c = y;
-                        sv = tt * y;
-                    }
-                }
-                prm[tid] = make_float4(c, sv, tt, __int_as_float(p | (q << 8)));
-            }
-            __syncthreads();
-            // every thread has read the previous sweep's flag: clear it for the next sweep
-            if (t == 0 && tid == 0) rotated[par ^ 1] = 0;
-            // A: block (pair bi rows, pair bj columns); columns first (A P), then rows (P^T .)
+
+    // ---------------------------------------------------------------- 4. back to G's basis
+    for (int mm = warp; mm < r; mm += kEigThreads / 32) {
+        float* y = Y + mm * kEigLd;
+        for (int k = l - 3; k >= 0; --k) {
+            const float t = tau[k];
+            if (t == 0.0f) continue;
+            const int m = l - k - 1;
+            const float* v = HV + k * kMaxL;
+            float s = 0.0f;
+            for (int i = lane; i < m; i += 32) s = fmaf(v[i], y[k + 1 + i], s);
 #pragma unroll
-            for (int u = 0; u < kJacobiBlocks; ++u) {
-                const int bi = bi_[u], bj = bj_[u];
-                if (bi < 0) break;
-                const float4 fi = prm[bi], fj = prm[bj];
-                const int pqi = __float_as_int(fi.w), pqj = __float_as_int(fj.w);
-                const int p = pqi & 255, q = pqi >> 8, p2 = pqj & 255, q2 = pqj >> 8;
-                const float ci = fi.x, si = fi.y, cj = fj.x, sj = fj.y;
-                const bool rq = q < l, cq = q2 < l;
-                const float a_pp = A[p][p2], a_pq = cq ? A[p][q2] : 0.0f;
-                const float a_qp = rq ? A[q][p2] : 0.0f, a_qq = (rq && cq) ? A[q][q2] : 0.0f;
-                if (bi == bj && si != 0.0f) {
-                    // the rotated pair itself: a_pq is annihilated exactly and
-                    // the diagonal moves by t a_pq
-                    const float ta = fi.z * a_pq;
-                    A[p][p] = a_pp - ta;
-                    A[q][q] = a_qq + ta;
-                    A[p][q] = 0.0f;
-                    A[q][p] = 0.0f;
-                } else {
-                    const float x_pp = cj * a_pp - sj * a_pq, x_pq = sj * a_pp + cj * a_pq;
-                    const float x_qp = cj * a_qp - sj * a_qq, x_qq = sj * a_qp + cj * a_qq;
-                    A[p][p2] = ci * x_pp - si * x_qp;
-                    if (cq) A[p][q2] = ci * x_pq - si * x_qq;
-                    if (rq) A[q][p2] = si * x_pp + ci * x_qp;
-                    if (rq && cq) A[q][q2] = si * x_pq + ci * x_qq;
-                }
-            }
-            // V: (row, column pair bj)
-#pragma unroll
-            for (int u = 0; u < kJacobiVItems; ++u) {
-                const int row = vr_[u], bj = vb_[u];
-                if (row < 0) break;
-                const float4 fj = prm[bj];
-                const int p2 = __float_as_int(fj.w) & 255, q2 = __float_as_int(fj.w) >> 8;
-                if (q2 >= l || fj.y == 0.0f) continue;
-                const float cj = fj.x, sj = fj.y;
-                const float vp = V[row][p2], vq = V[row][q2];
-                V[row][p2] = cj * vp - sj * vq;
-                V[row][q2] = sj * vp + cj * vq;
-            }
-            __syncthreads();
+            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            s *= t;
+            __syncwarp();
+            for (int i = lane; i < m; i += 32) y[k + 1 + i] = fmaf(-s, v[i], y[k + 1 + i]);
+            __syncwarp();
         }
-        if (!rotated[par]) break;
-    }
-    if (tid < l) {  // rank of eigenvalue tid: largest first, ties by lower index (NaN as -inf: a permutation)
-        const float d = isnan(A[tid][tid]) ? -INFINITY : A[tid][tid];
-        int rank = 0;
-        for (int j = 0; j < l; ++j) {
-            const float dj = isnan(A[j][j]) ? -INFINITY : A[j][j];
-            rank += (dj > d || (dj == d && j < tid)) ? 1 : 0;
-        }
-        idx[rank] = tid;
-        float ss = 0.0f;
-        for (int i = 0; i < l; ++i) ss = fmaf(V[i][tid], V[i][tid], ss);
-        float y = ss > 0.0f ? rsqrtf(ss) : 0.0f;
-        y = y * fmaf(-0.5f * ss * y, y, 1.5f);  // one Newton step
-        vnorm[tid] = y;
     }
     __syncthreads();
-    for (int e = tid; e < l * r; e += kJacobiThreads) {
-        const int c = idx[e % r];
-        if (bd_in(kBkMsJacobi, static_cast<int64_t>(blockIdx.x) * l * r + e, static_cast<int64_t>(gridDim.x) * l * r))
-            ur[e] = V[e / r][c] * vnorm[c];
+    for (int e = tid; e < l * r; e += kEigThreads) {
+        const int i = e / r, mm = e - i * r;
+        if (bd_in(kBkMsEig, static_cast<int64_t>(blockIdx.x) * l * r + e, static_cast<int64_t>(gridDim.x) * l * r))
+            ur[e] = Y[mm * kEigLd + i];
     }
 }
 
@@ -1621,6 +1725,8 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     constexpr size_t kMgSmem = static_cast<size_t>(kMgStages) * kMgStage + kMgWBufs * kMgWTile + 1024;
     static_assert(kMgSmem <= 227 * 1024, "merge shared memory");
     if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(merge_tc_kernel), kMgSmem, mgc);
+    static std::atomic<size_t> eic[kHostMaxDevices];
+    if (e0 == cudaSuccess) e0 = ensure_dynamic_smem(reinterpret_cast<const void*>(eig_kernel), kEigSmem, eic);
     if (e0 != cudaSuccess) return e0;
     const MonoSoupWs lay = ws_layout(a.d_out, a.d_in, a.k, a.rank, a.l);
     char* w = static_cast<char*>(a.ws);
@@ -1850,7 +1956,7 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
             gram(Z, a.d_in, nb, Gk + static_cast<size_t>(i0) * ll);  // B B^T
         }
         // the k projected eigenproblems at once, one CTA each
-        launch_dep(perr, jacobi_kernel, static_cast<unsigned>(a.k), kJacobiThreads, 0, st, Gk, l, r, Uk);  // U_r [l][r]
+        launch_dep(perr, eig_kernel, static_cast<unsigned>(a.k), kEigThreads, kEigSmem, st, static_cast<const float2*>(Gk), l, r, Uk);  // U_r [l][r]
         const unsigned rq = static_cast<unsigned>((r + 3) / 4);
         launch_dep(perr, apply_t_kernel, dim3(blocks_for(a.d_out * rq), static_cast<unsigned>(a.k)), 256, 0, st, Yall, a.d_out, l,
                                                                                                   Uk, r, L);

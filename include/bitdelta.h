@@ -224,7 +224,8 @@ bd_status bd_materialize(const uint16_t* w_base, const uint32_t* signs, const fl
  * on the tensor cores on exact three-piece bf16 splits of their fp32
  * operands (fp32 accumulation; l <= 32 -- wider sketches use fp32 CUDA-core
  * products); the Gram matrices and their Cholesky factors are float-float,
- * the l x l eigenproblem fp32 Jacobi.  The result is rounded once to
+ * the l x l symmetric eigenproblem fp32 (Householder tridiagonalisation,
+ * bisection on Sturm counts, inverse iteration).  The result is rounded once to
  * `out_dtype`.
  *   w_base    device bf16 [d_out][d_in], 16-byte aligned
  *   w_ft      HOST array of k device pointers, each bf16 [d_out][d_in],
