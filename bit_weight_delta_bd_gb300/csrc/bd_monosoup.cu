@@ -954,7 +954,8 @@ __global__ void __launch_bounds__(256) chol_kernel(const float2* __restrict__ G_
 //      (tridiagonal elimination, tiny pivots replaced by a floor) from a fixed
 //      start vector, and one warp orthonormalises the r vectors in order of
 //      decreasing eigenvalue (Gram-Schmidt, twice, within clusters of close
-//      eigenvalues), which keeps the vectors of close eigenvalues apart;
+//      eigenvalues, which keeps the vectors of close eigenvalues apart; then
+//      one Newton-Schulz step over all r vectors);
 //   4. each vector is carried back to G's basis by the reflectors in reverse
 //      order (one warp per vector, no barrier).
 // ur[i][m] = entry i of the unit eigenvector of the m-th largest eigenvalue,
@@ -1196,10 +1197,37 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(const float2* __restri
         }
     }
     __syncthreads();
+    // One Newton-Schulz step over all r vectors (the rows of Y):
+    // Y <- (3 I - Y Y^T) Y / 2 keeps their span and takes an orthonormality
+    // error e to about 1.5 e^2 (plus fp32 dot-product rounding).  It covers
+    // the pairs that Gram-Schmidt leaves alone: inverse iteration makes the
+    // vectors of eigenvalues g apart orthogonal only to about 2^-23 scale / g,
+    // 2^-13 at the cluster threshold.  C = (3 I - Y Y^T) / 2 takes the
+    // pivots' space, the result A's (both free by now).
+    {
+        float* C = LU;
+        for (int e = tid; e < r * r; e += kEigThreads) {
+            const int a = e / r, b = e - a * r;
+            const float* ya = Y + a * kEigLd;
+            const float* yb = Y + b * kEigLd;
+            float d = 0.0f;
+            for (int i = 0; i < l; ++i) d = fmaf(ya[i], yb[i], d);
+            C[e] = (a == b ? 1.5f : 0.0f) - 0.5f * d;
+        }
+        __syncthreads();
+        for (int e = tid; e < r * l; e += kEigThreads) {
+            const int mm = e / l, i = e - mm * l;
+            const float* c = C + mm * r;
+            float s = 0.0f;
+            for (int b = 0; b < r; ++b) s = fmaf(c[b], Y[b * kEigLd + i], s);
+            A[mm * kEigLd + i] = s;
+        }
+        __syncthreads();
+    }
 
     // ---------------------------------------------------------------- 4. back to G's basis
     for (int mm = warp; mm < r; mm += kEigThreads / 32) {
-        float* y = Y + mm * kEigLd;
+        float* y = A + mm * kEigLd;
         for (int k = l - 3; k >= 0; --k) {
             const float t = tau[k];
             if (t == 0.0f) continue;
@@ -1219,7 +1247,7 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(const float2* __restri
     for (int e = tid; e < l * r; e += kEigThreads) {
         const int i = e / r, mm = e - i * r;
         if (bd_in(kBkMsEig, static_cast<int64_t>(blockIdx.x) * l * r + e, static_cast<int64_t>(gridDim.x) * l * r))
-            ur[e] = Y[mm * kEigLd + i];
+            ur[e] = A[mm * kEigLd + i];
     }
 }
 

@@ -184,6 +184,26 @@ def monosoup_noisy_checkpoints(seed: int, d_out: int, d_in: int, k: int, rank_si
     return wb, out
 
 
+def monosoup_spectrum_checkpoints(seed: int, d_out: int, d_in: int, k: int, s):
+    """MonoSoup inputs with a prescribed spectrum: W_i = bf16(W_base + U_i
+    diag(s) V_i^T) with U_i [d_out][len(s)] and V_i [d_in][len(s)] exactly
+    orthonormal (the Q factors of standard normal matrices), so that the
+    singular values of W_i - W_base are s up to the bf16 rounding of W_i
+    (repeated values stay repeated to that level).  Draw order: W_base, then
+    the two normal matrices per checkpoint.  Returns (w_base_bits,
+    [w_i_bits])."""
+    rng = np.random.default_rng(seed)
+    wb = base_weight(rng, d_out, d_in)
+    s = np.asarray(s, dtype=np.float64)
+    wb64 = bf16_bits_to_f32(wb).astype(np.float64)
+    out = []
+    for _ in range(k):
+        u, _r = np.linalg.qr(rng.standard_normal((d_out, len(s))))
+        v, _r = np.linalg.qr(rng.standard_normal((d_in, len(s))))
+        out.append(f32_to_bf16_bits((wb64 + (u * s) @ v.T).astype(np.float32)))
+    return wb, out
+
+
 def gaussian_test_matrix(seed: int, d_in: int, l: int) -> np.ndarray:
     """Standard normal fp32 [d_in][l]: the random test matrix a randomized
     range finder draws (here an input, so both sides see the same one)."""

@@ -177,6 +177,63 @@ def test_monosoup_full_rank_one_checkpoint(dev):
     np.testing.assert_allclose(got, oracle.bf16_to_f64(ws[0]), rtol=0, atol=2e-6)
 
 
+@pytest.mark.parametrize("name,d_out,d_in,k,spectrum,l,q", [
+    # two clusters of four equal singular values
+    ("clusters", 512, 384, 2, [2.0] * 4 + [1.0] * 4, 16, 1),
+    # one cluster of sixteen: every leading eigenvalue of the projected problem the same
+    ("one_cluster", 640, 512, 3, [1.5] * 16, 32, 1),
+    # a slow decay: neighbouring eigenvalues about 0.3 % of the largest apart, just
+    # outside any cluster, where inverse iteration alone leaves the vectors
+    # about 1e-4 from orthogonal
+    ("slow_decay", 640, 512, 3, [2.0 * (1.0 - 0.0015 * j) for j in range(16)], 32, 1),
+])
+def test_monosoup_repeated_and_close_singular_values(dev, name, d_out, d_in, k, spectrum, l, q):
+    """Task vectors whose leading singular values repeat or nearly repeat
+    (beyond them only the bf16 rounding of the checkpoints): the truncation
+    at r = len(spectrum) is still unique, and the randomized result must
+    match it to fp32 accuracy whatever basis of a repeated singular subspace
+    the eigensolver picks."""
+    r = len(spectrum)
+    wb, ws = synth.monosoup_spectrum_checkpoints(31 + d_out + r, d_out, d_in, k, spectrum)
+    om = synth.gaussian_test_matrix(37 + d_in, d_in, l)
+    ref = oracle.monosoup_merge(wb, ws, r)
+    base = oracle.bf16_to_f64(wb)
+    upd_ref = ref - base
+    got = run_gpu(dev, wb, ws, om, r, l, q, torch.float32).double().numpy()
+    rel = np.linalg.norm((got - base) - upd_ref) / np.linalg.norm(upd_ref)
+    assert rel <= 1e-4, f"{name}: relative error of the merged update {rel:.3e}"
+
+
+def test_monosoup_zero_task_vector(dev):
+    """One checkpoint equal to the base (Delta = 0: every pivot of its
+    CholeskyQR is dropped and its eigenproblem is the zero matrix): its term
+    is zero and the merge is W_base + (1/3)(tau_1 + tau_2)."""
+    wb, ws = synth.monosoup_checkpoints(41, 384, 256, 2, 8)
+    ws = [ws[0], wb.copy(), ws[1]]
+    om = synth.gaussian_test_matrix(43, 256, 16)
+    ref = oracle.monosoup_merge(wb, ws, 8)
+    base = oracle.bf16_to_f64(wb)
+    got = run_gpu(dev, wb, ws, om, 8, 16, 1, torch.float32).double().numpy()
+    rel = np.linalg.norm((got - base) - (ref - base)) / np.linalg.norm(ref - base)
+    assert rel <= 1e-4, rel
+
+
+@pytest.mark.parametrize("d_out,d_in,k,l", [
+    (4, 128, 2, 4),     # the narrowest sketch, rank = l = d_out
+    (64, 256, 1, 64),   # the widest sketch, rank = l = d_out (CUDA-core products)
+])
+def test_monosoup_rank_equals_sketch_width(dev, d_out, d_in, k, l):
+    """rank = l = d_out: every eigenvector of the projected problem is kept
+    and the sketch spans every row direction, so each tau_i is Delta_i and
+    the merge is the mean of the checkpoints (to fp32 accuracy)."""
+    wb, ws = synth.monosoup_checkpoints(47 + l, d_out, d_in, k, d_out)
+    om = synth.gaussian_test_matrix(53 + l, d_in, l)
+    got = run_gpu(dev, wb, ws, om, l, l, 1, torch.float32).double().numpy()
+    ref = oracle.monosoup_merge(wb, ws, l)
+    np.testing.assert_allclose(ref, sum(oracle.bf16_to_f64(w) for w in ws) / k, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=4e-6)
+
+
 def test_monosoup_ffn_sized(dev):
     """2048 x 2048, 3 checkpoints, rank 16: the oracle's full SVD still runs
     in seconds; the same bound as the small cases."""
