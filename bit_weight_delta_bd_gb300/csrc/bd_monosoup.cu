@@ -957,7 +957,7 @@ __global__ void __launch_bounds__(256) chol_kernel(const float2* __restrict__ G_
 //      eigenvalues, which keeps the vectors of close eigenvalues apart; then
 //      one Newton-Schulz step over all r vectors);
 //   4. each vector is carried back to G's basis by the reflectors in reverse
-//      order (one warp per vector, no barrier).
+//      order (a warp takes two vectors at a time, in registers).
 // ur[i][m] = entry i of the unit eigenvector of the m-th largest eigenvalue,
 // m < r.  Standard dense symmetric eigensolver steps (Householder
 // tridiagonalisation, Sturm bisection, inverse iteration), as in Golub and
@@ -1168,6 +1168,7 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(const float2* __restri
                     c0 = mm;
                     while (c0 > 0 && red[c0 - 1] - red[mm] <= 0x1p-10f * scale) --c0;
                 }
+                if (c0 == mm) continue;  // no earlier vector in its cluster: already a unit vector
                 float ya = lane < l ? Y[mm * kEigLd + lane] : 0.0f;
                 float yb = lane + 32 < l ? Y[mm * kEigLd + lane + 32] : 0.0f;
                 for (int i0 = c0; i0 < mm; ++i0) {
@@ -1226,22 +1227,40 @@ __global__ void __launch_bounds__(kEigThreads) eig_kernel(const float2* __restri
     }
 
     // ---------------------------------------------------------------- 4. back to G's basis
-    for (int mm = warp; mm < r; mm += kEigThreads / 32) {
-        float* y = A + mm * kEigLd;
+    // Warp w carries vectors w + 8 j (two at a time, entries lane and
+    // lane + 32 in registers) through the reflectors in reverse order:
+    // y <- y - tau (v^T y) v, v_i at entry k + 1 + i.
+    for (int j0 = warp; j0 < r; j0 += 2 * (kEigThreads / 32)) {
+        const int mA = j0, mB = j0 + kEigThreads / 32;
+        const bool hasB = mB < r;
+        float ya0 = lane < l ? A[mA * kEigLd + lane] : 0.0f;
+        float ya1 = lane + 32 < l ? A[mA * kEigLd + lane + 32] : 0.0f;
+        float yb0 = hasB && lane < l ? A[mB * kEigLd + lane] : 0.0f;
+        float yb1 = hasB && lane + 32 < l ? A[mB * kEigLd + lane + 32] : 0.0f;
         for (int k = l - 3; k >= 0; --k) {
             const float t = tau[k];
             if (t == 0.0f) continue;
             const int m = l - k - 1;
-            const float* v = HV + k * kMaxL;
-            float s = 0.0f;
-            for (int i = lane; i < m; i += 32) s = fmaf(v[i], y[k + 1 + i], s);
+            const int i0 = lane - (k + 1), i1 = lane + 32 - (k + 1);
+            const float v0 = (i0 >= 0 && i0 < m) ? HV[k * kMaxL + i0] : 0.0f;
+            const float v1 = (i1 >= 0 && i1 < m) ? HV[k * kMaxL + i1] : 0.0f;
+            float sa = fmaf(v0, ya0, v1 * ya1), sb = fmaf(v0, yb0, v1 * yb1);
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-            s *= t;
-            __syncwarp();
-            for (int i = lane; i < m; i += 32) y[k + 1 + i] = fmaf(-s, v[i], y[k + 1 + i]);
-            __syncwarp();
+            for (int o = 16; o > 0; o >>= 1) {
+                sa += __shfl_xor_sync(0xffffffffu, sa, o);
+                sb += __shfl_xor_sync(0xffffffffu, sb, o);
+            }
+            sa *= t;
+            sb *= t;
+            ya0 = fmaf(-sa, v0, ya0);
+            ya1 = fmaf(-sa, v1, ya1);
+            yb0 = fmaf(-sb, v0, yb0);
+            yb1 = fmaf(-sb, v1, yb1);
         }
+        if (lane < l) A[mA * kEigLd + lane] = ya0;
+        if (lane + 32 < l) A[mA * kEigLd + lane + 32] = ya1;
+        if (hasB && lane < l) A[mB * kEigLd + lane] = yb0;
+        if (hasB && lane + 32 < l) A[mB * kEigLd + lane + 32] = yb1;
     }
     __syncthreads();
     for (int e = tid; e < l * r; e += kEigThreads) {
