@@ -79,7 +79,7 @@ NCU_TRAFFIC = {
                                                                       939_384_576 + 60_230_955),
     ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
     # all 29 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("dd8526d27e9e3840", "bd_monosoup.cu", 2_412_478_720 + 109_467_392),
+    (MONOSOUP_CALL, "monosoup"): ("7fc578022883d69f", "bd_monosoup.cu", 2_412_437_504 + 106_908_672),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =

@@ -336,12 +336,16 @@ size_t dprod_smem()
 // A stage holds only the W_i and W_base tiles and the B tile (44 KB), so four
 // stages keep four tiles of Delta in flight per SM.  The W tiles of a stage
 // are free as soon as the piece warps hold their values (wfree), the B tile
-// when the stage's MMAs finish (empty).  The checkpoint varies fastest along
-// grid x (blockIdx.x = block * checkpoints + checkpoint), so the CTAs that
-// read the same W_base tiles run side by side and share them in L2.  Warp 0 issues the TMA
-// loads, warp 1 allocates tensor memory and issues the MMAs, warps 2..9 form
-// the pieces (lane quarter warp % 4, K half (warp - 2) / 4); warps 2..5 then
-// read the accumulator, one row per thread.
+// when the stage's MMAs finish (empty).  The CTAs are persistent, one per
+// SM: CTA c takes the units (row block, checkpoint, slice of the reduction
+// dimension) c, c + gridDim.x, ... and its ring runs on across them (a new
+// CTA per unit spent ~4 us per unit on its ramp and on the switch).  The
+// checkpoint varies fastest along the units, so the CTAs that read the same
+// W_base tiles run side by side and share them in L2.  Warp 0 issues the
+// TMA loads, warp 1 allocates tensor memory and issues the MMAs, warps 2..9
+// form the pieces (lane quarter warp % 4, K half (warp - 2) / 4), warps
+// 10..13 read each unit's accumulator, one row per thread (the next unit's
+// MMAs wait for those loads).
 constexpr int kTM = 128;                     // MMA M: Delta rows (MODE 0) or columns (MODE 1) of a CTA
 constexpr int kTK = 64;                      // reduction indices per stage
 constexpr int kTNB = 96;                     // MMA N: three pieces x 32 columns of the small operand
@@ -350,7 +354,8 @@ constexpr int kTWTile = kTM * kTK * 2;       // one bf16 tile of W: 16 KB
 constexpr int kTBTile = kTNB * kTK * 2;      // the B tile: 12 KB
 constexpr int kTStage = 2 * kTWTile + kTBTile;
 constexpr int kTConvWarps = 8;
-constexpr int kTThreads = 32 * (2 + kTConvWarps);
+constexpr int kTEpiWarp = 2 + kTConvWarps;         // warps kTEpiWarp .. + 3 drain the accumulator
+constexpr int kTThreads = 32 * (2 + kTConvWarps + 4);
 constexpr uint32_t kTTmemCols = 512;
 constexpr uint32_t kTDCol = 0;                // D: 96 columns
 constexpr uint32_t kTACol = 128;              // A ring: 3 pieces x 32 columns per stage
@@ -361,11 +366,13 @@ struct TProdParams {
     CUtensorMap b_map;             // W_base [d_out][d_in] bf16, box 64 x 128 (MODE 0) or 64 x 64 (MODE 1), 128-byte swizzle
     CUtensorMap w_map[kMaxBatch];  // W_i of checkpoint blockIdx.x % nz, same
     CUtensorMap s_map[kMaxBatch];  // its split small operand [128][Kp] bf16, box 64 x 96, 128-byte swizzle
-    float* part;                   // [checkpoints][gridDim.y][out rows][l]
+    float* part;                   // [checkpoints][ns][out rows][l]
     uint32_t* err;                 // the error word: a wait that timed out sets kErrTimeout
     int64_t d_out, d_in;
     int l;
-    int nz;                        // checkpoints of the batch (grid x = blocks * nz)
+    int nz;                        // checkpoints of the batch
+    int ns;                        // slices of the reduction dimension
+    int tiles;                     // row blocks x checkpoints
     int64_t k_per;                 // reduction indices per slice (a multiple of 64)
 };
 
@@ -463,18 +470,33 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
     extern __shared__ uint8_t dyn_raw[];
     __shared__ uint64_t full[kTStages], afull[kTStages], empty[kTStages];
     __shared__ uint64_t wfree[kTStages];  // the piece warps hold the stage's W values (W slots free)
-    __shared__ uint64_t done;
+    __shared__ uint64_t accfull, accempty;  // a unit's MMAs are done / the epilogue holds its accumulator
+    __shared__ uint64_t done;               // every MMA issued has finished (before tensor memory is freed)
     __shared__ uint32_t tmem_base;
     __shared__ volatile int abort;
     uint8_t* ring = dyn_raw + ((1024u - (smem_u32(dyn_raw) & 1023u)) & 1023u);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int nz = p.nz;
-    const int z = static_cast<int>(blockIdx.x % nz);                        // checkpoint of the batch
-    const int64_t o0 = static_cast<int64_t>(blockIdx.x / nz) * kTM;  // first output row of this CTA
     const int64_t klen = MODE == 0 ? p.d_in : p.d_out;
-    const int64_t kb = static_cast<int64_t>(blockIdx.y) * p.k_per;
-    const int64_t ke = kb + p.k_per < klen ? kb + p.k_per : klen;
-    const int nt = ke > kb ? static_cast<int>((ke - kb + kTK - 1) / kTK) : 0;
+    const int units = p.tiles * p.ns;
+    // unit u (this CTA takes u = blockIdx.x, blockIdx.x + gridDim.x, ...): slice u / tiles, row block
+    // (u % tiles) / nz, checkpoint u % nz -- the checkpoint varies fastest, so the CTAs that read the
+    // same W_base tiles run side by side
+    struct Unit {
+        int z, slice, nt;
+        int64_t o0, kb;
+    };
+    auto unit = [&](int u) {
+        Unit x;
+        const int tile = u % p.tiles;
+        x.slice = u / p.tiles;
+        x.z = tile % nz;
+        x.o0 = static_cast<int64_t>(tile / nz) * kTM;
+        x.kb = static_cast<int64_t>(x.slice) * p.k_per;
+        const int64_t ke = x.kb + p.k_per < klen ? x.kb + p.k_per : klen;
+        x.nt = ke > x.kb ? static_cast<int>((ke - x.kb + kTK - 1) / kTK) : 0;
+        return x;
+    };
     if (tid == 0) {
         for (int st = 0; st < kTStages; ++st) {
             mbar_init(&full[st], 1);
@@ -482,6 +504,8 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
             mbar_init(&empty[st], 1);
             mbar_init(&wfree[st], kTConvWarps);
         }
+        mbar_init(&accfull, 1);
+        mbar_init(&accempty, 4);
         mbar_init(&done, 1);
         abort = 0;
         fence_mbarrier_init();
@@ -510,30 +534,40 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int t = 0;
-            for (; t < nt; ++t) {
-                const int st = t % kTStages;
-                const uint32_t prev = static_cast<uint32_t>(t / kTStages - 1) & 1u;
-                if (t >= kTStages && !wait(&wfree[st], prev)) break;
-                uint8_t* sb = ring + static_cast<size_t>(st) * kTStage;
-                const int k0 = static_cast<int>(kb + static_cast<int64_t>(t) * kTK);
-                mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kTStage));
-                if (MODE == 0) {
-                    tma_load_2d(sb, &p.w_map[z], k0, static_cast<int>(o0), &full[st]);
-                    tma_load_2d(sb + kTWTile, &p.b_map, k0, static_cast<int>(o0), &full[st]);
-                } else {
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        const int cx = static_cast<int>(o0) + 64 * hb;
-                        tma_load_2d(sb + hb * (kTWTile / 2), &p.w_map[z], cx, k0, &full[st]);
-                        tma_load_2d(sb + kTWTile + hb * (kTWTile / 2), &p.b_map, cx, k0, &full[st]);
+            int g = 0;  // stages issued, over all units of this CTA
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x) {
+                const Unit x = unit(u);
+                for (int t = 0; t < x.nt; ++t, ++g) {
+                    const int st = g % kTStages;
+                    const uint32_t prev = static_cast<uint32_t>(g / kTStages - 1) & 1u;
+                    if (g >= kTStages && !wait(&wfree[st], prev)) {
+                        ok = false;
+                        break;
                     }
+                    uint8_t* sb = ring + static_cast<size_t>(st) * kTStage;
+                    const int k0 = static_cast<int>(x.kb + static_cast<int64_t>(t) * kTK);
+                    mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(kTStage));
+                    if (MODE == 0) {
+                        tma_load_2d(sb, &p.w_map[x.z], k0, static_cast<int>(x.o0), &full[st]);
+                        tma_load_2d(sb + kTWTile, &p.b_map, k0, static_cast<int>(x.o0), &full[st]);
+                    } else {
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {
+                            const int cx = static_cast<int>(x.o0) + 64 * hb;
+                            tma_load_2d(sb + hb * (kTWTile / 2), &p.w_map[x.z], cx, k0, &full[st]);
+                            tma_load_2d(sb + kTWTile + hb * (kTWTile / 2), &p.b_map, cx, k0, &full[st]);
+                        }
+                    }
+                    // the B tile once the stage's MMAs are done with it
+                    if (g >= kTStages && !wait(&empty[st], prev)) {
+                        ok = false;
+                        break;
+                    }
+                    tma_load_2d(sb + 2 * kTWTile, &p.s_map[x.z], k0, 0, &full[st]);
                 }
-                // the B tile once the stage's MMAs are done with it
-                if (t >= kTStages && !wait(&empty[st], prev)) break;
-                tma_load_2d(sb + 2 * kTWTile, &p.s_map[z], k0, 0, &full[st]);
             }
-            for (int i = (t > kTStages ? t - kTStages : 0); i < t; ++i) {  // every issued copy lands before exit
+            for (int i = (g > kTStages ? g - kTStages : 0); i < g; ++i) {  // every issued copy lands before exit
                 const uint64_t t0 = global_timer_ns();
                 while (!mbar_try_wait(&full[i % kTStages], static_cast<uint32_t>(i / kTStages) & 1u) &&
                        global_timer_ns() - t0 < kWaitLimitNs) {
@@ -550,32 +584,50 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
             // than 2^-20 |Delta_j S_j|, below the fp32 accumulation error over K.
             constexpr uint32_t idesc_a[3] = {idesc_bf16_f32(kTM, 96), idesc_bf16_f32(kTM, 64),
                                              idesc_bf16_f32(kTM, 32)};
-            for (int t = 0; t < nt; ++t) {
-                const int st = t % kTStages;
-                if (!wait(&afull[st], static_cast<uint32_t>(t / kTStages) & 1u)) break;
+            int g = 0, j = 0;  // stages and units done by this CTA
+            bool ok = true;
+            for (int u = blockIdx.x; ok && u < units; u += gridDim.x, ++j) {
+                const Unit x = unit(u);
+                // the accumulator: free once the epilogue holds the previous unit's values
+                if (j > 0 && !wait(&accempty, static_cast<uint32_t>(j - 1) & 1u)) break;
                 tc_fence_after();
-                const uint64_t bdesc = smem_desc_sw128(smem_u32(ring + static_cast<size_t>(st) * kTStage + 2 * kTWTile));
-                const uint32_t acol = tmem + kTACol + 96u * static_cast<uint32_t>(st);
+                for (int t = 0; t < x.nt; ++t, ++g) {
+                    const int st = g % kTStages;
+                    if (!wait(&afull[st], static_cast<uint32_t>(g / kTStages) & 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint64_t bdesc =
+                        smem_desc_sw128(smem_u32(ring + static_cast<size_t>(st) * kTStage + 2 * kTWTile));
+                    const uint32_t acol = tmem + kTACol + 96u * static_cast<uint32_t>(st);
 #pragma unroll
-                for (int kk = 0; kk < kTK / 16; ++kk) {
+                    for (int kk = 0; kk < kTK / 16; ++kk) {
 #pragma unroll
-                    for (int a = 0; a < 3; ++a)
-                        mma_ts(tmem + kTDCol, acol + 32u * a + 8u * kk, bdesc + static_cast<uint64_t>(2 * kk),
-                               idesc_a[a], (t | kk | a) != 0 ? 1u : 0u);
+                        for (int a = 0; a < 3; ++a)
+                            mma_ts(tmem + kTDCol, acol + 32u * a + 8u * kk, bdesc + static_cast<uint64_t>(2 * kk),
+                                   idesc_a[a], (t | kk | a) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(&empty[st]);
                 }
-                mma_commit(&empty[st]);
+                if (ok) mma_commit(&accfull);  // every MMA of the unit has finished when this arrives
             }
-            mma_commit(&done);  // every MMA issued above has finished when this arrives
+            mma_commit(&done);  // also after a wait gave up: no MMA may be in flight when tensor memory is freed
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(&done, 0u) && global_timer_ns() - t0 < kWaitLimitNs) {
+            }
         }
-    } else {
+    } else if (warp < kTEpiWarp) {
         // ------------------------------------------------------------ pieces of Delta -> tensor memory
         const int q = warp & 3;                  // lane quarter: rows 32 q .. 32 q + 31 of A
         const int kh = (warp - 2) >> 2;          // K half: 32 reduction indices (16 columns) of each stage
         const int rl = 32 * q + lane;            // this thread's row of A
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(32 * q) << 16);
-        for (int t = 0; t < nt; ++t) {
-            const int st = t % kTStages;
-            if (!__all_sync(0xffffffffu, wait(&full[st], static_cast<uint32_t>(t / kTStages) & 1u))) break;
+        int total = 0;  // stages of all units of this CTA
+        for (int u = blockIdx.x; u < units; u += gridDim.x) total += unit(u).nt;
+        for (int g = 0; g < total; ++g) {
+            const int st = g % kTStages;
+            if (!__all_sync(0xffffffffu, wait(&full[st], static_cast<uint32_t>(g / kTStages) & 1u))) break;
             const uint8_t* sb = ring + static_cast<size_t>(st) * kTStage;
             uint32_t v1[16], v2[16], v3[16];
             if (MODE == 0) {
@@ -618,36 +670,39 @@ __global__ void __launch_bounds__(kTThreads, 1) tprod_kernel(const __grid_consta
             __syncwarp();
             if (lane == 0) mbar_arrive(&afull[st]);
         }
-    }
-    // ---------------------------------------------------------------- epilogue (warps 2..5): one row of D per thread
-    if (warp >= 2 && warp < 6) {
+    } else {
+        // ------------------------------------------------------------ epilogue: one row of D per thread, per unit
         const int q = warp & 3;
-        const bool ok = __all_sync(0xffffffffu, wait(&done, 0u)) && !abort;
-        tc_fence_after();
-        if (ok) {
-            const int rl = 32 * q + lane;
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kTDCol;
-            uint32_t d0[32], d1[32], d2[32];
+        const int rl = 32 * q + lane;
+        const uint32_t taddr = tmem + (static_cast<uint32_t>(32 * q) << 16) + kTDCol;
+        const int64_t nrows = MODE == 0 ? p.d_out : p.d_in;
+        int j = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++j) {
+            const Unit x = unit(u);
+            if (!__all_sync(0xffffffffu, wait(&accfull, static_cast<uint32_t>(j) & 1u))) break;
+            tc_fence_after();
+            // D[m][c] + D[m][32 + c] + D[m][64 + c], added in that order (64 registers live)
+            uint32_t d0[32], d1[32];
             tmem_ld32(taddr, d0);
             tmem_ld32(taddr + 32, d1);
-            tmem_ld32(taddr + 64, d2);
-            const int64_t nrows = MODE == 0 ? p.d_out : p.d_in;
-            const int64_t row = o0 + rl;
+#pragma unroll
+            for (int c = 0; c < 32; ++c) d0[c] = __float_as_uint(__uint_as_float(d0[c]) + __uint_as_float(d1[c]));
+            tmem_ld32(taddr + 64, d1);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&accempty);  // the next unit's MMAs may overwrite D
+#pragma unroll
+            for (int c = 0; c < 32; ++c) d0[c] = __float_as_uint(__uint_as_float(d0[c]) + __uint_as_float(d1[c]));
+            const int64_t row = x.o0 + rl;
             if (row < nrows) {
-                float* out = p.part + ((static_cast<int64_t>(z) * gridDim.y + blockIdx.y) * nrows + row) * p.l;
+                const int64_t ob = ((static_cast<int64_t>(x.z) * p.ns + x.slice) * nrows + row) * p.l;
+                float* out = p.part + ob;
 #pragma unroll
                 for (int c = 0; c < 32; c += 4) {
                     if (c >= p.l) break;
-                    float4 y;
-                    y.x = nt > 0 ? (__uint_as_float(d0[c]) + __uint_as_float(d1[c])) + __uint_as_float(d2[c]) : 0.0f;
-                    y.y = nt > 0 ? (__uint_as_float(d0[c + 1]) + __uint_as_float(d1[c + 1])) + __uint_as_float(d2[c + 1])
-                                 : 0.0f;
-                    y.z = nt > 0 ? (__uint_as_float(d0[c + 2]) + __uint_as_float(d1[c + 2])) + __uint_as_float(d2[c + 2])
-                                 : 0.0f;
-                    y.w = nt > 0 ? (__uint_as_float(d0[c + 3]) + __uint_as_float(d1[c + 3])) + __uint_as_float(d2[c + 3])
-                                 : 0.0f;
-                    if (bd_in_range(kBkMsProd, ((static_cast<int64_t>(z) * gridDim.y + blockIdx.y) * nrows + row) * p.l + c,
-                                    4, static_cast<int64_t>(nz) * gridDim.y * nrows * p.l))
+                    const float4 y = make_float4(__uint_as_float(d0[c]), __uint_as_float(d0[c + 1]),
+                                                 __uint_as_float(d0[c + 2]), __uint_as_float(d0[c + 3]));
+                    if (bd_in_range(kBkMsProd, ob + c, 4, static_cast<int64_t>(nz) * p.ns * nrows * p.l))
                         *reinterpret_cast<float4*>(out + c) = y;
                 }
             }
@@ -1876,6 +1931,10 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     } pend;
     bool sp_ready = false;  // the last CholeskyQR pass wrote the next product's split operand
     const int64_t tr_blocks = (a.d_out + kTM - 1) / kTM, tc_blocks = a.d_in / kTM;
+    // the tensor-core products run one persistent CTA per SM over their units
+    auto persistent_ctas = [&](int64_t units) {
+        return static_cast<unsigned>(units < sms ? units : sms);
+    };
     // Y_z = Delta_z S_z for the batch (S_z = Omega, or Z_z with zs)
     auto sketch = [&](int i0, int nb, bool zs) {
         if (perr != cudaSuccess) return;
@@ -1891,7 +1950,9 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                 return;
             }
             tp_sk.nz = nb;
-            launch_dep(perr, tprod_kernel<0>, dim3(static_cast<unsigned>(tr_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem, st, tp_sk);
+            tp_sk.ns = ns;
+            tp_sk.tiles = static_cast<int>(tr_blocks * nb);
+            launch_dep(perr, tprod_kernel<0>, dim3(persistent_ctas(tr_blocks * nb * ns)), kTThreads, kTSmem, st, tp_sk);
             pend = {Yp, ns, Yall + static_cast<size_t>(i0) * a.d_out * l};  // summed by the next Gram pass
             sp_ready = false;
             return;
@@ -1925,7 +1986,9 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
                 return;
             }
             tp_lf.nz = nb;
-            launch_dep(perr, tprod_kernel<1>, dim3(static_cast<unsigned>(tc_blocks * nb), static_cast<unsigned>(ns)), kTThreads, kTSmem, st, tp_lf);
+            tp_lf.ns = ns;
+            tp_lf.tiles = static_cast<int>(tc_blocks * nb);
+            launch_dep(perr, tprod_kernel<1>, dim3(persistent_ctas(tc_blocks * nb * ns)), kTThreads, kTSmem, st, tp_lf);
             pend = {Zp, ns, Zall + static_cast<size_t>(i0) * a.d_in * l};
             sp_ready = false;
             return;
