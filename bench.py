@@ -78,13 +78,13 @@ NCU_TRAFFIC = {
     ("route + gather + prefill_kernel (grouped)", "multi_prefill"): ("4c65a422a15ad932", "bd_prefill.cu",
                                                                       939_384_576 + 60_230_955),
     ("materialize_kernel", "materialize"): ("62ad2eca0a51c12a", "bd_materialize.cu", 499_278_421 + 417_748_608),
-    # all 29 launches of one merge (launch list with DRAM counters, one pass)
-    (MONOSOUP_CALL, "monosoup"): ("7fc578022883d69f", "bd_monosoup.cu", 2_412_437_504 + 106_908_672),
+    # all 26 launches of one merge (launch list with DRAM counters, one pass)
+    (MONOSOUP_CALL, "monosoup"): ("da010de39fd26f35", "bd_monosoup.cu", 2_409_228_288 + 107_803_904),
 }
 
 # kernels each call launches: multi = prepare + fused kernel; multi_prefill =
 # router + plan + gather + grouped prefill; monosoup = the merge's launches
-LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4, "monosoup": 29}
+LAUNCHES_PER_CALL = {"multi": 2, "slice": 2, "multi_prefill": 4, "monosoup": 26}
 # workloads whose own figure is tensor throughput (TFLOP/s) rather than GB/s
 TENSOR_WORKLOADS = ("prefill", "multi_prefill")
 # the arithmetic type each workload computes in (the MonoSoup products and

@@ -1409,61 +1409,14 @@ __global__ void __launch_bounds__(kTriThreads) tri_solve_kernel(float* a_all, in
     }
 }
 
-// dst[j][row] = sum_c src[row][c] * M[c][j]  (c < l, j < m), written
-// transposed (the merge reads the factors of consecutive rows contiguously).
-// One thread per row and group of four outputs j: it reads its row with
-// 16-byte loads (l is a multiple of 4) and writes four coalesced columns.
-__global__ void __launch_bounds__(256) apply_t_kernel(const float* __restrict__ src_all, int64_t n, int l,
-                                                      const float* __restrict__ M_all, int m, float* __restrict__ dst_all)
-{
-    grid_launch_dependents();  // the next kernel of the merge may start launching
-    grid_dependency_wait();    // the previous kernel's results are visible
-    // checkpoint z = blockIdx.y: src_z [n][l], M_z [l][m], dst_z [m][n], each set consecutive
-    const float* src = src_all + static_cast<int64_t>(blockIdx.y) * n * l;
-    const float* M = M_all + static_cast<int64_t>(blockIdx.y) * l * m;
-    float* dst = dst_all + static_cast<int64_t>(blockIdx.y) * n * m;
-    __shared__ __align__(16) float sm[kMaxL][kMaxL];
-    for (int e = threadIdx.x; e < kMaxL * kMaxL; e += blockDim.x) {
-        const int c = e >> 6, j = e & 63;
-        sm[c][j] = (c < l && j < m && bd_in(kBkMsApply, blockIdx.y * l * m + c * m + j, gridDim.y * l * m))
-                       ? M[c * m + j]
-                       : 0.0f;
-    }
-    __syncthreads();
-    const int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int jg = static_cast<int>(o / n);
-    const int64_t row = o - static_cast<int64_t>(jg) * n;
-    if (4 * jg >= m) return;
-    if (!bd_in_range(kBkMsApply, blockIdx.y * n * l + row * l, l, static_cast<int64_t>(gridDim.y) * n * l)) return;
-    const float4* s = reinterpret_cast<const float4*>(src + row * l);
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    for (int c4 = 0; c4 < l / 4; ++c4) {
-        const float4 v = s[c4];
-        const float sv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int cc = 0; cc < 4; ++cc) {
-            const float4 mv = *reinterpret_cast<const float4*>(&sm[4 * c4 + cc][4 * jg]);
-            acc[0] = fmaf(sv[cc], mv.x, acc[0]);
-            acc[1] = fmaf(sv[cc], mv.y, acc[1]);
-            acc[2] = fmaf(sv[cc], mv.z, acc[2]);
-            acc[3] = fmaf(sv[cc], mv.w, acc[3]);
-        }
-    }
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-        if (4 * jg + t < m && bd_in(kBkMsApply, blockIdx.y * n * m + static_cast<int64_t>(4 * jg + t) * n + row,
-                                    static_cast<int64_t>(gridDim.y) * n * m))
-            dst[static_cast<int64_t>(4 * jg + t) * n + row] = acc[t];
-}
-
 // ---------------------------------------------------------------- the merge on the tensor cores
 // out[row][j] = W_base[row][j] + inv_k * sum_e L[e][row] R[e][j], e over the
-// K = k r factor columns (L [K][d_out], R [K][d_in] as written by
-// apply_t_kernel), rounded once to the output type.  Every factor value is
-// split into three bf16 pieces (as for the products) and the six piece pairs
-// (1,1), (1,2), (2,1), (1,3), (2,2), (3,1) are stacked along the reduction:
-// Ls[row][p K + e] = piece a_p of L[e][row], Rs[j][p K + e] = piece b_p of
-// R[e][j] (split_factors_kernel; a piece after the first is below 2^-7 of the
+// K = k r factor columns, rounded once to the output type.  Every factor
+// value is split into three bf16 pieces (as for the products) and the six
+// piece pairs (1,1), (1,2), (2,1), (1,3), (2,2), (3,1) are stacked along the
+// reduction: Ls[row][p K + e] = piece a_p of L[e][row], Rs[j][p K + e] =
+// piece b_p of R[e][j] (factor_split_kernel forms the factors and writes
+// them so; a piece after the first is below 2^-7 of the
 // value's magnitude and the third below 2^-15, so the three pairs left out
 // add up to less than 2^-21 |L[e][row] R[e][j]|), zero-padded to Kp = 6 K
 // rounded up to 64.  Persistent CTAs (one per SM) walk the 128-row x
@@ -1498,41 +1451,83 @@ __device__ __forceinline__ int merge_piece(int p, int side)
     return side == 0 ? a : b;
 }
 
-// dst[n][kk] (kk < Kp; n < rows) = piece merge_piece(kk / K, side) of
-// src[kk % K][n] for kk < 6 K, else 0.  Thread: one row and 8 consecutive kk
-// (one 16-byte store); rows vary fastest, so the reads of src are coalesced.
-__global__ void __launch_bounds__(256) split_factors_kernel(const float* __restrict__ src, int64_t rows, int K, int Kp,
-                                                            int side, uint16_t* __restrict__ dst)
+// The merge's factor operands straight from the bases and the eigenvectors:
+// row n of side 0 holds L_z[n][e] = sum_c Q_z[n][c] U_z[c][e] (Q_z the
+// d_out x l basis of checkpoint z), row n of side 1 holds R_z[n][e] =
+// sum_c Bt_z[n][c] U_z[c][e] (Bt_z = Delta_z^T Q_z, d_in x l), for every
+// checkpoint z < k and e < r (factor index E = z r + e, K = k r of them).
+// Each value is split into three bf16 pieces and stored as the stacked piece
+// pairs merge_tc_kernel reads: dst[n][p K + E] = piece merge_piece(p, side)
+// of it (p < 6), zero for p K + E >= 6 K up to Kp.  A warp takes one row at
+// a time (rows numbered with the d_out rows of side 0 first, the warps of
+// the grid striding over them), lane L taking E = L, L + 32, ...: the stores
+// of a warp are consecutive; the sum over c runs in order c = 0, 1, ...
+constexpr int kFsStageFloats = 12288;  // U of all checkpoints staged in shared memory up to 48 KB
+
+__global__ void __launch_bounds__(256) factor_split_kernel(const float* __restrict__ Yall,
+                                                           const float* __restrict__ Zall, int64_t d_out,
+                                                           int64_t d_in, int l, int k, int r,
+                                                           const float* __restrict__ Uk, int K, int Kp,
+                                                           uint16_t* __restrict__ Ls, uint16_t* __restrict__ Rs)
 {
+    extern __shared__ float su[];  // U when k l r <= kFsStageFloats
     grid_launch_dependents();  // the next kernel of the merge may start launching
     grid_dependency_wait();    // the previous kernel's results are visible
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t g = idx / rows, n = idx - g * rows;
-    if (g >= Kp / 8) return;
-    uint32_t w[4];
+    const int64_t nu = static_cast<int64_t>(k) * l * r;
+    const bool staged = nu <= kFsStageFloats;
+    if (staged) {
+        for (int e = threadIdx.x; e < nu; e += blockDim.x) su[e] = bd_in(kBkMsApply, e, nu) ? Uk[e] : 0.0f;
+        __syncthreads();
+    }
+    const float* U = staged ? su : Uk;
+    const int lane = threadIdx.x & 31;
+    const int wpb = blockDim.x >> 5;
+    for (int64_t gr = static_cast<int64_t>(blockIdx.x) * wpb + (threadIdx.x >> 5); gr < d_out + d_in;
+         gr += static_cast<int64_t>(gridDim.x) * wpb) {
+        const int side = gr < d_out ? 0 : 1;
+        const int64_t n = side ? gr - d_out : gr;
+        const int64_t rows = side ? d_in : d_out;
+        const float* src = side ? Zall : Yall;
+        uint16_t* dst = side ? Rs : Ls;
+        const int64_t nsrc = static_cast<int64_t>(k) * rows * l, ndst = rows * Kp;
+        for (int E = lane; E < K; E += 32) {
+            const int z = E / r, e = E - z * r;
+            const int64_t so = (static_cast<int64_t>(z) * rows + n) * l;
+            const int64_t uo = static_cast<int64_t>(z) * l * r + e;
+            float sv[kMaxL];  // the row of the basis, l <= kMaxL values (l is a multiple of 4)
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const int kk = static_cast<int>(8 * g) + j;
-        const int pr = kk / K, e = kk - pr * K;
-        uint32_t h = 0;
-        if (pr < kMgPairs) {
-            const float v = bd_in(kBkMsSplit, static_cast<int64_t>(e) * rows + n, static_cast<int64_t>(K) * rows)
-                                ? src[static_cast<int64_t>(e) * rows + n]
-                                : 0.0f;
-            const int pc = merge_piece(pr, side);
-            const uint32_t b1 = __float_as_uint(v) & 0xFFFF0000u;
-            const float r1 = __fsub_rn(v, __uint_as_float(b1));
+            for (int c4 = 0; c4 < kMaxL / 4; ++c4) {
+                const float4 v = 4 * c4 < l && bd_in_range(kBkMsApply, so + 4 * c4, 4, nsrc)
+                                     ? *reinterpret_cast<const float4*>(src + so + 4 * c4)
+                                     : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                sv[4 * c4] = v.x;
+                sv[4 * c4 + 1] = v.y;
+                sv[4 * c4 + 2] = v.z;
+                sv[4 * c4 + 3] = v.w;
+            }
+            float acc = 0.0f;
+#pragma unroll
+            for (int c = 0; c < kMaxL; ++c) {
+                if (c >= l) break;
+                const int64_t ui = uo + static_cast<int64_t>(c) * r;
+                acc = fmaf(sv[c], bd_in(kBkMsApply, ui, nu) ? U[ui] : 0.0f, acc);
+            }
+            const uint32_t b1 = __float_as_uint(acc) & 0xFFFF0000u;
+            const float r1 = __fsub_rn(acc, __uint_as_float(b1));
             const uint32_t b2 = __float_as_uint(r1) & 0xFFFF0000u;
             const float r2 = __fsub_rn(r1, __uint_as_float(b2));
-            h = (pc == 0 ? b1 : (pc == 1 ? b2 : __float_as_uint(r2))) >> 16;
+            const uint16_t p0 = static_cast<uint16_t>(b1 >> 16), p1 = static_cast<uint16_t>(b2 >> 16),
+                           p2 = static_cast<uint16_t>(__float_as_uint(r2) >> 16);
+#pragma unroll
+            for (int pr = 0; pr < kMgPairs; ++pr) {
+                const int64_t di = n * Kp + static_cast<int64_t>(pr) * K + E;
+                const int mp = merge_piece(pr, side);
+                if (bd_in(kBkMsSplit, di, ndst)) dst[di] = mp == 0 ? p0 : (mp == 1 ? p1 : p2);
+            }
         }
-        if (j & 1)
-            w[j >> 1] |= h << 16;
-        else
-            w[j >> 1] = h;
+        for (int kk = kMgPairs * K + lane; kk < Kp; kk += 32)
+            if (bd_in(kBkMsSplit, n * Kp + kk, ndst)) dst[n * Kp + kk] = 0;
     }
-    if (bd_in_range(kBkMsSplit, n * Kp + 8 * g, 8, rows * Kp))
-        *reinterpret_cast<uint4*>(dst + n * Kp + 8 * g) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 struct MergeParams {
@@ -2067,11 +2062,6 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
         }
         // the k projected eigenproblems at once, one CTA each
         launch_dep(perr, eig_kernel, static_cast<unsigned>(a.k), kEigThreads, kEigSmem, st, static_cast<const float2*>(Gk), l, r, Uk);  // U_r [l][r]
-        const unsigned rq = static_cast<unsigned>((r + 3) / 4);
-        launch_dep(perr, apply_t_kernel, dim3(blocks_for(a.d_out * rq), static_cast<unsigned>(a.k)), 256, 0, st, Yall, a.d_out, l,
-                                                                                                  Uk, r, L);
-        launch_dep(perr, apply_t_kernel, dim3(blocks_for(a.d_in * rq), static_cast<unsigned>(a.k)), 256, 0, st, Zall, a.d_in, l, Uk,
-                                                                                                 r, Rt);
     }
     if (perr != cudaSuccess) return perr;
     // the merge: split factors, then D = Ls Rs^T + W_base on the tensor cores
@@ -2081,8 +2071,12 @@ cudaError_t launch_monosoup(const MonoSoupArgs& a, cudaStream_t st)
     uint16_t* Rs = reinterpret_cast<uint16_t*>(w + lay.rs);
     static thread_local MergeParams mp;
     if (K > 0) {
-        launch_dep(perr, split_factors_kernel, blocks_for(a.d_out * (Kp / 8)), 256, 0, st, L, a.d_out, K, Kp, 0, Ls);
-        launch_dep(perr, split_factors_kernel, blocks_for(a.d_in * (Kp / 8)), 256, 0, st, Rt, a.d_in, K, Kp, 1, Rs);
+        const int64_t nu = static_cast<int64_t>(a.k) * l * r;
+        const size_t fs_smem = nu <= kFsStageFloats ? static_cast<size_t>(nu) * 4 : 0;
+        const int64_t fs_ctas = (a.d_out + a.d_in + 7) / 8;  // eight warps, each striding over the rows
+        launch_dep(perr, factor_split_kernel, static_cast<unsigned>(fs_ctas < 2 * sms ? fs_ctas : 2 * sms), 256, fs_smem, st,
+                   static_cast<const float*>(Yall), static_cast<const float*>(Zall), a.d_out, a.d_in, l, a.k, r,
+                   static_cast<const float*>(Uk), K, Kp, Ls, Rs);
     }
     if (!encode_tma_2d(&mp.a_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ls, static_cast<uint64_t>(Kp),
                        static_cast<uint64_t>(a.d_out), static_cast<uint64_t>(Kp) * 2, 64, kMgM,
