@@ -12,6 +12,7 @@
 // The kernel is bound by HBM bandwidth: per element it reads 4 bytes and
 // writes 1/8 byte.
 #include "bd_device.cuh"
+#include "bd_internal.h"
 
 namespace bd {
 namespace {
@@ -47,6 +48,8 @@ __global__ void __launch_bounds__(32 * kCompressRowsPerCta)
                     double* __restrict__ partials, uint32_t* err)
 {
     __shared__ double warp_sum[kCompressRowsPerCta];
+    grid_launch_dependents();  // a kernel launched after this one with programmatic dependent launch may start
+    grid_dependency_wait();    // the previous kernel's results are visible
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kCompressRowsPerCta + warp;
@@ -115,6 +118,8 @@ __global__ void __launch_bounds__(1024)
     alpha_finalize_kernel(const double* __restrict__ partials, int64_t n_parts, double n_elems, float* alpha)
 {
     __shared__ double sm[1024];
+    grid_launch_dependents();
+    grid_dependency_wait();
     double s = 0.0;
     for (int64_t i = threadIdx.x; i < n_parts; i += 1024)
         if (bd_in(kBkAlphaFinalize, i, n_parts)) s += partials[i];
@@ -151,13 +156,14 @@ cudaError_t launch_compress(const uint16_t* w_base, const uint16_t* w_ft, int64_
                             uint32_t* signs, float* alpha, double* partials, uint32_t* err, cudaStream_t stream)
 {
     const int64_t grid = (d_out + kCompressRowsPerCta - 1) / kCompressRowsPerCta;
-    compress_kernel<<<static_cast<unsigned>(grid), 32 * kCompressRowsPerCta, 0, stream>>>(
-        w_base, w_ft, d_out, d_in, per_row ? 1 : 0, signs, alpha, partials, err);
-    cudaError_t e = cudaGetLastError();
+    // programmatic dependent launches: each kernel's launch overlaps the end of the one before it
+    cudaError_t e = cudaSuccess;
+    launch_dep(e, compress_kernel, dim3(static_cast<unsigned>(grid)), dim3(32 * kCompressRowsPerCta), 0, stream, w_base,
+               w_ft, d_out, d_in, per_row ? 1 : 0, signs, alpha, partials, err);
     if (e != cudaSuccess || per_row) return e;
-    alpha_finalize_kernel<<<1, 1024, 0, stream>>>(partials, grid,
-                                                   static_cast<double>(d_out) * static_cast<double>(d_in), alpha);
-    return cudaGetLastError();
+    launch_dep(e, alpha_finalize_kernel, dim3(1), dim3(1024), 0, stream, static_cast<const double*>(partials), grid,
+               static_cast<double>(d_out) * static_cast<double>(d_in), alpha);
+    return e;
 }
 
 cudaError_t launch_debug_reconstruct(const uint16_t* w_base, const uint32_t* signs, const float* alpha, bool per_row,

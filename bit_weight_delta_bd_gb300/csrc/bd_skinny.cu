@@ -134,6 +134,7 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
     const int rank = static_cast<int>(cluster.block_rank());
     const int cl = static_cast<int>(blockIdx.x) / CK;  // cluster index
 
+    grid_launch_dependents();  // a kernel launched after this one with programmatic dependent launch may start
     if (tid == 0) {
         for (int s = 0; s < p.stages; ++s) {
             mbar_init(&sh.full[s], 1);
@@ -143,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 2) skinny_kernel(const __grid_consta
         fence_mbarrier_init();
     }
     __syncthreads();
+    grid_dependency_wait();  // the previous kernel's results (x, the signs, alpha) are visible
 
     // ---------------------------------------------------------------- pipeline
     // stage layout: [W half 0 | W half 1 | x half 0 | x half 1 | sign tile], 1024-byte aligned;
@@ -315,11 +317,15 @@ cudaError_t launch_nt(SkinnyParams& prm, size_t smem, cudaStream_t stream)
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = static_cast<unsigned>(prm.CK);
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // programmatic dependent launch: the launch overlaps the end of the kernel before it
+    // (the kernel waits for that kernel's results before its first global access)
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     // persistent clusters: as many as can be resident at once (cached per device,
@@ -340,6 +346,7 @@ cudaError_t launch_nt(SkinnyParams& prm, size_t smem, cudaStream_t stream)
     }
     prm.n_clusters = prm.n_blocks < n_res ? prm.n_blocks : n_res;
     cfg.gridDim = dim3(static_cast<unsigned>(prm.n_clusters * prm.CK));
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
