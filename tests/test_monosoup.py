@@ -80,7 +80,7 @@ def test_monosoup_matches_exact_truncated_svd(dev, d_out, d_in, k, r, l, q):
     (256, 384, 10, 4, 16, 1),    # two batches of checkpoints (8 + 2)
     (200, 256, 17, 4, 8, 1),     # three batches (8 + 8 + 1), ragged rows
     (512, 640, 3, 24, 64, 1),    # l = 64: CUDA-core products, three checkpoints in one batch
-    (256, 320, 10, 24, 64, 1),   # k l r = 15360: the merge factors read U from device memory, two batches
+    (256, 384, 10, 24, 64, 1),   # k l r = 15360: the merge factors read U from device memory, two batches
 ])
 def test_monosoup_batches_and_wide_sketches(dev, d_out, d_in, k, r, l, q):
     wb, ws = synth.monosoup_checkpoints(23 + k, d_out, d_in, k, min(r, d_out))
