@@ -68,9 +68,9 @@ DATA = "synthetic (seeded numpy / torch generators; shapes and distributions of 
 MONOSOUP_CALL = "bd_monosoup_merge (tensor-core products, Gram / Cholesky / tridiagonal eigensolver, tensor-core merge)"
 NCU_TRAFFIC = {
     # (kernel, workload): (source sha256[:16], source file, bytes per launch or ratio)
-    ("skinny_kernel<1>", "decode"): ("c133efac709bc60a", "bd_skinny.cu", 499_360_405 + 201_856),
+    ("skinny_kernel<1>", "decode"): ("0a72eed5c5ceea12", "bd_skinny.cu", 499_373_248 + 174_635),
     # 4 rows per CTA (kCompressRowsPerCta in bd_internal.h)
-    ("compress_kernel", "decode"): ("157f94bb54f54bb5", "bd_compress.cu", 939_588_267 + 6_411_563),
+    ("compress_kernel", "decode"): ("75f8daf3ca961f7e", "bd_compress.cu", 939_559_381 + 6_489_301),
     ("prefill_kernel", "prefill"): ("4c65a422a15ad932", "bd_prefill.cu", 619_373_995 + 65_847_595),
     # multi_kernel only (the prepare pass adds about 3.7 MB of x tiles and corrections)
     ("multi_prepare + multi_kernel<8>", "multi"): ("a3057edfbaaadd8d", "bd_multi.cu", 255_719_211 + 114_603),
