@@ -323,7 +323,7 @@ def _step_bytes(name, d_out, d_in, tokens, per_row, n_active, n_ckpt):
     return out + sum(linear_bytes(T, d_out, d_in, n_alpha) for T in tokens)
 
 
-class GpuRun:
+class DeviceRun:
     """Device copies of a workload (this rank's rows) and the calls of one step."""
 
     def __init__(self, wl: Workload, dev):
@@ -877,7 +877,7 @@ def _value(wl: Workload, ms_per_step: float) -> float:
 def make_run(wl: Workload, dev, sample_rows: int = 0):
     if wl.name == "slice":
         return SliceRun(wl, dev, wl.seed, sample_rows=sample_rows)
-    return GpuRun(wl, dev)
+    return DeviceRun(wl, dev)
 
 
 def measure(name, args, steps, warmup, world, rank, local, dev, peaks, want_cpu):
