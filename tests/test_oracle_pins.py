@@ -484,6 +484,20 @@ def test_monosoup_truncation_closed_form():
     np.testing.assert_allclose(got, wb + expect / k, rtol=0, atol=1e-12)
 
 
+def test_monosoup_truncation_repeated_singular_values():
+    """Singular values that repeat inside the kept rank (a cluster of three
+    and a pair, then a gap): the SVD may return any basis of a repeated
+    singular subspace, but the rank-r truncation is still unique and equals
+    the sum of the r leading terms U diag(s) V^T built without any SVD."""
+    rng = np.random.default_rng(5)
+    d_out, d_in, r = 20, 28, 5
+    s = np.array([3.0, 3.0, 3.0, 2.0, 2.0, 0.5, 0.25, 0.1])
+    u, v = _orthonormal(rng, d_out, len(s)), _orthonormal(rng, d_in, len(s))
+    wb = rng.standard_normal((d_out, d_in))
+    got = oracle.monosoup_merge_f64(wb, [wb + (u * s) @ v.T], r)
+    np.testing.assert_allclose(got, wb + (u[:, :r] * s[:r]) @ v[:, :r].T, rtol=0, atol=1e-12)
+
+
 def test_monosoup_special_cases():
     rng = np.random.default_rng(1)
     wb = rng.standard_normal((12, 16))
